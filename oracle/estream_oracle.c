@@ -1,0 +1,311 @@
+/*
+ * estream_oracle.c -- plain CPU oracle for one MoE layer's prefill.
+ *
+ * TEST INFRASTRUCTURE. This is the slow, obviously correct restatement of what
+ * the method computes, used only by the tests, by smoke() and by the bench's
+ * CPU-baseline leg. The CUDA library never links, loads or calls it, and it
+ * shares no code, header, table or constant with the CUDA sources.
+ *
+ * Source: "EStream: Fast and Memory-Efficient MoE Prefill through Expert
+ * Virtualization on Mobile NPUs" (arXiv 2609.06551).
+ *   - Eq. 1 (section 3.2): F_e(X_t) = W_e^d ( SiLU(W_e^g X_t) (*) W_e^u X_t ).
+ *   - Eq. 2 (section 3.2): Y_t = A_t + sum over (e, alpha) in R_l(t) of alpha * F_e(X_t).
+ *   - Section 3.2, "Composed Sparse Route and Parameter Binding", and the
+ *     route-map part of Algorithm 1: slot resolution psi_i = Phi_l(e_i),
+ *     per-slot counts, exclusive prefix sum, and a second pass that stores
+ *     (t_i, i) contiguously by slot.
+ *   - Eq. 4 (section 3.3): grouped placement Phi_l(e) = b*G + (pi_l(e) mod G)
+ *     when group floor(pi_l(e)/G) resides in bank b.
+ *
+ * Readings where the pages are silent (each is listed in the design notes):
+ *   - Router scores are a softmax over the E logits (the pages say only
+ *     "top-k of E experts"). Top-k order: larger logit first, equal logits ->
+ *     lower expert id first. Route index i = t*k + j (token-major, rank-minor).
+ *   - alpha = softmax probability p, or p / (sum of the k selected p, summed in
+ *     rank order) when renormalisation is asked for.
+ *   - Routing arithmetic is fp32 with one written exponential (below); the
+ *     expert FFN is evaluated in fp64 from the fp32/bf16 inputs widened exactly.
+ *   - Routes whose slot is "not resident" (Phi = -1) go to a trailing bucket P,
+ *     so the CSR always holds all R = T*k routes; offsets has P+2 entries.
+ *
+ * The written exponential (fp32; the same written definition is implemented
+ * independently by the CUDA routing kernel so that alpha is bit-exact):
+ *   for x < -87: 0
+ *   n = round-half-even( fl(x * LOG2E) )
+ *   r = fma(-n, LN2_HI, x);  r = fma(-n, LN2_LO, r)     Cody & Waite (1980)
+ *   p = Horner form of sum_{j=0..7} r^j / j!, one fma per step
+ *   exp(x) = p * 2^n                                      (exact scaling)
+ * LN2_HI is ln 2 rounded to fp32 with its 8 low significand bits cleared (so
+ * n * LN2_HI is exact for |n| < 256); LN2_LO = fp32(ln 2 - LN2_HI); LOG2E and
+ * the 1/j! are the round-to-nearest fp32 values of 1/ln 2 and 1/j!.
+ * Compile with -ffp-contract=off: every rounding step is written out.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ------------------------------------------------------------------------ */
+/* Written exponential                                                       */
+/* ------------------------------------------------------------------------ */
+
+static const float O_LOG2E = 0x1.715476p+0f;   /* fp32(1/ln 2) */
+static const float O_LN2_HI = 0x1.62e4p-1f;    /* ln 2 to 16 significant bits */
+static const float O_LN2_LO = 0x1.7f7d1cp-20f; /* fp32(ln 2 - O_LN2_HI) */
+
+float oracle_exp_f32(float x)
+{
+    if (x < -87.0f) return 0.0f;
+    float t = x * O_LOG2E;
+    float n = nearbyintf(t);              /* default rounding mode: half to even */
+    float r = fmaf(-n, O_LN2_HI, x);
+    r = fmaf(-n, O_LN2_LO, r);
+    /* 1/j! for j = 7..0, fp32 round-to-nearest */
+    float p = 0x1.a01a02p-13f;            /* 1/5040 */
+    p = fmaf(p, r, 0x1.6c16c2p-10f);      /* 1/720 */
+    p = fmaf(p, r, 0x1.111112p-7f);       /* 1/120 */
+    p = fmaf(p, r, 0x1.555556p-5f);       /* 1/24 */
+    p = fmaf(p, r, 0x1.555556p-3f);       /* 1/6 */
+    p = fmaf(p, r, 0.5f);                 /* 1/2 */
+    p = fmaf(p, r, 1.0f);                 /* 1/1 */
+    p = fmaf(p, r, 1.0f);                 /* 1/0! */
+    int ni = (int)n;                      /* in [-126, 0] for x in [-87, 0] */
+    union { uint32_t u; float f; } scale;
+    scale.u = (uint32_t)(ni + 127) << 23;
+    return p * scale.f;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Router: softmax top-k                                                     */
+/* ------------------------------------------------------------------------ */
+
+/* For every token t: ids of the k largest logits (ties -> lower id first) and
+ * their routing weights. Returns 0, or -1 on bad arguments. */
+int oracle_route_topk(const float* logits, int T, int E, int k, int renorm,
+                      int32_t* topk_ids, float* alpha)
+{
+    if (T < 0 || E < 1 || k < 1 || k > E) return -1;
+    float* prob = (float*)malloc(sizeof(float) * (size_t)E);
+    unsigned char* taken = (unsigned char*)malloc((size_t)E);
+    if (!prob || !taken) { free(prob); free(taken); return -1; }
+    for (int t = 0; t < T; ++t) {
+        const float* l = logits + (size_t)t * E;
+        /* softmax: subtract the maximum, exponentiate, sum in ascending e */
+        float m = l[0];
+        for (int e = 1; e < E; ++e) if (l[e] > m) m = l[e];
+        float s = 0.0f;
+        for (int e = 0; e < E; ++e) {
+            prob[e] = oracle_exp_f32(l[e] - m);
+            s = s + prob[e];
+        }
+        for (int e = 0; e < E; ++e) prob[e] = prob[e] / s;
+        /* selection: k passes, each taking the largest remaining logit */
+        memset(taken, 0, (size_t)E);
+        for (int j = 0; j < k; ++j) {
+            int best = -1;
+            for (int e = 0; e < E; ++e) {
+                if (taken[e]) continue;
+                if (best < 0 || l[e] > l[best]) best = e;   /* strict: ties keep the lower id */
+            }
+            taken[best] = 1;
+            topk_ids[(size_t)t * k + j] = best;
+            alpha[(size_t)t * k + j] = prob[best];
+        }
+        if (renorm) {
+            float z = 0.0f;
+            for (int j = 0; j < k; ++j) z = z + alpha[(size_t)t * k + j];
+            for (int j = 0; j < k; ++j) alpha[(size_t)t * k + j] = alpha[(size_t)t * k + j] / z;
+        }
+    }
+    free(prob);
+    free(taken);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Route map (CSR by physical slot)                                          */
+/* ------------------------------------------------------------------------ */
+
+/* Composed route binding of section 3.2 / Algorithm 1 (route-map part).
+ * Route i = t*k + j goes to logical expert e_i = topk_ids[i]. Its slot is
+ * psi_i = phi[e_i] (phi == NULL means the identity, which needs P == E);
+ * phi[e] == -1 means "not resident", which this restatement files under the
+ * trailing bucket P. Outputs:
+ *   offsets[0..P+1]: offsets[0] = 0, offsets[s+1] = offsets[s] + count[s]
+ *   rec_tok[p], rec_route[p]: the record (t_i, i) at position p.
+ * Returns 0, or -1 on bad arguments (an id or slot out of range). */
+int oracle_route_csr(const int32_t* topk_ids, int T, int k, const int32_t* phi,
+                     int E, int P, int32_t* offsets, int32_t* rec_tok,
+                     int32_t* rec_route)
+{
+    if (T < 0 || k < 1 || E < 1 || P < 0) return -1;
+    if (!phi && P != E) return -1;
+    const int R = T * k;
+    int32_t* psi = (int32_t*)malloc(sizeof(int32_t) * (size_t)(R > 0 ? R : 1));
+    int32_t* count = (int32_t*)calloc((size_t)P + 1, sizeof(int32_t));
+    int32_t* cursor = (int32_t*)malloc(sizeof(int32_t) * ((size_t)P + 2));
+    if (!psi || !count || !cursor) { free(psi); free(count); free(cursor); return -1; }
+    int rc = 0;
+    /* resolve the physical slot of every route */
+    for (int i = 0; i < R; ++i) {
+        int e = topk_ids[i];
+        if (e < 0 || e >= E) { rc = -1; break; }
+        int s = phi ? phi[e] : e;
+        if (s < -1 || s >= P) { rc = -1; break; }
+        psi[i] = (s < 0) ? P : s;
+    }
+    if (rc == 0) {
+        /* count routes per slot */
+        for (int i = 0; i < R; ++i) count[psi[i]] += 1;
+        /* exclusive prefix sum */
+        offsets[0] = 0;
+        for (int s = 0; s <= P; ++s) offsets[s + 1] = offsets[s] + count[s];
+        /* second pass: store (t_i, i) contiguously by slot, in ascending i */
+        for (int s = 0; s <= P; ++s) cursor[s] = offsets[s];
+        for (int i = 0; i < R; ++i) {
+            int p = cursor[psi[i]];
+            rec_tok[p] = i / k;
+            rec_route[p] = i;
+            cursor[psi[i]] = p + 1;
+        }
+    }
+    free(psi);
+    free(count);
+    free(cursor);
+    return rc;
+}
+
+/* Eq. 4: placement of grouped experts. perm[e] = pi(e) (storage position),
+ * bank_of_group[q] = the bank holding storage group q, or -1. Writes
+ * phi[e] = b*G + (pi(e) mod G) when group floor(pi(e)/G) is in bank b, else -1. */
+int oracle_grouped_placement(const int32_t* perm, int E, int G,
+                             const int32_t* bank_of_group, int32_t* phi)
+{
+    if (E < 1 || G < 1) return -1;
+    for (int e = 0; e < E; ++e) {
+        int pos = perm ? perm[e] : e;
+        if (pos < 0 || pos >= E) return -1;
+        int q = pos / G;          /* storage group */
+        int r = pos % G;          /* position inside the group */
+        int b = bank_of_group[q];
+        phi[e] = (b < 0) ? -1 : b * G + r;
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Expert FFN and layer output                                               */
+/* ------------------------------------------------------------------------ */
+
+/* Element access for the two input encodings: fp32, or bf16 bit patterns
+ * (the upper 16 bits of an fp32), both widened exactly to double. */
+static double load_elem(const void* base, size_t idx, int bf16)
+{
+    if (bf16) {
+        union { uint32_t u; float f; } v;
+        v.u = (uint32_t)((const uint16_t*)base)[idx] << 16;
+        return (double)v.f;
+    }
+    return (double)((const float*)base)[idx];
+}
+
+static double silu(double z) { return z / (1.0 + exp(-z)); }
+
+/* Eq. 1 for one token row: out[o] = sum_f Wd[o][f] * SiLU(g_f) * u_f with
+ * g_f = sum_h Wg[f][h] x[h], u_f = sum_h Wu[f][h] x[h].
+ * Wg, Wu are [F][H] and Wd is [H][F], row-major; x is the token's row offset
+ * into X. hbuf is caller scratch of F doubles. */
+static void expert_ffn_row(const void* X, size_t x_off, const void* Wg,
+                           const void* Wu, const void* Wd, size_t w_off_gu,
+                           size_t w_off_d, int H, int F, int bf16,
+                           double* hbuf, double* out)
+{
+    for (int f = 0; f < F; ++f) {
+        double g = 0.0, u = 0.0;
+        for (int h = 0; h < H; ++h) {
+            double xv = load_elem(X, x_off + (size_t)h, bf16);
+            g += load_elem(Wg, w_off_gu + (size_t)f * H + h, bf16) * xv;
+            u += load_elem(Wu, w_off_gu + (size_t)f * H + h, bf16) * xv;
+        }
+        hbuf[f] = silu(g) * u;
+    }
+    for (int o = 0; o < H; ++o) {
+        double y = 0.0;
+        for (int f = 0; f < F; ++f)
+            y += load_elem(Wd, w_off_d + (size_t)o * F + f, bf16) * hbuf[f];
+        out[o] = y;
+    }
+}
+
+/* Eq. 2 for the tokens listed in rows[0..n_rows): for list entry r, token
+ * t = rows[r],
+ *   Y_out[r][:] = A_t + sum_j alpha[t*k+j] * F_{topk_ids[t*k+j]}(X_t)
+ *                 + sum_{s < n_shared} F^shared_s(X_t)
+ * Routed weights: Wg, Wu [E][F][H], Wd [E][H][F]. Shared experts (weight 1):
+ * Sg, Su [n_shared][Fs][H], Sd [n_shared][H][Fs] (NULL when n_shared == 0).
+ * X is [T][H]; A is the residual [T][H] in double, or NULL for zero.
+ * bf16 != 0: X and every weight are bf16 bit patterns; else fp32. */
+int oracle_moe_layer_rows(const void* X, int T, int H, int E, int F, int k,
+                          const void* Wg, const void* Wu, const void* Wd,
+                          const int32_t* topk_ids, const float* alpha,
+                          int n_shared, int Fs, const void* Sg, const void* Su,
+                          const void* Sd, const double* A, int bf16,
+                          const int32_t* rows, int n_rows, double* Y_out)
+{
+    if (T < 0 || H < 1 || E < 1 || F < 1 || k < 1 || k > E || n_rows < 0) return -1;
+    if (n_shared > 0 && (Fs < 1 || !Sg || !Su || !Sd)) return -1;
+    for (int r = 0; r < n_rows; ++r)
+        if (rows[r] < 0 || rows[r] >= T) return -1;
+    for (int r = 0; r < n_rows; ++r)
+        for (int j = 0; j < k; ++j) {
+            int e = topk_ids[(size_t)rows[r] * k + j];
+            if (e < 0 || e >= E) return -1;
+        }
+    int Fmax = F > Fs ? F : Fs;
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int r = 0; r < n_rows; ++r) {
+        double* hbuf = (double*)malloc(sizeof(double) * (size_t)Fmax);
+        double* fo = (double*)malloc(sizeof(double) * (size_t)H);
+        if (!hbuf || !fo) {
+            free(hbuf);
+            free(fo);
+#pragma omp atomic write
+            bad = 1;
+            continue;
+        }
+        int t = rows[r];
+        double* y = Y_out + (size_t)r * H;
+        for (int o = 0; o < H; ++o) y[o] = A ? A[(size_t)t * H + o] : 0.0;
+        size_t x_off = (size_t)t * H;
+        for (int j = 0; j < k; ++j) {
+            int e = topk_ids[(size_t)t * k + j];
+            double a = (double)alpha[(size_t)t * k + j];
+            expert_ffn_row(X, x_off, Wg, Wu, Wd, (size_t)e * F * H,
+                           (size_t)e * H * F, H, F, bf16, hbuf, fo);
+            for (int o = 0; o < H; ++o) y[o] += a * fo[o];
+        }
+        for (int s = 0; s < n_shared; ++s) {
+            expert_ffn_row(X, x_off, Sg, Su, Sd, (size_t)s * Fs * H,
+                           (size_t)s * H * Fs, H, Fs, bf16, hbuf, fo);
+            for (int o = 0; o < H; ++o) y[o] += fo[o];
+        }
+        free(hbuf);
+        free(fo);
+    }
+    return bad ? -1 : 0;
+}
+
+/* Number of threads the layer oracle runs on (1 without OpenMP). */
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
