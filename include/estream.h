@@ -1,0 +1,275 @@
+/*
+ * estream.h -- C ABI of the GB300 MoE-layer prefill library (libestream.so).
+ *
+ * One MoE layer's prefill over T prompt tokens, as described in "EStream:
+ * Fast and Memory-Efficient MoE Prefill through Expert Virtualization on
+ * Mobile NPUs" (arXiv 2609.06551):
+ *   - section 3.2, Eq. 2: Y_t = A_t + sum over (e, alpha) in R_l(t) of
+ *     alpha * F_e(X_t), with Eq. 1: F_e(x) = W_e^d (SiLU(W_e^g x) (*) W_e^u x);
+ *   - section 3.2, "Composed Sparse Route and Parameter Binding" and
+ *     Algorithm 1: routes (e_i, t_i, alpha_i), slots psi_i = Phi_l(e_i), a
+ *     CSR of records (t_i, i) by slot, and slot addresses p_s^j = p_{B^j} +
+ *     s*S_j (Eq. 3) for the three parameter planes j in {g, u, d};
+ *   - section 3.3: a bounded arena of P = B*G fixed-address slots organised
+ *     in B banks of G slots; storage groups of G experts in an offline order
+ *     pi_l; placement Phi_l(e) = b*G + (pi_l(e) mod G) (Eq. 4); slot states
+ *     Available -> Filling -> Ready -> InUse -> Available;
+ *   - section 3.4: loading overlapped with execution; after routing, groups
+ *     with no routes are skipped.
+ *
+ * Conventions for every call:
+ *   - Every entry point returns an estream_status; nothing throws, exits or
+ *     aborts. Argument errors are reported before anything is enqueued.
+ *   - "device pointer" arguments are CUDA device memory owned by the caller;
+ *     the library never frees them. "host pointer" arguments are host memory.
+ *   - Calls taking `cuda_stream` (a cudaStream_t; NULL = legacy default
+ *     stream) enqueue their GPU work on it and return without waiting, except
+ *     where a call says it synchronises.
+ *   - Errors found by a kernel while it runs (a slot id out of range, a
+ *     bounded wait that ran out) are written to a device error word and
+ *     reported by estream_get_device_error / estream_workspace_error.
+ *   - Only sm_100-family GPUs built for here (sm_103a) are supported; other
+ *     devices get ESTREAM_ERR_UNSUPPORTED.
+ */
+#ifndef ESTREAM_H
+#define ESTREAM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ESTREAM_OK = 0,
+    ESTREAM_ERR_INVALID_ARG = 1,  /* bad pointer, size, alignment or shape */
+    ESTREAM_ERR_CAPACITY = 2,     /* T or k beyond what the context was bound for */
+    ESTREAM_ERR_NOT_BOUND = 3,    /* null or unbound context */
+    ESTREAM_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed */
+    ESTREAM_ERR_PAGER = 5,        /* the pager failed to fill a bank */
+    ESTREAM_ERR_TIMEOUT = 6,      /* a kernel's bounded wait ran out */
+    ESTREAM_ERR_DEVICE = 7,       /* a kernel found bad data (e.g. a slot id out of range) */
+    ESTREAM_ERR_UNSUPPORTED = 8   /* device or data type not supported */
+} estream_status;
+
+typedef enum { ESTREAM_F32 = 0, ESTREAM_BF16 = 1 } estream_dtype;
+
+/* Short English name of a status code (static storage). */
+const char* estream_status_string(estream_status s);
+
+/* ABI version of this header: major*10000 + minor*100 + patch. */
+int estream_version(void);
+
+/* ---------------------------------------------------------------------- */
+/* Routing and route map                                                   */
+/* ---------------------------------------------------------------------- */
+
+/* Bytes of device workspace estream_route_build needs for these sizes. */
+size_t estream_route_workspace_bytes(int T, int E, int k, int P);
+
+/*
+ * Router top-k and the route map of section 3.2 / Algorithm 1.
+ *
+ * logits    device, [T][E] fp32 row-major, finite values.
+ * T, E, k   tokens, experts, routes per token: T >= 0, 1 <= k <= E <= 1024, k <= 32.
+ * renorm    0: alpha = softmax probability; 1: alpha divided by the sum of
+ *           the token's k selected probabilities (summed in rank order).
+ * phi       device, [E] int32: Phi(e) = slot in [0, P), or -1 when expert e
+ *           is not resident; NULL means the identity and needs P == E.
+ * P         physical slots, 0 <= P <= 4096.
+ * topk_ids  device, [T*k] int32 out: route i = t*k + j is the token's j-th
+ *           expert, larger logit first, equal logits -> lower expert id.
+ * alpha     device, [T*k] fp32 out: the routing weight of route i.
+ * offsets   device, [P+2] int32 out: slot s owns records
+ *           [offsets[s], offsets[s+1]); the trailing bucket P holds the
+ *           routes whose expert is not resident; offsets[P+1] = T*k.
+ * rec_tok   device, [T*k] int32 out: t_i of the record at each position.
+ * rec_route device, [T*k] int32 out: route index i of the record; records
+ *           of one slot are in ascending i.
+ * workspace device, >= estream_route_workspace_bytes(T, E, k, P) bytes,
+ *           256-byte aligned; its contents need no initialisation (the call
+ *           clears the error word estream_workspace_error reads).
+ * The softmax uses a written fp32 exponential (Cody & Waite range
+ * reduction + degree-7 Taylor polynomial) so that alpha is reproducible bit
+ * for bit. Nothing is synchronised. A phi entry outside [-1, P) is reported
+ * through estream_workspace_error.
+ */
+estream_status estream_route_build(const float* logits, int T, int E, int k, int renorm,
+                                   const int32_t* phi, int P,
+                                   int32_t* topk_ids, float* alpha, int32_t* offsets,
+                                   int32_t* rec_tok, int32_t* rec_route,
+                                   void* workspace, size_t workspace_bytes,
+                                   void* cuda_stream);
+
+/* Synchronises `cuda_stream` and returns the error a route-build kernel
+ * recorded in `workspace` (ESTREAM_OK if none), then clears it. */
+estream_status estream_workspace_error(void* workspace, void* cuda_stream);
+
+/* ---------------------------------------------------------------------- */
+/* Expert arena, pager and layer prefill                                   */
+/* ---------------------------------------------------------------------- */
+
+enum {
+    ESTREAM_SCHED_AFTER_ROUTING = 0, /* start copies once the routes are known */
+    ESTREAM_SCHED_PREFETCH = 1       /* also fill free banks in storage order before routing */
+};
+
+typedef struct {
+    int L;                  /* sparse layers whose experts stream through this arena */
+    int E, H, F;            /* routed experts per layer, hidden size, expert FFN size */
+    int G, B;               /* experts per storage group (= slots per bank), banks; P = B*G */
+    int Q;                  /* copies kept in flight on the copy stream per bank fill (>= 1) */
+    estream_dtype wdtype;   /* type of X and of every weight: bf16 (tensor cores) or fp32 */
+    void* arena_dev;        /* device, >= estream_arena_bytes(...) bytes, 1024-byte aligned */
+    size_t arena_bytes;
+    const void* const* host_pool;   /* host array [L] of pinned pools, each laid out by
+                                       estream_pack_experts */
+    const int32_t* perm;    /* host, [L*E]: pi_l(e), the storage order; NULL = identity */
+    int n_shared, F_shared; /* always-on shared experts per layer (weight 1), their FFN size */
+    const void* const* shared_dev;  /* host array [L] of device pointers, each to one layer's
+                                       shared experts as laid out by estream_pack_shared;
+                                       NULL if none */
+    int T_max, k_max;       /* largest T and k a layer call will see (workspace capacity) */
+    int deterministic;      /* 1: per-route outputs + fixed-order combine (bit-reproducible Y) */
+    int schedule;           /* ESTREAM_SCHED_* */
+} estream_arena_desc;
+
+typedef struct estream_ctx estream_ctx;
+
+/* Bytes of arena for P = B*G slots of one expert each (gate, up, down). */
+size_t estream_arena_bytes(int E, int H, int F, int G, int B, estream_dtype wdtype);
+
+/* Bytes of one layer's pinned host pool: E experts, group-contiguous, then
+ * E fp32 down-weight scales in storage order (see estream_pack_experts). */
+size_t estream_pool_bytes(int E, int H, int F, estream_dtype wdtype);
+
+/* Bytes of one layer's packed shared experts (see estream_pack_shared). */
+size_t estream_shared_bytes(int n_shared, int H, int F_shared, estream_dtype wdtype);
+
+/*
+ * Validate `d`, compute the slot addresses of Eq. 3 and their TMA
+ * descriptors, create the copy stream and the per-bank events, and allocate
+ * the library workspace (sized for T_max, k_max). Copies no weights.
+ * Shapes: H % 256 == 0, F % 128 == 0, F_shared % 128 == 0, 1 <= G, 1 <= B,
+ * 1 <= E <= 1024. On success *out is a context owned by the caller, to be
+ * released with estream_unbind. The current CUDA device is the one used.
+ */
+estream_status estream_bind_arena(estream_ctx** out, const estream_arena_desc* d);
+
+/*
+ * Offline repack (host -> host) of one layer's expert weights into the
+ * layout the kernels consume and the pager streams (section 3.3, "Offline
+ * NPU-Consumable Weight Layout", restated for GB300). For storage group q
+ * (experts with pi(e) in [q*G, q*G+G)), in pi order, at byte offset q*G*W_e:
+ * [gate n_q x F x H][up n_q x F x H][down n_q x H x F], W_e = 3*H*F*elem.
+ * After the last group: E fp32 scales, one per storage position.
+ * bf16 layers: gate and up are copied unchanged; the down plane is stored
+ * as fp16 of (W_d * 2^s_e), with s_e = 15 - (binary exponent of max|W_d[e]|)
+ * so the largest magnitude lands in [2^14, 2^15); the stored scale is 2^-s_e
+ * and the down GEMM multiplies it back in. The conversion is exact for every
+ * weight within a factor 2^32 of the expert's largest one. fp32 layers are
+ * copied unchanged with scale 1.
+ * wg, wu: host [E][F][H]; wd: host [E][H][F] (bf16 or fp32 as d->wdtype);
+ * host_pool_out: host, estream_pool_bytes(...) bytes (pinned if streamed).
+ * Only d->E, H, F, G, wdtype and perm (row `layer`) are read. Pools must be
+ * packed before estream_bind_arena (which reads their scales).
+ */
+estream_status estream_pack_experts(const estream_arena_desc* d, int layer,
+                                    const void* wg, const void* wu, const void* wd,
+                                    void* host_pool_out);
+
+/*
+ * Repack (host -> host) of one layer's shared experts into
+ * [gate n_shared x F_shared x H][up (same)][down n_shared x H x F_shared]
+ * [n_shared fp32 scales], with the down plane converted as in
+ * estream_pack_experts. The caller copies the result to device memory and
+ * passes it in estream_arena_desc.shared_dev. sg, su: host
+ * [n_shared][F_shared][H]; sd: host [n_shared][H][F_shared];
+ * out: host, estream_shared_bytes(...) bytes. Reads d->n_shared, F_shared,
+ * H and wdtype.
+ */
+estream_status estream_pack_shared(const estream_arena_desc* d, const void* sg,
+                                   const void* su, const void* sd, void* out);
+
+/*
+ * Load every group of `layer` into the arena and keep it there (needs
+ * B*G >= E, i.e. ceil(E/G) <= B). Later calls for that layer copy nothing
+ * and run each kernel once over all experts. Enqueued on the copy stream;
+ * the first layer call waits for it.
+ */
+estream_status estream_arena_preload(estream_ctx* c, int layer, void* cuda_stream);
+
+/* Forget every bank's contents (the next call streams again). Waits for
+ * in-flight work on the library's streams. */
+estream_status estream_arena_invalidate(estream_ctx* c);
+
+/*
+ * One MoE layer's prefill: Y += sum_j alpha_{t,j} F_{e_{t,j}}(X_t) (+ the
+ * shared experts with weight 1), i.e. Eq. 2 with Y holding A_t on entry.
+ * X       device, [T][H] of d->wdtype, 16-byte aligned.
+ * logits  device, [T][E] fp32 (the router's logits for this layer).
+ * T, k    1 <= T <= T_max, 1 <= k <= min(k_max, E); renorm as in route_build.
+ * Y       device, [T][H] fp32, read and written.
+ * Steps: routing + route map over the storage order (K1), then per group
+ * with routes: bank fill on the copy stream (skipped when already resident),
+ * gate/up GEMM with the row gather and SiLU-mul fused (K2), down GEMM with
+ * the alpha-weighted scatter-add into Y (K3). When some group is not
+ * resident, the call copies the per-slot offsets to the host and
+ * synchronises `cuda_stream` once (after routing). All later GPU work of the
+ * call is ordered before any later work on `cuda_stream`.
+ */
+estream_status estream_moe_layer_prefill(estream_ctx* c, int layer, const void* X,
+                                         const float* logits, int T, int k, int renorm,
+                                         float* Y, void* cuda_stream);
+
+/* Timings and counters accumulated since the last estream_reset_stats. The
+ * per-kernel times are CUDA-event times on the launching stream, recorded
+ * only while timing is on (estream_set_timing); reading them synchronises. */
+typedef struct {
+    int calls;
+    int launches;            /* kernels (and memsets) this library enqueued */
+    double ms_route;         /* routing + route map kernels */
+    double ms_gateup;        /* K2 launches */
+    double ms_down;          /* K3 launches */
+    double ms_shared;        /* shared-expert K2 + K3 */
+    double ms_combine;       /* deterministic combine */
+    double ms_total;         /* first to last event of each call, summed */
+    int n_gateup, n_down;    /* K2 / K3 launches counted in ms_gateup / ms_down */
+    double h2d_bytes;        /* bytes copied into the arena */
+    int groups_loaded, groups_skipped, groups_hit;
+    double ms_io_busy;       /* copy-stream busy time (timing on) */
+} estream_stats;
+
+estream_status estream_set_timing(estream_ctx* c, int on);
+estream_status estream_reset_stats(estream_ctx* c);
+estream_status estream_last_stats(estream_ctx* c, estream_stats* out);
+
+/* Synchronises the library's streams, returns and clears the device error
+ * word (ESTREAM_OK, ESTREAM_ERR_TIMEOUT or ESTREAM_ERR_DEVICE). */
+estream_status estream_get_device_error(estream_ctx* c);
+
+/* Residency-table trace for tests: writes up to `cap` events as
+ * (bank, layer, group, state) int32 quadruples and returns their count in
+ * *n (states: 0 Available, 1 Filling, 2 Ready, 3 InUse). Tracing is kept for
+ * the last call only. */
+estream_status estream_residency_trace(estream_ctx* c, int32_t* out, int cap, int* n);
+
+/* Host-side fault injection for tests: the pager refuses to fill group
+ * `group` of `layer` (before any copy is issued) and the call returns
+ * ESTREAM_ERR_PAGER with the streams drained. group < 0 turns it off. */
+estream_status estream_inject_pager_fault(estream_ctx* c, int layer, int group);
+
+/* Drains the library's streams and frees everything the library owns
+ * (workspace, streams, events, the context). Caller memory is untouched. */
+void estream_unbind(estream_ctx* c);
+
+/* fp32 -> bf16 (round to nearest even) of n elements, device to device;
+ * used to chain layers (X_{l+1} = bf16(Y_l)). */
+estream_status estream_cast_f32_bf16(const float* src, void* dst, size_t n, void* cuda_stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ESTREAM_H */

@@ -1,0 +1,103 @@
+// Internal declarations shared by the CUDA translation units of libestream.
+// Not installed; the public ABI is include/estream.h.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "estream.h"
+
+namespace es {
+
+// Route-map chunk: one CTA of the scatter kernel places this many routes.
+constexpr int kRouteChunk = 1024;
+// Rows of one GEMM M tile (route records per tile).
+constexpr int kBM = 128;
+// Limits checked at the boundary.
+constexpr int kMaxE = 1024;
+constexpr int kMaxK = 32;
+constexpr int kMaxP = 4096;
+
+// Device error word values (first error wins).
+constexpr int kDevErrNone = 0;
+constexpr int kDevErrSlotRange = 1;  // a phi entry outside [-1, P)
+constexpr int kDevErrTimeout = 2;    // a bounded wait ran out
+constexpr int kDevErrRange = 3;      // an intermediate h value outside the fp16 range
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Layout of the route-build workspace (all offsets 256-byte aligned).
+struct RouteWorkspace {
+    size_t err_off;      // int32 device error word
+    size_t hist_off;     // int32 [nchunk][P+1]: per-chunk counts, then per-chunk bases
+    size_t mblk_off;     // int32 [P+2]: exclusive prefix of ceil(count[s]/kBM), s < P
+    size_t total;
+    int nchunk;
+};
+RouteWorkspace route_workspace_layout(int T, int k, int P);
+
+// Enqueue the full route build (K1). `ws` must hold route_workspace_layout(T,k,P).
+// rec_pos (optional, [T*k]) receives, for route i, its position in the CSR.
+cudaError_t launch_route_build(const float* logits, int T, int E, int k, int renorm,
+                               const int32_t* phi, int P, int32_t* topk_ids, float* alpha,
+                               int32_t* offsets, int32_t* rec_tok, int32_t* rec_route,
+                               int32_t* rec_pos, void* ws, cudaStream_t stream,
+                               int* n_launches);
+
+// Identity route map for the shared experts: n_shared segments of T rows,
+// rec_tok[p] = p mod T, offsets[s] = s*T, mblk[s] = s*ceil(T/kBM).
+cudaError_t launch_identity_map(int T, int n_shared, int32_t* offsets, int32_t* rec_tok,
+                                int32_t* mblk, cudaStream_t stream);
+
+// ---------------------------------------------------------------------------
+// Grouped expert GEMMs (K2 gate/up + SwiGLU, K3 down + weighted scatter-add)
+// ---------------------------------------------------------------------------
+
+struct GemmSegments {
+    const int32_t* offsets;    // CSR offsets (indexed by segment)
+    const int32_t* mblk;       // exclusive prefix of m-blocks per segment
+    const int32_t* rec_tok;    // token of each record
+    const int32_t* rec_route;  // route of each record (K3 alpha lookup; may be null)
+    const float* alpha;        // route weights, or null for weight 1
+    const float* seg_scale;    // per segment: 2^-s of the down weights' offline scale
+    int seg_begin, seg_count;  // segments [seg_begin, seg_begin+seg_count)
+    int slot_base;             // arena slot of segment seg_begin
+    int max_tiles_m;           // host upper bound on m-blocks in the range
+};
+
+// K2 (bf16 tensor cores): h[p, :] = fp16(SiLU(X[tok(p)] Wg_slot^T) * (X[tok(p)] Wu_slot^T)).
+cudaError_t launch_gateup(const CUtensorMap* tm_x, const CUtensorMap* tm_wg,
+                          const CUtensorMap* tm_wu, const GemmSegments& seg, void* h,
+                          int H, int F, int slot_rows_gu, int* dev_err, int num_sms,
+                          cudaStream_t stream);
+
+// K3 (fp16 tensor cores): Y[tok(p), :] += alpha(p) * scale(seg) * (h[p] Wd_slot^T), or
+// out_rows[p, :] = ... when out_rows != null (deterministic mode).
+cudaError_t launch_down(const CUtensorMap* tm_h, const CUtensorMap* tm_wd,
+                        const GemmSegments& seg, float* Y, float* out_rows, int H, int F,
+                        int slot_rows_d, int* dev_err, int num_sms, cudaStream_t stream);
+
+// fp32 path (CUDA-core FMA): the same two steps for fp32 X and weights.
+// Weight planes are [slots][F][H] (gate, up) and [slots][H][F] (down).
+cudaError_t launch_gateup_f32(const float* X, const float* wg, const float* wu,
+                              const GemmSegments& seg, float* h, int H, int F, int max_rows,
+                              cudaStream_t stream);
+cudaError_t launch_down_f32(const float* h, const float* wd, const GemmSegments& seg, float* Y,
+                            float* out_rows, int H, int F, int max_rows, cudaStream_t stream);
+
+// K4: Y[t, :] += sum_j rows[pos[t*k+j], :] (j ascending), then
+// + sum_s shared_rows[s*T + t, :] (s ascending) when n_shared > 0.
+cudaError_t launch_combine(const float* rows, const int32_t* pos, int T, int k, int H,
+                           const float* shared_rows, int n_shared, float* Y,
+                           cudaStream_t stream);
+
+cudaError_t launch_cast_f32_bf16(const float* src, void* dst, size_t n, cudaStream_t stream);
+
+// Tensor-map helper (driver entry point resolved at run time).
+CUresult encode_tmap_2d(CUtensorMap* tm, CUtensorMapDataType dtype, const void* base,
+                        uint64_t inner, uint64_t outer, uint64_t row_stride_bytes,
+                        uint32_t box_inner, uint32_t box_outer);
+
+}  // namespace es

@@ -1,0 +1,630 @@
+// K2 / K3: the routed expert FFN as two grouped GEMMs on the 5th-generation
+// tensor cores (tcgen05 + TMEM), fed by TMA.
+//
+// "EStream: Fast and Memory-Efficient MoE Prefill through Expert
+// Virtualization on Mobile NPUs", section 3.2 ("Fused Expert Execution with
+// Intra-NPU Pipelining") and Eq. 1: for every non-empty slot s the routed
+// rows of X are gathered, the gate and up projections are evaluated as tile
+// pairs, SiLU(g) * u is applied to completed pairs, the down projection is
+// evaluated, and completed down tiles are multiplied by the route weight and
+// scatter-added into the token accumulator Y (Eq. 2).
+//
+// GB300 form. One persistent kernel per GEMM walks a list of 128-row tiles
+// built from the route map (segment = slot, m-block, n-block), with three
+// warp roles per CTA:
+//   warp 0     TMA producer into a 4-stage shared-memory ring. For K2 the A
+//              tile is a row gather of X by record token (tile::gather4, four
+//              rows per instruction, 128-byte swizzle); for K3 it is a plain
+//              tile of h (records are contiguous by slot).
+//   warp 1     allocates 512 TMEM columns (two 128x256 fp32 accumulators) and
+//              one elected lane issues tcgen05.mma (M=128, N=256, K=16 per
+//              instruction, kind::f16), committing stages back to the producer
+//              and finished accumulators to the epilogue.
+//   warps 2-5  epilogue: tcgen05.ld of the accumulator; K2 writes
+//              h = SiLU(g) * u as fp16; K3 scales by alpha times the expert's
+//              down-weight scale and adds into Y[t] with vector fp32
+//              reductions (or stores the scaled row for the deterministic
+//              combine).
+// Operand types: K2 multiplies bf16 X by bf16 W_g / W_u. K3 multiplies fp16 h
+// by fp16 W_d, which the offline packer converted from bf16 with an exact
+// per-expert power-of-two scale: fp16 keeps 3 more significand bits of h than
+// bf16 would, which is what keeps Y within the accuracy bound.
+// The gate and up weight tiles of one n-block sit back to back in shared
+// memory, so a single N=256 instruction produces both halves of a pair.
+// Every wait is bounded: on timeout the kernel records an error word, lets
+// outstanding copies and MMAs land, frees TMEM and returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "estream_internal.h"
+
+namespace es {
+namespace {
+
+constexpr int kStages = 4;
+constexpr int kRowBytes = 128;                    // one swizzle row of K
+constexpr int kTileABytes = kBM * kRowBytes;      // 16 KB
+constexpr int kTileBBytes = 256 * kRowBytes;      // 32 KB
+constexpr int kStageBytes = kTileABytes + kTileBBytes;
+constexpr int kAccCols = 256;
+constexpr int kTmemCols = 512;
+constexpr int kThreads = 192;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+constexpr uint64_t kDrainLimitNs = 100000000ull;  // 0.1 s
+constexpr float kHalfMax = 65504.0f;
+
+// Shared-memory map (offsets from a 1024-byte aligned base).
+constexpr int kOffA = 0;
+constexpr int kOffB = kStages * kTileABytes;
+constexpr int kOffBar = kOffB + kStages * kTileBBytes;
+// barriers: full[kStages], empty[kStages], acc_full[2], acc_empty[2], drain
+constexpr int kNumBars = 2 * kStages + 5;
+constexpr int kOffMisc = kOffBar + 8 * kNumBars;  // tmem base, abort flag
+constexpr int kOffTable = kOffMisc + 16;
+
+size_t gemm_smem_bytes(int seg_count) {
+    return 1024 + kOffTable + sizeof(int) * static_cast<size_t>(seg_count + 1);
+}
+
+// ----------------------------------------------------------------------------
+// PTX wrappers
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void record_error(int* err, int code) {
+    if (err) atomicCAS(err, kDevErrNone, code);
+}
+
+// Bounded wait for the phase of `parity` to complete. Returns false when the
+// limit ran out (recording a timeout and raising the CTA's abort flag) or
+// when another role already aborted.
+__device__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* dev_err,
+                          uint64_t limit_ns = kWaitLimitNs) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    uint32_t spins = 0;
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((++spins & 63u) == 0) {
+            if (*abort_flag) return false;
+            if (global_ns() - t0 > limit_ns) {
+                *abort_flag = 1;
+                record_error(dev_err, kDevErrTimeout);
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm, int x, int y,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+// Four arbitrary rows (r0..r3) of a 2D tensor, columns [x, x + box width).
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* tm, int x, int r0,
+                                            int r1, int r2, int r3, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive once on `bar` when every tcgen05 operation this thread issued so far
+// has completed.
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b),
+                 "f"(c), "f"(d)
+                 : "memory");
+}
+__device__ __forceinline__ void st_v4(void* addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major operand tile whose rows are
+// 128 bytes, stored with the 128-byte swizzle (8-row atoms of 1024 bytes):
+// start address >> 4 in bits 0-13, leading-dimension offset (unused for this
+// layout, set to 1) in bits 16-29, stride between 8-row atoms (1024 B >> 4)
+// in bits 32-45, descriptor version 1 in bits 46-47, swizzle mode 2 (128 B)
+// in bits 61-63.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    uint64_t d = static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(1) << 16;
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    d |= static_cast<uint64_t>(2) << 61;
+    return d;
+}
+
+// Instruction descriptor (kind::f16): fp32 accumulator (bits 4-5 = 1), A and
+// B type in bits 7-9 / 10-12 (fp16 = 0, bf16 = 1, the same for both), both
+// K-major (bits 15, 16 = 0), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+__device__ __forceinline__ uint32_t make_idesc(bool bf16, int M, int N) {
+    const uint32_t ab = bf16 ? 1u : 0u;
+    return (1u << 4) | (ab << 7) | (ab << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+           (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+__device__ __forceinline__ float silu_mul(float g, float u) {
+    return __fdividef(g, 1.0f + __expf(-g)) * u;
+}
+
+struct Tile {
+    int seg;   // segment index relative to seg_begin
+    int mb;    // m-block inside the segment
+    int nb;    // n-block
+    int row0;  // first record of the tile
+    int rows;  // valid records in the tile (1..kBM)
+};
+
+// Tiles are numbered segment by segment; inside a segment n-block-major with
+// the m-blocks fastest, so the CTAs running at the same time share one
+// weight n-block (read from HBM about once) while the gathered rows of the
+// segment stay in L2.
+__device__ __forceinline__ Tile decode_tile(int t, const int* table, int seg_count, int NB,
+                                            const int32_t* offsets, int seg_begin) {
+    int lo = 0, hi = seg_count;  // largest lo with table[lo] * NB <= t
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (table[mid] * NB <= t) lo = mid; else hi = mid;
+    }
+    Tile ti;
+    ti.seg = lo;
+    const int nmb = table[lo + 1] - table[lo];
+    const int l = t - table[lo] * NB;
+    ti.nb = l / nmb;
+    ti.mb = l - ti.nb * nmb;
+    const int s_lo = offsets[seg_begin + lo];
+    const int s_hi = offsets[seg_begin + lo + 1];
+    ti.row0 = s_lo + ti.mb * kBM;
+    ti.rows = min(kBM, s_hi - ti.row0);
+    return ti;
+}
+
+template <bool kGateUp>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_expert_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b0,
+                  const __grid_constant__ CUtensorMap tm_b1, const GemmSegments seg, void* h_out,
+                  float* Y, float* out_rows, int H, int F, int slot_rows, int* dev_err) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_addr(smem);
+    const uint32_t sA = sbase + kOffA;
+    const uint32_t sB = sbase + kOffB;
+    const uint32_t bar0 = sbase + kOffBar;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
+    auto accf_bar = [&](int a) { return bar0 + 8u * (2 * kStages + a); };
+    auto acce_bar = [&](int a) { return bar0 + 8u * (2 * kStages + 2 + a); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 4);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
+    int* table = reinterpret_cast<int*>(smem + kOffTable);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    // m-block prefix of the segment range, relative to its first segment
+    const int m0 = seg.mblk[seg.seg_begin];
+    for (int s = threadIdx.x; s <= seg.seg_count; s += blockDim.x)
+        table[s] = seg.mblk[seg.seg_begin + s] - m0;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(accf_bar(a), 1);
+            mbar_init(acce_bar(a), 4);  // one arrival per epilogue warp
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int NB = kGateUp ? (F / 128) : (H / 256);
+    const int K = kGateUp ? H : F;
+    const int BKe = 64;  // 16-bit elements per 128-byte row
+    const int num_kb = K / BKe;
+    const int total = table[seg.seg_count] * NB;
+
+    if (warp == 0) {
+        // ------------------------------ TMA producer ------------------------------
+        int stage = 0;
+        uint32_t phase = 0;
+        int issued[kStages];
+        for (int s = 0; s < kStages; ++s) issued[s] = -1;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+            const Tile ti = decode_tile(t, table, seg.seg_count, NB, seg.offsets, seg.seg_begin);
+            const int slot = seg.slot_base + ti.seg;
+            const int brow = slot * slot_rows + ti.nb * (kGateUp ? 128 : 256);
+            int tok[4] = {0, 0, 0, 0};
+            if (kGateUp) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int r = min(lane * 4 + q, ti.rows - 1);
+                    tok[q] = seg.rec_tok[ti.row0 + r];
+                }
+            }
+            for (int kb = 0; kb < num_kb; ++kb) {
+                bool w = true;
+                if (lane == 0) w = mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, dev_err);
+                w = __shfl_sync(0xffffffffu, w, 0);
+                if (!w) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(full_bar(stage), kStageBytes);
+                    issued[stage] = static_cast<int>(phase);
+                }
+                __syncwarp();
+                const uint32_t a_dst = sA + stage * kTileABytes;
+                const uint32_t b_dst = sB + stage * kTileBBytes;
+                const int x = kb * BKe;
+                if (kGateUp) {
+                    tma_gather4(a_dst + lane * 4 * kRowBytes, &tm_a, x, tok[0], tok[1], tok[2],
+                                tok[3], full_bar(stage));
+                    if (lane == 0) {
+                        tma_load_2d(b_dst, &tm_b0, x, brow, full_bar(stage));
+                        tma_load_2d(b_dst + 128 * kRowBytes, &tm_b1, x, brow, full_bar(stage));
+                    }
+                } else if (lane == 0) {
+                    tma_load_2d(a_dst, &tm_a, x, ti.row0, full_bar(stage));
+                    tma_load_2d(b_dst, &tm_b0, x, brow, full_bar(stage));
+                }
+                if (++stage == kStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        if (!ok && lane == 0) {
+            // let every copy already issued land before the CTA goes away
+            for (int s = 0; s < kStages; ++s)
+                if (issued[s] >= 0)
+                    mbar_wait(full_bar(s), static_cast<uint32_t>(issued[s]), abort_flag, nullptr,
+                              kDrainLimitNs);
+        }
+    } else if (warp == 1) {
+        // ------------------------------ MMA issuer ------------------------------
+        if (lane == 0) {
+            // K2: bf16 x bf16; K3: fp16 x fp16
+            const uint32_t idesc = make_idesc(kGateUp, 128, 256);
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            bool issued_any = false;
+            for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+                if (!mbar_wait(acce_bar(acc), acc_phase ^ 1u, abort_flag, dev_err)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kAccCols);
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait(full_bar(stage), phase, abort_flag, dev_err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t adesc = sw128_desc(sA + stage * kTileABytes);
+                    const uint64_t bdesc = sw128_desc(sB + stage * kTileBBytes);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)  // 4 x 32 bytes of K per stage
+                        umma_f16(d_tmem, adesc + 2u * kk, bdesc + 2u * kk, idesc,
+                                   (kb | kk) != 0 ? 1u : 0u);
+                    issued_any = true;
+                    umma_commit(empty_bar(stage));
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                umma_commit(accf_bar(acc));
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1u;
+            }
+            if (!ok && issued_any) {
+                // wait (bounded) for the MMAs already issued before TMEM is freed
+                umma_commit(drain_bar);
+                mbar_wait(drain_bar, 0, abort_flag, nullptr, kDrainLimitNs);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------ epilogue ------------------------------
+        const int quarter = warp & 3;  // TMEM lanes this warp may read
+        const int row = quarter * 32 + lane;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int t = blockIdx.x; t < total; t += gridDim.x) {
+            const Tile ti = decode_tile(t, table, seg.seg_count, NB, seg.offsets, seg.seg_begin);
+            bool w = true;
+            if (lane == 0) w = mbar_wait(accf_bar(acc), acc_phase, abort_flag, dev_err);
+            w = __shfl_sync(0xffffffffu, w, 0);
+            if (!w) break;
+            tc_fence_after();
+            const bool valid = row < ti.rows;
+            const int p = ti.row0 + row;
+            const uint32_t tacc = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                  static_cast<uint32_t>(acc * kAccCols);
+            if constexpr (kGateUp) {
+                bool in_range = true;
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t g[32], u[32];
+                    tmem_ld32(tacc + c * 32, g);
+                    tmem_ld32(tacc + 128 + c * 32, u);
+                    tmem_ld_wait();
+                    if (valid) {
+                        const size_t col = static_cast<size_t>(ti.nb) * 128 + c * 32;
+                        __half* dst = static_cast<__half*>(h_out) + static_cast<size_t>(p) * F + col;
+                        uint32_t packed[16];
+#pragma unroll
+                        for (int v = 0; v < 16; ++v) {
+                            const float h0 = silu_mul(__uint_as_float(g[2 * v]), __uint_as_float(u[2 * v]));
+                            const float h1 = silu_mul(__uint_as_float(g[2 * v + 1]), __uint_as_float(u[2 * v + 1]));
+                            in_range = in_range && fabsf(h0) <= kHalfMax && fabsf(h1) <= kHalfMax;
+                            const __half2 p2 = __floats2half2_rn(h0, h1);
+                            packed[v] = *reinterpret_cast<const uint32_t*>(&p2);
+                        }
+#pragma unroll
+                        for (int v = 0; v < 4; ++v)
+                            st_v4(dst + 8 * v, packed[4 * v], packed[4 * v + 1], packed[4 * v + 2],
+                                  packed[4 * v + 3]);
+                    }
+                }
+                if (!in_range) record_error(dev_err, kDevErrRange);
+            } else {
+                int tok = 0;
+                float a = 0.0f;
+                if (valid) {
+                    tok = seg.rec_tok[p];
+                    a = seg.alpha ? seg.alpha[seg.rec_route[p]] : 1.0f;
+                    a *= seg.seg_scale[seg.seg_begin + ti.seg];  // undo the W_d scale
+                }
+#pragma unroll 1
+                for (int c = 0; c < 8; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(tacc + c * 32, v);
+                    tmem_ld_wait();
+                    if (valid) {
+                        const size_t col = static_cast<size_t>(ti.nb) * 256 + c * 32;
+                        if (out_rows) {
+                            float* dst = out_rows + static_cast<size_t>(p) * H + col;
+#pragma unroll
+                            for (int q = 0; q < 8; ++q)
+                                st_v4(dst + 4 * q, __float_as_uint(a * __uint_as_float(v[4 * q])),
+                                      __float_as_uint(a * __uint_as_float(v[4 * q + 1])),
+                                      __float_as_uint(a * __uint_as_float(v[4 * q + 2])),
+                                      __float_as_uint(a * __uint_as_float(v[4 * q + 3])));
+                        } else {
+                            float* dst = Y + static_cast<size_t>(tok) * H + col;
+#pragma unroll
+                            for (int q = 0; q < 8; ++q)
+                                red_add_v4(dst + 4 * q, a * __uint_as_float(v[4 * q]),
+                                           a * __uint_as_float(v[4 * q + 1]),
+                                           a * __uint_as_float(v[4 * q + 2]),
+                                           a * __uint_as_float(v[4 * q + 3]));
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acce_bar(acc));
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+template <bool kGateUp>
+cudaError_t launch_gemm(const CUtensorMap* tm_a, const CUtensorMap* tm_b0, const CUtensorMap* tm_b1,
+                        const GemmSegments& seg, void* h_out, float* Y, float* out_rows, int H,
+                        int F, int slot_rows, int* dev_err, int num_sms, cudaStream_t stream) {
+    const int NB = kGateUp ? F / 128 : H / 256;
+    const long long max_tiles = static_cast<long long>(seg.max_tiles_m) * NB;
+    if (max_tiles <= 0 || seg.seg_count <= 0) return cudaSuccess;
+    const int grid = static_cast<int>(max_tiles < num_sms ? max_tiles : num_sms);
+    const size_t smem = gemm_smem_bytes(seg.seg_count);
+    auto kern = k_expert_gemm<kGateUp>;
+    cudaError_t rc = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          static_cast<int>(smem));
+    if (rc != cudaSuccess) return rc;
+    kern<<<grid, kThreads, smem, stream>>>(*tm_a, *tm_b0, *tm_b1, seg, h_out, Y, out_rows, H, F,
+                                           slot_rows, dev_err);
+    return cudaGetLastError();
+}
+
+// Deterministic combine: one thread per 4 columns of one token.
+__global__ void k_combine(const float* __restrict__ rows, const int32_t* __restrict__ pos, int T,
+                          int k, int H, const float* __restrict__ shared_rows, int n_shared,
+                          float* __restrict__ Y) {
+    const int H4 = H / 4;
+    const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (idx >= static_cast<long long>(T) * H4) return;
+    const int t = static_cast<int>(idx / H4);
+    const int c = static_cast<int>(idx % H4) * 4;
+    float4 y = *reinterpret_cast<const float4*>(Y + static_cast<size_t>(t) * H + c);
+    for (int j = 0; j < k; ++j) {
+        const int p = pos[t * k + j];
+        const float4 v = *reinterpret_cast<const float4*>(rows + static_cast<size_t>(p) * H + c);
+        y.x += v.x; y.y += v.y; y.z += v.z; y.w += v.w;
+    }
+    for (int s = 0; s < n_shared; ++s) {
+        const float4 v = *reinterpret_cast<const float4*>(
+            shared_rows + (static_cast<size_t>(s) * T + t) * H + c);
+        y.x += v.x; y.y += v.y; y.z += v.z; y.w += v.w;
+    }
+    *reinterpret_cast<float4*>(Y + static_cast<size_t>(t) * H + c) = y;
+}
+
+}  // namespace
+
+cudaError_t launch_gateup(const CUtensorMap* tm_x, const CUtensorMap* tm_wg,
+                          const CUtensorMap* tm_wu, const GemmSegments& seg, void* h, int H, int F,
+                          int slot_rows_gu, int* dev_err, int num_sms, cudaStream_t stream) {
+    return launch_gemm<true>(tm_x, tm_wg, tm_wu, seg, h, nullptr, nullptr, H, F, slot_rows_gu,
+                             dev_err, num_sms, stream);
+}
+
+cudaError_t launch_down(const CUtensorMap* tm_h, const CUtensorMap* tm_wd, const GemmSegments& seg,
+                        float* Y, float* out_rows, int H, int F, int slot_rows_d, int* dev_err,
+                        int num_sms, cudaStream_t stream) {
+    return launch_gemm<false>(tm_h, tm_wd, tm_wd, seg, nullptr, Y, out_rows, H, F, slot_rows_d,
+                              dev_err, num_sms, stream);
+}
+
+cudaError_t launch_combine(const float* rows, const int32_t* pos, int T, int k, int H,
+                           const float* shared_rows, int n_shared, float* Y, cudaStream_t stream) {
+    const long long n = static_cast<long long>(T) * (H / 4);
+    if (n == 0) return cudaSuccess;
+    k_combine<<<static_cast<unsigned>((n + 255) / 256), 256, 0, stream>>>(rows, pos, T, k, H,
+                                                                          shared_rows, n_shared, Y);
+    return cudaGetLastError();
+}
+
+// ----------------------------------------------------------------------------
+// Tensor maps
+// ----------------------------------------------------------------------------
+namespace {
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+}  // namespace
+
+CUresult encode_tmap_2d(CUtensorMap* tm, CUtensorMapDataType dtype, const void* base, uint64_t inner,
+                        uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner,
+                        uint32_t box_outer) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return CUDA_ERROR_NOT_FOUND;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {row_stride_bytes};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(tm, dtype, 2,
+              const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+}  // namespace es

@@ -1,0 +1,325 @@
+// K1: router top-k and the route map (CSR of records by physical slot).
+//
+// "EStream: Fast and Memory-Efficient MoE Prefill through Expert
+// Virtualization on Mobile NPUs", section 3.2 ("Composed Sparse Route and
+// Parameter Binding") and Algorithm 1 (route-map construction): every route i
+// (token t_i, logical expert e_i, weight alpha_i) is resolved to its slot
+// psi_i = Phi(e_i); routes are counted per slot, an exclusive prefix sum
+// gives where each slot's records begin, and a second pass stores (t_i, i)
+// contiguously by slot, in ascending i. Routes whose expert is not resident
+// (Phi = -1) are filed under a trailing bucket P.
+//
+// GPU form (three launches after one memset):
+//   k_route_topk    one thread per token: softmax top-k, alpha, and per-chunk
+//                   slot counts (global atomics; counts are order-free).
+//   k_route_scan    one CTA: per-slot chunk bases and slot offsets (exclusive
+//                   prefix sums), plus the m-block prefix the GEMMs schedule by.
+//   k_route_scatter one CTA per chunk of 1024 routes: ranks inside a warp by
+//                   __match_any_sync, across warps in ascending warp order, so
+//                   the placement is the stable one Algorithm 1 produces.
+#include <cuda_bf16.h>
+
+#include "estream_internal.h"
+
+namespace es {
+
+// ---------------------------------------------------------------------------
+// Written fp32 exponential, the same written definition the CPU oracle uses,
+// implemented here on its own so both sides round identically:
+//   x < -87 -> 0; n = nearest-even(fl(x * LOG2E));
+//   r = fma(-n, LN2_HI, x); r = fma(-n, LN2_LO, r)   (Cody & Waite, 1980)
+//   p = Horner of sum_{j<=7} r^j/j!, one fma per step;  result = p * 2^n.
+// LN2_HI = fp32(ln 2) with its 8 low significand bits cleared, LN2_LO =
+// fp32(ln 2 - LN2_HI); LOG2E and 1/j! are round-to-nearest fp32 values.
+// Every operation is an explicit round-to-nearest intrinsic (no contraction).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float route_exp(float x) {
+    if (x < -87.0f) return 0.0f;
+    const float kLog2e = 0x1.715476p+0f;
+    const float kLn2Hi = 0x1.62e4p-1f;
+    const float kLn2Lo = 0x1.7f7d1cp-20f;
+    const int n = __float2int_rn(__fmul_rn(x, kLog2e));
+    const float nf = static_cast<float>(n);
+    float r = __fmaf_rn(-nf, kLn2Hi, x);
+    r = __fmaf_rn(-nf, kLn2Lo, r);
+    float p = 0x1.a01a02p-13f;           // 1/7!
+    p = __fmaf_rn(p, r, 0x1.6c16c2p-10f);  // 1/6!
+    p = __fmaf_rn(p, r, 0x1.111112p-7f);   // 1/5!
+    p = __fmaf_rn(p, r, 0x1.555556p-5f);   // 1/4!
+    p = __fmaf_rn(p, r, 0x1.555556p-3f);   // 1/3!
+    p = __fmaf_rn(p, r, 0.5f);             // 1/2!
+    p = __fmaf_rn(p, r, 1.0f);             // 1/1!
+    p = __fmaf_rn(p, r, 1.0f);             // 1/0!
+    return __fmul_rn(p, __int_as_float((n + 127) << 23));
+}
+
+__device__ __forceinline__ void record_error(int* err, int code) {
+    if (err) atomicCAS(err, kDevErrNone, code);
+}
+
+// One thread per token. Selection walks the strict total order
+// (logit descending, expert id ascending): pass j takes the best expert that
+// comes after pass j-1's pick in that order, so no "taken" mask is needed.
+__global__ void __launch_bounds__(128) k_route_topk(
+    const float* __restrict__ logits, int T, int E, int k, int renorm,
+    const int32_t* __restrict__ phi, int P, int32_t* __restrict__ topk_ids,
+    float* __restrict__ alpha, int32_t* __restrict__ hist, int* __restrict__ err) {
+    const int t = blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= T) return;
+    const float* l = logits + static_cast<size_t>(t) * E;
+
+    float m = l[0];
+    for (int e = 1; e < E; ++e) {
+        const float v = l[e];
+        if (v > m) m = v;
+    }
+    float s = 0.0f;
+    for (int e = 0; e < E; ++e) s = __fadd_rn(s, route_exp(__fsub_rn(l[e], m)));
+
+    float a[kMaxK];
+    int ids[kMaxK];
+    float prev_l = __int_as_float(0x7f800000);  // +inf: everything comes after it
+    int prev_id = -1;
+    for (int j = 0; j < k; ++j) {
+        int best = -1;
+        float bl = 0.0f;
+        for (int e = 0; e < E; ++e) {
+            const float v = l[e];
+            const bool after_prev = (v < prev_l) || (v == prev_l && e > prev_id);
+            if (!after_prev) continue;
+            if (best < 0 || v > bl) {
+                best = e;
+                bl = v;
+            }
+        }
+        prev_l = bl;
+        prev_id = best;
+        ids[j] = best;
+        a[j] = __fdiv_rn(route_exp(__fsub_rn(bl, m)), s);
+    }
+    if (renorm) {
+        float z = 0.0f;
+        for (int j = 0; j < k; ++j) z = __fadd_rn(z, a[j]);
+        for (int j = 0; j < k; ++j) a[j] = __fdiv_rn(a[j], z);
+    }
+    const int nb = P + 1;
+    for (int j = 0; j < k; ++j) {
+        const int i = t * k + j;
+        topk_ids[i] = ids[j];
+        alpha[i] = a[j];
+        int slot = phi ? phi[ids[j]] : ids[j];
+        if (slot < -1 || slot >= P) {
+            record_error(err, kDevErrSlotRange);
+            slot = -1;
+        }
+        const int b = slot < 0 ? P : slot;
+        atomicAdd(&hist[(i / kRouteChunk) * nb + b], 1);
+    }
+}
+
+// In-place exclusive scan of n ints in shared memory by one CTA of
+// blockDim.x (multiple of 32, <= 1024) threads. Returns the total.
+__device__ int block_exclusive_scan(int* data, int n, int* warp_sums) {
+    const int tid = threadIdx.x;
+    const int nthr = blockDim.x;
+    const int per = (n + nthr - 1) / nthr;
+    const int lo = min(n, tid * per);
+    const int hi = min(n, lo + per);
+    int local = 0;
+    for (int x = lo; x < hi; ++x) local += data[x];
+    const int lane = tid & 31, warp = tid >> 5;
+    int incl = local;
+    for (int d = 1; d < 32; d <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += v;
+    }
+    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const int nw = nthr >> 5;
+        int w = lane < nw ? warp_sums[lane] : 0;
+        int wi = w;
+        for (int d = 1; d < 32; d <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, wi, d);
+            if (lane >= d) wi += v;
+        }
+        if (lane < nw) warp_sums[lane] = wi - w;  // exclusive warp offsets
+        if (lane == 31) warp_sums[32] = wi;       // grand total
+    }
+    __syncthreads();
+    int run = warp_sums[warp] + incl - local;
+    for (int x = lo; x < hi; ++x) {
+        const int v = data[x];
+        data[x] = run;
+        run += v;
+    }
+    const int total = warp_sums[32];
+    __syncthreads();
+    return total;
+}
+
+// One CTA. hist[c][b] (counts) becomes the base position of chunk c's first
+// record of slot b; offsets[b] = sum of counts of slots < b; mblk[s] = sum over
+// slots < s of ceil(count/kBM) for s <= P (the trailing bucket has no GEMM work).
+__global__ void __launch_bounds__(1024) k_route_scan(int32_t* __restrict__ hist, int nchunk,
+                                                     int P, int R, int32_t* __restrict__ offsets,
+                                                     int32_t* __restrict__ mblk) {
+    extern __shared__ int smem[];
+    const int nb = P + 1;
+    int* cnt = smem;               // [nb] counts -> slot offsets
+    int* mb = smem + nb;           // [nb] m-blocks -> m-block prefix
+    int* warp_sums = smem + 2 * nb;  // [33]
+    for (int b = threadIdx.x; b < nb; b += blockDim.x) {
+        int run = 0;
+        for (int c = 0; c < nchunk; ++c) {
+            const int v = hist[c * nb + b];
+            hist[c * nb + b] = run;
+            run += v;
+        }
+        cnt[b] = run;
+        mb[b] = (b < P) ? (run + kBM - 1) / kBM : 0;
+    }
+    __syncthreads();
+    block_exclusive_scan(cnt, nb, warp_sums);
+    block_exclusive_scan(mb, nb, warp_sums);
+    for (int b = threadIdx.x; b < nb; b += blockDim.x) {
+        offsets[b] = cnt[b];
+        mblk[b] = mb[b];
+        for (int c = 0; c < nchunk; ++c) hist[c * nb + b] += cnt[b];
+    }
+    if (threadIdx.x == 0) {
+        offsets[P + 1] = R;
+        mblk[P + 1] = mb[P];
+    }
+}
+
+__global__ void __launch_bounds__(kRouteChunk) k_route_scatter(
+    const int32_t* __restrict__ topk_ids, const int32_t* __restrict__ phi, int P, int k, int R,
+    const int32_t* __restrict__ base, int32_t* __restrict__ rec_tok,
+    int32_t* __restrict__ rec_route, int32_t* __restrict__ rec_pos) {
+    extern __shared__ int cnt[];  // [P+1] records placed so far in this chunk, per slot
+    const int nb = P + 1;
+    for (int b = threadIdx.x; b < nb; b += blockDim.x) cnt[b] = 0;
+    __syncthreads();
+    const int c = blockIdx.x;
+    const int i = c * kRouteChunk + threadIdx.x;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const bool valid = i < R;
+    int b = P;
+    if (valid) {
+        const int e = topk_ids[i];
+        const int slot = phi ? phi[e] : e;
+        b = (slot < 0 || slot >= P) ? P : slot;
+    }
+    const int key = valid ? b : -(lane + 1);  // invalid lanes match nobody
+    const unsigned peers = __match_any_sync(0xffffffffu, key);
+    const unsigned lt_mask = (1u << lane) - 1u;
+    const int rank = __popc(peers & lt_mask);
+    const int leader = __ffs(peers) - 1;
+    int pos = 0;
+    const int nwarps = blockDim.x >> 5;
+    for (int w = 0; w < nwarps; ++w) {
+        if (warp == w) {
+            const int before = valid ? cnt[b] : 0;
+            __syncwarp();
+            if (valid && lane == leader) cnt[b] = before + __popc(peers);
+            pos = base[c * nb + b] + before + rank;
+        }
+        __syncthreads();
+    }
+    if (valid) {
+        rec_tok[pos] = i / k;
+        rec_route[pos] = i;
+        if (rec_pos) rec_pos[i] = pos;
+    }
+}
+
+__global__ void k_identity_map(int T, int n_shared, int32_t* __restrict__ offsets,
+                               int32_t* __restrict__ rec_tok, int32_t* __restrict__ mblk) {
+    const int p = blockIdx.x * blockDim.x + threadIdx.x;
+    if (p < T * n_shared) rec_tok[p] = p % T;
+    if (p <= n_shared) {
+        offsets[p] = p * T;
+        mblk[p] = p * ((T + kBM - 1) / kBM);
+    }
+}
+
+__global__ void k_cast_f32_bf16(const float* __restrict__ src, __nv_bfloat16* __restrict__ dst,
+                                size_t n) {
+    const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+    for (size_t x = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; x < n; x += stride)
+        dst[x] = __float2bfloat16_rn(src[x]);
+}
+
+RouteWorkspace route_workspace_layout(int T, int k, int P) {
+    RouteWorkspace w;
+    const size_t R = static_cast<size_t>(T) * k;
+    w.nchunk = static_cast<int>((R + kRouteChunk - 1) / kRouteChunk);
+    size_t off = 0;
+    w.err_off = off;
+    off = align_up(off + sizeof(int32_t), 256);
+    w.hist_off = off;
+    off = align_up(off + sizeof(int32_t) * static_cast<size_t>(w.nchunk > 0 ? w.nchunk : 1) * (P + 1), 256);
+    w.mblk_off = off;
+    off = align_up(off + sizeof(int32_t) * static_cast<size_t>(P + 2), 256);
+    w.total = off;
+    return w;
+}
+
+cudaError_t launch_route_build(const float* logits, int T, int E, int k, int renorm,
+                               const int32_t* phi, int P, int32_t* topk_ids, float* alpha,
+                               int32_t* offsets, int32_t* rec_tok, int32_t* rec_route,
+                               int32_t* rec_pos, void* ws, cudaStream_t stream,
+                               int* n_launches) {
+    const RouteWorkspace w = route_workspace_layout(T, k, P);
+    char* base = static_cast<char*>(ws);
+    int* err = reinterpret_cast<int*>(base + w.err_off);
+    int32_t* hist = reinterpret_cast<int32_t*>(base + w.hist_off);
+    int32_t* mblk = reinterpret_cast<int32_t*>(base + w.mblk_off);
+    const int R = T * k;
+    const int nb = P + 1;
+    int launches = 0;
+    cudaError_t rc;
+    if (R == 0) {
+        rc = cudaMemsetAsync(err, 0, sizeof(int), stream);
+        if (rc == cudaSuccess) rc = cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (P + 2), stream);
+        if (rc == cudaSuccess) rc = cudaMemsetAsync(mblk, 0, sizeof(int32_t) * (P + 2), stream);
+        if (n_launches) *n_launches += 3;
+        return rc;
+    }
+    // one memset clears the error word and the per-chunk counts (contiguous)
+    rc = cudaMemsetAsync(base + w.err_off, 0,
+                         w.hist_off - w.err_off + sizeof(int32_t) * static_cast<size_t>(w.nchunk) * nb,
+                         stream);
+    if (rc != cudaSuccess) return rc;
+    ++launches;
+    k_route_topk<<<(T + 127) / 128, 128, 0, stream>>>(logits, T, E, k, renorm, phi, P, topk_ids,
+                                                     alpha, hist, err);
+    ++launches;
+    const size_t scan_smem = sizeof(int) * (2 * static_cast<size_t>(nb) + 33);
+    k_route_scan<<<1, 1024, scan_smem, stream>>>(hist, w.nchunk, P, R, offsets, mblk);
+    ++launches;
+    k_route_scatter<<<w.nchunk, kRouteChunk, sizeof(int) * nb, stream>>>(
+        topk_ids, phi, P, k, R, hist, rec_tok, rec_route, rec_pos);
+    ++launches;
+    if (n_launches) *n_launches += launches;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_identity_map(int T, int n_shared, int32_t* offsets, int32_t* rec_tok,
+                                int32_t* mblk, cudaStream_t stream) {
+    const int n = T * n_shared > n_shared + 1 ? T * n_shared : n_shared + 1;
+    k_identity_map<<<(n + 255) / 256, 256, 0, stream>>>(T, n_shared, offsets, rec_tok, mblk);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_cast_f32_bf16(const float* src, void* dst, size_t n, cudaStream_t stream) {
+    if (n == 0) return cudaSuccess;
+    size_t blocks = (n + 255) / 256;
+    if (blocks > 4096) blocks = 4096;
+    k_cast_f32_bf16<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+        src, static_cast<__nv_bfloat16*>(dst), n);
+    return cudaGetLastError();
+}
+
+}  // namespace es

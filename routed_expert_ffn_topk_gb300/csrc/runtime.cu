@@ -1,0 +1,942 @@
+// Host runtime of libestream: the C ABI, the bounded expert arena, the pager
+// and the sequencing of one MoE layer's prefill.
+//
+// "EStream: Fast and Memory-Efficient MoE Prefill through Expert
+// Virtualization on Mobile NPUs":
+//   - section 3.2 / Eq. 3: the arena has three parameter planes B^g, B^u,
+//     B^d with fixed bases; slot s of plane j sits at p_{B^j} + s*S_j. Here
+//     each plane is described once, at bind time, by a TMA tensor map whose
+//     row coordinate s*F (or s*H) addresses the slot: only coordinates change
+//     per invocation, never descriptors.
+//   - section 3.3: P = B*G slots in B banks of G; storage group q of G
+//     experts in the order pi fills one bank; residency states Available ->
+//     Filling -> Ready -> InUse -> Available; a Ready bank with no routed
+//     work is released directly.
+//   - section 3.4: loading overlaps execution; after routing, groups with no
+//     routes are skipped; optionally the first banks are filled in storage
+//     order before the routes are known.
+// GB300 form: the loader is a copy stream issuing cudaMemcpyAsync from pinned
+// host memory; "published after fill" is a CUDA event recorded after a
+// bank's copies and waited on by the compute stream; "released after the
+// last consumer" is an event recorded after the bank's down GEMM and waited
+// on by the copy stream before the bank is refilled.
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <deque>
+#include <new>
+#include <vector>
+
+#include "estream_internal.h"
+
+using namespace es;
+
+namespace {
+
+enum BankState { kAvailable = 0, kFilling = 1, kReady = 2, kInUse = 3 };
+
+struct Bank {
+    int layer = -1, group = -1;  // contents (valid while layer >= 0)
+    bool release_pending = false;
+    cudaEvent_t ready = nullptr;
+    cudaEvent_t released = nullptr;
+};
+
+enum TimedKind { kTRoute = 0, kTGateUp, kTDown, kTShared, kTCombine, kTTotal, kTIo, kTKinds };
+
+struct Timed {
+    int kind;
+    cudaEvent_t a, b;
+};
+
+}  // namespace
+
+struct estream_ctx {
+    estream_arena_desc d{};
+    int P = 0, n_groups = 0, es = 2, num_sms = 0, device = 0;
+    size_t S_gu = 0, S_d = 0, W_e = 0;
+    std::vector<const void*> host_pool;
+    std::vector<int32_t> perm;
+    std::vector<const void*> shared_dev;
+    char *plane_g = nullptr, *plane_u = nullptr, *plane_d = nullptr;
+    CUtensorMap tm_wg{}, tm_wu{}, tm_wd{}, tm_h{}, tm_hs{};
+    std::vector<CUtensorMap> tm_sg, tm_su, tm_sd;
+
+    // library-owned device workspace
+    char* ws = nullptr;
+    size_t ws_bytes = 0;
+    int32_t *d_perm = nullptr, *topk_ids = nullptr, *rec_tok = nullptr, *rec_route = nullptr,
+            *rec_pos = nullptr, *offsets = nullptr, *sh_offsets = nullptr, *sh_mblk = nullptr,
+            *sh_rec_tok = nullptr;
+    float *alpha = nullptr, *out_rows = nullptr, *out_shared = nullptr;
+    float* d_scale = nullptr;                  // [L*E] down-weight scales, storage order
+    std::vector<const float*> shared_scale;    // [L] device pointers into shared buffers
+    void *route_ws = nullptr, *h = nullptr, *h_shared = nullptr;
+    int* dev_err = nullptr;
+    int32_t* h_offsets = nullptr;  // pinned host copy of offsets
+
+    cudaStream_t copy_stream = nullptr;
+    cudaEvent_t copy_done = nullptr, preload_done = nullptr;
+    bool preload_pending = false;
+    std::vector<Bank> banks;
+
+    bool timing = false;
+    estream_stats stats{};
+    std::vector<Timed> timed;
+    std::vector<cudaEvent_t> event_pool;
+    std::vector<int32_t> trace;
+    int fault_layer = -1, fault_group = -1;
+};
+
+namespace {
+
+cudaEvent_t pool_event(estream_ctx* c) {
+    if (!c->event_pool.empty()) {
+        cudaEvent_t e = c->event_pool.back();
+        c->event_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    return e;
+}
+
+// Record a (start, end) pair around some work when timing is on.
+struct TimedScope {
+    estream_ctx* c;
+    cudaStream_t s;
+    int kind;
+    cudaEvent_t a = nullptr;
+    TimedScope(estream_ctx* c_, cudaStream_t s_, int kind_) : c(c_), s(s_), kind(kind_) {
+        if (c->timing) {
+            a = pool_event(c);
+            if (a) cudaEventRecord(a, s);
+        }
+    }
+    void end() {
+        if (!a) return;
+        cudaEvent_t b = pool_event(c);
+        if (b) {
+            cudaEventRecord(b, s);
+            c->timed.push_back({kind, a, b});
+        } else {
+            c->event_pool.push_back(a);
+        }
+        a = nullptr;
+    }
+    ~TimedScope() { end(); }
+};
+
+void trace_state(estream_ctx* c, int bank, int layer, int group, int state) {
+    c->trace.push_back(bank);
+    c->trace.push_back(layer);
+    c->trace.push_back(group);
+    c->trace.push_back(state);
+}
+
+bool device_supported(int dev) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess)
+        return false;
+    if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        return false;
+    return major == 10 && minor == 3;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+float bf16_bits_to_float(uint16_t b) {
+    uint32_t u = static_cast<uint32_t>(b) << 16;
+    float f;
+    std::memcpy(&f, &u, sizeof(f));
+    return f;
+}
+
+// Offline conversion of one expert's down plane (n elements). bf16: store
+// fp16(w * 2^s) with the largest |w| scaled into [2^14, 2^15) and return
+// 2^-s; fp32: copy and return 1.
+float convert_down(const void* src, size_t n, estream_dtype t, void* dst) {
+    if (t == ESTREAM_F32) {
+        std::memcpy(dst, src, n * sizeof(float));
+        return 1.0f;
+    }
+    const uint16_t* w = static_cast<const uint16_t*>(src);
+    float mx = 0.0f;
+    for (size_t x = 0; x < n; ++x) mx = std::max(mx, std::fabs(bf16_bits_to_float(w[x])));
+    int s = 0;
+    if (mx > 0.0f && std::isfinite(mx)) {
+        int ex = 0;
+        std::frexp(mx, &ex);  // mx = m * 2^ex, m in [0.5, 1)
+        s = 15 - ex;
+    }
+    const float up = std::ldexp(1.0f, s);
+    __half* out = static_cast<__half*>(dst);
+    for (size_t x = 0; x < n; ++x) out[x] = __float2half_rn(bf16_bits_to_float(w[x]) * up);
+    return std::ldexp(1.0f, -s);
+}
+
+size_t elem_size(estream_dtype t) { return t == ESTREAM_F32 ? 4 : 2; }
+
+estream_status desc_shape_ok(const estream_arena_desc* d) {
+    if (!d) return ESTREAM_ERR_INVALID_ARG;
+    if (d->wdtype != ESTREAM_F32 && d->wdtype != ESTREAM_BF16) return ESTREAM_ERR_UNSUPPORTED;
+    if (d->E < 1 || d->E > kMaxE || d->H < 256 || d->F < 128) return ESTREAM_ERR_INVALID_ARG;
+    if (d->H % 256 != 0 || d->F % 128 != 0) return ESTREAM_ERR_INVALID_ARG;
+    if (d->G < 1 || d->B < 1 || static_cast<long long>(d->G) * d->B > kMaxP)
+        return ESTREAM_ERR_INVALID_ARG;
+    return ESTREAM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* estream_status_string(estream_status s) {
+    switch (s) {
+        case ESTREAM_OK: return "ok";
+        case ESTREAM_ERR_INVALID_ARG: return "invalid argument";
+        case ESTREAM_ERR_CAPACITY: return "capacity exceeded";
+        case ESTREAM_ERR_NOT_BOUND: return "context not bound";
+        case ESTREAM_ERR_CUDA: return "CUDA error";
+        case ESTREAM_ERR_PAGER: return "pager failure";
+        case ESTREAM_ERR_TIMEOUT: return "device wait timed out";
+        case ESTREAM_ERR_DEVICE: return "device-detected data error";
+        case ESTREAM_ERR_UNSUPPORTED: return "unsupported device or type";
+    }
+    return "unknown status";
+}
+
+int estream_version(void) { return 10000; }
+
+size_t estream_route_workspace_bytes(int T, int E, int k, int P) {
+    if (T < 0 || E < 1 || k < 1 || P < 0 || P > kMaxP) return 0;
+    (void)E;
+    return route_workspace_layout(T, k, P).total;
+}
+
+estream_status estream_route_build(const float* logits, int T, int E, int k, int renorm,
+                                   const int32_t* phi, int P, int32_t* topk_ids, float* alpha,
+                                   int32_t* offsets, int32_t* rec_tok, int32_t* rec_route,
+                                   void* workspace, size_t workspace_bytes, void* cuda_stream) {
+    if (T < 0 || E < 1 || E > kMaxE || k < 1 || k > E || k > kMaxK || P < 0 || P > kMaxP)
+        return ESTREAM_ERR_INVALID_ARG;
+    if (!phi && P != E) return ESTREAM_ERR_INVALID_ARG;
+    if (!offsets || !workspace || !aligned(workspace, 256)) return ESTREAM_ERR_INVALID_ARG;
+    if (T > 0 && (!logits || !topk_ids || !alpha || !rec_tok || !rec_route))
+        return ESTREAM_ERR_INVALID_ARG;
+    if (static_cast<long long>(T) * k > (1ll << 30)) return ESTREAM_ERR_CAPACITY;
+    if (workspace_bytes < route_workspace_layout(T, k, P).total) return ESTREAM_ERR_CAPACITY;
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    cudaError_t rc = launch_route_build(logits, T, E, k, renorm, phi, P, topk_ids, alpha, offsets,
+                                        rec_tok, rec_route, nullptr, workspace, s, nullptr);
+    return rc == cudaSuccess ? ESTREAM_OK : ESTREAM_ERR_CUDA;
+}
+
+estream_status estream_workspace_error(void* workspace, void* cuda_stream) {
+    if (!workspace) return ESTREAM_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    int* err = reinterpret_cast<int*>(static_cast<char*>(workspace) +
+                                      route_workspace_layout(0, 1, 0).err_off);
+    int host = 0;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return ESTREAM_ERR_CUDA;
+    if (cudaMemcpy(&host, err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return ESTREAM_ERR_CUDA;
+    if (cudaMemset(err, 0, sizeof(int)) != cudaSuccess) return ESTREAM_ERR_CUDA;
+    if (host == kDevErrNone) return ESTREAM_OK;
+    return host == kDevErrTimeout ? ESTREAM_ERR_TIMEOUT : ESTREAM_ERR_DEVICE;
+}
+
+size_t estream_arena_bytes(int E, int H, int F, int G, int B, estream_dtype wdtype) {
+    (void)E;
+    if (H < 1 || F < 1 || G < 1 || B < 1) return 0;
+    return static_cast<size_t>(B) * G * 3 * static_cast<size_t>(H) * F * elem_size(wdtype);
+}
+
+size_t estream_pool_bytes(int E, int H, int F, estream_dtype wdtype) {
+    if (E < 1 || H < 1 || F < 1) return 0;
+    return static_cast<size_t>(E) * 3 * static_cast<size_t>(H) * F * elem_size(wdtype) +
+           align_up(sizeof(float) * E, 16);
+}
+
+size_t estream_shared_bytes(int n_shared, int H, int F_shared, estream_dtype wdtype) {
+    if (n_shared < 1 || H < 1 || F_shared < 1) return 0;
+    return static_cast<size_t>(n_shared) * 3 * static_cast<size_t>(H) * F_shared *
+               elem_size(wdtype) +
+           align_up(sizeof(float) * n_shared, 16);
+}
+
+estream_status estream_pack_experts(const estream_arena_desc* d, int layer, const void* wg,
+                                    const void* wu, const void* wd, void* host_pool_out) {
+    estream_status st = desc_shape_ok(d);
+    if (st != ESTREAM_OK) return st;
+    if (!wg || !wu || !wd || !host_pool_out || layer < 0 || layer >= std::max(1, d->L))
+        return ESTREAM_ERR_INVALID_ARG;
+    const size_t es_ = elem_size(d->wdtype);
+    const size_t S = static_cast<size_t>(d->H) * d->F * es_;  // one plane slice of one expert
+    const size_t W = 3 * S;
+    const int32_t* perm = d->perm ? d->perm + static_cast<size_t>(layer) * d->E : nullptr;
+    std::vector<char> seen(d->E, 0);
+    for (int e = 0; e < d->E; ++e) {
+        const int pos = perm ? perm[e] : e;
+        if (pos < 0 || pos >= d->E || seen[pos]) return ESTREAM_ERR_INVALID_ARG;
+        seen[pos] = 1;
+    }
+    char* out = static_cast<char*>(host_pool_out);
+    float* scales = reinterpret_cast<float*>(out + static_cast<size_t>(d->E) * W);
+    const size_t n_elem = static_cast<size_t>(d->H) * d->F;
+    for (int e = 0; e < d->E; ++e) {
+        const int pos = perm ? perm[e] : e;
+        const int q = pos / d->G, r = pos % d->G;
+        const int n_q = std::min(d->G, d->E - q * d->G);
+        char* grp = out + static_cast<size_t>(q) * d->G * W;
+        std::memcpy(grp + static_cast<size_t>(r) * S, static_cast<const char*>(wg) + e * S, S);
+        std::memcpy(grp + static_cast<size_t>(n_q) * S + static_cast<size_t>(r) * S,
+                    static_cast<const char*>(wu) + e * S, S);
+        void* down = grp + 2 * static_cast<size_t>(n_q) * S + static_cast<size_t>(r) * S;
+        scales[pos] = convert_down(static_cast<const char*>(wd) + e * S, n_elem, d->wdtype, down);
+    }
+    return ESTREAM_OK;
+}
+
+estream_status estream_pack_shared(const estream_arena_desc* d, const void* sg, const void* su,
+                                   const void* sd, void* out) {
+    if (!d || !sg || !su || !sd || !out || d->n_shared < 1 || d->F_shared < 1 || d->H < 1)
+        return ESTREAM_ERR_INVALID_ARG;
+    if (d->wdtype != ESTREAM_F32 && d->wdtype != ESTREAM_BF16) return ESTREAM_ERR_UNSUPPORTED;
+    const size_t n_elem = static_cast<size_t>(d->H) * d->F_shared;
+    const size_t S = n_elem * elem_size(d->wdtype);
+    const size_t ns = static_cast<size_t>(d->n_shared);
+    char* o = static_cast<char*>(out);
+    std::memcpy(o, sg, ns * S);
+    std::memcpy(o + ns * S, su, ns * S);
+    float* scales = reinterpret_cast<float*>(o + 3 * ns * S);
+    for (size_t s = 0; s < ns; ++s)
+        scales[s] = convert_down(static_cast<const char*>(sd) + s * S, n_elem, d->wdtype,
+                                 o + 2 * ns * S + s * S);
+    return ESTREAM_OK;
+}
+
+void estream_unbind(estream_ctx* c);
+
+estream_status estream_bind_arena(estream_ctx** out, const estream_arena_desc* d) {
+    if (!out) return ESTREAM_ERR_INVALID_ARG;
+    *out = nullptr;
+    estream_status st = desc_shape_ok(d);
+    if (st != ESTREAM_OK) return st;
+    if (d->L < 1 || d->T_max < 1 || d->k_max < 1 || d->k_max > d->E || d->k_max > kMaxK ||
+        d->Q < 1 || !d->arena_dev || !aligned(d->arena_dev, 256) || !d->host_pool)
+        return ESTREAM_ERR_INVALID_ARG;
+    if (d->schedule != ESTREAM_SCHED_AFTER_ROUTING && d->schedule != ESTREAM_SCHED_PREFETCH)
+        return ESTREAM_ERR_INVALID_ARG;
+    if (d->n_shared < 0 || (d->n_shared > 0 && (d->F_shared < 128 || d->F_shared % 128 != 0 ||
+                                                 !d->shared_dev)))
+        return ESTREAM_ERR_INVALID_ARG;
+    if (d->arena_bytes < estream_arena_bytes(d->E, d->H, d->F, d->G, d->B, d->wdtype))
+        return ESTREAM_ERR_CAPACITY;
+    if (static_cast<long long>(d->T_max) * d->k_max > (1ll << 30)) return ESTREAM_ERR_CAPACITY;
+    for (int l = 0; l < d->L; ++l) {
+        if (!d->host_pool[l]) return ESTREAM_ERR_INVALID_ARG;
+        if (d->n_shared > 0 && (!d->shared_dev[l] || !aligned(d->shared_dev[l], 16)))
+            return ESTREAM_ERR_INVALID_ARG;
+        if (d->perm) {
+            std::vector<char> seen(d->E, 0);
+            for (int e = 0; e < d->E; ++e) {
+                const int p = d->perm[static_cast<size_t>(l) * d->E + e];
+                if (p < 0 || p >= d->E || seen[p]) return ESTREAM_ERR_INVALID_ARG;
+                seen[p] = 1;
+            }
+        }
+    }
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return ESTREAM_ERR_CUDA;
+    if (!device_supported(dev)) return ESTREAM_ERR_UNSUPPORTED;
+
+    estream_ctx* c = new (std::nothrow) estream_ctx();
+    if (!c) return ESTREAM_ERR_CUDA;
+    c->d = *d;
+    c->device = dev;
+    c->P = d->B * d->G;
+    c->n_groups = (d->E + d->G - 1) / d->G;
+    c->es = static_cast<int>(elem_size(d->wdtype));
+    c->S_gu = static_cast<size_t>(d->F) * d->H * c->es;
+    c->S_d = c->S_gu;
+    c->W_e = 3 * c->S_gu;
+    c->host_pool.assign(d->host_pool, d->host_pool + d->L);
+    c->perm.resize(static_cast<size_t>(d->L) * d->E);
+    for (int l = 0; l < d->L; ++l)
+        for (int e = 0; e < d->E; ++e)
+            c->perm[static_cast<size_t>(l) * d->E + e] =
+                d->perm ? d->perm[static_cast<size_t>(l) * d->E + e] : e;
+    if (d->n_shared > 0) c->shared_dev.assign(d->shared_dev, d->shared_dev + d->L);
+    c->d.host_pool = nullptr;
+    c->d.perm = nullptr;
+    c->d.shared_dev = nullptr;
+    cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, dev);
+
+    // Eq. 3: plane bases; slot s of plane j at base_j + s * S_j
+    const size_t plane_bytes = static_cast<size_t>(c->P) * c->S_gu;
+    c->plane_g = static_cast<char*>(d->arena_dev);
+    c->plane_u = c->plane_g + plane_bytes;
+    c->plane_d = c->plane_u + plane_bytes;
+
+    const bool f32 = d->wdtype == ESTREAM_F32;
+    const int R_cap = d->T_max * d->k_max;
+    const int E = d->E;
+
+    // workspace layout
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off = align_up(off + (bytes ? bytes : 1), 1024);
+        return o;
+    };
+    const size_t o_err = take(sizeof(int));
+    const size_t o_perm = take(sizeof(int32_t) * c->perm.size());
+    const size_t o_scale = take(sizeof(float) * c->perm.size());
+    const size_t o_ids = take(sizeof(int32_t) * R_cap);
+    const size_t o_alpha = take(sizeof(float) * R_cap);
+    const size_t o_rtok = take(sizeof(int32_t) * R_cap);
+    const size_t o_rroute = take(sizeof(int32_t) * R_cap);
+    const size_t o_rpos = take(sizeof(int32_t) * R_cap);
+    const size_t o_offs = take(sizeof(int32_t) * (E + 2));
+    const size_t o_rws = take(route_workspace_layout(d->T_max, d->k_max, E).total);
+    const size_t o_h = take(static_cast<size_t>(R_cap) * d->F * c->es);
+    size_t o_sh_offs = 0, o_sh_mblk = 0, o_sh_tok = 0, o_hs = 0, o_outs = 0, o_out = 0;
+    const int RS_cap = d->n_shared * d->T_max;
+    if (d->n_shared > 0) {
+        o_sh_offs = take(sizeof(int32_t) * (d->n_shared + 2));
+        o_sh_mblk = take(sizeof(int32_t) * (d->n_shared + 2));
+        o_sh_tok = take(sizeof(int32_t) * RS_cap);
+        o_hs = take(static_cast<size_t>(RS_cap) * d->F_shared * c->es);
+    }
+    if (d->deterministic) {
+        o_out = take(static_cast<size_t>(R_cap) * d->H * sizeof(float));
+        if (d->n_shared > 0) o_outs = take(static_cast<size_t>(RS_cap) * d->H * sizeof(float));
+    }
+    c->ws_bytes = off;
+    st = ESTREAM_ERR_CUDA;
+    do {
+        if (cudaMalloc(&c->ws, c->ws_bytes) != cudaSuccess) break;
+        c->dev_err = reinterpret_cast<int*>(c->ws + o_err);
+        c->d_perm = reinterpret_cast<int32_t*>(c->ws + o_perm);
+        c->d_scale = reinterpret_cast<float*>(c->ws + o_scale);
+        c->topk_ids = reinterpret_cast<int32_t*>(c->ws + o_ids);
+        c->alpha = reinterpret_cast<float*>(c->ws + o_alpha);
+        c->rec_tok = reinterpret_cast<int32_t*>(c->ws + o_rtok);
+        c->rec_route = reinterpret_cast<int32_t*>(c->ws + o_rroute);
+        c->rec_pos = reinterpret_cast<int32_t*>(c->ws + o_rpos);
+        c->offsets = reinterpret_cast<int32_t*>(c->ws + o_offs);
+        c->route_ws = c->ws + o_rws;
+        c->h = c->ws + o_h;
+        if (d->n_shared > 0) {
+            c->sh_offsets = reinterpret_cast<int32_t*>(c->ws + o_sh_offs);
+            c->sh_mblk = reinterpret_cast<int32_t*>(c->ws + o_sh_mblk);
+            c->sh_rec_tok = reinterpret_cast<int32_t*>(c->ws + o_sh_tok);
+            c->h_shared = c->ws + o_hs;
+        }
+        if (d->deterministic) {
+            c->out_rows = reinterpret_cast<float*>(c->ws + o_out);
+            if (d->n_shared > 0) c->out_shared = reinterpret_cast<float*>(c->ws + o_outs);
+        }
+        if (cudaMemset(c->ws, 0, o_perm) != cudaSuccess) break;
+        if (cudaMemcpy(c->d_perm, c->perm.data(), sizeof(int32_t) * c->perm.size(),
+                       cudaMemcpyHostToDevice) != cudaSuccess)
+            break;
+        bool sc_ok = true;
+        for (int l = 0; l < d->L && sc_ok; ++l)
+            sc_ok = cudaMemcpy(c->d_scale + static_cast<size_t>(l) * E,
+                               static_cast<const char*>(c->host_pool[l]) + static_cast<size_t>(E) * c->W_e,
+                               sizeof(float) * E, cudaMemcpyHostToDevice) == cudaSuccess;
+        if (!sc_ok) break;
+        if (cudaMallocHost(&c->h_offsets, sizeof(int32_t) * (E + 2)) != cudaSuccess) break;
+        if (cudaStreamCreateWithFlags(&c->copy_stream, cudaStreamNonBlocking) != cudaSuccess) break;
+        if (cudaEventCreateWithFlags(&c->copy_done, cudaEventDisableTiming) != cudaSuccess) break;
+        if (cudaEventCreateWithFlags(&c->preload_done, cudaEventDisableTiming) != cudaSuccess) break;
+        c->banks.resize(d->B);
+        bool ev_ok = true;
+        for (auto& b : c->banks) {
+            ev_ok = ev_ok && cudaEventCreateWithFlags(&b.ready, cudaEventDisableTiming) == cudaSuccess;
+            ev_ok = ev_ok &&
+                    cudaEventCreateWithFlags(&b.released, cudaEventDisableTiming) == cudaSuccess;
+        }
+        if (!ev_ok) break;
+        // tensor maps (fixed bases, Eq. 3); the fp32 path reads the planes directly
+        bool tm_ok = true;
+        const CUtensorMapDataType BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+        const CUtensorMapDataType HF = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+        if (d->n_shared > 0) {
+            c->shared_scale.resize(d->L);
+            const size_t sp = static_cast<size_t>(d->n_shared) * d->F_shared * d->H * c->es;
+            for (int l = 0; l < d->L; ++l)
+                c->shared_scale[l] = reinterpret_cast<const float*>(
+                    static_cast<const char*>(c->shared_dev[l]) + 3 * sp);
+        }
+        if (!f32) {
+            tm_ok = tm_ok && encode_tmap_2d(&c->tm_wg, BF, c->plane_g, d->H,
+                                            static_cast<uint64_t>(c->P) * d->F,
+                                            static_cast<uint64_t>(d->H) * 2, 64, 128) == CUDA_SUCCESS;
+            tm_ok = tm_ok && encode_tmap_2d(&c->tm_wu, BF, c->plane_u, d->H,
+                                            static_cast<uint64_t>(c->P) * d->F,
+                                            static_cast<uint64_t>(d->H) * 2, 64, 128) == CUDA_SUCCESS;
+            tm_ok = tm_ok && encode_tmap_2d(&c->tm_wd, HF, c->plane_d, d->F,
+                                            static_cast<uint64_t>(c->P) * d->H,
+                                            static_cast<uint64_t>(d->F) * 2, 64, 256) == CUDA_SUCCESS;
+            tm_ok = tm_ok && encode_tmap_2d(&c->tm_h, HF, c->h, d->F, static_cast<uint64_t>(R_cap),
+                                            static_cast<uint64_t>(d->F) * 2, 64, 128) == CUDA_SUCCESS;
+            if (d->n_shared > 0) {
+                const int Fs = d->F_shared;
+                tm_ok = tm_ok && encode_tmap_2d(&c->tm_hs, HF, c->h_shared, Fs,
+                                                static_cast<uint64_t>(RS_cap),
+                                                static_cast<uint64_t>(Fs) * 2, 64, 128) == CUDA_SUCCESS;
+                c->tm_sg.resize(d->L);
+                c->tm_su.resize(d->L);
+                c->tm_sd.resize(d->L);
+                const size_t sp = static_cast<size_t>(d->n_shared) * Fs * d->H * 2;
+                for (int l = 0; l < d->L && tm_ok; ++l) {
+                    const char* base = static_cast<const char*>(c->shared_dev[l]);
+                    tm_ok = tm_ok && encode_tmap_2d(&c->tm_sg[l], BF, base, d->H,
+                                                    static_cast<uint64_t>(d->n_shared) * Fs,
+                                                    static_cast<uint64_t>(d->H) * 2, 64, 128) == CUDA_SUCCESS;
+                    tm_ok = tm_ok && encode_tmap_2d(&c->tm_su[l], BF, base + sp, d->H,
+                                                    static_cast<uint64_t>(d->n_shared) * Fs,
+                                                    static_cast<uint64_t>(d->H) * 2, 64, 128) == CUDA_SUCCESS;
+                    tm_ok = tm_ok && encode_tmap_2d(&c->tm_sd[l], HF, base + 2 * sp, Fs,
+                                                    static_cast<uint64_t>(d->n_shared) * d->H,
+                                                    static_cast<uint64_t>(Fs) * 2, 64, 256) == CUDA_SUCCESS;
+                }
+            }
+        }
+        if (!tm_ok) break;
+        st = ESTREAM_OK;
+    } while (false);
+    if (st != ESTREAM_OK) {
+        estream_unbind(c);
+        return st;
+    }
+    *out = c;
+    return ESTREAM_OK;
+}
+
+}  // extern "C"
+
+namespace {
+
+// Copies of storage group q of `layer` into bank b: three plane slices.
+estream_status fill_bank(estream_ctx* c, int layer, int q, int b, size_t* bytes) {
+    const int G = c->d.G;
+    const int n_q = std::min(G, c->d.E - q * G);
+    const char* src = static_cast<const char*>(c->host_pool[layer]) +
+                      static_cast<size_t>(q) * G * c->W_e;
+    const size_t gbytes = static_cast<size_t>(n_q) * c->S_gu;
+    const size_t dbytes = static_cast<size_t>(n_q) * c->S_d;
+    Bank& bk = c->banks[b];
+    if (bk.release_pending) {
+        if (cudaStreamWaitEvent(c->copy_stream, bk.released, 0) != cudaSuccess) return ESTREAM_ERR_CUDA;
+        bk.release_pending = false;
+    }
+    trace_state(c, b, layer, q, kFilling);
+    bk.layer = layer;
+    bk.group = q;
+    TimedScope io(c, c->copy_stream, kTIo);
+    const size_t slot0 = static_cast<size_t>(b) * G;
+    if (cudaMemcpyAsync(c->plane_g + slot0 * c->S_gu, src, gbytes, cudaMemcpyHostToDevice,
+                        c->copy_stream) != cudaSuccess ||
+        cudaMemcpyAsync(c->plane_u + slot0 * c->S_gu, src + gbytes, gbytes, cudaMemcpyHostToDevice,
+                        c->copy_stream) != cudaSuccess ||
+        cudaMemcpyAsync(c->plane_d + slot0 * c->S_d, src + 2 * gbytes, dbytes,
+                        cudaMemcpyHostToDevice, c->copy_stream) != cudaSuccess)
+        return ESTREAM_ERR_CUDA;
+    io.end();
+    if (cudaEventRecord(bk.ready, c->copy_stream) != cudaSuccess) return ESTREAM_ERR_CUDA;
+    trace_state(c, b, layer, q, kReady);
+    *bytes += 2 * gbytes + dbytes;
+    return ESTREAM_OK;
+}
+
+// K2 + K3 over segments [seg_begin, seg_begin + seg_count) of the routed
+// route map, whose experts sit in consecutive arena slots from slot_base.
+estream_status run_routed(estream_ctx* c, cudaStream_t s, const CUtensorMap* tm_x, const void* X,
+                          int layer, const int32_t* mblk, int seg_begin, int seg_count,
+                          int slot_base, int max_tiles_m, int max_rows, float* Y) {
+    GemmSegments seg{};
+    seg.offsets = c->offsets;
+    seg.mblk = mblk;
+    seg.rec_tok = c->rec_tok;
+    seg.rec_route = c->rec_route;
+    seg.alpha = c->alpha;
+    seg.seg_scale = c->d_scale + static_cast<size_t>(layer) * c->d.E;
+    seg.seg_begin = seg_begin;
+    seg.seg_count = seg_count;
+    seg.slot_base = slot_base;
+    seg.max_tiles_m = max_tiles_m;
+    const bool f32 = c->d.wdtype == ESTREAM_F32;
+    {
+        TimedScope ts(c, s, kTGateUp);
+        const cudaError_t rc =
+            f32 ? launch_gateup_f32(static_cast<const float*>(X),
+                                    reinterpret_cast<const float*>(c->plane_g),
+                                    reinterpret_cast<const float*>(c->plane_u), seg,
+                                    static_cast<float*>(c->h), c->d.H, c->d.F, max_rows, s)
+                : launch_gateup(tm_x, &c->tm_wg, &c->tm_wu, seg, c->h, c->d.H, c->d.F, c->d.F,
+                                c->dev_err, c->num_sms, s);
+        if (rc != cudaSuccess) return ESTREAM_ERR_CUDA;
+        c->stats.n_gateup += c->timing ? 1 : 0;
+    }
+    {
+        TimedScope ts(c, s, kTDown);
+        const cudaError_t rc =
+            f32 ? launch_down_f32(static_cast<const float*>(c->h),
+                                  reinterpret_cast<const float*>(c->plane_d), seg, Y, c->out_rows,
+                                  c->d.H, c->d.F, max_rows, s)
+                : launch_down(&c->tm_h, &c->tm_wd, seg, Y, c->out_rows, c->d.H, c->d.F, c->d.H,
+                              c->dev_err, c->num_sms, s);
+        if (rc != cudaSuccess) return ESTREAM_ERR_CUDA;
+        c->stats.n_down += c->timing ? 1 : 0;
+    }
+    c->stats.launches += 2;
+    return ESTREAM_OK;
+}
+
+// Shared experts: identity route map over all T tokens, weight 1.
+estream_status run_shared(estream_ctx* c, cudaStream_t s, const CUtensorMap* tm_x, const void* X,
+                          int layer, int T, float* Y) {
+    TimedScope ts(c, s, kTShared);
+    const int ns = c->d.n_shared;
+    if (launch_identity_map(T, ns, c->sh_offsets, c->sh_rec_tok, c->sh_mblk, s) != cudaSuccess)
+        return ESTREAM_ERR_CUDA;
+    GemmSegments seg{};
+    seg.offsets = c->sh_offsets;
+    seg.mblk = c->sh_mblk;
+    seg.rec_tok = c->sh_rec_tok;
+    seg.rec_route = nullptr;
+    seg.alpha = nullptr;
+    seg.seg_scale = c->shared_scale[layer];
+    seg.seg_begin = 0;
+    seg.seg_count = ns;
+    seg.slot_base = 0;
+    seg.max_tiles_m = ns * ((T + kBM - 1) / kBM);
+    const int Fs = c->d.F_shared;
+    cudaError_t rc;
+    if (c->d.wdtype == ESTREAM_F32) {
+        const float* base = static_cast<const float*>(c->shared_dev[layer]);
+        const size_t sp = static_cast<size_t>(ns) * Fs * c->d.H;
+        rc = launch_gateup_f32(static_cast<const float*>(X), base, base + sp, seg,
+                               static_cast<float*>(c->h_shared), c->d.H, Fs, ns * T, s);
+        if (rc == cudaSuccess)
+            rc = launch_down_f32(static_cast<const float*>(c->h_shared), base + 2 * sp, seg, Y,
+                                 c->out_shared, c->d.H, Fs, ns * T, s);
+    } else {
+        rc = launch_gateup(tm_x, &c->tm_sg[layer], &c->tm_su[layer], seg, c->h_shared, c->d.H, Fs,
+                           Fs, c->dev_err, c->num_sms, s);
+        if (rc == cudaSuccess)
+            rc = launch_down(&c->tm_hs, &c->tm_sd[layer], seg, Y, c->out_shared, c->d.H, Fs,
+                             c->d.H, c->dev_err, c->num_sms, s);
+    }
+    if (rc != cudaSuccess) return ESTREAM_ERR_CUDA;
+    c->stats.launches += 3;
+    return ESTREAM_OK;
+}
+
+bool layer_resident(const estream_ctx* c, int layer) {
+    if (c->n_groups > c->d.B) return false;
+    for (int q = 0; q < c->n_groups; ++q)
+        if (c->banks[q].layer != layer || c->banks[q].group != q) return false;
+    return true;
+}
+
+void drain(estream_ctx* c, cudaStream_t s) {
+    cudaStreamSynchronize(c->copy_stream);
+    cudaStreamSynchronize(s);
+}
+
+}  // namespace
+
+extern "C" {
+
+estream_status estream_arena_preload(estream_ctx* c, int layer, void* cuda_stream) {
+    if (!c) return ESTREAM_ERR_NOT_BOUND;
+    if (layer < 0 || layer >= c->d.L) return ESTREAM_ERR_INVALID_ARG;
+    if (c->n_groups > c->d.B) return ESTREAM_ERR_CAPACITY;
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    c->trace.clear();
+    // the copy stream must not overwrite banks that earlier work on `s` reads
+    if (cudaEventRecord(c->copy_done, s) != cudaSuccess ||
+        cudaStreamWaitEvent(c->copy_stream, c->copy_done, 0) != cudaSuccess)
+        return ESTREAM_ERR_CUDA;
+    size_t bytes = 0;
+    for (int q = 0; q < c->n_groups; ++q) {
+        estream_status st = fill_bank(c, layer, q, q, &bytes);
+        if (st != ESTREAM_OK) return st;
+    }
+    c->stats.h2d_bytes += static_cast<double>(bytes);
+    c->stats.groups_loaded += c->n_groups;
+    if (cudaEventRecord(c->preload_done, c->copy_stream) != cudaSuccess) return ESTREAM_ERR_CUDA;
+    c->preload_pending = true;
+    return ESTREAM_OK;
+}
+
+estream_status estream_arena_invalidate(estream_ctx* c) {
+    if (!c) return ESTREAM_ERR_NOT_BOUND;
+    if (cudaStreamSynchronize(c->copy_stream) != cudaSuccess) return ESTREAM_ERR_CUDA;
+    for (auto& b : c->banks) {
+        b.layer = -1;
+        b.group = -1;
+    }
+    return ESTREAM_OK;
+}
+
+estream_status estream_moe_layer_prefill(estream_ctx* c, int layer, const void* X,
+                                         const float* logits, int T, int k, int renorm, float* Y,
+                                         void* cuda_stream) {
+    if (!c) return ESTREAM_ERR_NOT_BOUND;
+    if (layer < 0 || layer >= c->d.L || !X || !logits || !Y || T < 1 || k < 1 || k > c->d.E)
+        return ESTREAM_ERR_INVALID_ARG;
+    if (!aligned(X, 16) || !aligned(Y, 16)) return ESTREAM_ERR_INVALID_ARG;
+    if (T > c->d.T_max || k > c->d.k_max) return ESTREAM_ERR_CAPACITY;
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    const int E = c->d.E, G = c->d.G, H = c->d.H;
+    const bool f32 = c->d.wdtype == ESTREAM_F32;
+    c->trace.clear();
+    c->stats.calls += 1;
+    TimedScope total(c, s, kTTotal);
+
+    CUtensorMap tm_x{};
+    if (!f32 && encode_tmap_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, H, T,
+                               static_cast<uint64_t>(H) * 2, 64, 1) != CUDA_SUCCESS)
+        return ESTREAM_ERR_CUDA;
+    if (c->preload_pending) {
+        if (cudaStreamWaitEvent(s, c->preload_done, 0) != cudaSuccess) return ESTREAM_ERR_CUDA;
+        c->preload_pending = false;
+    }
+    const bool resident = layer_resident(c, layer);
+    const int R = T * k;
+
+    // optional early fill of free banks in storage order (section 3.4)
+    std::deque<int> free_banks;
+    for (int b = 0; b < c->d.B; ++b) free_banks.push_back(b);
+    std::vector<int> prefetched(c->n_groups, -1);
+    size_t bytes = 0;
+    if (!resident && c->d.schedule == ESTREAM_SCHED_PREFETCH) {
+        const int npre = std::min(c->d.B, c->n_groups);
+        for (int q = 0; q < npre; ++q) {
+            if (layer == c->fault_layer && q == c->fault_group) break;  // handled below
+            const int b = free_banks.front();
+            free_banks.pop_front();
+            estream_status st = fill_bank(c, layer, q, b, &bytes);
+            if (st != ESTREAM_OK) { drain(c, s); return st; }
+            prefetched[q] = b;
+        }
+    }
+
+    // K1: routing + route map over logical experts in storage order (Phi = pi, P = E)
+    {
+        TimedScope ts(c, s, kTRoute);
+        int launches = 0;
+        if (launch_route_build(logits, T, E, k, renorm, c->d_perm + static_cast<size_t>(layer) * E, E,
+                               c->topk_ids, c->alpha, c->offsets, c->rec_tok, c->rec_route,
+                               c->d.deterministic ? c->rec_pos : nullptr, c->route_ws, s,
+                               &launches) != cudaSuccess) {
+            drain(c, s);
+            return ESTREAM_ERR_CUDA;
+        }
+        c->stats.launches += launches;
+    }
+    const int32_t* mblk = reinterpret_cast<const int32_t*>(
+        static_cast<char*>(c->route_ws) + route_workspace_layout(T, k, E).mblk_off);
+    float* Y_routed = c->d.deterministic ? nullptr : Y;
+
+    // shared experts need no arena: they run first and overlap the first fills
+    if (c->d.n_shared > 0) {
+        estream_status st = run_shared(c, s, &tm_x, X, layer, T, c->d.deterministic ? nullptr : Y);
+        if (st != ESTREAM_OK) { drain(c, s); return st; }
+    }
+
+    estream_status st = ESTREAM_OK;
+    if (resident) {
+        // every group sits in bank q: one launch pair over all slots, no host sync
+        for (int q = 0; q < c->n_groups; ++q) trace_state(c, q, layer, q, kInUse);
+        st = run_routed(c, s, &tm_x, X, layer, mblk, 0, E, 0, (R + kBM - 1) / kBM + E, R, Y_routed);
+        c->stats.groups_hit += c->n_groups;
+        for (int q = 0; q < c->n_groups && st == ESTREAM_OK; ++q) {
+            if (cudaEventRecord(c->banks[q].released, s) != cudaSuccess) st = ESTREAM_ERR_CUDA;
+            c->banks[q].release_pending = true;
+            trace_state(c, q, layer, q, kAvailable);
+        }
+    } else {
+        // routes known -> per-group counts on the host (one D2H + sync)
+        if (cudaMemcpyAsync(c->h_offsets, c->offsets, sizeof(int32_t) * (E + 2),
+                            cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+            cudaStreamSynchronize(s) != cudaSuccess) {
+            drain(c, s);
+            return ESTREAM_ERR_CUDA;
+        }
+        for (int q = 0; q < c->n_groups && st == ESTREAM_OK; ++q) {
+            const int s0 = q * G, s1 = std::min(E, s0 + G);
+            const int cnt = c->h_offsets[s1] - c->h_offsets[s0];
+            int b = prefetched[q];
+            if (cnt == 0) {
+                c->stats.groups_skipped += 1;
+                if (b >= 0) {  // a Ready bank with no routed work is released directly
+                    trace_state(c, b, layer, q, kAvailable);
+                    free_banks.push_front(b);
+                }
+                continue;
+            }
+            if (b < 0) {
+                if (layer == c->fault_layer && q == c->fault_group) {
+                    drain(c, s);
+                    return ESTREAM_ERR_PAGER;
+                }
+                b = free_banks.front();
+                free_banks.pop_front();
+                st = fill_bank(c, layer, q, b, &bytes);
+                if (st != ESTREAM_OK) break;
+            }
+            c->stats.groups_loaded += 1;
+            if (cudaStreamWaitEvent(s, c->banks[b].ready, 0) != cudaSuccess) { st = ESTREAM_ERR_CUDA; break; }
+            trace_state(c, b, layer, q, kInUse);
+            int mt = 0;
+            for (int e = s0; e < s1; ++e)
+                mt += (c->h_offsets[e + 1] - c->h_offsets[e] + kBM - 1) / kBM;
+            st = run_routed(c, s, &tm_x, X, layer, mblk, s0, s1 - s0, b * G, mt, cnt, Y_routed);
+            if (st != ESTREAM_OK) break;
+            if (cudaEventRecord(c->banks[b].released, s) != cudaSuccess) { st = ESTREAM_ERR_CUDA; break; }
+            c->banks[b].release_pending = true;
+            trace_state(c, b, layer, q, kAvailable);
+            free_banks.push_back(b);
+        }
+        // the caller's stream also covers the copies of this call
+        if (st == ESTREAM_OK && (cudaEventRecord(c->copy_done, c->copy_stream) != cudaSuccess ||
+                                 cudaStreamWaitEvent(s, c->copy_done, 0) != cudaSuccess))
+            st = ESTREAM_ERR_CUDA;
+    }
+    if (st != ESTREAM_OK) {
+        drain(c, s);
+        return st;
+    }
+    c->stats.h2d_bytes += static_cast<double>(bytes);
+    if (c->d.deterministic) {
+        TimedScope ts(c, s, kTCombine);
+        if (launch_combine(c->out_rows, c->rec_pos, T, k, H, c->out_shared, c->d.n_shared, Y, s) !=
+            cudaSuccess) {
+            drain(c, s);
+            return ESTREAM_ERR_CUDA;
+        }
+        c->stats.launches += 1;
+    }
+    return ESTREAM_OK;
+}
+
+estream_status estream_set_timing(estream_ctx* c, int on) {
+    if (!c) return ESTREAM_ERR_NOT_BOUND;
+    c->timing = on != 0;
+    return ESTREAM_OK;
+}
+
+estream_status estream_reset_stats(estream_ctx* c) {
+    if (!c) return ESTREAM_ERR_NOT_BOUND;
+    if (cudaStreamSynchronize(c->copy_stream) != cudaSuccess) return ESTREAM_ERR_CUDA;
+    for (auto& t : c->timed) {
+        cudaEventSynchronize(t.b);
+        c->event_pool.push_back(t.a);
+        c->event_pool.push_back(t.b);
+    }
+    c->timed.clear();
+    c->stats = estream_stats{};
+    return ESTREAM_OK;
+}
+
+estream_status estream_last_stats(estream_ctx* c, estream_stats* out) {
+    if (!c) return ESTREAM_ERR_NOT_BOUND;
+    if (!out) return ESTREAM_ERR_INVALID_ARG;
+    estream_status st = ESTREAM_OK;
+    for (auto& t : c->timed) {
+        float ms = 0.0f;
+        if (cudaEventSynchronize(t.b) != cudaSuccess ||
+            cudaEventElapsedTime(&ms, t.a, t.b) != cudaSuccess) {
+            st = ESTREAM_ERR_CUDA;
+            ms = 0.0f;
+        }
+        switch (t.kind) {
+            case kTRoute: c->stats.ms_route += ms; break;
+            case kTGateUp: c->stats.ms_gateup += ms; break;
+            case kTDown: c->stats.ms_down += ms; break;
+            case kTShared: c->stats.ms_shared += ms; break;
+            case kTCombine: c->stats.ms_combine += ms; break;
+            case kTTotal: c->stats.ms_total += ms; break;
+            case kTIo: c->stats.ms_io_busy += ms; break;
+        }
+        c->event_pool.push_back(t.a);
+        c->event_pool.push_back(t.b);
+    }
+    c->timed.clear();
+    *out = c->stats;
+    return st;
+}
+
+estream_status estream_get_device_error(estream_ctx* c) {
+    if (!c) return ESTREAM_ERR_NOT_BOUND;
+    if (cudaStreamSynchronize(c->copy_stream) != cudaSuccess) return ESTREAM_ERR_CUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess) return ESTREAM_ERR_CUDA;
+    int host = 0;
+    if (cudaMemcpy(&host, c->dev_err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return ESTREAM_ERR_CUDA;
+    if (host == kDevErrNone) return ESTREAM_OK;
+    if (cudaMemset(c->dev_err, 0, sizeof(int)) != cudaSuccess) return ESTREAM_ERR_CUDA;
+    return host == kDevErrTimeout ? ESTREAM_ERR_TIMEOUT : ESTREAM_ERR_DEVICE;
+}
+
+estream_status estream_residency_trace(estream_ctx* c, int32_t* out, int cap, int* n) {
+    if (!c) return ESTREAM_ERR_NOT_BOUND;
+    if (!n || cap < 0 || (cap > 0 && !out)) return ESTREAM_ERR_INVALID_ARG;
+    const int events = static_cast<int>(c->trace.size() / 4);
+    const int m = std::min(events, cap);
+    if (m > 0) std::memcpy(out, c->trace.data(), sizeof(int32_t) * 4 * m);
+    *n = events;
+    return ESTREAM_OK;
+}
+
+estream_status estream_inject_pager_fault(estream_ctx* c, int layer, int group) {
+    if (!c) return ESTREAM_ERR_NOT_BOUND;
+    c->fault_layer = group < 0 ? -1 : layer;
+    c->fault_group = group < 0 ? -1 : group;
+    return ESTREAM_OK;
+}
+
+void estream_unbind(estream_ctx* c) {
+    if (!c) return;
+    if (c->copy_stream) cudaStreamSynchronize(c->copy_stream);
+    for (auto& t : c->timed) {
+        cudaEventSynchronize(t.b);
+        cudaEventDestroy(t.a);
+        cudaEventDestroy(t.b);
+    }
+    for (cudaEvent_t e : c->event_pool) cudaEventDestroy(e);
+    for (auto& b : c->banks) {
+        if (b.ready) cudaEventSynchronize(b.ready), cudaEventDestroy(b.ready);
+        if (b.released) cudaEventSynchronize(b.released), cudaEventDestroy(b.released);
+    }
+    if (c->copy_done) cudaEventDestroy(c->copy_done);
+    if (c->preload_done) cudaEventDestroy(c->preload_done);
+    if (c->copy_stream) cudaStreamDestroy(c->copy_stream);
+    if (c->h_offsets) cudaFreeHost(c->h_offsets);
+    if (c->ws) {
+        cudaDeviceSynchronize();
+        cudaFree(c->ws);
+    }
+    delete c;
+}
+
+estream_status estream_cast_f32_bf16(const float* src, void* dst, size_t n, void* cuda_stream) {
+    if ((!src || !dst) && n > 0) return ESTREAM_ERR_INVALID_ARG;
+    return launch_cast_f32_bf16(src, dst, n, static_cast<cudaStream_t>(cuda_stream)) == cudaSuccess
+               ? ESTREAM_OK
+               : ESTREAM_ERR_CUDA;
+}
+
+}  // extern "C"

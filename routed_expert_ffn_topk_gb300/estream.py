@@ -1,0 +1,293 @@
+"""Python binding of libestream (the C ABI in include/estream.h).
+
+Argument marshalling only: torch tensors become device/host pointers, the
+current torch CUDA stream becomes the ``cuda_stream`` argument, and status
+codes become exceptions. Every step of the MoE layer runs in the library's
+CUDA kernels; there is no other implementation behind these names, and the
+module refuses to load when the library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libestream.so")
+
+OK, ERR_INVALID_ARG, ERR_CAPACITY, ERR_NOT_BOUND, ERR_CUDA, ERR_PAGER, ERR_TIMEOUT, \
+    ERR_DEVICE, ERR_UNSUPPORTED = range(9)
+F32, BF16 = 0, 1
+SCHED_AFTER_ROUTING, SCHED_PREFETCH = 0, 1
+STATE_NAMES = {0: "Available", 1: "Filling", 2: "Ready", 3: "InUse"}
+
+
+class EStreamError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+class ArenaDesc(ctypes.Structure):
+    _fields_ = [
+        ("L", ctypes.c_int), ("E", ctypes.c_int), ("H", ctypes.c_int), ("F", ctypes.c_int),
+        ("G", ctypes.c_int), ("B", ctypes.c_int), ("Q", ctypes.c_int),
+        ("wdtype", ctypes.c_int),
+        ("arena_dev", ctypes.c_void_p), ("arena_bytes", ctypes.c_size_t),
+        ("host_pool", ctypes.POINTER(ctypes.c_void_p)),
+        ("perm", ctypes.POINTER(ctypes.c_int32)),
+        ("n_shared", ctypes.c_int), ("F_shared", ctypes.c_int),
+        ("shared_dev", ctypes.POINTER(ctypes.c_void_p)),
+        ("T_max", ctypes.c_int), ("k_max", ctypes.c_int),
+        ("deterministic", ctypes.c_int), ("schedule", ctypes.c_int),
+    ]
+
+
+class Stats(ctypes.Structure):
+    _fields_ = [
+        ("calls", ctypes.c_int), ("launches", ctypes.c_int),
+        ("ms_route", ctypes.c_double), ("ms_gateup", ctypes.c_double),
+        ("ms_down", ctypes.c_double), ("ms_shared", ctypes.c_double),
+        ("ms_combine", ctypes.c_double), ("ms_total", ctypes.c_double),
+        ("n_gateup", ctypes.c_int), ("n_down", ctypes.c_int),
+        ("h2d_bytes", ctypes.c_double),
+        ("groups_loaded", ctypes.c_int), ("groups_skipped", ctypes.c_int),
+        ("groups_hit", ctypes.c_int),
+        ("ms_io_busy", ctypes.c_double),
+    ]
+
+
+_lib = None
+
+# name -> (restype, argtypes)
+_P, _I, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+SIGNATURES = {
+    "estream_status_string": (ctypes.c_char_p, [_I]),
+    "estream_version": (_I, []),
+    "estream_route_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
+    "estream_route_build": (_I, [_P, _I, _I, _I, _I, _P, _I, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "estream_workspace_error": (_I, [_P, _P]),
+    "estream_arena_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "estream_pool_bytes": (_SZ, [_I, _I, _I, _I]),
+    "estream_shared_bytes": (_SZ, [_I, _I, _I, _I]),
+    "estream_pack_shared": (_I, [ctypes.POINTER(ArenaDesc), _P, _P, _P, _P]),
+    "estream_bind_arena": (_I, [ctypes.POINTER(_P), ctypes.POINTER(ArenaDesc)]),
+    "estream_pack_experts": (_I, [ctypes.POINTER(ArenaDesc), _I, _P, _P, _P, _P]),
+    "estream_arena_preload": (_I, [_P, _I, _P]),
+    "estream_arena_invalidate": (_I, [_P]),
+    "estream_moe_layer_prefill": (_I, [_P, _I, _P, _P, _I, _I, _I, _P, _P]),
+    "estream_set_timing": (_I, [_P, _I]),
+    "estream_reset_stats": (_I, [_P]),
+    "estream_last_stats": (_I, [_P, ctypes.POINTER(Stats)]),
+    "estream_get_device_error": (_I, [_P]),
+    "estream_residency_trace": (_I, [_P, _P, _I, ctypes.POINTER(_I)]),
+    "estream_inject_pager_fault": (_I, [_P, _I, _I]),
+    "estream_unbind": (None, [_P]),
+    "estream_cast_f32_bf16": (_I, [_P, _P, _SZ, _P]),
+}
+
+
+def lib():
+    """Load libestream.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"libestream.so not found at {LIB_PATH}; build it with "
+                "`python -c 'import __graft_entry__ as g; g.build()'`")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().estream_status_string(status).decode()
+
+
+def _check(status: int, where: str) -> None:
+    if status != OK:
+        raise EStreamError(status, where)
+
+
+def _dptr(t: torch.Tensor | None):
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream=None):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
+
+
+def version() -> int:
+    return lib().estream_version()
+
+
+# ---------------------------------------------------------------------------
+# routing + route map
+# ---------------------------------------------------------------------------
+
+def route_workspace_bytes(T: int, E: int, k: int, P: int) -> int:
+    return lib().estream_route_workspace_bytes(T, E, k, P)
+
+
+def route_build(logits: torch.Tensor, k: int, renorm: bool, phi: torch.Tensor | None = None,
+                P: int | None = None, out: dict | None = None, workspace: torch.Tensor | None = None,
+                stream=None) -> dict:
+    """estream_route_build on device tensors. Returns a dict with topk_ids,
+    alpha, offsets, rec_tok, rec_route (allocated when not given in ``out``)."""
+    T, E = logits.shape
+    P = E if P is None else P
+    dev = logits.device
+    R = T * k
+    o = dict(out or {})
+    o.setdefault("topk_ids", torch.empty(max(R, 1), dtype=torch.int32, device=dev))
+    o.setdefault("alpha", torch.empty(max(R, 1), dtype=torch.float32, device=dev))
+    o.setdefault("offsets", torch.empty(P + 2, dtype=torch.int32, device=dev))
+    o.setdefault("rec_tok", torch.empty(max(R, 1), dtype=torch.int32, device=dev))
+    o.setdefault("rec_route", torch.empty(max(R, 1), dtype=torch.int32, device=dev))
+    nbytes = route_workspace_bytes(T, E, k, P)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
+    st = lib().estream_route_build(
+        _dptr(logits), T, E, k, int(bool(renorm)), _dptr(phi), P, _dptr(o["topk_ids"]),
+        _dptr(o["alpha"]), _dptr(o["offsets"]), _dptr(o["rec_tok"]), _dptr(o["rec_route"]),
+        _dptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "estream_route_build")
+    o["workspace"] = workspace
+    return o
+
+
+def workspace_error(workspace: torch.Tensor, stream=None) -> int:
+    return lib().estream_workspace_error(_dptr(workspace), _stream(stream))
+
+
+def cast_f32_bf16(src: torch.Tensor, dst: torch.Tensor, stream=None) -> None:
+    assert src.dtype == torch.float32 and dst.dtype == torch.bfloat16 and src.numel() == dst.numel()
+    _check(lib().estream_cast_f32_bf16(_dptr(src), _dptr(dst), src.numel(), _stream(stream)),
+           "estream_cast_f32_bf16")
+
+
+# ---------------------------------------------------------------------------
+# arena / layer
+# ---------------------------------------------------------------------------
+
+def arena_bytes(E, H, F, G, B, wdtype) -> int:
+    return lib().estream_arena_bytes(E, H, F, G, B, wdtype)
+
+
+def pool_bytes(E, H, F, wdtype) -> int:
+    return lib().estream_pool_bytes(E, H, F, wdtype)
+
+
+def shared_bytes(n_shared, H, F_shared, wdtype) -> int:
+    return lib().estream_shared_bytes(n_shared, H, F_shared, wdtype)
+
+
+def pack_shared(desc: ArenaDesc, sg: torch.Tensor, su: torch.Tensor, sd: torch.Tensor,
+                out: torch.Tensor) -> None:
+    for t in (sg, su, sd, out):
+        assert t.device.type == "cpu" and t.is_contiguous()
+    _check(lib().estream_pack_shared(ctypes.byref(desc), sg.data_ptr(), su.data_ptr(),
+                                     sd.data_ptr(), out.data_ptr()), "estream_pack_shared")
+
+
+def make_desc(L, E, H, F, G, B, wdtype, arena: torch.Tensor, pools, perm=None, n_shared=0,
+              F_shared=0, shared=None, T_max=1, k_max=1, deterministic=False,
+              schedule=SCHED_AFTER_ROUTING, Q=1):
+    """Fill an ArenaDesc; returns (desc, keepalive) -- keep both alive while bound."""
+    d = ArenaDesc()
+    d.L, d.E, d.H, d.F, d.G, d.B, d.Q = L, E, H, F, G, B, Q
+    d.wdtype = wdtype
+    d.arena_dev = arena.data_ptr() if arena is not None else None
+    d.arena_bytes = arena.numel() * arena.element_size() if arena is not None else 0
+    pool_arr = (ctypes.c_void_p * L)(*[p.data_ptr() if p is not None else None for p in pools])
+    d.host_pool = ctypes.cast(pool_arr, ctypes.POINTER(ctypes.c_void_p))
+    keep = [pool_arr]
+    if perm is not None:
+        perm_arr = (ctypes.c_int32 * (L * E))(*[int(v) for v in torch.as_tensor(perm).reshape(-1).tolist()])
+        d.perm = ctypes.cast(perm_arr, ctypes.POINTER(ctypes.c_int32))
+        keep.append(perm_arr)
+    d.n_shared, d.F_shared = n_shared, F_shared
+    if n_shared and shared is not None:
+        sh_arr = (ctypes.c_void_p * L)(*[s.data_ptr() for s in shared])
+        d.shared_dev = ctypes.cast(sh_arr, ctypes.POINTER(ctypes.c_void_p))
+        keep.append(sh_arr)
+    d.T_max, d.k_max = T_max, k_max
+    d.deterministic = int(bool(deterministic))
+    d.schedule = schedule
+    return d, keep
+
+
+def pack_experts(desc: ArenaDesc, layer: int, wg: torch.Tensor, wu: torch.Tensor, wd: torch.Tensor,
+                 pool_out: torch.Tensor) -> None:
+    for t in (wg, wu, wd, pool_out):
+        assert t.device.type == "cpu" and t.is_contiguous()
+    _check(lib().estream_pack_experts(ctypes.byref(desc), layer, wg.data_ptr(), wu.data_ptr(),
+                                      wd.data_ptr(), pool_out.data_ptr()), "estream_pack_experts")
+
+
+def bind_arena(desc: ArenaDesc) -> int:
+    ctx = ctypes.c_void_p()
+    _check(lib().estream_bind_arena(ctypes.byref(ctx), ctypes.byref(desc)), "estream_bind_arena")
+    return ctx.value
+
+
+def arena_preload(ctx, layer: int, stream=None) -> None:
+    _check(lib().estream_arena_preload(ctx, layer, _stream(stream)), "estream_arena_preload")
+
+
+def arena_invalidate(ctx) -> None:
+    _check(lib().estream_arena_invalidate(ctx), "estream_arena_invalidate")
+
+
+def moe_layer_prefill(ctx, layer: int, X: torch.Tensor, logits: torch.Tensor, k: int,
+                      renorm: bool, Y: torch.Tensor, stream=None) -> None:
+    T = X.shape[0]
+    _check(lib().estream_moe_layer_prefill(ctx, layer, _dptr(X), _dptr(logits), T, k,
+                                           int(bool(renorm)), _dptr(Y), _stream(stream)),
+           "estream_moe_layer_prefill")
+
+
+def set_timing(ctx, on: bool) -> None:
+    _check(lib().estream_set_timing(ctx, int(bool(on))), "estream_set_timing")
+
+
+def reset_stats(ctx) -> None:
+    _check(lib().estream_reset_stats(ctx), "estream_reset_stats")
+
+
+def last_stats(ctx) -> dict:
+    s = Stats()
+    _check(lib().estream_last_stats(ctx, ctypes.byref(s)), "estream_last_stats")
+    return {name: getattr(s, name) for name, _ in Stats._fields_}
+
+
+def get_device_error(ctx) -> int:
+    return lib().estream_get_device_error(ctx)
+
+
+def residency_trace(ctx, cap: int = 4096):
+    buf = (ctypes.c_int32 * (4 * cap))()
+    n = ctypes.c_int()
+    _check(lib().estream_residency_trace(ctx, buf, cap, ctypes.byref(n)), "estream_residency_trace")
+    m = min(n.value, cap)
+    return [tuple(buf[4 * i:4 * i + 4]) for i in range(m)]
+
+
+def inject_pager_fault(ctx, layer: int, group: int) -> None:
+    _check(lib().estream_inject_pager_fault(ctx, layer, group), "estream_inject_pager_fault")
+
+
+def unbind(ctx) -> None:
+    if ctx:
+        lib().estream_unbind(ctx)

@@ -1,0 +1,84 @@
+"""Owner of the memory one bound arena needs, for a Workload.
+
+Allocates (through torch) the device arena, the pinned host pools packed by
+``estream_pack_experts``, the packed shared experts on the device, and binds
+the library context. ``prefill`` is the C-ABI layer call. Nothing here
+computes any part of the layer.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import estream as es
+from .workloads import Workload, ceil_div
+
+
+class BoundLayerStack:
+    """One arena bound for every layer of a workload.
+
+    mode="resident": B = ceil(E/G) banks and every layer's groups preloaded
+    (only for single-layer workloads); mode="paged": the workload's (G, B).
+    """
+
+    def __init__(self, wl: Workload, mode: str = "resident", perm=None, G=None, B=None,
+                 deterministic=False, schedule=es.SCHED_AFTER_ROUTING, T_max=None, k_max=None,
+                 device="cuda"):
+        cfg = wl.cfg
+        self.cfg, self.wl, self.mode = cfg, wl, mode
+        self.dtype = es.BF16 if cfg.dtype == "bf16" else es.F32
+        L = len(wl.layers)
+        G = G or cfg.G
+        if mode == "resident":
+            B = B or ceil_div(cfg.E, G)
+        else:
+            B = B or cfg.B
+        self.G, self.B = G, B
+        self.T_max = T_max or cfg.T
+        self.k_max = k_max or cfg.k
+        if perm is None:
+            perm = torch.arange(cfg.E, dtype=torch.int32).repeat(L, 1)
+        self.perm = torch.as_tensor(perm, dtype=torch.int32).reshape(L, cfg.E)
+        self.arena = torch.empty(es.arena_bytes(cfg.E, cfg.H, cfg.F, G, B, self.dtype),
+                                 dtype=torch.uint8, device=device)
+        pin = torch.cuda.is_available()
+        nbytes = es.pool_bytes(cfg.E, cfg.H, cfg.F, self.dtype)
+        self.pools = [torch.empty(nbytes, dtype=torch.uint8, pin_memory=pin) for _ in range(L)]
+        self.shared = []
+        desc, keep = es.make_desc(L, cfg.E, cfg.H, cfg.F, G, B, self.dtype, self.arena, self.pools,
+                                  perm=self.perm, n_shared=cfg.n_shared, F_shared=cfg.F_shared,
+                                  shared=None, T_max=self.T_max, k_max=self.k_max,
+                                  deterministic=deterministic, schedule=schedule)
+        for l, lw in enumerate(wl.layers):
+            es.pack_experts(desc, l, lw.Wg.contiguous(), lw.Wu.contiguous(), lw.Wd.contiguous(),
+                            self.pools[l])
+            if cfg.n_shared:
+                buf = torch.empty(es.shared_bytes(cfg.n_shared, cfg.H, cfg.F_shared, self.dtype),
+                                  dtype=torch.uint8)
+                es.pack_shared(desc, lw.Sg.contiguous(), lw.Su.contiguous(), lw.Sd.contiguous(), buf)
+                self.shared.append(buf.to(device))
+        self.desc, self.keep = es.make_desc(
+            L, cfg.E, cfg.H, cfg.F, G, B, self.dtype, self.arena, self.pools, perm=self.perm,
+            n_shared=cfg.n_shared, F_shared=cfg.F_shared, shared=self.shared or None,
+            T_max=self.T_max, k_max=self.k_max, deterministic=deterministic, schedule=schedule)
+        self.ctx = es.bind_arena(self.desc)
+        if mode == "resident":
+            if L != 1:
+                raise ValueError("resident mode holds one layer")
+            es.arena_preload(self.ctx, 0)
+
+    def prefill(self, layer: int, X: torch.Tensor, logits: torch.Tensor, Y: torch.Tensor,
+                k=None, renorm=None, stream=None) -> None:
+        cfg = self.cfg
+        es.moe_layer_prefill(self.ctx, layer, X, logits, cfg.k if k is None else k,
+                             cfg.renorm if renorm is None else renorm, Y, stream)
+
+    def close(self) -> None:
+        if getattr(self, "ctx", None):
+            es.unbind(self.ctx)
+            self.ctx = None
+
+    def __del__(self):  # pragma: no cover
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,42 @@
+"""Shared helpers of the GPU parity tests: tolerance checks against the
+oracle, and device setup."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from routed_expert_ffn_topk_gb300 import workloads as W
+
+# Tolerance for Y (bf16 weights/activations, fp32 accumulation): normwise
+# max |dY| / max |Y_ref| <= 2e-2 and mean |dY| / mean |Y_ref| <= 1e-3.
+MAX_REL = 2e-2
+MEAN_REL = 1e-3
+
+
+def y_errors(y_gpu, y_ref):
+    y_gpu = np.asarray(y_gpu, dtype=np.float64)
+    y_ref = np.asarray(y_ref, dtype=np.float64)
+    d = np.abs(y_gpu - y_ref)
+    return d.max() / np.abs(y_ref).max(), d.mean() / np.abs(y_ref).mean()
+
+
+def assert_y_close(y_gpu, y_ref, what=""):
+    assert np.all(np.isfinite(y_gpu)), f"{what}: non-finite output"
+    mx, mean = y_errors(y_gpu, y_ref)
+    assert mx <= MAX_REL and mean <= MEAN_REL, f"{what}: max_rel {mx:.3e} mean_rel {mean:.3e}"
+    return mx, mean
+
+
+def oracle_layer(wl: W.Workload, layer: int, X_cpu, rows=None, residual=None):
+    """Oracle routing + Eq. 2 for the listed rows of one layer."""
+    cfg = wl.cfg
+    lw = wl.layers[layer]
+    ids, alpha = oracle.route_topk(wl.logits[layer].numpy(), cfg.k, cfg.renorm)
+    shared = (lw.Sg, lw.Su, lw.Sd) if cfg.n_shared else None
+    return oracle.moe_layer_rows(X_cpu, lw.Wg, lw.Wu, lw.Wd, ids, alpha, rows=rows,
+                                 shared=shared, residual=residual)
+
+
+def device():
+    return torch.device("cuda", 0)

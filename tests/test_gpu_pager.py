@@ -1,0 +1,144 @@
+"""Arena pager and residency protocol (section 3.3 / 3.4 of the EStream
+paper): results independent of arena size and storage order, every bank
+published before use and released before refill, empty groups skipped, host
+fault injection."""
+import numpy as np
+import pytest
+import torch
+
+from routed_expert_ffn_topk_gb300 import workloads as W
+from tests import _gpu
+from tests.test_gpu_layer import run_layer, small_workload
+
+pytestmark = pytest.mark.gpu
+
+
+def _stack(wl, **kw):
+    from routed_expert_ffn_topk_gb300.layer import BoundLayerStack
+    return BoundLayerStack(wl, **kw)
+
+
+def test_deterministic_mode_bit_identical_across_arenas():
+    """With the fixed-order combine, Y does not depend on the arena size,
+    the group size or the storage order pi, resident or paged."""
+    from routed_expert_ffn_topk_gb300 import estream as es
+    wl = small_workload("c2")
+    E = wl.cfg.E
+    ys = []
+    for mode, G, B, seed, sched in [("resident", 4, None, None, es.SCHED_AFTER_ROUTING),
+                                    ("paged", 4, 2, 1, es.SCHED_AFTER_ROUTING),
+                                    ("paged", 2, 3, 2, es.SCHED_PREFETCH),
+                                    ("paged", 16, 1, 3, es.SCHED_AFTER_ROUTING),
+                                    ("paged", 3, 2, 4, es.SCHED_PREFETCH)]:
+        perm = None if seed is None else W.random_permutation(E, seed)
+        st = _stack(wl, mode=mode, G=G, B=B, perm=perm, deterministic=True, schedule=sched)
+        try:
+            ys.append(run_layer(st, wl))
+        finally:
+            st.close()
+    for y in ys[1:]:
+        np.testing.assert_array_equal(y, ys[0])
+    _gpu.assert_y_close(ys[0], _gpu.oracle_layer(wl, 0, wl.X), "deterministic")
+
+
+def _check_trace(trace, layer):
+    """Per bank: Available -> Filling -> Ready -> (InUse -> Available | Available)."""
+    state = {}
+    content = {}
+    for bank, l, g, s in trace:
+        prev = state.get(bank, 0)
+        if s == 1:
+            assert prev == 0, f"bank {bank} filled while {prev}"
+        elif s == 2:
+            assert prev == 1 and content[bank] == (l, g)
+        elif s == 3:
+            assert prev == 2 and content[bank] == (l, g), f"bank {bank} used before Ready"
+        elif s == 0:
+            assert prev in (2, 3)
+        content[bank] = (l, g)
+        state[bank] = s
+    assert all(v == 0 for v in state.values()), "a bank was left in use"
+
+
+@pytest.mark.parametrize("sched", [0, 1])
+def test_residency_protocol_and_bytes(sched):
+    from routed_expert_ffn_topk_gb300 import estream as es
+    wl = small_workload("c2")
+    cfg = wl.cfg
+    # make expert storage group 1 (positions 4..7 under identity pi) unused
+    lg = wl.logits[0].clone()
+    lg[:, 4:8] = -30.0
+    wl.logits[0] = lg
+    st = _stack(wl, mode="paged", G=4, B=2, schedule=sched)
+    try:
+        es.set_timing(st.ctx, True)
+        y = run_layer(st, wl)
+        stats = es.last_stats(st.ctx)
+        trace = es.residency_trace(st.ctx)
+    finally:
+        st.close()
+    _check_trace(trace, 0)
+    W_e = 3 * cfg.H * cfg.F * 2
+    n_groups = cfg.E // 4
+    loaded = stats["groups_loaded"]
+    assert stats["groups_skipped"] == 1 and loaded == n_groups - 1
+    prefetch_extra = 1 if sched == 1 else 0   # group 1 is among the first B=2 prefetched
+    assert stats["h2d_bytes"] == (loaded + prefetch_extra) * 4 * W_e
+    used = {g for (_, _, g, s) in trace if s == 3}
+    assert 1 not in used
+    _gpu.assert_y_close(y, _gpu.oracle_layer(wl, 0, wl.X), "skip")
+
+
+def test_pager_fault_injection_leaves_context_usable():
+    from routed_expert_ffn_topk_gb300 import estream as es
+    wl = small_workload("c2")
+    st = _stack(wl, mode="paged", G=4, B=2)
+    try:
+        es.inject_pager_fault(st.ctx, 0, 2)
+        dev = _gpu.device()
+        Y = torch.zeros(wl.cfg.T, wl.cfg.H, device=dev)
+        with pytest.raises(es.EStreamError) as ei:
+            st.prefill(0, wl.X.to(dev), wl.logits[0].to(dev), Y)
+        assert ei.value.status == es.ERR_PAGER
+        es.inject_pager_fault(st.ctx, 0, -1)
+        y = run_layer(st, wl)
+    finally:
+        st.close()
+    _gpu.assert_y_close(y, _gpu.oracle_layer(wl, 0, wl.X), "after fault")
+
+
+def test_capacity_and_argument_errors():
+    from routed_expert_ffn_topk_gb300 import estream as es
+    wl = small_workload("c2")
+    st = _stack(wl, mode="resident")
+    dev = _gpu.device()
+    try:
+        X = torch.zeros(wl.cfg.T + 1, wl.cfg.H, dtype=torch.bfloat16, device=dev)
+        lg = torch.zeros(wl.cfg.T + 1, wl.cfg.E, device=dev)
+        Y = torch.zeros(wl.cfg.T + 1, wl.cfg.H, device=dev)
+        with pytest.raises(es.EStreamError) as ei:
+            st.prefill(0, X, lg, Y)
+        assert ei.value.status == es.ERR_CAPACITY
+        with pytest.raises(es.EStreamError) as ei:
+            st.prefill(0, X[:4], lg[:4], Y[:4], k=wl.cfg.k + 1)
+        assert ei.value.status == es.ERR_CAPACITY
+        with pytest.raises(es.EStreamError) as ei:
+            st.prefill(3, X[:4], lg[:4], Y[:4])
+        assert ei.value.status == es.ERR_INVALID_ARG
+    finally:
+        st.close()
+
+
+def test_ragged_token_counts_reuse_one_context():
+    """T below T_max, including T=1 and T not a multiple of the tile."""
+    wl = small_workload("c2")
+    st = _stack(wl, mode="paged", G=4, B=2)
+    try:
+        for T in (1, 7, 129, wl.cfg.T):
+            X = wl.X[:T].contiguous()
+            sub = W.Workload(wl.cfg, [wl.logits[0][:T].contiguous()], X, wl.layers)
+            y = run_layer(st, sub, X=X)
+            ref = _gpu.oracle_layer(sub, 0, X)
+            _gpu.assert_y_close(y, ref, f"T={T}")
+    finally:
+        st.close()
