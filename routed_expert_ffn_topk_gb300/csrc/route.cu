@@ -284,7 +284,6 @@ cudaError_t launch_route_build(const float* logits, int T, int E, int k, int ren
         rc = cudaMemsetAsync(err, 0, sizeof(int), stream);
         if (rc == cudaSuccess) rc = cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (P + 2), stream);
         if (rc == cudaSuccess) rc = cudaMemsetAsync(mblk, 0, sizeof(int32_t) * (P + 2), stream);
-        if (n_launches) *n_launches += 3;
         return rc;
     }
     // one memset clears the error word and the per-chunk counts (contiguous)
@@ -292,7 +291,6 @@ cudaError_t launch_route_build(const float* logits, int T, int E, int k, int ren
                          w.hist_off - w.err_off + sizeof(int32_t) * static_cast<size_t>(w.nchunk) * nb,
                          stream);
     if (rc != cudaSuccess) return rc;
-    ++launches;
     k_route_topk<<<(T + 127) / 128, 128, 0, stream>>>(logits, T, E, k, renorm, phi, P, topk_ids,
                                                      alpha, hist, err);
     ++launches;
