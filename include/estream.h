@@ -106,6 +106,32 @@ estream_status estream_route_build(const float* logits, int T, int E, int k, int
  * recorded in `workspace` (ESTREAM_OK if none), then clears it. */
 estream_status estream_workspace_error(void* workspace, void* cuda_stream);
 
+/*
+ * estream_route_build without a workspace argument, for callers that cannot
+ * give this library device scratch memory (for example a serving process
+ * that reserved all device memory up front and allows no cudaMalloc on its
+ * request path, since an allocation there can synchronise the device or fail
+ * once the budget is carved up). The paper has no counterpart of this call.
+ * Inputs, outputs and results are those of estream_route_build; it allocates
+ * nothing. Its scratch is a 1 MiB file-scope device array held by every GPU
+ * that loads the library until the process exits:
+ *   - sizes whose estream_route_workspace_bytes(T, E, k, P) exceeds 1 MiB are
+ *     rejected with ESTREAM_ERR_CAPACITY before anything is enqueued;
+ *   - all calls on a device share the array, which keeps the previous call's
+ *     contents; each call clears what must start at zero on its own stream;
+ *     calls whose GPU work overlaps (other streams, unordered threads) race
+ *     on it and give wrong results;
+ *   - the first call on a device looks the array's address up (with that
+ *     device current); make it before any stream capture on the device;
+ *   - a phi entry outside [-1, P) is filed under the trailing bucket as
+ *     estream_route_build does, but is not reported.
+ */
+estream_status estream_route_build_noalloc(const float* logits, int T, int E, int k, int renorm,
+                                           const int32_t* phi, int P,
+                                           int32_t* topk_ids, float* alpha, int32_t* offsets,
+                                           int32_t* rec_tok, int32_t* rec_route,
+                                           void* cuda_stream);
+
 /* ---------------------------------------------------------------------- */
 /* Expert arena, pager and layer prefill                                   */
 /* ---------------------------------------------------------------------- */

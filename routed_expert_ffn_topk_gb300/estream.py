@@ -68,6 +68,7 @@ SIGNATURES = {
     "estream_route_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
     "estream_route_build": (_I, [_P, _I, _I, _I, _I, _P, _I, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "estream_workspace_error": (_I, [_P, _P]),
+    "estream_route_build_noalloc": (_I, [_P, _I, _I, _I, _I, _P, _I, _P, _P, _P, _P, _P, _P]),
     "estream_arena_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "estream_pool_bytes": (_SZ, [_I, _I, _I, _I]),
     "estream_shared_bytes": (_SZ, [_I, _I, _I, _I]),
@@ -164,6 +165,28 @@ def route_build(logits: torch.Tensor, k: int, renorm: bool, phi: torch.Tensor | 
         _dptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
     _check(st, "estream_route_build")
     o["workspace"] = workspace
+    return o
+
+
+def route_build_noalloc(logits: torch.Tensor, k: int, renorm: bool, phi: torch.Tensor | None = None,
+                        P: int | None = None, out: dict | None = None, stream=None) -> dict:
+    """estream_route_build_noalloc: the same outputs as route_build, with the
+    library's static device scratch instead of a caller workspace."""
+    T, E = logits.shape
+    P = E if P is None else P
+    dev = logits.device
+    R = T * k
+    o = dict(out or {})
+    o.setdefault("topk_ids", torch.empty(max(R, 1), dtype=torch.int32, device=dev))
+    o.setdefault("alpha", torch.empty(max(R, 1), dtype=torch.float32, device=dev))
+    o.setdefault("offsets", torch.empty(P + 2, dtype=torch.int32, device=dev))
+    o.setdefault("rec_tok", torch.empty(max(R, 1), dtype=torch.int32, device=dev))
+    o.setdefault("rec_route", torch.empty(max(R, 1), dtype=torch.int32, device=dev))
+    st = lib().estream_route_build_noalloc(
+        _dptr(logits), T, E, k, int(bool(renorm)), _dptr(phi), P, _dptr(o["topk_ids"]),
+        _dptr(o["alpha"]), _dptr(o["offsets"]), _dptr(o["rec_tok"]), _dptr(o["rec_route"]),
+        _stream(stream))
+    _check(st, "estream_route_build_noalloc")
     return o
 
 
