@@ -68,16 +68,16 @@ struct GemmSegments {
 };
 
 // K2 (bf16 tensor cores): h[p, :] = fp16(SiLU(X[tok(p)] Wg_slot^T) * (X[tok(p)] Wu_slot^T)).
-cudaError_t launch_gateup(const CUtensorMap* tm_x, const CUtensorMap* tm_wg,
-                          const CUtensorMap* tm_wu, const GemmSegments& seg, void* h,
-                          int H, int F, int slot_rows_gu, int* dev_err, int num_sms,
-                          cudaStream_t stream);
+// X: device [T][H] bf16, 16-byte aligned rows.
+cudaError_t launch_gateup(const void* X, const CUtensorMap* tm_wg, const CUtensorMap* tm_wu,
+                          const GemmSegments& seg, void* h, int H, int F, int* dev_err,
+                          int num_sms, cudaStream_t stream);
 
 // K3 (fp16 tensor cores): Y[tok(p), :] += alpha(p) * scale(seg) * (h[p] Wd_slot^T), or
 // out_rows[p, :] = ... when out_rows != null (deterministic mode).
 cudaError_t launch_down(const CUtensorMap* tm_h, const CUtensorMap* tm_wd,
                         const GemmSegments& seg, float* Y, float* out_rows, int H, int F,
-                        int slot_rows_d, int* dev_err, int num_sms, cudaStream_t stream);
+                        int* dev_err, int num_sms, cudaStream_t stream);
 
 // fp32 path (CUDA-core FMA): the same two steps for fp32 X and weights.
 // Weight planes are [slots][F][H] (gate, up) and [slots][H][F] (down).

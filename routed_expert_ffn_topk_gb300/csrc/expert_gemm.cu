@@ -12,10 +12,16 @@
 // GB300 form. One persistent kernel per GEMM walks a list of 128-row tiles
 // built from the route map (segment = slot, m-block, n-block), with three
 // warp roles per CTA:
-//   warp 0     TMA producer into a 4-stage shared-memory ring. For K2 the A
-//              tile is a row gather of X by record token (tile::gather4, four
-//              rows per instruction, 128-byte swizzle); for K3 it is a plain
-//              tile of h (records are contiguous by slot).
+//   warp 0     TMA producer into a 4-stage shared-memory ring: the weight
+//              tile of every stage, and for K3 also the A tile of h (records
+//              are contiguous by slot, so a plain 2D box).
+//   warps 6-9  (K2 only) the row gather: each record's 128-byte slice of
+//              X[tok] is copied into its row of the stage's A tile with 16-byte
+//              cp.async, writing the 128-byte-swizzled layout the MMA reads
+//              (chunk c of row r at c ^ (r mod 8)). TMA tile::gather4 moves
+//              only four 128-byte rows per instruction, which measured ~2.3x
+//              slower for this kernel than plain tiles; the LSU path keeps
+//              the gather fused at tile speed.
 //   warp 1     allocates 512 TMEM columns (two 128x256 fp32 accumulators) and
 //              one elected lane issues tcgen05.mma (M=128, N=256, K=16 per
 //              instruction, kind::f16), committing stages back to the producer
@@ -49,7 +55,10 @@ constexpr int kTileBBytes = 256 * kRowBytes;      // 32 KB
 constexpr int kStageBytes = kTileABytes + kTileBBytes;
 constexpr int kAccCols = 256;
 constexpr int kTmemCols = 512;
-constexpr int kThreads = 192;
+constexpr int kThreadsDown = 192;       // TMA, MMA, 4 epilogue warps
+constexpr int kThreadsGateUp = 320;     // + 4 row-gather warps
+constexpr int kGatherWarp0 = 6;
+constexpr int kGatherDepth = 2;         // cp.async groups kept in flight per gather thread
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr uint64_t kDrainLimitNs = 100000000ull;  // 0.1 s
 constexpr float kHalfMax = 65504.0f;
@@ -133,16 +142,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm,
         "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar)
         : "memory");
 }
-// Four arbitrary rows (r0..r3) of a 2D tensor, columns [x, x + box width).
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* tm, int x, int r0,
-                                            int r1, int r2, int r3, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
-        : "memory");
-}
-
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
                  "r"(ncols)
@@ -264,11 +263,28 @@ __device__ __forceinline__ Tile decode_tile(int t, const int* table, int seg_cou
     return ti;
 }
 
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+// Make this thread's completed generic-proxy shared-memory writes visible to
+// the async proxy (the tensor cores read operands through it).
+__device__ __forceinline__ void fence_proxy_async() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 template <bool kGateUp>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kGateUp ? kThreadsGateUp : kThreadsDown, 1)
     k_expert_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b0,
-                  const __grid_constant__ CUtensorMap tm_b1, const GemmSegments seg, void* h_out,
-                  float* Y, float* out_rows, int H, int F, int slot_rows, int* dev_err) {
+                  const __grid_constant__ CUtensorMap tm_b1, const GemmSegments seg,
+                  const __nv_bfloat16* __restrict__ x_src, void* h_out, float* Y, float* out_rows,
+                  int H, int F, int* dev_err) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
@@ -294,7 +310,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         table[s] = seg.mblk[seg.seg_begin + s] - m0;
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(full_bar(s), 1);
+            // K2: the TMA producer's expect_tx arrival + one per gather thread
+            mbar_init(full_bar(s), kGateUp ? 1 + kBM : 1);
             mbar_init(empty_bar(s), 1);
         }
         for (int a = 0; a < 2; ++a) {
@@ -331,15 +348,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
             const Tile ti = decode_tile(t, table, seg.seg_count, NB, seg.offsets, seg.seg_begin);
             const int slot = seg.slot_base + ti.seg;
-            const int brow = slot * slot_rows + ti.nb * (kGateUp ? 128 : 256);
-            int tok[4] = {0, 0, 0, 0};
-            if (kGateUp) {
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int r = min(lane * 4 + q, ti.rows - 1);
-                    tok[q] = seg.rec_tok[ti.row0 + r];
-                }
-            }
+            // weight planes are tile-major: the (n-block, k-block) tile of a
+            // slot is one contiguous box of 128 (K2) or 256 (K3) rows of 64
+            const int tile_rows = kGateUp ? 128 : 256;
+            const int brow0 = ((slot * NB + ti.nb) * num_kb) * tile_rows;
             for (int kb = 0; kb < num_kb; ++kb) {
                 bool w = true;
                 if (lane == 0) w = mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, dev_err);
@@ -349,23 +361,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(full_bar(stage), kStageBytes);
+                    mbar_arrive_expect_tx(full_bar(stage), kGateUp ? kTileBBytes : kStageBytes);
                     issued[stage] = static_cast<int>(phase);
                 }
                 __syncwarp();
                 const uint32_t a_dst = sA + stage * kTileABytes;
                 const uint32_t b_dst = sB + stage * kTileBBytes;
                 const int x = kb * BKe;
+                const int brow = brow0 + kb * tile_rows;
                 if (kGateUp) {
-                    tma_gather4(a_dst + lane * 4 * kRowBytes, &tm_a, x, tok[0], tok[1], tok[2],
-                                tok[3], full_bar(stage));
                     if (lane == 0) {
-                        tma_load_2d(b_dst, &tm_b0, x, brow, full_bar(stage));
-                        tma_load_2d(b_dst + 128 * kRowBytes, &tm_b1, x, brow, full_bar(stage));
+                        tma_load_2d(b_dst, &tm_b0, 0, brow, full_bar(stage));
+                        tma_load_2d(b_dst + 128 * kRowBytes, &tm_b1, 0, brow, full_bar(stage));
                     }
                 } else if (lane == 0) {
                     tma_load_2d(a_dst, &tm_a, x, ti.row0, full_bar(stage));
-                    tma_load_2d(b_dst, &tm_b0, x, brow, full_bar(stage));
+                    tma_load_2d(b_dst, &tm_b0, 0, brow, full_bar(stage));
                 }
                 if (++stage == kStages) {
                     stage = 0;
@@ -380,6 +391,67 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_wait(full_bar(s), static_cast<uint32_t>(issued[s]), abort_flag, nullptr,
                               kDrainLimitNs);
         }
+    } else if (kGateUp && warp >= kGatherWarp0) {
+        // ------------------------------ row gather (K2) ------------------------------
+        // Gather warp w covers rows [32w, 32w+32) of every A stage; in copy
+        // instruction i lane l moves 16-byte chunk (l mod 8) of row
+        // 32w + 4i + l/8, so each warp-instruction reads four whole 128-byte
+        // rows. Every thread arrives on a stage once its own copies are
+        // complete (wait_group) and fenced to the async proxy; kGatherDepth
+        // stages stay in flight per thread.
+        const int gw = warp - kGatherWarp0;
+        const uint32_t chunk = static_cast<uint32_t>(lane & 7);
+        int stage = 0;
+        uint32_t phase = 0;
+        int pend[kGatherDepth + 1];
+        int npend = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+            const Tile ti = decode_tile(t, table, seg.seg_count, NB, seg.offsets, seg.seg_begin);
+            const __nv_bfloat16* src_row[8];
+            uint32_t dst_off[8];
+            unsigned live = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int r = gw * 32 + 4 * i + (lane >> 3);
+                dst_off[i] = static_cast<uint32_t>(r) * kRowBytes + ((chunk ^ static_cast<uint32_t>(r & 7)) << 4);
+                const bool lv = r < ti.rows;
+                live |= lv ? (1u << i) : 0u;
+                src_row[i] = lv ? x_src + static_cast<size_t>(seg.rec_tok[ti.row0 + r]) * H + chunk * 8
+                                : x_src;
+            }
+            for (int kb = 0; kb < num_kb; ++kb) {
+                bool w = true;
+                if (lane == 0) w = mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, dev_err);
+                w = __shfl_sync(0xffffffffu, w, 0);
+                if (!w) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t base = sA + stage * kTileABytes;
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    if (live & (1u << i)) cp_async_16(base + dst_off[i], src_row[i] + kb * 64);
+                cp_async_commit();
+                pend[npend++] = stage;
+                if (npend > kGatherDepth) {
+                    cp_async_wait<kGatherDepth>();
+                    fence_proxy_async();
+                    mbar_arrive(full_bar(pend[0]));
+#pragma unroll
+                    for (int q = 0; q < kGatherDepth; ++q) pend[q] = pend[q + 1];
+                    --npend;
+                }
+                if (++stage == kStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        // the stages still pending: complete, fence, publish
+        cp_async_wait<0>();
+        fence_proxy_async();
+        for (int q = 0; q < npend; ++q) mbar_arrive(full_bar(pend[q]));
     } else if (warp == 1) {
         // ------------------------------ MMA issuer ------------------------------
         if (lane == 0) {
@@ -429,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         __syncwarp();
-    } else {
+    } else if (warp >= 2 && warp < 6) {
         // ------------------------------ epilogue ------------------------------
         const int quarter = warp & 3;  // TMEM lanes this warp may read
         const int row = quarter * 32 + lane;
@@ -526,8 +598,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <bool kGateUp>
 cudaError_t launch_gemm(const CUtensorMap* tm_a, const CUtensorMap* tm_b0, const CUtensorMap* tm_b1,
-                        const GemmSegments& seg, void* h_out, float* Y, float* out_rows, int H,
-                        int F, int slot_rows, int* dev_err, int num_sms, cudaStream_t stream) {
+                        const GemmSegments& seg, const void* x_src, void* h_out, float* Y,
+                        float* out_rows, int H, int F, int* dev_err, int num_sms,
+                        cudaStream_t stream) {
     const int NB = kGateUp ? F / 128 : H / 256;
     const long long max_tiles = static_cast<long long>(seg.max_tiles_m) * NB;
     if (max_tiles <= 0 || seg.seg_count <= 0) return cudaSuccess;
@@ -537,8 +610,9 @@ cudaError_t launch_gemm(const CUtensorMap* tm_a, const CUtensorMap* tm_b0, const
     cudaError_t rc = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           static_cast<int>(smem));
     if (rc != cudaSuccess) return rc;
-    kern<<<grid, kThreads, smem, stream>>>(*tm_a, *tm_b0, *tm_b1, seg, h_out, Y, out_rows, H, F,
-                                           slot_rows, dev_err);
+    kern<<<grid, kGateUp ? kThreadsGateUp : kThreadsDown, smem, stream>>>(
+        *tm_a, *tm_b0, *tm_b1, seg, static_cast<const __nv_bfloat16*>(x_src), h_out, Y, out_rows, H,
+        F, dev_err);
     return cudaGetLastError();
 }
 
@@ -567,17 +641,17 @@ __global__ void k_combine(const float* __restrict__ rows, const int32_t* __restr
 
 }  // namespace
 
-cudaError_t launch_gateup(const CUtensorMap* tm_x, const CUtensorMap* tm_wg,
-                          const CUtensorMap* tm_wu, const GemmSegments& seg, void* h, int H, int F,
-                          int slot_rows_gu, int* dev_err, int num_sms, cudaStream_t stream) {
-    return launch_gemm<true>(tm_x, tm_wg, tm_wu, seg, h, nullptr, nullptr, H, F, slot_rows_gu,
-                             dev_err, num_sms, stream);
+cudaError_t launch_gateup(const void* X, const CUtensorMap* tm_wg, const CUtensorMap* tm_wu,
+                          const GemmSegments& seg, void* h, int H, int F, int* dev_err, int num_sms,
+                          cudaStream_t stream) {
+    return launch_gemm<true>(tm_wg, tm_wg, tm_wu, seg, X, h, nullptr, nullptr, H, F, dev_err,
+                             num_sms, stream);
 }
 
 cudaError_t launch_down(const CUtensorMap* tm_h, const CUtensorMap* tm_wd, const GemmSegments& seg,
-                        float* Y, float* out_rows, int H, int F, int slot_rows_d, int* dev_err,
-                        int num_sms, cudaStream_t stream) {
-    return launch_gemm<false>(tm_h, tm_wd, tm_wd, seg, nullptr, Y, out_rows, H, F, slot_rows_d,
+                        float* Y, float* out_rows, int H, int F, int* dev_err, int num_sms,
+                        cudaStream_t stream) {
+    return launch_gemm<false>(tm_h, tm_wd, tm_wd, seg, nullptr, nullptr, Y, out_rows, H, F,
                               dev_err, num_sms, stream);
 }
 

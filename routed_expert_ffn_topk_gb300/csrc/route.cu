@@ -10,7 +10,7 @@
 // (Phi = -1) are filed under a trailing bucket P.
 //
 // GPU form (three launches after one memset):
-//   k_route_topk    one thread per token: softmax top-k, alpha, and per-chunk
+//   k_route_topk    one warp per token: softmax top-k, alpha, and per-chunk
 //                   slot counts (global atomics; counts are order-free).
 //   k_route_scan    one CTA: per-slot chunk bases and slot offsets (exclusive
 //                   prefix sums), plus the m-block prefix the GEMMs schedule by.
@@ -57,63 +57,104 @@ __device__ __forceinline__ void record_error(int* err, int code) {
     if (err) atomicCAS(err, kDevErrNone, code);
 }
 
-// One thread per token. Selection walks the strict total order
-// (logit descending, expert id ascending): pass j takes the best expert that
-// comes after pass j-1's pick in that order, so no "taken" mask is needed.
-__global__ void __launch_bounds__(128) k_route_topk(
+// One warp per token; lane l holds the logits of experts l, l+32, l+64, ...
+// The softmax denominator is summed in ascending expert order (the same
+// sequence of fp32 additions as the written definition): the warp streams the
+// per-expert exponentials to every lane with shuffles, one expert at a time.
+// Selection walks the strict total order (logit descending, expert id
+// ascending): round j takes the best expert after round j-1's pick in that
+// order, found by a warp-wide (value, id) reduction.
+constexpr int kTopkWarps = 8;
+constexpr int kMaxPerLane = kMaxE / 32;
+
+__device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib) {
+    return va > vb || (va == vb && ia < ib);
+}
+
+__global__ void __launch_bounds__(32 * kTopkWarps) k_route_topk(
     const float* __restrict__ logits, int T, int E, int k, int renorm,
     const int32_t* __restrict__ phi, int P, int32_t* __restrict__ topk_ids,
     float* __restrict__ alpha, int32_t* __restrict__ hist, int* __restrict__ err) {
-    const int t = blockIdx.x * blockDim.x + threadIdx.x;
-    if (t >= T) return;
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * kTopkWarps + (threadIdx.x >> 5);
+    if (t >= T) return;  // whole warps exit together
     const float* l = logits + static_cast<size_t>(t) * E;
-
-    float m = l[0];
-    for (int e = 1; e < E; ++e) {
-        const float v = l[e];
-        if (v > m) m = v;
+    const int nj = (E + 31) >> 5;
+    const float kNegInf = __int_as_float(0xff800000);
+    float v[kMaxPerLane];
+#pragma unroll
+    for (int j = 0; j < kMaxPerLane; ++j) {
+        const int e = lane + 32 * j;
+        v[j] = (j < nj && e < E) ? l[e] : kNegInf;
     }
-    float s = 0.0f;
-    for (int e = 0; e < E; ++e) s = __fadd_rn(s, route_exp(__fsub_rn(l[e], m)));
+    float m = kNegInf;
+#pragma unroll
+    for (int j = 0; j < kMaxPerLane; ++j) m = fmaxf(m, v[j]);
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, d));
 
-    float a[kMaxK];
-    int ids[kMaxK];
-    float prev_l = __int_as_float(0x7f800000);  // +inf: everything comes after it
-    int prev_id = -1;
-    for (int j = 0; j < k; ++j) {
-        int best = -1;
-        float bl = 0.0f;
-        for (int e = 0; e < E; ++e) {
-            const float v = l[e];
-            const bool after_prev = (v < prev_l) || (v == prev_l && e > prev_id);
-            if (!after_prev) continue;
-            if (best < 0 || v > bl) {
-                best = e;
-                bl = v;
+    // denominator: sequential fp32 sum over e = 0, 1, ..., E-1
+    float s = 0.0f;
+#pragma unroll
+    for (int j = 0; j < kMaxPerLane; ++j) {
+        if (j >= nj) break;
+        const int e = lane + 32 * j;
+        const float p = (e < E) ? route_exp(__fsub_rn(v[j], m)) : 0.0f;
+        const int n_here = min(32, E - 32 * j);
+        for (int src = 0; src < n_here; ++src)
+            s = __fadd_rn(s, __shfl_sync(0xffffffffu, p, src));
+    }
+
+    float prev_v = __int_as_float(0x7f800000);  // +inf: every expert comes after it
+    int prev_i = -1;
+    float a_mine = 0.0f;   // lane j keeps route j's weight
+    int id_mine = -1;
+    for (int r = 0; r < k; ++r) {
+        float bv = kNegInf;
+        int bi = 0x7fffffff;
+#pragma unroll
+        for (int j = 0; j < kMaxPerLane; ++j) {
+            if (j >= nj) break;
+            const int e = lane + 32 * j;
+            if (e >= E) break;
+            const bool after_prev = (v[j] < prev_v) || (v[j] == prev_v && e > prev_i);
+            if (after_prev && ranks_before(v[j], e, bv, bi)) {
+                bv = v[j];
+                bi = e;
             }
         }
-        prev_l = bl;
-        prev_id = best;
-        ids[j] = best;
-        a[j] = __fdiv_rn(route_exp(__fsub_rn(bl, m)), s);
+#pragma unroll
+        for (int d = 16; d > 0; d >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, d);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, d);
+            if (ranks_before(ov, oi, bv, bi)) {
+                bv = ov;
+                bi = oi;
+            }
+        }
+        prev_v = bv;
+        prev_i = bi;
+        if (lane == r) {
+            id_mine = bi;
+            a_mine = __fdiv_rn(route_exp(__fsub_rn(bv, m)), s);
+        }
     }
     if (renorm) {
-        float z = 0.0f;
-        for (int j = 0; j < k; ++j) z = __fadd_rn(z, a[j]);
-        for (int j = 0; j < k; ++j) a[j] = __fdiv_rn(a[j], z);
+        float z = 0.0f;  // summed in rank order
+        for (int r = 0; r < k; ++r) z = __fadd_rn(z, __shfl_sync(0xffffffffu, a_mine, r));
+        a_mine = __fdiv_rn(a_mine, z);
     }
-    const int nb = P + 1;
-    for (int j = 0; j < k; ++j) {
-        const int i = t * k + j;
-        topk_ids[i] = ids[j];
-        alpha[i] = a[j];
-        int slot = phi ? phi[ids[j]] : ids[j];
+    if (lane < k) {
+        const int i = t * k + lane;
+        topk_ids[i] = id_mine;
+        alpha[i] = a_mine;
+        int slot = phi ? phi[id_mine] : id_mine;
         if (slot < -1 || slot >= P) {
             record_error(err, kDevErrSlotRange);
             slot = -1;
         }
         const int b = slot < 0 ? P : slot;
-        atomicAdd(&hist[(i / kRouteChunk) * nb + b], 1);
+        atomicAdd(&hist[(i / kRouteChunk) * (P + 1) + b], 1);
     }
 }
 
@@ -291,8 +332,8 @@ cudaError_t launch_route_build(const float* logits, int T, int E, int k, int ren
                          w.hist_off - w.err_off + sizeof(int32_t) * static_cast<size_t>(w.nchunk) * nb,
                          stream);
     if (rc != cudaSuccess) return rc;
-    k_route_topk<<<(T + 127) / 128, 128, 0, stream>>>(logits, T, E, k, renorm, phi, P, topk_ids,
-                                                     alpha, hist, err);
+    k_route_topk<<<(T + kTopkWarps - 1) / kTopkWarps, 32 * kTopkWarps, 0, stream>>>(
+        logits, T, E, k, renorm, phi, P, topk_ids, alpha, hist, err);
     ++launches;
     const size_t scan_smem = sizeof(int) * (2 * static_cast<size_t>(nb) + 33);
     k_route_scan<<<1, 1024, scan_smem, stream>>>(hist, w.nchunk, P, R, offsets, mblk);

@@ -157,10 +157,40 @@ float bf16_bits_to_float(uint16_t b) {
     return f;
 }
 
-// Offline conversion of one expert's down plane (n elements). bf16: store
-// fp16(w * 2^s) with the largest |w| scaled into [2^14, 2^15) and return
-// 2^-s; fp32: copy and return 1.
-float convert_down(const void* src, size_t n, estream_dtype t, void* dst) {
+// Offline repack of one expert's plane for the tensor-core path (section
+// 3.3, "Offline NPU-Consumable Weight Layout", restated for TMA): the
+// [rows][cols] row-major matrix (rows = output features, cols = the
+// reduction) is stored tile-major as [rows/tile_rows][cols/64][tile_rows][64],
+// so the TMA box of one (n-block, k-block) is a single contiguous run of
+// tile_rows * 128 bytes instead of tile_rows strided 128-byte pieces.
+template <typename Out, typename Conv>
+void pack_tiles(const uint16_t* src, int rows, int cols, int tile_rows, Out* dst, Conv conv) {
+    const int nkb = cols / 64;
+    size_t o = 0;
+    for (int nb = 0; nb < rows / tile_rows; ++nb)
+        for (int kb = 0; kb < nkb; ++kb)
+            for (int r = 0; r < tile_rows; ++r) {
+                const uint16_t* row = src + static_cast<size_t>(nb * tile_rows + r) * cols + kb * 64;
+                for (int c = 0; c < 64; ++c) dst[o++] = conv(row[c]);
+            }
+}
+
+// Gate or up plane of one expert: bf16 copied into 128-row tiles; fp32 copied
+// unchanged (the fp32 path reads row-major planes).
+void pack_gate_up(const void* src, int F, int H, estream_dtype t, void* dst) {
+    if (t == ESTREAM_F32) {
+        std::memcpy(dst, src, sizeof(float) * static_cast<size_t>(F) * H);
+        return;
+    }
+    pack_tiles(static_cast<const uint16_t*>(src), F, H, 128, static_cast<uint16_t*>(dst),
+               [](uint16_t v) { return v; });
+}
+
+// Down plane of one expert ([H][F]). bf16: stored as fp16(w * 2^s) in
+// 256-row tiles with the largest |w| scaled into [2^14, 2^15); returns 2^-s.
+// fp32: copied unchanged, returns 1.
+float pack_down(const void* src, int H, int F, estream_dtype t, void* dst) {
+    const size_t n = static_cast<size_t>(H) * F;
     if (t == ESTREAM_F32) {
         std::memcpy(dst, src, n * sizeof(float));
         return 1.0f;
@@ -175,8 +205,8 @@ float convert_down(const void* src, size_t n, estream_dtype t, void* dst) {
         s = 15 - ex;
     }
     const float up = std::ldexp(1.0f, s);
-    __half* out = static_cast<__half*>(dst);
-    for (size_t x = 0; x < n; ++x) out[x] = __float2half_rn(bf16_bits_to_float(w[x]) * up);
+    pack_tiles(w, H, F, 256, static_cast<__half*>(dst),
+               [up](uint16_t v) { return __float2half_rn(bf16_bits_to_float(v) * up); });
     return std::ldexp(1.0f, -s);
 }
 
@@ -288,17 +318,17 @@ estream_status estream_pack_experts(const estream_arena_desc* d, int layer, cons
     }
     char* out = static_cast<char*>(host_pool_out);
     float* scales = reinterpret_cast<float*>(out + static_cast<size_t>(d->E) * W);
-    const size_t n_elem = static_cast<size_t>(d->H) * d->F;
     for (int e = 0; e < d->E; ++e) {
         const int pos = perm ? perm[e] : e;
         const int q = pos / d->G, r = pos % d->G;
         const int n_q = std::min(d->G, d->E - q * d->G);
         char* grp = out + static_cast<size_t>(q) * d->G * W;
-        std::memcpy(grp + static_cast<size_t>(r) * S, static_cast<const char*>(wg) + e * S, S);
-        std::memcpy(grp + static_cast<size_t>(n_q) * S + static_cast<size_t>(r) * S,
-                    static_cast<const char*>(wu) + e * S, S);
+        pack_gate_up(static_cast<const char*>(wg) + e * S, d->F, d->H, d->wdtype,
+                     grp + static_cast<size_t>(r) * S);
+        pack_gate_up(static_cast<const char*>(wu) + e * S, d->F, d->H, d->wdtype,
+                     grp + static_cast<size_t>(n_q) * S + static_cast<size_t>(r) * S);
         void* down = grp + 2 * static_cast<size_t>(n_q) * S + static_cast<size_t>(r) * S;
-        scales[pos] = convert_down(static_cast<const char*>(wd) + e * S, n_elem, d->wdtype, down);
+        scales[pos] = pack_down(static_cast<const char*>(wd) + e * S, d->H, d->F, d->wdtype, down);
     }
     return ESTREAM_OK;
 }
@@ -308,16 +338,19 @@ estream_status estream_pack_shared(const estream_arena_desc* d, const void* sg, 
     if (!d || !sg || !su || !sd || !out || d->n_shared < 1 || d->F_shared < 1 || d->H < 1)
         return ESTREAM_ERR_INVALID_ARG;
     if (d->wdtype != ESTREAM_F32 && d->wdtype != ESTREAM_BF16) return ESTREAM_ERR_UNSUPPORTED;
+    if (d->H % 256 != 0 || d->F_shared % 128 != 0) return ESTREAM_ERR_INVALID_ARG;
     const size_t n_elem = static_cast<size_t>(d->H) * d->F_shared;
     const size_t S = n_elem * elem_size(d->wdtype);
     const size_t ns = static_cast<size_t>(d->n_shared);
     char* o = static_cast<char*>(out);
-    std::memcpy(o, sg, ns * S);
-    std::memcpy(o + ns * S, su, ns * S);
     float* scales = reinterpret_cast<float*>(o + 3 * ns * S);
-    for (size_t s = 0; s < ns; ++s)
-        scales[s] = convert_down(static_cast<const char*>(sd) + s * S, n_elem, d->wdtype,
-                                 o + 2 * ns * S + s * S);
+    for (size_t s = 0; s < ns; ++s) {
+        pack_gate_up(static_cast<const char*>(sg) + s * S, d->F_shared, d->H, d->wdtype, o + s * S);
+        pack_gate_up(static_cast<const char*>(su) + s * S, d->F_shared, d->H, d->wdtype,
+                     o + ns * S + s * S);
+        scales[s] = pack_down(static_cast<const char*>(sd) + s * S, d->H, d->F_shared, d->wdtype,
+                              o + 2 * ns * S + s * S);
+    }
     return ESTREAM_OK;
 }
 
@@ -339,6 +372,10 @@ estream_status estream_bind_arena(estream_ctx** out, const estream_arena_desc* d
     if (d->arena_bytes < estream_arena_bytes(d->E, d->H, d->F, d->G, d->B, d->wdtype))
         return ESTREAM_ERR_CAPACITY;
     if (static_cast<long long>(d->T_max) * d->k_max > (1ll << 30)) return ESTREAM_ERR_CAPACITY;
+    // tile row indices of the weight planes are 32-bit
+    if (static_cast<long long>(d->B) * d->G * d->F * d->H / 64 >= (1ll << 31) ||
+        static_cast<long long>(d->n_shared) * d->F_shared * d->H / 64 >= (1ll << 31))
+        return ESTREAM_ERR_CAPACITY;
     for (int l = 0; l < d->L; ++l) {
         if (!d->host_pool[l]) return ESTREAM_ERR_INVALID_ARG;
         if (d->n_shared > 0 && (!d->shared_dev[l] || !aligned(d->shared_dev[l], 16)))
@@ -477,15 +514,14 @@ estream_status estream_bind_arena(estream_ctx** out, const estream_arena_desc* d
                     static_cast<const char*>(c->shared_dev[l]) + 3 * sp);
         }
         if (!f32) {
-            tm_ok = tm_ok && encode_tmap_2d(&c->tm_wg, BF, c->plane_g, d->H,
-                                            static_cast<uint64_t>(c->P) * d->F,
-                                            static_cast<uint64_t>(d->H) * 2, 64, 128) == CUDA_SUCCESS;
-            tm_ok = tm_ok && encode_tmap_2d(&c->tm_wu, BF, c->plane_u, d->H,
-                                            static_cast<uint64_t>(c->P) * d->F,
-                                            static_cast<uint64_t>(d->H) * 2, 64, 128) == CUDA_SUCCESS;
-            tm_ok = tm_ok && encode_tmap_2d(&c->tm_wd, HF, c->plane_d, d->F,
-                                            static_cast<uint64_t>(c->P) * d->H,
-                                            static_cast<uint64_t>(d->F) * 2, 64, 256) == CUDA_SUCCESS;
+            // tile-major planes: one 128-byte row of 64 elements per tensor row
+            const uint64_t plane_rows = static_cast<uint64_t>(c->P) * d->F * d->H / 64;
+            tm_ok = tm_ok && encode_tmap_2d(&c->tm_wg, BF, c->plane_g, 64, plane_rows, 128, 64,
+                                            128) == CUDA_SUCCESS;
+            tm_ok = tm_ok && encode_tmap_2d(&c->tm_wu, BF, c->plane_u, 64, plane_rows, 128, 64,
+                                            128) == CUDA_SUCCESS;
+            tm_ok = tm_ok && encode_tmap_2d(&c->tm_wd, HF, c->plane_d, 64, plane_rows, 128, 64,
+                                            256) == CUDA_SUCCESS;
             tm_ok = tm_ok && encode_tmap_2d(&c->tm_h, HF, c->h, d->F, static_cast<uint64_t>(R_cap),
                                             static_cast<uint64_t>(d->F) * 2, 64, 128) == CUDA_SUCCESS;
             if (d->n_shared > 0) {
@@ -499,15 +535,13 @@ estream_status estream_bind_arena(estream_ctx** out, const estream_arena_desc* d
                 const size_t sp = static_cast<size_t>(d->n_shared) * Fs * d->H * 2;
                 for (int l = 0; l < d->L && tm_ok; ++l) {
                     const char* base = static_cast<const char*>(c->shared_dev[l]);
-                    tm_ok = tm_ok && encode_tmap_2d(&c->tm_sg[l], BF, base, d->H,
-                                                    static_cast<uint64_t>(d->n_shared) * Fs,
-                                                    static_cast<uint64_t>(d->H) * 2, 64, 128) == CUDA_SUCCESS;
-                    tm_ok = tm_ok && encode_tmap_2d(&c->tm_su[l], BF, base + sp, d->H,
-                                                    static_cast<uint64_t>(d->n_shared) * Fs,
-                                                    static_cast<uint64_t>(d->H) * 2, 64, 128) == CUDA_SUCCESS;
-                    tm_ok = tm_ok && encode_tmap_2d(&c->tm_sd[l], HF, base + 2 * sp, Fs,
-                                                    static_cast<uint64_t>(d->n_shared) * d->H,
-                                                    static_cast<uint64_t>(Fs) * 2, 64, 256) == CUDA_SUCCESS;
+                    const uint64_t srows = static_cast<uint64_t>(d->n_shared) * Fs * d->H / 64;
+                    tm_ok = tm_ok && encode_tmap_2d(&c->tm_sg[l], BF, base, 64, srows, 128, 64,
+                                                    128) == CUDA_SUCCESS;
+                    tm_ok = tm_ok && encode_tmap_2d(&c->tm_su[l], BF, base + sp, 64, srows, 128,
+                                                    64, 128) == CUDA_SUCCESS;
+                    tm_ok = tm_ok && encode_tmap_2d(&c->tm_sd[l], HF, base + 2 * sp, 64, srows, 128,
+                                                    64, 256) == CUDA_SUCCESS;
                 }
             }
         }
@@ -560,7 +594,7 @@ estream_status fill_bank(estream_ctx* c, int layer, int q, int b, size_t* bytes)
 
 // K2 + K3 over segments [seg_begin, seg_begin + seg_count) of the routed
 // route map, whose experts sit in consecutive arena slots from slot_base.
-estream_status run_routed(estream_ctx* c, cudaStream_t s, const CUtensorMap* tm_x, const void* X,
+estream_status run_routed(estream_ctx* c, cudaStream_t s, const void* X,
                           int layer, const int32_t* mblk, int seg_begin, int seg_count,
                           int slot_base, int max_tiles_m, int max_rows, float* Y) {
     GemmSegments seg{};
@@ -582,8 +616,8 @@ estream_status run_routed(estream_ctx* c, cudaStream_t s, const CUtensorMap* tm_
                                     reinterpret_cast<const float*>(c->plane_g),
                                     reinterpret_cast<const float*>(c->plane_u), seg,
                                     static_cast<float*>(c->h), c->d.H, c->d.F, max_rows, s)
-                : launch_gateup(tm_x, &c->tm_wg, &c->tm_wu, seg, c->h, c->d.H, c->d.F, c->d.F,
-                                c->dev_err, c->num_sms, s);
+                : launch_gateup(X, &c->tm_wg, &c->tm_wu, seg, c->h, c->d.H, c->d.F, c->dev_err,
+                                c->num_sms, s);
         if (rc != cudaSuccess) return ESTREAM_ERR_CUDA;
         c->stats.n_gateup += c->timing ? 1 : 0;
     }
@@ -593,8 +627,8 @@ estream_status run_routed(estream_ctx* c, cudaStream_t s, const CUtensorMap* tm_
             f32 ? launch_down_f32(static_cast<const float*>(c->h),
                                   reinterpret_cast<const float*>(c->plane_d), seg, Y, c->out_rows,
                                   c->d.H, c->d.F, max_rows, s)
-                : launch_down(&c->tm_h, &c->tm_wd, seg, Y, c->out_rows, c->d.H, c->d.F, c->d.H,
-                              c->dev_err, c->num_sms, s);
+                : launch_down(&c->tm_h, &c->tm_wd, seg, Y, c->out_rows, c->d.H, c->d.F, c->dev_err,
+                              c->num_sms, s);
         if (rc != cudaSuccess) return ESTREAM_ERR_CUDA;
         c->stats.n_down += c->timing ? 1 : 0;
     }
@@ -603,7 +637,7 @@ estream_status run_routed(estream_ctx* c, cudaStream_t s, const CUtensorMap* tm_
 }
 
 // Shared experts: identity route map over all T tokens, weight 1.
-estream_status run_shared(estream_ctx* c, cudaStream_t s, const CUtensorMap* tm_x, const void* X,
+estream_status run_shared(estream_ctx* c, cudaStream_t s, const void* X,
                           int layer, int T, float* Y) {
     TimedScope ts(c, s, kTShared);
     const int ns = c->d.n_shared;
@@ -631,11 +665,11 @@ estream_status run_shared(estream_ctx* c, cudaStream_t s, const CUtensorMap* tm_
             rc = launch_down_f32(static_cast<const float*>(c->h_shared), base + 2 * sp, seg, Y,
                                  c->out_shared, c->d.H, Fs, ns * T, s);
     } else {
-        rc = launch_gateup(tm_x, &c->tm_sg[layer], &c->tm_su[layer], seg, c->h_shared, c->d.H, Fs,
-                           Fs, c->dev_err, c->num_sms, s);
+        rc = launch_gateup(X, &c->tm_sg[layer], &c->tm_su[layer], seg, c->h_shared, c->d.H, Fs,
+                           c->dev_err, c->num_sms, s);
         if (rc == cudaSuccess)
             rc = launch_down(&c->tm_hs, &c->tm_sd[layer], seg, Y, c->out_shared, c->d.H, Fs,
-                             c->d.H, c->dev_err, c->num_sms, s);
+                             c->dev_err, c->num_sms, s);
     }
     if (rc != cudaSuccess) return ESTREAM_ERR_CUDA;
     c->stats.launches += 3;
@@ -700,15 +734,10 @@ estream_status estream_moe_layer_prefill(estream_ctx* c, int layer, const void* 
     if (T > c->d.T_max || k > c->d.k_max) return ESTREAM_ERR_CAPACITY;
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
     const int E = c->d.E, G = c->d.G, H = c->d.H;
-    const bool f32 = c->d.wdtype == ESTREAM_F32;
     c->trace.clear();
     c->stats.calls += 1;
     TimedScope total(c, s, kTTotal);
 
-    CUtensorMap tm_x{};
-    if (!f32 && encode_tmap_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, H, T,
-                               static_cast<uint64_t>(H) * 2, 64, 1) != CUDA_SUCCESS)
-        return ESTREAM_ERR_CUDA;
     if (c->preload_pending) {
         if (cudaStreamWaitEvent(s, c->preload_done, 0) != cudaSuccess) return ESTREAM_ERR_CUDA;
         c->preload_pending = false;
@@ -752,7 +781,7 @@ estream_status estream_moe_layer_prefill(estream_ctx* c, int layer, const void* 
 
     // shared experts need no arena: they run first and overlap the first fills
     if (c->d.n_shared > 0) {
-        estream_status st = run_shared(c, s, &tm_x, X, layer, T, c->d.deterministic ? nullptr : Y);
+        estream_status st = run_shared(c, s, X, layer, T, c->d.deterministic ? nullptr : Y);
         if (st != ESTREAM_OK) { drain(c, s); return st; }
     }
 
@@ -760,7 +789,7 @@ estream_status estream_moe_layer_prefill(estream_ctx* c, int layer, const void* 
     if (resident) {
         // every group sits in bank q: one launch pair over all slots, no host sync
         for (int q = 0; q < c->n_groups; ++q) trace_state(c, q, layer, q, kInUse);
-        st = run_routed(c, s, &tm_x, X, layer, mblk, 0, E, 0, (R + kBM - 1) / kBM + E, R, Y_routed);
+        st = run_routed(c, s, X, layer, mblk, 0, E, 0, (R + kBM - 1) / kBM + E, R, Y_routed);
         c->stats.groups_hit += c->n_groups;
         for (int q = 0; q < c->n_groups && st == ESTREAM_OK; ++q) {
             if (cudaEventRecord(c->banks[q].released, s) != cudaSuccess) st = ESTREAM_ERR_CUDA;
@@ -803,7 +832,7 @@ estream_status estream_moe_layer_prefill(estream_ctx* c, int layer, const void* 
             int mt = 0;
             for (int e = s0; e < s1; ++e)
                 mt += (c->h_offsets[e + 1] - c->h_offsets[e] + kBM - 1) / kBM;
-            st = run_routed(c, s, &tm_x, X, layer, mblk, s0, s1 - s0, b * G, mt, cnt, Y_routed);
+            st = run_routed(c, s, X, layer, mblk, s0, s1 - s0, b * G, mt, cnt, Y_routed);
             if (st != ESTREAM_OK) break;
             if (cudaEventRecord(c->banks[b].released, s) != cudaSuccess) { st = ESTREAM_ERR_CUDA; break; }
             c->banks[b].release_pending = true;

@@ -101,6 +101,12 @@ def test_sizes(es):
     assert es.shared_bytes(2, 2048, 1408, es.BF16) == 2 * 3 * 2048 * 1408 * 2 + 16
 
 
+def untile(flat, rows, cols, tile_rows):
+    """Inverse of the tile-major plane layout [rows/tr][cols/64][tr][64]."""
+    t = flat.reshape(rows // tile_rows, cols // 64, tile_rows, 64)
+    return t.transpose(0, 2, 1, 3).reshape(rows, cols)
+
+
 def _bf16_bits(t):
     return t.view(torch.int16).numpy().view(np.uint16)
 
@@ -108,8 +114,10 @@ def _bf16_bits(t):
 @pytest.mark.parametrize("G", [1, 3, 4, 8])
 def test_pack_experts_layout(es, G):
     """Group q holds the experts at storage positions [qG, qG+G) in order,
-    as [gate][up][down]; the down plane is fp16(W_d * 2^s) with the scale
-    2^-s stored after the groups, and converts back exactly."""
+    as [gate][up][down], each plane tile-major (128-row tiles for gate/up,
+    256-row tiles for down, 64 columns each); the down plane is
+    fp16(W_d * 2^s) with the scale 2^-s stored after the groups, and converts
+    back exactly."""
     E, H, F = 7, 256, 128
     g = torch.Generator().manual_seed(3)
     Wg = (torch.randn(E, F, H, generator=g) * 0.02).bfloat16()
@@ -129,15 +137,16 @@ def test_pack_experts_layout(es, G):
         q, r = divmod(pos, G)
         n_q = min(G, E - q * G)
         base = q * G * W
-        gate = raw[base + r * S: base + (r + 1) * S].view(np.uint16)
-        up = raw[base + n_q * S + r * S: base + n_q * S + (r + 1) * S].view(np.uint16)
-        down = raw[base + 2 * n_q * S + r * S: base + 2 * n_q * S + (r + 1) * S].view(np.float16)
-        np.testing.assert_array_equal(gate, _bf16_bits(Wg[e]).ravel())
-        np.testing.assert_array_equal(up, _bf16_bits(Wu[e]).ravel())
+        gate = untile(raw[base + r * S: base + (r + 1) * S].view(np.uint16), F, H, 128)
+        up = untile(raw[base + n_q * S + r * S: base + n_q * S + (r + 1) * S].view(np.uint16), F, H, 128)
+        down = untile(raw[base + 2 * n_q * S + r * S: base + 2 * n_q * S + (r + 1) * S].view(np.float16),
+                      H, F, 256)
+        np.testing.assert_array_equal(gate, _bf16_bits(Wg[e]))
+        np.testing.assert_array_equal(up, _bf16_bits(Wu[e]))
         sc = float(scales[pos])
         assert sc > 0 and np.log2(sc) == int(np.log2(sc))      # a power of two
         back = down.astype(np.float64) * sc
-        np.testing.assert_array_equal(back, Wd[e].double().numpy().ravel())
+        np.testing.assert_array_equal(back, Wd[e].double().numpy())
         assert 2.0 ** 14 <= np.abs(down.astype(np.float64)).max() < 2.0 ** 15
 
 
