@@ -28,6 +28,24 @@ if ROOT not in sys.path:
 METRIC = "MoE-layer prefill tokens/sec and grouped-GEMM TFLOP/s vs bf16 peak (1 GB300)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
+# DRAM bytes (read + write) of one gate/up (K2) launch, from the ncu capture
+# summarised in profiles/k_expert_gemm_olmoe_resident.md. Reported only while
+# the kernel source is the one that was captured.
+PROFILED_TRAFFIC = {
+    "c2": {"kernel_sha256_16": "b2debf94adefc874", "bytes": 568974336},
+}
+KERNEL_SRC = os.path.join(ROOT, "routed_expert_ffn_topk_gb300", "csrc", "expert_gemm.cu")
+
+
+def profiled_traffic(config: str):
+    import hashlib
+    rec = PROFILED_TRAFFIC.get(config)
+    if not rec:
+        return None
+    with open(KERNEL_SRC, "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()[:16]
+    return rec["bytes"] if sha == rec["kernel_sha256_16"] else None
+
 
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -309,6 +327,8 @@ def run_ours(args, rank, world, local_rank):
                 "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": None}
     roof["peak_source"] = peaks["source"]
+    roof["traffic"] = profiled_traffic(cfg.key) if L == 1 else None
+    roof["algorithmic_bytes_per_launch"] = int(per_launch_k2_bytes)
     roof["ms_per_launch"] = round(k2_ms, 4)
     flops_step = cfg.flops_per_layer() * L
     gemm_ms = (stats["ms_gateup"] + stats["ms_down"] + stats["ms_shared"]) / args.steps
@@ -363,11 +383,7 @@ def run_ours(args, rank, world, local_rank):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16 gate/up, fp16 down (fp32 accumulate)" if cfg.dtype == "bf16" else "f32",
         "data": "synthetic (seeded; random-init weights)",
-        "config": {"workload": f"{cfg.key} {cfg.name}: T={cfg.T} H={cfg.H} E={cfg.E} k={cfg.k} "
-                               f"F={cfg.F}" + (f" shared={cfg.n_shared}x{cfg.F_shared}" if cfg.n_shared else "")
-                               + (f" layers={L}" if L > 1 else "") + f", experts {mode}",
-                   "tokens_per_step_per_gpu": cfg.T, "l2": "flushed (256 MiB write) before every step",
-                   "parallelism": f"replicas x{world}"},
+        "config": workload_config(cfg, world, mode),
         "tflops": round(tflops, 1), "grouped_gemm_tflops": round(gemm_tflops, 1),
         "frac_bf16_peak": round(gemm_tflops / peaks["bf16_tflops"], 4),
         "roofline": roof, "kernels": kernels,
@@ -467,6 +483,15 @@ def measure_paged(args, cfg, wl, dev, stream, flush, peaks):
 # reference arm: the CPU oracle
 # --------------------------------------------------------------------------
 
+def workload_config(cfg, world, mode="resident"):
+    L = cfg.layers
+    return {"workload": f"{cfg.key} {cfg.name}: T={cfg.T} H={cfg.H} E={cfg.E} k={cfg.k} "
+                        f"F={cfg.F}" + (f" shared={cfg.n_shared}x{cfg.F_shared}" if cfg.n_shared else "")
+                        + (f" layers={L}" if L > 1 else "") + f", experts {mode}",
+            "tokens_per_step_per_gpu": cfg.T, "l2": "flushed (256 MiB write) before every step",
+            "parallelism": f"replicas x{world}"}
+
+
 def run_reference(args, rank, world):
     from routed_expert_ffn_topk_gb300 import workloads as W
     cfg = W.CONFIGS[args.config]
@@ -486,7 +511,7 @@ def run_reference(args, rank, world):
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic (seeded)",
-            "config": {"workload": f"{cfg.key} {cfg.name}: T={cfg.T} H={cfg.H} E={cfg.E} k={cfg.k} F={cfg.F}"},
+            "config": workload_config(cfg, world),
             "cpu_baseline": {"value": round(tps, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
                              "sample": f"routing of all {cfg.T} tokens + Eq.2 for {n} sampled tokens per step"},
             "e2e": {"value": round(tps, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
