@@ -152,16 +152,16 @@ class ClockSampler:
 # --------------------------------------------------------------------------
 
 def algorithmic(cfg, n_active_per_layer):
-    """Algorithmic bytes of K2 and K3 for one layer:
-    K2: gate+up weights of the active experts + X once + h written;
-    K3: down weights of the active experts + h read + Y read and written."""
+    """Algorithmic bytes and FLOPs of one layer's routed fused expert kernel
+    (see the design doc): the weights of the experts with routes (gate, up, down:
+    3*H*F*2 bytes each), X read once (T*H*2) and Y read and written
+    (2*T*H*4). The fp16 h intermediate (2*R*F*2 bytes, L2-resident at these
+    sizes) is implementation traffic and not counted. Returned as the old
+    (gate/up, down) split so callers can sum them."""
     H, F, T, R = cfg.H, cfg.F, cfg.T, cfg.T * cfg.k
-    es_ = 2
-    k2 = n_active_per_layer * 2 * H * F * es_ + T * H * es_ + R * F * 2
-    k3 = n_active_per_layer * H * F * 2 + R * F * 2 + 2 * T * H * 4
-    k2_flops = 4.0 * H * F * R
-    k3_flops = 2.0 * H * F * R
-    return k2, k3, k2_flops, k3_flops
+    gu = n_active_per_layer * 2 * H * F * 2 + T * H * 2
+    dn = n_active_per_layer * H * F * 2 + 2 * T * H * 4
+    return gu, dn, 4.0 * H * F * R, 2.0 * H * F * R
 
 
 def active_experts(cfg, logits_layers):
@@ -302,44 +302,44 @@ def run_ours(args, rank, world, local_rank):
     value = tokens / (ms_per_step / 1e3)
     gpu_launches = stats["launches"] + (L - 1) * args.steps   # + the bf16 casts between layers
 
-    # ---- per-kernel roofline (CUDA events inside the library, same stream) ----
+    # ---- roofline of the fused expert kernel (CUDA events inside the library, same stream) ----
     n_active = active_experts(cfg, wl.logits)
-    k2b = k3b = k2f = k3f = 0.0
+    ffn_b = ffn_f = 0.0
     for l in range(L):
         a, b, c, d = algorithmic(cfg, n_active[l])
-        k2b += a; k3b += b; k2f += c; k3f += d
-    n_k2 = max(1, stats["n_gateup"])
-    n_k3 = max(1, stats["n_down"])
-    k2_ms = stats["ms_gateup"] / n_k2
-    k3_ms = stats["ms_down"] / n_k3
-    per_launch_k2_bytes = k2b / (n_k2 / args.steps)
-    per_launch_k2_flops = k2f / (n_k2 / args.steps)
-    ai = k2f / k2b
+        ffn_b += a + b
+        ffn_f += c + d
+    n_ffn = max(1, stats["n_ffn"])
+    ffn_ms = stats["ms_ffn"] / n_ffn
+    launches_per_step = n_ffn / args.steps
+    per_launch_bytes = ffn_b / launches_per_step
+    per_launch_flops = ffn_f / launches_per_step
+    ai = ffn_f / ffn_b
     ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    kname = "k_expert_ffn (gather + gate/up + SwiGLU + down + scatter)"
     if ai < ridge:
-        achieved = per_launch_k2_bytes / (k2_ms / 1e3) / 1e9
-        roof = {"kernel": "k_expert_gemm<gate/up> (K2)", "bound": "hbm", "achieved": round(achieved, 1),
+        achieved = per_launch_bytes / (ffn_ms / 1e3) / 1e9
+        roof = {"kernel": kname, "bound": "hbm", "achieved": round(achieved, 1),
                 "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                 "traffic": None}
     else:
-        achieved = per_launch_k2_flops / (k2_ms / 1e3) / 1e12
-        roof = {"kernel": "k_expert_gemm<gate/up> (K2)", "bound": "tensor", "achieved": round(achieved, 1),
+        achieved = per_launch_flops / (ffn_ms / 1e3) / 1e12
+        roof = {"kernel": kname, "bound": "tensor", "achieved": round(achieved, 1),
                 "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": None}
     roof["peak_source"] = peaks["source"]
     roof["traffic"] = profiled_traffic(cfg.key) if L == 1 else None
-    roof["algorithmic_bytes_per_launch"] = int(per_launch_k2_bytes)
-    roof["ms_per_launch"] = round(k2_ms, 4)
+    roof["algorithmic_bytes_per_launch"] = int(per_launch_bytes)
+    roof["algorithmic_flops_per_launch"] = int(per_launch_flops)
+    roof["ms_per_launch"] = round(ffn_ms, 4)
     flops_step = cfg.flops_per_layer() * L
-    gemm_ms = (stats["ms_gateup"] + stats["ms_down"] + stats["ms_shared"]) / args.steps
+    gemm_ms = (stats["ms_ffn"] + stats["ms_shared"]) / args.steps
     kernels = {
         "route_ms": round(stats["ms_route"] / args.steps, 4),
-        "gateup_ms": round(stats["ms_gateup"] / args.steps, 4),
-        "down_ms": round(stats["ms_down"] / args.steps, 4),
+        "ffn_ms": round(stats["ms_ffn"] / args.steps, 4),
         "shared_ms": round(stats["ms_shared"] / args.steps, 4),
-        "down_GBps": round(k3b / (stats["ms_down"] / args.steps / 1e3) / 1e9, 1),
-        "down_TFLOPs": round(k3f / (stats["ms_down"] / args.steps / 1e3) / 1e12, 1),
-        "gateup_TFLOPs": round(k2f / (stats["ms_gateup"] / args.steps / 1e3) / 1e12, 1),
+        "ffn_GBps": round(ffn_b / (stats["ms_ffn"] / args.steps / 1e3) / 1e9, 1),
+        "ffn_TFLOPs": round(ffn_f / (stats["ms_ffn"] / args.steps / 1e3) / 1e12, 1),
     }
     tflops = flops_step / (ms_per_step / 1e3) / 1e12
     gemm_tflops = flops_step / (gemm_ms / 1e3) / 1e12
@@ -463,8 +463,7 @@ def measure_paged(args, cfg, wl, dev, stream, flush, peaks):
         best = ms if best is None else min(best, ms)
     h2d_peak = (1 << 30) / (best / 1e3) / 1e9
     del big, bigd, dst
-    t_exec = stats["ms_route"] / len(times) + (stats["ms_gateup"] + stats["ms_down"] +
-                                               stats["ms_shared"]) / len(times)
+    t_exec = (stats["ms_route"] + stats["ms_ffn"] + stats["ms_shared"]) / len(times)
     h2d_gbs = bytes_per_call / (t_paged / 1e3) / 1e9
     return {
         "arena": f"P={cfg.P} (G={cfg.G}, B={cfg.B})", "tokens_per_s": round(cfg.T / (t_paged / 1e3), 1),

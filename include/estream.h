@@ -254,14 +254,13 @@ estream_status estream_moe_layer_prefill(estream_ctx* c, int layer, const void* 
  * only while timing is on (estream_set_timing); reading them synchronises. */
 typedef struct {
     int calls;
-    int launches;            /* kernels (and memsets) this library enqueued */
-    double ms_route;         /* routing + route map kernels */
-    double ms_gateup;        /* K2 launches */
-    double ms_down;          /* K3 launches */
-    double ms_shared;        /* shared-expert K2 + K3 */
+    int launches;            /* kernels this library enqueued (memsets and copies not counted) */
+    double ms_route;         /* routing + route map (memset + one kernel) */
+    double ms_ffn;           /* routed fused expert kernel (gather, gate/up, SwiGLU, down, scatter) */
+    double ms_shared;        /* shared experts (identity map + fused expert kernel) */
     double ms_combine;       /* deterministic combine */
     double ms_total;         /* first to last event of each call, summed */
-    int n_gateup, n_down;    /* K2 / K3 launches counted in ms_gateup / ms_down */
+    int n_ffn;               /* routed fused expert launches counted in ms_ffn */
     double h2d_bytes;        /* bytes copied into the arena */
     int groups_loaded, groups_skipped, groups_hit;
     double ms_io_busy;       /* copy-stream busy time (timing on) */

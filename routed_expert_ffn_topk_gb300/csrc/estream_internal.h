@@ -31,6 +31,7 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // Layout of the route-build workspace (all offsets 256-byte aligned).
 struct RouteWorkspace {
     size_t err_off;      // int32 device error word
+    size_t sync_off;     // int32 grid-barrier counter of the fused route kernel
     size_t hist_off;     // int32 [nchunk][P+1]: per-chunk counts, then per-chunk bases
     size_t mblk_off;     // int32 [P+2]: exclusive prefix of ceil(count[s]/kBM), s < P
     size_t total;
@@ -40,16 +41,19 @@ RouteWorkspace route_workspace_layout(int T, int k, int P);
 
 // Enqueue the full route build (K1). `ws` must hold route_workspace_layout(T,k,P).
 // rec_pos (optional, [T*k]) receives, for route i, its position in the CSR.
+// done (optional) is zeroed over the route map's m-blocks (mblk[P] ints) for
+// the fused expert kernel's m-block counters.
 cudaError_t launch_route_build(const float* logits, int T, int E, int k, int renorm,
                                const int32_t* phi, int P, int32_t* topk_ids, float* alpha,
                                int32_t* offsets, int32_t* rec_tok, int32_t* rec_route,
-                               int32_t* rec_pos, void* ws, cudaStream_t stream,
-                               int* n_launches);
+                               int32_t* rec_pos, int32_t* done, void* ws,
+                               cudaStream_t stream, int* n_launches);
 
 // Identity route map for the shared experts: n_shared segments of T rows,
-// rec_tok[p] = p mod T, offsets[s] = s*T, mblk[s] = s*ceil(T/kBM).
+// rec_tok[p] = p mod T, offsets[s] = s*T, mblk[s] = s*ceil(T/kBM); zeroes
+// done[0 .. n_shared*ceil(T/kBM)).
 cudaError_t launch_identity_map(int T, int n_shared, int32_t* offsets, int32_t* rec_tok,
-                                int32_t* mblk, cudaStream_t stream);
+                                int32_t* mblk, int32_t* done, cudaStream_t stream);
 
 // ---------------------------------------------------------------------------
 // Grouped expert GEMMs (K2 gate/up + SwiGLU, K3 down + weighted scatter-add)
@@ -67,17 +71,18 @@ struct GemmSegments {
     int max_tiles_m;           // host upper bound on m-blocks in the range
 };
 
-// K2 (bf16 tensor cores): h[p, :] = fp16(SiLU(X[tok(p)] Wg_slot^T) * (X[tok(p)] Wu_slot^T)).
-// X: device [T][H] bf16, 16-byte aligned rows.
-cudaError_t launch_gateup(const void* X, const CUtensorMap* tm_wg, const CUtensorMap* tm_wu,
-                          const GemmSegments& seg, void* h, int H, int F, int* dev_err,
-                          int num_sms, cudaStream_t stream);
-
-// K3 (fp16 tensor cores): Y[tok(p), :] += alpha(p) * scale(seg) * (h[p] Wd_slot^T), or
-// out_rows[p, :] = ... when out_rows != null (deterministic mode).
-cudaError_t launch_down(const CUtensorMap* tm_h, const CUtensorMap* tm_wd,
-                        const GemmSegments& seg, float* Y, float* out_rows, int H, int F,
-                        int* dev_err, int num_sms, cudaStream_t stream);
+// Fused expert FFN (one cooperative launch), phases bit 0 / bit 1:
+//   gate/up: h[p, :] = fp16(SiLU(X[tok(p)] Wg_slot^T) * (X[tok(p)] Wu_slot^T)) (bf16 MMA);
+//   down:    Y[tok(p), :] += alpha(p) * scale(seg) * (h[p] Wd_slot^T) (fp16 MMA), or
+//            out_rows[p, :] = ... when out_rows != null (deterministic mode).
+// X: device [T][H] bf16 (16-byte aligned rows); h: [rows][F] fp16; done: one
+// zeroed int per absolute m-block of the route map (mblk indices).
+// tm_h: TMA map of h ([rows][F] fp16, 64 x 128 boxes, 128-byte swizzle).
+cudaError_t launch_expert_ffn(const CUtensorMap* tm_wg, const CUtensorMap* tm_wu,
+                              const CUtensorMap* tm_wd, const CUtensorMap* tm_h,
+                              const GemmSegments& seg, const void* X,
+                              void* h, float* Y, float* out_rows, int* done, int H, int F,
+                              int phases, int* dev_err, int num_sms, cudaStream_t stream);
 
 // fp32 path (CUDA-core FMA): the same two steps for fp32 X and weights.
 // Weight planes are [slots][F][H] (gate, up) and [slots][H][F] (down).

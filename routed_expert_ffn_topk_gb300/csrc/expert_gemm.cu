@@ -1,5 +1,5 @@
-// K2 / K3: the routed expert FFN as two grouped GEMMs on the 5th-generation
-// tensor cores (tcgen05 + TMEM), fed by TMA.
+// The routed expert FFN as one fused, persistent operator on the
+// 5th-generation tensor cores (tcgen05 + TMEM), fed by TMA and cp.async.
 //
 // "EStream: Fast and Memory-Efficient MoE Prefill through Expert
 // Virtualization on Mobile NPUs", section 3.2 ("Fused Expert Execution with
@@ -7,38 +7,43 @@
 // rows of X are gathered, the gate and up projections are evaluated as tile
 // pairs, SiLU(g) * u is applied to completed pairs, the down projection is
 // evaluated, and completed down tiles are multiplied by the route weight and
-// scatter-added into the token accumulator Y (Eq. 2).
+// scatter-added into the token accumulator Y (Eq. 2) -- one route-aware
+// operator, as the paper builds it.
 //
-// GB300 form. One persistent kernel per GEMM walks a list of 128-row tiles
-// built from the route map (segment = slot, m-block, n-block), with three
-// warp roles per CTA:
-//   warp 0     TMA producer into a 4-stage shared-memory ring: the weight
-//              tile of every stage, and for K3 also the A tile of h (records
-//              are contiguous by slot, so a plain 2D box).
-//   warps 6-9  (K2 only) the row gather: each record's 128-byte slice of
-//              X[tok] is copied into its row of the stage's A tile with 16-byte
-//              cp.async, writing the 128-byte-swizzled layout the MMA reads
-//              (chunk c of row r at c ^ (r mod 8)). TMA tile::gather4 moves
-//              only four 128-byte rows per instruction, which measured ~2.3x
-//              slower for this kernel than plain tiles; the LSU path keeps
-//              the gather fused at tile speed.
-//   warp 1     allocates 512 TMEM columns (two 128x256 fp32 accumulators) and
-//              one elected lane issues tcgen05.mma (M=128, N=256, K=16 per
-//              instruction, kind::f16), committing stages back to the producer
-//              and finished accumulators to the epilogue.
-//   warps 2-5  epilogue: tcgen05.ld of the accumulator; K2 writes
-//              h = SiLU(g) * u as fp16; K3 scales by alpha times the expert's
-//              down-weight scale and adds into Y[t] with vector fp32
-//              reductions (or stores the scaled row for the deterministic
-//              combine).
-// Operand types: K2 multiplies bf16 X by bf16 W_g / W_u. K3 multiplies fp16 h
-// by fp16 W_d, which the offline packer converted from bf16 with an exact
-// per-expert power-of-two scale: fp16 keeps 3 more significand bits of h than
-// bf16 would, which is what keeps Y within the accuracy bound.
+// GB300 form. One cooperative kernel per call walks a list of 128-row tiles
+// built from the route map: first every gate/up tile (segment, n-block of 128
+// h columns, m-block), then every down tile (segment, n-block of 256 Y
+// columns, m-block). Warp roles per CTA (one CTA per SM):
+//   warp 0     TMA producer into a 4-stage ring: the weight tiles (gate + up
+//              2 x 16 KB, or down 32 KB, per stage) and, for down tiles, the
+//              16 KB A tile of h once the m-block's gate/up tiles have all
+//              published (records are contiguous by slot, so a plain box).
+//   warp 1     allocates 512 TMEM columns (two 128x256 fp32 accumulators);
+//              one lane issues tcgen05.mma (M=128, N=256, K=16 per
+//              instruction, kind::f16), committing stages back to the
+//              producers and finished accumulators to the epilogue.
+//   warps 2-5  epilogue: tcgen05.ld of the accumulator. Gate/up tiles write
+//              h = SiLU(g) * u as fp16 and publish "m-block done" counters;
+//              down tiles scale by alpha times the expert's down-weight scale
+//              and add into Y[t] with vector fp32 reductions (or store the
+//              scaled row for the deterministic combine).
+//   warps 6-9  row gather of gate/up tiles: each record's 128-byte slice of
+//              X[tok] for the stage's K range is copied with 16-byte cp.async
+//              into the 128-byte-swizzled layout the MMA reads (chunk c of row
+//              r at c ^ (r mod 8)). TMA tile::gather4 moves only four rows per
+//              instruction and measured ~2.3x slower here. For down tiles
+//              these warps only pass the stages through.
 // The gate and up weight tiles of one n-block sit back to back in shared
 // memory, so a single N=256 instruction produces both halves of a pair.
+// Operand types: gate/up multiply bf16 X by bf16 W_g / W_u; down multiplies
+// fp16 h by fp16 W_d, which the offline packer converted from bf16 with an
+// exact per-expert power-of-two scale: fp16 keeps 3 more significand bits of
+// h than bf16 would, which is what keeps Y within the accuracy bound.
 // Every wait is bounded: on timeout the kernel records an error word, lets
-// outstanding copies and MMAs land, frees TMEM and returns.
+// outstanding copies and MMAs land, frees TMEM and returns. The cross-CTA
+// wait (down tile on gate/up tiles) is deadlock-free because the launch is
+// cooperative (all CTAs resident) and every gate/up tile precedes every down
+// tile in each CTA's tile order.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -52,13 +57,11 @@ constexpr int kStages = 4;
 constexpr int kRowBytes = 128;                    // one swizzle row of K
 constexpr int kTileABytes = kBM * kRowBytes;      // 16 KB
 constexpr int kTileBBytes = 256 * kRowBytes;      // 32 KB
-constexpr int kStageBytes = kTileABytes + kTileBBytes;
 constexpr int kAccCols = 256;
 constexpr int kTmemCols = 512;
-constexpr int kThreadsDown = 192;       // TMA, MMA, 4 epilogue warps
-constexpr int kThreadsGateUp = 320;     // + 4 row-gather warps
-constexpr int kGatherWarp0 = 6;
-constexpr int kGatherDepth = 2;         // cp.async groups kept in flight per gather thread
+constexpr int kThreads = 320;           // TMA, MMA, 4 epilogue warps, 4 A-loader warps
+constexpr int kLoaderWarp0 = 6;
+constexpr int kLoaderDepth = 2;         // cp.async groups kept in flight per loader thread
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr uint64_t kDrainLimitNs = 100000000ull;  // 0.1 s
 constexpr float kHalfMax = 65504.0f;
@@ -279,23 +282,50 @@ __device__ __forceinline__ void fence_proxy_async() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-template <bool kGateUp>
-__global__ void __launch_bounds__(kGateUp ? kThreadsGateUp : kThreadsDown, 1)
-    k_expert_gemm(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b0,
-                  const __grid_constant__ CUtensorMap tm_b1, const GemmSegments seg,
-                  const __nv_bfloat16* __restrict__ x_src, void* h_out, float* Y, float* out_rows,
-                  int H, int F, int* dev_err) {
+// Acquire load of a counter another CTA publishes.
+__device__ __forceinline__ int ld_acquire(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void red_release_add(int* p, int v) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+struct FfnArgs {
+    GemmSegments seg;
+    const __nv_bfloat16* x;  // [T][H]: gate/up A rows (gathered)
+    __half* h;               // [rows][F]: written by gate/up tiles, read by down tiles
+    float* Y;                // [T][H] accumulator
+    float* out_rows;         // deterministic mode: [rows][H], else null
+    int* done;               // per absolute m-block: epilogue-warp publications of gate/up tiles
+    int* dev_err;
+    int H, F;
+    int phases;              // bit 0: gate/up tiles, bit 1: down tiles
+};
+
+// Orders this thread's generic-proxy global accesses with its async-proxy
+// (TMA) accesses: h is written with st.global and read back with TMA.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    k_expert_ffn(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant__ CUtensorMap tm_wu,
+                 const __grid_constant__ CUtensorMap tm_wd, const __grid_constant__ CUtensorMap tm_h,
+                 const FfnArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
+    const GemmSegments& seg = a.seg;
     const uint32_t sbase = smem_addr(smem);
     const uint32_t sA = sbase + kOffA;
     const uint32_t sB = sbase + kOffB;
     const uint32_t bar0 = sbase + kOffBar;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
-    auto accf_bar = [&](int a) { return bar0 + 8u * (2 * kStages + a); };
-    auto acce_bar = [&](int a) { return bar0 + 8u * (2 * kStages + 2 + a); };
+    auto accf_bar = [&](int q) { return bar0 + 8u * (2 * kStages + q); };
+    auto acce_bar = [&](int q) { return bar0 + 8u * (2 * kStages + 2 + q); };
     const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 4);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
@@ -310,13 +340,12 @@ __global__ void __launch_bounds__(kGateUp ? kThreadsGateUp : kThreadsDown, 1)
         table[s] = seg.mblk[seg.seg_begin + s] - m0;
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            // K2: the TMA producer's expect_tx arrival + one per gather thread
-            mbar_init(full_bar(s), kGateUp ? 1 + kBM : 1);
+            mbar_init(full_bar(s), 1 + kBM);  // producer's expect_tx + one per loader thread
             mbar_init(empty_bar(s), 1);
         }
-        for (int a = 0; a < 2; ++a) {
-            mbar_init(accf_bar(a), 1);
-            mbar_init(acce_bar(a), 4);  // one arrival per epilogue warp
+        for (int q = 0; q < 2; ++q) {
+            mbar_init(accf_bar(q), 1);
+            mbar_init(acce_bar(q), 4);  // one arrival per epilogue warp
         }
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
@@ -332,52 +361,83 @@ __global__ void __launch_bounds__(kGateUp ? kThreadsGateUp : kThreadsDown, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    const int NB = kGateUp ? (F / 128) : (H / 256);
-    const int K = kGateUp ? H : F;
-    const int BKe = 64;  // 16-bit elements per 128-byte row
-    const int num_kb = K / BKe;
-    const int total = table[seg.seg_count] * NB;
+    const int H = a.H, F = a.F;
+    const int NBA = F / 128, NBB = H / 256;   // n-blocks of gate/up and of down tiles
+    const int KBA = H / 64, KBB = F / 64;     // k-blocks (64 elements = 128 bytes)
+    const int MB = table[seg.seg_count];
+    const int TA = (a.phases & 1) ? MB * NBA : 0;
+    const int TB = (a.phases & 2) ? MB * NBB : 0;
+    const int total = TA + TB;
+    const int done_target = 4 * NBA;          // every epilogue warp of every gate/up n-block
 
     if (warp == 0) {
-        // ------------------------------ TMA producer ------------------------------
+        // ------------------------------ TMA producer (weights) ------------------------------
         int stage = 0;
         uint32_t phase = 0;
         int issued[kStages];
         for (int s = 0; s < kStages; ++s) issued[s] = -1;
         bool ok = true;
         for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-            const Tile ti = decode_tile(t, table, seg.seg_count, NB, seg.offsets, seg.seg_begin);
+            const bool gu = t < TA;
+            const Tile ti = decode_tile(gu ? t : t - TA, table, seg.seg_count, gu ? NBA : NBB,
+                                        seg.offsets, seg.seg_begin);
             const int slot = seg.slot_base + ti.seg;
-            // weight planes are tile-major: the (n-block, k-block) tile of a
-            // slot is one contiguous box of 128 (K2) or 256 (K3) rows of 64
-            const int tile_rows = kGateUp ? 128 : 256;
-            const int brow0 = ((slot * NB + ti.nb) * num_kb) * tile_rows;
+            // weight planes are tile-major: the (n-block, k-block) box of a slot
+            // is one contiguous run of 128 (gate/up) or 256 (down) rows of 128 B
+            const int num_kb = gu ? KBA : KBB;
+            const int tile_rows = gu ? 128 : 256;
+            const int brow0 = (slot * (gu ? NBA : NBB) + ti.nb) * num_kb * tile_rows;
+            if (!gu) {
+                // the m-block's h rows are complete once every epilogue warp of
+                // every gate/up n-block has published
+                const int* cnt = a.done + seg.mblk[seg.seg_begin + ti.seg] + ti.mb;
+                bool w = true;
+                if (lane == 0 && ld_acquire(cnt) < done_target) {
+                    const uint64_t t0 = global_ns();
+                    while (ld_acquire(cnt) < done_target) {
+                        if (*abort_flag) {
+                            w = false;
+                            break;
+                        }
+                        if (global_ns() - t0 > kWaitLimitNs) {
+                            *abort_flag = 1;
+                            record_error(a.dev_err, kDevErrTimeout);
+                            w = false;
+                            break;
+                        }
+                    }
+                }
+                if (lane == 0) fence_proxy_async_global();  // before the TMA reads of h
+                w = __shfl_sync(0xffffffffu, w, 0);
+                if (!w) {
+                    ok = false;
+                    break;
+                }
+            }
             for (int kb = 0; kb < num_kb; ++kb) {
                 bool w = true;
-                if (lane == 0) w = mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, dev_err);
+                if (lane == 0) w = mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, a.dev_err);
                 w = __shfl_sync(0xffffffffu, w, 0);
                 if (!w) {
                     ok = false;
                     break;
                 }
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(full_bar(stage), kGateUp ? kTileBBytes : kStageBytes);
+                    mbar_arrive_expect_tx(full_bar(stage),
+                                          gu ? kTileBBytes : kTileBBytes + kTileABytes);
                     issued[stage] = static_cast<int>(phase);
+                    const uint32_t b_dst = sB + stage * kTileBBytes;
+                    const int brow = brow0 + kb * tile_rows;
+                    if (gu) {
+                        tma_load_2d(b_dst, &tm_wg, 0, brow, full_bar(stage));
+                        tma_load_2d(b_dst + 128 * kRowBytes, &tm_wu, 0, brow, full_bar(stage));
+                    } else {
+                        tma_load_2d(sA + stage * kTileABytes, &tm_h, kb * 64, ti.row0,
+                                    full_bar(stage));
+                        tma_load_2d(b_dst, &tm_wd, 0, brow, full_bar(stage));
+                    }
                 }
                 __syncwarp();
-                const uint32_t a_dst = sA + stage * kTileABytes;
-                const uint32_t b_dst = sB + stage * kTileBBytes;
-                const int x = kb * BKe;
-                const int brow = brow0 + kb * tile_rows;
-                if (kGateUp) {
-                    if (lane == 0) {
-                        tma_load_2d(b_dst, &tm_b0, 0, brow, full_bar(stage));
-                        tma_load_2d(b_dst + 128 * kRowBytes, &tm_b1, 0, brow, full_bar(stage));
-                    }
-                } else if (lane == 0) {
-                    tma_load_2d(a_dst, &tm_a, x, ti.row0, full_bar(stage));
-                    tma_load_2d(b_dst, &tm_b0, 0, brow, full_bar(stage));
-                }
                 if (++stage == kStages) {
                     stage = 0;
                     phase ^= 1u;
@@ -391,38 +451,70 @@ __global__ void __launch_bounds__(kGateUp ? kThreadsGateUp : kThreadsDown, 1)
                     mbar_wait(full_bar(s), static_cast<uint32_t>(issued[s]), abort_flag, nullptr,
                               kDrainLimitNs);
         }
-    } else if (kGateUp && warp >= kGatherWarp0) {
-        // ------------------------------ row gather (K2) ------------------------------
-        // Gather warp w covers rows [32w, 32w+32) of every A stage; in copy
+    } else if (warp >= kLoaderWarp0) {
+        // ------------------------------ A-operand loader ------------------------------
+        // Loader warp w covers rows [32w, 32w+32) of every A stage; in copy
         // instruction i lane l moves 16-byte chunk (l mod 8) of row
         // 32w + 4i + l/8, so each warp-instruction reads four whole 128-byte
         // rows. Every thread arrives on a stage once its own copies are
-        // complete (wait_group) and fenced to the async proxy; kGatherDepth
+        // complete (wait_group) and fenced to the async proxy; kLoaderDepth
         // stages stay in flight per thread.
-        const int gw = warp - kGatherWarp0;
+        const int gw = warp - kLoaderWarp0;
         const uint32_t chunk = static_cast<uint32_t>(lane & 7);
         int stage = 0;
         uint32_t phase = 0;
-        int pend[kGatherDepth + 1];
+        int pend[kLoaderDepth + 1];
         int npend = 0;
         bool ok = true;
         for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-            const Tile ti = decode_tile(t, table, seg.seg_count, NB, seg.offsets, seg.seg_begin);
-            const __nv_bfloat16* src_row[8];
+            const bool gu = t < TA;
+            const Tile ti = decode_tile(gu ? t : t - TA, table, seg.seg_count, gu ? NBA : NBB,
+                                        seg.offsets, seg.seg_begin);
+            const int num_kb = gu ? KBA : KBB;
+            if (!gu) {
+                // down tile: the producer loads A (h) with TMA; publish the
+                // stages still pending, then only pass this tile's stages on
+                if (npend > 0) {
+                    cp_async_wait<0>();
+                    fence_proxy_async();
+                    for (int q = 0; q < npend; ++q) mbar_arrive(full_bar(pend[q]));
+                    npend = 0;
+                }
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    bool w = true;
+                    if (lane == 0) w = mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, a.dev_err);
+                    w = __shfl_sync(0xffffffffu, w, 0);
+                    if (!w) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive(full_bar(stage));
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                continue;
+            }
+            const uint8_t* src_row[8];
             uint32_t dst_off[8];
             unsigned live = 0;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int r = gw * 32 + 4 * i + (lane >> 3);
-                dst_off[i] = static_cast<uint32_t>(r) * kRowBytes + ((chunk ^ static_cast<uint32_t>(r & 7)) << 4);
+                dst_off[i] = static_cast<uint32_t>(r) * kRowBytes +
+                             ((chunk ^ static_cast<uint32_t>(r & 7)) << 4);
                 const bool lv = r < ti.rows;
                 live |= lv ? (1u << i) : 0u;
-                src_row[i] = lv ? x_src + static_cast<size_t>(seg.rec_tok[ti.row0 + r]) * H + chunk * 8
-                                : x_src;
+                const uint8_t* row = reinterpret_cast<const uint8_t*>(a.x);
+                if (lv)
+                    row = reinterpret_cast<const uint8_t*>(
+                        a.x + static_cast<size_t>(seg.rec_tok[ti.row0 + r]) * H);
+                src_row[i] = row + chunk * 16;
             }
             for (int kb = 0; kb < num_kb; ++kb) {
                 bool w = true;
-                if (lane == 0) w = mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, dev_err);
+                if (lane == 0) w = mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, a.dev_err);
                 w = __shfl_sync(0xffffffffu, w, 0);
                 if (!w) {
                     ok = false;
@@ -431,15 +523,15 @@ __global__ void __launch_bounds__(kGateUp ? kThreadsGateUp : kThreadsDown, 1)
                 const uint32_t base = sA + stage * kTileABytes;
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
-                    if (live & (1u << i)) cp_async_16(base + dst_off[i], src_row[i] + kb * 64);
+                    if (live & (1u << i)) cp_async_16(base + dst_off[i], src_row[i] + kb * kRowBytes);
                 cp_async_commit();
                 pend[npend++] = stage;
-                if (npend > kGatherDepth) {
-                    cp_async_wait<kGatherDepth>();
+                if (npend > kLoaderDepth) {
+                    cp_async_wait<kLoaderDepth>();
                     fence_proxy_async();
                     mbar_arrive(full_bar(pend[0]));
 #pragma unroll
-                    for (int q = 0; q < kGatherDepth; ++q) pend[q] = pend[q + 1];
+                    for (int q = 0; q < kLoaderDepth; ++q) pend[q] = pend[q + 1];
                     --npend;
                 }
                 if (++stage == kStages) {
@@ -455,8 +547,8 @@ __global__ void __launch_bounds__(kGateUp ? kThreadsGateUp : kThreadsDown, 1)
     } else if (warp == 1) {
         // ------------------------------ MMA issuer ------------------------------
         if (lane == 0) {
-            // K2: bf16 x bf16; K3: fp16 x fp16
-            const uint32_t idesc = make_idesc(kGateUp, 128, 256);
+            const uint32_t idesc_gu = make_idesc(true, 128, 256);   // bf16 x bf16
+            const uint32_t idesc_dn = make_idesc(false, 128, 256);  // fp16 x fp16
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
@@ -464,14 +556,17 @@ __global__ void __launch_bounds__(kGateUp ? kThreadsGateUp : kThreadsDown, 1)
             bool ok = true;
             bool issued_any = false;
             for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-                if (!mbar_wait(acce_bar(acc), acc_phase ^ 1u, abort_flag, dev_err)) {
+                const bool gu = t < TA;
+                const int num_kb = gu ? KBA : KBB;
+                const uint32_t idesc = gu ? idesc_gu : idesc_dn;
+                if (!mbar_wait(acce_bar(acc), acc_phase ^ 1u, abort_flag, a.dev_err)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kAccCols);
                 for (int kb = 0; kb < num_kb; ++kb) {
-                    if (!mbar_wait(full_bar(stage), phase, abort_flag, dev_err)) {
+                    if (!mbar_wait(full_bar(stage), phase, abort_flag, a.dev_err)) {
                         ok = false;
                         break;
                     }
@@ -481,7 +576,7 @@ __global__ void __launch_bounds__(kGateUp ? kThreadsGateUp : kThreadsDown, 1)
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)  // 4 x 32 bytes of K per stage
                         umma_f16(d_tmem, adesc + 2u * kk, bdesc + 2u * kk, idesc,
-                                   (kb | kk) != 0 ? 1u : 0u);
+                                 (kb | kk) != 0 ? 1u : 0u);
                     issued_any = true;
                     umma_commit(empty_bar(stage));
                     if (++stage == kStages) {
@@ -501,16 +596,18 @@ __global__ void __launch_bounds__(kGateUp ? kThreadsGateUp : kThreadsDown, 1)
             }
         }
         __syncwarp();
-    } else if (warp >= 2 && warp < 6) {
-        // ------------------------------ epilogue ------------------------------
+    } else {
+        // ------------------------------ epilogue (warps 2-5) ------------------------------
         const int quarter = warp & 3;  // TMEM lanes this warp may read
         const int row = quarter * 32 + lane;
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x) {
-            const Tile ti = decode_tile(t, table, seg.seg_count, NB, seg.offsets, seg.seg_begin);
+            const bool gu = t < TA;
+            const Tile ti = decode_tile(gu ? t : t - TA, table, seg.seg_count, gu ? NBA : NBB,
+                                        seg.offsets, seg.seg_begin);
             bool w = true;
-            if (lane == 0) w = mbar_wait(accf_bar(acc), acc_phase, abort_flag, dev_err);
+            if (lane == 0) w = mbar_wait(accf_bar(acc), acc_phase, abort_flag, a.dev_err);
             w = __shfl_sync(0xffffffffu, w, 0);
             if (!w) break;
             tc_fence_after();
@@ -518,7 +615,7 @@ __global__ void __launch_bounds__(kGateUp ? kThreadsGateUp : kThreadsDown, 1)
             const int p = ti.row0 + row;
             const uint32_t tacc = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                   static_cast<uint32_t>(acc * kAccCols);
-            if constexpr (kGateUp) {
+            if (gu) {
                 bool in_range = true;
 #pragma unroll 1
                 for (int c = 0; c < 4; ++c) {
@@ -528,7 +625,7 @@ __global__ void __launch_bounds__(kGateUp ? kThreadsGateUp : kThreadsDown, 1)
                     tmem_ld_wait();
                     if (valid) {
                         const size_t col = static_cast<size_t>(ti.nb) * 128 + c * 32;
-                        __half* dst = static_cast<__half*>(h_out) + static_cast<size_t>(p) * F + col;
+                        __half* dst = a.h + static_cast<size_t>(p) * F + col;
                         uint32_t packed[16];
 #pragma unroll
                         for (int v = 0; v < 16; ++v) {
@@ -544,14 +641,21 @@ __global__ void __launch_bounds__(kGateUp ? kThreadsGateUp : kThreadsDown, 1)
                                   packed[4 * v + 3]);
                     }
                 }
-                if (!in_range) record_error(dev_err, kDevErrRange);
+                if (!in_range) record_error(a.dev_err, kDevErrRange);
+                // publish this warp's rows of the tile to the down tiles (which
+                // read h through TMA, the async proxy)
+                fence_proxy_async_global();
+                __threadfence();
+                __syncwarp();
+                if (lane == 0 && (a.phases & 2))
+                    red_release_add(a.done + seg.mblk[seg.seg_begin + ti.seg] + ti.mb, 1);
             } else {
                 int tok = 0;
-                float a = 0.0f;
+                float al = 0.0f;
                 if (valid) {
                     tok = seg.rec_tok[p];
-                    a = seg.alpha ? seg.alpha[seg.rec_route[p]] : 1.0f;
-                    a *= seg.seg_scale[seg.seg_begin + ti.seg];  // undo the W_d scale
+                    al = seg.alpha ? seg.alpha[seg.rec_route[p]] : 1.0f;
+                    al *= seg.seg_scale[seg.seg_begin + ti.seg];  // undo the W_d scale
                 }
 #pragma unroll 1
                 for (int c = 0; c < 8; ++c) {
@@ -560,22 +664,22 @@ __global__ void __launch_bounds__(kGateUp ? kThreadsGateUp : kThreadsDown, 1)
                     tmem_ld_wait();
                     if (valid) {
                         const size_t col = static_cast<size_t>(ti.nb) * 256 + c * 32;
-                        if (out_rows) {
-                            float* dst = out_rows + static_cast<size_t>(p) * H + col;
+                        if (a.out_rows) {
+                            float* dst = a.out_rows + static_cast<size_t>(p) * H + col;
 #pragma unroll
                             for (int q = 0; q < 8; ++q)
-                                st_v4(dst + 4 * q, __float_as_uint(a * __uint_as_float(v[4 * q])),
-                                      __float_as_uint(a * __uint_as_float(v[4 * q + 1])),
-                                      __float_as_uint(a * __uint_as_float(v[4 * q + 2])),
-                                      __float_as_uint(a * __uint_as_float(v[4 * q + 3])));
+                                st_v4(dst + 4 * q, __float_as_uint(al * __uint_as_float(v[4 * q])),
+                                      __float_as_uint(al * __uint_as_float(v[4 * q + 1])),
+                                      __float_as_uint(al * __uint_as_float(v[4 * q + 2])),
+                                      __float_as_uint(al * __uint_as_float(v[4 * q + 3])));
                         } else {
-                            float* dst = Y + static_cast<size_t>(tok) * H + col;
+                            float* dst = a.Y + static_cast<size_t>(tok) * H + col;
 #pragma unroll
                             for (int q = 0; q < 8; ++q)
-                                red_add_v4(dst + 4 * q, a * __uint_as_float(v[4 * q]),
-                                           a * __uint_as_float(v[4 * q + 1]),
-                                           a * __uint_as_float(v[4 * q + 2]),
-                                           a * __uint_as_float(v[4 * q + 3]));
+                                red_add_v4(dst + 4 * q, al * __uint_as_float(v[4 * q]),
+                                           al * __uint_as_float(v[4 * q + 1]),
+                                           al * __uint_as_float(v[4 * q + 2]),
+                                           al * __uint_as_float(v[4 * q + 3]));
                         }
                     }
                 }
@@ -594,26 +698,6 @@ __global__ void __launch_bounds__(kGateUp ? kThreadsGateUp : kThreadsDown, 1)
         tc_fence_after();
         tmem_dealloc(tmem_base, kTmemCols);
     }
-}
-
-template <bool kGateUp>
-cudaError_t launch_gemm(const CUtensorMap* tm_a, const CUtensorMap* tm_b0, const CUtensorMap* tm_b1,
-                        const GemmSegments& seg, const void* x_src, void* h_out, float* Y,
-                        float* out_rows, int H, int F, int* dev_err, int num_sms,
-                        cudaStream_t stream) {
-    const int NB = kGateUp ? F / 128 : H / 256;
-    const long long max_tiles = static_cast<long long>(seg.max_tiles_m) * NB;
-    if (max_tiles <= 0 || seg.seg_count <= 0) return cudaSuccess;
-    const int grid = static_cast<int>(max_tiles < num_sms ? max_tiles : num_sms);
-    const size_t smem = gemm_smem_bytes(seg.seg_count);
-    auto kern = k_expert_gemm<kGateUp>;
-    cudaError_t rc = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          static_cast<int>(smem));
-    if (rc != cudaSuccess) return rc;
-    kern<<<grid, kGateUp ? kThreadsGateUp : kThreadsDown, smem, stream>>>(
-        *tm_a, *tm_b0, *tm_b1, seg, static_cast<const __nv_bfloat16*>(x_src), h_out, Y, out_rows, H,
-        F, dev_err);
-    return cudaGetLastError();
 }
 
 // Deterministic combine: one thread per 4 columns of one token.
@@ -641,18 +725,38 @@ __global__ void k_combine(const float* __restrict__ rows, const int32_t* __restr
 
 }  // namespace
 
-cudaError_t launch_gateup(const void* X, const CUtensorMap* tm_wg, const CUtensorMap* tm_wu,
-                          const GemmSegments& seg, void* h, int H, int F, int* dev_err, int num_sms,
-                          cudaStream_t stream) {
-    return launch_gemm<true>(tm_wg, tm_wg, tm_wu, seg, X, h, nullptr, nullptr, H, F, dev_err,
-                             num_sms, stream);
-}
-
-cudaError_t launch_down(const CUtensorMap* tm_h, const CUtensorMap* tm_wd, const GemmSegments& seg,
-                        float* Y, float* out_rows, int H, int F, int* dev_err, int num_sms,
-                        cudaStream_t stream) {
-    return launch_gemm<false>(tm_h, tm_wd, tm_wd, seg, nullptr, nullptr, Y, out_rows, H, F,
-                              dev_err, num_sms, stream);
+cudaError_t launch_expert_ffn(const CUtensorMap* tm_wg, const CUtensorMap* tm_wu,
+                              const CUtensorMap* tm_wd, const CUtensorMap* tm_h,
+                              const GemmSegments& seg, const void* X,
+                              void* h, float* Y, float* out_rows, int* done, int H, int F,
+                              int phases, int* dev_err, int num_sms, cudaStream_t stream) {
+    const long long max_tiles = static_cast<long long>(seg.max_tiles_m) *
+                                (((phases & 1) ? F / 128 : 0) + ((phases & 2) ? H / 256 : 0));
+    if (max_tiles <= 0 || seg.seg_count <= 0) return cudaSuccess;
+    const int grid = static_cast<int>(max_tiles < num_sms ? max_tiles : num_sms);
+    const size_t smem = gemm_smem_bytes(seg.seg_count);
+    cudaError_t rc = cudaFuncSetAttribute(k_expert_ffn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          static_cast<int>(smem));
+    if (rc != cudaSuccess) return rc;
+    FfnArgs args;
+    args.seg = seg;
+    args.x = static_cast<const __nv_bfloat16*>(X);
+    args.h = static_cast<__half*>(h);
+    args.Y = Y;
+    args.out_rows = out_rows;
+    args.done = done;
+    args.dev_err = dev_err;
+    args.H = H;
+    args.F = F;
+    args.phases = phases;
+    void* kargs[] = {const_cast<CUtensorMap*>(tm_wg), const_cast<CUtensorMap*>(tm_wu),
+                     const_cast<CUtensorMap*>(tm_wd), const_cast<CUtensorMap*>(tm_h), &args};
+    // cooperative: every CTA is resident, so a down tile may wait for the
+    // gate/up tiles of its m-block that other CTAs own
+    rc = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(k_expert_ffn), grid, kThreads,
+                                     kargs, smem, stream);
+    if (rc != cudaSuccess) return rc;
+    return cudaGetLastError();
 }
 
 cudaError_t launch_combine(const float* rows, const int32_t* pos, int T, int k, int H,

@@ -9,15 +9,18 @@
 // contiguously by slot, in ascending i. Routes whose expert is not resident
 // (Phi = -1) are filed under a trailing bucket P.
 //
-// GPU form (three launches after one memset):
-//   k_route_topk    one warp per token: softmax top-k, alpha, and per-chunk
-//                   slot counts (global atomics; counts are order-free).
-//   k_route_scan    one CTA: per-slot chunk bases and slot offsets (exclusive
-//                   prefix sums), plus the m-block prefix the GEMMs schedule by.
-//   k_route_scatter one CTA per chunk of 1024 routes: ranks inside a warp by
-//                   __match_any_sync, across warps in ascending warp order, so
-//                   the placement is the stable one Algorithm 1 produces.
+// GPU form: one memset, then one cooperative kernel (k_route_fused) in three
+// phases separated by bounded grid barriers:
+//   1. one warp per token: softmax top-k, alpha, and per-chunk slot counts
+//      (global atomics; counts are order-free);
+//   2. CTA 0: per-slot chunk bases and slot offsets (exclusive prefix sums),
+//      plus the m-block prefix the GEMMs schedule by;
+//   3. one CTA per chunk of 1024 routes: ranks inside a warp by
+//      __match_any_sync, across warps and passes in ascending order, so the
+//      placement is the stable one Algorithm 1 produces.
 #include <cuda_bf16.h>
+
+#include <algorithm>
 
 #include "estream_internal.h"
 
@@ -64,20 +67,19 @@ __device__ __forceinline__ void record_error(int* err, int code) {
 // Selection walks the strict total order (logit descending, expert id
 // ascending): round j takes the best expert after round j-1's pick in that
 // order, found by a warp-wide (value, id) reduction.
-constexpr int kTopkWarps = 8;
 constexpr int kMaxPerLane = kMaxE / 32;
+constexpr int kRouteThreads = 512;
+constexpr uint64_t kGridWaitLimitNs = 1000000000ull;  // 1 s
 
 __device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib) {
     return va > vb || (va == vb && ia < ib);
 }
 
-__global__ void __launch_bounds__(32 * kTopkWarps) k_route_topk(
-    const float* __restrict__ logits, int T, int E, int k, int renorm,
+__device__ __forceinline__ void topk_token(
+    int t, const float* __restrict__ logits, int E, int k, int renorm,
     const int32_t* __restrict__ phi, int P, int32_t* __restrict__ topk_ids,
     float* __restrict__ alpha, int32_t* __restrict__ hist, int* __restrict__ err) {
     const int lane = threadIdx.x & 31;
-    const int t = blockIdx.x * kTopkWarps + (threadIdx.x >> 5);
-    if (t >= T) return;  // whole warps exit together
     const float* l = logits + static_cast<size_t>(t) * E;
     const int nj = (E + 31) >> 5;
     const float kNegInf = __int_as_float(0xff800000);
@@ -202,10 +204,8 @@ __device__ int block_exclusive_scan(int* data, int n, int* warp_sums) {
 // One CTA. hist[c][b] (counts) becomes the base position of chunk c's first
 // record of slot b; offsets[b] = sum of counts of slots < b; mblk[s] = sum over
 // slots < s of ceil(count/kBM) for s <= P (the trailing bucket has no GEMM work).
-__global__ void __launch_bounds__(1024) k_route_scan(int32_t* __restrict__ hist, int nchunk,
-                                                     int P, int R, int32_t* __restrict__ offsets,
-                                                     int32_t* __restrict__ mblk) {
-    extern __shared__ int smem[];
+__device__ void scan_phase(int32_t* __restrict__ hist, int nchunk, int P, int R,
+                           int32_t* __restrict__ offsets, int32_t* __restrict__ mblk, int* smem) {
     const int nb = P + 1;
     int* cnt = smem;               // [nb] counts -> slot offsets
     int* mb = smem + nb;           // [nb] m-blocks -> m-block prefix
@@ -234,51 +234,116 @@ __global__ void __launch_bounds__(1024) k_route_scan(int32_t* __restrict__ hist,
     }
 }
 
-__global__ void __launch_bounds__(kRouteChunk) k_route_scatter(
-    const int32_t* __restrict__ topk_ids, const int32_t* __restrict__ phi, int P, int k, int R,
-    const int32_t* __restrict__ base, int32_t* __restrict__ rec_tok,
-    int32_t* __restrict__ rec_route, int32_t* __restrict__ rec_pos) {
-    extern __shared__ int cnt[];  // [P+1] records placed so far in this chunk, per slot
+// Places the records of chunk c (routes [c*1024, c*1024 + 1024)) in
+// kRouteChunk / blockDim.x passes of one route per thread.
+__device__ void scatter_chunk(int c, const int32_t* __restrict__ topk_ids,
+                              const int32_t* __restrict__ phi, int P, int k, int R,
+                              const int32_t* __restrict__ base, int32_t* __restrict__ rec_tok,
+                              int32_t* __restrict__ rec_route, int32_t* __restrict__ rec_pos,
+                              int* cnt) {
     const int nb = P + 1;
     for (int b = threadIdx.x; b < nb; b += blockDim.x) cnt[b] = 0;
     __syncthreads();
-    const int c = blockIdx.x;
-    const int i = c * kRouteChunk + threadIdx.x;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const bool valid = i < R;
-    int b = P;
-    if (valid) {
-        const int e = topk_ids[i];
-        const int slot = phi ? phi[e] : e;
-        b = (slot < 0 || slot >= P) ? P : slot;
-    }
-    const int key = valid ? b : -(lane + 1);  // invalid lanes match nobody
-    const unsigned peers = __match_any_sync(0xffffffffu, key);
-    const unsigned lt_mask = (1u << lane) - 1u;
-    const int rank = __popc(peers & lt_mask);
-    const int leader = __ffs(peers) - 1;
-    int pos = 0;
     const int nwarps = blockDim.x >> 5;
-    for (int w = 0; w < nwarps; ++w) {
-        if (warp == w) {
-            const int before = valid ? cnt[b] : 0;
-            __syncwarp();
-            if (valid && lane == leader) cnt[b] = before + __popc(peers);
-            pos = base[c * nb + b] + before + rank;
+    for (int pass = 0; pass < kRouteChunk; pass += blockDim.x) {
+        const int i = c * kRouteChunk + pass + threadIdx.x;
+        const bool valid = i < R;
+        int b = P;
+        if (valid) {
+            const int e = topk_ids[i];
+            const int slot = phi ? phi[e] : e;
+            b = (slot < 0 || slot >= P) ? P : slot;
         }
-        __syncthreads();
+        const int key = valid ? b : -(lane + 1);  // invalid lanes match nobody
+        const unsigned peers = __match_any_sync(0xffffffffu, key);
+        const unsigned lt_mask = (1u << lane) - 1u;
+        const int rank = __popc(peers & lt_mask);
+        const int leader = __ffs(peers) - 1;
+        int pos = 0;
+        for (int w = 0; w < nwarps; ++w) {
+            if (warp == w) {
+                const int before = valid ? cnt[b] : 0;
+                __syncwarp();
+                if (valid && lane == leader) cnt[b] = before + __popc(peers);
+                pos = base[c * nb + b] + before + rank;
+            }
+            __syncthreads();
+        }
+        if (valid) {
+            rec_tok[pos] = i / k;
+            rec_route[pos] = i;
+            if (rec_pos) rec_pos[i] = pos;
+        }
     }
-    if (valid) {
-        rec_tok[pos] = i / k;
-        rec_route[pos] = i;
-        if (rec_pos) rec_pos[i] = pos;
+    __syncthreads();
+}
+
+// Grid-wide barrier for a cooperative launch, bounded in time: returns false
+// (after recording a timeout) if the other CTAs did not arrive within the limit.
+__device__ bool grid_barrier(int* counter, int generation, int* err, int* ok_flag) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        atomicAdd(counter, 1);
+        const int target = generation * gridDim.x;
+        uint64_t t0;
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+        int seen;
+        bool ok = true;
+        while (true) {
+            asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(seen) : "l"(counter) : "memory");
+            if (seen >= target) break;
+            uint64_t t1;
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t1));
+            if (t1 - t0 > kGridWaitLimitNs) {
+                record_error(err, kDevErrTimeout);
+                ok = false;
+                break;
+            }
+        }
+        __threadfence();
+        *ok_flag = ok ? 1 : 0;
     }
+    __syncthreads();
+    return *ok_flag != 0;
+}
+
+__global__ void __launch_bounds__(kRouteThreads) k_route_fused(
+    const float* __restrict__ logits, int T, int E, int k, int renorm,
+    const int32_t* __restrict__ phi, int P, int32_t* __restrict__ topk_ids,
+    float* __restrict__ alpha, int32_t* __restrict__ offsets, int32_t* __restrict__ rec_tok,
+    int32_t* __restrict__ rec_route, int32_t* __restrict__ rec_pos, int32_t* __restrict__ hist,
+    int32_t* __restrict__ mblk, int32_t* __restrict__ done, int* __restrict__ sync,
+    int* __restrict__ err, int nchunk) {
+    extern __shared__ int smem[];
+    __shared__ int ok_flag;
+    const int R = T * k;
+    // 1. router + per-chunk counts, one warp per token
+    const int warps = gridDim.x * (blockDim.x >> 5);
+    for (int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T; t += warps)
+        topk_token(t, logits, E, k, renorm, phi, P, topk_ids, alpha, hist, err);
+    if (!grid_barrier(sync, 1, err, &ok_flag)) return;
+    // 2. prefix sums (one CTA)
+    if (blockIdx.x == 0) scan_phase(hist, nchunk, P, R, offsets, mblk, smem);
+    if (!grid_barrier(sync, 2, err, &ok_flag)) return;
+    // 3. stable placement, one chunk of 1024 routes per CTA at a time; the
+    //    expert kernel's per-m-block counters start from zero
+    if (done) {
+        const int mb_total = mblk[P];
+        for (int m = blockIdx.x * blockDim.x + threadIdx.x; m < mb_total; m += gridDim.x * blockDim.x)
+            done[m] = 0;
+    }
+    for (int c = blockIdx.x; c < nchunk; c += gridDim.x)
+        scatter_chunk(c, topk_ids, phi, P, k, R, hist, rec_tok, rec_route, rec_pos, smem);
 }
 
 __global__ void k_identity_map(int T, int n_shared, int32_t* __restrict__ offsets,
-                               int32_t* __restrict__ rec_tok, int32_t* __restrict__ mblk) {
+                               int32_t* __restrict__ rec_tok, int32_t* __restrict__ mblk,
+                               int32_t* __restrict__ done) {
     const int p = blockIdx.x * blockDim.x + threadIdx.x;
     if (p < T * n_shared) rec_tok[p] = p % T;
+    if (done && p < n_shared * ((T + kBM - 1) / kBM)) done[p] = 0;
     if (p <= n_shared) {
         offsets[p] = p * T;
         mblk[p] = p * ((T + kBM - 1) / kBM);
@@ -298,7 +363,8 @@ RouteWorkspace route_workspace_layout(int T, int k, int P) {
     w.nchunk = static_cast<int>((R + kRouteChunk - 1) / kRouteChunk);
     size_t off = 0;
     w.err_off = off;
-    off = align_up(off + sizeof(int32_t), 256);
+    w.sync_off = off + sizeof(int32_t);
+    off = align_up(off + 2 * sizeof(int32_t), 256);
     w.hist_off = off;
     off = align_up(off + sizeof(int32_t) * static_cast<size_t>(w.nchunk > 0 ? w.nchunk : 1) * (P + 1), 256);
     w.mblk_off = off;
@@ -310,8 +376,8 @@ RouteWorkspace route_workspace_layout(int T, int k, int P) {
 cudaError_t launch_route_build(const float* logits, int T, int E, int k, int renorm,
                                const int32_t* phi, int P, int32_t* topk_ids, float* alpha,
                                int32_t* offsets, int32_t* rec_tok, int32_t* rec_route,
-                               int32_t* rec_pos, void* ws, cudaStream_t stream,
-                               int* n_launches) {
+                               int32_t* rec_pos, int32_t* done, void* ws,
+                               cudaStream_t stream, int* n_launches) {
     const RouteWorkspace w = route_workspace_layout(T, k, P);
     char* base = static_cast<char*>(ws);
     int* err = reinterpret_cast<int*>(base + w.err_off);
@@ -327,28 +393,42 @@ cudaError_t launch_route_build(const float* logits, int T, int E, int k, int ren
         if (rc == cudaSuccess) rc = cudaMemsetAsync(mblk, 0, sizeof(int32_t) * (P + 2), stream);
         return rc;
     }
-    // one memset clears the error word and the per-chunk counts (contiguous)
+    // one memset clears the error word, the barrier counter and the
+    // per-chunk counts (contiguous)
     rc = cudaMemsetAsync(base + w.err_off, 0,
                          w.hist_off - w.err_off + sizeof(int32_t) * static_cast<size_t>(w.nchunk) * nb,
                          stream);
     if (rc != cudaSuccess) return rc;
-    k_route_topk<<<(T + kTopkWarps - 1) / kTopkWarps, 32 * kTopkWarps, 0, stream>>>(
-        logits, T, E, k, renorm, phi, P, topk_ids, alpha, hist, err);
-    ++launches;
-    const size_t scan_smem = sizeof(int) * (2 * static_cast<size_t>(nb) + 33);
-    k_route_scan<<<1, 1024, scan_smem, stream>>>(hist, w.nchunk, P, R, offsets, mblk);
-    ++launches;
-    k_route_scatter<<<w.nchunk, kRouteChunk, sizeof(int) * nb, stream>>>(
-        topk_ids, phi, P, k, R, hist, rec_tok, rec_route, rec_pos);
+    int* sync = reinterpret_cast<int*>(base + w.sync_off);
+    static int co_resident = 0;  // CTAs of k_route_fused that fit on the device at once
+    if (co_resident == 0) {
+        int dev = 0, sms = 0, per_sm = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        cudaFuncSetAttribute(k_route_fused, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(sizeof(int) * (2 * (kMaxP + 1) + 33)));
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            &per_sm, k_route_fused, kRouteThreads, sizeof(int) * (2 * (kMaxP + 1) + 33));
+        co_resident = sms * (per_sm > 0 ? per_sm : 1);
+    }
+    const int want = std::max((T + kRouteThreads / 32 - 1) / (kRouteThreads / 32), w.nchunk);
+    const int grid = std::max(1, std::min(co_resident, want));
+    const size_t smem = sizeof(int) * (2 * static_cast<size_t>(nb) + 33);
+    void* args[] = {&logits, &T, &E, &k, &renorm, &phi, &P, &topk_ids, &alpha, &offsets,
+                    &rec_tok, &rec_route, &rec_pos, &hist, &mblk, &done, &sync, &err,
+                    const_cast<int*>(&w.nchunk)};
+    rc = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(k_route_fused), grid,
+                                     kRouteThreads, args, smem, stream);
+    if (rc != cudaSuccess) return rc;
     ++launches;
     if (n_launches) *n_launches += launches;
     return cudaGetLastError();
 }
 
 cudaError_t launch_identity_map(int T, int n_shared, int32_t* offsets, int32_t* rec_tok,
-                                int32_t* mblk, cudaStream_t stream) {
+                                int32_t* mblk, int32_t* done, cudaStream_t stream) {
     const int n = T * n_shared > n_shared + 1 ? T * n_shared : n_shared + 1;
-    k_identity_map<<<(n + 255) / 256, 256, 0, stream>>>(T, n_shared, offsets, rec_tok, mblk);
+    k_identity_map<<<(n + 255) / 256, 256, 0, stream>>>(T, n_shared, offsets, rec_tok, mblk, done);
     return cudaGetLastError();
 }
 

@@ -47,7 +47,7 @@ struct Bank {
     cudaEvent_t released = nullptr;
 };
 
-enum TimedKind { kTRoute = 0, kTGateUp, kTDown, kTShared, kTCombine, kTTotal, kTIo, kTKinds };
+enum TimedKind { kTRoute = 0, kTFfn, kTShared, kTCombine, kTTotal, kTIo, kTKinds };
 
 struct Timed {
     int kind;
@@ -75,6 +75,7 @@ struct estream_ctx {
             *sh_rec_tok = nullptr;
     float *alpha = nullptr, *out_rows = nullptr, *out_shared = nullptr;
     float* d_scale = nullptr;                  // [L*E] down-weight scales, storage order
+    int32_t *done = nullptr, *sh_done = nullptr;  // per-m-block counters of the fused expert kernel
     std::vector<const float*> shared_scale;    // [L] device pointers into shared buffers
     void *route_ws = nullptr, *h = nullptr, *h_shared = nullptr;
     int* dev_err = nullptr;
@@ -263,7 +264,7 @@ estream_status estream_route_build(const float* logits, int T, int E, int k, int
     if (workspace_bytes < route_workspace_layout(T, k, P).total) return ESTREAM_ERR_CAPACITY;
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
     cudaError_t rc = launch_route_build(logits, T, E, k, renorm, phi, P, topk_ids, alpha, offsets,
-                                        rec_tok, rec_route, nullptr, workspace, s, nullptr);
+                                        rec_tok, rec_route, nullptr, nullptr, workspace, s, nullptr);
     return rc == cudaSuccess ? ESTREAM_OK : ESTREAM_ERR_CUDA;
 }
 
@@ -442,10 +443,13 @@ estream_status estream_bind_arena(estream_ctx** out, const estream_arena_desc* d
     const size_t o_rpos = take(sizeof(int32_t) * R_cap);
     const size_t o_offs = take(sizeof(int32_t) * (E + 2));
     const size_t o_rws = take(route_workspace_layout(d->T_max, d->k_max, E).total);
+    const size_t o_done = take(sizeof(int32_t) * ((R_cap + kBM - 1) / kBM + E + 1));
     const size_t o_h = take(static_cast<size_t>(R_cap) * d->F * c->es);
     size_t o_sh_offs = 0, o_sh_mblk = 0, o_sh_tok = 0, o_hs = 0, o_outs = 0, o_out = 0;
     const int RS_cap = d->n_shared * d->T_max;
+    size_t o_sh_done = 0;
     if (d->n_shared > 0) {
+        o_sh_done = take(sizeof(int32_t) * (d->n_shared * ((d->T_max + kBM - 1) / kBM) + 1));
         o_sh_offs = take(sizeof(int32_t) * (d->n_shared + 2));
         o_sh_mblk = take(sizeof(int32_t) * (d->n_shared + 2));
         o_sh_tok = take(sizeof(int32_t) * RS_cap);
@@ -469,8 +473,10 @@ estream_status estream_bind_arena(estream_ctx** out, const estream_arena_desc* d
         c->rec_pos = reinterpret_cast<int32_t*>(c->ws + o_rpos);
         c->offsets = reinterpret_cast<int32_t*>(c->ws + o_offs);
         c->route_ws = c->ws + o_rws;
+        c->done = reinterpret_cast<int32_t*>(c->ws + o_done);
         c->h = c->ws + o_h;
         if (d->n_shared > 0) {
+            c->sh_done = reinterpret_cast<int32_t*>(c->ws + o_sh_done);
             c->sh_offsets = reinterpret_cast<int32_t*>(c->ws + o_sh_offs);
             c->sh_mblk = reinterpret_cast<int32_t*>(c->ws + o_sh_mblk);
             c->sh_rec_tok = reinterpret_cast<int32_t*>(c->ws + o_sh_tok);
@@ -594,9 +600,9 @@ estream_status fill_bank(estream_ctx* c, int layer, int q, int b, size_t* bytes)
 
 // K2 + K3 over segments [seg_begin, seg_begin + seg_count) of the routed
 // route map, whose experts sit in consecutive arena slots from slot_base.
-estream_status run_routed(estream_ctx* c, cudaStream_t s, const void* X,
-                          int layer, const int32_t* mblk, int seg_begin, int seg_count,
-                          int slot_base, int max_tiles_m, int max_rows, float* Y) {
+estream_status run_routed(estream_ctx* c, cudaStream_t s, const void* X, int layer,
+                          const int32_t* mblk, int seg_begin, int seg_count, int slot_base,
+                          int max_tiles_m, int max_rows, float* Y) {
     GemmSegments seg{};
     seg.offsets = c->offsets;
     seg.mblk = mblk;
@@ -608,31 +614,24 @@ estream_status run_routed(estream_ctx* c, cudaStream_t s, const void* X,
     seg.seg_count = seg_count;
     seg.slot_base = slot_base;
     seg.max_tiles_m = max_tiles_m;
-    const bool f32 = c->d.wdtype == ESTREAM_F32;
-    {
-        TimedScope ts(c, s, kTGateUp);
-        const cudaError_t rc =
-            f32 ? launch_gateup_f32(static_cast<const float*>(X),
-                                    reinterpret_cast<const float*>(c->plane_g),
-                                    reinterpret_cast<const float*>(c->plane_u), seg,
-                                    static_cast<float*>(c->h), c->d.H, c->d.F, max_rows, s)
-                : launch_gateup(X, &c->tm_wg, &c->tm_wu, seg, c->h, c->d.H, c->d.F, c->dev_err,
-                                c->num_sms, s);
-        if (rc != cudaSuccess) return ESTREAM_ERR_CUDA;
-        c->stats.n_gateup += c->timing ? 1 : 0;
+    TimedScope ts(c, s, kTFfn);
+    cudaError_t rc;
+    if (c->d.wdtype == ESTREAM_F32) {
+        rc = launch_gateup_f32(static_cast<const float*>(X), reinterpret_cast<const float*>(c->plane_g),
+                               reinterpret_cast<const float*>(c->plane_u), seg,
+                               static_cast<float*>(c->h), c->d.H, c->d.F, max_rows, s);
+        if (rc == cudaSuccess)
+            rc = launch_down_f32(static_cast<const float*>(c->h),
+                                 reinterpret_cast<const float*>(c->plane_d), seg, Y, c->out_rows,
+                                 c->d.H, c->d.F, max_rows, s);
+        c->stats.launches += 2;
+    } else {
+        rc = launch_expert_ffn(&c->tm_wg, &c->tm_wu, &c->tm_wd, &c->tm_h, seg, X, c->h, Y, c->out_rows,
+                               c->done, c->d.H, c->d.F, 3, c->dev_err, c->num_sms, s);
+        c->stats.launches += 1;
     }
-    {
-        TimedScope ts(c, s, kTDown);
-        const cudaError_t rc =
-            f32 ? launch_down_f32(static_cast<const float*>(c->h),
-                                  reinterpret_cast<const float*>(c->plane_d), seg, Y, c->out_rows,
-                                  c->d.H, c->d.F, max_rows, s)
-                : launch_down(&c->tm_h, &c->tm_wd, seg, Y, c->out_rows, c->d.H, c->d.F, c->dev_err,
-                              c->num_sms, s);
-        if (rc != cudaSuccess) return ESTREAM_ERR_CUDA;
-        c->stats.n_down += c->timing ? 1 : 0;
-    }
-    c->stats.launches += 2;
+    if (rc != cudaSuccess) return ESTREAM_ERR_CUDA;
+    c->stats.n_ffn += c->timing ? 1 : 0;
     return ESTREAM_OK;
 }
 
@@ -641,7 +640,8 @@ estream_status run_shared(estream_ctx* c, cudaStream_t s, const void* X,
                           int layer, int T, float* Y) {
     TimedScope ts(c, s, kTShared);
     const int ns = c->d.n_shared;
-    if (launch_identity_map(T, ns, c->sh_offsets, c->sh_rec_tok, c->sh_mblk, s) != cudaSuccess)
+    if (launch_identity_map(T, ns, c->sh_offsets, c->sh_rec_tok, c->sh_mblk, c->sh_done, s) !=
+        cudaSuccess)
         return ESTREAM_ERR_CUDA;
     GemmSegments seg{};
     seg.offsets = c->sh_offsets;
@@ -665,14 +665,12 @@ estream_status run_shared(estream_ctx* c, cudaStream_t s, const void* X,
             rc = launch_down_f32(static_cast<const float*>(c->h_shared), base + 2 * sp, seg, Y,
                                  c->out_shared, c->d.H, Fs, ns * T, s);
     } else {
-        rc = launch_gateup(X, &c->tm_sg[layer], &c->tm_su[layer], seg, c->h_shared, c->d.H, Fs,
-                           c->dev_err, c->num_sms, s);
-        if (rc == cudaSuccess)
-            rc = launch_down(&c->tm_hs, &c->tm_sd[layer], seg, Y, c->out_shared, c->d.H, Fs,
-                             c->dev_err, c->num_sms, s);
+        rc = launch_expert_ffn(&c->tm_sg[layer], &c->tm_su[layer], &c->tm_sd[layer], &c->tm_hs, seg, X,
+                               c->h_shared, Y, c->out_shared, c->sh_done, c->d.H, Fs, 3, c->dev_err,
+                               c->num_sms, s);
     }
     if (rc != cudaSuccess) return ESTREAM_ERR_CUDA;
-    c->stats.launches += 3;
+    c->stats.launches += c->d.wdtype == ESTREAM_F32 ? 3 : 2;
     return ESTREAM_OK;
 }
 
@@ -768,7 +766,7 @@ estream_status estream_moe_layer_prefill(estream_ctx* c, int layer, const void* 
         int launches = 0;
         if (launch_route_build(logits, T, E, k, renorm, c->d_perm + static_cast<size_t>(layer) * E, E,
                                c->topk_ids, c->alpha, c->offsets, c->rec_tok, c->rec_route,
-                               c->d.deterministic ? c->rec_pos : nullptr, c->route_ws, s,
+                               c->d.deterministic ? c->rec_pos : nullptr, c->done, c->route_ws, s,
                                &launches) != cudaSuccess) {
             drain(c, s);
             return ESTREAM_ERR_CUDA;
@@ -893,8 +891,7 @@ estream_status estream_last_stats(estream_ctx* c, estream_stats* out) {
         }
         switch (t.kind) {
             case kTRoute: c->stats.ms_route += ms; break;
-            case kTGateUp: c->stats.ms_gateup += ms; break;
-            case kTDown: c->stats.ms_down += ms; break;
+            case kTFfn: c->stats.ms_ffn += ms; break;
             case kTShared: c->stats.ms_shared += ms; break;
             case kTCombine: c->stats.ms_combine += ms; break;
             case kTTotal: c->stats.ms_total += ms; break;

@@ -47,10 +47,10 @@ class ArenaDesc(ctypes.Structure):
 class Stats(ctypes.Structure):
     _fields_ = [
         ("calls", ctypes.c_int), ("launches", ctypes.c_int),
-        ("ms_route", ctypes.c_double), ("ms_gateup", ctypes.c_double),
-        ("ms_down", ctypes.c_double), ("ms_shared", ctypes.c_double),
+        ("ms_route", ctypes.c_double), ("ms_ffn", ctypes.c_double),
+        ("ms_shared", ctypes.c_double),
         ("ms_combine", ctypes.c_double), ("ms_total", ctypes.c_double),
-        ("n_gateup", ctypes.c_int), ("n_down", ctypes.c_int),
+        ("n_ffn", ctypes.c_int),
         ("h2d_bytes", ctypes.c_double),
         ("groups_loaded", ctypes.c_int), ("groups_skipped", ctypes.c_int),
         ("groups_hit", ctypes.c_int),
