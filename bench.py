@@ -28,11 +28,11 @@ if ROOT not in sys.path:
 METRIC = "MoE-layer prefill tokens/sec and grouped-GEMM TFLOP/s vs bf16 peak (1 GB300)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
-# DRAM bytes (read + write) of one gate/up (K2) launch, from the ncu capture
-# summarised in profiles/k_expert_gemm_olmoe_resident.md. Reported only while
+# DRAM bytes (read + write) of one fused expert-kernel launch, from the ncu
+# capture summarised in profiles/k_expert_ffn_olmoe_resident.md. Reported only while
 # the kernel source is the one that was captured.
 PROFILED_TRAFFIC = {
-    "c2": {"kernel_sha256_16": "b2debf94adefc874", "bytes": 568974336},
+    "c2": {"kernel_sha256_16": "809e0b88470d9003", "bytes": 878069248},
 }
 KERNEL_SRC = os.path.join(ROOT, "routed_expert_ffn_topk_gb300", "csrc", "expert_gemm.cu")
 
