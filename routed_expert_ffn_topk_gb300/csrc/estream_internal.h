@@ -11,8 +11,6 @@
 
 namespace es {
 
-// Route-map chunk: one CTA of the scatter kernel places this many routes.
-constexpr int kRouteChunk = 1024;
 // Rows of one GEMM M tile (route records per tile).
 constexpr int kBM = 128;
 // Limits checked at the boundary.
@@ -32,7 +30,7 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 struct RouteWorkspace {
     size_t err_off;      // int32 device error word
     size_t sync_off;     // int32 grid-barrier counter of the fused route kernel
-    size_t hist_off;     // int32 [nchunk][P+1]: per-chunk counts, then per-chunk bases
+    size_t hist_off;     // int32 [P+1][nchunk]: per-chunk counts, then per-chunk bases
     size_t mblk_off;     // int32 [P+2]: exclusive prefix of ceil(count[s]/kBM), s < P
     size_t total;
     int nchunk;

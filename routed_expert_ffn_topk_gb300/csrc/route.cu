@@ -9,15 +9,18 @@
 // contiguously by slot, in ascending i. Routes whose expert is not resident
 // (Phi = -1) are filed under a trailing bucket P.
 //
-// GPU form: one memset, then one cooperative kernel (k_route_fused) in three
-// phases separated by bounded grid barriers:
-//   1. one warp per token: softmax top-k, alpha, and per-chunk slot counts
-//      (global atomics; counts are order-free);
-//   2. CTA 0: per-slot chunk bases and slot offsets (exclusive prefix sums),
-//      plus the m-block prefix the GEMMs schedule by;
-//   3. one CTA per chunk of 1024 routes: ranks inside a warp by
-//      __match_any_sync, across warps and passes in ascending order, so the
-//      placement is the stable one Algorithm 1 produces.
+// GPU form: one 8-byte memset, then one cooperative kernel (k_route_fused)
+// in three phases separated by bounded grid barriers. Routes are processed in
+// chunks of kChunkTokens tokens (16 * k routes):
+//   1. one CTA per chunk, one warp per token: softmax top-k, alpha, and the
+//      chunk's slot counts (shared-memory atomics; counts are order-free),
+//      written bucket-major as hist[slot][chunk];
+//   2. CTA 0: per slot, a warp scan over chunks gives each chunk's base inside
+//      the slot; a block scan over slot totals gives the slot offsets, and the
+//      m-block prefix the expert kernel schedules by;
+//   3. one CTA per chunk: ranks inside a warp by __match_any_sync, across
+//      warps in ascending order, so the placement is the stable one
+//      Algorithm 1 produces.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -69,6 +72,7 @@ __device__ __forceinline__ void record_error(int* err, int code) {
 // order, found by a warp-wide (value, id) reduction.
 constexpr int kMaxPerLane = kMaxE / 32;
 constexpr int kRouteThreads = 512;
+constexpr int kChunkTokens = kRouteThreads / 32;  // one token per warp
 constexpr uint64_t kGridWaitLimitNs = 1000000000ull;  // 1 s
 
 __device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib) {
@@ -78,7 +82,7 @@ __device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib)
 __device__ __forceinline__ void topk_token(
     int t, const float* __restrict__ logits, int E, int k, int renorm,
     const int32_t* __restrict__ phi, int P, int32_t* __restrict__ topk_ids,
-    float* __restrict__ alpha, int32_t* __restrict__ hist, int* __restrict__ err) {
+    float* __restrict__ alpha, int* counts, int* __restrict__ err) {
     const int lane = threadIdx.x & 31;
     const float* l = logits + static_cast<size_t>(t) * E;
     const int nj = (E + 31) >> 5;
@@ -156,7 +160,7 @@ __device__ __forceinline__ void topk_token(
             slot = -1;
         }
         const int b = slot < 0 ? P : slot;
-        atomicAdd(&hist[(i / kRouteChunk) * (P + 1) + b], 1);
+        atomicAdd(&counts[b], 1);
     }
 }
 
@@ -201,24 +205,37 @@ __device__ int block_exclusive_scan(int* data, int n, int* warp_sums) {
     return total;
 }
 
-// One CTA. hist[c][b] (counts) becomes the base position of chunk c's first
-// record of slot b; offsets[b] = sum of counts of slots < b; mblk[s] = sum over
-// slots < s of ceil(count/kBM) for s <= P (the trailing bucket has no GEMM work).
+// One CTA. hist[b][c] (counts, bucket-major) becomes the base position of
+// chunk c's first record of slot b; offsets[b] = sum of counts of slots < b;
+// mblk[s] = sum over slots < s of ceil(count/kBM) for s <= P (the trailing
+// bucket has no GEMM work). Each warp scans whole slots, 32 chunks per step.
 __device__ void scan_phase(int32_t* __restrict__ hist, int nchunk, int P, int R,
                            int32_t* __restrict__ offsets, int32_t* __restrict__ mblk, int* smem) {
     const int nb = P + 1;
-    int* cnt = smem;               // [nb] counts -> slot offsets
-    int* mb = smem + nb;           // [nb] m-blocks -> m-block prefix
+    int* cnt = smem;                 // [nb] slot totals -> slot offsets
+    int* mb = smem + nb;             // [nb] m-blocks -> m-block prefix
     int* warp_sums = smem + 2 * nb;  // [33]
-    for (int b = threadIdx.x; b < nb; b += blockDim.x) {
-        int run = 0;
-        for (int c = 0; c < nchunk; ++c) {
-            const int v = hist[c * nb + b];
-            hist[c * nb + b] = run;
-            run += v;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nwarps = blockDim.x >> 5;
+    for (int b = warp; b < nb; b += nwarps) {
+        int32_t* row = hist + static_cast<size_t>(b) * nchunk;
+        int carry = 0;
+        for (int c0 = 0; c0 < nchunk; c0 += 32) {
+            const int c = c0 + lane;
+            const int v = c < nchunk ? row[c] : 0;
+            int incl = v;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int o = __shfl_up_sync(0xffffffffu, incl, d);
+                if (lane >= d) incl += o;
+            }
+            if (c < nchunk) row[c] = carry + incl - v;  // base inside the slot
+            carry += __shfl_sync(0xffffffffu, incl, 31);
         }
-        cnt[b] = run;
-        mb[b] = (b < P) ? (run + kBM - 1) / kBM : 0;
+        if (lane == 0) {
+            cnt[b] = carry;
+            mb[b] = (b < P) ? (carry + kBM - 1) / kBM : 0;
+        }
     }
     __syncthreads();
     block_exclusive_scan(cnt, nb, warp_sums);
@@ -226,17 +243,18 @@ __device__ void scan_phase(int32_t* __restrict__ hist, int nchunk, int P, int R,
     for (int b = threadIdx.x; b < nb; b += blockDim.x) {
         offsets[b] = cnt[b];
         mblk[b] = mb[b];
-        for (int c = 0; c < nchunk; ++c) hist[c * nb + b] += cnt[b];
     }
+    __syncthreads();
+    for (int x = threadIdx.x; x < nb * nchunk; x += blockDim.x) hist[x] += cnt[x / nchunk];
     if (threadIdx.x == 0) {
         offsets[P + 1] = R;
         mblk[P + 1] = mb[P];
     }
 }
 
-// Places the records of chunk c (routes [c*1024, c*1024 + 1024)) in
-// kRouteChunk / blockDim.x passes of one route per thread.
-__device__ void scatter_chunk(int c, const int32_t* __restrict__ topk_ids,
+// Places the records of chunk c (the routes of tokens [c*kChunkTokens,
+// (c+1)*kChunkTokens)) in passes of one route per thread.
+__device__ void scatter_chunk(int c, int nchunk, const int32_t* __restrict__ topk_ids,
                               const int32_t* __restrict__ phi, int P, int k, int R,
                               const int32_t* __restrict__ base, int32_t* __restrict__ rec_tok,
                               int32_t* __restrict__ rec_route, int32_t* __restrict__ rec_pos,
@@ -246,9 +264,11 @@ __device__ void scatter_chunk(int c, const int32_t* __restrict__ topk_ids,
     __syncthreads();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int nwarps = blockDim.x >> 5;
-    for (int pass = 0; pass < kRouteChunk; pass += blockDim.x) {
-        const int i = c * kRouteChunk + pass + threadIdx.x;
-        const bool valid = i < R;
+    const int r0 = c * kChunkTokens * k;
+    const int r1 = min(R, r0 + kChunkTokens * k);
+    for (int pass = r0; pass < r1; pass += blockDim.x) {
+        const int i = pass + threadIdx.x;
+        const bool valid = i < r1;
         int b = P;
         if (valid) {
             const int e = topk_ids[i];
@@ -261,12 +281,13 @@ __device__ void scatter_chunk(int c, const int32_t* __restrict__ topk_ids,
         const int rank = __popc(peers & lt_mask);
         const int leader = __ffs(peers) - 1;
         int pos = 0;
-        for (int w = 0; w < nwarps; ++w) {
+        const int active_warps = min(nwarps, (r1 - pass + 31) >> 5);
+        for (int w = 0; w < active_warps; ++w) {
             if (warp == w) {
                 const int before = valid ? cnt[b] : 0;
                 __syncwarp();
                 if (valid && lane == leader) cnt[b] = before + __popc(peers);
-                pos = base[c * nb + b] + before + rank;
+                pos = base[static_cast<size_t>(b) * nchunk + c] + before + rank;
             }
             __syncthreads();
         }
@@ -319,23 +340,31 @@ __global__ void __launch_bounds__(kRouteThreads) k_route_fused(
     extern __shared__ int smem[];
     __shared__ int ok_flag;
     const int R = T * k;
-    // 1. router + per-chunk counts, one warp per token
-    const int warps = gridDim.x * (blockDim.x >> 5);
-    for (int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T; t += warps)
-        topk_token(t, logits, E, k, renorm, phi, P, topk_ids, alpha, hist, err);
+    const int nb = P + 1;
+    // 1. router + the chunk's slot counts, one warp per token
+    for (int c = blockIdx.x; c < nchunk; c += gridDim.x) {
+        for (int b = threadIdx.x; b < nb; b += blockDim.x) smem[b] = 0;
+        __syncthreads();
+        const int t = c * kChunkTokens + (threadIdx.x >> 5);
+        if (t < T) topk_token(t, logits, E, k, renorm, phi, P, topk_ids, alpha, smem, err);
+        __syncthreads();
+        for (int b = threadIdx.x; b < nb; b += blockDim.x)
+            hist[static_cast<size_t>(b) * nchunk + c] = smem[b];
+        __syncthreads();
+    }
     if (!grid_barrier(sync, 1, err, &ok_flag)) return;
     // 2. prefix sums (one CTA)
     if (blockIdx.x == 0) scan_phase(hist, nchunk, P, R, offsets, mblk, smem);
     if (!grid_barrier(sync, 2, err, &ok_flag)) return;
-    // 3. stable placement, one chunk of 1024 routes per CTA at a time; the
-    //    expert kernel's per-m-block counters start from zero
+    // 3. stable placement, one chunk per CTA at a time; the expert kernel's
+    //    per-m-block counters start from zero
     if (done) {
         const int mb_total = mblk[P];
         for (int m = blockIdx.x * blockDim.x + threadIdx.x; m < mb_total; m += gridDim.x * blockDim.x)
             done[m] = 0;
     }
     for (int c = blockIdx.x; c < nchunk; c += gridDim.x)
-        scatter_chunk(c, topk_ids, phi, P, k, R, hist, rec_tok, rec_route, rec_pos, smem);
+        scatter_chunk(c, nchunk, topk_ids, phi, P, k, R, hist, rec_tok, rec_route, rec_pos, smem);
 }
 
 __global__ void k_identity_map(int T, int n_shared, int32_t* __restrict__ offsets,
@@ -359,8 +388,8 @@ __global__ void k_cast_f32_bf16(const float* __restrict__ src, __nv_bfloat16* __
 
 RouteWorkspace route_workspace_layout(int T, int k, int P) {
     RouteWorkspace w;
-    const size_t R = static_cast<size_t>(T) * k;
-    w.nchunk = static_cast<int>((R + kRouteChunk - 1) / kRouteChunk);
+    (void)k;
+    w.nchunk = (T + kChunkTokens - 1) / kChunkTokens;
     size_t off = 0;
     w.err_off = off;
     w.sync_off = off + sizeof(int32_t);
@@ -393,11 +422,9 @@ cudaError_t launch_route_build(const float* logits, int T, int E, int k, int ren
         if (rc == cudaSuccess) rc = cudaMemsetAsync(mblk, 0, sizeof(int32_t) * (P + 2), stream);
         return rc;
     }
-    // one memset clears the error word, the barrier counter and the
-    // per-chunk counts (contiguous)
-    rc = cudaMemsetAsync(base + w.err_off, 0,
-                         w.hist_off - w.err_off + sizeof(int32_t) * static_cast<size_t>(w.nchunk) * nb,
-                         stream);
+    // clear the error word and the grid-barrier counter (the kernel writes
+    // every per-chunk count itself)
+    rc = cudaMemsetAsync(base + w.err_off, 0, 2 * sizeof(int32_t), stream);
     if (rc != cudaSuccess) return rc;
     int* sync = reinterpret_cast<int*>(base + w.sync_off);
     static int co_resident = 0;  // CTAs of k_route_fused that fit on the device at once
@@ -411,8 +438,7 @@ cudaError_t launch_route_build(const float* logits, int T, int E, int k, int ren
             &per_sm, k_route_fused, kRouteThreads, sizeof(int) * (2 * (kMaxP + 1) + 33));
         co_resident = sms * (per_sm > 0 ? per_sm : 1);
     }
-    const int want = std::max((T + kRouteThreads / 32 - 1) / (kRouteThreads / 32), w.nchunk);
-    const int grid = std::max(1, std::min(co_resident, want));
+    const int grid = std::max(1, std::min(co_resident, w.nchunk));
     const size_t smem = sizeof(int) * (2 * static_cast<size_t>(nb) + 33);
     void* args[] = {&logits, &T, &E, &k, &renorm, &phi, &P, &topk_ids, &alpha, &offsets,
                     &rec_tok, &rec_route, &rec_pos, &hist, &mblk, &done, &sync, &err,
