@@ -376,6 +376,8 @@ def run_ours(args, rank, world, local_rank):
 
     # ---- arena-paged run of the same config (host-link bound) ----
     paged = measure_paged(args, cfg, wl, dev, stream, flush, peaks) if not args.no_paged else None
+    if paged is not None and args.pipeline_study and cfg.layers == 1:
+        paged["pipeline_study"] = pipeline_study(cfg, wl, dev, flush)
 
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
@@ -429,9 +431,16 @@ def measure_paged(args, cfg, wl, dev, stream, flush, peaks):
             b.synchronize()
             times.append(a.elapsed_time(b))
     stats = es.last_stats(st.ctx)
+    adsf, t_ne = es.pipeline_trace(st.ctx)       # the last call's groups
     es.set_timing(st.ctx, False)
     st.close()
     t_paged = sum(times) / len(times)
+    model = None
+    if len(adsf):
+        L_k, X_k = adsf[:, 1] - adsf[:, 0], adsf[:, 3] - adsf[:, 2]
+        t_model, _ = es.maxplus_pipeline(L_k, X_k, 1, cfg.B, t_ne)
+        model = {"eq5_predicted_ms": round(t_model, 4), "measured_ms": round(float(adsf[-1, 3]), 4),
+                 "groups": int(len(adsf)), "q": 1, "b": cfg.B, "T_ne_ms": round(t_ne, 4)}
     bytes_per_call = stats["h2d_bytes"] / len(times)
 
     # the same bytes, copy only (host link alone), and the link's own peak
@@ -472,10 +481,84 @@ def measure_paged(args, cfg, wl, dev, stream, flush, peaks):
         "frac_h2d_peak": round(h2d_gbs / h2d_peak, 4),
         "t_io_alone_ms": round(t_io, 4), "t_exec_ms": round(t_exec, 4),
         "hidden_fraction": round((t_io + t_exec - t_paged) / t_io, 4) if t_io > 0 else None,
+        "compute_hidden_fraction": round((t_io + t_exec - t_paged) / t_exec, 4) if t_exec > 0 else None,
         "bubble_rate": round(1 - max(t_io, t_exec) / t_paged, 4),
         "groups_loaded_per_layer": stats["groups_loaded"] / len(times),
         "groups_skipped_per_layer": stats["groups_skipped"] / len(times),
+        "max_plus_model": model,
     }
+
+
+def pipeline_study(cfg, wl, dev, flush, reps=5):
+    """Section 3.4 on this GPU: the three loading schedules of Fig. 6
+    (on-demand = one bank, after routing, prefetch before routing) with their
+    bubble rates, and the auto-configurator of Eqs. 8-10 profiled with one
+    call per candidate group size and checked against a measured sweep of
+    (G, B) under the same memory budget (the Fig. 10 analogue)."""
+    import torch
+
+    from routed_expert_ffn_topk_gb300 import estream as es
+    from routed_expert_ffn_topk_gb300.layer import BoundLayerStack
+    stream = torch.cuda.current_stream()
+    X = wl.X.to(dev)
+    lg = wl.logits[0].to(dev)
+    Y = torch.zeros(cfg.T, cfg.H, dtype=torch.float32, device=dev)
+    W_e = cfg.expert_bytes()
+
+    def timed(st, n):
+        ms, last = [], None
+        for _ in range(n):
+            flush.zero_()
+            es.arena_invalidate(st.ctx)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            st.prefill(0, X, lg, Y)
+            b.record(stream)
+            b.synchronize()
+            ms.append(a.elapsed_time(b))
+        return sorted(ms)[len(ms) // 2]
+
+    def profile(G, B, sched=es.SCHED_AFTER_ROUTING):
+        st = BoundLayerStack(wl, mode="paged", G=G, B=B, schedule=sched)
+        try:
+            timed(st, 2)
+            es.set_timing(st.ctx, True)
+            t = timed(st, reps)
+            adsf, t_ne = es.pipeline_trace(st.ctx)
+            es.set_timing(st.ctx, False)
+        finally:
+            st.close()
+        return t, adsf, t_ne
+
+    out = {"schedules": {}, "autoconfig": {}}
+    t_io = None
+    for name, B, sched in (("on_demand", 1, es.SCHED_AFTER_ROUTING),
+                           ("after_routing", cfg.B, es.SCHED_AFTER_ROUTING),
+                           ("prefetch_before_routing", cfg.B, es.SCHED_PREFETCH)):
+        t, adsf, t_ne = profile(cfg.G, B, sched)
+        io = float((adsf[:, 1] - adsf[:, 0]).sum()) if len(adsf) else 0.0
+        ex = float((adsf[:, 3] - adsf[:, 2]).sum()) if len(adsf) else 0.0
+        out["schedules"][name] = {"G": cfg.G, "B": B, "ms": round(t, 4),
+                                  "bubble_rate": round(1 - max(io, ex) / t, 4)}
+    budget = cfg.P * W_e                      # the config's arena budget
+    profiles, measured = {}, {}
+    for g in (1, 2, 4, 8, 16):
+        if g > cfg.E:
+            continue
+        t, adsf, t_ne = profile(g, 2 if budget >= 2 * g * W_e else 1)
+        profiles[g] = (adsf[:, 1] - adsf[:, 0], adsf[:, 3] - adsf[:, 2])
+        bmax = es.bank_bound(g, budget, 0.0, W_e, cfg.E)
+        for b in range(1, min(bmax, 4) + 1):
+            tm, _, _ = profile(g, b)
+            measured[(g, b)] = tm
+    G, B, T = es.autoconfig(profiles, t_ne, 1, budget, W_e, cfg.E)
+    best = min(measured, key=measured.get)
+    out["autoconfig"] = {"budget_bytes": budget, "chosen": [G, B], "predicted_ms": round(T, 4),
+                         "chosen_measured_ms": round(measured.get((G, B), float("nan")), 4),
+                         "sweep_best": list(best), "sweep_best_ms": round(measured[best], 4),
+                         "regret": round(measured.get((G, B), float("nan")) / measured[best] - 1, 4),
+                         "sweep": {f"G{g}_B{b}": round(v, 4) for (g, b), v in sorted(measured.items())}}
+    return out
 
 
 # --------------------------------------------------------------------------
@@ -527,6 +610,8 @@ def main(argv=None):
     ap.add_argument("--paged-steps", type=int, default=10)
     ap.add_argument("--no-paged", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--pipeline-study", action="store_true",
+                    help="also measure the loading schedules and the (G, B) auto-configuration")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -145,7 +145,7 @@ typedef struct {
     int L;                  /* sparse layers whose experts stream through this arena */
     int E, H, F;            /* routed experts per layer, hidden size, expert FFN size */
     int G, B;               /* experts per storage group (= slots per bank), banks; P = B*G */
-    int Q;                  /* copies kept in flight on the copy stream per bank fill (>= 1) */
+    int Q;                  /* reads in flight: Q copy streams, group fill k on stream k mod Q (>= 1) */
     estream_dtype wdtype;   /* type of X and of every weight: bf16 (tensor cores) or fp32 */
     void* arena_dev;        /* device, >= estream_arena_bytes(...) bytes, 1024-byte aligned */
     size_t arena_bytes;
@@ -279,6 +279,51 @@ estream_status estream_get_device_error(estream_ctx* c);
  * *n (states: 0 Available, 1 Filling, 2 Ready, 3 InUse). Tracing is kept for
  * the last call only. */
 estream_status estream_residency_trace(estream_ctx* c, int32_t* out, int cap, int* n);
+
+/* Per-group pipeline trace of the last paged layer call made with timing on
+ * (estream_set_timing): for each group filled by that call, in order, the
+ * times in ms since the call began at which its read started (a) and ended
+ * (d) on its copy stream and its execution started (s) and ended (f) on the
+ * compute stream -- the quantities of EStream section 3.4, Eq. 5 (a group
+ * filled before routing and then found empty has s = f, no execution). adsf:
+ * host [cap][4]; *n receives the number of groups; *t_ne (optional) the time
+ * routing finished. Synchronises on the recorded events. */
+estream_status estream_pipeline_trace(estream_ctx* c, double* adsf, int cap, int* n,
+                                      double* t_ne);
+
+/* ---------------------------------------------------------------------- */
+/* Pipeline model and automatic configuration (host only)                 */
+/* ---------------------------------------------------------------------- */
+
+/*
+ * Max-plus recurrence of EStream section 3.4, Eq. 5, over K groups:
+ *   a_k = max(d_{k-q}, f_{k-b}), d_k = a_k + L_k,
+ *   s_k = max(d_k, T_ne, f_{k-1}), f_k = s_k + X_k, with d_j = f_j = 0 for j <= 0.
+ * L, X: host [K] read and execution times; q >= 1 reads in flight; b >= 1
+ * banks. Returns T_pipe = f_K (T_ne when K = 0; -1 on bad arguments) and,
+ * if adsf is not NULL, writes (a_k, d_k, s_k, f_k) to adsf[4(k-1) .. +3].
+ */
+double estream_maxplus_pipeline(const double* L, const double* X, int K, int q, int b,
+                                double T_ne, double* adsf);
+
+/* Eq. 8: largest feasible bank count for group size g under a memory budget:
+ * min(floor((M_max - M_other) / (g * W_e)), ceil(N_e / g)); 0 if none. */
+int estream_bank_bound(int g, double M_max, double M_other, double W_e, int N_e);
+
+/*
+ * Eqs. 9-10: for each candidate group size g_values[i] (with its calibrated
+ * per-group read times L_per_g[i][0..K_per_g[i]) and execution times
+ * X_per_g[i][...] from one profiled call, e.g. estream_pipeline_trace),
+ * choose B*(g) = argmin over Q0 <= b <= B_max(g) of T_pipe, then G* =
+ * argmin over feasible g of T_pipe(g, Q0, B*(g)). Ties keep the smaller b
+ * and the earlier g. M_other_per_g may be NULL (0). Writes *G_out, *B_out
+ * and (if not NULL) the predicted *T_out; ESTREAM_ERR_CAPACITY if no g is
+ * feasible (B_max(g) < Q0 for all).
+ */
+estream_status estream_autoconfig(int n_g, const int* g_values, const int* K_per_g,
+                                  const double* const* L_per_g, const double* const* X_per_g,
+                                  double T_ne, int Q0, double M_max, const double* M_other_per_g,
+                                  double W_e, int N_e, int* G_out, int* B_out, double* T_out);
 
 /* Host-side fault injection for tests: the pager refuses to fill group
  * `group` of `layer` (before any copy is issued) and the call returns

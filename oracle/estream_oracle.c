@@ -309,3 +309,47 @@ int oracle_num_threads(void)
     return 1;
 #endif
 }
+
+/* ------------------------------------------------------------------------ */
+/* Pipeline model                                                            */
+/* ------------------------------------------------------------------------ */
+
+/* Max-plus recurrence of the UFS-NPU pipeline (section 3.4, Eq. 5), for K
+ * scheduled groups with read times L[k] and execution times X[k]
+ * (k = 1..K stored at index k-1), queue depth q, bank count b and
+ * non-expert completion T_ne:
+ *   a_k = max(d_{k-q}, f_{k-b})      (a read waits for a queue slot and a free bank)
+ *   d_k = a_k + L_k
+ *   s_k = max(d_k, T_ne, f_{k-1})    (execution waits for its data, the
+ *                                     non-expert work and the previous group)
+ *   f_k = s_k + X_k
+ * with d_j = f_j = 0 for j <= 0. Writes (a, d, s, f) per group into adsf if
+ * not NULL and returns T_pipe = f_K. */
+double oracle_maxplus(const double* L, const double* X, int K, int q, int b, double T_ne,
+                      double* adsf)
+{
+    if (K <= 0) return T_ne > 0.0 ? T_ne : 0.0;
+    double* d = (double*)calloc((size_t)K + 1, sizeof(double));
+    double* f = (double*)calloc((size_t)K + 1, sizeof(double));
+    if (!d || !f) { free(d); free(f); return -1.0; }
+    for (int k = 1; k <= K; ++k) {
+        double dq = (k - q >= 1) ? d[k - q] : 0.0;
+        double fb = (k - b >= 1) ? f[k - b] : 0.0;
+        double a = dq > fb ? dq : fb;
+        d[k] = a + L[k - 1];
+        double s = d[k];
+        if (T_ne > s) s = T_ne;
+        if (f[k - 1] > s) s = f[k - 1];   /* f[0] = 0 */
+        f[k] = s + X[k - 1];
+        if (adsf) {
+            adsf[4 * (k - 1) + 0] = a;
+            adsf[4 * (k - 1) + 1] = d[k];
+            adsf[4 * (k - 1) + 2] = s;
+            adsf[4 * (k - 1) + 3] = f[k];
+        }
+    }
+    double out = f[K];
+    free(d);
+    free(f);
+    return out;
+}

@@ -64,6 +64,8 @@ def _declare(lib) -> None:
     lib.oracle_moe_layer_rows.restype = i
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = i
+    lib.oracle_maxplus.argtypes = [P, P, i, i, i, ctypes.c_double, P]
+    lib.oracle_maxplus.restype = ctypes.c_double
 
 
 def load(path: str | None = None):
@@ -196,6 +198,17 @@ def moe_layer_rows(X, Wg, Wu, Wd, topk_ids, alpha, rows=None, shared=None,
     if rc != 0:
         raise ValueError("oracle_moe_layer_rows: bad arguments")
     return Y
+
+
+def maxplus(L, X, q: int, b: int, T_ne: float = 0.0, lib=None):
+    """Section 3.4, Eq. 5: (T_pipe, per-group (a, d, s, f))."""
+    lib = lib or load()
+    L = np.ascontiguousarray(L, dtype=np.float64)
+    X = np.ascontiguousarray(X, dtype=np.float64)
+    K = len(L)
+    out = np.zeros((max(K, 1), 4), dtype=np.float64)
+    t = lib.oracle_maxplus(_ptr(L), _ptr(X), K, q, b, float(T_ne), _ptr(out))
+    return t, out[:K]
 
 
 def num_threads(lib=None) -> int:

@@ -18,7 +18,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OBJ_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libestream.so")
-SOURCES = ["route.cu", "route_static.cu", "expert_gemm.cu", "expert_f32.cu", "runtime.cu"]
+SOURCES = ["route.cu", "route_static.cu", "expert_gemm.cu", "expert_f32.cu", "runtime.cu",
+           "pipeline_model.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

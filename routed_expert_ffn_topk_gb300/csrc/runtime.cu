@@ -81,7 +81,8 @@ struct estream_ctx {
     int* dev_err = nullptr;
     int32_t* h_offsets = nullptr;  // pinned host copy of offsets
 
-    cudaStream_t copy_stream = nullptr;
+    cudaStream_t copy_stream = nullptr;        // copy_streams[0]
+    std::vector<cudaStream_t> copy_streams;    // Q streams: group k is read on stream k mod Q
     cudaEvent_t copy_done = nullptr, preload_done = nullptr;
     bool preload_pending = false;
     std::vector<Bank> banks;
@@ -91,6 +92,10 @@ struct estream_ctx {
     std::vector<Timed> timed;
     std::vector<cudaEvent_t> event_pool;
     std::vector<int32_t> trace;
+    // per-group pipeline events of the last timed paged call (Eq. 5 a/d/s/f)
+    struct GroupEvents { cudaEvent_t a, d, s, f; };
+    std::vector<GroupEvents> pipe;
+    cudaEvent_t pipe_t0 = nullptr, pipe_tne = nullptr;
     int fault_layer = -1, fault_group = -1;
 };
 
@@ -497,7 +502,12 @@ estream_status estream_bind_arena(estream_ctx** out, const estream_arena_desc* d
                                sizeof(float) * E, cudaMemcpyHostToDevice) == cudaSuccess;
         if (!sc_ok) break;
         if (cudaMallocHost(&c->h_offsets, sizeof(int32_t) * (E + 2)) != cudaSuccess) break;
-        if (cudaStreamCreateWithFlags(&c->copy_stream, cudaStreamNonBlocking) != cudaSuccess) break;
+        bool cs_ok = true;
+        c->copy_streams.resize(d->Q, nullptr);
+        for (int q = 0; q < d->Q && cs_ok; ++q)
+            cs_ok = cudaStreamCreateWithFlags(&c->copy_streams[q], cudaStreamNonBlocking) == cudaSuccess;
+        if (!cs_ok) break;
+        c->copy_stream = c->copy_streams[0];
         if (cudaEventCreateWithFlags(&c->copy_done, cudaEventDisableTiming) != cudaSuccess) break;
         if (cudaEventCreateWithFlags(&c->preload_done, cudaEventDisableTiming) != cudaSuccess) break;
         c->banks.resize(d->B);
@@ -567,7 +577,8 @@ estream_status estream_bind_arena(estream_ctx** out, const estream_arena_desc* d
 namespace {
 
 // Copies of storage group q of `layer` into bank b: three plane slices.
-estream_status fill_bank(estream_ctx* c, int layer, int q, int b, size_t* bytes) {
+estream_status fill_bank(estream_ctx* c, int layer, int q, int b, size_t* bytes,
+                         cudaStream_t cs, estream_ctx::GroupEvents* ev = nullptr) {
     const int G = c->d.G;
     const int n_q = std::min(G, c->d.E - q * G);
     const char* src = static_cast<const char*>(c->host_pool[layer]) +
@@ -576,23 +587,25 @@ estream_status fill_bank(estream_ctx* c, int layer, int q, int b, size_t* bytes)
     const size_t dbytes = static_cast<size_t>(n_q) * c->S_d;
     Bank& bk = c->banks[b];
     if (bk.release_pending) {
-        if (cudaStreamWaitEvent(c->copy_stream, bk.released, 0) != cudaSuccess) return ESTREAM_ERR_CUDA;
+        if (cudaStreamWaitEvent(cs, bk.released, 0) != cudaSuccess) return ESTREAM_ERR_CUDA;
         bk.release_pending = false;
     }
+    if (ev) cudaEventRecord(ev->a, cs);
     trace_state(c, b, layer, q, kFilling);
     bk.layer = layer;
     bk.group = q;
-    TimedScope io(c, c->copy_stream, kTIo);
+    TimedScope io(c, cs, kTIo);
     const size_t slot0 = static_cast<size_t>(b) * G;
-    if (cudaMemcpyAsync(c->plane_g + slot0 * c->S_gu, src, gbytes, cudaMemcpyHostToDevice,
-                        c->copy_stream) != cudaSuccess ||
+    if (cudaMemcpyAsync(c->plane_g + slot0 * c->S_gu, src, gbytes, cudaMemcpyHostToDevice, cs) !=
+            cudaSuccess ||
         cudaMemcpyAsync(c->plane_u + slot0 * c->S_gu, src + gbytes, gbytes, cudaMemcpyHostToDevice,
-                        c->copy_stream) != cudaSuccess ||
+                        cs) != cudaSuccess ||
         cudaMemcpyAsync(c->plane_d + slot0 * c->S_d, src + 2 * gbytes, dbytes,
-                        cudaMemcpyHostToDevice, c->copy_stream) != cudaSuccess)
+                        cudaMemcpyHostToDevice, cs) != cudaSuccess)
         return ESTREAM_ERR_CUDA;
     io.end();
-    if (cudaEventRecord(bk.ready, c->copy_stream) != cudaSuccess) return ESTREAM_ERR_CUDA;
+    if (ev) cudaEventRecord(ev->d, cs);
+    if (cudaEventRecord(bk.ready, cs) != cudaSuccess) return ESTREAM_ERR_CUDA;
     trace_state(c, b, layer, q, kReady);
     *bytes += 2 * gbytes + dbytes;
     return ESTREAM_OK;
@@ -682,8 +695,46 @@ bool layer_resident(const estream_ctx* c, int layer) {
 }
 
 void drain(estream_ctx* c, cudaStream_t s) {
-    cudaStreamSynchronize(c->copy_stream);
+    for (cudaStream_t cs : c->copy_streams) cudaStreamSynchronize(cs);
     cudaStreamSynchronize(s);
+}
+
+estream_status sync_copies(estream_ctx* c) {
+    for (cudaStream_t cs : c->copy_streams)
+        if (cudaStreamSynchronize(cs) != cudaSuccess) return ESTREAM_ERR_CUDA;
+    return ESTREAM_OK;
+}
+
+// The copy streams wait for all work enqueued so far on `s` (a bank may only
+// be overwritten once earlier work on `s` no longer reads it).
+estream_status copies_after(estream_ctx* c, cudaStream_t s) {
+    if (cudaEventRecord(c->copy_done, s) != cudaSuccess) return ESTREAM_ERR_CUDA;
+    for (cudaStream_t cs : c->copy_streams)
+        if (cudaStreamWaitEvent(cs, c->copy_done, 0) != cudaSuccess) return ESTREAM_ERR_CUDA;
+    return ESTREAM_OK;
+}
+
+// `s` waits for everything enqueued so far on the copy streams.
+estream_status stream_after_copies(estream_ctx* c, cudaStream_t s) {
+    for (cudaStream_t cs : c->copy_streams) {
+        if (cudaEventRecord(c->copy_done, cs) != cudaSuccess ||
+            cudaStreamWaitEvent(s, c->copy_done, 0) != cudaSuccess)
+            return ESTREAM_ERR_CUDA;
+    }
+    return ESTREAM_OK;
+}
+
+void release_pipe_events(estream_ctx* c) {
+    for (auto& g : c->pipe) {
+        c->event_pool.push_back(g.a);
+        c->event_pool.push_back(g.d);
+        c->event_pool.push_back(g.s);
+        c->event_pool.push_back(g.f);
+    }
+    c->pipe.clear();
+    if (c->pipe_t0) c->event_pool.push_back(c->pipe_t0);
+    if (c->pipe_tne) c->event_pool.push_back(c->pipe_tne);
+    c->pipe_t0 = c->pipe_tne = nullptr;
 }
 
 }  // namespace
@@ -696,17 +747,22 @@ estream_status estream_arena_preload(estream_ctx* c, int layer, void* cuda_strea
     if (c->n_groups > c->d.B) return ESTREAM_ERR_CAPACITY;
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
     c->trace.clear();
-    // the copy stream must not overwrite banks that earlier work on `s` reads
-    if (cudaEventRecord(c->copy_done, s) != cudaSuccess ||
-        cudaStreamWaitEvent(c->copy_stream, c->copy_done, 0) != cudaSuccess)
-        return ESTREAM_ERR_CUDA;
+    // the copies must not overwrite banks that earlier work on `s` reads
+    estream_status st0 = copies_after(c, s);
+    if (st0 != ESTREAM_OK) return st0;
     size_t bytes = 0;
     for (int q = 0; q < c->n_groups; ++q) {
-        estream_status st = fill_bank(c, layer, q, q, &bytes);
+        estream_status st = fill_bank(c, layer, q, q, &bytes, c->copy_streams[q % c->d.Q]);
         if (st != ESTREAM_OK) return st;
     }
     c->stats.h2d_bytes += static_cast<double>(bytes);
     c->stats.groups_loaded += c->n_groups;
+    // preload_done covers every copy stream
+    for (cudaStream_t cs : c->copy_streams) {
+        if (cudaEventRecord(c->copy_done, cs) != cudaSuccess ||
+            cudaStreamWaitEvent(c->copy_stream, c->copy_done, 0) != cudaSuccess)
+            return ESTREAM_ERR_CUDA;
+    }
     if (cudaEventRecord(c->preload_done, c->copy_stream) != cudaSuccess) return ESTREAM_ERR_CUDA;
     c->preload_pending = true;
     return ESTREAM_OK;
@@ -714,7 +770,7 @@ estream_status estream_arena_preload(estream_ctx* c, int layer, void* cuda_strea
 
 estream_status estream_arena_invalidate(estream_ctx* c) {
     if (!c) return ESTREAM_ERR_NOT_BOUND;
-    if (cudaStreamSynchronize(c->copy_stream) != cudaSuccess) return ESTREAM_ERR_CUDA;
+    if (sync_copies(c) != ESTREAM_OK) return ESTREAM_ERR_CUDA;
     for (auto& b : c->banks) {
         b.layer = -1;
         b.group = -1;
@@ -735,6 +791,23 @@ estream_status estream_moe_layer_prefill(estream_ctx* c, int layer, const void* 
     c->trace.clear();
     c->stats.calls += 1;
     TimedScope total(c, s, kTTotal);
+    release_pipe_events(c);
+    const bool trace_pipe = c->timing;
+    if (trace_pipe) {
+        c->pipe_t0 = pool_event(c);
+        if (c->pipe_t0) cudaEventRecord(c->pipe_t0, s);
+    }
+    std::vector<int> ev_of(c->n_groups, -1);  // group -> index into c->pipe (timing on)
+    auto new_group_events = [&](int q) -> int {
+        if (!trace_pipe) return -1;
+        c->pipe.push_back({pool_event(c), pool_event(c), pool_event(c), pool_event(c)});
+        ev_of[q] = static_cast<int>(c->pipe.size()) - 1;
+        return ev_of[q];
+    };
+    auto events_of = [&](int q) -> estream_ctx::GroupEvents* {
+        return ev_of[q] >= 0 ? &c->pipe[ev_of[q]] : nullptr;
+    };
+    int n_fills = 0;  // bank fills issued by this call: fill k uses copy stream k mod Q
 
     if (c->preload_pending) {
         if (cudaStreamWaitEvent(s, c->preload_done, 0) != cudaSuccess) return ESTREAM_ERR_CUDA;
@@ -754,7 +827,9 @@ estream_status estream_moe_layer_prefill(estream_ctx* c, int layer, const void* 
             if (layer == c->fault_layer && q == c->fault_group) break;  // handled below
             const int b = free_banks.front();
             free_banks.pop_front();
-            estream_status st = fill_bank(c, layer, q, b, &bytes);
+            new_group_events(q);
+            estream_status st = fill_bank(c, layer, q, b, &bytes,
+                                          c->copy_streams[n_fills++ % c->d.Q], events_of(q));
             if (st != ESTREAM_OK) { drain(c, s); return st; }
             prefetched[q] = b;
         }
@@ -772,6 +847,10 @@ estream_status estream_moe_layer_prefill(estream_ctx* c, int layer, const void* 
             return ESTREAM_ERR_CUDA;
         }
         c->stats.launches += launches;
+    }
+    if (trace_pipe) {
+        c->pipe_tne = pool_event(c);
+        if (c->pipe_tne) cudaEventRecord(c->pipe_tne, s);
     }
     const int32_t* mblk = reinterpret_cast<const int32_t*>(
         static_cast<char*>(c->route_ws) + route_workspace_layout(T, k, E).mblk_off);
@@ -811,6 +890,10 @@ estream_status estream_moe_layer_prefill(estream_ctx* c, int layer, const void* 
                 if (b >= 0) {  // a Ready bank with no routed work is released directly
                     trace_state(c, b, layer, q, kAvailable);
                     free_banks.push_front(b);
+                    if (auto* ev = events_of(q)) {  // retired: no execution
+                        cudaEventRecord(ev->s, s);
+                        cudaEventRecord(ev->f, s);
+                    }
                 }
                 continue;
             }
@@ -821,26 +904,29 @@ estream_status estream_moe_layer_prefill(estream_ctx* c, int layer, const void* 
                 }
                 b = free_banks.front();
                 free_banks.pop_front();
-                st = fill_bank(c, layer, q, b, &bytes);
+                new_group_events(q);
+                st = fill_bank(c, layer, q, b, &bytes, c->copy_streams[n_fills++ % c->d.Q],
+                               events_of(q));
                 if (st != ESTREAM_OK) break;
             }
+            estream_ctx::GroupEvents* ev = events_of(q);
             c->stats.groups_loaded += 1;
             if (cudaStreamWaitEvent(s, c->banks[b].ready, 0) != cudaSuccess) { st = ESTREAM_ERR_CUDA; break; }
+            if (ev) cudaEventRecord(ev->s, s);
             trace_state(c, b, layer, q, kInUse);
             int mt = 0;
             for (int e = s0; e < s1; ++e)
                 mt += (c->h_offsets[e + 1] - c->h_offsets[e] + kBM - 1) / kBM;
             st = run_routed(c, s, X, layer, mblk, s0, s1 - s0, b * G, mt, cnt, Y_routed);
             if (st != ESTREAM_OK) break;
+            if (ev) cudaEventRecord(ev->f, s);
             if (cudaEventRecord(c->banks[b].released, s) != cudaSuccess) { st = ESTREAM_ERR_CUDA; break; }
             c->banks[b].release_pending = true;
             trace_state(c, b, layer, q, kAvailable);
             free_banks.push_back(b);
         }
         // the caller's stream also covers the copies of this call
-        if (st == ESTREAM_OK && (cudaEventRecord(c->copy_done, c->copy_stream) != cudaSuccess ||
-                                 cudaStreamWaitEvent(s, c->copy_done, 0) != cudaSuccess))
-            st = ESTREAM_ERR_CUDA;
+        if (st == ESTREAM_OK) st = stream_after_copies(c, s);
     }
     if (st != ESTREAM_OK) {
         drain(c, s);
@@ -867,7 +953,7 @@ estream_status estream_set_timing(estream_ctx* c, int on) {
 
 estream_status estream_reset_stats(estream_ctx* c) {
     if (!c) return ESTREAM_ERR_NOT_BOUND;
-    if (cudaStreamSynchronize(c->copy_stream) != cudaSuccess) return ESTREAM_ERR_CUDA;
+    if (sync_copies(c) != ESTREAM_OK) return ESTREAM_ERR_CUDA;
     for (auto& t : c->timed) {
         cudaEventSynchronize(t.b);
         c->event_pool.push_back(t.a);
@@ -907,7 +993,7 @@ estream_status estream_last_stats(estream_ctx* c, estream_stats* out) {
 
 estream_status estream_get_device_error(estream_ctx* c) {
     if (!c) return ESTREAM_ERR_NOT_BOUND;
-    if (cudaStreamSynchronize(c->copy_stream) != cudaSuccess) return ESTREAM_ERR_CUDA;
+    if (sync_copies(c) != ESTREAM_OK) return ESTREAM_ERR_CUDA;
     if (cudaDeviceSynchronize() != cudaSuccess) return ESTREAM_ERR_CUDA;
     int host = 0;
     if (cudaMemcpy(&host, c->dev_err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
@@ -927,6 +1013,31 @@ estream_status estream_residency_trace(estream_ctx* c, int32_t* out, int cap, in
     return ESTREAM_OK;
 }
 
+estream_status estream_pipeline_trace(estream_ctx* c, double* adsf, int cap, int* n, double* t_ne) {
+    if (!c) return ESTREAM_ERR_NOT_BOUND;
+    if (!n || cap < 0 || (cap > 0 && !adsf)) return ESTREAM_ERR_INVALID_ARG;
+    *n = 0;
+    if (!c->pipe_t0) return ESTREAM_OK;
+    auto since = [&](cudaEvent_t e, double* out) {
+        float ms = 0.0f;
+        if (!e || cudaEventSynchronize(e) != cudaSuccess ||
+            cudaEventElapsedTime(&ms, c->pipe_t0, e) != cudaSuccess)
+            return false;
+        *out = ms;
+        return true;
+    };
+    if (t_ne && !since(c->pipe_tne, t_ne)) return ESTREAM_ERR_CUDA;
+    const int m = std::min(cap, static_cast<int>(c->pipe.size()));
+    for (int k = 0; k < m; ++k) {
+        const auto& g = c->pipe[k];
+        if (!since(g.a, adsf + 4 * k) || !since(g.d, adsf + 4 * k + 1) ||
+            !since(g.s, adsf + 4 * k + 2) || !since(g.f, adsf + 4 * k + 3))
+            return ESTREAM_ERR_CUDA;
+    }
+    *n = static_cast<int>(c->pipe.size());
+    return ESTREAM_OK;
+}
+
 estream_status estream_inject_pager_fault(estream_ctx* c, int layer, int group) {
     if (!c) return ESTREAM_ERR_NOT_BOUND;
     c->fault_layer = group < 0 ? -1 : layer;
@@ -936,7 +1047,9 @@ estream_status estream_inject_pager_fault(estream_ctx* c, int layer, int group) 
 
 void estream_unbind(estream_ctx* c) {
     if (!c) return;
-    if (c->copy_stream) cudaStreamSynchronize(c->copy_stream);
+    for (cudaStream_t cs : c->copy_streams)
+        if (cs) cudaStreamSynchronize(cs);
+    release_pipe_events(c);
     for (auto& t : c->timed) {
         cudaEventSynchronize(t.b);
         cudaEventDestroy(t.a);
@@ -949,7 +1062,8 @@ void estream_unbind(estream_ctx* c) {
     }
     if (c->copy_done) cudaEventDestroy(c->copy_done);
     if (c->preload_done) cudaEventDestroy(c->preload_done);
-    if (c->copy_stream) cudaStreamDestroy(c->copy_stream);
+    for (cudaStream_t cs : c->copy_streams)
+        if (cs) cudaStreamDestroy(cs);
     if (c->h_offsets) cudaFreeHost(c->h_offsets);
     if (c->ws) {
         cudaDeviceSynchronize();

@@ -84,6 +84,12 @@ SIGNATURES = {
     "estream_get_device_error": (_I, [_P]),
     "estream_residency_trace": (_I, [_P, _P, _I, ctypes.POINTER(_I)]),
     "estream_inject_pager_fault": (_I, [_P, _I, _I]),
+    "estream_pipeline_trace": (_I, [_P, _P, _I, ctypes.POINTER(_I), ctypes.POINTER(ctypes.c_double)]),
+    "estream_maxplus_pipeline": (ctypes.c_double, [_P, _P, _I, _I, _I, ctypes.c_double, _P]),
+    "estream_bank_bound": (_I, [_I, ctypes.c_double, ctypes.c_double, ctypes.c_double, _I]),
+    "estream_autoconfig": (_I, [_I, _P, _P, _P, _P, ctypes.c_double, _I, ctypes.c_double, _P,
+                                ctypes.c_double, _I, ctypes.POINTER(_I), ctypes.POINTER(_I),
+                                ctypes.POINTER(ctypes.c_double)]),
     "estream_unbind": (None, [_P]),
     "estream_cast_f32_bf16": (_I, [_P, _P, _SZ, _P]),
 }
@@ -305,6 +311,55 @@ def residency_trace(ctx, cap: int = 4096):
     _check(lib().estream_residency_trace(ctx, buf, cap, ctypes.byref(n)), "estream_residency_trace")
     m = min(n.value, cap)
     return [tuple(buf[4 * i:4 * i + 4]) for i in range(m)]
+
+
+def pipeline_trace(ctx, cap: int = 4096):
+    """Per-group (a, d, s, f) times in ms of the last timed paged call, and
+    the time routing finished."""
+    import numpy as np
+    buf = np.zeros((cap, 4), dtype=np.float64)
+    n = ctypes.c_int()
+    tne = ctypes.c_double()
+    _check(lib().estream_pipeline_trace(ctx, buf.ctypes.data_as(ctypes.c_void_p), cap,
+                                        ctypes.byref(n), ctypes.byref(tne)), "estream_pipeline_trace")
+    return buf[:min(n.value, cap)].copy(), tne.value
+
+
+def maxplus_pipeline(L, X, q: int, b: int, T_ne: float = 0.0):
+    """Eq. 5: returns (T_pipe, adsf[K][4])."""
+    import numpy as np
+    L = np.ascontiguousarray(L, dtype=np.float64)
+    X = np.ascontiguousarray(X, dtype=np.float64)
+    K = len(L)
+    out = np.zeros((max(K, 1), 4), dtype=np.float64)
+    t = lib().estream_maxplus_pipeline(L.ctypes.data_as(ctypes.c_void_p), X.ctypes.data_as(ctypes.c_void_p),
+                                       K, q, b, T_ne, out.ctypes.data_as(ctypes.c_void_p))
+    return t, out[:K]
+
+
+def bank_bound(g, M_max, M_other, W_e, N_e) -> int:
+    return lib().estream_bank_bound(g, M_max, M_other, W_e, N_e)
+
+
+def autoconfig(profiles: dict, T_ne: float, Q0: int, M_max: float, W_e: float, N_e: int,
+               M_other: dict | None = None):
+    """Eqs. 9-10 over {g: (L[], X[])}. Returns (G*, B*, T_pipe*)."""
+    import numpy as np
+    gs = list(profiles)
+    Ls = [np.ascontiguousarray(profiles[g][0], dtype=np.float64) for g in gs]
+    Xs = [np.ascontiguousarray(profiles[g][1], dtype=np.float64) for g in gs]
+    g_arr = (ctypes.c_int * len(gs))(*gs)
+    k_arr = (ctypes.c_int * len(gs))(*[len(x) for x in Ls])
+    L_arr = (ctypes.c_void_p * len(gs))(*[x.ctypes.data for x in Ls])
+    X_arr = (ctypes.c_void_p * len(gs))(*[x.ctypes.data for x in Xs])
+    mo = None
+    if M_other is not None:
+        mo = (ctypes.c_double * len(gs))(*[float(M_other[g]) for g in gs])
+    G, B, T = ctypes.c_int(), ctypes.c_int(), ctypes.c_double()
+    _check(lib().estream_autoconfig(len(gs), g_arr, k_arr, L_arr, X_arr, T_ne, Q0, M_max, mo, W_e,
+                                    N_e, ctypes.byref(G), ctypes.byref(B), ctypes.byref(T)),
+           "estream_autoconfig")
+    return G.value, B.value, T.value
 
 
 def inject_pager_fault(ctx, layer: int, group: int) -> None:

@@ -300,5 +300,44 @@ def pin_layer_special(lib):
     np.testing.assert_array_equal(Yb, Yf)
 
 
+# --------------------------------------------------------------------------
+# pipeline model
+# --------------------------------------------------------------------------
+
+def pin_maxplus(lib):
+    """Eq. 5 against a hand-worked fixture and closed forms: with unlimited
+    banks and one read in flight it is the two-machine flow shop
+    max_k (sum_{j<=k} L_j + sum_{j>=k} X_j); with one bank everything is
+    serial, sum_k (L_k + X_k); with unlimited reads and banks every read
+    starts at 0; more banks or reads never make it slower."""
+    fx = _read_golden("maxplus_example.txt")
+    t, adsf = O.maxplus(fx["L"], fx["X"], int(fx["q"][0]), int(fx["b"][0]), fx["T_ne"][0], lib=lib)
+    for col, key in enumerate("adsf"):
+        np.testing.assert_array_equal(adsf[:, col], fx[key])
+    assert t == fx["f"][-1]
+    rng = _rng(4)
+    for K in (1, 2, 5, 17):
+        L = rng.uniform(0.1, 3.0, K).round(3)
+        X = rng.uniform(0.1, 3.0, K).round(3)
+        flow = max(L[:k + 1].sum() + X[k:].sum() for k in range(K))
+        t, _ = O.maxplus(L, X, 1, K + 5, 0.0, lib=lib)
+        assert abs(t - flow) < 1e-9, (t, flow)
+        t1, _ = O.maxplus(L, X, 1, 1, 0.0, lib=lib)
+        assert abs(t1 - (L.sum() + X.sum())) < 1e-9
+        tp, adsf = O.maxplus(L, X, K + 5, K + 5, 0.0, lib=lib)
+        assert np.all(adsf[:, 0] == 0.0)
+        np.testing.assert_allclose(adsf[:, 1], L)
+        # no bank limit and every read done before the non-expert work ends:
+        # execution is one serial run starting at T_ne
+        tn, adsf = O.maxplus(L, X, 1, K + 5, 100.0, lib=lib)
+        assert np.all(adsf[:, 2] >= 100.0) and abs(tn - (100.0 + X.sum())) < 1e-9
+        prev = None
+        for b in range(1, K + 3):
+            tb, _ = O.maxplus(L, X, 2, b, 0.5, lib=lib)
+            assert prev is None or tb <= prev + 1e-12
+            prev = tb
+        assert O.maxplus(L, X, 2, 3, 0.0, lib=lib)[0] <= O.maxplus(L, X, 1, 3, 0.0, lib=lib)[0] + 1e-12
+
+
 ALL_PINS = [pin_exp, pin_topk, pin_topk_golden, pin_csr, pin_csr_golden, pin_placement,
-            pin_layer_dense, pin_layer_textbook, pin_layer_special]
+            pin_layer_dense, pin_layer_textbook, pin_layer_special, pin_maxplus]

@@ -142,3 +142,33 @@ def test_ragged_token_counts_reuse_one_context():
             _gpu.assert_y_close(y, ref, f"T={T}")
     finally:
         st.close()
+
+
+@pytest.mark.parametrize("Q", [1, 2])
+def test_pipeline_trace_matches_max_plus_model(Q):
+    """Per-group read/execution times recorded by the pager follow the
+    max-plus recurrence of section 3.4 (Eq. 5): event order a <= d <= s <= f,
+    no execution before its read ends, no bank refilled before its previous
+    group finished, and the model fed the measured L = d - a, X = f - s
+    predicts the measured completion."""
+    from routed_expert_ffn_topk_gb300 import estream as es
+    wl = small_workload("c2")
+    st = _stack(wl, mode="paged", G=2, B=2, Q=Q)
+    try:
+        es.set_timing(st.ctx, True)
+        y = run_layer(st, wl)
+        adsf, t_ne = es.pipeline_trace(st.ctx)
+        stats = es.last_stats(st.ctx)
+    finally:
+        st.close()
+    _gpu.assert_y_close(y, _gpu.oracle_layer(wl, 0, wl.X), f"Q={Q}")
+    K = len(adsf)
+    assert K == stats["groups_loaded"] and K >= 2
+    a, d, s, f = adsf.T
+    eps = 1e-3
+    assert np.all(a <= d + eps) and np.all(d <= s + eps) and np.all(s <= f + eps)
+    assert np.all(s[1:] >= f[:-1] - eps)           # one execution at a time
+    assert np.all(a[2:] >= f[:-2] - eps)           # bank reuse waits for release (b = 2)
+    L, X = d - a, f - s
+    t_model, _ = es.maxplus_pipeline(L, X, Q, 2, t_ne)
+    assert abs(t_model - f[-1]) <= 0.25 * f[-1] + 0.05, (t_model, f[-1])

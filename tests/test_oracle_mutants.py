@@ -37,6 +37,11 @@ MUTANTS = {
     "bottom_dropped": ("psi[i] = (s < 0) ? P : s;", "psi[i] = (s < 0) ? 0 : s;"),
     "rec_route_token": ("rec_route[p] = i;", "rec_route[p] = i / k;"),
     "placement_no_mod": ("int r = pos % G;", "int r = pos / G;"),
+    "maxplus_queue_off_by_one": ("double dq = (k - q >= 1) ? d[k - q] : 0.0;",
+                                 "double dq = (k - q + 1 >= 1) ? d[k - q + 1] : 0.0;"),
+    "maxplus_no_bank_limit": ("double fb = (k - b >= 1) ? f[k - b] : 0.0;", "double fb = 0.0;"),
+    "maxplus_no_serial_exec": ("if (f[k - 1] > s) s = f[k - 1];   /* f[0] = 0 */", "(void)0;"),
+    "maxplus_ignores_nonexpert": ("if (T_ne > s) s = T_ne;", "(void)0;"),
 }
 
 RUNNER = r"""
