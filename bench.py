@@ -316,7 +316,10 @@ def run_ours(args, rank, world, local_rank):
     per_launch_flops = ffn_f / launches_per_step
     ai = ffn_f / ffn_b
     ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
-    kname = "k_expert_ffn (gather + gate/up + SwiGLU + down + scatter)"
+    # the form the library's automatic choice takes for this layer shape
+    pair = cfg.T * cfg.k >= es.PAIR_MIN_ROWS * cfg.E
+    kname = ("k_expert_ffn_pair (CTA pairs, 256-record tiles" if pair else
+             "k_expert_ffn (128-record tiles") + ": gather + gate/up + SwiGLU + down + scatter)"
     if ai < ridge:
         achieved = per_launch_bytes / (ffn_ms / 1e3) / 1e9
         roof = {"kernel": kname, "bound": "hbm", "achieved": round(achieved, 1),

@@ -141,6 +141,21 @@ enum {
     ESTREAM_SCHED_PREFETCH = 1       /* also fill free banks in storage order before routing */
 };
 
+/* Form of the bf16 fused expert kernel (no counterpart in the paper, whose
+ * NPU has one matrix unit per core). SINGLE: 128-record tiles, one SM each.
+ * PAIR: 256-record tiles on a cluster of two SMs (tcgen05.mma.cta_group::2),
+ * each SM holding half of every weight tile: less shared-memory and L2
+ * traffic per FLOP, but up to 255 padded rows per expert instead of 127.
+ * AUTO: PAIR when an expert segment holds on average at least
+ * ESTREAM_PAIR_MIN_ROWS records (T*k/E for routed experts, T for shared
+ * ones; the measured crossover lies between 128 and 192), else SINGLE. */
+enum {
+    ESTREAM_FFN_AUTO = 0,
+    ESTREAM_FFN_SINGLE = 1,
+    ESTREAM_FFN_PAIR = 2
+};
+#define ESTREAM_PAIR_MIN_ROWS 160
+
 typedef struct {
     int L;                  /* sparse layers whose experts stream through this arena */
     int E, H, F;            /* routed experts per layer, hidden size, expert FFN size */
@@ -159,6 +174,7 @@ typedef struct {
     int T_max, k_max;       /* largest T and k a layer call will see (workspace capacity) */
     int deterministic;      /* 1: per-route outputs + fixed-order combine (bit-reproducible Y) */
     int schedule;           /* ESTREAM_SCHED_* */
+    int ffn_form;           /* ESTREAM_FFN_* (bf16 only; fp32 ignores it) */
 } estream_arena_desc;
 
 typedef struct estream_ctx estream_ctx;

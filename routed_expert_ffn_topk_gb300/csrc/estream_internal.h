@@ -82,6 +82,15 @@ cudaError_t launch_expert_ffn(const CUtensorMap* tm_wg, const CUtensorMap* tm_wu
                               void* h, float* Y, float* out_rows, int* done, int H, int F,
                               int phases, int* dev_err, int num_sms, cudaStream_t stream);
 
+// The same operator on CTA pairs (clusters of two, tcgen05.mma.cta_group::2,
+// 256-record pair tiles); tm_wd_half maps the down planes with 64 x 128
+// boxes (each CTA loads half of a 256-row W_d box).
+cudaError_t launch_expert_ffn_pair(const CUtensorMap* tm_wg, const CUtensorMap* tm_wu,
+                                   const CUtensorMap* tm_wd_half, const CUtensorMap* tm_h,
+                                   const GemmSegments& seg, const void* X, void* h, float* Y,
+                                   float* out_rows, int* done, int H, int F, int phases,
+                                   int* dev_err, cudaStream_t stream);
+
 // fp32 path (CUDA-core FMA): the same two steps for fp32 X and weights.
 // Weight planes are [slots][F][H] (gate, up) and [slots][H][F] (down).
 cudaError_t launch_gateup_f32(const float* X, const float* wg, const float* wu,

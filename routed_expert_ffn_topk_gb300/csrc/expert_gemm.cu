@@ -310,6 +310,68 @@ __device__ __forceinline__ void fence_proxy_async_global() {
     asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
+// Epilogue of a gate/up tile for one TMEM lane (one record): columns
+// [0, 128) of the accumulator hold the gate half and [128, 256) the up half
+// of 128 h columns; h = fp16(SiLU(g) * u) goes to dst[0 .. 128). Values
+// outside fp16's range are reported through dev_err.
+__device__ __forceinline__ void epilogue_gate_up(uint32_t tacc, bool valid, __half* dst,
+                                                 int* dev_err) {
+    bool in_range = true;
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+        uint32_t g[32], u[32];
+        tmem_ld32(tacc + c * 32, g);
+        tmem_ld32(tacc + 128 + c * 32, u);
+        tmem_ld_wait();
+        if (valid) {
+            uint32_t packed[16];
+#pragma unroll
+            for (int v = 0; v < 16; ++v) {
+                const float h0 = silu_mul(__uint_as_float(g[2 * v]), __uint_as_float(u[2 * v]));
+                const float h1 = silu_mul(__uint_as_float(g[2 * v + 1]), __uint_as_float(u[2 * v + 1]));
+                in_range = in_range && fabsf(h0) <= kHalfMax && fabsf(h1) <= kHalfMax;
+                const __half2 p2 = __floats2half2_rn(h0, h1);
+                packed[v] = *reinterpret_cast<const uint32_t*>(&p2);
+            }
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+                st_v4(dst + c * 32 + 8 * v, packed[4 * v], packed[4 * v + 1], packed[4 * v + 2],
+                      packed[4 * v + 3]);
+        }
+    }
+    if (!in_range) record_error(dev_err, kDevErrRange);
+}
+
+// Epilogue of a down tile for one TMEM lane: the 256 accumulator columns
+// times `al` are added into y_row[col0 ..] with vector reductions, or stored
+// to out_row[col0 ..] when out_row is given (deterministic mode).
+__device__ __forceinline__ void epilogue_down(uint32_t tacc, bool valid, float al, float* out_row,
+                                              float* y_row, int col0) {
+#pragma unroll 1
+    for (int c = 0; c < 8; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tacc + c * 32, v);
+        tmem_ld_wait();
+        if (valid) {
+            const int col = col0 + c * 32;
+            if (out_row) {
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    st_v4(out_row + col + 4 * q, __float_as_uint(al * __uint_as_float(v[4 * q])),
+                          __float_as_uint(al * __uint_as_float(v[4 * q + 1])),
+                          __float_as_uint(al * __uint_as_float(v[4 * q + 2])),
+                          __float_as_uint(al * __uint_as_float(v[4 * q + 3])));
+            } else {
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    red_add_v4(y_row + col + 4 * q, al * __uint_as_float(v[4 * q]),
+                               al * __uint_as_float(v[4 * q + 1]), al * __uint_as_float(v[4 * q + 2]),
+                               al * __uint_as_float(v[4 * q + 3]));
+            }
+        }
+    }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     k_expert_ffn(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant__ CUtensorMap tm_wu,
                  const __grid_constant__ CUtensorMap tm_wd, const __grid_constant__ CUtensorMap tm_h,
@@ -616,32 +678,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t tacc = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                   static_cast<uint32_t>(acc * kAccCols);
             if (gu) {
-                bool in_range = true;
-#pragma unroll 1
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t g[32], u[32];
-                    tmem_ld32(tacc + c * 32, g);
-                    tmem_ld32(tacc + 128 + c * 32, u);
-                    tmem_ld_wait();
-                    if (valid) {
-                        const size_t col = static_cast<size_t>(ti.nb) * 128 + c * 32;
-                        __half* dst = a.h + static_cast<size_t>(p) * F + col;
-                        uint32_t packed[16];
-#pragma unroll
-                        for (int v = 0; v < 16; ++v) {
-                            const float h0 = silu_mul(__uint_as_float(g[2 * v]), __uint_as_float(u[2 * v]));
-                            const float h1 = silu_mul(__uint_as_float(g[2 * v + 1]), __uint_as_float(u[2 * v + 1]));
-                            in_range = in_range && fabsf(h0) <= kHalfMax && fabsf(h1) <= kHalfMax;
-                            const __half2 p2 = __floats2half2_rn(h0, h1);
-                            packed[v] = *reinterpret_cast<const uint32_t*>(&p2);
-                        }
-#pragma unroll
-                        for (int v = 0; v < 4; ++v)
-                            st_v4(dst + 8 * v, packed[4 * v], packed[4 * v + 1], packed[4 * v + 2],
-                                  packed[4 * v + 3]);
-                    }
-                }
-                if (!in_range) record_error(a.dev_err, kDevErrRange);
+                epilogue_gate_up(tacc, valid,
+                                 a.h + static_cast<size_t>(p) * F + static_cast<size_t>(ti.nb) * 128,
+                                 a.dev_err);
                 // publish this warp's rows of the tile to the down tiles (which
                 // read h through TMA, the async proxy)
                 fence_proxy_async_global();
@@ -657,32 +696,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     al = seg.alpha ? seg.alpha[seg.rec_route[p]] : 1.0f;
                     al *= seg.seg_scale[seg.seg_begin + ti.seg];  // undo the W_d scale
                 }
-#pragma unroll 1
-                for (int c = 0; c < 8; ++c) {
-                    uint32_t v[32];
-                    tmem_ld32(tacc + c * 32, v);
-                    tmem_ld_wait();
-                    if (valid) {
-                        const size_t col = static_cast<size_t>(ti.nb) * 256 + c * 32;
-                        if (a.out_rows) {
-                            float* dst = a.out_rows + static_cast<size_t>(p) * H + col;
-#pragma unroll
-                            for (int q = 0; q < 8; ++q)
-                                st_v4(dst + 4 * q, __float_as_uint(al * __uint_as_float(v[4 * q])),
-                                      __float_as_uint(al * __uint_as_float(v[4 * q + 1])),
-                                      __float_as_uint(al * __uint_as_float(v[4 * q + 2])),
-                                      __float_as_uint(al * __uint_as_float(v[4 * q + 3])));
-                        } else {
-                            float* dst = a.Y + static_cast<size_t>(tok) * H + col;
-#pragma unroll
-                            for (int q = 0; q < 8; ++q)
-                                red_add_v4(dst + 4 * q, al * __uint_as_float(v[4 * q]),
-                                           al * __uint_as_float(v[4 * q + 1]),
-                                           al * __uint_as_float(v[4 * q + 2]),
-                                           al * __uint_as_float(v[4 * q + 3]));
-                        }
-                    }
-                }
+                epilogue_down(tacc, valid, al,
+                              a.out_rows ? a.out_rows + static_cast<size_t>(p) * H : nullptr,
+                              a.Y + static_cast<size_t>(tok) * H, ti.nb * 256);
             }
             tc_fence_before();
             __syncwarp();
@@ -697,6 +713,554 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+// ----------------------------------------------------------------------------
+// CTA-pair form: tcgen05.mma.cta_group::2, M = 256 rows over two SMs.
+// ----------------------------------------------------------------------------
+// A pair tile is (segment, n-block, pair m-block of 256 records). CTA r of the
+// cluster pair owns records [128r, 128r+128) of the pair m-block: it gathers
+// (gate/up) or TMA-loads (down, h) its 128 A rows, and holds half of the
+// N = 256 B tile -- rank 0 the gate rows, rank 1 the up rows of the h n-block;
+// or rows [128r, 128r+128) of the 256-row W_d box. The leader (rank 0) issues
+// the MMAs, which read both CTAs' shared memory; each CTA receives its 128
+// rows of the 128 x 256 fp32 result in its own TMEM, so the epilogue is the
+// single-CTA one. Per SM a stage is 32 KB (A 16 KB + half of B 16 KB) instead
+// of 48 KB for the same 128 x 256 x 64 of MMA work per SM, so the ring holds
+// six stages and each weight byte crosses from L2 to the SMs once per pair.
+// Completion: every stage's TMA bytes and loader arrivals land on the
+// leader's full barrier; the leader's commits are multicast to both CTAs'
+// empty and accumulator-full barriers; both CTAs' epilogue warps arrive on
+// the leader's accumulator-empty barrier.
+constexpr int kPStages = 6;
+constexpr int kPHalf = 128 * kRowBytes;                // 16 KB
+constexpr int kPOffA = 0;
+constexpr int kPOffB = kPStages * kPHalf;
+constexpr int kPOffBar = kPOffB + kPStages * kPHalf;
+constexpr int kPNumBars = 2 * kPStages + 5;
+constexpr int kPOffMisc = kPOffBar + 8 * kPNumBars;
+constexpr int kPOffTable = kPOffMisc + 16;
+constexpr int kPairRows = 2 * kBM;
+constexpr int kLoaderWarps = 4;
+constexpr int kEpiWarps = 4;
+
+size_t pair_smem_bytes(int seg_count) {
+    return 1024 + kPOffTable + sizeof(int) * static_cast<size_t>(seg_count + 1);
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// Address of the same shared-memory offset in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_rank(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                     : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cl(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// mbar_wait with cluster-scope acquire (arrivals come from the peer CTA).
+__device__ bool mbar_wait_cl(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* dev_err) {
+    if (mbar_try_wait_cl(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    uint32_t spins = 0;
+    while (true) {
+        if (mbar_try_wait_cl(bar, parity)) return true;
+        if ((++spins & 63u) == 0) {
+            if (*abort_flag) return false;
+            if (global_ns() - t0 > kWaitLimitNs) {
+                *abort_flag = 1;
+                record_error(dev_err, kDevErrTimeout);
+                return false;
+            }
+        }
+    }
+}
+// Release of this thread's shared-memory writes at cluster scope, restricted
+// to shared::cta memory (lighter than a full cluster-scope release, which
+// also waits for the thread's global-memory traffic), followed by a relaxed
+// arrival on a barrier of the peer CTA: the hand-off of a shared-memory
+// payload to the other CTA of the pair.
+__device__ __forceinline__ void mbar_arrive_remote_smem_release(uint32_t cl_addr) {
+    asm volatile(
+        "fence.release.sync_restrict::shared::cta.cluster;\n\t"
+        "mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cl_addr)
+        : "memory");
+}
+// Arrive on a barrier given by its shared::cluster address (either CTA).
+__device__ __forceinline__ void mbar_arrive_cl(uint32_t cl_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cl_addr)
+                 : "memory");
+}
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* tm, int x, int y,
+                                                 uint32_t cl_bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(cl_bar)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void umma_f16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                              uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive once on the barrier at offset `bar` in both CTAs of the pair when
+// the MMAs issued so far have completed.
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(bar),
+        "h"(static_cast<uint16_t>(3))
+        : "memory");
+}
+
+struct PairTile {
+    int seg;    // segment index relative to seg_begin
+    int pm;     // pair m-block inside the segment
+    int nb;     // n-block
+    int row0;   // first record of this CTA's half
+    int rows;   // valid records in this CTA's half (0..kBM)
+    int rows1;  // valid records in rank 1's half (0..kBM)
+};
+
+__device__ __forceinline__ PairTile decode_pair(int t, const int* table, int seg_count, int NB,
+                                                const int32_t* offsets, int seg_begin, int rank) {
+    int lo = 0, hi = seg_count;  // largest lo with table[lo] * NB <= t
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (table[mid] * NB <= t) lo = mid; else hi = mid;
+    }
+    PairTile ti;
+    ti.seg = lo;
+    const int npm = table[lo + 1] - table[lo];
+    const int l = t - table[lo] * NB;
+    ti.nb = l / npm;
+    ti.pm = l - ti.nb * npm;
+    const int s_lo = offsets[seg_begin + lo];
+    const int s_hi = offsets[seg_begin + lo + 1];
+    const int pr0 = s_lo + ti.pm * kPairRows;
+    const int tot = min(kPairRows, s_hi - pr0);
+    ti.row0 = pr0 + kBM * rank;
+    ti.rows = max(0, min(kBM, tot - kBM * rank));
+    ti.rows1 = max(0, min(kBM, tot - kBM));
+    return ti;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    k_expert_ffn_pair(const __grid_constant__ CUtensorMap tm_wg,
+                      const __grid_constant__ CUtensorMap tm_wu,
+                      const __grid_constant__ CUtensorMap tm_wd,
+                      const __grid_constant__ CUtensorMap tm_h, const FfnArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ int warp_total[kThreads / 32];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    const GemmSegments& seg = a.seg;
+    const uint32_t rank = cluster_rank();
+    const int pair = static_cast<int>(blockIdx.x >> 1);
+    const int n_pairs = static_cast<int>(gridDim.x >> 1);
+    const uint32_t sbase = smem_addr(smem);
+    const uint32_t sA = sbase + kPOffA;
+    const uint32_t sB = sbase + kPOffB;
+    const uint32_t bar0 = sbase + kPOffBar;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (kPStages + s); };
+    auto accf_bar = [&](int q) { return bar0 + 8u * (2 * kPStages + q); };
+    auto acce_bar = [&](int q) { return bar0 + 8u * (2 * kPStages + 2 + q); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * kPStages + 4);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kPOffMisc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kPOffMisc + 4);
+    int* table = reinterpret_cast<int*>(smem + kPOffTable);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    // pair m-blocks per segment (ceil(count / 256)), exclusive prefix in table
+    {
+        const int n = seg.seg_count;
+        const int per = (n + kThreads - 1) / kThreads;
+        const int lo = min(n, static_cast<int>(threadIdx.x) * per);
+        const int hi = min(n, lo + per);
+        int sum = 0;
+        for (int s = lo; s < hi; ++s) {
+            const int cnt = seg.offsets[seg.seg_begin + s + 1] - seg.offsets[seg.seg_begin + s];
+            sum += (cnt + kPairRows - 1) / kPairRows;
+        }
+        int incl = sum;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, d);
+            if (lane >= d) incl += v;
+        }
+        if (lane == 31) warp_total[warp] = incl;
+        __syncthreads();
+        int run = incl - sum;
+        for (int w = 0; w < warp; ++w) run += warp_total[w];
+        for (int s = lo; s < hi; ++s) {
+            table[s] = run;
+            const int cnt = seg.offsets[seg.seg_begin + s + 1] - seg.offsets[seg.seg_begin + s];
+            run += (cnt + kPairRows - 1) / kPairRows;
+        }
+        if (threadIdx.x == kThreads - 1) table[n] = run;
+    }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kPStages; ++s) {
+            // leader: the producer's expect_tx + one arrival per loader warp
+            // of both CTAs (the peer's full barriers stay unused)
+            mbar_init(full_bar(s), 1 + 2 * kLoaderWarps);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int q = 0; q < 2; ++q) {
+            mbar_init(accf_bar(q), 1);
+            mbar_init(acce_bar(q), 2 * kEpiWarps);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_addr(tmem_slot), kTmemCols);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // both CTAs' barriers exist before any remote arrival
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int H = a.H, F = a.F;
+    const int NBA = F / 128, NBB = H / 256;
+    const int KBA = H / 64, KBB = F / 64;
+    const int PM = table[seg.seg_count];
+    const int TA = (a.phases & 1) ? PM * NBA : 0;
+    const int TB = (a.phases & 2) ? PM * NBB : 0;
+    const int total = TA + TB;
+    const int done_target = kEpiWarps * NBA;
+
+    if (warp == 0) {
+        // ------------------------------ TMA producer ------------------------------
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int t = pair; ok && t < total; t += n_pairs) {
+            const bool gu = t < TA;
+            const PairTile ti = decode_pair(gu ? t : t - TA, table, seg.seg_count, gu ? NBA : NBB,
+                                            seg.offsets, seg.seg_begin, static_cast<int>(rank));
+            const int slot = seg.slot_base + ti.seg;
+            const int num_kb = gu ? KBA : KBB;
+            // tile-major planes: the (n-block, k-block) box of a slot is one
+            // contiguous run of 128 (gate, up) or 256 (down) rows of 128 bytes
+            int brow0;
+            const CUtensorMap* tm_b;
+            if (gu) {
+                brow0 = (slot * NBA + ti.nb) * KBA * 128;
+                tm_b = rank == 0 ? &tm_wg : &tm_wu;
+            } else {
+                brow0 = (slot * NBB + ti.nb) * KBB * 256 + kBM * static_cast<int>(rank);
+                tm_b = &tm_wd;
+            }
+            const int brow_step = gu ? 128 : 256;
+            const bool load_h = !gu && ti.rows > 0;
+            if (load_h) {
+                // this half's h rows are complete once every epilogue warp of
+                // every gate/up n-block of its m-block has published
+                const int* cnt = a.done + seg.mblk[seg.seg_begin + ti.seg] + 2 * ti.pm +
+                                 static_cast<int>(rank);
+                bool w = true;
+                if (lane == 0 && ld_acquire(cnt) < done_target) {
+                    const uint64_t t0 = global_ns();
+                    while (ld_acquire(cnt) < done_target) {
+                        if (*abort_flag) {
+                            w = false;
+                            break;
+                        }
+                        if (global_ns() - t0 > kWaitLimitNs) {
+                            *abort_flag = 1;
+                            record_error(a.dev_err, kDevErrTimeout);
+                            w = false;
+                            break;
+                        }
+                    }
+                }
+                if (lane == 0) fence_proxy_async_global();  // before the TMA reads of h
+                w = __shfl_sync(0xffffffffu, w, 0);
+                if (!w) {
+                    ok = false;
+                    break;
+                }
+            }
+            const uint32_t tx = 2 * kPHalf + (gu ? 0 : kPHalf * (1 + (ti.rows1 > 0 ? 1 : 0)));
+            for (int kb = 0; kb < num_kb; ++kb) {
+                bool w = true;
+                if (lane == 0) w = mbar_wait_cl(empty_bar(stage), phase ^ 1u, abort_flag, a.dev_err);
+                w = __shfl_sync(0xffffffffu, w, 0);
+                if (!w) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), tx);
+                    const uint32_t lbar = map_rank(full_bar(stage), 0);
+                    tma_load_2d_pair(sB + stage * kPHalf, tm_b, 0, brow0 + kb * brow_step, lbar);
+                    if (load_h)
+                        tma_load_2d_pair(sA + stage * kPHalf, &tm_h, kb * 64, ti.row0, lbar);
+                }
+                __syncwarp();
+                if (++stage == kPStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        if (!ok && lane == 0) {
+            // give copies already issued time to land before the CTA goes away
+            const uint64_t t0 = global_ns();
+            while (global_ns() - t0 < kDrainLimitNs / 100) {
+            }
+        }
+    } else if (warp >= kLoaderWarp0) {
+        // ------------------------------ A-operand loader ------------------------------
+        // As in the single-CTA kernel, but each warp arrives once per stage
+        // (after every lane's copies completed and were fenced) on the
+        // leader's full barrier: a local arrival in the leader, a restricted
+        // shared-memory release and a relaxed remote arrival in the peer.
+        const int gw = warp - kLoaderWarp0;
+        const uint32_t chunk = static_cast<uint32_t>(lane & 7);
+        int stage = 0;
+        uint32_t phase = 0;
+        int pend[kLoaderDepth + 1];
+        int npend = 0;
+        bool ok = true;
+        auto publish = [&](int s) {
+            __syncwarp();
+            if (lane == 0) {
+                if (rank == 0)
+                    mbar_arrive(full_bar(s));
+                else
+                    mbar_arrive_remote_smem_release(map_rank(full_bar(s), 0));
+            }
+        };
+        for (int t = pair; ok && t < total; t += n_pairs) {
+            const bool gu = t < TA;
+            const PairTile ti = decode_pair(gu ? t : t - TA, table, seg.seg_count, gu ? NBA : NBB,
+                                            seg.offsets, seg.seg_begin, static_cast<int>(rank));
+            const int num_kb = gu ? KBA : KBB;
+            if (!gu) {
+                if (npend > 0) {
+                    cp_async_wait<0>();
+                    fence_proxy_async();
+                    for (int q = 0; q < npend; ++q) publish(pend[q]);
+                    npend = 0;
+                }
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    bool w = true;
+                    if (lane == 0) w = mbar_wait_cl(empty_bar(stage), phase ^ 1u, abort_flag, a.dev_err);
+                    w = __shfl_sync(0xffffffffu, w, 0);
+                    if (!w) {
+                        ok = false;
+                        break;
+                    }
+                    publish(stage);
+                    if (++stage == kPStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                continue;
+            }
+            const uint8_t* src_row[8];
+            uint32_t dst_off[8];
+            unsigned live = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int r = gw * 32 + 4 * i + (lane >> 3);
+                dst_off[i] = static_cast<uint32_t>(r) * kRowBytes +
+                             ((chunk ^ static_cast<uint32_t>(r & 7)) << 4);
+                const bool lv = r < ti.rows;
+                live |= lv ? (1u << i) : 0u;
+                const uint8_t* row = reinterpret_cast<const uint8_t*>(a.x);
+                if (lv)
+                    row = reinterpret_cast<const uint8_t*>(
+                        a.x + static_cast<size_t>(seg.rec_tok[ti.row0 + r]) * H);
+                src_row[i] = row + chunk * 16;
+            }
+            for (int kb = 0; kb < num_kb; ++kb) {
+                bool w = true;
+                if (lane == 0) w = mbar_wait_cl(empty_bar(stage), phase ^ 1u, abort_flag, a.dev_err);
+                w = __shfl_sync(0xffffffffu, w, 0);
+                if (!w) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t base = sA + stage * kPHalf;
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    if (live & (1u << i)) cp_async_16(base + dst_off[i], src_row[i] + kb * kRowBytes);
+                cp_async_commit();
+                pend[npend++] = stage;
+                if (npend > kLoaderDepth) {
+                    cp_async_wait<kLoaderDepth>();
+                    fence_proxy_async();
+                    publish(pend[0]);
+#pragma unroll
+                    for (int q = 0; q < kLoaderDepth; ++q) pend[q] = pend[q + 1];
+                    --npend;
+                }
+                if (++stage == kPStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        cp_async_wait<0>();
+        fence_proxy_async();
+        for (int q = 0; q < npend; ++q) publish(pend[q]);
+    } else if (warp == 1) {
+        // ------------------------------ MMA issuer (leader CTA) ------------------------------
+        if (lane == 0 && rank == 0) {
+            const uint32_t idesc_gu = make_idesc(true, kPairRows, 256);   // bf16 x bf16
+            const uint32_t idesc_dn = make_idesc(false, kPairRows, 256);  // fp16 x fp16
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            bool issued_any = false;
+            for (int t = pair; ok && t < total; t += n_pairs) {
+                const bool gu = t < TA;
+                const int num_kb = gu ? KBA : KBB;
+                const uint32_t idesc = gu ? idesc_gu : idesc_dn;
+                if (!mbar_wait_cl(acce_bar(acc), acc_phase ^ 1u, abort_flag, a.dev_err)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kAccCols);
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait_cl(full_bar(stage), phase, abort_flag, a.dev_err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t adesc = sw128_desc(sA + stage * kPHalf);
+                    const uint64_t bdesc = sw128_desc(sB + stage * kPHalf);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        umma_f16_pair(d_tmem, adesc + 2u * kk, bdesc + 2u * kk, idesc,
+                                      (kb | kk) != 0 ? 1u : 0u);
+                    issued_any = true;
+                    umma_commit_pair(empty_bar(stage));
+                    if (++stage == kPStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                umma_commit_pair(accf_bar(acc));
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1u;
+            }
+            if (!ok && issued_any) {
+                umma_commit_pair(drain_bar);
+                mbar_wait_cl(drain_bar, 0, abort_flag, nullptr);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------ epilogue (warps 2-5) ------------------------------
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        const uint32_t leader_acce0 = map_rank(acce_bar(0), 0);
+        const uint32_t leader_acce1 = map_rank(acce_bar(1), 0);
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int t = pair; t < total; t += n_pairs) {
+            const bool gu = t < TA;
+            const PairTile ti = decode_pair(gu ? t : t - TA, table, seg.seg_count, gu ? NBA : NBB,
+                                            seg.offsets, seg.seg_begin, static_cast<int>(rank));
+            bool w = true;
+            if (lane == 0) w = mbar_wait_cl(accf_bar(acc), acc_phase, abort_flag, a.dev_err);
+            w = __shfl_sync(0xffffffffu, w, 0);
+            if (!w) break;
+            tc_fence_after();
+            const bool valid = row < ti.rows;
+            const int p = ti.row0 + row;
+            const uint32_t tacc = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                  static_cast<uint32_t>(acc * kAccCols);
+            if (gu) {
+                epilogue_gate_up(tacc, valid, a.h + static_cast<size_t>(p) * F +
+                                                   static_cast<size_t>(ti.nb) * 128, a.dev_err);
+                fence_proxy_async_global();
+                __threadfence();
+                __syncwarp();
+                if (lane == 0 && (a.phases & 2) && ti.rows > 0)
+                    red_release_add(a.done + seg.mblk[seg.seg_begin + ti.seg] + 2 * ti.pm +
+                                        static_cast<int>(rank),
+                                    1);
+            } else {
+                float al = 0.0f;
+                int tok = 0;
+                if (valid) {
+                    tok = seg.rec_tok[p];
+                    al = seg.alpha ? seg.alpha[seg.rec_route[p]] : 1.0f;
+                    al *= seg.seg_scale[seg.seg_begin + ti.seg];
+                }
+                epilogue_down(tacc, valid, al,
+                              a.out_rows ? a.out_rows + static_cast<size_t>(p) * H : nullptr,
+                              a.Y + static_cast<size_t>(tok) * H, ti.nb * 256);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if (rank == 0)
+                    mbar_arrive(acce_bar(acc));
+                else
+                    mbar_arrive_cl(acc == 0 ? leader_acce0 : leader_acce1);
+            }
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // the peer's shared memory and TMEM stay until the pair is done
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, kTmemCols);
     }
 }
 
@@ -755,6 +1319,89 @@ cudaError_t launch_expert_ffn(const CUtensorMap* tm_wg, const CUtensorMap* tm_wu
     // gate/up tiles of its m-block that other CTAs own
     rc = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(k_expert_ffn), grid, kThreads,
                                      kargs, smem, stream);
+    if (rc != cudaSuccess) return rc;
+    return cudaGetLastError();
+}
+
+// Co-resident CTA pairs of k_expert_ffn_pair at its largest shared-memory
+// size (the bound for every smaller launch), per device.
+static int max_pairs(int device) {
+    static int cache[64] = {0};
+    if (device < 0 || device >= 64) return 0;
+    if (cache[device] > 0) return cache[device];
+    const size_t smem = pair_smem_bytes(kMaxP);
+    if (cudaFuncSetAttribute(k_expert_ffn_pair, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+        return 0;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    int nsm = 0;
+    cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, device);
+    cfg.gridDim = dim3(static_cast<unsigned>(nsm & ~1));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(k_expert_ffn_pair), &cfg) !=
+        cudaSuccess)
+        return 0;
+    cache[device] = n;
+    return n;
+}
+
+cudaError_t launch_expert_ffn_pair(const CUtensorMap* tm_wg, const CUtensorMap* tm_wu,
+                                   const CUtensorMap* tm_wd_half, const CUtensorMap* tm_h,
+                                   const GemmSegments& seg, const void* X, void* h, float* Y,
+                                   float* out_rows, int* done, int H, int F, int phases,
+                                   int* dev_err, cudaStream_t stream) {
+    const long long max_tiles = static_cast<long long>(seg.max_tiles_m) *
+                                (((phases & 1) ? F / 128 : 0) + ((phases & 2) ? H / 256 : 0));
+    if (max_tiles <= 0 || seg.seg_count <= 0) return cudaSuccess;
+    int device = 0;
+    cudaError_t rc = cudaGetDevice(&device);
+    if (rc != cudaSuccess) return rc;
+    const int cap = max_pairs(device);
+    if (cap <= 0) return cudaErrorLaunchOutOfResources;
+    const int pairs = static_cast<int>(max_tiles < cap ? max_tiles : cap);
+    const size_t smem = pair_smem_bytes(seg.seg_count);
+    rc = cudaFuncSetAttribute(k_expert_ffn_pair, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(smem));
+    if (rc != cudaSuccess) return rc;
+    FfnArgs args;
+    args.seg = seg;
+    args.x = static_cast<const __nv_bfloat16*>(X);
+    args.h = static_cast<__half*>(h);
+    args.Y = Y;
+    args.out_rows = out_rows;
+    args.done = done;
+    args.dev_err = dev_err;
+    args.H = H;
+    args.F = F;
+    args.phases = phases;
+    void* kargs[] = {const_cast<CUtensorMap*>(tm_wg), const_cast<CUtensorMap*>(tm_wu),
+                     const_cast<CUtensorMap*>(tm_wd_half), const_cast<CUtensorMap*>(tm_h), &args};
+    // clusters of two CTAs; cooperative, so every pair is resident and a down
+    // tile may wait for gate/up tiles that other pairs own
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute at[2];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    at[1].id = cudaLaunchAttributeCooperative;
+    at[1].val.cooperative = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = at;
+    cfg.numAttrs = 2;
+    rc = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(k_expert_ffn_pair), kargs);
     if (rc != cudaSuccess) return rc;
     return cudaGetLastError();
 }

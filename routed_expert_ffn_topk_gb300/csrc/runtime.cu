@@ -64,8 +64,8 @@ struct estream_ctx {
     std::vector<int32_t> perm;
     std::vector<const void*> shared_dev;
     char *plane_g = nullptr, *plane_u = nullptr, *plane_d = nullptr;
-    CUtensorMap tm_wg{}, tm_wu{}, tm_wd{}, tm_h{}, tm_hs{};
-    std::vector<CUtensorMap> tm_sg, tm_su, tm_sd;
+    CUtensorMap tm_wg{}, tm_wu{}, tm_wd{}, tm_wd_half{}, tm_h{}, tm_hs{};
+    std::vector<CUtensorMap> tm_sg, tm_su, tm_sd, tm_sd_half;
 
     // library-owned device workspace
     char* ws = nullptr;
@@ -372,6 +372,9 @@ estream_status estream_bind_arena(estream_ctx** out, const estream_arena_desc* d
         return ESTREAM_ERR_INVALID_ARG;
     if (d->schedule != ESTREAM_SCHED_AFTER_ROUTING && d->schedule != ESTREAM_SCHED_PREFETCH)
         return ESTREAM_ERR_INVALID_ARG;
+    if (d->ffn_form != ESTREAM_FFN_AUTO && d->ffn_form != ESTREAM_FFN_SINGLE &&
+        d->ffn_form != ESTREAM_FFN_PAIR)
+        return ESTREAM_ERR_INVALID_ARG;
     if (d->n_shared < 0 || (d->n_shared > 0 && (d->F_shared < 128 || d->F_shared % 128 != 0 ||
                                                  !d->shared_dev)))
         return ESTREAM_ERR_INVALID_ARG;
@@ -538,6 +541,8 @@ estream_status estream_bind_arena(estream_ctx** out, const estream_arena_desc* d
                                             128) == CUDA_SUCCESS;
             tm_ok = tm_ok && encode_tmap_2d(&c->tm_wd, HF, c->plane_d, 64, plane_rows, 128, 64,
                                             256) == CUDA_SUCCESS;
+            tm_ok = tm_ok && encode_tmap_2d(&c->tm_wd_half, HF, c->plane_d, 64, plane_rows, 128,
+                                            64, 128) == CUDA_SUCCESS;
             tm_ok = tm_ok && encode_tmap_2d(&c->tm_h, HF, c->h, d->F, static_cast<uint64_t>(R_cap),
                                             static_cast<uint64_t>(d->F) * 2, 64, 128) == CUDA_SUCCESS;
             if (d->n_shared > 0) {
@@ -548,6 +553,7 @@ estream_status estream_bind_arena(estream_ctx** out, const estream_arena_desc* d
                 c->tm_sg.resize(d->L);
                 c->tm_su.resize(d->L);
                 c->tm_sd.resize(d->L);
+                c->tm_sd_half.resize(d->L);
                 const size_t sp = static_cast<size_t>(d->n_shared) * Fs * d->H * 2;
                 for (int l = 0; l < d->L && tm_ok; ++l) {
                     const char* base = static_cast<const char*>(c->shared_dev[l]);
@@ -558,6 +564,8 @@ estream_status estream_bind_arena(estream_ctx** out, const estream_arena_desc* d
                                                     64, 128) == CUDA_SUCCESS;
                     tm_ok = tm_ok && encode_tmap_2d(&c->tm_sd[l], HF, base + 2 * sp, 64, srows, 128,
                                                     64, 256) == CUDA_SUCCESS;
+                    tm_ok = tm_ok && encode_tmap_2d(&c->tm_sd_half[l], HF, base + 2 * sp, 64,
+                                                    srows, 128, 64, 128) == CUDA_SUCCESS;
                 }
             }
         }
@@ -611,11 +619,20 @@ estream_status fill_bank(estream_ctx* c, int layer, int q, int b, size_t* bytes,
     return ESTREAM_OK;
 }
 
+// Form of the bf16 fused expert kernel for `rows` records over `segments`
+// expert segments: ESTREAM_FFN_AUTO takes the CTA-pair form (256-record
+// tiles) when a segment holds on average at least ESTREAM_PAIR_MIN_ROWS.
+bool pair_form(const estream_ctx* c, long long rows, int segments) {
+    if (c->d.ffn_form == ESTREAM_FFN_PAIR) return true;
+    if (c->d.ffn_form == ESTREAM_FFN_SINGLE) return false;
+    return segments > 0 && rows >= static_cast<long long>(ESTREAM_PAIR_MIN_ROWS) * segments;
+}
+
 // K2 + K3 over segments [seg_begin, seg_begin + seg_count) of the routed
 // route map, whose experts sit in consecutive arena slots from slot_base.
 estream_status run_routed(estream_ctx* c, cudaStream_t s, const void* X, int layer,
                           const int32_t* mblk, int seg_begin, int seg_count, int slot_base,
-                          int max_tiles_m, int max_rows, float* Y) {
+                          int max_tiles_m, int max_rows, bool pair, float* Y) {
     GemmSegments seg{};
     seg.offsets = c->offsets;
     seg.mblk = mblk;
@@ -639,8 +656,12 @@ estream_status run_routed(estream_ctx* c, cudaStream_t s, const void* X, int lay
                                  c->d.H, c->d.F, max_rows, s);
         c->stats.launches += 2;
     } else {
-        rc = launch_expert_ffn(&c->tm_wg, &c->tm_wu, &c->tm_wd, &c->tm_h, seg, X, c->h, Y, c->out_rows,
-                               c->done, c->d.H, c->d.F, 3, c->dev_err, c->num_sms, s);
+        rc = pair
+                 ? launch_expert_ffn_pair(&c->tm_wg, &c->tm_wu, &c->tm_wd_half, &c->tm_h, seg, X, c->h,
+                                          Y, c->out_rows, c->done, c->d.H, c->d.F, 3, c->dev_err, s)
+                 : launch_expert_ffn(&c->tm_wg, &c->tm_wu, &c->tm_wd, &c->tm_h, seg, X, c->h, Y,
+                                     c->out_rows, c->done, c->d.H, c->d.F, 3, c->dev_err,
+                                     c->num_sms, s);
         c->stats.launches += 1;
     }
     if (rc != cudaSuccess) return ESTREAM_ERR_CUDA;
@@ -678,9 +699,13 @@ estream_status run_shared(estream_ctx* c, cudaStream_t s, const void* X,
             rc = launch_down_f32(static_cast<const float*>(c->h_shared), base + 2 * sp, seg, Y,
                                  c->out_shared, c->d.H, Fs, ns * T, s);
     } else {
-        rc = launch_expert_ffn(&c->tm_sg[layer], &c->tm_su[layer], &c->tm_sd[layer], &c->tm_hs, seg, X,
-                               c->h_shared, Y, c->out_shared, c->sh_done, c->d.H, Fs, 3, c->dev_err,
-                               c->num_sms, s);
+        rc = pair_form(c, T, 1)
+                 ? launch_expert_ffn_pair(&c->tm_sg[layer], &c->tm_su[layer], &c->tm_sd_half[layer],
+                                          &c->tm_hs, seg, X, c->h_shared, Y, c->out_shared,
+                                          c->sh_done, c->d.H, Fs, 3, c->dev_err, s)
+                 : launch_expert_ffn(&c->tm_sg[layer], &c->tm_su[layer], &c->tm_sd[layer], &c->tm_hs,
+                                     seg, X, c->h_shared, Y, c->out_shared, c->sh_done, c->d.H, Fs,
+                                     3, c->dev_err, c->num_sms, s);
     }
     if (rc != cudaSuccess) return ESTREAM_ERR_CUDA;
     c->stats.launches += c->d.wdtype == ESTREAM_F32 ? 3 : 2;
@@ -866,7 +891,8 @@ estream_status estream_moe_layer_prefill(estream_ctx* c, int layer, const void* 
     if (resident) {
         // every group sits in bank q: one launch pair over all slots, no host sync
         for (int q = 0; q < c->n_groups; ++q) trace_state(c, q, layer, q, kInUse);
-        st = run_routed(c, s, X, layer, mblk, 0, E, 0, (R + kBM - 1) / kBM + E, R, Y_routed);
+        st = run_routed(c, s, X, layer, mblk, 0, E, 0, (R + kBM - 1) / kBM + E, R,
+                        pair_form(c, R, E), Y_routed);
         c->stats.groups_hit += c->n_groups;
         for (int q = 0; q < c->n_groups && st == ESTREAM_OK; ++q) {
             if (cudaEventRecord(c->banks[q].released, s) != cudaSuccess) st = ESTREAM_ERR_CUDA;
@@ -914,10 +940,14 @@ estream_status estream_moe_layer_prefill(estream_ctx* c, int layer, const void* 
             if (cudaStreamWaitEvent(s, c->banks[b].ready, 0) != cudaSuccess) { st = ESTREAM_ERR_CUDA; break; }
             if (ev) cudaEventRecord(ev->s, s);
             trace_state(c, b, layer, q, kInUse);
-            int mt = 0;
-            for (int e = s0; e < s1; ++e)
-                mt += (c->h_offsets[e + 1] - c->h_offsets[e] + kBM - 1) / kBM;
-            st = run_routed(c, s, X, layer, mblk, s0, s1 - s0, b * G, mt, cnt, Y_routed);
+            int mt = 0, active = 0;
+            for (int e = s0; e < s1; ++e) {
+                const int n = c->h_offsets[e + 1] - c->h_offsets[e];
+                mt += (n + kBM - 1) / kBM;
+                active += n > 0 ? 1 : 0;
+            }
+            st = run_routed(c, s, X, layer, mblk, s0, s1 - s0, b * G, mt, cnt,
+                            pair_form(c, cnt, active), Y_routed);
             if (st != ESTREAM_OK) break;
             if (ev) cudaEventRecord(ev->f, s);
             if (cudaEventRecord(c->banks[b].released, s) != cudaSuccess) { st = ESTREAM_ERR_CUDA; break; }

@@ -20,6 +20,8 @@ OK, ERR_INVALID_ARG, ERR_CAPACITY, ERR_NOT_BOUND, ERR_CUDA, ERR_PAGER, ERR_TIMEO
     ERR_DEVICE, ERR_UNSUPPORTED = range(9)
 F32, BF16 = 0, 1
 SCHED_AFTER_ROUTING, SCHED_PREFETCH = 0, 1
+FFN_AUTO, FFN_SINGLE, FFN_PAIR = 0, 1, 2
+PAIR_MIN_ROWS = 160
 STATE_NAMES = {0: "Available", 1: "Filling", 2: "Ready", 3: "InUse"}
 
 
@@ -41,6 +43,7 @@ class ArenaDesc(ctypes.Structure):
         ("shared_dev", ctypes.POINTER(ctypes.c_void_p)),
         ("T_max", ctypes.c_int), ("k_max", ctypes.c_int),
         ("deterministic", ctypes.c_int), ("schedule", ctypes.c_int),
+        ("ffn_form", ctypes.c_int),
     ]
 
 
@@ -232,7 +235,7 @@ def pack_shared(desc: ArenaDesc, sg: torch.Tensor, su: torch.Tensor, sd: torch.T
 
 def make_desc(L, E, H, F, G, B, wdtype, arena: torch.Tensor, pools, perm=None, n_shared=0,
               F_shared=0, shared=None, T_max=1, k_max=1, deterministic=False,
-              schedule=SCHED_AFTER_ROUTING, Q=1):
+              schedule=SCHED_AFTER_ROUTING, Q=1, ffn_form=FFN_AUTO):
     """Fill an ArenaDesc; returns (desc, keepalive) -- keep both alive while bound."""
     d = ArenaDesc()
     d.L, d.E, d.H, d.F, d.G, d.B, d.Q = L, E, H, F, G, B, Q
@@ -254,6 +257,7 @@ def make_desc(L, E, H, F, G, B, wdtype, arena: torch.Tensor, pools, perm=None, n
     d.T_max, d.k_max = T_max, k_max
     d.deterministic = int(bool(deterministic))
     d.schedule = schedule
+    d.ffn_form = ffn_form
     return d, keep
 
 

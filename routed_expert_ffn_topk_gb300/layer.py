@@ -22,7 +22,7 @@ class BoundLayerStack:
 
     def __init__(self, wl: Workload, mode: str = "resident", perm=None, G=None, B=None,
                  deterministic=False, schedule=es.SCHED_AFTER_ROUTING, T_max=None, k_max=None,
-                 Q=1, device="cuda"):
+                 Q=1, ffn_form=es.FFN_AUTO, device="cuda"):
         cfg = wl.cfg
         self.cfg, self.wl, self.mode = cfg, wl, mode
         self.dtype = es.BF16 if cfg.dtype == "bf16" else es.F32
@@ -59,7 +59,8 @@ class BoundLayerStack:
         self.desc, self.keep = es.make_desc(
             L, cfg.E, cfg.H, cfg.F, G, B, self.dtype, self.arena, self.pools, perm=self.perm,
             n_shared=cfg.n_shared, F_shared=cfg.F_shared, shared=self.shared or None,
-            T_max=self.T_max, k_max=self.k_max, deterministic=deterministic, schedule=schedule, Q=Q)
+            T_max=self.T_max, k_max=self.k_max, deterministic=deterministic, schedule=schedule, Q=Q,
+            ffn_form=ffn_form)
         self.ctx = es.bind_arena(self.desc)
         if mode == "resident":
             if L != 1:

@@ -71,20 +71,24 @@ def test_layer_residual_accumulates():
     _gpu.assert_y_close(y - A.numpy(), ref - A.double().numpy(), "residual")
 
 
-@pytest.mark.parametrize("key,mode", [("c2", "resident"), ("c2", "paged"), ("c3", "paged"),
-                                      ("c5", "resident"), ("c5", "paged")])
-def test_layer_full_size_sampled(key, mode):
+@pytest.mark.parametrize("key,mode,form", [("c2", "resident", "auto"), ("c2", "resident", "pair"),
+                                           ("c2", "paged", "auto"), ("c3", "paged", "auto"),
+                                           ("c3", "resident", "single"), ("c5", "resident", "auto"),
+                                           ("c5", "paged", "auto")])
+def test_layer_full_size_sampled(key, mode, form):
+    from routed_expert_ffn_topk_gb300 import estream as es
     from routed_expert_ffn_topk_gb300.layer import BoundLayerStack
     cfg = W.CONFIGS[key]
     wl = W.make_workload(cfg)
-    st = BoundLayerStack(wl, mode=mode)
+    f = {"auto": es.FFN_AUTO, "single": es.FFN_SINGLE, "pair": es.FFN_PAIR}[form]
+    st = BoundLayerStack(wl, mode=mode, ffn_form=f)
     try:
         y = run_layer(st, wl)
     finally:
         st.close()
     rows = W.sample_rows(cfg.T, 24 if cfg.H * cfg.F < 2e7 else 10, seed=3)
     ref = _gpu.oracle_layer(wl, 0, wl.X, rows=rows.numpy())
-    _gpu.assert_y_close(y[rows.numpy()], ref, f"{key}/{mode} sampled")
+    _gpu.assert_y_close(y[rows.numpy()], ref, f"{key}/{mode}/{form} sampled")
 
 
 def test_layer_stack_chained_full_size():
