@@ -266,6 +266,31 @@ __device__ __forceinline__ Tile decode_tile(int t, const int* table, int seg_cou
     return ti;
 }
 
+// The idx-th tile of worker b (a CTA, or a CTA pair) among G workers, or -1
+// past its last. Gate/up tiles [0, TA) go round-robin (worker b gets b,
+// b + G, ...). Down tiles [TA, TA + TB) first top up the workers that got one
+// gate/up tile fewer, KBA / KBB tiles each (round-robin over those), then go
+// round-robin over all workers starting at the first of them, so that the
+// k-blocks per worker (KBA per gate/up tile, KBB per down tile) even out.
+// Each worker runs all its gate/up tiles before its down tiles, which keeps
+// the cross-CTA wait of a down tile deadlock-free.
+__device__ __forceinline__ int tile_of(int b, int G, int TA, int TB, int KBA, int KBB, int idx) {
+    const int q = TA / G, rem = TA - q * G;
+    const int n_gu = q + (b < rem ? 1 : 0);
+    if (idx < n_gu) return b + idx * G;
+    idx -= n_gu;
+    const int lows = G - rem;
+    const int n_extra = rem ? KBA / KBB : 0;
+    const int A = static_cast<int>(min(static_cast<long long>(TB), static_cast<long long>(n_extra) * lows));
+    if (b >= rem && b - rem < A) {
+        const int nA = (A - (b - rem) + lows - 1) / lows;
+        if (idx < nA) return TA + (b - rem) + idx * lows;
+        idx -= nA;
+    }
+    const long long j = static_cast<long long>(A) + (b - rem + G) % G + static_cast<long long>(idx) * G;
+    return j < TB ? TA + static_cast<int>(j) : -1;
+}
+
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
@@ -429,7 +454,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int MB = table[seg.seg_count];
     const int TA = (a.phases & 1) ? MB * NBA : 0;
     const int TB = (a.phases & 2) ? MB * NBB : 0;
-    const int total = TA + TB;
     const int done_target = 4 * NBA;          // every epilogue warp of every gate/up n-block
 
     if (warp == 0) {
@@ -439,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int issued[kStages];
         for (int s = 0; s < kStages; ++s) issued[s] = -1;
         bool ok = true;
-        for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+        for (int it = 0, t; ok && (t = tile_of(blockIdx.x, gridDim.x, TA, TB, KBA, KBB, it)) >= 0; ++it) {
             const bool gu = t < TA;
             const Tile ti = decode_tile(gu ? t : t - TA, table, seg.seg_count, gu ? NBA : NBB,
                                         seg.offsets, seg.seg_begin);
@@ -528,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int pend[kLoaderDepth + 1];
         int npend = 0;
         bool ok = true;
-        for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+        for (int it = 0, t; ok && (t = tile_of(blockIdx.x, gridDim.x, TA, TB, KBA, KBB, it)) >= 0; ++it) {
             const bool gu = t < TA;
             const Tile ti = decode_tile(gu ? t : t - TA, table, seg.seg_count, gu ? NBA : NBB,
                                         seg.offsets, seg.seg_begin);
@@ -617,7 +641,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t acc_phase = 0;
             bool ok = true;
             bool issued_any = false;
-            for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+            for (int it = 0, t; ok && (t = tile_of(blockIdx.x, gridDim.x, TA, TB, KBA, KBB, it)) >= 0; ++it) {
                 const bool gu = t < TA;
                 const int num_kb = gu ? KBA : KBB;
                 const uint32_t idesc = gu ? idesc_gu : idesc_dn;
@@ -664,7 +688,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = quarter * 32 + lane;
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int t = blockIdx.x; t < total; t += gridDim.x) {
+        for (int it = 0, t; (t = tile_of(blockIdx.x, gridDim.x, TA, TB, KBA, KBB, it)) >= 0; ++it) {
             const bool gu = t < TA;
             const Tile ti = decode_tile(gu ? t : t - TA, table, seg.seg_count, gu ? NBA : NBB,
                                         seg.offsets, seg.seg_begin);
@@ -967,7 +991,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int PM = table[seg.seg_count];
     const int TA = (a.phases & 1) ? PM * NBA : 0;
     const int TB = (a.phases & 2) ? PM * NBB : 0;
-    const int total = TA + TB;
     const int done_target = kEpiWarps * NBA;
 
     if (warp == 0) {
@@ -975,7 +998,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
-        for (int t = pair; ok && t < total; t += n_pairs) {
+        for (int it = 0, t; ok && (t = tile_of(pair, n_pairs, TA, TB, KBA, KBB, it)) >= 0; ++it) {
             const bool gu = t < TA;
             const PairTile ti = decode_pair(gu ? t : t - TA, table, seg.seg_count, gu ? NBA : NBB,
                                             seg.offsets, seg.seg_begin, static_cast<int>(rank));
@@ -1073,7 +1096,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive_remote_smem_release(map_rank(full_bar(s), 0));
             }
         };
-        for (int t = pair; ok && t < total; t += n_pairs) {
+        for (int it = 0, t; ok && (t = tile_of(pair, n_pairs, TA, TB, KBA, KBB, it)) >= 0; ++it) {
             const bool gu = t < TA;
             const PairTile ti = decode_pair(gu ? t : t - TA, table, seg.seg_count, gu ? NBA : NBB,
                                             seg.offsets, seg.seg_begin, static_cast<int>(rank));
@@ -1159,7 +1182,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t acc_phase = 0;
             bool ok = true;
             bool issued_any = false;
-            for (int t = pair; ok && t < total; t += n_pairs) {
+            for (int it = 0, t; ok && (t = tile_of(pair, n_pairs, TA, TB, KBA, KBB, it)) >= 0; ++it) {
                 const bool gu = t < TA;
                 const int num_kb = gu ? KBA : KBB;
                 const uint32_t idesc = gu ? idesc_gu : idesc_dn;
@@ -1207,7 +1230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t leader_acce1 = map_rank(acce_bar(1), 0);
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int t = pair; t < total; t += n_pairs) {
+        for (int it = 0, t; (t = tile_of(pair, n_pairs, TA, TB, KBA, KBB, it)) >= 0; ++it) {
             const bool gu = t < TA;
             const PairTile ti = decode_pair(gu ? t : t - TA, table, seg.seg_count, gu ? NBA : NBB,
                                             seg.offsets, seg.seg_begin, static_cast<int>(rank));
