@@ -32,7 +32,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # capture summarised in profiles/k_expert_ffn_olmoe_resident.md. Reported only while
 # the kernel source is the one that was captured.
 PROFILED_TRAFFIC = {
-    "c2": {"kernel_sha256_16": "809e0b88470d9003", "bytes": 878069248},
+    "c2": {"kernel_sha256_16": "ab12bb3771a2a949", "bytes": 877929728},
 }
 KERNEL_SRC = os.path.join(ROOT, "routed_expert_ffn_topk_gb300", "csrc", "expert_gemm.cu")
 
@@ -326,10 +326,14 @@ def run_ours(args, rank, world, local_rank):
                 "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                 "traffic": None}
     else:
+        # the kernel is timed inside a loop of back-to-back steps lasting seconds, so the
+        # denominator is the sustained (power-capped) bf16 figure; the burst one is kept beside it
+        sus = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
         achieved = per_launch_flops / (ffn_ms / 1e3) / 1e12
         roof = {"kernel": kname, "bound": "tensor", "achieved": round(achieved, 1),
-                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": None}
+                "peak": sus, "peak_kind": "sustained", "unit": "TFLOP/s",
+                "frac": round(achieved / sus, 4),
+                "frac_of_burst_peak": round(achieved / peaks["bf16_tflops"], 4), "traffic": None}
     roof["peak_source"] = peaks["source"]
     roof["traffic"] = profiled_traffic(cfg.key) if L == 1 else None
     roof["algorithmic_bytes_per_launch"] = int(per_launch_bytes)
