@@ -385,6 +385,8 @@ def run_ours(args, rank, world, local_rank):
     paged = measure_paged(args, cfg, wl, dev, stream, flush, peaks) if not args.no_paged else None
     if paged is not None and args.pipeline_study and cfg.layers == 1:
         paged["pipeline_study"] = pipeline_study(cfg, wl, dev, flush)
+    if paged is not None and args.pipeline_study and cfg.layers > 1:
+        paged["layer_granular_study"] = layer_granular_study(cfg, wl, dev, flush)
 
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
@@ -565,6 +567,59 @@ def pipeline_study(cfg, wl, dev, flush, reps=5):
                          "sweep_best": list(best), "sweep_best_ms": round(measured[best], 4),
                          "regret": round(measured.get((G, B), float("nan")) / measured[best] - 1, 4),
                          "sweep": {f"G{g}_B{b}": round(v, 4) for (g, b), v in sorted(measured.items())}}
+    return out
+
+
+def layer_granular_study(cfg, wl, dev, flush, reps=3):
+    """Section 4 (layer-granular baselines): a whole L-layer step streamed
+    through the config's group-granular arena (P = B*G slots reused across
+    layers), against banks that each hold one whole layer (G = E) with two
+    banks (Layer-B=2) or L banks (Layer-B=L, every layer's experts held at
+    once). Every step starts from an empty arena, so each layer's experts
+    stream once; reported: ms per step and arena bytes."""
+    import torch
+
+    from routed_expert_ffn_topk_gb300 import estream as es
+    from routed_expert_ffn_topk_gb300.layer import BoundLayerStack
+    stream = torch.cuda.current_stream()
+    L = cfg.layers
+    X0 = wl.X.to(dev)
+    logits = [lg.to(dev) for lg in wl.logits]
+    out = {}
+    variants = (("group_granular", cfg.G, cfg.B, es.SCHED_AFTER_ROUTING),
+                ("group_granular_prefetch", cfg.G, cfg.B, es.SCHED_PREFETCH),
+                ("layer_B2", cfg.E, 2, es.SCHED_PREFETCH),
+                ("layer_BL", cfg.E, L, es.SCHED_PREFETCH))
+    for name, G, B, sched in variants:
+        st = BoundLayerStack(wl, mode="paged", G=G, B=B, schedule=sched)
+        try:
+            def step():
+                es.arena_invalidate(st.ctx)
+                X = X0
+                for l in range(L):
+                    Y = X.float()
+                    st.prefill(l, X, logits[l], Y)
+                    if l + 1 < L:
+                        Xn = torch.empty_like(X)
+                        es.cast_f32_bf16(Y, Xn)
+                        X = Xn
+            step()
+            torch.cuda.synchronize()
+            ms = []
+            for _ in range(reps):
+                flush.zero_()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                step()
+                b.record(stream)
+                b.synchronize()
+                ms.append(a.elapsed_time(b))
+            assert es.get_device_error(st.ctx) == es.OK
+        finally:
+            arena = st.arena.numel()
+            st.close()
+        out[name] = {"G": G, "B": B, "schedule": "prefetch" if sched == es.SCHED_PREFETCH else "after_routing",
+                     "arena_bytes": int(arena), "ms_per_step": round(sorted(ms)[len(ms) // 2], 4)}
     return out
 
 

@@ -4,4 +4,5 @@ Imported only by the tests, ``__graft_entry__.smoke()`` and the bench's
 CPU-baseline leg; the product library never touches it.
 """
 from .oracle import (build, load, exp_f32, route_topk, route_csr,  # noqa: F401
-                     grouped_placement, moe_layer_rows, num_threads, maxplus)
+                     grouped_placement, moe_layer_rows, num_threads, maxplus,
+                     router_logits)

@@ -215,6 +215,27 @@ static double load_elem(const void* base, size_t idx, int bf16)
 
 static double silu(double z) { return z / (1.0 + exp(-z)); }
 
+/* Router logits upstream of the top-k (the layer input X_t mapped to one
+ * score per expert; the pages name the router and its top-k selection in
+ * section 1 and list a routing operator among the NPU operators in section 4,
+ * without its form). Reading: the bias-free linear router of top-k MoE
+ * layers, l[t][e] = sum over h of X[t][h] * W_r[e][h], evaluated in fp64 from
+ * the exactly widened inputs (X [T][H], W_r [E][H], both fp32 or both bf16
+ * bit patterns), ascending h. Returns 0, or -1 on bad arguments. */
+int oracle_router_logits(const void* X, int T, int H, const void* W_r, int E, int bf16,
+                         double* logits)
+{
+    if (T < 0 || H < 1 || E < 1 || (T > 0 && (!X || !W_r || !logits))) return -1;
+    for (int t = 0; t < T; ++t)
+        for (int e = 0; e < E; ++e) {
+            double acc = 0.0;
+            for (int h = 0; h < H; ++h)
+                acc += load_elem(X, (size_t)t * H + h, bf16) * load_elem(W_r, (size_t)e * H + h, bf16);
+            logits[(size_t)t * E + e] = acc;
+        }
+    return 0;
+}
+
 /* Eq. 1 for one token row: out[o] = sum_f Wd[o][f] * SiLU(g_f) * u_f with
  * g_f = sum_h Wg[f][h] x[h], u_f = sum_h Wu[f][h] x[h].
  * Wg, Wu are [F][H] and Wd is [H][F], row-major; x is the token's row offset

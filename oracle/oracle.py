@@ -66,6 +66,8 @@ def _declare(lib) -> None:
     lib.oracle_num_threads.restype = i
     lib.oracle_maxplus.argtypes = [P, P, i, i, i, ctypes.c_double, P]
     lib.oracle_maxplus.restype = ctypes.c_double
+    lib.oracle_router_logits.argtypes = [P, i, i, P, i, i, P]
+    lib.oracle_router_logits.restype = i
 
 
 def load(path: str | None = None):
@@ -209,6 +211,24 @@ def maxplus(L, X, q: int, b: int, T_ne: float = 0.0, lib=None):
     out = np.zeros((max(K, 1), 4), dtype=np.float64)
     t = lib.oracle_maxplus(_ptr(L), _ptr(X), K, q, b, float(T_ne), _ptr(out))
     return t, out[:K]
+
+
+def router_logits(X, W_r, lib=None) -> np.ndarray:
+    """Router logits l[t][e] = sum_h X[t][h] * W_r[e][h] in fp64 (the linear
+    router upstream of the top-k; reading stated in the C file)."""
+    lib = lib or load()
+    Xa, bx = _as_weight(X)
+    Wa, bw = _as_weight(W_r)
+    if bx != bw:
+        raise ValueError("X and W_r must share one encoding")
+    T, H = Xa.shape
+    E, H2 = Wa.shape
+    if H2 != H:
+        raise ValueError("X and W_r disagree on H")
+    out = np.zeros((T, E), dtype=np.float64)
+    if lib.oracle_router_logits(_ptr(Xa), T, H, _ptr(Wa), E, bx, _ptr(out)) != 0:
+        raise ValueError("oracle_router_logits: bad arguments")
+    return out
 
 
 def num_threads(lib=None) -> int:

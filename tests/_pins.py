@@ -339,5 +339,46 @@ def pin_maxplus(lib):
         assert O.maxplus(L, X, 2, 3, 0.0, lib=lib)[0] <= O.maxplus(L, X, 1, 3, 0.0, lib=lib)[0] + 1e-12
 
 
+# --------------------------------------------------------------------------
+# router logits
+# --------------------------------------------------------------------------
+
+def _bf16_bits(a):
+    return (np.ascontiguousarray(a, dtype=np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+def _bf16_widen(b):
+    return (b.astype(np.uint32) << 16).view(np.float32)
+
+
+def pin_router(lib):
+    """Router logits l = X W_r^T against exact integer arithmetic (small
+    integer inputs, where every fp64 partial sum is exact), numpy's fp64
+    matmul on random inputs (equal up to rounding order), a one-hot W_r (each
+    expert reads one input feature, exactly), and bf16 inputs equal to their
+    fp32 widening."""
+    rng = _rng(11)
+    for T, H, E in ((1, 1, 1), (3, 7, 5), (9, 64, 12), (4, 5, 9)):
+        Xi = rng.integers(-8, 9, (T, H))
+        Wi = rng.integers(-8, 9, (E, H))
+        got = O.router_logits(Xi.astype(np.float32), Wi.astype(np.float32), lib=lib)
+        exact = np.array([[sum(int(Xi[t, h]) * int(Wi[e, h]) for h in range(H)) for e in range(E)]
+                          for t in range(T)], dtype=np.float64)
+        np.testing.assert_array_equal(got, exact)
+    X = rng.standard_normal((17, 96)).astype(np.float32)
+    W = rng.standard_normal((10, 96)).astype(np.float32)
+    got = O.router_logits(X, W, lib=lib)
+    ref = X.astype(np.float64) @ W.astype(np.float64).T
+    scale = np.abs(X).astype(np.float64) @ np.abs(W).astype(np.float64).T
+    assert np.all(np.abs(got - ref) <= 1e-13 * scale)
+    cols = rng.integers(0, 96, 10)
+    onehot = np.zeros((10, 96), dtype=np.float32)
+    onehot[np.arange(10), cols] = 1.0
+    np.testing.assert_array_equal(O.router_logits(X, onehot, lib=lib), X[:, cols].astype(np.float64))
+    Xb, Wb = _bf16_bits(X), _bf16_bits(W)
+    np.testing.assert_array_equal(O.router_logits(Xb, Wb, lib=lib),
+                                  O.router_logits(_bf16_widen(Xb), _bf16_widen(Wb), lib=lib))
+
+
 ALL_PINS = [pin_exp, pin_topk, pin_topk_golden, pin_csr, pin_csr_golden, pin_placement,
-            pin_layer_dense, pin_layer_textbook, pin_layer_special, pin_maxplus]
+            pin_layer_dense, pin_layer_textbook, pin_layer_special, pin_maxplus, pin_router]

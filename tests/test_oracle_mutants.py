@@ -42,6 +42,9 @@ MUTANTS = {
     "maxplus_no_bank_limit": ("double fb = (k - b >= 1) ? f[k - b] : 0.0;", "double fb = 0.0;"),
     "maxplus_no_serial_exec": ("if (f[k - 1] > s) s = f[k - 1];   /* f[0] = 0 */", "(void)0;"),
     "maxplus_ignores_nonexpert": ("if (T_ne > s) s = T_ne;", "(void)0;"),
+    "router_w_transposed": ("load_elem(W_r, (size_t)e * H + h, bf16)", "load_elem(W_r, (size_t)h * E + e, bf16)"),
+    "router_first_term_dropped": ("for (int h = 0; h < H; ++h)\n                acc +=",
+                                  "for (int h = 1; h < H; ++h)\n                acc +="),
 }
 
 RUNNER = r"""
