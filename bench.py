@@ -381,6 +381,9 @@ def run_ours(args, rank, world, local_rank):
     for st in stacks:
         st.close()
 
+    # ---- router logits upstream of the top-k (its own kernel, not part of the step) ----
+    router = measure_router(cfg, X0, dev, stream, flush, peaks, args.steps) if cfg.dtype == "bf16" else None
+
     # ---- arena-paged run of the same config (host-link bound) ----
     paged = measure_paged(args, cfg, wl, dev, stream, flush, peaks) if not args.no_paged else None
     if paged is not None and args.pipeline_study and cfg.layers == 1:
@@ -402,9 +405,44 @@ def run_ours(args, rank, world, local_rank):
                 "h2d_bytes_per_step": h2d_b, "d2h_bytes_per_step": d2h_b},
         "gpu_launches": gpu_launches,
         "clocks": clocks.summary(),
+        "router": router,
         "paged": paged,
     }
     return line
+
+
+def measure_router(cfg, X0, dev, stream, flush, peaks, steps):
+    """estream_router_logits on the config's X and a seeded W_r [E, H]: CUDA
+    events around each call on the launching stream, L2 flushed before each."""
+    import torch
+
+    from routed_expert_ffn_topk_gb300 import estream as es
+    from routed_expert_ffn_topk_gb300 import workloads as W
+    _, W_r = W.make_router(1, cfg.H, cfg.E, seed=W.CONFIG_SEEDS[cfg.key] + 500)
+    W_r = W_r.to(dev)
+    T, H, E = cfg.T, cfg.H, cfg.E
+    logits = torch.empty(T, E, dtype=torch.float32, device=dev)
+    ws = torch.empty(max(es.router_workspace_bytes(T, H, E), 256), dtype=torch.uint8, device=dev)
+    for _ in range(3):
+        es.router_logits(X0, W_r, logits=logits, workspace=ws)
+    ms = []
+    for _ in range(max(steps, 5)):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        es.router_logits(X0, W_r, logits=logits, workspace=ws)
+        b.record(stream)
+        b.synchronize()
+        ms.append(a.elapsed_time(b))
+    assert es.workspace_error(ws) == es.OK
+    t = sorted(ms)[len(ms) // 2]
+    nbytes = T * H * 2 + E * H * 2 + T * E * 4
+    gbs = nbytes / (t / 1e3) / 1e9
+    return {"kernel": "k_router_partial + k_router_reduce (tcgen05, split-K, fixed-order sum)",
+            "ms": round(t, 4), "algorithmic_bytes": nbytes, "GBps": round(gbs, 1),
+            "frac_hbm": round(gbs / peaks["hbm_gbs"], 4),
+            "TFLOPs": round(2.0 * T * H * E / (t / 1e3) / 1e12, 1),
+            "workspace_bytes": int(ws.numel())}
 
 
 def measure_paged(args, cfg, wl, dev, stream, flush, peaks):

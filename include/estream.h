@@ -102,9 +102,39 @@ estream_status estream_route_build(const float* logits, int T, int E, int k, int
                                    void* workspace, size_t workspace_bytes,
                                    void* cuda_stream);
 
-/* Synchronises `cuda_stream` and returns the error a route-build kernel
- * recorded in `workspace` (ESTREAM_OK if none), then clears it. */
+/* Synchronises `cuda_stream` and returns the error a route-build or
+ * router-logits kernel recorded in `workspace` (ESTREAM_OK if none), then
+ * clears it. */
 estream_status estream_workspace_error(void* workspace, void* cuda_stream);
+
+/* Bytes of device workspace estream_router_logits needs for these sizes on
+ * the current device (>= 256); 0 for invalid sizes. */
+size_t estream_router_workspace_bytes(int T, int H, int E);
+
+/*
+ * Router logits upstream of the top-k: logits[t][e] = sum over h of
+ * X[t][h] * W_r[e][h]. The pages name the router (a token goes to the top-k
+ * of E experts, section 1) and run routing on the accelerator from the layer
+ * input (section 4) without giving its form; this is the bias-free linear
+ * router of top-k MoE layers. The output feeds estream_route_build or
+ * estream_moe_layer_prefill.
+ *
+ * X         device, [T][H] bf16 row-major, 16-byte aligned.
+ * W_r       device, [E][H] bf16 row-major (one row per expert), 16-byte aligned.
+ * T, H, E   T >= 0; H a multiple of 64; 1 <= E <= 1024.
+ * logits    device, [T][E] fp32 out.
+ * workspace device, >= estream_router_workspace_bytes(T, H, E) bytes,
+ *           256-byte aligned; no initialisation needed. Its first word is the
+ *           error word estream_workspace_error reads (a bounded wait that ran
+ *           out is reported there).
+ * Computed on the tensor cores (bf16 products, fp32 accumulation) with the
+ * K range split into chunks whose fp32 partial sums are added in a fixed
+ * order: the result does not depend on timing, but its rounding differs
+ * from a sequential fp32 sum. Nothing is synchronised.
+ */
+estream_status estream_router_logits(const void* X, int T, int H, const void* W_r, int E,
+                                     float* logits, void* workspace, size_t workspace_bytes,
+                                     void* cuda_stream);
 
 /*
  * estream_route_build without a workspace argument, for callers that cannot

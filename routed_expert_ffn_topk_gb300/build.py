@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OBJ_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libestream.so")
 SOURCES = ["route.cu", "route_static.cu", "expert_gemm.cu", "expert_f32.cu", "runtime.cu",
-           "pipeline_model.cu"]
+           "pipeline_model.cu", "router.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -44,7 +44,8 @@ def _stale(out: str, deps) -> bool:
 def build(force: bool = False, verbose: bool = False) -> str:
     nvcc = _nvcc()
     os.makedirs(OBJ_DIR, exist_ok=True)
-    headers = [os.path.join(CSRC, "estream_internal.h"), os.path.join(INCLUDE, "estream.h")]
+    headers = [os.path.join(CSRC, "estream_internal.h"), os.path.join(CSRC, "tc_ptx.cuh"),
+               os.path.join(INCLUDE, "estream.h")]
     common = [nvcc, *ARCH, "-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
               "-I" + INCLUDE, "-I" + CSRC]
     jobs = []

@@ -1,0 +1,291 @@
+// Router logits upstream of the top-k: l[t][e] = sum_h X[t][h] * W_r[e][h].
+//
+// "EStream: Fast and Memory-Efficient MoE Prefill through Expert
+// Virtualization on Mobile NPUs", section 1 (a router assigns each token to
+// the top-k of E experts) and section 4 (routing is one of the operators run
+// on the accelerator, on the layer input). The form of the router is not on
+// the pages; this is the bias-free linear router of top-k MoE layers.
+//
+// GB300 form. The contraction is [T, H] x [H, E] with E small (8..1024), so
+// one 128-token tile per CTA would leave most SMs idle. The K range is split
+// into S chunks so that about one wave of CTAs covers the GPU: CTA (m, n, s)
+// multiplies tokens [128m, 128m+128) by experts [N n, N n + N) over its
+// k-blocks with tcgen05.mma.kind::f16 (bf16, fp32 accumulate in TMEM), both
+// operands TMA-loaded with 128-byte swizzle through a 4-stage ring, and
+// stores its fp32 partial sums. A second kernel adds the S partials of every
+// logit in ascending s, so the logits do not depend on timing. With S = 1
+// the partial kernel writes the logits directly.
+// Warp roles: warp 0 TMA producer, warp 1 TMEM allocation and the MMA issue,
+// warps 2-5 epilogue (TMEM lanes = tokens). Every wait is bounded.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "estream_internal.h"
+
+namespace es {
+namespace {
+
+#include "tc_ptx.cuh"
+
+constexpr int kRStages = 4;
+constexpr int kRThreads = 192;
+constexpr int kRTileA = 128 * 128;  // 128 tokens x 64 bf16
+
+struct RouterArgs {
+    float* out;        // [S][T][E] partials, or [T][E] logits when S == 1
+    int* dev_err;      // optional
+    int T, E, KB, S, N;
+    uint32_t tx_bytes;  // bytes one stage's two boxes deliver
+};
+
+size_t router_smem_bytes(int N) {
+    return 1024 + static_cast<size_t>(kRStages) * (kRTileA + N * 128) + 8 * (2 * kRStages + 1) + 16;
+}
+
+__global__ void __launch_bounds__(kRThreads, 1)
+    k_router_partial(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
+                     const RouterArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    const int N = a.N;
+    const int tileB = N * 128;
+    const uint32_t sbase = smem_addr(smem);
+    const uint32_t sA = sbase;
+    const uint32_t sB = sbase + kRStages * kRTileA;
+    const uint32_t bar0 = sB + kRStages * tileB;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (kRStages + s); };
+    const uint32_t acc_bar = bar0 + 8u * (2 * kRStages);
+    uint8_t* misc = smem + (bar0 - sbase) + 8 * (2 * kRStages + 1);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int m0 = blockIdx.x * 128;
+    const int n0 = blockIdx.y * N;
+    const int s = blockIdx.z;
+    const int kb0 = static_cast<int>(static_cast<long long>(s) * a.KB / a.S);
+    const int kb1 = static_cast<int>(static_cast<long long>(s + 1) * a.KB / a.S);
+    const uint32_t tmem_cols = N <= 32 ? 32u : (N <= 64 ? 64u : (N <= 128 ? 128u : 256u));
+
+    if (threadIdx.x == 0) {
+        for (int q = 0; q < kRStages; ++q) {
+            mbar_init(full_bar(q), 1);
+            mbar_init(empty_bar(q), 1);
+        }
+        mbar_init(acc_bar, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_addr(tmem_slot), tmem_cols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int issued[kRStages];
+            for (int q = 0; q < kRStages; ++q) issued[q] = -1;
+            bool ok = true;
+            for (int kb = kb0, i = 0; kb < kb1; ++kb, ++i) {
+                const int st = i % kRStages;
+                const uint32_t ph = static_cast<uint32_t>(i / kRStages) & 1u;
+                if (!mbar_wait(empty_bar(st), ph ^ 1u, abort_flag, a.dev_err)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(full_bar(st), a.tx_bytes);
+                issued[st] = static_cast<int>(ph);
+                tma_load_2d(sA + st * kRTileA, &tm_x, kb * 64, m0, full_bar(st));
+                tma_load_2d(sB + st * tileB, &tm_w, kb * 64, n0, full_bar(st));
+            }
+            if (!ok)
+                for (int q = 0; q < kRStages; ++q)
+                    if (issued[q] >= 0)
+                        mbar_wait(full_bar(q), static_cast<uint32_t>(issued[q]), abort_flag, nullptr,
+                                  kDrainLimitNs);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idesc = make_idesc(true, 128, N);
+            bool any = false;
+            for (int kb = kb0, i = 0; kb < kb1; ++kb, ++i) {
+                const int st = i % kRStages;
+                const uint32_t ph = static_cast<uint32_t>(i / kRStages) & 1u;
+                if (!mbar_wait(full_bar(st), ph, abort_flag, a.dev_err)) break;
+                tc_fence_after();
+                const uint64_t adesc = sw128_desc(sA + st * kRTileA);
+                const uint64_t bdesc = sw128_desc(sB + st * tileB);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    umma_f16(tmem_base, adesc + 2u * kk, bdesc + 2u * kk, idesc, (i | kk) != 0 ? 1u : 0u);
+                any = true;
+                umma_commit(empty_bar(st));
+            }
+            // the accumulator barrier completes once every MMA issued so far
+            // has finished (also after an abort, so TMEM can be freed)
+            if (any) umma_commit(acc_bar);
+            else mbar_arrive(acc_bar);
+        }
+        __syncwarp();
+    } else {
+        const int quarter = warp & 3;
+        const int t = m0 + quarter * 32 + lane;
+        bool w = true;
+        if (lane == 0) w = mbar_wait(acc_bar, 0, abort_flag, a.dev_err);
+        w = __shfl_sync(0xffffffffu, w, 0);
+        tc_fence_after();
+        if (w && !*abort_flag) {
+            float* row = a.out + (static_cast<size_t>(a.S == 1 ? 0 : s) * a.T + t) * a.E;
+            for (int c0 = 0; c0 < N; c0 += 32) {
+                uint32_t v[32];
+                tmem_ld32(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + c0, v);
+                tmem_ld_wait();
+                if (t < a.T) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int e = n0 + c0 + j;
+                        if (c0 + j < N && e < a.E) row[e] = __uint_as_float(v[j]);
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, tmem_cols);
+    }
+}
+
+// logits[i] = sum over s ascending of partial[s][i], i over T*E.
+__global__ void k_router_reduce(const float* __restrict__ partial, int S, long long n,
+                                float* __restrict__ logits) {
+    const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    float acc = partial[i];
+    for (int s = 1; s < S; ++s) acc += partial[static_cast<size_t>(s) * n + i];
+    logits[i] = acc;
+}
+
+}  // namespace
+
+RouterPlan router_plan(int T, int H, int E, int num_sms) {
+    RouterPlan p{};
+    p.N = E >= 256 ? 256 : ((E + 15) / 16) * 16;
+    p.m_tiles = (T + 127) / 128;
+    p.n_tiles = (E + p.N - 1) / p.N;
+    p.KB = H / 64;
+    // enough K chunks to fill about one wave, but at least four k-blocks per
+    // chunk (a CTA's fixed cost -- barriers, TMEM, the first TMA round trip --
+    // is that of a few k-blocks, and every chunk adds a partial to the sum)
+    const long long tiles = static_cast<long long>(p.m_tiles) * p.n_tiles;
+    long long S = tiles > 0 ? (num_sms + tiles - 1) / tiles : 1;
+    if (S > p.KB / 4) S = p.KB / 4;
+    if (S < 1) S = 1;
+    p.S = static_cast<int>(S);
+    p.partial_bytes = p.S > 1 ? static_cast<size_t>(p.S) * T * E * sizeof(float) : 0;
+    return p;
+}
+
+cudaError_t launch_router_logits(const void* X, int T, int H, const void* W_r, int E, float* logits,
+                                 float* partial, const RouterPlan& p, int* dev_err,
+                                 cudaStream_t stream) {
+    if (T == 0) return cudaSuccess;
+    // boxes no taller than the tensors; the MMA still reads 128 x N rows, the
+    // rows past T or E hold stale data whose results are never stored
+    CUtensorMap tm_x, tm_w;
+    const CUtensorMapDataType BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const uint32_t box_x = static_cast<uint32_t>(T < 128 ? T : 128);
+    const uint32_t box_w = static_cast<uint32_t>(E < p.N ? E : p.N);
+    if (encode_tmap_2d(&tm_x, BF, X, static_cast<uint64_t>(H), static_cast<uint64_t>(T),
+                       static_cast<uint64_t>(H) * 2, 64, box_x) != CUDA_SUCCESS ||
+        encode_tmap_2d(&tm_w, BF, W_r, static_cast<uint64_t>(H), static_cast<uint64_t>(E),
+                       static_cast<uint64_t>(H) * 2, 64, box_w) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    const size_t smem = router_smem_bytes(p.N);
+    cudaError_t rc = cudaFuncSetAttribute(k_router_partial, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          static_cast<int>(smem));
+    if (rc != cudaSuccess) return rc;
+    RouterArgs args;
+    args.out = p.S > 1 ? partial : logits;
+    args.dev_err = dev_err;
+    args.T = T;
+    args.E = E;
+    args.KB = p.KB;
+    args.S = p.S;
+    args.N = p.N;
+    args.tx_bytes = (box_x + box_w) * 128u;
+    k_router_partial<<<dim3(p.m_tiles, p.n_tiles, p.S), kRThreads, smem, stream>>>(tm_x, tm_w, args);
+    rc = cudaGetLastError();
+    if (rc != cudaSuccess || p.S == 1) return rc;
+    const long long n = static_cast<long long>(T) * E;
+    k_router_reduce<<<static_cast<unsigned>((n + 255) / 256), 256, 0, stream>>>(partial, p.S, n, logits);
+    return cudaGetLastError();
+}
+
+}  // namespace es
+
+// ----------------------------------------------------------------------------
+// C ABI
+// ----------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kRouterErrBytes = 256;  // error word, then the partial sums
+
+int router_current_sms() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+
+bool router_shape_ok(int T, int H, int E) {
+    return T >= 0 && H >= 64 && H % 64 == 0 && E >= 1 && E <= es::kMaxE;
+}
+
+bool router_aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+
+extern "C" size_t estream_router_workspace_bytes(int T, int H, int E) {
+    if (!router_shape_ok(T, H, E)) return 0;
+    const int sms = router_current_sms();
+    if (sms <= 0) return 0;
+    return kRouterErrBytes + es::router_plan(T, H, E, sms).partial_bytes;
+}
+
+extern "C" estream_status estream_router_logits(const void* X, int T, int H, const void* W_r, int E,
+                                                float* logits, void* workspace,
+                                                size_t workspace_bytes, void* cuda_stream) {
+    if (!router_shape_ok(T, H, E) || !workspace || !router_aligned(workspace, 256))
+        return ESTREAM_ERR_INVALID_ARG;
+    if (T > 0 && (!X || !W_r || !logits || !router_aligned(X, 16) || !router_aligned(W_r, 16) ||
+                  !router_aligned(logits, 4)))
+        return ESTREAM_ERR_INVALID_ARG;
+    int dev = 0, major = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess)
+        return ESTREAM_ERR_CUDA;
+    if (major != 10) return ESTREAM_ERR_UNSUPPORTED;
+    const int sms = router_current_sms();
+    if (sms <= 0) return ESTREAM_ERR_CUDA;
+    const es::RouterPlan plan = es::router_plan(T, H, E, sms);
+    if (workspace_bytes < kRouterErrBytes + plan.partial_bytes) return ESTREAM_ERR_CAPACITY;
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    char* ws = static_cast<char*>(workspace);
+    if (cudaMemsetAsync(ws, 0, sizeof(int), s) != cudaSuccess) return ESTREAM_ERR_CUDA;
+    const cudaError_t rc = es::launch_router_logits(X, T, H, W_r, E, logits,
+                                                    reinterpret_cast<float*>(ws + kRouterErrBytes),
+                                                    plan, reinterpret_cast<int*>(ws), s);
+    return rc == cudaSuccess ? ESTREAM_OK : ESTREAM_ERR_CUDA;
+}

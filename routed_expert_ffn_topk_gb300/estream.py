@@ -72,6 +72,8 @@ SIGNATURES = {
     "estream_route_build": (_I, [_P, _I, _I, _I, _I, _P, _I, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "estream_workspace_error": (_I, [_P, _P]),
     "estream_route_build_noalloc": (_I, [_P, _I, _I, _I, _I, _P, _I, _P, _P, _P, _P, _P, _P]),
+    "estream_router_workspace_bytes": (_SZ, [_I, _I, _I]),
+    "estream_router_logits": (_I, [_P, _I, _I, _P, _I, _P, _P, _SZ, _P]),
     "estream_arena_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "estream_pool_bytes": (_SZ, [_I, _I, _I, _I]),
     "estream_shared_bytes": (_SZ, [_I, _I, _I, _I]),
@@ -175,6 +177,26 @@ def route_build(logits: torch.Tensor, k: int, renorm: bool, phi: torch.Tensor | 
     _check(st, "estream_route_build")
     o["workspace"] = workspace
     return o
+
+
+def router_workspace_bytes(T: int, H: int, E: int) -> int:
+    return lib().estream_router_workspace_bytes(T, H, E)
+
+
+def router_logits(X: torch.Tensor, W_r: torch.Tensor, logits: torch.Tensor | None = None,
+                  workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """estream_router_logits: logits [T, E] fp32 = X [T, H] bf16 @ W_r [E, H] bf16 ^T."""
+    T, H = X.shape
+    E = W_r.shape[0]
+    if logits is None:
+        logits = torch.empty(T, E, dtype=torch.float32, device=X.device)
+    if workspace is None:
+        workspace = torch.empty(max(router_workspace_bytes(T, H, E), 256), dtype=torch.uint8,
+                                device=X.device)
+    st = lib().estream_router_logits(_dptr(X), T, H, _dptr(W_r), E, _dptr(logits), _dptr(workspace),
+                                     workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "estream_router_logits")
+    return logits
 
 
 def route_build_noalloc(logits: torch.Tensor, k: int, renorm: bool, phi: torch.Tensor | None = None,

@@ -73,6 +73,23 @@ class BoundLayerStack:
         es.moe_layer_prefill(self.ctx, layer, X, logits, cfg.k if k is None else k,
                              cfg.renorm if renorm is None else renorm, Y, stream)
 
+    def prefill_from_router(self, layer: int, X: torch.Tensor, W_r: torch.Tensor, Y: torch.Tensor,
+                            k=None, renorm=None, stream=None) -> torch.Tensor:
+        """Router logits = X W_r^T (estream_router_logits), then the layer call;
+        returns the logits (kept in a buffer reused across calls)."""
+        T = X.shape[0]
+        E = W_r.shape[0]
+        buf = getattr(self, "_router_buf", None)
+        if buf is None or buf[0].shape[0] < T * E or buf[1].device != X.device:
+            ws_bytes = max(es.router_workspace_bytes(self.T_max, X.shape[1], E), 256)
+            buf = (torch.empty(self.T_max * E, dtype=torch.float32, device=X.device),
+                   torch.empty(ws_bytes, dtype=torch.uint8, device=X.device))
+            self._router_buf = buf
+        logits = buf[0][:T * E].view(T, E)
+        es.router_logits(X, W_r, logits=logits, workspace=buf[1], stream=stream)
+        self.prefill(layer, X, logits, Y, k=k, renorm=renorm, stream=stream)
+        return logits
+
     def close(self) -> None:
         if getattr(self, "ctx", None):
             es.unbind(self.ctx)

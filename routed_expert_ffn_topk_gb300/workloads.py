@@ -116,6 +116,16 @@ class Workload:
     layers: list              # per layer LayerWeights
 
 
+def make_router(T: int, H: int, E: int, seed: int, dtype=torch.bfloat16):
+    """Seeded inputs of the router upstream of the top-k, drawn from their own
+    generator (so the layer workloads' draws are unchanged): X [T, H] ~ N(0, 1)
+    and W_r [E, H] ~ N(0, 1/H), giving logits of about unit variance."""
+    gen = torch.Generator().manual_seed(seed)
+    X = torch.randn((T, H), generator=gen, dtype=torch.float32).to(dtype)
+    W_r = (torch.randn((E, H), generator=gen, dtype=torch.float32) / math.sqrt(H)).to(dtype)
+    return X, W_r
+
+
 def _randn(gen, shape, std, dtype):
     return (torch.randn(shape, generator=gen, dtype=torch.float32) * std).to(dtype)
 
