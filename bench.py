@@ -438,7 +438,7 @@ def measure_router(cfg, X0, dev, stream, flush, peaks, steps):
     t = sorted(ms)[len(ms) // 2]
     nbytes = T * H * 2 + E * H * 2 + T * E * 4
     gbs = nbytes / (t / 1e3) / 1e9
-    return {"kernel": "k_router_partial + k_router_reduce (tcgen05, split-K, fixed-order sum)",
+    return {"kernel": "k_router_partial (tcgen05, K split over a CTA cluster, fixed-order DSMEM sum)",
             "ms": round(t, 4), "algorithmic_bytes": nbytes, "GBps": round(gbs, 1),
             "frac_hbm": round(gbs / peaks["hbm_gbs"], 4),
             "TFLOPs": round(2.0 * T * H * E / (t / 1e3) / 1e12, 1),

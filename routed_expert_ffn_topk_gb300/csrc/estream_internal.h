@@ -106,16 +106,15 @@ cudaError_t launch_combine(const float* rows, const int32_t* pos, int T, int k, 
                            cudaStream_t stream);
 
 // Router logits l[T][E] = X[T][H] W_r[E][H]^T (bf16 in, fp32 out) on the
-// tensor cores, K split S ways; S > 1 needs partial_bytes of device scratch.
+// tensor cores, K split S <= 8 ways across the CTAs of one cluster.
 struct RouterPlan {
     int N;              // experts per tile (multiple of 16, <= 256)
     int m_tiles, n_tiles, KB, S;
-    size_t partial_bytes;
+    size_t partial_bytes;  // device scratch beyond the error word (0)
 };
 RouterPlan router_plan(int T, int H, int E, int num_sms);
 cudaError_t launch_router_logits(const void* X, int T, int H, const void* W_r, int E, float* logits,
-                                 float* partial, const RouterPlan& p, int* dev_err,
-                                 cudaStream_t stream);
+                                 const RouterPlan& p, int* dev_err, cudaStream_t stream);
 
 cudaError_t launch_cast_f32_bf16(const float* src, void* dst, size_t n, cudaStream_t stream);
 

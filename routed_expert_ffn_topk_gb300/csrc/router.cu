@@ -8,13 +8,15 @@
 //
 // GB300 form. The contraction is [T, H] x [H, E] with E small (8..1024), so
 // one 128-token tile per CTA would leave most SMs idle. The K range is split
-// into S chunks so that about one wave of CTAs covers the GPU: CTA (m, n, s)
-// multiplies tokens [128m, 128m+128) by experts [N n, N n + N) over its
-// k-blocks with tcgen05.mma.kind::f16 (bf16, fp32 accumulate in TMEM), both
-// operands TMA-loaded with 128-byte swizzle through a 4-stage ring, and
-// stores its fp32 partial sums. A second kernel adds the S partials of every
-// logit in ascending s, so the logits do not depend on timing. With S = 1
-// the partial kernel writes the logits directly.
+// into S <= 8 chunks so that about one wave of CTAs covers the GPU: CTA
+// (m, n, s) multiplies tokens [128m, 128m+128) by experts [N n, N n + N)
+// over its k-blocks with tcgen05.mma.kind::f16 (bf16, fp32 accumulate in
+// TMEM), both operands TMA-loaded with 128-byte swizzle through a 4-stage
+// ring. The S CTAs of a tile form one thread-block cluster: each stages its
+// fp32 partial in its own shared memory, and after a cluster barrier CTA s
+// adds, for its slice of the tile's rows, the S partials read through
+// distributed shared memory in ascending chunk order -- one kernel, no
+// partial sums in HBM, and logits that do not depend on timing.
 // Warp roles: warp 0 TMA producer, warp 1 TMEM allocation and the MMA issue,
 // warps 2-5 epilogue (TMEM lanes = tokens). Every wait is bounded.
 #include <cuda.h>
@@ -30,13 +32,26 @@ namespace {
 constexpr int kRStages = 4;
 constexpr int kRThreads = 192;
 constexpr int kRTileA = 128 * 128;  // 128 tokens x 64 bf16
+constexpr int kRMaxSplit = 8;       // portable cluster size
 
 struct RouterArgs {
-    float* out;        // [S][T][E] partials, or [T][E] logits when S == 1
-    int* dev_err;      // optional
+    float* logits;      // [T][E]
+    int* dev_err;       // optional
     int T, E, KB, S, N;
     uint32_t tx_bytes;  // bytes one stage's two boxes deliver
 };
+
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                     : "memory");
+}
+__device__ __forceinline__ float ld_cluster_f32(uint32_t local_addr, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    return v;
+}
 
 size_t router_smem_bytes(int N) {
     return 1024 + static_cast<size_t>(kRStages) * (kRTileA + N * 128) + 8 * (2 * kRStages + 1) + 16;
@@ -137,44 +152,51 @@ __global__ void __launch_bounds__(kRThreads, 1)
         }
         __syncwarp();
     } else {
+        // the tile's partial sums into this CTA's shared memory (the stage
+        // buffers are free once every MMA has completed), rows padded by one
+        // float against bank conflicts
         const int quarter = warp & 3;
-        const int t = m0 + quarter * 32 + lane;
+        const int row = quarter * 32 + lane;
         bool w = true;
         if (lane == 0) w = mbar_wait(acc_bar, 0, abort_flag, a.dev_err);
         w = __shfl_sync(0xffffffffu, w, 0);
         tc_fence_after();
         if (w && !*abort_flag) {
-            float* row = a.out + (static_cast<size_t>(a.S == 1 ? 0 : s) * a.T + t) * a.E;
+            float* part = reinterpret_cast<float*>(smem) + row * (N + 1);
             for (int c0 = 0; c0 < N; c0 += 32) {
                 uint32_t v[32];
                 tmem_ld32(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + c0, v);
                 tmem_ld_wait();
-                if (t < a.T) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int e = n0 + c0 + j;
-                        if (c0 + j < N && e < a.E) row[e] = __uint_as_float(v[j]);
-                    }
-                }
+                for (int j = 0; j < 32; ++j)
+                    if (c0 + j < N) part[c0 + j] = __uint_as_float(v[j]);
             }
         }
     }
     tc_fence_before();
     __syncthreads();
+    cluster_sync_all();  // every chunk's partial is in place
+    {
+        // CTA s of the cluster sums rows [r0, r1) of the tile over the chunks
+        const int rows_per = (128 + a.S - 1) / a.S;
+        const int r0 = s * rows_per;
+        const int r1 = min(128, r0 + rows_per);
+        const bool ok = !*abort_flag;
+        for (int i = threadIdx.x; ok && i < (r1 - r0) * N; i += kRThreads) {
+            const int r = r0 + i / N, c = i % N;
+            const int t = m0 + r, e = n0 + c;
+            if (t >= a.T || e >= a.E) continue;
+            const uint32_t off = sbase + static_cast<uint32_t>((r * (N + 1) + c) * 4);
+            float acc = ld_cluster_f32(off, 0);
+            for (int q = 1; q < a.S; ++q) acc += ld_cluster_f32(off, static_cast<uint32_t>(q));
+            a.logits[static_cast<size_t>(t) * a.E + e] = acc;
+        }
+    }
+    cluster_sync_all();  // no CTA leaves while its partial may still be read
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem_base, tmem_cols);
     }
-}
-
-// logits[i] = sum over s ascending of partial[s][i], i over T*E.
-__global__ void k_router_reduce(const float* __restrict__ partial, int S, long long n,
-                                float* __restrict__ logits) {
-    const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (i >= n) return;
-    float acc = partial[i];
-    for (int s = 1; s < S; ++s) acc += partial[static_cast<size_t>(s) * n + i];
-    logits[i] = acc;
 }
 
 }  // namespace
@@ -191,15 +213,15 @@ RouterPlan router_plan(int T, int H, int E, int num_sms) {
     const long long tiles = static_cast<long long>(p.m_tiles) * p.n_tiles;
     long long S = tiles > 0 ? (num_sms + tiles - 1) / tiles : 1;
     if (S > p.KB / 4) S = p.KB / 4;
+    if (S > kRMaxSplit) S = kRMaxSplit;
     if (S < 1) S = 1;
     p.S = static_cast<int>(S);
-    p.partial_bytes = p.S > 1 ? static_cast<size_t>(p.S) * T * E * sizeof(float) : 0;
+    p.partial_bytes = 0;  // partial sums stay in shared memory
     return p;
 }
 
 cudaError_t launch_router_logits(const void* X, int T, int H, const void* W_r, int E, float* logits,
-                                 float* partial, const RouterPlan& p, int* dev_err,
-                                 cudaStream_t stream) {
+                                 const RouterPlan& p, int* dev_err, cudaStream_t stream) {
     if (T == 0) return cudaSuccess;
     // boxes no taller than the tensors; the MMA still reads 128 x N rows, the
     // rows past T or E hold stale data whose results are never stored
@@ -217,7 +239,7 @@ cudaError_t launch_router_logits(const void* X, int T, int H, const void* W_r, i
                                           static_cast<int>(smem));
     if (rc != cudaSuccess) return rc;
     RouterArgs args;
-    args.out = p.S > 1 ? partial : logits;
+    args.logits = logits;
     args.dev_err = dev_err;
     args.T = T;
     args.E = E;
@@ -225,11 +247,22 @@ cudaError_t launch_router_logits(const void* X, int T, int H, const void* W_r, i
     args.S = p.S;
     args.N = p.N;
     args.tx_bytes = (box_x + box_w) * 128u;
-    k_router_partial<<<dim3(p.m_tiles, p.n_tiles, p.S), kRThreads, smem, stream>>>(tm_x, tm_w, args);
-    rc = cudaGetLastError();
-    if (rc != cudaSuccess || p.S == 1) return rc;
-    const long long n = static_cast<long long>(T) * E;
-    k_router_reduce<<<static_cast<unsigned>((n + 255) / 256), 256, 0, stream>>>(partial, p.S, n, logits);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 1;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = static_cast<unsigned>(p.S);
+    cfg.gridDim = dim3(static_cast<unsigned>(p.m_tiles), static_cast<unsigned>(p.n_tiles),
+                       static_cast<unsigned>(p.S));
+    cfg.blockDim = dim3(kRThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    void* kargs[] = {&tm_x, &tm_w, &args};
+    rc = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(k_router_partial), kargs);
+    if (rc != cudaSuccess) return rc;
     return cudaGetLastError();
 }
 
@@ -240,7 +273,7 @@ cudaError_t launch_router_logits(const void* X, int T, int H, const void* W_r, i
 // ----------------------------------------------------------------------------
 namespace {
 
-constexpr size_t kRouterErrBytes = 256;  // error word, then the partial sums
+constexpr size_t kRouterErrBytes = 256;  // the error word
 
 int router_current_sms() {
     int dev = 0, n = 0;
@@ -284,8 +317,7 @@ extern "C" estream_status estream_router_logits(const void* X, int T, int H, con
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
     char* ws = static_cast<char*>(workspace);
     if (cudaMemsetAsync(ws, 0, sizeof(int), s) != cudaSuccess) return ESTREAM_ERR_CUDA;
-    const cudaError_t rc = es::launch_router_logits(X, T, H, W_r, E, logits,
-                                                    reinterpret_cast<float*>(ws + kRouterErrBytes),
-                                                    plan, reinterpret_cast<int*>(ws), s);
+    const cudaError_t rc =
+        es::launch_router_logits(X, T, H, W_r, E, logits, plan, reinterpret_cast<int*>(ws), s);
     return rc == cudaSuccess ? ESTREAM_OK : ESTREAM_ERR_CUDA;
 }
