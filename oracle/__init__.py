@@ -5,4 +5,4 @@ CPU-baseline leg; the product library never touches it.
 """
 from .oracle import (build, load, exp_f32, route_topk, route_csr,  # noqa: F401
                      grouped_placement, moe_layer_rows, num_threads, maxplus,
-                     router_logits)
+                     router_logits, down_scale_exp, q4_quantize, q4_dequantize)

@@ -215,6 +215,123 @@ static double load_elem(const void* base, size_t idx, int bf16)
 
 static double silu(double z) { return z / (1.0 + exp(-z)); }
 
+/* ------------------------------------------------------------------------ */
+/* 4-bit expert weights (weight-only Q4_0-style block quantisation)          */
+/* ------------------------------------------------------------------------ */
+
+/* Section 4 ("Numerical representation") stores expert matrices as weight-only
+ * GGUF Q4_0: blocks of 32 consecutive weights along the reduction dimension,
+ * one scale per block, a 4-bit code per weight with offset 8. Reading used
+ * here (the pages give only the format's name):
+ *   m   = the block's element of largest magnitude (the first one on ties);
+ *   d   = m / -8, rounded to 5 significant bits (round to nearest, ties to
+ *         even), then to the matrix-operand type (bf16, or fp16 when fp16 is
+ *         set) -- with at most 5 significant bits in d, every (q - 8) * d is
+ *         exact in either type;
+ *   q_j = clamp(rint(x_j / d) + 8, 0, 15)   (fp32 division, ties to even);
+ *   a block of zeros has d = 0 and every q_j = 8.
+ * The weight the layer uses is w_j = (q_j - 8) * d. For a down plane the
+ * weights are first multiplied by 2^s, s = 15 - e where the plane's largest
+ * magnitude is f * 2^e with f in [0.5, 1) (s = 0 for an all-zero plane), and
+ * the dequantised weight is divided by 2^s again. */
+
+static float round_sig5(float x)
+{
+    union { float f; uint32_t u; } v;
+    v.f = x;
+    const uint32_t drop = 19;                    /* keep 1 implicit + 4 stored bits */
+    const uint32_t half = 1u << (drop - 1);
+    const uint32_t lsb = (v.u >> drop) & 1u;
+    v.u = (v.u + half - 1u + lsb) & ~((1u << drop) - 1u);
+    return v.f;
+}
+
+static float to_bf16_rne(float x)
+{
+    union { float f; uint32_t u; } v;
+    v.f = x;
+    v.u = (v.u + 0x7FFFu + ((v.u >> 16) & 1u)) & 0xFFFF0000u;
+    return v.f;
+}
+
+/* fp16 round to nearest even, returned as the fp32 of the fp16 value
+ * (finite inputs below 65520 in magnitude). */
+static float to_fp16_rne(float x)
+{
+    const double ax = fabs((double)x);
+    if (ax == 0.0) return x;
+    int e;
+    frexp(ax, &e);                      /* ax = f * 2^e, f in [0.5, 1) */
+    int q = e - 11;                     /* quantum of an 11-bit significand */
+    if (q < -24) q = -24;               /* subnormal range: fixed quantum 2^-24 */
+    const double scaled = ldexp(ax, -q);
+    double r = nearbyint(scaled);       /* default rounding mode: ties to even */
+    const double out = ldexp(r, q);
+    return (float)(x < 0 ? -out : out);
+}
+
+int oracle_down_scale_exp(const void* w, size_t n, int bf16)
+{
+    double mx = 0.0;
+    for (size_t i = 0; i < n; ++i) {
+        const double a = fabs(load_elem(w, i, bf16));
+        if (a > mx) mx = a;
+    }
+    if (mx == 0.0) return 0;
+    int e;
+    frexp(mx, &e);
+    return 15 - e;
+}
+
+/* Quantise a [rows][cols] matrix (cols % 32 == 0) row by row along cols.
+ * codes: [rows][cols] bytes 0..15; d: [rows][cols/32] fp32 (the stored scale,
+ * widened exactly); scale_exp s multiplies the weights by 2^s first. */
+int oracle_q4_quantize(const void* w, int rows, int cols, int bf16, int scale_exp, int fp16,
+                       uint8_t* codes, float* d)
+{
+    if (rows < 0 || cols < 32 || cols % 32 != 0 || !w || !codes || !d) return -1;
+    const int nb = cols / 32;
+    for (int r = 0; r < rows; ++r)
+        for (int b = 0; b < nb; ++b) {
+            float x[32];
+            float m = 0.0f;
+            for (int j = 0; j < 32; ++j) {
+                x[j] = (float)ldexp(load_elem(w, (size_t)r * cols + (size_t)b * 32 + j, bf16), scale_exp);
+                if (fabsf(x[j]) > fabsf(m)) m = x[j];
+            }
+            float dd = 0.0f;
+            if (m != 0.0f) {
+                dd = round_sig5(m / -8.0f);
+                dd = fp16 ? to_fp16_rne(dd) : to_bf16_rne(dd);
+            }
+            d[(size_t)r * nb + b] = dd;
+            for (int j = 0; j < 32; ++j) {
+                int q = 8;
+                if (dd != 0.0f) {
+                    q = (int)rintf(x[j] / dd) + 8;
+                    if (q < 0) q = 0;
+                    if (q > 15) q = 15;
+                }
+                codes[(size_t)r * cols + (size_t)b * 32 + j] = (uint8_t)q;
+            }
+        }
+    return 0;
+}
+
+/* w[r][c] = (codes[r][c] - 8) * d[r][c/32] * 2^-scale_exp, in fp32 (exact). */
+int oracle_q4_dequantize(const uint8_t* codes, const float* d, int rows, int cols, int scale_exp,
+                         float* w)
+{
+    if (rows < 0 || cols < 32 || cols % 32 != 0 || !codes || !d || !w) return -1;
+    const int nb = cols / 32;
+    for (int r = 0; r < rows; ++r)
+        for (int c = 0; c < cols; ++c)
+            w[(size_t)r * cols + c] =
+                (float)ldexp(((double)codes[(size_t)r * cols + c] - 8.0) * (double)d[(size_t)r * nb + c / 32],
+                             -scale_exp);
+    return 0;
+}
+
 /* Router logits upstream of the top-k (the layer input X_t mapped to one
  * score per expert; the pages name the router and its top-k selection in
  * section 1 and list a routing operator among the NPU operators in section 4,

@@ -68,6 +68,12 @@ def _declare(lib) -> None:
     lib.oracle_maxplus.restype = ctypes.c_double
     lib.oracle_router_logits.argtypes = [P, i, i, P, i, i, P]
     lib.oracle_router_logits.restype = i
+    lib.oracle_down_scale_exp.argtypes = [P, ctypes.c_size_t, i]
+    lib.oracle_down_scale_exp.restype = i
+    lib.oracle_q4_quantize.argtypes = [P, i, i, i, i, i, P, P]
+    lib.oracle_q4_quantize.restype = i
+    lib.oracle_q4_dequantize.argtypes = [P, P, i, i, i, P]
+    lib.oracle_q4_dequantize.restype = i
 
 
 def load(path: str | None = None):
@@ -229,6 +235,40 @@ def router_logits(X, W_r, lib=None) -> np.ndarray:
     if lib.oracle_router_logits(_ptr(Xa), T, H, _ptr(Wa), E, bx, _ptr(out)) != 0:
         raise ValueError("oracle_router_logits: bad arguments")
     return out
+
+
+def down_scale_exp(W, lib=None) -> int:
+    """The power-of-two exponent s applied to a down plane before it is
+    quantised or converted (its largest magnitude lands in [2^14, 2^15))."""
+    lib = lib or load()
+    a, b = _as_weight(W)
+    return lib.oracle_down_scale_exp(_ptr(a), a.size, b)
+
+
+def q4_quantize(W, fp16: bool, scale_exp: int = 0, lib=None):
+    """Q4_0-style block quantisation of a [rows][cols] matrix along cols:
+    (codes [rows][cols] uint8 in 0..15, d [rows][cols/32] fp32)."""
+    lib = lib or load()
+    a, b = _as_weight(W)
+    rows, cols = a.shape
+    codes = np.zeros((rows, cols), dtype=np.uint8)
+    d = np.zeros((rows, cols // 32), dtype=np.float32)
+    if lib.oracle_q4_quantize(_ptr(a), rows, cols, b, scale_exp, int(bool(fp16)), _ptr(codes),
+                              _ptr(d)) != 0:
+        raise ValueError("oracle_q4_quantize: bad arguments")
+    return codes, d
+
+
+def q4_dequantize(codes, d, scale_exp: int = 0, lib=None) -> np.ndarray:
+    """w = (q - 8) * d * 2^-scale_exp as fp32."""
+    lib = lib or load()
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    d = np.ascontiguousarray(d, dtype=np.float32)
+    rows, cols = codes.shape
+    w = np.zeros((rows, cols), dtype=np.float32)
+    if lib.oracle_q4_dequantize(_ptr(codes), _ptr(d), rows, cols, scale_exp, _ptr(w)) != 0:
+        raise ValueError("oracle_q4_dequantize: bad arguments")
+    return w
 
 
 def num_threads(lib=None) -> int:

@@ -380,5 +380,70 @@ def pin_router(lib):
                                   O.router_logits(_bf16_widen(Xb), _bf16_widen(Wb), lib=lib))
 
 
+# --------------------------------------------------------------------------
+# 4-bit expert weights
+# --------------------------------------------------------------------------
+
+def pin_q4_golden(lib):
+    """The hand-worked blocks of tests/golden/q4_block_example.txt, in both
+    operand types (every scale there is exact in bf16 and fp16)."""
+    fx = _read_golden("q4_block_example.txt")
+    A = np.array([((j % 16) - 8) / 8.0 for j in range(32)], dtype=np.float32)
+    B = np.zeros(32, dtype=np.float32)
+    B[:6] = np.array(fx["B_x"], dtype=np.float32)
+    C = np.zeros(32, dtype=np.float32)
+    for fp16 in (False, True):
+        codes, d = O.q4_quantize(np.stack([A, B, C]), fp16=fp16, lib=lib)
+        for row, key in enumerate("ABC"):
+            assert d[row, 0] == np.float32(fx[key + "_d"][0]), (key, d[row, 0])
+            np.testing.assert_array_equal(codes[row], fx[key + "_q"])
+        w = O.q4_dequantize(codes, d, lib=lib)
+        np.testing.assert_array_equal(w[0], A)          # block A lies on its grid
+        np.testing.assert_array_equal(w[2], C)
+    assert O.down_scale_exp(np.array([[0.77, -0.5]], dtype=np.float32), lib=lib) == fx["s_for_0.77"][0]
+    assert O.down_scale_exp(np.array([[-1.0, 0.25]], dtype=np.float32), lib=lib) == fx["s_for_1.0"][0]
+
+
+def pin_q4_properties(lib):
+    """Random blocks: every element whose code is not clamped lies within d/2
+    of its dequantised value; codes in 0..15 and the largest element within
+    8 |d - m/-8| of -8 d; a block already on a 5-bit grid is reproduced
+    exactly; scaling a block by 2^k scales d by 2^k and keeps the codes;
+    negating it negates d and keeps the codes; the pre-scale 2^s of a down
+    plane is undone by the dequantiser."""
+    rng = _rng(12)
+    W = (rng.standard_normal((16, 128)) * 0.02).astype(np.float32)
+    for fp16 in (False, True):
+        codes, d = O.q4_quantize(W, fp16=fp16, lib=lib)
+        assert codes.max() <= 15
+        w = O.q4_dequantize(codes, d, lib=lib).astype(np.float64)
+        dd = np.repeat(np.abs(d.astype(np.float64)), 32, axis=1)
+        inner = (codes > 0) & (codes < 15)
+        assert np.all(np.abs(w - W)[inner] <= dd[inner] / 2 * (1 + 1e-6))
+        blocks = W.reshape(16, 4, 32)
+        m = np.take_along_axis(blocks, np.abs(blocks).argmax(axis=2)[..., None], axis=2)[..., 0]
+        assert np.all(np.abs(m / -8 - d) <= np.abs(m / -8) * 2.0 ** -5 * (1 + 1e-6))
+        c2, d2 = O.q4_quantize(W * 4, fp16=fp16, lib=lib)
+        np.testing.assert_array_equal(c2, codes)
+        np.testing.assert_array_equal(d2, d * 4)
+        c3, d3 = O.q4_quantize(-W, fp16=fp16, lib=lib)
+        np.testing.assert_array_equal(c3, codes)
+        np.testing.assert_array_equal(d3, -d)
+    grid_d = np.float32(-1.0625 * 2.0 ** -6)                 # 5 significant bits
+    q = rng.integers(0, 16, (2, 32))
+    q[:, 0] = 0                                               # the block maximum is -8 d
+    G = ((q - 8) * grid_d).astype(np.float32)
+    cg, dg = O.q4_quantize(G, fp16=False, lib=lib)
+    np.testing.assert_array_equal(cg, q)
+    np.testing.assert_array_equal(O.q4_dequantize(cg, dg, lib=lib), G)
+    s = O.down_scale_exp(W, lib=lib)
+    cs, ds = O.q4_quantize(W, fp16=True, scale_exp=s, lib=lib)
+    ws = O.q4_dequantize(cs, ds, scale_exp=s, lib=lib).astype(np.float64)
+    dd = np.repeat(np.abs(ds.astype(np.float64)), 32, axis=1) * 2.0 ** -s
+    inner = (cs > 0) & (cs < 15)
+    assert np.all(np.abs(ws - W)[inner] <= dd[inner] / 2 * (1 + 1e-6))
+
+
 ALL_PINS = [pin_exp, pin_topk, pin_topk_golden, pin_csr, pin_csr_golden, pin_placement,
-            pin_layer_dense, pin_layer_textbook, pin_layer_special, pin_maxplus, pin_router]
+            pin_layer_dense, pin_layer_textbook, pin_layer_special, pin_maxplus, pin_router,
+            pin_q4_golden, pin_q4_properties]

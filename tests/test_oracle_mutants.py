@@ -43,6 +43,13 @@ MUTANTS = {
     "maxplus_no_serial_exec": ("if (f[k - 1] > s) s = f[k - 1];   /* f[0] = 0 */", "(void)0;"),
     "maxplus_ignores_nonexpert": ("if (T_ne > s) s = T_ne;", "(void)0;"),
     "router_w_transposed": ("load_elem(W_r, (size_t)e * H + h, bf16)", "load_elem(W_r, (size_t)h * E + e, bf16)"),
+    "q4_divisor_7": ("dd = round_sig5(m / -8.0f);", "dd = round_sig5(m / -7.0f);"),
+    "q4_scale_not_rounded": ("dd = round_sig5(m / -8.0f);", "dd = m / -8.0f;"),
+    "q4_truncating_code": ("q = (int)rintf(x[j] / dd) + 8;", "q = (int)(x[j] / dd) + 8;"),
+    "q4_no_upper_clamp": ("if (q > 15) q = 15;", "(void)0;"),
+    "q4_offset_7": ("((double)codes[(size_t)r * cols + c] - 8.0)", "((double)codes[(size_t)r * cols + c] - 7.0)"),
+    "q4_last_of_ties": ("if (fabsf(x[j]) > fabsf(m)) m = x[j];", "if (fabsf(x[j]) >= fabsf(m)) m = x[j];"),
+    "down_scale_off_by_one": ("return 15 - e;", "return 14 - e;"),
     "router_first_term_dropped": ("for (int h = 0; h < H; ++h)\n                acc +=",
                                   "for (int h = 1; h < H; ++h)\n                acc +="),
 }
