@@ -384,6 +384,9 @@ def run_ours(args, rank, world, local_rank):
     # ---- router logits upstream of the top-k (its own kernel, not part of the step) ----
     router = measure_router(cfg, X0, dev, stream, flush, peaks, args.steps) if cfg.dtype == "bf16" else None
 
+    # ---- the same layer with 4-bit experts ----
+    q4 = measure_q4(args, cfg, wl, dev, stream, flush, peaks) if cfg.dtype == "bf16" and not args.no_q4 else None
+
     # ---- arena-paged run of the same config (host-link bound) ----
     paged = measure_paged(args, cfg, wl, dev, stream, flush, peaks) if not args.no_paged else None
     if paged is not None and args.pipeline_study and cfg.layers == 1:
@@ -406,6 +409,7 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": gpu_launches,
         "clocks": clocks.summary(),
         "router": router,
+        "q4": q4,
         "paged": paged,
     }
     return line
@@ -443,6 +447,67 @@ def measure_router(cfg, X0, dev, stream, flush, peaks, steps):
             "frac_hbm": round(gbs / peaks["hbm_gbs"], 4),
             "TFLOPs": round(2.0 * T * H * E / (t / 1e3) / 1e12, 1),
             "workspace_bytes": int(ws.numel())}
+
+
+def measure_q4(args, cfg, wl, dev, stream, flush, peaks):
+    """The same layer (layer 0) with 4-bit experts (ESTREAM_Q4): resident,
+    timed like the main step, with the fused kernel's roofline from the
+    packed weight bytes (3*H*F*9/16 per active expert) + X + Y; and paged
+    through the config's arena, every group streamed (arena invalidated)."""
+    import torch
+
+    from routed_expert_ffn_topk_gb300 import estream as es
+    from routed_expert_ffn_topk_gb300 import workloads as W
+    from routed_expert_ffn_topk_gb300.layer import BoundLayerStack
+    wl1 = W.Workload(cfg.__class__(**{**cfg.__dict__, "layers": 1}), [wl.logits[0]], wl.X, [wl.layers[0]])
+    X = wl.X.to(dev)
+    lg = wl.logits[0].to(dev)
+    Y = torch.empty(cfg.T, cfg.H, dtype=torch.float32, device=dev)
+    out = {"format": "4-bit codes, one scale per 32 weights along the reduction (Q4_0-style)"}
+    for mode in ("resident", "paged"):
+        st = BoundLayerStack(wl1, mode=mode, wdtype=es.Q4)
+        try:
+            def one():
+                if mode == "paged":
+                    es.arena_invalidate(st.ctx)
+                Y.copy_(X)
+                st.prefill(0, X, lg, Y)
+            for _ in range(3):
+                one()
+            torch.cuda.synchronize()
+            es.reset_stats(st.ctx)
+            es.set_timing(st.ctx, True)
+            ms = []
+            n = max(3, args.steps if mode == "resident" else min(args.steps, args.paged_steps))
+            for _ in range(n):
+                flush.zero_()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                one()
+                b.record(stream)
+                b.synchronize()
+                ms.append(a.elapsed_time(b))
+            stats = es.last_stats(st.ctx)
+            es.set_timing(st.ctx, False)
+            assert es.get_device_error(st.ctx) == es.OK
+        finally:
+            st.close()
+        t = sum(ms) / len(ms)
+        rec = {"ms_per_layer": round(t, 4), "tokens_per_s": round(cfg.T / (t / 1e3), 1)}
+        if mode == "resident":
+            n_act = active_experts(cfg, [wl.logits[0]])[0]
+            ffn_ms = stats["ms_ffn"] / max(1, stats["n_ffn"])
+            nbytes = n_act * 3 * cfg.H * cfg.F * 9 // 16 + cfg.T * cfg.H * 2 + 2 * cfg.T * cfg.H * 4
+            gbs = nbytes / (ffn_ms / 1e3) / 1e9
+            rec.update({"kernel": "k_expert_ffn_q4", "ffn_ms": round(ffn_ms, 4),
+                        "algorithmic_bytes_per_launch": int(nbytes), "GBps": round(gbs, 1),
+                        "frac_hbm": round(gbs / peaks["hbm_gbs"], 4),
+                        "TFLOPs": round(6.0 * cfg.H * cfg.F * cfg.T * cfg.k / (ffn_ms / 1e3) / 1e12, 1)})
+        else:
+            h2d = stats["h2d_bytes"] / len(ms)
+            rec.update({"h2d_bytes_per_layer": int(h2d), "h2d_GBps": round(h2d / (t / 1e3) / 1e9, 1)})
+        out[mode] = rec
+    return out
 
 
 def measure_paged(args, cfg, wl, dev, stream, flush, peaks):
@@ -709,6 +774,7 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--paged-steps", type=int, default=10)
     ap.add_argument("--no-paged", action="store_true")
+    ap.add_argument("--no-q4", action="store_true", help="skip the 4-bit-expert measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--pipeline-study", action="store_true",
                     help="also measure the loading schedules and the (G, B) auto-configuration")

@@ -53,7 +53,14 @@ typedef enum {
     ESTREAM_ERR_UNSUPPORTED = 8   /* device or data type not supported */
 } estream_status;
 
-typedef enum { ESTREAM_F32 = 0, ESTREAM_BF16 = 1 } estream_dtype;
+/* Arithmetic types of a context. F32: X and weights fp32 (CUDA cores).
+ * BF16: X and weights bf16 (tensor cores; the down weights are converted to
+ * fp16 at pack time). Q4: X bf16; every expert weight 4-bit -- blocks of 32
+ * weights along the reduction share one scale, value = (code - 8) * scale
+ * (the paper stores expert matrices as weight-only GGUF Q4_0, section 4);
+ * packed from bf16 master weights by estream_pack_experts /
+ * estream_pack_shared. */
+typedef enum { ESTREAM_F32 = 0, ESTREAM_BF16 = 1, ESTREAM_Q4 = 2 } estream_dtype;
 
 /* Short English name of a status code (static storage). */
 const char* estream_status_string(estream_status s);
@@ -191,7 +198,7 @@ typedef struct {
     int E, H, F;            /* routed experts per layer, hidden size, expert FFN size */
     int G, B;               /* experts per storage group (= slots per bank), banks; P = B*G */
     int Q;                  /* reads in flight: Q copy streams, group fill k on stream k mod Q (>= 1) */
-    estream_dtype wdtype;   /* type of X and of every weight: bf16 (tensor cores) or fp32 */
+    estream_dtype wdtype;   /* arithmetic types of X and the weights (estream_dtype) */
     void* arena_dev;        /* device, >= estream_arena_bytes(...) bytes, 1024-byte aligned */
     size_t arena_bytes;
     const void* const* host_pool;   /* host array [L] of pinned pools, each laid out by
@@ -204,7 +211,8 @@ typedef struct {
     int T_max, k_max;       /* largest T and k a layer call will see (workspace capacity) */
     int deterministic;      /* 1: per-route outputs + fixed-order combine (bit-reproducible Y) */
     int schedule;           /* ESTREAM_SCHED_* */
-    int ffn_form;           /* ESTREAM_FFN_* (bf16 only; fp32 ignores it) */
+    int ffn_form;           /* ESTREAM_FFN_* (bf16; fp32 ignores it; Q4 runs the single-SM form
+                               and rejects ESTREAM_FFN_PAIR with ESTREAM_ERR_UNSUPPORTED) */
 } estream_arena_desc;
 
 typedef struct estream_ctx estream_ctx;
@@ -242,7 +250,19 @@ estream_status estream_bind_arena(estream_ctx** out, const estream_arena_desc* d
  * and the down GEMM multiplies it back in. The conversion is exact for every
  * weight within a factor 2^32 of the expert's largest one. fp32 layers are
  * copied unchanged with scale 1.
- * wg, wu: host [E][F][H]; wd: host [E][H][F] (bf16 or fp32 as d->wdtype);
+ * Q4 layers (from bf16 master weights): each plane is quantised in blocks of
+ * 32 weights along its reduction dimension (H for gate and up, F for down;
+ * the down weights first multiplied by 2^s_e as above). Block scale: the
+ * element of largest magnitude m (the first on ties) gives d = m / -8
+ * rounded to 5 significant bits (ties to even), then to bf16 (gate, up) or
+ * fp16 (down); codes q = clamp(rint(w / d) + 8, 0, 15) (fp32 division, ties
+ * to even); a zero block has d = 0 and codes 8. The weight used is
+ * (q - 8) * d, exact in the operand type. Layout: tile-major boxes of
+ * (128 rows of gate/up or 256 rows of down) x 64 weights, each box being the
+ * rows' codes (32 bytes a row: in its byte-word w, bits 4i..4i+3 hold weight
+ * 8w + 2i and bits 16 + 4i.. weight 8w + 2i + 1) followed by the rows' two
+ * block scales (uint16 bits); W_e = 3 * H * F * 9 / 16 bytes.
+ * wg, wu: host [E][F][H]; wd: host [E][H][F] (fp32 for F32, bf16 for BF16 and Q4);
  * host_pool_out: host, estream_pool_bytes(...) bytes (pinned if streamed).
  * Only d->E, H, F, G, wdtype and perm (row `layer`) are read. Pools must be
  * packed before estream_bind_arena (which reads their scales).

@@ -91,6 +91,15 @@ cudaError_t launch_expert_ffn_pair(const CUtensorMap* tm_wg, const CUtensorMap* 
                                    float* out_rows, int* done, int H, int F, int phases,
                                    int* dev_err, cudaStream_t stream);
 
+// The same operator on 4-bit weights (single-SM form): planes hold
+// Q4_0-style packed boxes (see estream_pack_experts), slot s of a plane at
+// plane + s * S_gu (gate, up) or s * S_d (down).
+cudaError_t launch_expert_ffn_q4(const uint8_t* plane_g, const uint8_t* plane_u, const uint8_t* plane_d,
+                                 size_t S_gu, size_t S_d, const CUtensorMap* tm_h,
+                                 const GemmSegments& seg, const void* X, void* h, float* Y,
+                                 float* out_rows, int* done, int H, int F, int phases, int* dev_err,
+                                 int num_sms, cudaStream_t stream);
+
 // fp32 path (CUDA-core FMA): the same two steps for fp32 X and weights.
 // Weight planes are [slots][F][H] (gate, up) and [slots][H][F] (down).
 cudaError_t launch_gateup_f32(const float* X, const float* wg, const float* wu,

@@ -246,6 +246,253 @@ __device__ __forceinline__ void epilogue_down(uint32_t tacc, bool valid, float a
     }
 }
 
+// ----------------------------------------------------------------------------
+// Roles shared by the single-SM kernels (bf16 weights and 4-bit weights)
+// ----------------------------------------------------------------------------
+
+// Barriers of a stage ring: full[s] at full0 + 8 s, empty[s] at empty0 + 8 s.
+struct Ring {
+    uint32_t full0, empty0;
+    __device__ __forceinline__ uint32_t full(int s) const { return full0 + 8u * s; }
+    __device__ __forceinline__ uint32_t empty(int s) const { return empty0 + 8u * s; }
+};
+
+// This CTA's walk over the tile list (tile_of order) and the decode of a tile.
+struct TileWalk {
+    const GemmSegments* seg;
+    const int* table;  // m-block prefix of the segment range, in shared memory
+    int TA, TB, NBA, NBB, KBA, KBB;
+    __device__ __forceinline__ int tile(int it) const {
+        return tile_of(blockIdx.x, gridDim.x, TA, TB, KBA, KBB, it);
+    }
+    __device__ __forceinline__ Tile decode(int t) const {
+        const bool gu = t < TA;
+        return decode_tile(gu ? t : t - TA, table, seg->seg_count, gu ? NBA : NBB, seg->offsets,
+                           seg->seg_begin);
+    }
+};
+
+// Lane 0: bounded wait until *cnt >= target (an m-block's gate/up tiles have
+// all published). Returns false on abort or timeout (recorded).
+__device__ bool wait_counter(const int* cnt, int target, volatile int* abort_flag, int* dev_err) {
+    if (ld_acquire(cnt) >= target) return true;
+    const uint64_t t0 = global_ns();
+    while (ld_acquire(cnt) < target) {
+        if (*abort_flag) return false;
+        if (global_ns() - t0 > kWaitLimitNs) {
+            *abort_flag = 1;
+            record_error(dev_err, kDevErrTimeout);
+            return false;
+        }
+    }
+    return true;
+}
+
+// A-operand loader (4 warps): the row gather of gate/up tiles. Loader warp
+// gw covers rows [32 gw, 32 gw + 32) of every A stage; in copy instruction i
+// lane l moves 16-byte chunk (l mod 8) of row 32 gw + 4i + l/8, so each
+// warp-instruction reads four whole 128-byte rows. Every thread arrives on a
+// stage once its own copies are complete (wait_group) and fenced to the async
+// proxy; kDepth stages stay in flight per thread, and the pending ones are
+// published before a down tile (whose A comes by TMA) so the CTA never waits
+// on a counter with its own stages unpublished. Down tiles' stages are only
+// passed on (one arrival per thread).
+template <int kSt, int kDepth>
+__device__ void role_gather(const FfnArgs& a, const TileWalk& w, Ring ring, uint32_t sA,
+                            volatile int* abort_flag, int gw, int lane) {
+    const GemmSegments& seg = *w.seg;
+    const uint32_t chunk = static_cast<uint32_t>(lane & 7);
+    int stage = 0;
+    uint32_t phase = 0;
+    int pend[kDepth + 1];
+    int npend = 0;
+    bool ok = true;
+    for (int it = 0, t; ok && (t = w.tile(it)) >= 0; ++it) {
+        const bool gu = t < w.TA;
+        const Tile ti = w.decode(t);
+        const int num_kb = gu ? w.KBA : w.KBB;
+        if (!gu) {
+            if (npend > 0) {
+                cp_async_wait<0>();
+                fence_proxy_async();
+                for (int q = 0; q < npend; ++q) mbar_arrive(ring.full(pend[q]));
+                npend = 0;
+            }
+            for (int kb = 0; kb < num_kb; ++kb) {
+                bool wt = true;
+                if (lane == 0) wt = mbar_wait(ring.empty(stage), phase ^ 1u, abort_flag, a.dev_err);
+                wt = __shfl_sync(0xffffffffu, wt, 0);
+                if (!wt) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive(ring.full(stage));
+                if (++stage == kSt) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            continue;
+        }
+        const uint8_t* src_row[8];
+        uint32_t dst_off[8];
+        unsigned live = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int r = gw * 32 + 4 * i + (lane >> 3);
+            dst_off[i] = static_cast<uint32_t>(r) * kRowBytes +
+                         ((chunk ^ static_cast<uint32_t>(r & 7)) << 4);
+            const bool lv = r < ti.rows;
+            live |= lv ? (1u << i) : 0u;
+            const uint8_t* row = reinterpret_cast<const uint8_t*>(a.x);
+            if (lv)
+                row = reinterpret_cast<const uint8_t*>(
+                    a.x + static_cast<size_t>(seg.rec_tok[ti.row0 + r]) * a.H);
+            src_row[i] = row + chunk * 16;
+        }
+        for (int kb = 0; kb < num_kb; ++kb) {
+            bool wt = true;
+            if (lane == 0) wt = mbar_wait(ring.empty(stage), phase ^ 1u, abort_flag, a.dev_err);
+            wt = __shfl_sync(0xffffffffu, wt, 0);
+            if (!wt) {
+                ok = false;
+                break;
+            }
+            const uint32_t base = sA + stage * kTileABytes;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (live & (1u << i)) cp_async_16(base + dst_off[i], src_row[i] + kb * kRowBytes);
+            cp_async_commit();
+            pend[npend++] = stage;
+            if (npend > kDepth) {
+                cp_async_wait<kDepth>();
+                fence_proxy_async();
+                mbar_arrive(ring.full(pend[0]));
+#pragma unroll
+                for (int q = 0; q < kDepth; ++q) pend[q] = pend[q + 1];
+                --npend;
+            }
+            if (++stage == kSt) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    }
+    // the stages still pending: complete, fence, publish
+    cp_async_wait<0>();
+    fence_proxy_async();
+    for (int q = 0; q < npend; ++q) mbar_arrive(ring.full(pend[q]));
+}
+
+// MMA issuer (one thread): per tile, wait for a free accumulator, then per
+// stage tcgen05.mma M=128 N=256 K=16 x 4, commit the stage back to the
+// producers and the finished accumulator to the epilogue. Gate/up tiles are
+// bf16 x bf16, down tiles fp16 x fp16.
+template <int kSt>
+__device__ void role_mma(const FfnArgs& a, const TileWalk& w, Ring ring, uint32_t sA, uint32_t sB,
+                         uint32_t accf0, uint32_t acce0, uint32_t drain_bar, uint32_t tmem_base,
+                         volatile int* abort_flag) {
+    const uint32_t idesc_gu = make_idesc(true, 128, 256);
+    const uint32_t idesc_dn = make_idesc(false, 128, 256);
+    int stage = 0;
+    uint32_t phase = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    bool issued_any = false;
+    for (int it = 0, t; ok && (t = w.tile(it)) >= 0; ++it) {
+        const bool gu = t < w.TA;
+        const int num_kb = gu ? w.KBA : w.KBB;
+        const uint32_t idesc = gu ? idesc_gu : idesc_dn;
+        if (!mbar_wait(acce0 + 8u * acc, acc_phase ^ 1u, abort_flag, a.dev_err)) {
+            ok = false;
+            break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kAccCols);
+        for (int kb = 0; kb < num_kb; ++kb) {
+            if (!mbar_wait(ring.full(stage), phase, abort_flag, a.dev_err)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint64_t adesc = sw128_desc(sA + stage * kTileABytes);
+            const uint64_t bdesc = sw128_desc(sB + stage * kTileBBytes);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)  // 4 x 32 bytes of K per stage
+                umma_f16(d_tmem, adesc + 2u * kk, bdesc + 2u * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
+            issued_any = true;
+            umma_commit(ring.empty(stage));
+            if (++stage == kSt) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+        if (!ok) break;
+        umma_commit(accf0 + 8u * acc);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+    }
+    if (!ok && issued_any) {
+        // wait (bounded) for the MMAs already issued before TMEM is freed
+        umma_commit(drain_bar);
+        mbar_wait(drain_bar, 0, abort_flag, nullptr, kDrainLimitNs);
+    }
+}
+
+// Epilogue (4 warps, TMEM lanes = records): gate/up tiles write
+// h = fp16(SiLU(g) u) and publish the m-block counter; down tiles add
+// alpha * scale * acc into Y (or store the row in deterministic mode).
+__device__ void role_epilogue(const FfnArgs& a, const TileWalk& w, uint32_t accf0, uint32_t acce0,
+                              uint32_t tmem_base, volatile int* abort_flag, int warp, int lane) {
+    const GemmSegments& seg = *w.seg;
+    const int quarter = warp & 3;  // TMEM lanes this warp may read
+    const int row = quarter * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int it = 0, t; (t = w.tile(it)) >= 0; ++it) {
+        const bool gu = t < w.TA;
+        const Tile ti = w.decode(t);
+        bool wt = true;
+        if (lane == 0) wt = mbar_wait(accf0 + 8u * acc, acc_phase, abort_flag, a.dev_err);
+        wt = __shfl_sync(0xffffffffu, wt, 0);
+        if (!wt) break;
+        tc_fence_after();
+        const bool valid = row < ti.rows;
+        const int p = ti.row0 + row;
+        const uint32_t tacc = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                              static_cast<uint32_t>(acc * kAccCols);
+        if (gu) {
+            epilogue_gate_up(tacc, valid,
+                             a.h + static_cast<size_t>(p) * a.F + static_cast<size_t>(ti.nb) * 128,
+                             a.dev_err);
+            // publish this warp's rows of the tile to the down tiles (which
+            // read h through TMA, the async proxy)
+            fence_proxy_async_global();
+            __threadfence();
+            __syncwarp();
+            if (lane == 0 && (a.phases & 2))
+                red_release_add(a.done + seg.mblk[seg.seg_begin + ti.seg] + ti.mb, 1);
+        } else {
+            int tok = 0;
+            float al = 0.0f;
+            if (valid) {
+                tok = seg.rec_tok[p];
+                al = seg.alpha ? seg.alpha[seg.rec_route[p]] : 1.0f;
+                al *= seg.seg_scale[seg.seg_begin + ti.seg];  // undo the W_d scale
+            }
+            epilogue_down(tacc, valid, al,
+                          a.out_rows ? a.out_rows + static_cast<size_t>(p) * a.H : nullptr,
+                          a.Y + static_cast<size_t>(tok) * a.H, ti.nb * 256);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acce0 + 8u * acc);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+    }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     k_expert_ffn(const __grid_constant__ CUtensorMap tm_wg, const __grid_constant__ CUtensorMap tm_wu,
                  const __grid_constant__ CUtensorMap tm_wd, const __grid_constant__ CUtensorMap tm_h,
@@ -304,6 +551,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int TA = (a.phases & 1) ? MB * NBA : 0;
     const int TB = (a.phases & 2) ? MB * NBB : 0;
     const int done_target = 4 * NBA;          // every epilogue warp of every gate/up n-block
+    const TileWalk walk{&seg, table, TA, TB, NBA, NBB, KBA, KBB};
+    const Ring ring{full_bar(0), empty_bar(0)};
 
     if (warp == 0) {
         // ------------------------------ TMA producer (weights) ------------------------------
@@ -312,10 +561,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         int issued[kStages];
         for (int s = 0; s < kStages; ++s) issued[s] = -1;
         bool ok = true;
-        for (int it = 0, t; ok && (t = tile_of(blockIdx.x, gridDim.x, TA, TB, KBA, KBB, it)) >= 0; ++it) {
+        for (int it = 0, t; ok && (t = walk.tile(it)) >= 0; ++it) {
             const bool gu = t < TA;
-            const Tile ti = decode_tile(gu ? t : t - TA, table, seg.seg_count, gu ? NBA : NBB,
-                                        seg.offsets, seg.seg_begin);
+            const Tile ti = walk.decode(t);
             const int slot = seg.slot_base + ti.seg;
             // weight planes are tile-major: the (n-block, k-block) box of a slot
             // is one contiguous run of 128 (gate/up) or 256 (down) rows of 128 B
@@ -327,21 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // every gate/up n-block has published
                 const int* cnt = a.done + seg.mblk[seg.seg_begin + ti.seg] + ti.mb;
                 bool w = true;
-                if (lane == 0 && ld_acquire(cnt) < done_target) {
-                    const uint64_t t0 = global_ns();
-                    while (ld_acquire(cnt) < done_target) {
-                        if (*abort_flag) {
-                            w = false;
-                            break;
-                        }
-                        if (global_ns() - t0 > kWaitLimitNs) {
-                            *abort_flag = 1;
-                            record_error(a.dev_err, kDevErrTimeout);
-                            w = false;
-                            break;
-                        }
-                    }
-                }
+                if (lane == 0) w = wait_counter(cnt, done_target, abort_flag, a.dev_err);
                 if (lane == 0) fence_proxy_async_global();  // before the TMA reads of h
                 w = __shfl_sync(0xffffffffu, w, 0);
                 if (!w) {
@@ -387,198 +621,293 @@ __global__ void __launch_bounds__(kThreads, 1)
                               kDrainLimitNs);
         }
     } else if (warp >= kLoaderWarp0) {
-        // ------------------------------ A-operand loader ------------------------------
-        // Loader warp w covers rows [32w, 32w+32) of every A stage; in copy
-        // instruction i lane l moves 16-byte chunk (l mod 8) of row
-        // 32w + 4i + l/8, so each warp-instruction reads four whole 128-byte
-        // rows. Every thread arrives on a stage once its own copies are
-        // complete (wait_group) and fenced to the async proxy; kLoaderDepth
-        // stages stay in flight per thread.
-        const int gw = warp - kLoaderWarp0;
-        const uint32_t chunk = static_cast<uint32_t>(lane & 7);
-        int stage = 0;
-        uint32_t phase = 0;
-        int pend[kLoaderDepth + 1];
-        int npend = 0;
-        bool ok = true;
-        for (int it = 0, t; ok && (t = tile_of(blockIdx.x, gridDim.x, TA, TB, KBA, KBB, it)) >= 0; ++it) {
-            const bool gu = t < TA;
-            const Tile ti = decode_tile(gu ? t : t - TA, table, seg.seg_count, gu ? NBA : NBB,
-                                        seg.offsets, seg.seg_begin);
-            const int num_kb = gu ? KBA : KBB;
-            if (!gu) {
-                // down tile: the producer loads A (h) with TMA; publish the
-                // stages still pending, then only pass this tile's stages on
-                if (npend > 0) {
-                    cp_async_wait<0>();
-                    fence_proxy_async();
-                    for (int q = 0; q < npend; ++q) mbar_arrive(full_bar(pend[q]));
-                    npend = 0;
-                }
-                for (int kb = 0; kb < num_kb; ++kb) {
-                    bool w = true;
-                    if (lane == 0) w = mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, a.dev_err);
-                    w = __shfl_sync(0xffffffffu, w, 0);
-                    if (!w) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive(full_bar(stage));
-                    if (++stage == kStages) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-                continue;
-            }
-            const uint8_t* src_row[8];
-            uint32_t dst_off[8];
-            unsigned live = 0;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int r = gw * 32 + 4 * i + (lane >> 3);
-                dst_off[i] = static_cast<uint32_t>(r) * kRowBytes +
-                             ((chunk ^ static_cast<uint32_t>(r & 7)) << 4);
-                const bool lv = r < ti.rows;
-                live |= lv ? (1u << i) : 0u;
-                const uint8_t* row = reinterpret_cast<const uint8_t*>(a.x);
-                if (lv)
-                    row = reinterpret_cast<const uint8_t*>(
-                        a.x + static_cast<size_t>(seg.rec_tok[ti.row0 + r]) * H);
-                src_row[i] = row + chunk * 16;
-            }
-            for (int kb = 0; kb < num_kb; ++kb) {
-                bool w = true;
-                if (lane == 0) w = mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, a.dev_err);
-                w = __shfl_sync(0xffffffffu, w, 0);
-                if (!w) {
-                    ok = false;
-                    break;
-                }
-                const uint32_t base = sA + stage * kTileABytes;
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    if (live & (1u << i)) cp_async_16(base + dst_off[i], src_row[i] + kb * kRowBytes);
-                cp_async_commit();
-                pend[npend++] = stage;
-                if (npend > kLoaderDepth) {
-                    cp_async_wait<kLoaderDepth>();
-                    fence_proxy_async();
-                    mbar_arrive(full_bar(pend[0]));
-#pragma unroll
-                    for (int q = 0; q < kLoaderDepth; ++q) pend[q] = pend[q + 1];
-                    --npend;
-                }
-                if (++stage == kStages) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
-            }
-        }
-        // the stages still pending: complete, fence, publish
-        cp_async_wait<0>();
-        fence_proxy_async();
-        for (int q = 0; q < npend; ++q) mbar_arrive(full_bar(pend[q]));
+        role_gather<kStages, kLoaderDepth>(a, walk, ring, sA, abort_flag, warp - kLoaderWarp0, lane);
     } else if (warp == 1) {
-        // ------------------------------ MMA issuer ------------------------------
-        if (lane == 0) {
-            const uint32_t idesc_gu = make_idesc(true, 128, 256);   // bf16 x bf16
-            const uint32_t idesc_dn = make_idesc(false, 128, 256);  // fp16 x fp16
-            int stage = 0;
-            uint32_t phase = 0;
-            int acc = 0;
-            uint32_t acc_phase = 0;
-            bool ok = true;
-            bool issued_any = false;
-            for (int it = 0, t; ok && (t = tile_of(blockIdx.x, gridDim.x, TA, TB, KBA, KBB, it)) >= 0; ++it) {
-                const bool gu = t < TA;
-                const int num_kb = gu ? KBA : KBB;
-                const uint32_t idesc = gu ? idesc_gu : idesc_dn;
-                if (!mbar_wait(acce_bar(acc), acc_phase ^ 1u, abort_flag, a.dev_err)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kAccCols);
-                for (int kb = 0; kb < num_kb; ++kb) {
-                    if (!mbar_wait(full_bar(stage), phase, abort_flag, a.dev_err)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint64_t adesc = sw128_desc(sA + stage * kTileABytes);
-                    const uint64_t bdesc = sw128_desc(sB + stage * kTileBBytes);
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)  // 4 x 32 bytes of K per stage
-                        umma_f16(d_tmem, adesc + 2u * kk, bdesc + 2u * kk, idesc,
-                                 (kb | kk) != 0 ? 1u : 0u);
-                    issued_any = true;
-                    umma_commit(empty_bar(stage));
-                    if (++stage == kStages) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-                if (!ok) break;
-                umma_commit(accf_bar(acc));
-                acc ^= 1;
-                if (acc == 0) acc_phase ^= 1u;
-            }
-            if (!ok && issued_any) {
-                // wait (bounded) for the MMAs already issued before TMEM is freed
-                umma_commit(drain_bar);
-                mbar_wait(drain_bar, 0, abort_flag, nullptr, kDrainLimitNs);
-            }
-        }
+        if (lane == 0)
+            role_mma<kStages>(a, walk, ring, sA, sB, accf_bar(0), acce_bar(0), drain_bar, tmem_base,
+                              abort_flag);
         __syncwarp();
     } else {
-        // ------------------------------ epilogue (warps 2-5) ------------------------------
-        const int quarter = warp & 3;  // TMEM lanes this warp may read
-        const int row = quarter * 32 + lane;
-        int acc = 0;
-        uint32_t acc_phase = 0;
-        for (int it = 0, t; (t = tile_of(blockIdx.x, gridDim.x, TA, TB, KBA, KBB, it)) >= 0; ++it) {
-            const bool gu = t < TA;
-            const Tile ti = decode_tile(gu ? t : t - TA, table, seg.seg_count, gu ? NBA : NBB,
-                                        seg.offsets, seg.seg_begin);
-            bool w = true;
-            if (lane == 0) w = mbar_wait(accf_bar(acc), acc_phase, abort_flag, a.dev_err);
-            w = __shfl_sync(0xffffffffu, w, 0);
-            if (!w) break;
-            tc_fence_after();
-            const bool valid = row < ti.rows;
-            const int p = ti.row0 + row;
-            const uint32_t tacc = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                                  static_cast<uint32_t>(acc * kAccCols);
-            if (gu) {
-                epilogue_gate_up(tacc, valid,
-                                 a.h + static_cast<size_t>(p) * F + static_cast<size_t>(ti.nb) * 128,
-                                 a.dev_err);
-                // publish this warp's rows of the tile to the down tiles (which
-                // read h through TMA, the async proxy)
-                fence_proxy_async_global();
-                __threadfence();
-                __syncwarp();
-                if (lane == 0 && (a.phases & 2))
-                    red_release_add(a.done + seg.mblk[seg.seg_begin + ti.seg] + ti.mb, 1);
+        role_epilogue(a, walk, accf_bar(0), acce_bar(0), tmem_base, abort_flag, warp, lane);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+// ----------------------------------------------------------------------------
+// 4-bit expert weights, single-SM form
+// ----------------------------------------------------------------------------
+// The weight planes hold Q4_0-style blocks (section 4 of the paper stores
+// expert matrices as weight-only GGUF Q4_0): per (n-block, k-block) box, the
+// 4-bit codes of each row's 64 weights (32 bytes; in byte-word w, bits 4i..
+// 4i+3 hold k = 8w + 2i and bits 16 + 4i.. hold k = 8w + 2i + 1) followed by
+// the row's two block scales (bf16 for gate and up, fp16 for down), a value
+// being (q - 8) * d. Roles: warp 0 streams packed boxes with plain bulk
+// copies into a 3-deep ring (a stage is 9 KB instead of 32 KB of bf16);
+// warps 10-13 expand each packed stage into the 128-byte-swizzled bf16/fp16
+// B tile of the 4-deep MMA ring -- the paper's "vector workers decode them into
+// matrix-engine operands" (section 3.2) -- and, for down tiles, wait for the
+// m-block's h rows and load them with TMA; the gather, MMA and epilogue roles
+// are the bf16 kernel's. Every expanded operand is exact: (q - 8) and d each
+// have at most 5 significant bits, so their product fits bf16 and fp16.
+constexpr int kQStages = 4;                   // MMA ring (expanded operands)
+constexpr int kQPStages = 3;                  // packed-weight ring
+constexpr int kQMaxSegs = kMaxE;              // segments are experts of one layer
+constexpr int kQBoxGU = 128 * 32 + 128 * 4;   // 4608 B: one gate or up box
+constexpr int kQBoxDn = 256 * 32 + 256 * 4;   // 9216 B: one down box
+constexpr int kQPBytes = kQBoxDn;             // a packed stage: gate + up, or down
+constexpr int kConvWarps = 8;                 // one B row per converter thread and stage
+constexpr int kQThreads = 320 + 32 * kConvWarps;
+constexpr int kConvWarp0 = 10;
+constexpr int kQOffA = 0;
+constexpr int kQOffB = kQStages * kTileABytes;
+constexpr int kQOffP = kQOffB + kQStages * kTileBBytes;
+constexpr int kQOffBar = kQOffP + kQPStages * kQPBytes;
+// barriers: full[4], empty[4], pfull[3], pempty[3], acc_full[2], acc_empty[2], drain
+constexpr int kQNumBars = 2 * kQStages + 2 * kQPStages + 5;
+constexpr int kQOffMisc = kQOffBar + 8 * kQNumBars;
+constexpr int kQOffTable = kQOffMisc + 16;
+
+size_t q4_smem_bytes(int seg_count) {
+    return 1024 + kQOffTable + sizeof(int) * static_cast<size_t>(seg_count + 1);
+}
+
+struct Q4Planes {
+    const uint8_t* g;  // slot s of the gate plane at g + s * S_gu
+    const uint8_t* u;
+    const uint8_t* d;  // slot s of the down plane at d + s * S_d
+    size_t S_gu, S_d;
+};
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+// Expand one packed row (64 codes, two block scales) into 64 operands of
+// B-tile row r: 8 chunks of 16 bytes, chunk c at (c ^ (r mod 8)) * 16. A code
+// q becomes the number 128 + q (bf16 0x4300 | q) or 1024 + q (fp16
+// 0x6400 | q) by bit placement; subtracting 136 (1032) gives q - 8 and the
+// multiplication by d the weight, both exact.
+template <bool kFp16>
+__device__ __forceinline__ void expand_row(uint32_t codes, uint32_t scales, uint32_t dst_row, int r) {
+    uint32_t w[8], sc;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]) : "r"(codes));
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7]) : "r"(codes + 16));
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(sc) : "r"(scales));
+    const uint32_t magic = kFp16 ? 0x64006400u : 0x43004300u;
+    const uint32_t offset = kFp16 ? 0x64086408u : 0x43084308u;
+    const uint32_t d_lo = (sc & 0xFFFFu) * 0x10001u;  // block 0's scale in both halves
+    const uint32_t d_hi = (sc >> 16) * 0x10001u;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const uint32_t d2 = c < 4 ? d_lo : d_hi;
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t v = ((w[c] >> (4 * i)) & 0x000F000Fu) | magic;
+            uint32_t t;
+            if (kFp16) {
+                asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(t) : "r"(v), "r"(offset));
+                asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(o[i]) : "r"(t), "r"(d2));
             } else {
-                int tok = 0;
-                float al = 0.0f;
-                if (valid) {
-                    tok = seg.rec_tok[p];
-                    al = seg.alpha ? seg.alpha[seg.rec_route[p]] : 1.0f;
-                    al *= seg.seg_scale[seg.seg_begin + ti.seg];  // undo the W_d scale
-                }
-                epilogue_down(tacc, valid, al,
-                              a.out_rows ? a.out_rows + static_cast<size_t>(p) * H : nullptr,
-                              a.Y + static_cast<size_t>(tok) * H, ti.nb * 256);
+                asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(t) : "r"(v), "r"(offset));
+                asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(o[i]) : "r"(t), "r"(d2));
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(acce_bar(acc));
-            acc ^= 1;
-            if (acc == 0) acc_phase ^= 1u;
         }
+        const uint32_t dst = dst_row + ((static_cast<uint32_t>(c) ^ static_cast<uint32_t>(r & 7)) << 4);
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(o[0]), "r"(o[1]),
+                     "r"(o[2]), "r"(o[3])
+                     : "memory");
+    }
+}
+
+// Converter warps (cw = 0..7, thread ct = 32 cw + lane expands B row ct of
+// every stage: rows 0-127 the gate box, 128-255 the up box, or the 256 rows
+// of the down box).
+__device__ void role_convert(const FfnArgs& a, const TileWalk& w, Ring ring, Ring pring, uint32_t sA,
+                             uint32_t sB, uint32_t sP, const CUtensorMap* tm_h, int done_target,
+                             volatile int* abort_flag, int cw, int lane) {
+    const GemmSegments& seg = *w.seg;
+    const int ct = cw * 32 + lane;
+    int g = 0;
+    bool ok = true;
+    for (int it = 0, t; ok && (t = w.tile(it)) >= 0; ++it) {
+        const bool gu = t < w.TA;
+        const Tile ti = w.decode(t);
+        const int num_kb = gu ? w.KBA : w.KBB;
+        for (int kb = 0; kb < num_kb; ++kb, ++g) {
+            const int s = g % kQStages;
+            const uint32_t ph = static_cast<uint32_t>(g / kQStages) & 1u;
+            const int ps = g % kQPStages;
+            const uint32_t pph = static_cast<uint32_t>(g / kQPStages) & 1u;
+            bool wt = true;
+            if (lane == 0)
+                wt = mbar_wait(pring.full(ps), pph, abort_flag, a.dev_err) &&
+                     mbar_wait(ring.empty(s), ph ^ 1u, abort_flag, a.dev_err);
+            if (!gu && kb == 0 && cw == 0 && lane == 0 && wt) {
+                // the m-block's h rows are complete once every epilogue warp
+                // of every gate/up n-block has published
+                wt = wait_counter(a.done + seg.mblk[seg.seg_begin + ti.seg] + ti.mb, done_target,
+                                  abort_flag, a.dev_err);
+                fence_proxy_async_global();  // before the TMA reads of h
+            }
+            wt = __shfl_sync(0xffffffffu, wt, 0);
+            if (!wt) {
+                ok = false;
+                break;
+            }
+            const uint32_t pb = sP + ps * kQPBytes;
+            const uint32_t bb = sB + s * kTileBBytes;
+            if (gu) {
+                const uint32_t box = pb + (ct < 128 ? 0u : static_cast<uint32_t>(kQBoxGU));
+                const int r = ct & 127;
+                expand_row<false>(box + r * 32, box + 4096 + r * 4, bb + ct * kRowBytes, ct);
+            } else {
+                expand_row<true>(pb + ct * 32, pb + 8192 + ct * 4, bb + ct * kRowBytes, ct);
+            }
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) {
+                if (!gu && cw == 0) {
+                    mbar_arrive_expect_tx(ring.full(s), kTileABytes);
+                    tma_load_2d(sA + s * kTileABytes, tm_h, kb * 64, ti.row0, ring.full(s));
+                } else {
+                    mbar_arrive(ring.full(s));
+                }
+                mbar_arrive(pring.empty(ps));
+            }
+        }
+    }
+    if (!ok && cw == 0 && lane == 0) {
+        // give an h load already issued time to land before the CTA goes away
+        const uint64_t t0 = global_ns();
+        while (global_ns() - t0 < kDrainLimitNs / 100) {
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kQThreads, 1)
+    k_expert_ffn_q4(const __grid_constant__ CUtensorMap tm_h, const Q4Planes planes, const FfnArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    const GemmSegments& seg = a.seg;
+    const uint32_t sbase = smem_addr(smem);
+    const uint32_t sA = sbase + kQOffA;
+    const uint32_t sB = sbase + kQOffB;
+    const uint32_t sP = sbase + kQOffP;
+    const uint32_t bar0 = sbase + kQOffBar;
+    const Ring ring{bar0, bar0 + 8u * kQStages};
+    const Ring pring{bar0 + 8u * (2 * kQStages), bar0 + 8u * (2 * kQStages + kQPStages)};
+    const uint32_t accf0 = bar0 + 8u * (2 * kQStages + 2 * kQPStages);
+    const uint32_t acce0 = accf0 + 16u;
+    const uint32_t drain_bar = acce0 + 16u;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kQOffMisc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kQOffMisc + 4);
+    int* table = reinterpret_cast<int*>(smem + kQOffTable);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    const int m0 = seg.mblk[seg.seg_begin];
+    for (int s = threadIdx.x; s <= seg.seg_count; s += blockDim.x)
+        table[s] = seg.mblk[seg.seg_begin + s] - m0;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kQStages; ++s) {
+            mbar_init(ring.full(s), kBM + kConvWarps);  // one per loader thread + one per converter warp
+            mbar_init(ring.empty(s), 1);
+        }
+        for (int s = 0; s < kQPStages; ++s) {
+            mbar_init(pring.full(s), 1);   // the producer's expect_tx
+            mbar_init(pring.empty(s), kConvWarps);  // one per converter warp
+        }
+        for (int q = 0; q < 2; ++q) {
+            mbar_init(accf0 + 8u * q, 1);
+            mbar_init(acce0 + 8u * q, 4);
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int H = a.H, F = a.F;
+    const int NBA = F / 128, NBB = H / 256;
+    const int KBA = H / 64, KBB = F / 64;
+    const int MB = table[seg.seg_count];
+    const int TA = (a.phases & 1) ? MB * NBA : 0;
+    const int TB = (a.phases & 2) ? MB * NBB : 0;
+    const TileWalk walk{&seg, table, TA, TB, NBA, NBB, KBA, KBB};
+
+    if (warp == 0) {
+        // ------------------------------ packed-weight producer ------------------------------
+        if (lane == 0) {
+            int issued[kQPStages];
+            for (int s = 0; s < kQPStages; ++s) issued[s] = -1;
+            bool ok = true;
+            int g = 0;
+            for (int it = 0, t; ok && (t = walk.tile(it)) >= 0; ++it) {
+                const bool gu = t < TA;
+                const Tile ti = walk.decode(t);
+                const size_t slot = static_cast<size_t>(seg.slot_base + ti.seg);
+                const int num_kb = gu ? KBA : KBB;
+                const uint8_t* src0 = gu ? planes.g + slot * planes.S_gu + static_cast<size_t>(ti.nb) * KBA * kQBoxGU
+                                         : planes.d + slot * planes.S_d + static_cast<size_t>(ti.nb) * KBB * kQBoxDn;
+                const uint8_t* src1 = planes.u + slot * planes.S_gu + static_cast<size_t>(ti.nb) * KBA * kQBoxGU;
+                for (int kb = 0; kb < num_kb; ++kb, ++g) {
+                    const int ps = g % kQPStages;
+                    const uint32_t pph = static_cast<uint32_t>(g / kQPStages) & 1u;
+                    if (!mbar_wait(pring.empty(ps), pph ^ 1u, abort_flag, a.dev_err)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(pring.full(ps), kQPBytes);
+                    issued[ps] = static_cast<int>(pph);
+                    const uint32_t dst = sP + ps * kQPBytes;
+                    if (gu) {
+                        bulk_load(dst, src0 + static_cast<size_t>(kb) * kQBoxGU, kQBoxGU, pring.full(ps));
+                        bulk_load(dst + kQBoxGU, src1 + static_cast<size_t>(kb) * kQBoxGU, kQBoxGU,
+                                  pring.full(ps));
+                    } else {
+                        bulk_load(dst, src0 + static_cast<size_t>(kb) * kQBoxDn, kQBoxDn, pring.full(ps));
+                    }
+                }
+            }
+            if (!ok)
+                for (int s = 0; s < kQPStages; ++s)
+                    if (issued[s] >= 0)
+                        mbar_wait(pring.full(s), static_cast<uint32_t>(issued[s]), abort_flag, nullptr,
+                                  kDrainLimitNs);
+        }
+        __syncwarp();
+    } else if (warp >= kConvWarp0) {
+        role_convert(a, walk, ring, pring, sA, sB, sP, &tm_h, 4 * NBA, abort_flag, warp - kConvWarp0, lane);
+    } else if (warp >= kLoaderWarp0) {
+        role_gather<kQStages, kLoaderDepth>(a, walk, ring, sA, abort_flag, warp - kLoaderWarp0, lane);
+    } else if (warp == 1) {
+        if (lane == 0)
+            role_mma<kQStages>(a, walk, ring, sA, sB, accf0, acce0, drain_bar, tmem_base, abort_flag);
+        __syncwarp();
+    } else {
+        role_epilogue(a, walk, accf0, acce0, tmem_base, abort_flag, warp, lane);
     }
 
     tc_fence_before();
@@ -1274,6 +1603,41 @@ cudaError_t launch_expert_ffn_pair(const CUtensorMap* tm_wg, const CUtensorMap* 
     cfg.attrs = at;
     cfg.numAttrs = 2;
     rc = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(k_expert_ffn_pair), kargs);
+    if (rc != cudaSuccess) return rc;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_expert_ffn_q4(const uint8_t* plane_g, const uint8_t* plane_u, const uint8_t* plane_d,
+                                 size_t S_gu, size_t S_d, const CUtensorMap* tm_h,
+                                 const GemmSegments& seg, const void* X, void* h, float* Y,
+                                 float* out_rows, int* done, int H, int F, int phases, int* dev_err,
+                                 int num_sms, cudaStream_t stream) {
+    const long long max_tiles = static_cast<long long>(seg.max_tiles_m) *
+                                (((phases & 1) ? F / 128 : 0) + ((phases & 2) ? H / 256 : 0));
+    if (max_tiles <= 0 || seg.seg_count <= 0) return cudaSuccess;
+    if (seg.seg_count > kQMaxSegs) return cudaErrorInvalidValue;
+    const int grid = static_cast<int>(max_tiles < num_sms ? max_tiles : num_sms);
+    const size_t smem = q4_smem_bytes(seg.seg_count);
+    cudaError_t rc = cudaFuncSetAttribute(k_expert_ffn_q4, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          static_cast<int>(smem));
+    if (rc != cudaSuccess) return rc;
+    Q4Planes planes{plane_g, plane_u, plane_d, S_gu, S_d};
+    FfnArgs args;
+    args.seg = seg;
+    args.x = static_cast<const __nv_bfloat16*>(X);
+    args.h = static_cast<__half*>(h);
+    args.Y = Y;
+    args.out_rows = out_rows;
+    args.done = done;
+    args.dev_err = dev_err;
+    args.H = H;
+    args.F = F;
+    args.phases = phases;
+    void* kargs[] = {const_cast<CUtensorMap*>(tm_h), &planes, &args};
+    // cooperative: every CTA is resident, so a down tile may wait for the
+    // gate/up tiles of its m-block that other CTAs own
+    rc = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(k_expert_ffn_q4), grid, kQThreads,
+                                     kargs, smem, stream);
     if (rc != cudaSuccess) return rc;
     return cudaGetLastError();
 }

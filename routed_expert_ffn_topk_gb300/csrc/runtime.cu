@@ -163,6 +163,126 @@ float bf16_bits_to_float(uint16_t b) {
     return f;
 }
 
+// Element size of X and of the h intermediate (bf16 X and fp16 h unless fp32).
+size_t elem_size(estream_dtype t) { return t == ESTREAM_F32 ? 4 : 2; }
+
+// Bytes of one expert's [rows][cols] plane as stored in the arena: 4 or 2
+// bytes per weight, or for 4-bit weights half a byte per weight plus a 2-byte
+// scale per 32 weights (9/16 of a byte per weight).
+size_t plane_slot_bytes(estream_dtype t, int rows, int cols) {
+    const size_t n = static_cast<size_t>(rows) * cols;
+    if (t == ESTREAM_Q4) return n / 16 * 9;
+    return n * elem_size(t);
+}
+
+// Bytes of one expert's master weights as the packers read them (4-bit
+// experts are packed from bf16).
+size_t master_bytes(estream_dtype t, int rows, int cols) {
+    return static_cast<size_t>(rows) * cols * (t == ESTREAM_F32 ? 4 : 2);
+}
+
+// ---- 4-bit packing (Q4_0-style blocks of 32 weights along the reduction) ----
+// Scale of a block: the element of largest magnitude m (the first on ties)
+// gives d = m / -8, rounded to 5 significant bits (ties to even), then to the
+// operand type; code q = clamp(rint(x / d) + 8, 0, 15) (fp32 division, ties
+// to even); a zero block has d = 0 and codes 8. With 5 significant bits in d
+// every (q - 8) * d is exact in bf16 and in fp16.
+float round_to_5_bits(float x) {
+    uint32_t u;
+    std::memcpy(&u, &x, sizeof(u));
+    const uint32_t keep_from = 19;  // fp32 keeps 23 fraction bits, d keeps 4
+    const uint32_t low = u & ((1u << keep_from) - 1u);
+    const uint32_t half = 1u << (keep_from - 1);
+    u &= ~((1u << keep_from) - 1u);
+    if (low > half || (low == half && ((u >> keep_from) & 1u))) u += 1u << keep_from;
+    float y;
+    std::memcpy(&y, &u, sizeof(y));
+    return y;
+}
+
+uint16_t float_to_bf16_bits_rne(float x) {
+    uint32_t u;
+    std::memcpy(&u, &x, sizeof(u));
+    const uint32_t lsb = (u >> 16) & 1u;
+    return static_cast<uint16_t>((u + 0x7FFFu + lsb) >> 16);
+}
+
+// One (n-block, k-block) box of a 4-bit plane: tile_rows rows x 64 weights of
+// src (fp32 values, row stride cols), written as tile_rows x 32 code bytes
+// (byte-word w of a row: bits 4i..4i+3 = code of weight 8w + 2i, bits
+// 16 + 4i.. = code of weight 8w + 2i + 1) then tile_rows x 2 scales (uint16
+// bits of bf16, or of fp16 when fp16 is set).
+void pack_q4_box(const float* src, int cols, int tile_rows, bool fp16, uint8_t* dst) {
+    uint8_t* codes = dst;
+    uint16_t* scales = reinterpret_cast<uint16_t*>(dst + static_cast<size_t>(tile_rows) * 32);
+    for (int r = 0; r < tile_rows; ++r) {
+        const float* row = src + static_cast<size_t>(r) * cols;
+        uint8_t q[64];
+        for (int b = 0; b < 2; ++b) {
+            const float* x = row + 32 * b;
+            float m = 0.0f;
+            for (int j = 0; j < 32; ++j)
+                if (std::fabs(x[j]) > std::fabs(m)) m = x[j];
+            float d = 0.0f;
+            uint16_t bits = 0;
+            if (m != 0.0f) {
+                const float d5 = round_to_5_bits(m / -8.0f);
+                if (fp16) {
+                    const __half hd = __float2half_rn(d5);
+                    d = __half2float(hd);
+                    std::memcpy(&bits, &hd, sizeof(bits));
+                } else {
+                    bits = float_to_bf16_bits_rne(d5);
+                    d = bf16_bits_to_float(bits);
+                }
+            }
+            scales[2 * r + b] = bits;
+            for (int j = 0; j < 32; ++j) {
+                int c = 8;
+                if (d != 0.0f) c = std::min(15, std::max(0, static_cast<int>(std::nearbyint(x[j] / d)) + 8));
+                q[32 * b + j] = static_cast<uint8_t>(c);
+            }
+        }
+        for (int w = 0; w < 8; ++w) {
+            uint32_t word = 0;
+            for (int i = 0; i < 4; ++i) {
+                word |= static_cast<uint32_t>(q[8 * w + 2 * i]) << (4 * i);
+                word |= static_cast<uint32_t>(q[8 * w + 2 * i + 1]) << (16 + 4 * i);
+            }
+            std::memcpy(codes + static_cast<size_t>(r) * 32 + 4 * w, &word, sizeof(word));
+        }
+    }
+}
+
+// A whole [rows][cols] bf16 plane, times 2^scale_exp, into tile-major 4-bit
+// boxes ([rows/tile_rows][cols/64] boxes of tile_rows rows).
+void pack_q4_plane(const uint16_t* src, int rows, int cols, int tile_rows, bool fp16, int scale_exp,
+                   uint8_t* dst) {
+    const size_t box = static_cast<size_t>(tile_rows) * 36;
+    std::vector<float> tile(static_cast<size_t>(tile_rows) * 64);
+    size_t o = 0;
+    for (int nb = 0; nb < rows / tile_rows; ++nb)
+        for (int kb = 0; kb < cols / 64; ++kb) {
+            for (int r = 0; r < tile_rows; ++r)
+                for (int c = 0; c < 64; ++c)
+                    tile[static_cast<size_t>(r) * 64 + c] = std::ldexp(
+                        bf16_bits_to_float(src[static_cast<size_t>(nb * tile_rows + r) * cols + kb * 64 + c]),
+                        scale_exp);
+            pack_q4_box(tile.data(), 64, tile_rows, fp16, dst + o);
+            o += box;
+        }
+}
+
+// Exponent s that puts the largest |w| of a bf16 plane in [2^14, 2^15).
+int down_scale_exp(const uint16_t* w, size_t n) {
+    float mx = 0.0f;
+    for (size_t x = 0; x < n; ++x) mx = std::max(mx, std::fabs(bf16_bits_to_float(w[x])));
+    if (!(mx > 0.0f) || !std::isfinite(mx)) return 0;
+    int ex = 0;
+    std::frexp(mx, &ex);  // mx = m * 2^ex, m in [0.5, 1)
+    return 15 - ex;
+}
+
 // Offline repack of one expert's plane for the tensor-core path (section
 // 3.3, "Offline NPU-Consumable Weight Layout", restated for TMA): the
 // [rows][cols] row-major matrix (rows = output features, cols = the
@@ -184,6 +304,10 @@ void pack_tiles(const uint16_t* src, int rows, int cols, int tile_rows, Out* dst
 // Gate or up plane of one expert: bf16 copied into 128-row tiles; fp32 copied
 // unchanged (the fp32 path reads row-major planes).
 void pack_gate_up(const void* src, int F, int H, estream_dtype t, void* dst) {
+    if (t == ESTREAM_Q4) {
+        pack_q4_plane(static_cast<const uint16_t*>(src), F, H, 128, false, 0, static_cast<uint8_t*>(dst));
+        return;
+    }
     if (t == ESTREAM_F32) {
         std::memcpy(dst, src, sizeof(float) * static_cast<size_t>(F) * H);
         return;
@@ -202,13 +326,10 @@ float pack_down(const void* src, int H, int F, estream_dtype t, void* dst) {
         return 1.0f;
     }
     const uint16_t* w = static_cast<const uint16_t*>(src);
-    float mx = 0.0f;
-    for (size_t x = 0; x < n; ++x) mx = std::max(mx, std::fabs(bf16_bits_to_float(w[x])));
-    int s = 0;
-    if (mx > 0.0f && std::isfinite(mx)) {
-        int ex = 0;
-        std::frexp(mx, &ex);  // mx = m * 2^ex, m in [0.5, 1)
-        s = 15 - ex;
+    const int s = down_scale_exp(w, n);
+    if (t == ESTREAM_Q4) {
+        pack_q4_plane(w, H, F, 256, true, s, static_cast<uint8_t*>(dst));
+        return std::ldexp(1.0f, -s);
     }
     const float up = std::ldexp(1.0f, s);
     pack_tiles(w, H, F, 256, static_cast<__half*>(dst),
@@ -216,11 +337,11 @@ float pack_down(const void* src, int H, int F, estream_dtype t, void* dst) {
     return std::ldexp(1.0f, -s);
 }
 
-size_t elem_size(estream_dtype t) { return t == ESTREAM_F32 ? 4 : 2; }
 
 estream_status desc_shape_ok(const estream_arena_desc* d) {
     if (!d) return ESTREAM_ERR_INVALID_ARG;
-    if (d->wdtype != ESTREAM_F32 && d->wdtype != ESTREAM_BF16) return ESTREAM_ERR_UNSUPPORTED;
+    if (d->wdtype != ESTREAM_F32 && d->wdtype != ESTREAM_BF16 && d->wdtype != ESTREAM_Q4)
+        return ESTREAM_ERR_UNSUPPORTED;
     if (d->E < 1 || d->E > kMaxE || d->H < 256 || d->F < 128) return ESTREAM_ERR_INVALID_ARG;
     if (d->H % 256 != 0 || d->F % 128 != 0) return ESTREAM_ERR_INVALID_ARG;
     if (d->G < 1 || d->B < 1 || static_cast<long long>(d->G) * d->B > kMaxP)
@@ -290,19 +411,17 @@ estream_status estream_workspace_error(void* workspace, void* cuda_stream) {
 size_t estream_arena_bytes(int E, int H, int F, int G, int B, estream_dtype wdtype) {
     (void)E;
     if (H < 1 || F < 1 || G < 1 || B < 1) return 0;
-    return static_cast<size_t>(B) * G * 3 * static_cast<size_t>(H) * F * elem_size(wdtype);
+    return static_cast<size_t>(B) * G * 3 * plane_slot_bytes(wdtype, F, H);
 }
 
 size_t estream_pool_bytes(int E, int H, int F, estream_dtype wdtype) {
     if (E < 1 || H < 1 || F < 1) return 0;
-    return static_cast<size_t>(E) * 3 * static_cast<size_t>(H) * F * elem_size(wdtype) +
-           align_up(sizeof(float) * E, 16);
+    return static_cast<size_t>(E) * 3 * plane_slot_bytes(wdtype, F, H) + align_up(sizeof(float) * E, 16);
 }
 
 size_t estream_shared_bytes(int n_shared, int H, int F_shared, estream_dtype wdtype) {
     if (n_shared < 1 || H < 1 || F_shared < 1) return 0;
-    return static_cast<size_t>(n_shared) * 3 * static_cast<size_t>(H) * F_shared *
-               elem_size(wdtype) +
+    return static_cast<size_t>(n_shared) * 3 * plane_slot_bytes(wdtype, F_shared, H) +
            align_up(sizeof(float) * n_shared, 16);
 }
 
@@ -312,8 +431,8 @@ estream_status estream_pack_experts(const estream_arena_desc* d, int layer, cons
     if (st != ESTREAM_OK) return st;
     if (!wg || !wu || !wd || !host_pool_out || layer < 0 || layer >= std::max(1, d->L))
         return ESTREAM_ERR_INVALID_ARG;
-    const size_t es_ = elem_size(d->wdtype);
-    const size_t S = static_cast<size_t>(d->H) * d->F * es_;  // one plane slice of one expert
+    const size_t Sin = master_bytes(d->wdtype, d->F, d->H);    // one input matrix of one expert
+    const size_t S = plane_slot_bytes(d->wdtype, d->F, d->H);  // one packed plane slice
     const size_t W = 3 * S;
     const int32_t* perm = d->perm ? d->perm + static_cast<size_t>(layer) * d->E : nullptr;
     std::vector<char> seen(d->E, 0);
@@ -329,12 +448,12 @@ estream_status estream_pack_experts(const estream_arena_desc* d, int layer, cons
         const int q = pos / d->G, r = pos % d->G;
         const int n_q = std::min(d->G, d->E - q * d->G);
         char* grp = out + static_cast<size_t>(q) * d->G * W;
-        pack_gate_up(static_cast<const char*>(wg) + e * S, d->F, d->H, d->wdtype,
+        pack_gate_up(static_cast<const char*>(wg) + e * Sin, d->F, d->H, d->wdtype,
                      grp + static_cast<size_t>(r) * S);
-        pack_gate_up(static_cast<const char*>(wu) + e * S, d->F, d->H, d->wdtype,
+        pack_gate_up(static_cast<const char*>(wu) + e * Sin, d->F, d->H, d->wdtype,
                      grp + static_cast<size_t>(n_q) * S + static_cast<size_t>(r) * S);
         void* down = grp + 2 * static_cast<size_t>(n_q) * S + static_cast<size_t>(r) * S;
-        scales[pos] = pack_down(static_cast<const char*>(wd) + e * S, d->H, d->F, d->wdtype, down);
+        scales[pos] = pack_down(static_cast<const char*>(wd) + e * Sin, d->H, d->F, d->wdtype, down);
     }
     return ESTREAM_OK;
 }
@@ -343,18 +462,19 @@ estream_status estream_pack_shared(const estream_arena_desc* d, const void* sg, 
                                    const void* sd, void* out) {
     if (!d || !sg || !su || !sd || !out || d->n_shared < 1 || d->F_shared < 1 || d->H < 1)
         return ESTREAM_ERR_INVALID_ARG;
-    if (d->wdtype != ESTREAM_F32 && d->wdtype != ESTREAM_BF16) return ESTREAM_ERR_UNSUPPORTED;
+    if (d->wdtype != ESTREAM_F32 && d->wdtype != ESTREAM_BF16 && d->wdtype != ESTREAM_Q4)
+        return ESTREAM_ERR_UNSUPPORTED;
     if (d->H % 256 != 0 || d->F_shared % 128 != 0) return ESTREAM_ERR_INVALID_ARG;
-    const size_t n_elem = static_cast<size_t>(d->H) * d->F_shared;
-    const size_t S = n_elem * elem_size(d->wdtype);
+    const size_t Sin = master_bytes(d->wdtype, d->F_shared, d->H);
+    const size_t S = plane_slot_bytes(d->wdtype, d->F_shared, d->H);
     const size_t ns = static_cast<size_t>(d->n_shared);
     char* o = static_cast<char*>(out);
     float* scales = reinterpret_cast<float*>(o + 3 * ns * S);
     for (size_t s = 0; s < ns; ++s) {
-        pack_gate_up(static_cast<const char*>(sg) + s * S, d->F_shared, d->H, d->wdtype, o + s * S);
-        pack_gate_up(static_cast<const char*>(su) + s * S, d->F_shared, d->H, d->wdtype,
+        pack_gate_up(static_cast<const char*>(sg) + s * Sin, d->F_shared, d->H, d->wdtype, o + s * S);
+        pack_gate_up(static_cast<const char*>(su) + s * Sin, d->F_shared, d->H, d->wdtype,
                      o + ns * S + s * S);
-        scales[s] = pack_down(static_cast<const char*>(sd) + s * S, d->H, d->F_shared, d->wdtype,
+        scales[s] = pack_down(static_cast<const char*>(sd) + s * Sin, d->H, d->F_shared, d->wdtype,
                               o + 2 * ns * S + s * S);
     }
     return ESTREAM_OK;
@@ -375,6 +495,7 @@ estream_status estream_bind_arena(estream_ctx** out, const estream_arena_desc* d
     if (d->ffn_form != ESTREAM_FFN_AUTO && d->ffn_form != ESTREAM_FFN_SINGLE &&
         d->ffn_form != ESTREAM_FFN_PAIR)
         return ESTREAM_ERR_INVALID_ARG;
+    if (d->ffn_form == ESTREAM_FFN_PAIR && d->wdtype == ESTREAM_Q4) return ESTREAM_ERR_UNSUPPORTED;
     if (d->n_shared < 0 || (d->n_shared > 0 && (d->F_shared < 128 || d->F_shared % 128 != 0 ||
                                                  !d->shared_dev)))
         return ESTREAM_ERR_INVALID_ARG;
@@ -409,9 +530,9 @@ estream_status estream_bind_arena(estream_ctx** out, const estream_arena_desc* d
     c->P = d->B * d->G;
     c->n_groups = (d->E + d->G - 1) / d->G;
     c->es = static_cast<int>(elem_size(d->wdtype));
-    c->S_gu = static_cast<size_t>(d->F) * d->H * c->es;
-    c->S_d = c->S_gu;
-    c->W_e = 3 * c->S_gu;
+    c->S_gu = plane_slot_bytes(d->wdtype, d->F, d->H);
+    c->S_d = plane_slot_bytes(d->wdtype, d->H, d->F);
+    c->W_e = 2 * c->S_gu + c->S_d;
     c->host_pool.assign(d->host_pool, d->host_pool + d->L);
     c->perm.resize(static_cast<size_t>(d->L) * d->E);
     for (int l = 0; l < d->L; ++l)
@@ -527,12 +648,13 @@ estream_status estream_bind_arena(estream_ctx** out, const estream_arena_desc* d
         const CUtensorMapDataType HF = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
         if (d->n_shared > 0) {
             c->shared_scale.resize(d->L);
-            const size_t sp = static_cast<size_t>(d->n_shared) * d->F_shared * d->H * c->es;
+            const size_t sp = static_cast<size_t>(d->n_shared) * plane_slot_bytes(d->wdtype, d->F_shared, d->H);
             for (int l = 0; l < d->L; ++l)
                 c->shared_scale[l] = reinterpret_cast<const float*>(
                     static_cast<const char*>(c->shared_dev[l]) + 3 * sp);
         }
-        if (!f32) {
+        const bool q4 = d->wdtype == ESTREAM_Q4;  // 4-bit planes are read with plain bulk copies
+        if (!f32 && !q4) {
             // tile-major planes: one 128-byte row of 64 elements per tensor row
             const uint64_t plane_rows = static_cast<uint64_t>(c->P) * d->F * d->H / 64;
             tm_ok = tm_ok && encode_tmap_2d(&c->tm_wg, BF, c->plane_g, 64, plane_rows, 128, 64,
@@ -543,13 +665,19 @@ estream_status estream_bind_arena(estream_ctx** out, const estream_arena_desc* d
                                             256) == CUDA_SUCCESS;
             tm_ok = tm_ok && encode_tmap_2d(&c->tm_wd_half, HF, c->plane_d, 64, plane_rows, 128,
                                             64, 128) == CUDA_SUCCESS;
+        }
+        if (!f32) {
             tm_ok = tm_ok && encode_tmap_2d(&c->tm_h, HF, c->h, d->F, static_cast<uint64_t>(R_cap),
                                             static_cast<uint64_t>(d->F) * 2, 64, 128) == CUDA_SUCCESS;
+            if (d->n_shared > 0)
+                tm_ok = tm_ok && encode_tmap_2d(&c->tm_hs, HF, c->h_shared, d->F_shared,
+                                                static_cast<uint64_t>(RS_cap),
+                                                static_cast<uint64_t>(d->F_shared) * 2, 64, 128) ==
+                                     CUDA_SUCCESS;
+        }
+        if (!f32 && !q4) {
             if (d->n_shared > 0) {
                 const int Fs = d->F_shared;
-                tm_ok = tm_ok && encode_tmap_2d(&c->tm_hs, HF, c->h_shared, Fs,
-                                                static_cast<uint64_t>(RS_cap),
-                                                static_cast<uint64_t>(Fs) * 2, 64, 128) == CUDA_SUCCESS;
                 c->tm_sg.resize(d->L);
                 c->tm_su.resize(d->L);
                 c->tm_sd.resize(d->L);
@@ -623,6 +751,7 @@ estream_status fill_bank(estream_ctx* c, int layer, int q, int b, size_t* bytes,
 // expert segments: ESTREAM_FFN_AUTO takes the CTA-pair form (256-record
 // tiles) when a segment holds on average at least ESTREAM_PAIR_MIN_ROWS.
 bool pair_form(const estream_ctx* c, long long rows, int segments) {
+    if (c->d.wdtype == ESTREAM_Q4) return false;  // 4-bit weights: single-SM form only
     if (c->d.ffn_form == ESTREAM_FFN_PAIR) return true;
     if (c->d.ffn_form == ESTREAM_FFN_SINGLE) return false;
     return segments > 0 && rows >= static_cast<long long>(ESTREAM_PAIR_MIN_ROWS) * segments;
@@ -655,6 +784,13 @@ estream_status run_routed(estream_ctx* c, cudaStream_t s, const void* X, int lay
                                  reinterpret_cast<const float*>(c->plane_d), seg, Y, c->out_rows,
                                  c->d.H, c->d.F, max_rows, s);
         c->stats.launches += 2;
+    } else if (c->d.wdtype == ESTREAM_Q4) {
+        rc = launch_expert_ffn_q4(reinterpret_cast<const uint8_t*>(c->plane_g),
+                                  reinterpret_cast<const uint8_t*>(c->plane_u),
+                                  reinterpret_cast<const uint8_t*>(c->plane_d), c->S_gu, c->S_d,
+                                  &c->tm_h, seg, X, c->h, Y, c->out_rows, c->done, c->d.H, c->d.F, 3,
+                                  c->dev_err, c->num_sms, s);
+        c->stats.launches += 1;
     } else {
         rc = pair
                  ? launch_expert_ffn_pair(&c->tm_wg, &c->tm_wu, &c->tm_wd_half, &c->tm_h, seg, X, c->h,
@@ -698,6 +834,13 @@ estream_status run_shared(estream_ctx* c, cudaStream_t s, const void* X,
         if (rc == cudaSuccess)
             rc = launch_down_f32(static_cast<const float*>(c->h_shared), base + 2 * sp, seg, Y,
                                  c->out_shared, c->d.H, Fs, ns * T, s);
+    } else if (c->d.wdtype == ESTREAM_Q4) {
+        const uint8_t* base = static_cast<const uint8_t*>(c->shared_dev[layer]);
+        const size_t S1 = plane_slot_bytes(ESTREAM_Q4, Fs, c->d.H);  // one shared expert's plane
+        const size_t sp = static_cast<size_t>(ns) * S1;
+        rc = launch_expert_ffn_q4(base, base + sp, base + 2 * sp, S1, S1, &c->tm_hs, seg, X,
+                                  c->h_shared, Y, c->out_shared, c->sh_done, c->d.H, Fs, 3,
+                                  c->dev_err, c->num_sms, s);
     } else {
         rc = pair_form(c, T, 1)
                  ? launch_expert_ffn_pair(&c->tm_sg[layer], &c->tm_su[layer], &c->tm_sd_half[layer],

@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(_PKG, "libestream.so")
 
 OK, ERR_INVALID_ARG, ERR_CAPACITY, ERR_NOT_BOUND, ERR_CUDA, ERR_PAGER, ERR_TIMEOUT, \
     ERR_DEVICE, ERR_UNSUPPORTED = range(9)
-F32, BF16 = 0, 1
+F32, BF16, Q4 = 0, 1, 2
 SCHED_AFTER_ROUTING, SCHED_PREFETCH = 0, 1
 FFN_AUTO, FFN_SINGLE, FFN_PAIR = 0, 1, 2
 PAIR_MIN_ROWS = 160

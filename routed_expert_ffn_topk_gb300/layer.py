@@ -22,10 +22,11 @@ class BoundLayerStack:
 
     def __init__(self, wl: Workload, mode: str = "resident", perm=None, G=None, B=None,
                  deterministic=False, schedule=es.SCHED_AFTER_ROUTING, T_max=None, k_max=None,
-                 Q=1, ffn_form=es.FFN_AUTO, device="cuda"):
+                 Q=1, ffn_form=es.FFN_AUTO, wdtype=None, device="cuda"):
         cfg = wl.cfg
         self.cfg, self.wl, self.mode = cfg, wl, mode
-        self.dtype = es.BF16 if cfg.dtype == "bf16" else es.F32
+        # wdtype=es.Q4 packs the (bf16) weights of a bf16 workload as 4-bit experts
+        self.dtype = wdtype if wdtype is not None else (es.BF16 if cfg.dtype == "bf16" else es.F32)
         L = len(wl.layers)
         G = G or cfg.G
         if mode == "resident":

@@ -40,3 +40,32 @@ def oracle_layer(wl: W.Workload, layer: int, X_cpu, rows=None, residual=None):
 
 def device():
     return torch.device("cuda", 0)
+
+
+def q4_weights(lw):
+    """The weights a 4-bit layer computes with, dequantised by the oracle:
+    gate/up with bf16 block scales, down pre-scaled by 2^s with fp16 scales."""
+    def gu(W):
+        return np.stack([oracle.q4_dequantize(*oracle.q4_quantize(W[e], fp16=False)) for e in range(W.shape[0])])
+
+    def dn(W):
+        out = []
+        for e in range(W.shape[0]):
+            s = oracle.down_scale_exp(W[e])
+            c, d = oracle.q4_quantize(W[e], fp16=True, scale_exp=s)
+            out.append(oracle.q4_dequantize(c, d, scale_exp=s))
+        return np.stack(out)
+    shared = None
+    if lw.Sg is not None:
+        shared = (gu(lw.Sg), gu(lw.Su), dn(lw.Sd))
+    return gu(lw.Wg), gu(lw.Wu), dn(lw.Wd), shared
+
+
+def oracle_layer_q4(wl: W.Workload, layer: int, X_cpu, rows=None, dq=None):
+    """Oracle routing + Eq. 2 with the dequantised 4-bit weights (X widened
+    exactly to fp32)."""
+    cfg = wl.cfg
+    Wg, Wu, Wd, shared = dq if dq is not None else q4_weights(wl.layers[layer])
+    ids, alpha = oracle.route_topk(wl.logits[layer].numpy(), cfg.k, cfg.renorm)
+    Xf = torch.as_tensor(X_cpu).float().numpy()
+    return oracle.moe_layer_rows(Xf, Wg, Wu, Wd, ids, alpha, rows=rows, shared=shared)
