@@ -259,7 +259,7 @@ def run_ours(args, rank, world, local_rank):
 
     stack = None
 
-    def timed_loop(st, steps, per_step_hook=None):
+    def timed_loop(st, steps, per_step_hook=None, graph=None):
         times = []
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(steps)]
@@ -268,7 +268,10 @@ def run_ours(args, rank, world, local_rank):
             if per_step_hook:
                 per_step_hook()
             ev[i][0].record(stream)
-            step(st)
+            if graph is not None:
+                graph.replay()
+            else:
+                step(st)
             ev[i][1].record(stream)
         torch.cuda.synchronize()
         for a, b in ev:
@@ -282,19 +285,32 @@ def run_ours(args, rank, world, local_rank):
     for_all(es.reset_stats)
     for_all(es.set_timing, True)
     clocks = ClockSampler(local_rank, None)
+    graph, graph_note = None, "eager (--no-graph)"
     with clocks:
         t_end = time.time() + 0.6   # let the sampler see the GPU under this load
         while time.time() < t_end:
             step(stack)
         torch.cuda.synchronize()
-        barrier(world)
-        torch.cuda.synchronize()
+        # per-kernel times from the library's own CUDA events (eager steps)
         for_all(es.reset_stats)
-        times = timed_loop(stack, args.steps)
+        timed_loop(stack, args.steps)
+        torch.cuda.synchronize()
+        stats = merged_stats()
+        for_all(es.set_timing, False)
+        assert all(e == es.OK for e in for_all(es.get_device_error))
+        # the timed step: one CUDA-graph replay of the whole step (the L2 flush
+        # stays outside the graph); eager launches if capture is refused
+        if not args.no_graph:
+            try:
+                graph = capture_graph(step)
+                graph_note = "cuda-graph replay"
+            except Exception as ex:  # capture refused: time eager launches
+                graph, graph_note = None, f"eager (graph capture failed: {type(ex).__name__})"
+        barrier(world)
+        torch.cuda.synchronize()
+        times = timed_loop(stack, args.steps, graph=graph)
         torch.cuda.synchronize()
         barrier(world)
-    stats = merged_stats()
-    for_all(es.set_timing, False)
     assert all(e == es.OK for e in for_all(es.get_device_error))
     total_ms = max_over_ranks(sum(times), world, dev)
     ms_per_step = total_ms / args.steps
@@ -360,7 +376,10 @@ def run_ours(args, rank, world, local_rank):
         Xbuf[0].copy_(Xh, non_blocking=True)
         for l in range(L):
             logits[l].copy_(lgh[l], non_blocking=True)
-        step(stack)
+        if graph is not None:
+            graph.replay()
+        else:
+            step(stack)
         Yh.copy_(Y[L - 1], non_blocking=True)
 
     for _ in range(3):
@@ -378,6 +397,8 @@ def run_ours(args, rank, world, local_rank):
     e2e_ms = max_over_ranks(sum(e_times), world, dev) / args.steps
     h2d_b = Xh.numel() * Xh.element_size() + sum(t.numel() * 4 for t in lgh)
     d2h_b = Yh.numel() * 4
+    torch.cuda.synchronize()
+    graph = None  # the graph references the contexts' events: release it before they go
     for st in stacks:
         st.close()
 
@@ -400,7 +421,7 @@ def run_ours(args, rank, world, local_rank):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16 gate/up, fp16 down (fp32 accumulate)" if cfg.dtype == "bf16" else "f32",
         "data": "synthetic (seeded; random-init weights)",
-        "config": workload_config(cfg, world, mode),
+        "config": {**workload_config(cfg, world, mode), "step": graph_note},
         "tflops": round(tflops, 1), "grouped_gemm_tflops": round(gemm_tflops, 1),
         "frac_bf16_peak": round(gemm_tflops / peaks["bf16_tflops"], 4),
         "roofline": roof, "kernels": kernels,
@@ -413,6 +434,24 @@ def run_ours(args, rank, world, local_rank):
         "paged": paged,
     }
     return line
+
+
+def capture_graph(fn):
+    """Capture fn() (launches on torch's current stream) into a CUDA graph,
+    after two warm runs on the capture side stream."""
+    import torch
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(2):
+            fn()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    torch.cuda.synchronize()
+    return g
 
 
 def measure_router(cfg, X0, dev, stream, flush, peaks, steps):
@@ -775,6 +814,7 @@ def main(argv=None):
     ap.add_argument("--paged-steps", type=int, default=10)
     ap.add_argument("--no-paged", action="store_true")
     ap.add_argument("--no-q4", action="store_true", help="skip the 4-bit-expert measurement")
+    ap.add_argument("--no-graph", action="store_true", help="time eager launches, not a CUDA-graph replay")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--pipeline-study", action="store_true",
                     help="also measure the loading schedules and the (G, B) auto-configuration")

@@ -30,8 +30,9 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 struct RouteWorkspace {
     size_t err_off;      // int32 device error word
     size_t sync_off;     // int32 grid-barrier counter of the fused route kernel
-    size_t hist_off;     // int32 [P+1][nchunk]: per-chunk counts, then per-chunk bases
+    size_t hist_off;     // int32 [P+1][nchunk]: per-chunk counts, then bases inside the slot
     size_t mblk_off;     // int32 [P+2]: exclusive prefix of ceil(count[s]/kBM), s < P
+    size_t tot_off;      // int32 [P+1]: per-slot totals
     size_t total;
     int nchunk;
 };

@@ -15,11 +15,13 @@
 //   1. one CTA per chunk, one warp per token: softmax top-k, alpha, and the
 //      chunk's slot counts (shared-memory atomics; counts are order-free),
 //      written bucket-major as hist[slot][chunk];
-//   2. CTA 0: per slot, a warp scan over chunks gives each chunk's base inside
-//      the slot; a block scan over slot totals gives the slot offsets, and the
-//      m-block prefix the expert kernel schedules by;
-//   3. one CTA per chunk: ranks inside a warp by __match_any_sync, across
-//      warps in ascending order, so the placement is the stable one
+//   2. every warp of the grid scans whole slots (a warp per slot): each
+//      chunk's base inside the slot, and the slot's total;
+//   3. every CTA forms the slot offsets and the m-block prefix (the expert
+//      kernel schedules by it) from the slot totals with block scans in its
+//      shared memory -- CTA 0 also stores them -- then, one CTA per chunk,
+//      places the chunk's records: ranks inside a warp by __match_any_sync,
+//      across warps in ascending order, so the placement is the stable one
 //      Algorithm 1 produces.
 #include <cuda_bf16.h>
 
@@ -205,50 +207,35 @@ __device__ int block_exclusive_scan(int* data, int n, int* warp_sums) {
     return total;
 }
 
-// One CTA. hist[b][c] (counts, bucket-major) becomes the base position of
-// chunk c's first record of slot b; offsets[b] = sum of counts of slots < b;
-// mblk[s] = sum over slots < s of ceil(count/kBM) for s <= P (the trailing
-// bucket has no GEMM work). Each warp scans whole slots, 32 chunks per step.
-__device__ void scan_phase(int32_t* __restrict__ hist, int nchunk, int P, int R,
-                           int32_t* __restrict__ offsets, int32_t* __restrict__ mblk, int* smem) {
-    const int nb = P + 1;
-    int* cnt = smem;                 // [nb] slot totals -> slot offsets
-    int* mb = smem + nb;             // [nb] m-blocks -> m-block prefix
-    int* warp_sums = smem + 2 * nb;  // [33]
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int nwarps = blockDim.x >> 5;
-    for (int b = warp; b < nb; b += nwarps) {
+// Grid-wide: warp g of the grid scans slots g, g + (warps in the grid), ...:
+// hist[b][c] (counts, bucket-major) becomes the base of chunk c's first
+// record inside slot b, and totals[b] the slot's count. Lane l handles a
+// contiguous run of chunks, so its loads are independent of one another.
+__device__ void scan_slots(int32_t* __restrict__ hist, int nchunk, int nb,
+                           int32_t* __restrict__ totals) {
+    const int lane = threadIdx.x & 31;
+    const int gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int nw = gridDim.x * (blockDim.x >> 5);
+    const int per = (nchunk + 31) / 32;
+    for (int b = gw; b < nb; b += nw) {
         int32_t* row = hist + static_cast<size_t>(b) * nchunk;
-        int carry = 0;
-        for (int c0 = 0; c0 < nchunk; c0 += 32) {
-            const int c = c0 + lane;
-            const int v = c < nchunk ? row[c] : 0;
-            int incl = v;
+        const int lo = min(nchunk, lane * per);
+        const int hi = min(nchunk, lo + per);
+        int local = 0;
+        for (int c = lo; c < hi; ++c) local += __ldcg(row + c);
+        int incl = local;
 #pragma unroll
-            for (int d = 1; d < 32; d <<= 1) {
-                const int o = __shfl_up_sync(0xffffffffu, incl, d);
-                if (lane >= d) incl += o;
-            }
-            if (c < nchunk) row[c] = carry + incl - v;  // base inside the slot
-            carry += __shfl_sync(0xffffffffu, incl, 31);
+        for (int d = 1; d < 32; d <<= 1) {
+            const int o = __shfl_up_sync(0xffffffffu, incl, d);
+            if (lane >= d) incl += o;
         }
-        if (lane == 0) {
-            cnt[b] = carry;
-            mb[b] = (b < P) ? (carry + kBM - 1) / kBM : 0;
+        int run = incl - local;
+        for (int c = lo; c < hi; ++c) {
+            const int v = __ldcg(row + c);
+            row[c] = run;
+            run += v;
         }
-    }
-    __syncthreads();
-    block_exclusive_scan(cnt, nb, warp_sums);
-    block_exclusive_scan(mb, nb, warp_sums);
-    for (int b = threadIdx.x; b < nb; b += blockDim.x) {
-        offsets[b] = cnt[b];
-        mblk[b] = mb[b];
-    }
-    __syncthreads();
-    for (int x = threadIdx.x; x < nb * nchunk; x += blockDim.x) hist[x] += cnt[x / nchunk];
-    if (threadIdx.x == 0) {
-        offsets[P + 1] = R;
-        mblk[P + 1] = mb[P];
+        if (lane == 31) totals[b] = incl;
     }
 }
 
@@ -256,9 +243,9 @@ __device__ void scan_phase(int32_t* __restrict__ hist, int nchunk, int P, int R,
 // (c+1)*kChunkTokens)) in passes of one route per thread.
 __device__ void scatter_chunk(int c, int nchunk, const int32_t* __restrict__ topk_ids,
                               const int32_t* __restrict__ phi, int P, int k, int R,
-                              const int32_t* __restrict__ base, int32_t* __restrict__ rec_tok,
-                              int32_t* __restrict__ rec_route, int32_t* __restrict__ rec_pos,
-                              int* cnt) {
+                              const int32_t* __restrict__ base, const int* slot_off,
+                              int32_t* __restrict__ rec_tok, int32_t* __restrict__ rec_route,
+                              int32_t* __restrict__ rec_pos, int* cnt) {
     const int nb = P + 1;
     for (int b = threadIdx.x; b < nb; b += blockDim.x) cnt[b] = 0;
     __syncthreads();
@@ -287,7 +274,7 @@ __device__ void scatter_chunk(int c, int nchunk, const int32_t* __restrict__ top
                 const int before = valid ? cnt[b] : 0;
                 __syncwarp();
                 if (valid && lane == leader) cnt[b] = before + __popc(peers);
-                pos = base[static_cast<size_t>(b) * nchunk + c] + before + rank;
+                pos = slot_off[b] + __ldcg(base + static_cast<size_t>(b) * nchunk + c) + before + rank;
             }
             __syncthreads();
         }
@@ -335,8 +322,8 @@ __global__ void __launch_bounds__(kRouteThreads) k_route_fused(
     const int32_t* __restrict__ phi, int P, int32_t* __restrict__ topk_ids,
     float* __restrict__ alpha, int32_t* __restrict__ offsets, int32_t* __restrict__ rec_tok,
     int32_t* __restrict__ rec_route, int32_t* __restrict__ rec_pos, int32_t* __restrict__ hist,
-    int32_t* __restrict__ mblk, int32_t* __restrict__ done, int* __restrict__ sync,
-    int* __restrict__ err, int nchunk) {
+    int32_t* __restrict__ mblk, int32_t* __restrict__ totals, int32_t* __restrict__ done,
+    int* __restrict__ sync, int* __restrict__ err, int nchunk) {
     extern __shared__ int smem[];
     __shared__ int ok_flag;
     const int R = T * k;
@@ -353,18 +340,39 @@ __global__ void __launch_bounds__(kRouteThreads) k_route_fused(
         __syncthreads();
     }
     if (!grid_barrier(sync, 1, err, &ok_flag)) return;
-    // 2. prefix sums (one CTA)
-    if (blockIdx.x == 0) scan_phase(hist, nchunk, P, R, offsets, mblk, smem);
+    // 2. per-slot scans over chunks, spread over every warp of the grid
+    scan_slots(hist, nchunk, nb, totals);
     if (!grid_barrier(sync, 2, err, &ok_flag)) return;
-    // 3. stable placement, one chunk per CTA at a time; the expert kernel's
+    // 3. slot offsets and m-block prefix from the totals (in every CTA), then
+    //    stable placement, one chunk per CTA at a time; the expert kernel's
     //    per-m-block counters start from zero
-    if (done) {
-        const int mb_total = mblk[P];
+    int* off = smem;                 // [nb] slot offsets
+    int* mb = smem + nb;             // [nb] m-block prefix, then the placement's counters
+    int* warp_sums = smem + 2 * nb;  // [33]
+    for (int b = threadIdx.x; b < nb; b += blockDim.x) {
+        const int v = __ldcg(totals + b);
+        off[b] = v;
+        mb[b] = b < P ? (v + kBM - 1) / kBM : 0;
+    }
+    __syncthreads();
+    block_exclusive_scan(off, nb, warp_sums);
+    const int mb_total = block_exclusive_scan(mb, nb, warp_sums);
+    if (blockIdx.x == 0) {
+        for (int b = threadIdx.x; b < nb; b += blockDim.x) {
+            offsets[b] = off[b];
+            mblk[b] = mb[b];
+        }
+        if (threadIdx.x == 0) {
+            offsets[P + 1] = R;
+            mblk[P + 1] = mb_total;
+        }
+    }
+    if (done)
         for (int m = blockIdx.x * blockDim.x + threadIdx.x; m < mb_total; m += gridDim.x * blockDim.x)
             done[m] = 0;
-    }
+    __syncthreads();
     for (int c = blockIdx.x; c < nchunk; c += gridDim.x)
-        scatter_chunk(c, nchunk, topk_ids, phi, P, k, R, hist, rec_tok, rec_route, rec_pos, smem);
+        scatter_chunk(c, nchunk, topk_ids, phi, P, k, R, hist, off, rec_tok, rec_route, rec_pos, mb);
 }
 
 __global__ void k_identity_map(int T, int n_shared, int32_t* __restrict__ offsets,
@@ -398,6 +406,8 @@ RouteWorkspace route_workspace_layout(int T, int k, int P) {
     off = align_up(off + sizeof(int32_t) * static_cast<size_t>(w.nchunk > 0 ? w.nchunk : 1) * (P + 1), 256);
     w.mblk_off = off;
     off = align_up(off + sizeof(int32_t) * static_cast<size_t>(P + 2), 256);
+    w.tot_off = off;
+    off = align_up(off + sizeof(int32_t) * static_cast<size_t>(P + 1), 256);
     w.total = off;
     return w;
 }
@@ -412,6 +422,7 @@ cudaError_t launch_route_build(const float* logits, int T, int E, int k, int ren
     int* err = reinterpret_cast<int*>(base + w.err_off);
     int32_t* hist = reinterpret_cast<int32_t*>(base + w.hist_off);
     int32_t* mblk = reinterpret_cast<int32_t*>(base + w.mblk_off);
+    int32_t* totals = reinterpret_cast<int32_t*>(base + w.tot_off);
     const int R = T * k;
     const int nb = P + 1;
     int launches = 0;
@@ -441,7 +452,7 @@ cudaError_t launch_route_build(const float* logits, int T, int E, int k, int ren
     const int grid = std::max(1, std::min(co_resident, w.nchunk));
     const size_t smem = sizeof(int) * (2 * static_cast<size_t>(nb) + 33);
     void* args[] = {&logits, &T, &E, &k, &renorm, &phi, &P, &topk_ids, &alpha, &offsets,
-                    &rec_tok, &rec_route, &rec_pos, &hist, &mblk, &done, &sync, &err,
+                    &rec_tok, &rec_route, &rec_pos, &hist, &mblk, &totals, &done, &sync, &err,
                     const_cast<int*>(&w.nchunk)};
     rc = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(k_route_fused), grid,
                                      kRouteThreads, args, smem, stream);

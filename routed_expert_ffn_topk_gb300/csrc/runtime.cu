@@ -1243,6 +1243,9 @@ void estream_unbind(estream_ctx* c) {
         cudaFree(c->ws);
     }
     delete c;
+    // an error of the teardown itself (e.g. an event still referenced by a
+    // caller's CUDA graph) must not surface in the caller's next CUDA call
+    (void)cudaGetLastError();
 }
 
 estream_status estream_cast_f32_bf16(const float* src, void* dst, size_t n, void* cuda_stream) {
