@@ -32,9 +32,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # capture summarised in profiles/k_expert_ffn_olmoe_resident.md. Reported only while
 # the kernel source is the one that was captured.
 PROFILED_TRAFFIC = {
-    "c2": {"kernel_sha256_16": "ab12bb3771a2a949", "bytes": 877929728},
+    "c2": {"kernel_sha256_16": "375060dedc8f72dc", "bytes": 877335040},
 }
-KERNEL_SRC = os.path.join(ROOT, "routed_expert_ffn_topk_gb300", "csrc", "expert_gemm.cu")
+KERNEL_SRC = [os.path.join(ROOT, "routed_expert_ffn_topk_gb300", "csrc", f)
+              for f in ("expert_gemm.cu", "tc_ptx.cuh")]
 
 
 def profiled_traffic(config: str):
@@ -42,9 +43,11 @@ def profiled_traffic(config: str):
     rec = PROFILED_TRAFFIC.get(config)
     if not rec:
         return None
-    with open(KERNEL_SRC, "rb") as f:
-        sha = hashlib.sha256(f.read()).hexdigest()[:16]
-    return rec["bytes"] if sha == rec["kernel_sha256_16"] else None
+    h = hashlib.sha256()
+    for path in KERNEL_SRC:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return rec["bytes"] if h.hexdigest()[:16] == rec["kernel_sha256_16"] else None
 
 
 def load_peaks():
