@@ -258,10 +258,11 @@ estream_status estream_bind_arena(estream_ctx** out, const estream_arena_desc* d
  * fp16 (down); codes q = clamp(rint(w / d) + 8, 0, 15) (fp32 division, ties
  * to even); a zero block has d = 0 and codes 8. The weight used is
  * (q - 8) * d, exact in the operand type. Layout: tile-major boxes of
- * (128 rows of gate/up or 256 rows of down) x 64 weights, each box being the
- * rows' codes (32 bytes a row: in its byte-word w, bits 4i..4i+3 hold weight
- * 8w + 2i and bits 16 + 4i.. weight 8w + 2i + 1) followed by the rows' two
- * block scales (uint16 bits); W_e = 3 * H * F * 9 / 16 bytes.
+ * (R = 128 rows of gate/up or 256 rows of down) x 64 weights, each box
+ * being two column blocks of codes -- block j holds every row's 16 bytes of
+ * weights 32j..32j+31 (in byte-word w of a row, bits 4i..4i+3 hold weight
+ * 32j + 8w + 2i and bits 16 + 4i.. weight 32j + 8w + 2i + 1) -- followed by
+ * the rows' two block scales (uint16 bits); W_e = 3 * H * F * 9 / 16 bytes.
  * wg, wu: host [E][F][H]; wd: host [E][H][F] (fp32 for F32, bf16 for BF16 and Q4);
  * host_pool_out: host, estream_pool_bytes(...) bytes (pinned if streamed).
  * Only d->E, H, F, G, wdtype and perm (row `layer`) are read. Pools must be

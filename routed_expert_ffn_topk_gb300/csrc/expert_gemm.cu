@@ -643,11 +643,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 // 4-bit expert weights, single-SM form
 // ----------------------------------------------------------------------------
 // The weight planes hold Q4_0-style blocks (section 4 of the paper stores
-// expert matrices as weight-only GGUF Q4_0): per (n-block, k-block) box, the
-// 4-bit codes of each row's 64 weights (32 bytes; in byte-word w, bits 4i..
-// 4i+3 hold k = 8w + 2i and bits 16 + 4i.. hold k = 8w + 2i + 1) followed by
-// the row's two block scales (bf16 for gate and up, fp16 for down), a value
-// being (q - 8) * d. Roles: warp 0 streams packed boxes with plain bulk
+// expert matrices as weight-only GGUF Q4_0): per (n-block, k-block) box of
+// R rows, two column blocks of codes -- block j holds each row's 16 bytes of
+// weights 32j..32j+31 (in byte-word w, bits 4i..4i+3 hold k = 32j + 8w + 2i
+// and bits 16 + 4i.. hold k = 32j + 8w + 2i + 1), so a row's halves sit
+// R * 16 bytes apart -- followed by the rows' two block scales (bf16 for gate
+// and up, fp16 for down), a value being (q - 8) * d. Roles: warp 0 streams packed boxes with plain bulk
 // copies into a 3-deep ring (a stage is 9 KB instead of 32 KB of bf16);
 // warps 10-13 expand each packed stage into the 128-byte-swizzled bf16/fp16
 // B tile of the 4-deep MMA ring -- the paper's "vector workers decode them into
@@ -691,18 +692,20 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
         : "memory");
 }
 
-// Expand one packed row (64 codes, two block scales) into 64 operands of
-// B-tile row r: 8 chunks of 16 bytes, chunk c at (c ^ (r mod 8)) * 16. A code
+// Expand one packed row (64 codes: 16 bytes at codes_lo, 16 at codes_hi; two
+// block scales) into 64 operands of B-tile row r: 8 chunks of 16 bytes,
+// chunk c at (c ^ (r mod 8)) * 16. A code
 // q becomes the number 128 + q (bf16 0x4300 | q) or 1024 + q (fp16
 // 0x6400 | q) by bit placement; subtracting 136 (1032) gives q - 8 and the
 // multiplication by d the weight, both exact.
 template <bool kFp16>
-__device__ __forceinline__ void expand_row(uint32_t codes, uint32_t scales, uint32_t dst_row, int r) {
+__device__ __forceinline__ void expand_row(uint32_t codes_lo, uint32_t codes_hi, uint32_t scales,
+                                           uint32_t dst_row, int r) {
     uint32_t w[8], sc;
     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]) : "r"(codes));
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]) : "r"(codes_lo));
     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7]) : "r"(codes + 16));
+                 : "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7]) : "r"(codes_hi));
     asm volatile("ld.shared.u32 %0, [%1];" : "=r"(sc) : "r"(scales));
     const uint32_t magic = kFp16 ? 0x64006400u : 0x43004300u;
     const uint32_t offset = kFp16 ? 0x64086408u : 0x43084308u;
@@ -771,9 +774,11 @@ __device__ void role_convert(const FfnArgs& a, const TileWalk& w, Ring ring, Rin
             if (gu) {
                 const uint32_t box = pb + (ct < 128 ? 0u : static_cast<uint32_t>(kQBoxGU));
                 const int r = ct & 127;
-                expand_row<false>(box + r * 32, box + 4096 + r * 4, bb + ct * kRowBytes, ct);
+                expand_row<false>(box + r * 16, box + 2048 + r * 16, box + 4096 + r * 4,
+                                  bb + ct * kRowBytes, ct);
             } else {
-                expand_row<true>(pb + ct * 32, pb + 8192 + ct * 4, bb + ct * kRowBytes, ct);
+                expand_row<true>(pb + ct * 16, pb + 4096 + ct * 16, pb + 8192 + ct * 4,
+                                 bb + ct * kRowBytes, ct);
             }
             fence_proxy_async();
             __syncwarp();

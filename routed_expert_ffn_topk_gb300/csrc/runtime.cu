@@ -208,10 +208,13 @@ uint16_t float_to_bf16_bits_rne(float x) {
 }
 
 // One (n-block, k-block) box of a 4-bit plane: tile_rows rows x 64 weights of
-// src (fp32 values, row stride cols), written as tile_rows x 32 code bytes
-// (byte-word w of a row: bits 4i..4i+3 = code of weight 8w + 2i, bits
-// 16 + 4i.. = code of weight 8w + 2i + 1) then tile_rows x 2 scales (uint16
-// bits of bf16, or of fp16 when fp16 is set).
+// src (fp32 values, row stride cols), written as two column blocks of codes --
+// block j holds, for every row, the 16 bytes of weights 32j..32j+31 (byte-word
+// w of a block row: bits 4i..4i+3 = code of weight 32j + 8w + 2i, bits
+// 16 + 4i.. = code of weight 32j + 8w + 2i + 1) -- then tile_rows x 2 scales
+// (uint16 bits of bf16, or of fp16 when fp16 is set). A row's two 16-byte
+// halves sit tile_rows * 16 bytes apart, so threads reading consecutive rows
+// read consecutive 16-byte words.
 void pack_q4_box(const float* src, int cols, int tile_rows, bool fp16, uint8_t* dst) {
     uint8_t* codes = dst;
     uint16_t* scales = reinterpret_cast<uint16_t*>(dst + static_cast<size_t>(tile_rows) * 32);
@@ -249,7 +252,8 @@ void pack_q4_box(const float* src, int cols, int tile_rows, bool fp16, uint8_t* 
                 word |= static_cast<uint32_t>(q[8 * w + 2 * i]) << (4 * i);
                 word |= static_cast<uint32_t>(q[8 * w + 2 * i + 1]) << (16 + 4 * i);
             }
-            std::memcpy(codes + static_cast<size_t>(r) * 32 + 4 * w, &word, sizeof(word));
+            const size_t block = static_cast<size_t>(w / 4) * tile_rows * 16;
+            std::memcpy(codes + block + static_cast<size_t>(r) * 16 + 4 * (w % 4), &word, sizeof(word));
         }
     }
 }

@@ -17,9 +17,10 @@ def es():
 
 def decode_plane(raw, rows, cols, tile_rows, fp16):
     """Codes [rows][cols] and scales [rows][cols/32] (fp32) of one packed
-    plane: tile-major boxes of tile_rows x 64 weights, each the rows' 32 code
-    bytes (byte-word w: bits 4i.. weight 8w+2i, bits 16+4i.. weight 8w+2i+1)
-    then the rows' two scales."""
+    plane: tile-major boxes of tile_rows x 64 weights, each two column blocks
+    of codes (block j: every row's 16 bytes of weights 32j..32j+31; byte-word w:
+    bits 4i.. weight 32j+8w+2i, bits 16+4i.. weight 32j+8w+2i+1) then the
+    rows' two scales."""
     box = tile_rows * 36
     codes = np.zeros((rows, cols), dtype=np.uint8)
     scales = np.zeros((rows, cols // 32), dtype=np.float32)
@@ -27,10 +28,12 @@ def decode_plane(raw, rows, cols, tile_rows, fp16):
     for nb in range(rows // tile_rows):
         for kb in range(cols // 64):
             b = raw[o:o + box]
-            words = b[:tile_rows * 32].view(np.uint32).reshape(tile_rows, 8)
-            for i in range(4):
-                codes[nb * tile_rows:(nb + 1) * tile_rows, kb * 64 + 2 * i:kb * 64 + 64:8] = (words >> (4 * i)) & 0xF
-                codes[nb * tile_rows:(nb + 1) * tile_rows, kb * 64 + 2 * i + 1:kb * 64 + 64:8] = (words >> (16 + 4 * i)) & 0xF
+            for j in range(2):
+                words = b[j * tile_rows * 16:(j + 1) * tile_rows * 16].view(np.uint32).reshape(tile_rows, 4)
+                c0 = kb * 64 + 32 * j
+                for i in range(4):
+                    codes[nb * tile_rows:(nb + 1) * tile_rows, c0 + 2 * i:c0 + 32:8] = (words >> (4 * i)) & 0xF
+                    codes[nb * tile_rows:(nb + 1) * tile_rows, c0 + 2 * i + 1:c0 + 32:8] = (words >> (16 + 4 * i)) & 0xF
             sb = b[tile_rows * 32:].view(np.uint16).reshape(tile_rows, 2)
             if fp16:
                 sv = sb.view(np.float16).astype(np.float32)
