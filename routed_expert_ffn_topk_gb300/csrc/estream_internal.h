@@ -41,12 +41,13 @@ RouteWorkspace route_workspace_layout(int T, int k, int P);
 // Enqueue the full route build (K1). `ws` must hold route_workspace_layout(T,k,P).
 // rec_pos (optional, [T*k]) receives, for route i, its position in the CSR.
 // done (optional) is zeroed over the route map's m-blocks (mblk[P] ints) for
-// the fused expert kernel's m-block counters.
+// the fused expert kernel's m-block counters, and tickets[0..n_tickets) (the
+// dynamic tile counters of the call's expert-kernel launches) as well.
 cudaError_t launch_route_build(const float* logits, int T, int E, int k, int renorm,
                                const int32_t* phi, int P, int32_t* topk_ids, float* alpha,
                                int32_t* offsets, int32_t* rec_tok, int32_t* rec_route,
-                               int32_t* rec_pos, int32_t* done, void* ws,
-                               cudaStream_t stream, int* n_launches);
+                               int32_t* rec_pos, int32_t* done, int32_t* tickets, int n_tickets,
+                               void* ws, cudaStream_t stream, int* n_launches);
 
 // Identity route map for the shared experts: n_shared segments of T rows,
 // rec_tok[p] = p mod T, offsets[s] = s*T, mblk[s] = s*ceil(T/kBM); zeroes
@@ -75,13 +76,15 @@ struct GemmSegments {
 //   down:    Y[tok(p), :] += alpha(p) * scale(seg) * (h[p] Wd_slot^T) (fp16 MMA), or
 //            out_rows[p, :] = ... when out_rows != null (deterministic mode).
 // X: device [T][H] bf16 (16-byte aligned rows); h: [rows][F] fp16; done: one
-// zeroed int per absolute m-block of the route map (mblk indices).
+// zeroed int per absolute m-block of the route map (mblk indices); ticket: a
+// zeroed int for this launch's dynamic tile hand-out, or null for a static
+// assignment.
 // tm_h: TMA map of h ([rows][F] fp16, 64 x 128 boxes, 128-byte swizzle).
 cudaError_t launch_expert_ffn(const CUtensorMap* tm_wg, const CUtensorMap* tm_wu,
                               const CUtensorMap* tm_wd, const CUtensorMap* tm_h,
                               const GemmSegments& seg, const void* X,
-                              void* h, float* Y, float* out_rows, int* done, int H, int F,
-                              int phases, int* dev_err, int num_sms, cudaStream_t stream);
+                              void* h, float* Y, float* out_rows, int* done, int* ticket, int H,
+                              int F, int phases, int* dev_err, int num_sms, cudaStream_t stream);
 
 // The same operator on CTA pairs (clusters of two, tcgen05.mma.cta_group::2,
 // 256-record pair tiles); tm_wd_half maps the down planes with 64 x 128
@@ -98,8 +101,8 @@ cudaError_t launch_expert_ffn_pair(const CUtensorMap* tm_wg, const CUtensorMap* 
 cudaError_t launch_expert_ffn_q4(const uint8_t* plane_g, const uint8_t* plane_u, const uint8_t* plane_d,
                                  size_t S_gu, size_t S_d, const CUtensorMap* tm_h,
                                  const GemmSegments& seg, const void* X, void* h, float* Y,
-                                 float* out_rows, int* done, int H, int F, int phases, int* dev_err,
-                                 int num_sms, cudaStream_t stream);
+                                 float* out_rows, int* done, int* ticket, int H, int F, int phases,
+                                 int* dev_err, int num_sms, cudaStream_t stream);
 
 // fp32 path (CUDA-core FMA): the same two steps for fp32 X and weights.
 // Weight planes are [slots][F][H] (gate, up) and [slots][H][F] (down).

@@ -69,9 +69,11 @@ constexpr int kOffA = 0;
 constexpr int kOffB = kStages * kTileABytes;
 constexpr int kOffBar = kOffB + kStages * kTileBBytes;
 // barriers: full[kStages], empty[kStages], acc_full[2], acc_empty[2], drain
-constexpr int kNumBars = 2 * kStages + 5;
+// + tile ring: tile_full[4], tile_empty[4]
+constexpr int kNumBars = 2 * kStages + 5 + 2 * 4;
 constexpr int kOffMisc = kOffBar + 8 * kNumBars;  // tmem base, abort flag
-constexpr int kOffTable = kOffMisc + 16;
+constexpr int kOffRing = kOffMisc + 16;           // tile ring: 4 ints
+constexpr int kOffTable = kOffRing + 16;
 
 size_t gemm_smem_bytes(int seg_count) {
     return 1024 + kOffTable + sizeof(int) * static_cast<size_t>(seg_count + 1);
@@ -173,6 +175,7 @@ struct FfnArgs {
     float* Y;                // [T][H] accumulator
     float* out_rows;         // deterministic mode: [rows][H], else null
     int* done;               // per absolute m-block: epilogue-warp publications of gate/up tiles
+    int* ticket;             // dynamic tile counter (zero at launch), or null for the static order
     int* dev_err;
     int H, F;
     int phases;              // bit 0: gate/up tiles, bit 1: down tiles
@@ -257,19 +260,66 @@ struct Ring {
     __device__ __forceinline__ uint32_t empty(int s) const { return empty0 + 8u * s; }
 };
 
-// This CTA's walk over the tile list (tile_of order) and the decode of a tile.
+// This CTA's walk over the tile list and the decode of a tile. With a ticket
+// counter (zero at launch) tiles are handed out dynamically: the producer
+// thread takes tickets from the counter -- CTAs that run faster take more
+// tiles, absorbing the spread of tile times -- and publishes each in a
+// shared-memory ring that every other role reads in order. Tickets are taken in list order and
+// every gate/up tile precedes every down tile in the list, so a CTA takes all
+// its gate/up tiles before any down tile and the cross-CTA wait of a down
+// tile stays deadlock-free. Without a counter the static tile_of order is used.
+constexpr int kTileRing = 4;
+
 struct TileWalk {
     const GemmSegments* seg;
     const int* table;  // m-block prefix of the segment range, in shared memory
     int TA, TB, NBA, NBB, KBA, KBB;
-    __device__ __forceinline__ int tile(int it) const {
-        return tile_of(blockIdx.x, gridDim.x, TA, TB, KBA, KBB, it);
-    }
+    int* ticket;                 // per-launch counter, or null for the static order
+    volatile int* ring;          // [kTileRing] published tile ids (-1: no more)
+    uint32_t tfull0, tempty0;    // ring barriers, kTileRing each
+    volatile int* abort_flag;
+    int* dev_err;
+
     __device__ __forceinline__ Tile decode(int t) const {
         const bool gu = t < TA;
         return decode_tile(gu ? t : t - TA, table, seg->seg_count, gu ? NBA : NBB, seg->offsets,
                            seg->seg_begin);
     }
+    // Consumer side, one thread: the it-th tile of this CTA, or -1 after the last.
+    __device__ int tile_thread(int it) const {
+        if (!ticket) return tile_of(blockIdx.x, gridDim.x, TA, TB, KBA, KBB, it);
+        const int r = it % kTileRing;
+        const uint32_t ph = static_cast<uint32_t>(it / kTileRing) & 1u;
+        if (!mbar_wait(tfull0 + 8u * r, ph, abort_flag, dev_err)) return -1;
+        const int t = ring[r];
+        mbar_arrive(tempty0 + 8u * r);
+        return t;
+    }
+    // The same for a whole warp (lane 0 reads the ring).
+    __device__ int tile(int it) const {
+        if (!ticket) return tile_of(blockIdx.x, gridDim.x, TA, TB, KBA, KBB, it);
+        int t = -1;
+        if ((threadIdx.x & 31) == 0) t = tile_thread(it);
+        return __shfl_sync(0xffffffffu, t, 0);
+    }
+    // Producer side, one thread: publish the it-th tile. `pending` holds the
+    // ticket requested one tile earlier (first request before the walk).
+    __device__ int publish(int it, int& pending) const {
+        if (!ticket) return tile_of(blockIdx.x, gridDim.x, TA, TB, KBA, KBB, it);
+        const int r = it % kTileRing;
+        const uint32_t ph = static_cast<uint32_t>(it / kTileRing) & 1u;
+        if (!mbar_wait(tempty0 + 8u * r, ph ^ 1u, abort_flag, dev_err)) return -1;
+        int t = pending;
+        if (t >= 0 && t < TA + TB) {
+            pending = atomicAdd(ticket, 1);
+        } else {
+            t = -1;
+        }
+        ring[r] = t;
+        mbar_arrive(tfull0 + 8u * r);
+        return t;
+    }
+    __device__ int first_ticket() const { return ticket ? atomicAdd(ticket, 1) : 0; }
 };
 
 // Lane 0: bounded wait until *cnt >= target (an m-block's gate/up tiles have
@@ -400,7 +450,7 @@ __device__ void role_mma(const FfnArgs& a, const TileWalk& w, Ring ring, uint32_
     uint32_t acc_phase = 0;
     bool ok = true;
     bool issued_any = false;
-    for (int it = 0, t; ok && (t = w.tile(it)) >= 0; ++it) {
+    for (int it = 0, t; ok && (t = w.tile_thread(it)) >= 0; ++it) {
         const bool gu = t < w.TA;
         const int num_kb = gu ? w.KBA : w.KBB;
         const uint32_t idesc = gu ? idesc_gu : idesc_dn;
@@ -510,8 +560,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto accf_bar = [&](int q) { return bar0 + 8u * (2 * kStages + q); };
     auto acce_bar = [&](int q) { return bar0 + 8u * (2 * kStages + 2 + q); };
     const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 4);
+    const uint32_t tfull0 = bar0 + 8u * (2 * kStages + 5);
+    const uint32_t tempty0 = tfull0 + 8u * kTileRing;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
+    volatile int* tile_ring = reinterpret_cast<volatile int*>(smem + kOffRing);
     int* table = reinterpret_cast<int*>(smem + kOffTable);
 
     const int warp = threadIdx.x >> 5;
@@ -531,6 +584,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(acce_bar(q), 4);  // one arrival per epilogue warp
         }
         mbar_init(drain_bar, 1);
+        for (int r = 0; r < kTileRing; ++r) {
+            mbar_init(tfull0 + 8u * r, 1);
+            mbar_init(tempty0 + 8u * r, 4 + 1 + 4);  // loader warps, MMA thread, epilogue warps
+        }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -551,7 +608,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int TA = (a.phases & 1) ? MB * NBA : 0;
     const int TB = (a.phases & 2) ? MB * NBB : 0;
     const int done_target = 4 * NBA;          // every epilogue warp of every gate/up n-block
-    const TileWalk walk{&seg, table, TA, TB, NBA, NBB, KBA, KBB};
+    const TileWalk walk{&seg,     table,     TA,     TB,         NBA,       NBB, KBA,
+                        KBB,      a.ticket,  tile_ring, tfull0, tempty0, abort_flag, a.dev_err};
     const Ring ring{full_bar(0), empty_bar(0)};
 
     if (warp == 0) {
@@ -561,7 +619,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         int issued[kStages];
         for (int s = 0; s < kStages; ++s) issued[s] = -1;
         bool ok = true;
-        for (int it = 0, t; ok && (t = walk.tile(it)) >= 0; ++it) {
+        int pending = lane == 0 ? walk.first_ticket() : 0;
+        auto next_tile = [&](int it) {
+            int t = 0;
+            if (lane == 0) t = walk.publish(it, pending);
+            return __shfl_sync(0xffffffffu, t, 0);
+        };
+        for (int it = 0, t; ok && (t = next_tile(it)) >= 0; ++it) {
             const bool gu = t < TA;
             const Tile ti = walk.decode(t);
             const int slot = seg.slot_base + ti.seg;
@@ -669,10 +733,12 @@ constexpr int kQOffA = 0;
 constexpr int kQOffB = kQStages * kTileABytes;
 constexpr int kQOffP = kQOffB + kQStages * kTileBBytes;
 constexpr int kQOffBar = kQOffP + kQPStages * kQPBytes;
-// barriers: full[4], empty[4], pfull[3], pempty[3], acc_full[2], acc_empty[2], drain
-constexpr int kQNumBars = 2 * kQStages + 2 * kQPStages + 5;
+// barriers: full[4], empty[4], pfull[3], pempty[3], acc_full[2], acc_empty[2], drain,
+// tile_full[4], tile_empty[4]
+constexpr int kQNumBars = 2 * kQStages + 2 * kQPStages + 5 + 2 * 4;
 constexpr int kQOffMisc = kQOffBar + 8 * kQNumBars;
-constexpr int kQOffTable = kQOffMisc + 16;
+constexpr int kQOffRing = kQOffMisc + 16;
+constexpr int kQOffTable = kQOffRing + 16;
 
 size_t q4_smem_bytes(int seg_count) {
     return 1024 + kQOffTable + sizeof(int) * static_cast<size_t>(seg_count + 1);
@@ -817,8 +883,11 @@ __global__ void __launch_bounds__(kQThreads, 1)
     const uint32_t accf0 = bar0 + 8u * (2 * kQStages + 2 * kQPStages);
     const uint32_t acce0 = accf0 + 16u;
     const uint32_t drain_bar = acce0 + 16u;
+    const uint32_t tfull0 = drain_bar + 8u;
+    const uint32_t tempty0 = tfull0 + 8u * kTileRing;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kQOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kQOffMisc + 4);
+    volatile int* tile_ring = reinterpret_cast<volatile int*>(smem + kQOffRing);
     int* table = reinterpret_cast<int*>(smem + kQOffTable);
 
     const int warp = threadIdx.x >> 5;
@@ -841,6 +910,11 @@ __global__ void __launch_bounds__(kQThreads, 1)
             mbar_init(acce0 + 8u * q, 4);
         }
         mbar_init(drain_bar, 1);
+        for (int r = 0; r < kTileRing; ++r) {
+            mbar_init(tfull0 + 8u * r, 1);
+            // loader warps, MMA thread, epilogue warps, converter warps
+            mbar_init(tempty0 + 8u * r, 4 + 1 + 4 + kConvWarps);
+        }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -860,7 +934,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
     const int MB = table[seg.seg_count];
     const int TA = (a.phases & 1) ? MB * NBA : 0;
     const int TB = (a.phases & 2) ? MB * NBB : 0;
-    const TileWalk walk{&seg, table, TA, TB, NBA, NBB, KBA, KBB};
+    const TileWalk walk{&seg,     table,     TA,     TB,         NBA,       NBB, KBA,
+                        KBB,      a.ticket,  tile_ring, tfull0, tempty0, abort_flag, a.dev_err};
 
     if (warp == 0) {
         // ------------------------------ packed-weight producer ------------------------------
@@ -869,7 +944,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
             for (int s = 0; s < kQPStages; ++s) issued[s] = -1;
             bool ok = true;
             int g = 0;
-            for (int it = 0, t; ok && (t = walk.tile(it)) >= 0; ++it) {
+            int pending = walk.first_ticket();
+            for (int it = 0, t; ok && (t = walk.publish(it, pending)) >= 0; ++it) {
                 const bool gu = t < TA;
                 const Tile ti = walk.decode(t);
                 const size_t slot = static_cast<size_t>(seg.slot_base + ti.seg);
@@ -1498,8 +1574,8 @@ __global__ void k_combine(const float* __restrict__ rows, const int32_t* __restr
 cudaError_t launch_expert_ffn(const CUtensorMap* tm_wg, const CUtensorMap* tm_wu,
                               const CUtensorMap* tm_wd, const CUtensorMap* tm_h,
                               const GemmSegments& seg, const void* X,
-                              void* h, float* Y, float* out_rows, int* done, int H, int F,
-                              int phases, int* dev_err, int num_sms, cudaStream_t stream) {
+                              void* h, float* Y, float* out_rows, int* done, int* ticket, int H,
+                              int F, int phases, int* dev_err, int num_sms, cudaStream_t stream) {
     const long long max_tiles = static_cast<long long>(seg.max_tiles_m) *
                                 (((phases & 1) ? F / 128 : 0) + ((phases & 2) ? H / 256 : 0));
     if (max_tiles <= 0 || seg.seg_count <= 0) return cudaSuccess;
@@ -1515,6 +1591,7 @@ cudaError_t launch_expert_ffn(const CUtensorMap* tm_wg, const CUtensorMap* tm_wu
     args.Y = Y;
     args.out_rows = out_rows;
     args.done = done;
+    args.ticket = ticket;
     args.dev_err = dev_err;
     args.H = H;
     args.F = F;
@@ -1585,6 +1662,7 @@ cudaError_t launch_expert_ffn_pair(const CUtensorMap* tm_wg, const CUtensorMap* 
     args.Y = Y;
     args.out_rows = out_rows;
     args.done = done;
+    args.ticket = nullptr;
     args.dev_err = dev_err;
     args.H = H;
     args.F = F;
@@ -1615,8 +1693,8 @@ cudaError_t launch_expert_ffn_pair(const CUtensorMap* tm_wg, const CUtensorMap* 
 cudaError_t launch_expert_ffn_q4(const uint8_t* plane_g, const uint8_t* plane_u, const uint8_t* plane_d,
                                  size_t S_gu, size_t S_d, const CUtensorMap* tm_h,
                                  const GemmSegments& seg, const void* X, void* h, float* Y,
-                                 float* out_rows, int* done, int H, int F, int phases, int* dev_err,
-                                 int num_sms, cudaStream_t stream) {
+                                 float* out_rows, int* done, int* ticket, int H, int F, int phases,
+                                 int* dev_err, int num_sms, cudaStream_t stream) {
     const long long max_tiles = static_cast<long long>(seg.max_tiles_m) *
                                 (((phases & 1) ? F / 128 : 0) + ((phases & 2) ? H / 256 : 0));
     if (max_tiles <= 0 || seg.seg_count <= 0) return cudaSuccess;
@@ -1634,6 +1712,7 @@ cudaError_t launch_expert_ffn_q4(const uint8_t* plane_g, const uint8_t* plane_u,
     args.Y = Y;
     args.out_rows = out_rows;
     args.done = done;
+    args.ticket = ticket;
     args.dev_err = dev_err;
     args.H = H;
     args.F = F;

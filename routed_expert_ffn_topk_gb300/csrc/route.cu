@@ -323,7 +323,8 @@ __global__ void __launch_bounds__(kRouteThreads) k_route_fused(
     float* __restrict__ alpha, int32_t* __restrict__ offsets, int32_t* __restrict__ rec_tok,
     int32_t* __restrict__ rec_route, int32_t* __restrict__ rec_pos, int32_t* __restrict__ hist,
     int32_t* __restrict__ mblk, int32_t* __restrict__ totals, int32_t* __restrict__ done,
-    int* __restrict__ sync, int* __restrict__ err, int nchunk) {
+    int32_t* __restrict__ tickets, int n_tickets, int* __restrict__ sync, int* __restrict__ err,
+    int nchunk) {
     extern __shared__ int smem[];
     __shared__ int ok_flag;
     const int R = T * k;
@@ -362,6 +363,8 @@ __global__ void __launch_bounds__(kRouteThreads) k_route_fused(
             offsets[b] = off[b];
             mblk[b] = mb[b];
         }
+        if (tickets)
+            for (int x = threadIdx.x; x < n_tickets; x += blockDim.x) tickets[x] = 0;
         if (threadIdx.x == 0) {
             offsets[P + 1] = R;
             mblk[P + 1] = mb_total;
@@ -415,8 +418,8 @@ RouteWorkspace route_workspace_layout(int T, int k, int P) {
 cudaError_t launch_route_build(const float* logits, int T, int E, int k, int renorm,
                                const int32_t* phi, int P, int32_t* topk_ids, float* alpha,
                                int32_t* offsets, int32_t* rec_tok, int32_t* rec_route,
-                               int32_t* rec_pos, int32_t* done, void* ws,
-                               cudaStream_t stream, int* n_launches) {
+                               int32_t* rec_pos, int32_t* done, int32_t* tickets, int n_tickets,
+                               void* ws, cudaStream_t stream, int* n_launches) {
     const RouteWorkspace w = route_workspace_layout(T, k, P);
     char* base = static_cast<char*>(ws);
     int* err = reinterpret_cast<int*>(base + w.err_off);
@@ -452,8 +455,8 @@ cudaError_t launch_route_build(const float* logits, int T, int E, int k, int ren
     const int grid = std::max(1, std::min(co_resident, w.nchunk));
     const size_t smem = sizeof(int) * (2 * static_cast<size_t>(nb) + 33);
     void* args[] = {&logits, &T, &E, &k, &renorm, &phi, &P, &topk_ids, &alpha, &offsets,
-                    &rec_tok, &rec_route, &rec_pos, &hist, &mblk, &totals, &done, &sync, &err,
-                    const_cast<int*>(&w.nchunk)};
+                    &rec_tok, &rec_route, &rec_pos, &hist, &mblk, &totals, &done, &tickets,
+                    &n_tickets, &sync, &err, const_cast<int*>(&w.nchunk)};
     rc = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(k_route_fused), grid,
                                      kRouteThreads, args, smem, stream);
     if (rc != cudaSuccess) return rc;

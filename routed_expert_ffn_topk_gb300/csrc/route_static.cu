@@ -75,7 +75,7 @@ extern "C" estream_status estream_route_build_noalloc(const float* logits, int T
     void* ws = scratch_on_current_device();
     if (!ws) return ESTREAM_ERR_CUDA;
     cudaError_t rc = launch_route_build(logits, T, E, k, renorm, phi, P, topk_ids, alpha, offsets,
-                                        rec_tok, rec_route, nullptr, nullptr, ws,
+                                        rec_tok, rec_route, nullptr, nullptr, nullptr, 0, ws,
                                         static_cast<cudaStream_t>(cuda_stream), nullptr);
     return rc == cudaSuccess ? ESTREAM_OK : ESTREAM_ERR_CUDA;
 }

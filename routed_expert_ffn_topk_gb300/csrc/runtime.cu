@@ -76,6 +76,8 @@ struct estream_ctx {
     float *alpha = nullptr, *out_rows = nullptr, *out_shared = nullptr;
     float* d_scale = nullptr;                  // [L*E] down-weight scales, storage order
     int32_t *done = nullptr, *sh_done = nullptr;  // per-m-block counters of the fused expert kernel
+    int32_t* tickets = nullptr;  // [E+2] dynamic tile counters: [0] shared experts, [1+i] i-th routed launch
+    int n_ffn_launch = 0;        // routed expert-kernel launches so far in the current layer call
     std::vector<const float*> shared_scale;    // [L] device pointers into shared buffers
     void *route_ws = nullptr, *h = nullptr, *h_shared = nullptr;
     int* dev_err = nullptr;
@@ -394,7 +396,8 @@ estream_status estream_route_build(const float* logits, int T, int E, int k, int
     if (workspace_bytes < route_workspace_layout(T, k, P).total) return ESTREAM_ERR_CAPACITY;
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
     cudaError_t rc = launch_route_build(logits, T, E, k, renorm, phi, P, topk_ids, alpha, offsets,
-                                        rec_tok, rec_route, nullptr, nullptr, workspace, s, nullptr);
+                                        rec_tok, rec_route, nullptr, nullptr, nullptr, 0, workspace, s,
+                                        nullptr);
     return rc == cudaSuccess ? ESTREAM_OK : ESTREAM_ERR_CUDA;
 }
 
@@ -577,6 +580,7 @@ estream_status estream_bind_arena(estream_ctx** out, const estream_arena_desc* d
     const size_t o_offs = take(sizeof(int32_t) * (E + 2));
     const size_t o_rws = take(route_workspace_layout(d->T_max, d->k_max, E).total);
     const size_t o_done = take(sizeof(int32_t) * ((R_cap + kBM - 1) / kBM + E + 1));
+    const size_t o_tick = take(sizeof(int32_t) * (E + 2));
     const size_t o_h = take(static_cast<size_t>(R_cap) * d->F * c->es);
     size_t o_sh_offs = 0, o_sh_mblk = 0, o_sh_tok = 0, o_hs = 0, o_outs = 0, o_out = 0;
     const int RS_cap = d->n_shared * d->T_max;
@@ -607,6 +611,7 @@ estream_status estream_bind_arena(estream_ctx** out, const estream_arena_desc* d
         c->offsets = reinterpret_cast<int32_t*>(c->ws + o_offs);
         c->route_ws = c->ws + o_rws;
         c->done = reinterpret_cast<int32_t*>(c->ws + o_done);
+        c->tickets = reinterpret_cast<int32_t*>(c->ws + o_tick);
         c->h = c->ws + o_h;
         if (d->n_shared > 0) {
             c->sh_done = reinterpret_cast<int32_t*>(c->ws + o_sh_done);
@@ -778,6 +783,12 @@ estream_status run_routed(estream_ctx* c, cudaStream_t s, const void* X, int lay
     seg.slot_base = slot_base;
     seg.max_tiles_m = max_tiles_m;
     TimedScope ts(c, s, kTFfn);
+    // this launch's dynamic tile counter, zeroed by the call's route build. The
+    // 4-bit kernel takes its tiles dynamically (measured 5.5% faster on the
+    // OLMoE shape); the bf16 kernel keeps the balanced static order (3% faster
+    // than dynamic there).
+    int* ticket = c->n_ffn_launch < c->d.E + 1 ? c->tickets + 1 + c->n_ffn_launch : nullptr;
+    ++c->n_ffn_launch;
     cudaError_t rc;
     if (c->d.wdtype == ESTREAM_F32) {
         rc = launch_gateup_f32(static_cast<const float*>(X), reinterpret_cast<const float*>(c->plane_g),
@@ -792,15 +803,15 @@ estream_status run_routed(estream_ctx* c, cudaStream_t s, const void* X, int lay
         rc = launch_expert_ffn_q4(reinterpret_cast<const uint8_t*>(c->plane_g),
                                   reinterpret_cast<const uint8_t*>(c->plane_u),
                                   reinterpret_cast<const uint8_t*>(c->plane_d), c->S_gu, c->S_d,
-                                  &c->tm_h, seg, X, c->h, Y, c->out_rows, c->done, c->d.H, c->d.F, 3,
-                                  c->dev_err, c->num_sms, s);
+                                  &c->tm_h, seg, X, c->h, Y, c->out_rows, c->done, ticket, c->d.H,
+                                  c->d.F, 3, c->dev_err, c->num_sms, s);
         c->stats.launches += 1;
     } else {
         rc = pair
                  ? launch_expert_ffn_pair(&c->tm_wg, &c->tm_wu, &c->tm_wd_half, &c->tm_h, seg, X, c->h,
                                           Y, c->out_rows, c->done, c->d.H, c->d.F, 3, c->dev_err, s)
                  : launch_expert_ffn(&c->tm_wg, &c->tm_wu, &c->tm_wd, &c->tm_h, seg, X, c->h, Y,
-                                     c->out_rows, c->done, c->d.H, c->d.F, 3, c->dev_err,
+                                     c->out_rows, c->done, nullptr, c->d.H, c->d.F, 3, c->dev_err,
                                      c->num_sms, s);
         c->stats.launches += 1;
     }
@@ -843,16 +854,16 @@ estream_status run_shared(estream_ctx* c, cudaStream_t s, const void* X,
         const size_t S1 = plane_slot_bytes(ESTREAM_Q4, Fs, c->d.H);  // one shared expert's plane
         const size_t sp = static_cast<size_t>(ns) * S1;
         rc = launch_expert_ffn_q4(base, base + sp, base + 2 * sp, S1, S1, &c->tm_hs, seg, X,
-                                  c->h_shared, Y, c->out_shared, c->sh_done, c->d.H, Fs, 3,
-                                  c->dev_err, c->num_sms, s);
+                                  c->h_shared, Y, c->out_shared, c->sh_done, c->tickets, c->d.H, Fs,
+                                  3, c->dev_err, c->num_sms, s);
     } else {
         rc = pair_form(c, T, 1)
                  ? launch_expert_ffn_pair(&c->tm_sg[layer], &c->tm_su[layer], &c->tm_sd_half[layer],
                                           &c->tm_hs, seg, X, c->h_shared, Y, c->out_shared,
                                           c->sh_done, c->d.H, Fs, 3, c->dev_err, s)
                  : launch_expert_ffn(&c->tm_sg[layer], &c->tm_su[layer], &c->tm_sd[layer], &c->tm_hs,
-                                     seg, X, c->h_shared, Y, c->out_shared, c->sh_done, c->d.H, Fs,
-                                     3, c->dev_err, c->num_sms, s);
+                                     seg, X, c->h_shared, Y, c->out_shared, c->sh_done, nullptr,
+                                     c->d.H, Fs, 3, c->dev_err, c->num_sms, s);
     }
     if (rc != cudaSuccess) return ESTREAM_ERR_CUDA;
     c->stats.launches += c->d.wdtype == ESTREAM_F32 ? 3 : 2;
@@ -962,6 +973,7 @@ estream_status estream_moe_layer_prefill(estream_ctx* c, int layer, const void* 
     const int E = c->d.E, G = c->d.G, H = c->d.H;
     c->trace.clear();
     c->stats.calls += 1;
+    c->n_ffn_launch = 0;
     TimedScope total(c, s, kTTotal);
     release_pipe_events(c);
     const bool trace_pipe = c->timing;
@@ -1013,8 +1025,8 @@ estream_status estream_moe_layer_prefill(estream_ctx* c, int layer, const void* 
         int launches = 0;
         if (launch_route_build(logits, T, E, k, renorm, c->d_perm + static_cast<size_t>(layer) * E, E,
                                c->topk_ids, c->alpha, c->offsets, c->rec_tok, c->rec_route,
-                               c->d.deterministic ? c->rec_pos : nullptr, c->done, c->route_ws, s,
-                               &launches) != cudaSuccess) {
+                               c->d.deterministic ? c->rec_pos : nullptr, c->done, c->tickets, E + 2,
+                               c->route_ws, s, &launches) != cudaSuccess) {
             drain(c, s);
             return ESTREAM_ERR_CUDA;
         }
