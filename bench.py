@@ -245,9 +245,8 @@ def run_ours(args, rank, world, local_rank):
             for l in range(L):
                 X_l = X_in if l == 0 else Xbuf[l]
                 Y_l = Y_out if l == L - 1 else Y[l]
-                # Y_l starts as the residual X_l (Eq. 2's A_t)
-                Y_l.copy_(X_l)
-                stacks[l].prefill(0, X_l, lg_in[l], Y_l)
+                # Y_l = X_l + MoE_l(X_l): the residual of Eq. 2 is the layer input
+                stacks[l].prefill(0, X_l, lg_in[l], Y_l, residual=X_l)
                 if l + 1 < L:
                     es.cast_f32_bf16(Y_l, Xbuf[l + 1])
         return run

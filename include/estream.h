@@ -316,6 +316,20 @@ estream_status estream_moe_layer_prefill(estream_ctx* c, int layer, const void* 
                                          const float* logits, int T, int k, int renorm,
                                          float* Y, void* cuda_stream);
 
+/*
+ * The same layer with the residual of Eq. 2 given explicitly:
+ * Y = A + sum_j alpha_{t,j} F_{e_{t,j}}(X_t) (+ shared experts). Y is written,
+ * not read: the route build initialises each token's row from A while it
+ * routes the token, so the caller needs no separate copy of A into Y.
+ * A       device, [T][H] in X's type (bf16, or fp32 for ESTREAM_F32), 16-byte
+ *         aligned; A == X (the usual residual stream) is allowed.
+ * The other arguments and the behaviour are those of
+ * estream_moe_layer_prefill.
+ */
+estream_status estream_moe_layer_prefill_residual(estream_ctx* c, int layer, const void* X,
+                                                  const float* logits, int T, int k, int renorm,
+                                                  const void* A, float* Y, void* cuda_stream);
+
 /* Timings and counters accumulated since the last estream_reset_stats. The
  * per-kernel times are CUDA-event times on the launching stream, recorded
  * only while timing is on (estream_set_timing); reading them synchronises. */

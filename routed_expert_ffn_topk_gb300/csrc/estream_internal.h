@@ -38,6 +38,15 @@ struct RouteWorkspace {
 };
 RouteWorkspace route_workspace_layout(int T, int k, int P);
 
+// Optional fused initialisation Y[t][:] = fp32(A[t][:]) (the residual of
+// Eq. 2), done by the route build's token warps; H a multiple of 256.
+struct ResidualInit {
+    const void* A;   // [T][H], bf16 (elem_bytes 2) or fp32 (4)
+    int elem_bytes;
+    float* Y;        // [T][H]
+    int H;
+};
+
 // Enqueue the full route build (K1). `ws` must hold route_workspace_layout(T,k,P).
 // rec_pos (optional, [T*k]) receives, for route i, its position in the CSR.
 // done (optional) is zeroed over the route map's m-blocks (mblk[P] ints) for
@@ -47,7 +56,8 @@ cudaError_t launch_route_build(const float* logits, int T, int E, int k, int ren
                                const int32_t* phi, int P, int32_t* topk_ids, float* alpha,
                                int32_t* offsets, int32_t* rec_tok, int32_t* rec_route,
                                int32_t* rec_pos, int32_t* done, int32_t* tickets, int n_tickets,
-                               void* ws, cudaStream_t stream, int* n_launches);
+                               void* ws, cudaStream_t stream, int* n_launches,
+                               const ResidualInit* resid = nullptr);
 
 // Identity route map for the shared experts: n_shared segments of T rows,
 // rec_tok[p] = p mod T, offsets[s] = s*T, mblk[s] = s*ceil(T/kBM); zeroes

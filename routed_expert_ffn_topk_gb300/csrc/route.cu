@@ -166,6 +166,27 @@ __device__ __forceinline__ void topk_token(
     }
 }
 
+// Y[t][:] = fp32(A[t][:]), one warp per row (16-byte vectors; H % 256 == 0).
+__device__ __forceinline__ void init_residual_row(int t, const ResidualInit& r) {
+    const int lane = threadIdx.x & 31;
+    float4* y = reinterpret_cast<float4*>(r.Y + static_cast<size_t>(t) * r.H);
+    if (r.elem_bytes == 2) {
+        const uint4* a = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(r.A) +
+                                                        static_cast<size_t>(t) * r.H);
+        for (int c = lane; c < r.H / 8; c += 32) {
+            const uint4 v = a[c];  // 8 bf16: a bf16 is the high half of its fp32
+            y[2 * c] = make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u),
+                                   __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xFFFF0000u));
+            y[2 * c + 1] = make_float4(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xFFFF0000u),
+                                       __uint_as_float(v.w << 16), __uint_as_float(v.w & 0xFFFF0000u));
+        }
+    } else {
+        const float4* a = reinterpret_cast<const float4*>(static_cast<const float*>(r.A) +
+                                                          static_cast<size_t>(t) * r.H);
+        for (int c = lane; c < r.H / 4; c += 32) y[c] = a[c];
+    }
+}
+
 // In-place exclusive scan of n ints in shared memory by one CTA of
 // blockDim.x (multiple of 32, <= 1024) threads. Returns the total.
 __device__ int block_exclusive_scan(int* data, int n, int* warp_sums) {
@@ -324,7 +345,7 @@ __global__ void __launch_bounds__(kRouteThreads) k_route_fused(
     int32_t* __restrict__ rec_route, int32_t* __restrict__ rec_pos, int32_t* __restrict__ hist,
     int32_t* __restrict__ mblk, int32_t* __restrict__ totals, int32_t* __restrict__ done,
     int32_t* __restrict__ tickets, int n_tickets, int* __restrict__ sync, int* __restrict__ err,
-    int nchunk) {
+    int nchunk, ResidualInit resid) {
     extern __shared__ int smem[];
     __shared__ int ok_flag;
     const int R = T * k;
@@ -334,7 +355,10 @@ __global__ void __launch_bounds__(kRouteThreads) k_route_fused(
         for (int b = threadIdx.x; b < nb; b += blockDim.x) smem[b] = 0;
         __syncthreads();
         const int t = c * kChunkTokens + (threadIdx.x >> 5);
-        if (t < T) topk_token(t, logits, E, k, renorm, phi, P, topk_ids, alpha, smem, err);
+        if (t < T) {
+            topk_token(t, logits, E, k, renorm, phi, P, topk_ids, alpha, smem, err);
+            if (resid.A) init_residual_row(t, resid);
+        }
         __syncthreads();
         for (int b = threadIdx.x; b < nb; b += blockDim.x)
             hist[static_cast<size_t>(b) * nchunk + c] = smem[b];
@@ -419,7 +443,8 @@ cudaError_t launch_route_build(const float* logits, int T, int E, int k, int ren
                                const int32_t* phi, int P, int32_t* topk_ids, float* alpha,
                                int32_t* offsets, int32_t* rec_tok, int32_t* rec_route,
                                int32_t* rec_pos, int32_t* done, int32_t* tickets, int n_tickets,
-                               void* ws, cudaStream_t stream, int* n_launches) {
+                               void* ws, cudaStream_t stream, int* n_launches,
+                               const ResidualInit* resid_in) {
     const RouteWorkspace w = route_workspace_layout(T, k, P);
     char* base = static_cast<char*>(ws);
     int* err = reinterpret_cast<int*>(base + w.err_off);
@@ -441,6 +466,8 @@ cudaError_t launch_route_build(const float* logits, int T, int E, int k, int ren
     rc = cudaMemsetAsync(base + w.err_off, 0, 2 * sizeof(int32_t), stream);
     if (rc != cudaSuccess) return rc;
     int* sync = reinterpret_cast<int*>(base + w.sync_off);
+    ResidualInit resid{nullptr, 0, nullptr, 0};
+    if (resid_in) resid = *resid_in;
     static int co_resident = 0;  // CTAs of k_route_fused that fit on the device at once
     if (co_resident == 0) {
         int dev = 0, sms = 0, per_sm = 0;
@@ -456,7 +483,7 @@ cudaError_t launch_route_build(const float* logits, int T, int E, int k, int ren
     const size_t smem = sizeof(int) * (2 * static_cast<size_t>(nb) + 33);
     void* args[] = {&logits, &T, &E, &k, &renorm, &phi, &P, &topk_ids, &alpha, &offsets,
                     &rec_tok, &rec_route, &rec_pos, &hist, &mblk, &totals, &done, &tickets,
-                    &n_tickets, &sync, &err, const_cast<int*>(&w.nchunk)};
+                    &n_tickets, &sync, &err, const_cast<int*>(&w.nchunk), &resid};
     rc = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(k_route_fused), grid,
                                      kRouteThreads, args, smem, stream);
     if (rc != cudaSuccess) return rc;

@@ -961,13 +961,14 @@ estream_status estream_arena_invalidate(estream_ctx* c) {
     return ESTREAM_OK;
 }
 
-estream_status estream_moe_layer_prefill(estream_ctx* c, int layer, const void* X,
-                                         const float* logits, int T, int k, int renorm, float* Y,
-                                         void* cuda_stream) {
+// One layer call; with A non-null the route build also initialises Y = A.
+static estream_status prefill_impl(estream_ctx* c, int layer, const void* X, const float* logits,
+                                   int T, int k, int renorm, const void* A, float* Y,
+                                   void* cuda_stream) {
     if (!c) return ESTREAM_ERR_NOT_BOUND;
     if (layer < 0 || layer >= c->d.L || !X || !logits || !Y || T < 1 || k < 1 || k > c->d.E)
         return ESTREAM_ERR_INVALID_ARG;
-    if (!aligned(X, 16) || !aligned(Y, 16)) return ESTREAM_ERR_INVALID_ARG;
+    if (!aligned(X, 16) || !aligned(Y, 16) || (A && !aligned(A, 16))) return ESTREAM_ERR_INVALID_ARG;
     if (T > c->d.T_max || k > c->d.k_max) return ESTREAM_ERR_CAPACITY;
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
     const int E = c->d.E, G = c->d.G, H = c->d.H;
@@ -1023,10 +1024,11 @@ estream_status estream_moe_layer_prefill(estream_ctx* c, int layer, const void* 
     {
         TimedScope ts(c, s, kTRoute);
         int launches = 0;
+        const ResidualInit ri{A, c->es, Y, H};
         if (launch_route_build(logits, T, E, k, renorm, c->d_perm + static_cast<size_t>(layer) * E, E,
                                c->topk_ids, c->alpha, c->offsets, c->rec_tok, c->rec_route,
                                c->d.deterministic ? c->rec_pos : nullptr, c->done, c->tickets, E + 2,
-                               c->route_ws, s, &launches) != cudaSuccess) {
+                               c->route_ws, s, &launches, A ? &ri : nullptr) != cudaSuccess) {
             drain(c, s);
             return ESTREAM_ERR_CUDA;
         }
@@ -1132,6 +1134,19 @@ estream_status estream_moe_layer_prefill(estream_ctx* c, int layer, const void* 
         c->stats.launches += 1;
     }
     return ESTREAM_OK;
+}
+
+estream_status estream_moe_layer_prefill(estream_ctx* c, int layer, const void* X,
+                                         const float* logits, int T, int k, int renorm, float* Y,
+                                         void* cuda_stream) {
+    return prefill_impl(c, layer, X, logits, T, k, renorm, nullptr, Y, cuda_stream);
+}
+
+estream_status estream_moe_layer_prefill_residual(estream_ctx* c, int layer, const void* X,
+                                                  const float* logits, int T, int k, int renorm,
+                                                  const void* A, float* Y, void* cuda_stream) {
+    if (!A) return ESTREAM_ERR_INVALID_ARG;
+    return prefill_impl(c, layer, X, logits, T, k, renorm, A, Y, cuda_stream);
 }
 
 estream_status estream_set_timing(estream_ctx* c, int on) {

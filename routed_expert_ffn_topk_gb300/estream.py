@@ -83,6 +83,7 @@ SIGNATURES = {
     "estream_arena_preload": (_I, [_P, _I, _P]),
     "estream_arena_invalidate": (_I, [_P]),
     "estream_moe_layer_prefill": (_I, [_P, _I, _P, _P, _I, _I, _I, _P, _P]),
+    "estream_moe_layer_prefill_residual": (_I, [_P, _I, _P, _P, _I, _I, _I, _P, _P, _P]),
     "estream_set_timing": (_I, [_P, _I]),
     "estream_reset_stats": (_I, [_P]),
     "estream_last_stats": (_I, [_P, ctypes.POINTER(Stats)]),
@@ -311,6 +312,16 @@ def moe_layer_prefill(ctx, layer: int, X: torch.Tensor, logits: torch.Tensor, k:
     _check(lib().estream_moe_layer_prefill(ctx, layer, _dptr(X), _dptr(logits), T, k,
                                            int(bool(renorm)), _dptr(Y), _stream(stream)),
            "estream_moe_layer_prefill")
+
+
+def moe_layer_prefill_residual(ctx, layer: int, X: torch.Tensor, logits: torch.Tensor, k: int,
+                               renorm: bool, A: torch.Tensor, Y: torch.Tensor, stream=None) -> None:
+    """Y = A + the layer's MoE output (Y written, not read)."""
+    T = X.shape[0]
+    _check(lib().estream_moe_layer_prefill_residual(ctx, layer, _dptr(X), _dptr(logits), T, k,
+                                                    int(bool(renorm)), _dptr(A), _dptr(Y),
+                                                    _stream(stream)),
+           "estream_moe_layer_prefill_residual")
 
 
 def set_timing(ctx, on: bool) -> None:

@@ -69,10 +69,15 @@ class BoundLayerStack:
             es.arena_preload(self.ctx, 0)
 
     def prefill(self, layer: int, X: torch.Tensor, logits: torch.Tensor, Y: torch.Tensor,
-                k=None, renorm=None, stream=None) -> None:
+                k=None, renorm=None, stream=None, residual: torch.Tensor | None = None) -> None:
+        """Y += MoE(X), or Y = residual + MoE(X) when `residual` is given."""
         cfg = self.cfg
-        es.moe_layer_prefill(self.ctx, layer, X, logits, cfg.k if k is None else k,
-                             cfg.renorm if renorm is None else renorm, Y, stream)
+        k = cfg.k if k is None else k
+        renorm = cfg.renorm if renorm is None else renorm
+        if residual is None:
+            es.moe_layer_prefill(self.ctx, layer, X, logits, k, renorm, Y, stream)
+        else:
+            es.moe_layer_prefill_residual(self.ctx, layer, X, logits, k, renorm, residual, Y, stream)
 
     def prefill_from_router(self, layer: int, X: torch.Tensor, W_r: torch.Tensor, Y: torch.Tensor,
                             k=None, renorm=None, stream=None) -> torch.Tensor:

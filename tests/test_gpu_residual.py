@@ -1,0 +1,49 @@
+"""estream_moe_layer_prefill_residual: Y = A + MoE(X) with the residual rows
+written by the route build, against an explicit copy of A into Y followed by
+the accumulating call (bit for bit in deterministic mode) and the oracle."""
+import numpy as np
+import pytest
+import torch
+
+from tests import _gpu
+from tests.test_gpu_layer import small_workload
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("key,mode,q4", [("c2", "resident", False), ("c3", "paged", False),
+                                         ("c2", "resident", True), ("c1", "resident", False)])
+def test_residual_call(key, mode, q4):
+    from routed_expert_ffn_topk_gb300 import estream as es
+    from routed_expert_ffn_topk_gb300.layer import BoundLayerStack
+    wl = small_workload(key)
+    dev = _gpu.device()
+    ref = (_gpu.oracle_layer_q4(wl, 0, wl.X) if q4 else _gpu.oracle_layer(wl, 0, wl.X))
+    # a residual on the scale of the MoE output, so that Y - A keeps its precision
+    scale = float(np.abs(ref).mean())
+    A_cpu = (torch.randn(wl.X.shape, generator=torch.Generator().manual_seed(17)) * scale).to(wl.X.dtype)
+    st = BoundLayerStack(wl, mode=mode, deterministic=True, wdtype=es.Q4 if q4 else None)
+    try:
+        X = wl.X.to(dev)
+        lg = wl.logits[0].to(dev)
+        A = A_cpu.to(dev)
+        Y1 = A.float().clone()
+        st.prefill(0, X, lg, Y1)
+        Y2 = torch.full_like(Y1, float("nan"))   # every element must be written
+        st.prefill(0, X, lg, Y2, residual=A)
+        Y3 = torch.full_like(Y1, float("nan"))
+        st.prefill(0, X, lg, Y3, residual=X)      # the residual stream itself
+        torch.cuda.synchronize()
+        assert es.get_device_error(st.ctx) == es.OK
+        assert torch.equal(Y1.view(torch.int32), Y2.view(torch.int32))
+    finally:
+        st.close()
+    Ac = A_cpu.double().numpy()
+    _gpu.assert_y_close(Y2.cpu().numpy() - Ac, ref, f"residual A {key}/{mode}")
+    # Y3 = X + MoE: compared with the oracle's Y including the same residual
+    ref3 = (_gpu.oracle_layer_q4(wl, 0, wl.X) if q4 else None)
+    if ref3 is None:
+        ref3 = _gpu.oracle_layer(wl, 0, wl.X, residual=wl.X.double().numpy())
+    else:
+        ref3 = ref3 + wl.X.double().numpy()
+    _gpu.assert_y_close(Y3.cpu().numpy(), ref3, f"residual X {key}/{mode}")
