@@ -67,7 +67,8 @@ constexpr float kHalfMax = 65504.0f;
 // Shared-memory map (offsets from a 1024-byte aligned base).
 constexpr int kOffA = 0;
 constexpr int kOffB = kStages * kTileABytes;
-constexpr int kOffBar = kOffB + kStages * kTileBBytes;
+constexpr int kOffStg = kOffB + kStages * kTileBBytes;  // epilogue stages, 4 x 4 KB
+constexpr int kOffBar = kOffStg + 4 * 32 * 128;
 // barriers: full[kStages], empty[kStages], acc_full[2], acc_empty[2], drain
 // + tile ring: tile_full[4], tile_empty[4]
 constexpr int kNumBars = 2 * kStages + 5 + 2 * 4;
@@ -246,6 +247,111 @@ __device__ __forceinline__ void epilogue_down(uint32_t tacc, bool valid, float a
                                al * __uint_as_float(v[4 * q + 3]));
             }
         }
+    }
+}
+
+// Coalesced write-out. A tcgen05.ld gives each thread one record's row, so
+// storing straight from registers makes every warp instruction touch 32
+// different rows of h or Y with 16 bytes each. The staged epilogues instead
+// pass each 32 x 128-byte chunk of the warp's accumulator rows through a
+// 4 KB shared-memory stage and write it out row by row: one instruction then
+// covers four whole 128-byte rows (for Y, four full lines of vector
+// reductions). The stage stores 16-byte chunk j of row r at chunk
+// j ^ (r mod 8), which keeps both the row-wise writes and the column-wise
+// reads free of bank conflicts.
+constexpr int kStageWarpBytes = 32 * 128;
+
+__device__ __forceinline__ uint32_t stage_off(int r, int j) {
+    return static_cast<uint32_t>(r * 128 + ((j ^ (r & 7)) << 4));
+}
+
+// Row pointer of the record that lane `lane` writes in read-out step i
+// (rows 4 i .. 4 i + 3, eight lanes per row).
+template <typename T>
+__device__ __forceinline__ T* row_of_step(T* my_row, int i, int lane) {
+    return reinterpret_cast<T*>(
+        __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(my_row), 4 * i + (lane >> 3)));
+}
+
+// Gate/up epilogue through the stage: h = fp16(SiLU(g) u) of this lane's
+// record goes to dst_row[0 .. 128) (null for a padding record), 64 columns
+// (128 bytes) per pass.
+__device__ __forceinline__ void epilogue_gate_up_staged(uint32_t tacc, __half* dst_row,
+                                                        uint32_t stg, int lane, int* dev_err) {
+    bool in_range = true;
+    __half* dst[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) dst[i] = row_of_step(dst_row, i, lane);
+    const int j = lane & 7;
+#pragma unroll 1
+    for (int half = 0; half < 2; ++half) {
+#pragma unroll 1
+        for (int c2 = 0; c2 < 2; ++c2) {
+            const int c = 2 * half + c2;
+            uint32_t g[32], u[32];
+            tmem_ld32(tacc + c * 32, g);
+            tmem_ld32(tacc + 128 + c * 32, u);
+            tmem_ld_wait();
+            uint32_t packed[16];
+#pragma unroll
+            for (int v = 0; v < 16; ++v) {
+                const float h0 = silu_mul(__uint_as_float(g[2 * v]), __uint_as_float(u[2 * v]));
+                const float h1 = silu_mul(__uint_as_float(g[2 * v + 1]), __uint_as_float(u[2 * v + 1]));
+                in_range = in_range && fabsf(h0) <= kHalfMax && fabsf(h1) <= kHalfMax;
+                const __half2 p2 = __floats2half2_rn(h0, h1);
+                packed[v] = *reinterpret_cast<const uint32_t*>(&p2);
+            }
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+                st_shared_v4(stg + stage_off(lane, 4 * c2 + v), packed[4 * v], packed[4 * v + 1],
+                             packed[4 * v + 2], packed[4 * v + 3]);
+        }
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint4 x = ld_shared_v4(stg + stage_off(4 * i + (lane >> 3), j));
+            if (dst[i]) st_v4(dst[i] + half * 64 + 8 * j, x.x, x.y, x.z, x.w);
+        }
+        __syncwarp();
+    }
+    if (dst_row && !in_range) record_error(dev_err, kDevErrRange);
+}
+
+// Down epilogue through the stage: the 256 accumulator columns of this
+// lane's record times `al` are added into dst_row[0 .. 256) with vector
+// reductions (reduce) or stored there (the scaled-row buffer of the
+// deterministic mode); dst_row is null for a padding record.
+__device__ __forceinline__ void epilogue_down_staged(uint32_t tacc, float al, float* dst_row,
+                                                     bool reduce, uint32_t stg, int lane) {
+    float* dst[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) dst[i] = row_of_step(dst_row, i, lane);
+    const int j = lane & 7;
+#pragma unroll 1
+    for (int c = 0; c < 8; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tacc + c * 32, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            st_shared_v4(stg + stage_off(lane, q), __float_as_uint(al * __uint_as_float(v[4 * q])),
+                         __float_as_uint(al * __uint_as_float(v[4 * q + 1])),
+                         __float_as_uint(al * __uint_as_float(v[4 * q + 2])),
+                         __float_as_uint(al * __uint_as_float(v[4 * q + 3])));
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint4 x = ld_shared_v4(stg + stage_off(4 * i + (lane >> 3), j));
+            if (dst[i]) {
+                float* d = dst[i] + c * 32 + 4 * j;
+                if (reduce)
+                    red_add_v4(d, __uint_as_float(x.x), __uint_as_float(x.y), __uint_as_float(x.z),
+                               __uint_as_float(x.w));
+                else
+                    st_v4(d, x.x, x.y, x.z, x.w);
+            }
+        }
+        __syncwarp();
     }
 }
 
@@ -493,11 +599,15 @@ __device__ void role_mma(const FfnArgs& a, const TileWalk& w, Ring ring, uint32_
 // Epilogue (4 warps, TMEM lanes = records): gate/up tiles write
 // h = fp16(SiLU(g) u) and publish the m-block counter; down tiles add
 // alpha * scale * acc into Y (or store the row in deterministic mode).
+// With a stage (shared address of 4 x kStageWarpBytes, else 0) the rows are
+// written out coalesced through it.
 __device__ void role_epilogue(const FfnArgs& a, const TileWalk& w, uint32_t accf0, uint32_t acce0,
-                              uint32_t tmem_base, volatile int* abort_flag, int warp, int lane) {
+                              uint32_t tmem_base, volatile int* abort_flag, int warp, int lane,
+                              uint32_t stage0) {
     const GemmSegments& seg = *w.seg;
     const int quarter = warp & 3;  // TMEM lanes this warp may read
     const int row = quarter * 32 + lane;
+    const uint32_t stg = stage0 + static_cast<uint32_t>(quarter * kStageWarpBytes);
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int it = 0, t; (t = w.tile(it)) >= 0; ++it) {
@@ -513,9 +623,11 @@ __device__ void role_epilogue(const FfnArgs& a, const TileWalk& w, uint32_t accf
         const uint32_t tacc = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                               static_cast<uint32_t>(acc * kAccCols);
         if (gu) {
-            epilogue_gate_up(tacc, valid,
-                             a.h + static_cast<size_t>(p) * a.F + static_cast<size_t>(ti.nb) * 128,
-                             a.dev_err);
+            __half* dst = a.h + static_cast<size_t>(p) * a.F + static_cast<size_t>(ti.nb) * 128;
+            if (stage0)
+                epilogue_gate_up_staged(tacc, valid ? dst : nullptr, stg, lane, a.dev_err);
+            else
+                epilogue_gate_up(tacc, valid, dst, a.dev_err);
             // publish this warp's rows of the tile to the down tiles (which
             // read h through TMA, the async proxy)
             fence_proxy_async_global();
@@ -531,9 +643,15 @@ __device__ void role_epilogue(const FfnArgs& a, const TileWalk& w, uint32_t accf
                 al = seg.alpha ? seg.alpha[seg.rec_route[p]] : 1.0f;
                 al *= seg.seg_scale[seg.seg_begin + ti.seg];  // undo the W_d scale
             }
-            epilogue_down(tacc, valid, al,
-                          a.out_rows ? a.out_rows + static_cast<size_t>(p) * a.H : nullptr,
-                          a.Y + static_cast<size_t>(tok) * a.H, ti.nb * 256);
+            float* out_row = a.out_rows ? a.out_rows + static_cast<size_t>(p) * a.H : nullptr;
+            float* y_row = a.Y + static_cast<size_t>(tok) * a.H;
+            if (stage0) {
+                float* dst = out_row ? out_row : y_row;
+                epilogue_down_staged(tacc, al, valid ? dst + ti.nb * 256 : nullptr, !out_row, stg,
+                                     lane);
+            } else {
+                epilogue_down(tacc, valid, al, out_row, y_row, ti.nb * 256);
+            }
         }
         tc_fence_before();
         __syncwarp();
@@ -692,7 +810,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                               abort_flag);
         __syncwarp();
     } else {
-        role_epilogue(a, walk, accf_bar(0), acce_bar(0), tmem_base, abort_flag, warp, lane);
+        role_epilogue(a, walk, accf_bar(0), acce_bar(0), tmem_base, abort_flag, warp, lane,
+                      sbase + kOffStg);
     }
 
     tc_fence_before();
@@ -988,7 +1107,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
             role_mma<kQStages>(a, walk, ring, sA, sB, accf0, acce0, drain_bar, tmem_base, abort_flag);
         __syncwarp();
     } else {
-        role_epilogue(a, walk, accf0, acce0, tmem_base, abort_flag, warp, lane);
+        role_epilogue(a, walk, accf0, acce0, tmem_base, abort_flag, warp, lane, 0u);
     }
 
     tc_fence_before();
@@ -1020,7 +1139,8 @@ constexpr int kPStages = 6;
 constexpr int kPHalf = 128 * kRowBytes;                // 16 KB
 constexpr int kPOffA = 0;
 constexpr int kPOffB = kPStages * kPHalf;
-constexpr int kPOffBar = kPOffB + kPStages * kPHalf;
+constexpr int kPOffStg = kPOffB + kPStages * kPHalf;  // epilogue stages, 4 x 4 KB
+constexpr int kPOffBar = kPOffStg + 4 * 32 * 128;
 constexpr int kPNumBars = 2 * kPStages + 5;
 constexpr int kPOffMisc = kPOffBar + 8 * kPNumBars;
 constexpr int kPOffTable = kPOffMisc + 16;
@@ -1485,6 +1605,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------ epilogue (warps 2-5) ------------------------------
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
+        const uint32_t stg = sbase + kPOffStg + static_cast<uint32_t>(quarter * kStageWarpBytes);
         const uint32_t leader_acce0 = map_rank(acce_bar(0), 0);
         const uint32_t leader_acce1 = map_rank(acce_bar(1), 0);
         int acc = 0;
@@ -1503,8 +1624,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t tacc = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                   static_cast<uint32_t>(acc * kAccCols);
             if (gu) {
-                epilogue_gate_up(tacc, valid, a.h + static_cast<size_t>(p) * F +
-                                                   static_cast<size_t>(ti.nb) * 128, a.dev_err);
+                __half* dst = a.h + static_cast<size_t>(p) * F + static_cast<size_t>(ti.nb) * 128;
+                epilogue_gate_up_staged(tacc, valid ? dst : nullptr, stg, lane, a.dev_err);
                 fence_proxy_async_global();
                 __threadfence();
                 __syncwarp();
@@ -1520,9 +1641,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     al = seg.alpha ? seg.alpha[seg.rec_route[p]] : 1.0f;
                     al *= seg.seg_scale[seg.seg_begin + ti.seg];
                 }
-                epilogue_down(tacc, valid, al,
-                              a.out_rows ? a.out_rows + static_cast<size_t>(p) * H : nullptr,
-                              a.Y + static_cast<size_t>(tok) * H, ti.nb * 256);
+                float* dst = a.out_rows ? a.out_rows + static_cast<size_t>(p) * H
+                                        : a.Y + static_cast<size_t>(tok) * H;
+                epilogue_down_staged(tacc, al, valid ? dst + ti.nb * 256 : nullptr, !a.out_rows, stg,
+                                     lane);
             }
             tc_fence_before();
             __syncwarp();

@@ -130,6 +130,20 @@ __device__ __forceinline__ void st_v4(void* addr, uint32_t a, uint32_t b, uint32
                  "r"(d)
                  : "memory");
 }
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
 
 // Shared-memory matrix descriptor of a K-major operand tile whose rows are
 // 128 bytes, stored with the 128-byte swizzle (8-row atoms of 1024 bytes):
