@@ -550,7 +550,11 @@ def measure_q4(args, cfg, wl, dev, stream, flush, peaks):
     Y = torch.empty(cfg.T, cfg.H, dtype=torch.float32, device=dev)
     out = {"format": "4-bit codes, one scale per 32 weights along the reduction (Q4_0-style)"}
     for mode in ("resident", "paged"):
-        st = BoundLayerStack(wl1, mode=mode, wdtype=es.Q4)
+        # paged: banks free before routing are filled in storage order (the
+        # pages' prefetch schedule); with 28 MB groups the route-and-decide
+        # time at the start of a call is a larger share than with bf16
+        st = BoundLayerStack(wl1, mode=mode, wdtype=es.Q4,
+                             schedule=es.SCHED_PREFETCH if mode == "paged" else es.SCHED_AFTER_ROUTING)
         try:
             def one():
                 if mode == "paged":
@@ -590,7 +594,8 @@ def measure_q4(args, cfg, wl, dev, stream, flush, peaks):
                         "TFLOPs": round(6.0 * cfg.H * cfg.F * cfg.T * cfg.k / (ffn_ms / 1e3) / 1e12, 1)})
         else:
             h2d = stats["h2d_bytes"] / len(ms)
-            rec.update({"h2d_bytes_per_layer": int(h2d), "h2d_GBps": round(h2d / (t / 1e3) / 1e9, 1)})
+            rec.update({"schedule": "prefetch before routing", "h2d_bytes_per_layer": int(h2d),
+                        "h2d_GBps": round(h2d / (t / 1e3) / 1e9, 1)})
         out[mode] = rec
     return out
 
@@ -640,6 +645,29 @@ def measure_paged(args, cfg, wl, dev, stream, flush, peaks):
                  "groups": int(len(adsf)), "q": 1, "b": cfg.B, "T_ne_ms": round(t_ne, 4)}
     bytes_per_call = stats["h2d_bytes"] / len(times)
 
+    # the same layers through the prefetch-before-routing schedule
+    stp = BoundLayerStack(wl, mode="paged", schedule=es.SCHED_PREFETCH)
+    try:
+        for _ in range(2):
+            es.arena_invalidate(stp.ctx)
+            stp.prefill(0, X, logits[0], Y)
+        torch.cuda.synchronize()
+        times_pf = []
+        for i in range(steps):
+            for l in range(L):
+                flush.zero_()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                es.arena_invalidate(stp.ctx)
+                a.record(stream)
+                stp.prefill(l, X, logits[l], Y)
+                b.record(stream)
+                b.synchronize()
+                times_pf.append(a.elapsed_time(b))
+        assert es.get_device_error(stp.ctx) == es.OK
+    finally:
+        stp.close()
+    t_pf = sum(times_pf) / len(times_pf)
+
     # the same bytes, copy only (host link alone), and the link's own peak
     pool = st.pools[0]
     dst = torch.empty(int(bytes_per_call) if bytes_per_call else 1, dtype=torch.uint8, device=dev)
@@ -672,7 +700,10 @@ def measure_paged(args, cfg, wl, dev, stream, flush, peaks):
     t_exec = (stats["ms_route"] + stats["ms_ffn"] + stats["ms_shared"]) / len(times)
     h2d_gbs = bytes_per_call / (t_paged / 1e3) / 1e9
     return {
-        "arena": f"P={cfg.P} (G={cfg.G}, B={cfg.B})", "tokens_per_s": round(cfg.T / (t_paged / 1e3), 1),
+        "arena": f"P={cfg.P} (G={cfg.G}, B={cfg.B})", "schedule": "after routing",
+        "tokens_per_s": round(cfg.T / (t_paged / 1e3), 1),
+        "prefetch_before_routing": {"ms_per_layer": round(t_pf, 4),
+                                    "tokens_per_s": round(cfg.T / (t_pf / 1e3), 1)},
         "ms_per_layer": round(t_paged, 4), "h2d_bytes_per_layer": int(bytes_per_call),
         "h2d_GBps": round(h2d_gbs, 1), "h2d_peak_GBps": round(h2d_peak, 1),
         "frac_h2d_peak": round(h2d_gbs / h2d_peak, 4),
