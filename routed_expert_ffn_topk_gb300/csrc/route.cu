@@ -14,7 +14,9 @@
 // chunks of kChunkTokens tokens (16 * k routes):
 //   1. one CTA per chunk, one warp per token: softmax top-k, alpha, and the
 //      chunk's slot counts (shared-memory atomics; counts are order-free),
-//      written bucket-major as hist[slot][chunk];
+//      written bucket-major as hist[slot][chunk]; with a residual A the
+//      rows Y[t] = A[t] are written in the same phase, by the warps of CTAs
+//      added for them first;
 //   2. every warp of the grid scans whole slots (a warp per slot): each
 //      chunk's base inside the slot, and the slot's total;
 //   3. every CTA forms the slot offsets and the m-block prefix (the expert
@@ -167,24 +169,56 @@ __device__ __forceinline__ void topk_token(
 }
 
 // Y[t][:] = fp32(A[t][:]), one warp per row (16-byte vectors; H % 256 == 0).
-__device__ __forceinline__ void init_residual_row(int t, const ResidualInit& r) {
+// The first kResidStageBytes of the row are fetched into a per-warp
+// shared-memory stage with cp.async before the warp ranks its token, so the
+// load latency overlaps the top-k; the rest of a longer row is copied
+// directly afterwards.
+constexpr int kResidStageBytes = 4096;
+constexpr int kResidStageCta = kChunkTokens * kResidStageBytes;  // per CTA: one stage per warp
+
+// Issues the copies of row t's first bytes into `stage`; returns their count.
+__device__ __forceinline__ int stage_residual_row(int t, const ResidualInit& r, char* stage) {
     const int lane = threadIdx.x & 31;
-    float4* y = reinterpret_cast<float4*>(r.Y + static_cast<size_t>(t) * r.H);
-    if (r.elem_bytes == 2) {
-        const uint4* a = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(r.A) +
-                                                        static_cast<size_t>(t) * r.H);
-        for (int c = lane; c < r.H / 8; c += 32) {
-            const uint4 v = a[c];  // 8 bf16: a bf16 is the high half of its fp32
-            y[2 * c] = make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u),
-                                   __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xFFFF0000u));
-            y[2 * c + 1] = make_float4(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xFFFF0000u),
-                                       __uint_as_float(v.w << 16), __uint_as_float(v.w & 0xFFFF0000u));
+    const int row_bytes = r.H * r.elem_bytes;
+    const int staged = min(row_bytes, kResidStageBytes);
+    const char* src = static_cast<const char*>(r.A) + static_cast<size_t>(t) * row_bytes;
+    const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(stage));
+    for (int off = lane * 16; off < staged; off += 32 * 16)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + off), "l"(src + off)
+                     : "memory");
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    return staged;
+}
+
+// Widens bytes [b0, b1) of row t (taken from `src`, shared or global) into Y.
+__device__ __forceinline__ void widen_residual(const ResidualInit& r, int t, const char* src,
+                                               int b0, int b1) {
+    const int lane = threadIdx.x & 31;
+    float* y = r.Y + static_cast<size_t>(t) * r.H;
+    for (int off = b0 + lane * 16; off < b1; off += 32 * 16) {
+        const uint4 v = *reinterpret_cast<const uint4*>(src + off);
+        if (r.elem_bytes == 2) {  // 8 bf16: a bf16 is the high half of its fp32
+            float4* d = reinterpret_cast<float4*>(y + off / 2);
+            d[0] = make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u),
+                               __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xFFFF0000u));
+            d[1] = make_float4(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xFFFF0000u),
+                               __uint_as_float(v.w << 16), __uint_as_float(v.w & 0xFFFF0000u));
+        } else {
+            *reinterpret_cast<uint4*>(y + off / 4) = v;
         }
-    } else {
-        const float4* a = reinterpret_cast<const float4*>(static_cast<const float*>(r.A) +
-                                                          static_cast<size_t>(t) * r.H);
-        for (int c = lane; c < r.H / 4; c += 32) y[c] = a[c];
     }
+}
+
+// Completes row t: the staged bytes from shared memory, the rest from A.
+__device__ __forceinline__ void finish_residual_row(int t, const ResidualInit& r, const char* stage,
+                                                    int staged) {
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    __syncwarp();
+    widen_residual(r, t, stage, 0, staged);
+    const int row_bytes = r.H * r.elem_bytes;
+    if (staged < row_bytes)
+        widen_residual(r, t, static_cast<const char*>(r.A) + static_cast<size_t>(t) * row_bytes,
+                       staged, row_bytes);
 }
 
 // In-place exclusive scan of n ints in shared memory by one CTA of
@@ -338,6 +372,12 @@ __device__ bool grid_barrier(int* counter, int generation, int* err, int* ok_fla
     return *ok_flag != 0;
 }
 
+// Shared memory of k_route_fused before the residual stages: slot counts /
+// offsets, m-block prefix and scan scratch, rounded up to 16 bytes.
+__host__ __device__ constexpr size_t route_scratch_bytes(int nb) {
+    return (sizeof(int) * (2 * static_cast<size_t>(nb) + 33) + 15) & ~static_cast<size_t>(15);
+}
+
 __global__ void __launch_bounds__(kRouteThreads) k_route_fused(
     const float* __restrict__ logits, int T, int E, int k, int renorm,
     const int32_t* __restrict__ phi, int P, int32_t* __restrict__ topk_ids,
@@ -350,19 +390,36 @@ __global__ void __launch_bounds__(kRouteThreads) k_route_fused(
     __shared__ int ok_flag;
     const int R = T * k;
     const int nb = P + 1;
+    // residual stages after the counters and scan scratch (16-byte aligned)
+    const int warp = threadIdx.x >> 5;
+    char* rstage = reinterpret_cast<char*>(smem) + route_scratch_bytes(nb) +
+                   static_cast<size_t>(warp) * kResidStageBytes;
+    // Residual rows go to every warp of the grid, those of the CTAs without a
+    // top-k chunk first (the launch adds such CTAs when a residual is given),
+    // so that the copies run beside the top-k instead of after it. Those CTAs
+    // stage their first row at once; CTAs with chunks start theirs after the
+    // top-k, so that their copies do not queue ahead of the logits loads.
+    const int grid = static_cast<int>(gridDim.x);
+    const int nc = min(nchunk, grid);  // CTAs holding top-k chunks
+    const int b = static_cast<int>(blockIdx.x);
+    const int n_workers = grid * kChunkTokens;
+    int rrow = resid.A ? (b >= nc ? b - nc : b + grid - nc) * kChunkTokens + warp : T;
+    bool pre = rrow < T && b >= nc;
+    int staged = pre ? stage_residual_row(rrow, resid, rstage) : 0;
     // 1. router + the chunk's slot counts, one warp per token
     for (int c = blockIdx.x; c < nchunk; c += gridDim.x) {
-        for (int b = threadIdx.x; b < nb; b += blockDim.x) smem[b] = 0;
+        for (int x = threadIdx.x; x < nb; x += blockDim.x) smem[x] = 0;
         __syncthreads();
-        const int t = c * kChunkTokens + (threadIdx.x >> 5);
-        if (t < T) {
-            topk_token(t, logits, E, k, renorm, phi, P, topk_ids, alpha, smem, err);
-            if (resid.A) init_residual_row(t, resid);
-        }
+        const int t = c * kChunkTokens + warp;
+        if (t < T) topk_token(t, logits, E, k, renorm, phi, P, topk_ids, alpha, smem, err);
         __syncthreads();
-        for (int b = threadIdx.x; b < nb; b += blockDim.x)
-            hist[static_cast<size_t>(b) * nchunk + c] = smem[b];
+        for (int x = threadIdx.x; x < nb; x += blockDim.x)
+            hist[static_cast<size_t>(x) * nchunk + c] = smem[x];
         __syncthreads();
+    }
+    for (; rrow < T; rrow += n_workers, pre = false) {
+        if (!pre) staged = stage_residual_row(rrow, resid, rstage);
+        finish_residual_row(rrow, resid, rstage, staged);
     }
     if (!grid_barrier(sync, 1, err, &ok_flag)) return;
     // 2. per-slot scans over chunks, spread over every warp of the grid
@@ -473,14 +530,16 @@ cudaError_t launch_route_build(const float* logits, int T, int E, int k, int ren
         int dev = 0, sms = 0, per_sm = 0;
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        const size_t max_smem = route_scratch_bytes(kMaxP + 1) + kResidStageCta;
         cudaFuncSetAttribute(k_route_fused, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(sizeof(int) * (2 * (kMaxP + 1) + 33)));
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-            &per_sm, k_route_fused, kRouteThreads, sizeof(int) * (2 * (kMaxP + 1) + 33));
+                             static_cast<int>(max_smem));
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_route_fused, kRouteThreads,
+                                                      max_smem);
         co_resident = sms * (per_sm > 0 ? per_sm : 1);
     }
-    const int grid = std::max(1, std::min(co_resident, w.nchunk));
-    const size_t smem = sizeof(int) * (2 * static_cast<size_t>(nb) + 33);
+    // with a residual, up to as many CTAs again for its rows
+    const int grid = std::max(1, std::min(co_resident, resid.A ? 2 * w.nchunk : w.nchunk));
+    const size_t smem = route_scratch_bytes(nb) + (resid.A ? kResidStageCta : 0);
     void* args[] = {&logits, &T, &E, &k, &renorm, &phi, &P, &topk_ids, &alpha, &offsets,
                     &rec_tok, &rec_route, &rec_pos, &hist, &mblk, &totals, &done, &tickets,
                     &n_tickets, &sync, &err, const_cast<int*>(&w.nchunk), &resid};
