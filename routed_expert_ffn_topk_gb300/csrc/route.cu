@@ -73,16 +73,17 @@ __device__ __forceinline__ void record_error(int* err, int code) {
 // per-expert exponentials to every lane with shuffles, one expert at a time.
 // Selection walks the strict total order (logit descending, expert id
 // ascending): round j takes the best expert after round j-1's pick in that
-// order, found by a warp-wide (value, id) reduction.
+// order. Each logit is mapped to an unsigned key of the same order (-0 taken
+// as +0, which compares equal to it), so a round is one warp-wide max of the
+// keys and one min of the ids holding it. Lane j then forms route j's weight.
 constexpr int kMaxPerLane = kMaxE / 32;
 constexpr int kRouteThreads = 512;
 constexpr int kChunkTokens = kRouteThreads / 32;  // one token per warp
 constexpr uint64_t kGridWaitLimitNs = 1000000000ull;  // 1 s
 
-__device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib) {
-    return va > vb || (va == vb && ia < ib);
-}
-
+// kJ: logits held per lane (E <= 32 kJ), so that small E keeps the arrays in
+// registers.
+template <int kJ>
 __device__ __forceinline__ void topk_token(
     int t, const float* __restrict__ logits, int E, int k, int renorm,
     const int32_t* __restrict__ phi, int P, int32_t* __restrict__ topk_ids,
@@ -91,63 +92,75 @@ __device__ __forceinline__ void topk_token(
     const float* l = logits + static_cast<size_t>(t) * E;
     const int nj = (E + 31) >> 5;
     const float kNegInf = __int_as_float(0xff800000);
-    float v[kMaxPerLane];
+    float v[kJ];
 #pragma unroll
-    for (int j = 0; j < kMaxPerLane; ++j) {
+    for (int j = 0; j < kJ; ++j) {
         const int e = lane + 32 * j;
         v[j] = (j < nj && e < E) ? l[e] : kNegInf;
     }
     float m = kNegInf;
 #pragma unroll
-    for (int j = 0; j < kMaxPerLane; ++j) m = fmaxf(m, v[j]);
+    for (int j = 0; j < kJ; ++j) m = fmaxf(m, v[j]);
 #pragma unroll
     for (int d = 16; d > 0; d >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, d));
 
     // denominator: sequential fp32 sum over e = 0, 1, ..., E-1
     float s = 0.0f;
 #pragma unroll
-    for (int j = 0; j < kMaxPerLane; ++j) {
+    for (int j = 0; j < kJ; ++j) {
         if (j >= nj) break;
         const int e = lane + 32 * j;
         const float p = (e < E) ? route_exp(__fsub_rn(v[j], m)) : 0.0f;
         const int n_here = min(32, E - 32 * j);
-        for (int src = 0; src < n_here; ++src)
-            s = __fadd_rn(s, __shfl_sync(0xffffffffu, p, src));
+        if (n_here == 32) {
+#pragma unroll
+            for (int src = 0; src < 32; ++src) s = __fadd_rn(s, __shfl_sync(0xffffffffu, p, src));
+        } else {
+            for (int src = 0; src < n_here; ++src)
+                s = __fadd_rn(s, __shfl_sync(0xffffffffu, p, src));
+        }
     }
 
-    float prev_v = __int_as_float(0x7f800000);  // +inf: every expert comes after it
-    int prev_i = -1;
-    float a_mine = 0.0f;   // lane j keeps route j's weight
+    // order-preserving keys (entries past E are never candidates)
+    uint32_t key[kJ];
+#pragma unroll
+    for (int j = 0; j < kJ; ++j) {
+        const uint32_t b = __float_as_uint(__fadd_rn(v[j], 0.0f));  // -0 -> +0
+        key[j] = (j < nj && lane + 32 * j < E) ? ((b & 0x80000000u) ? ~b : (b | 0x80000000u)) : 0u;
+    }
+    uint32_t prev_k = 0xffffffffu;  // every expert comes after it
+    uint32_t prev_i = 0u;           // with prev_k = max, ids compare as "after" from 0 on
+    bool first = true;
+    uint32_t key_mine = 0u;  // lane j keeps route j's key and expert
     int id_mine = -1;
     for (int r = 0; r < k; ++r) {
-        float bv = kNegInf;
-        int bi = 0x7fffffff;
+        uint32_t bk = 0u, bi = 0xffffffffu;
 #pragma unroll
-        for (int j = 0; j < kMaxPerLane; ++j) {
+        for (int j = 0; j < kJ; ++j) {
             if (j >= nj) break;
-            const int e = lane + 32 * j;
-            if (e >= E) break;
-            const bool after_prev = (v[j] < prev_v) || (v[j] == prev_v && e > prev_i);
-            if (after_prev && ranks_before(v[j], e, bv, bi)) {
-                bv = v[j];
+            const uint32_t e = static_cast<uint32_t>(lane + 32 * j);
+            if (static_cast<int>(e) >= E) break;
+            const bool after_prev =
+                first || key[j] < prev_k || (key[j] == prev_k && e > prev_i);
+            if (after_prev && (key[j] > bk || (key[j] == bk && e < bi))) {
+                bk = key[j];
                 bi = e;
             }
         }
-#pragma unroll
-        for (int d = 16; d > 0; d >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, d);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, d);
-            if (ranks_before(ov, oi, bv, bi)) {
-                bv = ov;
-                bi = oi;
-            }
-        }
-        prev_v = bv;
-        prev_i = bi;
+        const uint32_t mk = __reduce_max_sync(0xffffffffu, bk);
+        const uint32_t mi = __reduce_min_sync(0xffffffffu, bk == mk ? bi : 0xffffffffu);
+        prev_k = mk;
+        prev_i = mi;
+        first = false;
         if (lane == r) {
-            id_mine = bi;
-            a_mine = __fdiv_rn(route_exp(__fsub_rn(bv, m)), s);
+            key_mine = mk;
+            id_mine = static_cast<int>(mi);
         }
+    }
+    float a_mine = 0.0f;
+    if (lane < k) {
+        const float bv = __uint_as_float((key_mine & 0x80000000u) ? (key_mine & 0x7fffffffu) : ~key_mine);
+        a_mine = __fdiv_rn(route_exp(__fsub_rn(bv, m)), s);
     }
     if (renorm) {
         float z = 0.0f;  // summed in rank order
@@ -378,7 +391,7 @@ __host__ __device__ constexpr size_t route_scratch_bytes(int nb) {
     return (sizeof(int) * (2 * static_cast<size_t>(nb) + 33) + 15) & ~static_cast<size_t>(15);
 }
 
-__global__ void __launch_bounds__(kRouteThreads) k_route_fused(
+__global__ void __launch_bounds__(kRouteThreads, 2) k_route_fused(
     const float* __restrict__ logits, int T, int E, int k, int renorm,
     const int32_t* __restrict__ phi, int P, int32_t* __restrict__ topk_ids,
     float* __restrict__ alpha, int32_t* __restrict__ offsets, int32_t* __restrict__ rec_tok,
@@ -411,7 +424,18 @@ __global__ void __launch_bounds__(kRouteThreads) k_route_fused(
         for (int x = threadIdx.x; x < nb; x += blockDim.x) smem[x] = 0;
         __syncthreads();
         const int t = c * kChunkTokens + warp;
-        if (t < T) topk_token(t, logits, E, k, renorm, phi, P, topk_ids, alpha, smem, err);
+        if (t < T) {
+            if (E <= 32)
+                topk_token<1>(t, logits, E, k, renorm, phi, P, topk_ids, alpha, smem, err);
+            else if (E <= 64)
+                topk_token<2>(t, logits, E, k, renorm, phi, P, topk_ids, alpha, smem, err);
+            else if (E <= 128)
+                topk_token<4>(t, logits, E, k, renorm, phi, P, topk_ids, alpha, smem, err);
+            else if (E <= 256)
+                topk_token<8>(t, logits, E, k, renorm, phi, P, topk_ids, alpha, smem, err);
+            else
+                topk_token<kMaxPerLane>(t, logits, E, k, renorm, phi, P, topk_ids, alpha, smem, err);
+        }
         __syncthreads();
         for (int x = threadIdx.x; x < nb; x += blockDim.x)
             hist[static_cast<size_t>(x) * nchunk + c] = smem[x];
