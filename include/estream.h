@@ -319,8 +319,9 @@ estream_status estream_moe_layer_prefill(estream_ctx* c, int layer, const void* 
 /*
  * The same layer with the residual of Eq. 2 given explicitly:
  * Y = A + sum_j alpha_{t,j} F_{e_{t,j}}(X_t) (+ shared experts). Y is written,
- * not read: the route build initialises each token's row from A while it
- * routes the token, so the caller needs no separate copy of A into Y.
+ * not read: the route build initialises the rows from A in the same pass
+ * that ranks the tokens' experts, so the caller needs no separate copy of A
+ * into Y.
  * A       device, [T][H] in X's type (bf16, or fp32 for ESTREAM_F32), 16-byte
  *         aligned; A == X (the usual residual stream) is allowed.
  * The other arguments and the behaviour are those of
