@@ -734,6 +734,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------ TMA producer (weights) ------------------------------
         int stage = 0;
         uint32_t phase = 0;
+        const uint64_t evict_first = policy_evict_first();
         int issued[kStages];
         for (int s = 0; s < kStages; ++s) issued[s] = -1;
         bool ok = true;
@@ -752,6 +753,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int num_kb = gu ? KBA : KBB;
             const int tile_rows = gu ? 128 : 256;
             const int brow0 = (slot * (gu ? NBA : NBB) + ti.nb) * num_kb * tile_rows;
+            // a segment of one m-block is its weight tiles' only reader: those
+            // tiles are loaded evict-first (tiles read by further m-blocks keep
+            // the default policy; marking them measured slower)
+            const bool only_reader = table[ti.seg + 1] - table[ti.seg] == 1;
             if (!gu) {
                 // the m-block's h rows are complete once every epilogue warp of
                 // every gate/up n-block has published
@@ -780,12 +785,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t b_dst = sB + stage * kTileBBytes;
                     const int brow = brow0 + kb * tile_rows;
                     if (gu) {
-                        tma_load_2d(b_dst, &tm_wg, 0, brow, full_bar(stage));
-                        tma_load_2d(b_dst + 128 * kRowBytes, &tm_wu, 0, brow, full_bar(stage));
+                        if (only_reader) {
+                            tma_load_2d_hint(b_dst, &tm_wg, 0, brow, full_bar(stage), evict_first);
+                            tma_load_2d_hint(b_dst + 128 * kRowBytes, &tm_wu, 0, brow,
+                                             full_bar(stage), evict_first);
+                        } else {
+                            tma_load_2d(b_dst, &tm_wg, 0, brow, full_bar(stage));
+                            tma_load_2d(b_dst + 128 * kRowBytes, &tm_wu, 0, brow, full_bar(stage));
+                        }
                     } else {
                         tma_load_2d(sA + stage * kTileABytes, &tm_h, kb * 64, ti.row0,
                                     full_bar(stage));
-                        tma_load_2d(b_dst, &tm_wd, 0, brow, full_bar(stage));
+                        if (only_reader)
+                            tma_load_2d_hint(b_dst, &tm_wd, 0, brow, full_bar(stage), evict_first);
+                        else
+                            tma_load_2d(b_dst, &tm_wd, 0, brow, full_bar(stage));
                     }
                 }
                 __syncwarp();
@@ -1219,6 +1233,14 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(cl_bar)
         : "memory");
 }
+__device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t dst, const CUtensorMap* tm, int x,
+                                                      int y, uint32_t cl_bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(cl_bar), "l"(policy)
+        : "memory");
+}
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
                  "r"(ncols)
@@ -1396,6 +1418,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const int brow_step = gu ? 128 : 256;
             const bool load_h = !gu && ti.rows > 0;
+            // a segment of one pair m-block is its weight tiles' only reader
+            const bool only_reader = table[ti.seg + 1] - table[ti.seg] == 1;
             if (load_h) {
                 // this half's h rows are complete once every epilogue warp of
                 // every gate/up n-block of its m-block has published
@@ -1436,7 +1460,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) {
                     if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), tx);
                     const uint32_t lbar = map_rank(full_bar(stage), 0);
-                    tma_load_2d_pair(sB + stage * kPHalf, tm_b, 0, brow0 + kb * brow_step, lbar);
+                    if (only_reader)
+                        tma_load_2d_pair_hint(sB + stage * kPHalf, tm_b, 0, brow0 + kb * brow_step,
+                                              lbar, policy_evict_first());
+                    else
+                        tma_load_2d_pair(sB + stage * kPHalf, tm_b, 0, brow0 + kb * brow_step, lbar);
                     if (load_h)
                         tma_load_2d_pair(sA + stage * kPHalf, &tm_h, kb * 64, ti.row0, lbar);
                 }
