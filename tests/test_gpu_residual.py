@@ -47,3 +47,33 @@ def test_residual_call(key, mode, q4):
     else:
         ref3 = ref3 + wl.X.double().numpy()
     _gpu.assert_y_close(Y3.cpu().numpy(), ref3, f"residual X {key}/{mode}")
+
+
+@pytest.mark.parametrize("T,E,k", [(4096, 300, 2), (100, 64, 8), (2500, 33, 3), (1, 8, 2)])
+def test_residual_rows_bit_exact(T, E, k):
+    """Residual rows at shapes that use every path of the route build's row
+    writers: CTAs added for rows only (small T), top-k CTAs that also take rows
+    (T = 4096: more chunks than added CTAs fit), ragged last chunks, one token,
+    and E above 256 (the widest per-lane logit arrays). Bit for bit against a
+    copy of A into Y followed by the accumulating call (deterministic mode)."""
+    from routed_expert_ffn_topk_gb300 import estream as es
+    from routed_expert_ffn_topk_gb300 import workloads as W
+    from routed_expert_ffn_topk_gb300.layer import BoundLayerStack
+    cfg = W.scaled(W.CONFIGS["c2"], T=T, H=256, E=E, k=k, F=128, key_suffix=f"-resid{T}")
+    wl = W.make_workload(cfg, seed=T + E)
+    dev = _gpu.device()
+    st = BoundLayerStack(wl, mode="resident", deterministic=True)
+    try:
+        X = wl.X.to(dev)
+        lg = wl.logits[0].to(dev)
+        A = torch.randn(X.shape, generator=torch.Generator().manual_seed(T), dtype=torch.float32)
+        A = A.to(X.dtype).to(dev)
+        Y1 = A.float().clone()
+        st.prefill(0, X, lg, Y1)
+        Y2 = torch.full_like(Y1, float("nan"))
+        st.prefill(0, X, lg, Y2, residual=A)
+        torch.cuda.synchronize()
+        assert es.get_device_error(st.ctx) == es.OK
+        assert torch.equal(Y1.view(torch.int32), Y2.view(torch.int32))
+    finally:
+        st.close()

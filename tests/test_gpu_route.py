@@ -60,6 +60,10 @@ def test_route_adversarial_logits():
     lg[80:120] = np.round(lg[80:120])               # many ties
     lg[120:160] *= 80.0                             # exponent underflow for most experts
     lg[160:200, :] = lg[160:161, :]                 # identical rows
+    lg[200:240] = 0.0
+    lg[200:240, ::3] = -0.0                         # signed zeros compare equal: id order decides
+    lg[240:260, ::2] = -0.0
+    lg[240:260, 1::4] = 1e-30                       # tiny positives above both zeros
     for renorm in (0, 1):
         _check(lg, k, renorm)
 
