@@ -15,9 +15,11 @@
 // h columns, m-block), then every down tile (segment, n-block of 256 Y
 // columns, m-block). Warp roles per CTA (one CTA per SM):
 //   warp 0     TMA producer into a 4-stage ring: the weight tiles (gate + up
-//              2 x 16 KB, or down 32 KB, per stage) and, for down tiles, the
-//              16 KB A tile of h once the m-block's gate/up tiles have all
-//              published (records are contiguous by slot, so a plain box).
+//              2 x 16 KB, or down 32 KB, per stage; evict-first in L2 when the
+//              segment has a single m-block, their only reader) and, for down
+//              tiles, the 16 KB A tile of h once the m-block's gate/up tiles
+//              have all published (records are contiguous by slot, so a plain
+//              box).
 //   warp 1     allocates 512 TMEM columns (two 128x256 fp32 accumulators);
 //              one lane issues tcgen05.mma (M=128, N=256, K=16 per
 //              instruction, kind::f16), committing stages back to the
@@ -26,7 +28,9 @@
 //              h = SiLU(g) * u as fp16 and publish "m-block done" counters;
 //              down tiles scale by alpha times the expert's down-weight scale
 //              and add into Y[t] with vector fp32 reductions (or store the
-//              scaled row for the deterministic combine).
+//              scaled row for the deterministic combine). Rows go out through
+//              a per-warp shared-memory stage, four whole rows per
+//              instruction.
 //   warps 6-9  row gather of gate/up tiles: each record's 128-byte slice of
 //              X[tok] for the stage's K range is copied with 16-byte cp.async
 //              into the 128-byte-swizzled layout the MMA reads (chunk c of row
