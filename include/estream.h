@@ -353,7 +353,11 @@ estream_status estream_reset_stats(estream_ctx* c);
 estream_status estream_last_stats(estream_ctx* c, estream_stats* out);
 
 /* Synchronises the library's streams, returns and clears the device error
- * word (ESTREAM_OK, ESTREAM_ERR_TIMEOUT or ESTREAM_ERR_DEVICE). */
+ * words (ESTREAM_OK, ESTREAM_ERR_TIMEOUT or ESTREAM_ERR_DEVICE): the
+ * context's, set by the expert kernels and kept until read, and the route
+ * build's, set by the latest call's routing. A route build whose grid
+ * barrier gave up leaves an empty route map, so the call computes no routed
+ * experts and this call reports ESTREAM_ERR_TIMEOUT. */
 estream_status estream_get_device_error(estream_ctx* c);
 
 /* Residency-table trace for tests: writes up to `cap` events as
@@ -406,6 +410,14 @@ estream_status estream_autoconfig(int n_g, const int* g_values, const int* K_per
                                   const double* const* L_per_g, const double* const* X_per_g,
                                   double T_ne, int Q0, double M_max, const double* M_other_per_g,
                                   double W_e, int N_e, int* G_out, int* B_out, double* T_out);
+
+/* Test of the route build's bounded grid barrier: in the next layer call one
+ * CTA of the route build does not arrive at its first grid barrier, so the
+ * other CTAs' wait (1 s) runs out. That call leaves an empty route map
+ * (no routed expert is computed; the residual rows, if given, are written),
+ * returns ESTREAM_OK, and estream_get_device_error then reports
+ * ESTREAM_ERR_TIMEOUT. Later calls are unaffected. No GPU fault is involved. */
+estream_status estream_inject_route_timeout(estream_ctx* c);
 
 /* Host-side fault injection for tests: the pager refuses to fill group
  * `group` of `layer` (before any copy is issued) and the call returns

@@ -57,7 +57,7 @@ cudaError_t launch_route_build(const float* logits, int T, int E, int k, int ren
                                int32_t* offsets, int32_t* rec_tok, int32_t* rec_route,
                                int32_t* rec_pos, int32_t* done, int32_t* tickets, int n_tickets,
                                void* ws, cudaStream_t stream, int* n_launches,
-                               const ResidualInit* resid = nullptr);
+                               const ResidualInit* resid = nullptr, int withhold_arrival = 0);
 
 // Identity route map for the shared experts: n_shared segments of T rows,
 // rec_tok[p] = p mod T, offsets[s] = s*T, mblk[s] = s*ceil(T/kBM); zeroes

@@ -1712,6 +1712,7 @@ __global__ void k_combine(const float* __restrict__ rows, const int32_t* __restr
     float4 y = *reinterpret_cast<const float4*>(Y + static_cast<size_t>(t) * H + c);
     for (int j = 0; j < k; ++j) {
         const int p = pos[t * k + j];
+        if (p < 0 || p >= T * k) continue;  // not placed (a route build that gave up)
         const float4 v = *reinterpret_cast<const float4*>(rows + static_cast<size_t>(p) * H + c);
         y.x += v.x; y.y += v.y; y.z += v.z; y.w += v.w;
     }

@@ -357,11 +357,14 @@ __device__ void scatter_chunk(int c, int nchunk, const int32_t* __restrict__ top
 
 // Grid-wide barrier for a cooperative launch, bounded in time: returns false
 // (after recording a timeout) if the other CTAs did not arrive within the limit.
-__device__ bool grid_barrier(int* counter, int generation, int* err, int* ok_flag) {
+// withhold: this CTA does not arrive (a test of the bounded wait: the other
+// CTAs' wait runs out and records a timeout; so does this CTA's own).
+__device__ bool grid_barrier(int* counter, int generation, int* err, int* ok_flag,
+                             bool withhold = false) {
     __syncthreads();
     if (threadIdx.x == 0) {
         __threadfence();
-        atomicAdd(counter, 1);
+        if (!withhold) atomicAdd(counter, 1);
         const int target = generation * gridDim.x;
         uint64_t t0;
         asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
@@ -391,6 +394,16 @@ __host__ __device__ constexpr size_t route_scratch_bytes(int nb) {
     return (sizeof(int) * (2 * static_cast<size_t>(nb) + 33) + 15) & ~static_cast<size_t>(15);
 }
 
+// After a grid barrier gave up (recorded as a timeout) CTA 0 leaves an empty
+// route map, so that kernels reading it find no records.
+__device__ void empty_route_map(int32_t* offsets, int32_t* mblk, int P) {
+    if (blockIdx.x != 0) return;
+    for (int b = threadIdx.x; b < P + 2; b += blockDim.x) {
+        offsets[b] = 0;
+        mblk[b] = 0;
+    }
+}
+
 __global__ void __launch_bounds__(kRouteThreads, 2) k_route_fused(
     const float* __restrict__ logits, int T, int E, int k, int renorm,
     const int32_t* __restrict__ phi, int P, int32_t* __restrict__ topk_ids,
@@ -398,7 +411,7 @@ __global__ void __launch_bounds__(kRouteThreads, 2) k_route_fused(
     int32_t* __restrict__ rec_route, int32_t* __restrict__ rec_pos, int32_t* __restrict__ hist,
     int32_t* __restrict__ mblk, int32_t* __restrict__ totals, int32_t* __restrict__ done,
     int32_t* __restrict__ tickets, int n_tickets, int* __restrict__ sync, int* __restrict__ err,
-    int nchunk, ResidualInit resid) {
+    int nchunk, ResidualInit resid, int withhold_arrival) {
     extern __shared__ int smem[];
     __shared__ int ok_flag;
     const int R = T * k;
@@ -445,10 +458,16 @@ __global__ void __launch_bounds__(kRouteThreads, 2) k_route_fused(
         if (!pre) staged = stage_residual_row(rrow, resid, rstage);
         finish_residual_row(rrow, resid, rstage, staged);
     }
-    if (!grid_barrier(sync, 1, err, &ok_flag)) return;
+    if (!grid_barrier(sync, 1, err, &ok_flag, withhold_arrival != 0 && blockIdx.x == 0)) {
+        empty_route_map(offsets, mblk, P);
+        return;
+    }
     // 2. per-slot scans over chunks, spread over every warp of the grid
     scan_slots(hist, nchunk, nb, totals);
-    if (!grid_barrier(sync, 2, err, &ok_flag)) return;
+    if (!grid_barrier(sync, 2, err, &ok_flag)) {
+        empty_route_map(offsets, mblk, P);
+        return;
+    }
     // 3. slot offsets and m-block prefix from the totals (in every CTA), then
     //    stable placement, one chunk per CTA at a time; the expert kernel's
     //    per-m-block counters start from zero
@@ -525,7 +544,7 @@ cudaError_t launch_route_build(const float* logits, int T, int E, int k, int ren
                                int32_t* offsets, int32_t* rec_tok, int32_t* rec_route,
                                int32_t* rec_pos, int32_t* done, int32_t* tickets, int n_tickets,
                                void* ws, cudaStream_t stream, int* n_launches,
-                               const ResidualInit* resid_in) {
+                               const ResidualInit* resid_in, int withhold_arrival) {
     const RouteWorkspace w = route_workspace_layout(T, k, P);
     char* base = static_cast<char*>(ws);
     int* err = reinterpret_cast<int*>(base + w.err_off);
@@ -566,7 +585,8 @@ cudaError_t launch_route_build(const float* logits, int T, int E, int k, int ren
     const size_t smem = route_scratch_bytes(nb) + (resid.A ? kResidStageCta : 0);
     void* args[] = {&logits, &T, &E, &k, &renorm, &phi, &P, &topk_ids, &alpha, &offsets,
                     &rec_tok, &rec_route, &rec_pos, &hist, &mblk, &totals, &done, &tickets,
-                    &n_tickets, &sync, &err, const_cast<int*>(&w.nchunk), &resid};
+                    &n_tickets, &sync, &err, const_cast<int*>(&w.nchunk), &resid,
+                    &withhold_arrival};
     rc = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(k_route_fused), grid,
                                      kRouteThreads, args, smem, stream);
     if (rc != cudaSuccess) return rc;

@@ -99,6 +99,7 @@ struct estream_ctx {
     std::vector<GroupEvents> pipe;
     cudaEvent_t pipe_t0 = nullptr, pipe_tne = nullptr;
     int fault_layer = -1, fault_group = -1;
+    bool route_withhold_next = false;  // test: the next route build withholds an arrival
 };
 
 namespace {
@@ -625,6 +626,9 @@ estream_status estream_bind_arena(estream_ctx** out, const estream_arena_desc* d
             if (d->n_shared > 0) c->out_shared = reinterpret_cast<float*>(c->ws + o_outs);
         }
         if (cudaMemset(c->ws, 0, o_perm) != cudaSuccess) break;
+        // the route build's error word and grid-barrier counter
+        if (cudaMemset(c->route_ws, 0, route_workspace_layout(0, 1, 0).hist_off) != cudaSuccess)
+            break;
         if (cudaMemcpy(c->d_perm, c->perm.data(), sizeof(int32_t) * c->perm.size(),
                        cudaMemcpyHostToDevice) != cudaSuccess)
             break;
@@ -1028,10 +1032,12 @@ static estream_status prefill_impl(estream_ctx* c, int layer, const void* X, con
         if (launch_route_build(logits, T, E, k, renorm, c->d_perm + static_cast<size_t>(layer) * E, E,
                                c->topk_ids, c->alpha, c->offsets, c->rec_tok, c->rec_route,
                                c->d.deterministic ? c->rec_pos : nullptr, c->done, c->tickets, E + 2,
-                               c->route_ws, s, &launches, A ? &ri : nullptr) != cudaSuccess) {
+                               c->route_ws, s, &launches, A ? &ri : nullptr,
+                               c->route_withhold_next ? 1 : 0) != cudaSuccess) {
             drain(c, s);
             return ESTREAM_ERR_CUDA;
         }
+        c->route_withhold_next = false;
         c->stats.launches += launches;
     }
     if (trace_pipe) {
@@ -1199,12 +1205,21 @@ estream_status estream_get_device_error(estream_ctx* c) {
     if (!c) return ESTREAM_ERR_NOT_BOUND;
     if (sync_copies(c) != ESTREAM_OK) return ESTREAM_ERR_CUDA;
     if (cudaDeviceSynchronize() != cudaSuccess) return ESTREAM_ERR_CUDA;
-    int host = 0;
-    if (cudaMemcpy(&host, c->dev_err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
-        return ESTREAM_ERR_CUDA;
-    if (host == kDevErrNone) return ESTREAM_OK;
-    if (cudaMemset(c->dev_err, 0, sizeof(int)) != cudaSuccess) return ESTREAM_ERR_CUDA;
-    return host == kDevErrTimeout ? ESTREAM_ERR_TIMEOUT : ESTREAM_ERR_DEVICE;
+    // the context's word (expert kernels, sticky until read) and the route
+    // build's own word (the latest call's routing)
+    int* words[2] = {c->dev_err, reinterpret_cast<int*>(static_cast<char*>(c->route_ws) +
+                                                        route_workspace_layout(0, 1, 0).err_off)};
+    int first = kDevErrNone;
+    for (int* w : words) {
+        int host = 0;
+        if (cudaMemcpy(&host, w, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+            return ESTREAM_ERR_CUDA;
+        if (host == kDevErrNone) continue;
+        if (first == kDevErrNone) first = host;
+        if (cudaMemset(w, 0, sizeof(int)) != cudaSuccess) return ESTREAM_ERR_CUDA;
+    }
+    if (first == kDevErrNone) return ESTREAM_OK;
+    return first == kDevErrTimeout ? ESTREAM_ERR_TIMEOUT : ESTREAM_ERR_DEVICE;
 }
 
 estream_status estream_residency_trace(estream_ctx* c, int32_t* out, int cap, int* n) {
@@ -1239,6 +1254,12 @@ estream_status estream_pipeline_trace(estream_ctx* c, double* adsf, int cap, int
             return ESTREAM_ERR_CUDA;
     }
     *n = static_cast<int>(c->pipe.size());
+    return ESTREAM_OK;
+}
+
+estream_status estream_inject_route_timeout(estream_ctx* c) {
+    if (!c) return ESTREAM_ERR_NOT_BOUND;
+    c->route_withhold_next = true;
     return ESTREAM_OK;
 }
 
