@@ -419,6 +419,15 @@ estream_status estream_autoconfig(int n_g, const int* g_values, const int* K_per
  * ESTREAM_ERR_TIMEOUT. Later calls are unaffected. No GPU fault is involved. */
 estream_status estream_inject_route_timeout(estream_ctx* c);
 
+/* Test of the expert kernels' bounded waits: the next layer call runs the
+ * routed expert kernels' down tiles without their gate/up tiles, so each down
+ * tile's wait for its m-block's h rows (2 s) runs out. Every CTA then stops,
+ * lets the copies and MMAs it issued complete, frees its tensor memory and
+ * returns; the call returns ESTREAM_OK and estream_get_device_error reports
+ * ESTREAM_ERR_TIMEOUT. Y then holds no routed contribution. Later calls are
+ * unaffected. No GPU fault is involved. */
+estream_status estream_inject_expert_timeout(estream_ctx* c);
+
 /* Host-side fault injection for tests: the pager refuses to fill group
  * `group` of `layer` (before any copy is issued) and the call returns
  * ESTREAM_ERR_PAGER with the streams drained. group < 0 turns it off. */

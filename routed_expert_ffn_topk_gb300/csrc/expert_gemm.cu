@@ -596,7 +596,7 @@ __device__ void role_mma(const FfnArgs& a, const TileWalk& w, Ring ring, uint32_
     if (!ok && issued_any) {
         // wait (bounded) for the MMAs already issued before TMEM is freed
         umma_commit(drain_bar);
-        mbar_wait(drain_bar, 0, abort_flag, nullptr, kDrainLimitNs);
+        mbar_wait_drain(drain_bar, 0);
     }
 }
 
@@ -816,9 +816,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok && lane == 0) {
             // let every copy already issued land before the CTA goes away
             for (int s = 0; s < kStages; ++s)
-                if (issued[s] >= 0)
-                    mbar_wait(full_bar(s), static_cast<uint32_t>(issued[s]), abort_flag, nullptr,
-                              kDrainLimitNs);
+                if (issued[s] >= 0) mbar_wait_drain(full_bar(s), static_cast<uint32_t>(issued[s]));
         }
     } else if (warp >= kLoaderWarp0) {
         role_gather<kStages, kLoaderDepth>(a, walk, ring, sA, abort_flag, warp - kLoaderWarp0, lane);
@@ -1111,9 +1109,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
             }
             if (!ok)
                 for (int s = 0; s < kQPStages; ++s)
-                    if (issued[s] >= 0)
-                        mbar_wait(pring.full(s), static_cast<uint32_t>(issued[s]), abort_flag, nullptr,
-                                  kDrainLimitNs);
+                    if (issued[s] >= 0) mbar_wait_drain(pring.full(s), static_cast<uint32_t>(issued[s]));
         }
         __syncwarp();
     } else if (warp >= kConvWarp0) {
@@ -1197,6 +1193,15 @@ __device__ __forceinline__ bool mbar_try_wait_cl(uint32_t bar, uint32_t parity) 
     return ok != 0;
 }
 // mbar_wait with cluster-scope acquire (arrivals come from the peer CTA).
+// The cluster-scope form of mbar_wait_drain (ignores the abort flag).
+__device__ bool mbar_wait_cl_drain(uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait_cl(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    while (!mbar_try_wait_cl(bar, parity))
+        if (global_ns() - t0 > kDrainLimitNs) return false;
+    return true;
+}
+
 __device__ bool mbar_wait_cl(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* dev_err) {
     if (mbar_try_wait_cl(bar, parity)) return true;
     const uint64_t t0 = global_ns();
@@ -1629,7 +1634,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok && issued_any) {
                 umma_commit_pair(drain_bar);
-                mbar_wait_cl(drain_bar, 0, abort_flag, nullptr);
+                mbar_wait_cl_drain(drain_bar, 0);
             }
         }
         __syncwarp();

@@ -124,8 +124,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
             if (!ok)
                 for (int q = 0; q < kRStages; ++q)
                     if (issued[q] >= 0)
-                        mbar_wait(full_bar(q), static_cast<uint32_t>(issued[q]), abort_flag, nullptr,
-                                  kDrainLimitNs);
+                        mbar_wait_drain(full_bar(q), static_cast<uint32_t>(issued[q]));
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -158,7 +157,12 @@ __global__ void __launch_bounds__(kRThreads, 1)
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
         bool w = true;
-        if (lane == 0) w = mbar_wait(acc_bar, 0, abort_flag, a.dev_err);
+        if (lane == 0) {
+            w = mbar_wait(acc_bar, 0, abort_flag, a.dev_err);
+            // after an abort the MMAs already issued still complete (the MMA
+            // thread always commits this barrier) before TMEM is freed
+            if (!w) mbar_wait_drain(acc_bar, 0);
+        }
         w = __shfl_sync(0xffffffffu, w, 0);
         tc_fence_after();
         if (w && !*abort_flag) {

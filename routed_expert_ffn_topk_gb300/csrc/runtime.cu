@@ -100,6 +100,8 @@ struct estream_ctx {
     cudaEvent_t pipe_t0 = nullptr, pipe_tne = nullptr;
     int fault_layer = -1, fault_group = -1;
     bool route_withhold_next = false;  // test: the next route build withholds an arrival
+    int ffn_phases = 3;                // routed expert kernels: bit 0 gate/up tiles, bit 1 down tiles
+    bool ffn_down_only_next = false;   // test: the next call runs the down tiles alone
 };
 
 namespace {
@@ -808,14 +810,14 @@ estream_status run_routed(estream_ctx* c, cudaStream_t s, const void* X, int lay
                                   reinterpret_cast<const uint8_t*>(c->plane_u),
                                   reinterpret_cast<const uint8_t*>(c->plane_d), c->S_gu, c->S_d,
                                   &c->tm_h, seg, X, c->h, Y, c->out_rows, c->done, ticket, c->d.H,
-                                  c->d.F, 3, c->dev_err, c->num_sms, s);
+                                  c->d.F, c->ffn_phases, c->dev_err, c->num_sms, s);
         c->stats.launches += 1;
     } else {
         rc = pair
                  ? launch_expert_ffn_pair(&c->tm_wg, &c->tm_wu, &c->tm_wd_half, &c->tm_h, seg, X, c->h,
-                                          Y, c->out_rows, c->done, c->d.H, c->d.F, 3, c->dev_err, s)
+                                          Y, c->out_rows, c->done, c->d.H, c->d.F, c->ffn_phases, c->dev_err, s)
                  : launch_expert_ffn(&c->tm_wg, &c->tm_wu, &c->tm_wd, &c->tm_h, seg, X, c->h, Y,
-                                     c->out_rows, c->done, nullptr, c->d.H, c->d.F, 3, c->dev_err,
+                                     c->out_rows, c->done, nullptr, c->d.H, c->d.F, c->ffn_phases, c->dev_err,
                                      c->num_sms, s);
         c->stats.launches += 1;
     }
@@ -974,6 +976,10 @@ static estream_status prefill_impl(estream_ctx* c, int layer, const void* X, con
         return ESTREAM_ERR_INVALID_ARG;
     if (!aligned(X, 16) || !aligned(Y, 16) || (A && !aligned(A, 16))) return ESTREAM_ERR_INVALID_ARG;
     if (T > c->d.T_max || k > c->d.k_max) return ESTREAM_ERR_CAPACITY;
+    // this call's routed expert kernels: both tile phases, or (a test of the
+    // bounded waits) the down tiles alone, whose m-block counters then never fill
+    c->ffn_phases = c->ffn_down_only_next ? 2 : 3;
+    c->ffn_down_only_next = false;
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
     const int E = c->d.E, G = c->d.G, H = c->d.H;
     c->trace.clear();
@@ -1254,6 +1260,12 @@ estream_status estream_pipeline_trace(estream_ctx* c, double* adsf, int cap, int
             return ESTREAM_ERR_CUDA;
     }
     *n = static_cast<int>(c->pipe.size());
+    return ESTREAM_OK;
+}
+
+estream_status estream_inject_expert_timeout(estream_ctx* c) {
+    if (!c) return ESTREAM_ERR_NOT_BOUND;
+    c->ffn_down_only_next = true;
     return ESTREAM_OK;
 }
 

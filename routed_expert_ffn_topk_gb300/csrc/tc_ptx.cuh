@@ -44,6 +44,16 @@ __device__ __forceinline__ void record_error(int* err, int code) {
 // Bounded wait for the phase of `parity` to complete. Returns false when the
 // limit ran out (recording a timeout and raising the CTA's abort flag) or
 // when another role already aborted.
+// Bounded wait that ignores the abort flag: after an abort it lets the copies
+// and MMAs already issued complete before shared memory or TMEM is released.
+__device__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns = kDrainLimitNs) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (global_ns() - t0 > limit_ns) return false;
+    return true;
+}
+
 __device__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* dev_err,
                           uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;

@@ -91,6 +91,7 @@ SIGNATURES = {
     "estream_residency_trace": (_I, [_P, _P, _I, ctypes.POINTER(_I)]),
     "estream_inject_pager_fault": (_I, [_P, _I, _I]),
     "estream_inject_route_timeout": (_I, [_P]),
+    "estream_inject_expert_timeout": (_I, [_P]),
     "estream_pipeline_trace": (_I, [_P, _P, _I, ctypes.POINTER(_I), ctypes.POINTER(ctypes.c_double)]),
     "estream_maxplus_pipeline": (ctypes.c_double, [_P, _P, _I, _I, _I, ctypes.c_double, _P]),
     "estream_bank_bound": (_I, [_I, ctypes.c_double, ctypes.c_double, ctypes.c_double, _I]),
@@ -398,6 +399,10 @@ def autoconfig(profiles: dict, T_ne: float, Q0: int, M_max: float, W_e: float, N
                                     N_e, ctypes.byref(G), ctypes.byref(B), ctypes.byref(T)),
            "estream_autoconfig")
     return G.value, B.value, T.value
+
+
+def inject_expert_timeout(ctx) -> None:
+    _check(lib().estream_inject_expert_timeout(ctx), "estream_inject_expert_timeout")
 
 
 def inject_route_timeout(ctx) -> None:

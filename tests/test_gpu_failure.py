@@ -49,3 +49,39 @@ def test_route_barrier_timeout_is_reported(mode, deterministic):
             assert float((Y2 - Y_ref).abs().max()) <= 1e-5 * scale
     finally:
         st.close()
+
+
+@pytest.mark.parametrize("form", ["single", "pair", "q4"])
+def test_expert_kernel_timeout_is_reported(form):
+    """The expert kernels' bounded waits: a call that runs the down tiles
+    without their gate/up tiles (a test hook) waits 2 s for m-block counters
+    that never fill; every CTA stops, drains and frees its tensor memory, the
+    timeout is reported, and the next call is normal."""
+    from routed_expert_ffn_topk_gb300 import estream as es
+    from routed_expert_ffn_topk_gb300.layer import BoundLayerStack
+    wl = small_workload("c2")
+    dev = _gpu.device()
+    kw = {"ffn_form": es.FFN_PAIR} if form == "pair" else (
+        {"wdtype": es.Q4} if form == "q4" else {"ffn_form": es.FFN_SINGLE})
+    st = BoundLayerStack(wl, mode="resident", deterministic=True, **kw)
+    try:
+        X = wl.X.to(dev)
+        lg = wl.logits[0].to(dev)
+        Y_ref = torch.full((X.shape[0], wl.cfg.H), float("nan"), device=dev)
+        st.prefill(0, X, lg, Y_ref, residual=X)
+        torch.cuda.synchronize()
+        assert es.get_device_error(st.ctx) == es.OK
+
+        es.inject_expert_timeout(st.ctx)
+        Y = torch.full_like(Y_ref, float("nan"))
+        st.prefill(0, X, lg, Y, residual=X)
+        torch.cuda.synchronize()
+        assert es.get_device_error(st.ctx) == es.ERR_TIMEOUT
+
+        Y2 = torch.full_like(Y_ref, float("nan"))
+        st.prefill(0, X, lg, Y2, residual=X)
+        torch.cuda.synchronize()
+        assert es.get_device_error(st.ctx) == es.OK
+        assert torch.equal(Y2.view(torch.int32), Y_ref.view(torch.int32))
+    finally:
+        st.close()
