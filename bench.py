@@ -32,7 +32,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # capture summarised in profiles/k_expert_ffn_olmoe_resident.md. Reported only while
 # the kernel source is the one that was captured.
 PROFILED_TRAFFIC = {
-    "c2": {"kernel_sha256_16": "017969067097c2fd", "bytes": 860039168},
+    "c2": {"kernel_sha256_16": "60876e9d8542c32e", "bytes": 859869696},
 }
 KERNEL_SRC = [os.path.join(ROOT, "routed_expert_ffn_topk_gb300", "csrc", f)
               for f in ("expert_gemm.cu", "tc_ptx.cuh")]
