@@ -191,8 +191,15 @@ __global__ void __launch_bounds__(kRThreads, 1)
             const int t = m0 + r, e = n0 + c;
             if (t >= a.T || e >= a.E) continue;
             const uint32_t off = sbase + static_cast<uint32_t>((r * (N + 1) + c) * 4);
-            float acc = ld_cluster_f32(off, 0);
-            for (int q = 1; q < a.S; ++q) acc += ld_cluster_f32(off, static_cast<uint32_t>(q));
+            // every partial's load in flight at once, then the sum in ascending chunk order
+            float v[kRMaxSplit];
+#pragma unroll
+            for (int q = 0; q < kRMaxSplit; ++q)
+                if (q < a.S) v[q] = ld_cluster_f32(off, static_cast<uint32_t>(q));
+            float acc = v[0];
+#pragma unroll
+            for (int q = 1; q < kRMaxSplit; ++q)
+                if (q < a.S) acc += v[q];
             a.logits[static_cast<size_t>(t) * a.E + e] = acc;
         }
     }
