@@ -330,6 +330,9 @@ __device__ void scatter_chunk(int c, int nchunk, const int32_t* __restrict__ top
             const int slot = phi ? phi[e] : e;
             b = (slot < 0 || slot >= P) ? P : slot;
         }
+        // the chunk's base inside the slot, loaded by every thread before the
+        // warps take their turns
+        const int cbase = valid ? __ldcg(base + static_cast<size_t>(b) * nchunk + c) : 0;
         const int key = valid ? b : -(lane + 1);  // invalid lanes match nobody
         const unsigned peers = __match_any_sync(0xffffffffu, key);
         const unsigned lt_mask = (1u << lane) - 1u;
@@ -342,7 +345,7 @@ __device__ void scatter_chunk(int c, int nchunk, const int32_t* __restrict__ top
                 const int before = valid ? cnt[b] : 0;
                 __syncwarp();
                 if (valid && lane == leader) cnt[b] = before + __popc(peers);
-                pos = slot_off[b] + __ldcg(base + static_cast<size_t>(b) * nchunk + c) + before + rank;
+                pos = slot_off[b] + cbase + before + rank;
             }
             __syncthreads();
         }
