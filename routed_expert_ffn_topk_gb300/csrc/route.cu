@@ -285,12 +285,22 @@ __device__ void scan_slots(int32_t* __restrict__ hist, int nchunk, int nb,
     const int gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int nw = gridDim.x * (blockDim.x >> 5);
     const int per = (nchunk + 31) / 32;
+    constexpr int kRegs = 16;  // a lane's counts kept in registers up to this many
     for (int b = gw; b < nb; b += nw) {
         int32_t* row = hist + static_cast<size_t>(b) * nchunk;
         const int lo = min(nchunk, lane * per);
         const int hi = min(nchunk, lo + per);
+        int vals[kRegs];
         int local = 0;
-        for (int c = lo; c < hi; ++c) local += __ldcg(row + c);
+        if (per <= kRegs) {
+            // every load in flight at once
+#pragma unroll
+            for (int j = 0; j < kRegs; ++j) vals[j] = lo + j < hi ? __ldcg(row + lo + j) : 0;
+#pragma unroll
+            for (int j = 0; j < kRegs; ++j) local += vals[j];
+        } else {
+            for (int c = lo; c < hi; ++c) local += __ldcg(row + c);
+        }
         int incl = local;
 #pragma unroll
         for (int d = 1; d < 32; d <<= 1) {
@@ -298,10 +308,19 @@ __device__ void scan_slots(int32_t* __restrict__ hist, int nchunk, int nb,
             if (lane >= d) incl += o;
         }
         int run = incl - local;
-        for (int c = lo; c < hi; ++c) {
-            const int v = __ldcg(row + c);
-            row[c] = run;
-            run += v;
+        if (per <= kRegs) {
+#pragma unroll
+            for (int j = 0; j < kRegs; ++j)
+                if (lo + j < hi) {
+                    row[lo + j] = run;
+                    run += vals[j];
+                }
+        } else {
+            for (int c = lo; c < hi; ++c) {
+                const int v = __ldcg(row + c);
+                row[c] = run;
+                run += v;
+            }
         }
         if (lane == 31) totals[b] = incl;
     }
