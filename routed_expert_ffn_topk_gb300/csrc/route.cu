@@ -449,10 +449,10 @@ __global__ void __launch_bounds__(kRouteThreads, 2) k_route_fused(
     // top-k, so that their copies do not queue ahead of the logits loads.
     const int grid = static_cast<int>(gridDim.x);
     const int nc = min(nchunk, grid);  // CTAs holding top-k chunks
-    const int b = static_cast<int>(blockIdx.x);
+    const int cta = static_cast<int>(blockIdx.x);
     const int n_workers = grid * kChunkTokens;
-    int rrow = resid.A ? (b >= nc ? b - nc : b + grid - nc) * kChunkTokens + warp : T;
-    bool pre = rrow < T && b >= nc;
+    int rrow = resid.A ? (cta >= nc ? cta - nc : cta + grid - nc) * kChunkTokens + warp : T;
+    bool pre = rrow < T && cta >= nc;
     int staged = pre ? stage_residual_row(rrow, resid, rstage) : 0;
     // 1. router + the chunk's slot counts, one warp per token
     for (int c = blockIdx.x; c < nchunk; c += gridDim.x) {
