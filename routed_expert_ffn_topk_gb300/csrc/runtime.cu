@@ -1157,6 +1157,7 @@ estream_status estream_moe_layer_prefill(estream_ctx* c, int layer, const void* 
 estream_status estream_moe_layer_prefill_residual(estream_ctx* c, int layer, const void* X,
                                                   const float* logits, int T, int k, int renorm,
                                                   const void* A, float* Y, void* cuda_stream) {
+    if (!c) return ESTREAM_ERR_NOT_BOUND;
     if (!A) return ESTREAM_ERR_INVALID_ARG;
     return prefill_impl(c, layer, X, logits, T, k, renorm, A, Y, cuda_stream);
 }

@@ -69,6 +69,11 @@ def test_layer_calls_need_context(es):
     assert L.estream_moe_layer_prefill(None, 0, None, None, 1, 1, 0, None, None) == es.ERR_NOT_BOUND
     assert L.estream_arena_preload(None, 0, None) == es.ERR_NOT_BOUND
     assert L.estream_get_device_error(None) == es.ERR_NOT_BOUND
+    assert L.estream_moe_layer_prefill_residual(None, 0, None, None, 1, 1, 0, None, None,
+                                                None) == es.ERR_NOT_BOUND
+    assert L.estream_inject_route_timeout(None) == es.ERR_NOT_BOUND
+    assert L.estream_inject_expert_timeout(None) == es.ERR_NOT_BOUND
+    assert L.estream_inject_pager_fault(None, 0, 0) == es.ERR_NOT_BOUND
     out = ctypes.c_void_p()
     assert L.estream_bind_arena(ctypes.byref(out), None) == es.ERR_INVALID_ARG
     L.estream_unbind(None)  # no-op
