@@ -16,7 +16,8 @@
 //      chunk's slot counts (shared-memory atomics; counts are order-free),
 //      written bucket-major as hist[slot][chunk]; with a residual A the
 //      rows Y[t] = A[t] are written in the same phase, by the warps of CTAs
-//      added for them first;
+//      added for them first (those CTAs then leave: the later phases and
+//      their grid barriers involve the chunks' CTAs only);
 //   2. every warp of the grid scans whole slots (a warp per slot): each
 //      chunk's base inside the slot, and the slot's total;
 //   3. every CTA forms the slot offsets and the m-block prefix (the expert
@@ -280,10 +281,10 @@ __device__ int block_exclusive_scan(int* data, int n, int* warp_sums) {
 // record inside slot b, and totals[b] the slot's count. Lane l handles a
 // contiguous run of chunks, so its loads are independent of one another.
 __device__ void scan_slots(int32_t* __restrict__ hist, int nchunk, int nb,
-                           int32_t* __restrict__ totals) {
+                           int32_t* __restrict__ totals, int n_part) {
     const int lane = threadIdx.x & 31;
     const int gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    const int nw = gridDim.x * (blockDim.x >> 5);
+    const int nw = n_part * (blockDim.x >> 5);
     const int per = (nchunk + 31) / 32;
     constexpr int kRegs = 16;  // a lane's counts kept in registers up to this many
     for (int b = gw; b < nb; b += nw) {
@@ -381,13 +382,15 @@ __device__ void scatter_chunk(int c, int nchunk, const int32_t* __restrict__ top
 // (after recording a timeout) if the other CTAs did not arrive within the limit.
 // withhold: this CTA does not arrive (a test of the bounded wait: the other
 // CTAs' wait runs out and records a timeout; so does this CTA's own).
-__device__ bool grid_barrier(int* counter, int generation, int* err, int* ok_flag,
+// Barrier of the first n_part CTAs of the grid (those that take part in the
+// route map).
+__device__ bool grid_barrier(int* counter, int generation, int n_part, int* err, int* ok_flag,
                              bool withhold = false) {
     __syncthreads();
     if (threadIdx.x == 0) {
         __threadfence();
         if (!withhold) atomicAdd(counter, 1);
-        const int target = generation * gridDim.x;
+        const int target = generation * n_part;
         uint64_t t0;
         asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
         int seen;
@@ -480,13 +483,15 @@ __global__ void __launch_bounds__(kRouteThreads, 2) k_route_fused(
         if (!pre) staged = stage_residual_row(rrow, resid, rstage);
         finish_residual_row(rrow, resid, rstage, staged);
     }
-    if (!grid_barrier(sync, 1, err, &ok_flag, withhold_arrival != 0 && blockIdx.x == 0)) {
+    // CTAs added for residual rows take no part in the route map
+    if (cta >= nc) return;
+    if (!grid_barrier(sync, 1, nc, err, &ok_flag, withhold_arrival != 0 && blockIdx.x == 0)) {
         empty_route_map(offsets, mblk, P);
         return;
     }
     // 2. per-slot scans over chunks, spread over every warp of the grid
-    scan_slots(hist, nchunk, nb, totals);
-    if (!grid_barrier(sync, 2, err, &ok_flag)) {
+    scan_slots(hist, nchunk, nb, totals, nc);
+    if (!grid_barrier(sync, 2, nc, err, &ok_flag)) {
         empty_route_map(offsets, mblk, P);
         return;
     }
@@ -517,7 +522,7 @@ __global__ void __launch_bounds__(kRouteThreads, 2) k_route_fused(
         }
     }
     if (done)
-        for (int m = blockIdx.x * blockDim.x + threadIdx.x; m < mb_total; m += gridDim.x * blockDim.x)
+        for (int m = blockIdx.x * blockDim.x + threadIdx.x; m < mb_total; m += nc * blockDim.x)
             done[m] = 0;
     __syncthreads();
     for (int c = blockIdx.x; c < nchunk; c += gridDim.x)
