@@ -18,14 +18,16 @@
 //      rows Y[t] = A[t] are written in the same phase, by the warps of CTAs
 //      added for them first (those CTAs then leave: the later phases and
 //      their grid barriers involve the chunks' CTAs only);
-//   2. every warp of the grid scans whole slots (a warp per slot): each
-//      chunk's base inside the slot, and the slot's total;
+//   2. every warp of the chunks' CTAs scans whole slots (a warp per slot):
+//      each chunk's base inside the slot, and the slot's total;
 //   3. every CTA forms the slot offsets and the m-block prefix (the expert
 //      kernel schedules by it) from the slot totals with block scans in its
 //      shared memory -- CTA 0 also stores them -- then, one CTA per chunk,
 //      places the chunk's records: ranks inside a warp by __match_any_sync,
 //      across warps in ascending order, so the placement is the stable one
 //      Algorithm 1 produces.
+// A grid barrier that gives up (1 s) records a timeout in the error word and
+// leaves an empty route map, so that kernels reading it find no records.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -489,7 +491,7 @@ __global__ void __launch_bounds__(kRouteThreads, 2) k_route_fused(
         empty_route_map(offsets, mblk, P);
         return;
     }
-    // 2. per-slot scans over chunks, spread over every warp of the grid
+    // 2. per-slot scans over chunks, spread over every warp of the chunks' CTAs
     scan_slots(hist, nchunk, nb, totals, nc);
     if (!grid_barrier(sync, 2, nc, err, &ok_flag)) {
         empty_route_map(offsets, mblk, P);
