@@ -167,8 +167,8 @@ class ClockSampler:
 # --------------------------------------------------------------------------
 
 def algorithmic(cfg, n_active_per_layer):
-    """Algorithmic bytes and FLOPs of one layer's routed fused expert kernel
-    at minimum: the weights of the experts with routes (gate, up, down:
+    """Algorithmic (minimum) bytes and FLOPs of one layer's routed fused
+    expert kernel: the weights of the experts with routes (gate, up, down:
     3*H*F*2 bytes each), X read once (T*H*2) and Y read and written
     (2*T*H*4). The fp16 h intermediate (2*R*F*2 bytes, L2-resident at these
     sizes) is implementation traffic and not counted. Returned as the old
