@@ -308,8 +308,30 @@ def arena_invalidate(ctx) -> None:
     _check(lib().estream_arena_invalidate(ctx), "estream_arena_invalidate")
 
 
+def _check_layer_args(X: torch.Tensor, logits: torch.Tensor, Y: torch.Tensor,
+                      A: torch.Tensor | None = None) -> None:
+    """Shapes and types the layer call reads and writes through plain
+    pointers: X [T, H] (bf16 or fp32), logits [T, E] fp32, Y [T, H] fp32 and
+    the residual A like X, all on one CUDA device."""
+    if X.dim() != 2 or logits.dim() != 2 or Y.dim() != 2:
+        raise ValueError("X, logits and Y must be 2-d")
+    T, H = X.shape
+    if logits.shape[0] != T or tuple(Y.shape) != (T, H):
+        raise ValueError(f"logits must be [T, E] and Y [T, H] with T={T}, H={H}")
+    if X.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("X must be bf16 or fp32")
+    if logits.dtype != torch.float32 or Y.dtype != torch.float32:
+        raise ValueError("logits and Y must be fp32")
+    if A is not None and (tuple(A.shape) != (T, H) or A.dtype != X.dtype):
+        raise ValueError("the residual must have X's shape and type")
+    tensors = [X, logits, Y] + ([A] if A is not None else [])
+    if any(not t.is_cuda for t in tensors) or len({t.device for t in tensors}) != 1:
+        raise ValueError("X, logits, Y (and the residual) must be on one CUDA device")
+
+
 def moe_layer_prefill(ctx, layer: int, X: torch.Tensor, logits: torch.Tensor, k: int,
                       renorm: bool, Y: torch.Tensor, stream=None) -> None:
+    _check_layer_args(X, logits, Y)
     T = X.shape[0]
     _check(lib().estream_moe_layer_prefill(ctx, layer, _dptr(X), _dptr(logits), T, k,
                                            int(bool(renorm)), _dptr(Y), _stream(stream)),
@@ -319,6 +341,7 @@ def moe_layer_prefill(ctx, layer: int, X: torch.Tensor, logits: torch.Tensor, k:
 def moe_layer_prefill_residual(ctx, layer: int, X: torch.Tensor, logits: torch.Tensor, k: int,
                                renorm: bool, A: torch.Tensor, Y: torch.Tensor, stream=None) -> None:
     """Y = A + the layer's MoE output (Y written, not read)."""
+    _check_layer_args(X, logits, Y, A)
     T = X.shape[0]
     _check(lib().estream_moe_layer_prefill_residual(ctx, layer, _dptr(X), _dptr(logits), T, k,
                                                     int(bool(renorm)), _dptr(A), _dptr(Y),

@@ -72,6 +72,11 @@ class BoundLayerStack:
                 k=None, renorm=None, stream=None, residual: torch.Tensor | None = None) -> None:
         """Y += MoE(X), or Y = residual + MoE(X) when `residual` is given."""
         cfg = self.cfg
+        if X.dim() != 2 or X.shape[1] != cfg.H or logits.dim() != 2 or logits.shape[1] != cfg.E:
+            raise ValueError(f"X must be [T, {cfg.H}] and logits [T, {cfg.E}]")
+        want = torch.float32 if self.dtype == es.F32 else torch.bfloat16
+        if X.dtype != want:
+            raise ValueError(f"X must be {want} for this arena")
         k = cfg.k if k is None else k
         renorm = cfg.renorm if renorm is None else renorm
         if residual is None:

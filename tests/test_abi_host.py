@@ -163,3 +163,30 @@ def test_pack_rejects_bad_perm(es):
     pool = torch.zeros(es.pool_bytes(E, H, F, es.BF16), dtype=torch.uint8)
     with pytest.raises(es.EStreamError):
         es.pack_experts(d, 0, z, z, zd, pool)
+
+
+def test_layer_call_argument_checks(es):
+    """The binding rejects tensors whose shapes or types do not fit the layer
+    call before any pointer reaches the library."""
+    import pytest
+    import torch
+    T, H, E = 8, 256, 4
+    X = torch.zeros(T, H, dtype=torch.bfloat16)
+    lg = torch.zeros(T, E, dtype=torch.float32)
+    Y = torch.zeros(T, H, dtype=torch.float32)
+    bad = [
+        (X, lg, torch.zeros(T, H + 1), None),               # Y shape
+        (X, torch.zeros(T + 1, E), Y, None),                # logits rows
+        (X, lg.double(), Y, None),                          # logits type
+        (X, lg, Y.half(), None),                            # Y type
+        (X.int(), lg, Y, None),                             # X type
+        (X, lg, Y, torch.zeros(T, H, dtype=torch.float32)), # residual type
+        (X, lg, Y, torch.zeros(T, H - 1, dtype=torch.bfloat16)),
+        (X, lg, Y, None),                                   # not on a CUDA device
+    ]
+    for x, l, y, a in bad:
+        with pytest.raises(ValueError):
+            if a is None:
+                es.moe_layer_prefill(None, 0, x, l, 2, False, y)
+            else:
+                es.moe_layer_prefill_residual(None, 0, x, l, 2, False, a, y)
