@@ -155,6 +155,27 @@ def route_workspace_bytes(T: int, E: int, k: int, P: int) -> int:
     return lib().estream_route_workspace_bytes(T, E, k, P)
 
 
+def _need(t: torch.Tensor, numel: int, dtype, name: str, device) -> None:
+    """A buffer the library writes or reads through a plain pointer."""
+    if t.dtype != dtype or t.numel() < numel or t.device != device:
+        raise ValueError(f"{name} must be {dtype} with at least {numel} elements on {device}")
+
+
+def _check_route_args(logits: torch.Tensor, k: int, phi, P: int, o: dict) -> None:
+    if logits.dim() != 2 or logits.dtype != torch.float32 or not logits.is_cuda:
+        raise ValueError("logits must be a [T, E] fp32 CUDA tensor")
+    T, E = logits.shape
+    R = T * k
+    dev = logits.device
+    if phi is not None:
+        _need(phi, E, torch.int32, "phi", dev)
+    _need(o["topk_ids"], R, torch.int32, "topk_ids", dev)
+    _need(o["alpha"], R, torch.float32, "alpha", dev)
+    _need(o["offsets"], P + 2, torch.int32, "offsets", dev)
+    _need(o["rec_tok"], R, torch.int32, "rec_tok", dev)
+    _need(o["rec_route"], R, torch.int32, "rec_route", dev)
+
+
 def route_build(logits: torch.Tensor, k: int, renorm: bool, phi: torch.Tensor | None = None,
                 P: int | None = None, out: dict | None = None, workspace: torch.Tensor | None = None,
                 stream=None) -> dict:
@@ -170,6 +191,7 @@ def route_build(logits: torch.Tensor, k: int, renorm: bool, phi: torch.Tensor | 
     o.setdefault("offsets", torch.empty(P + 2, dtype=torch.int32, device=dev))
     o.setdefault("rec_tok", torch.empty(max(R, 1), dtype=torch.int32, device=dev))
     o.setdefault("rec_route", torch.empty(max(R, 1), dtype=torch.int32, device=dev))
+    _check_route_args(logits, k, phi, P, o)
     nbytes = route_workspace_bytes(T, E, k, P)
     if workspace is None:
         workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
@@ -189,6 +211,11 @@ def router_workspace_bytes(T: int, H: int, E: int) -> int:
 def router_logits(X: torch.Tensor, W_r: torch.Tensor, logits: torch.Tensor | None = None,
                   workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """estream_router_logits: logits [T, E] fp32 = X [T, H] bf16 @ W_r [E, H] bf16 ^T."""
+    if (X.dim() != 2 or W_r.dim() != 2 or X.dtype != torch.bfloat16 or W_r.dtype != torch.bfloat16
+            or W_r.shape[1] != X.shape[1]):
+        raise ValueError("X must be [T, H] and W_r [E, H], both bf16")
+    if not X.is_cuda or W_r.device != X.device:
+        raise ValueError("X and W_r must be on one CUDA device")
     T, H = X.shape
     E = W_r.shape[0]
     if logits is None:
@@ -196,6 +223,8 @@ def router_logits(X: torch.Tensor, W_r: torch.Tensor, logits: torch.Tensor | Non
     if workspace is None:
         workspace = torch.empty(max(router_workspace_bytes(T, H, E), 256), dtype=torch.uint8,
                                 device=X.device)
+    if tuple(logits.shape) != (T, E) or logits.dtype != torch.float32 or logits.device != X.device:
+        raise ValueError(f"logits must be [{T}, {E}] fp32 on X's device")
     st = lib().estream_router_logits(_dptr(X), T, H, _dptr(W_r), E, _dptr(logits), _dptr(workspace),
                                      workspace.numel() * workspace.element_size(), _stream(stream))
     _check(st, "estream_router_logits")
@@ -216,6 +245,7 @@ def route_build_noalloc(logits: torch.Tensor, k: int, renorm: bool, phi: torch.T
     o.setdefault("offsets", torch.empty(P + 2, dtype=torch.int32, device=dev))
     o.setdefault("rec_tok", torch.empty(max(R, 1), dtype=torch.int32, device=dev))
     o.setdefault("rec_route", torch.empty(max(R, 1), dtype=torch.int32, device=dev))
+    _check_route_args(logits, k, phi, P, o)
     st = lib().estream_route_build_noalloc(
         _dptr(logits), T, E, k, int(bool(renorm)), _dptr(phi), P, _dptr(o["topk_ids"]),
         _dptr(o["alpha"]), _dptr(o["offsets"]), _dptr(o["rec_tok"]), _dptr(o["rec_route"]),

@@ -190,3 +190,23 @@ def test_layer_call_argument_checks(es):
                 es.moe_layer_prefill(None, 0, x, l, 2, False, y)
             else:
                 es.moe_layer_prefill_residual(None, 0, x, l, 2, False, a, y)
+
+
+def test_route_and_router_argument_checks(es):
+    """The route build and router wrappers reject tensors that do not fit
+    before any pointer reaches the library."""
+    import pytest
+    import torch
+    with pytest.raises(ValueError):
+        es.route_build(torch.zeros(4, 8), 2, False)                       # not on a CUDA device
+    with pytest.raises(ValueError):
+        es.route_build(torch.zeros(4, 8, dtype=torch.float64), 2, False)  # not fp32
+    with pytest.raises(ValueError):
+        es.route_build_noalloc(torch.zeros(8), 2, False)                  # not 2-d
+    X = torch.zeros(4, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        es.router_logits(X, torch.zeros(8, 64, dtype=torch.bfloat16))     # H differs
+    with pytest.raises(ValueError):
+        es.router_logits(X, torch.zeros(8, 128))                          # W_r not bf16
+    with pytest.raises(ValueError):
+        es.router_logits(X, torch.zeros(8, 128, dtype=torch.bfloat16))    # not on a CUDA device
