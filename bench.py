@@ -1,15 +1,19 @@
 """Benchmark of one MoE layer's prefill on GB300 (tokens/s and grouped-GEMM
 TFLOP/s), with the CPU oracle timed beside it.
 
-python bench.py [--gpus N] [--steps K] [--warmup W] [--config c2] [--impl ours|reference]
+python bench.py [--gpus N] [--steps K] [--warmup W] [--config c5] [--configs c2,c3,c4,c5]
+                [--impl ours|reference]
 
-One step = one MoE-layer prefill call through the C ABI over T tokens of
-seeded synthetic input (every layer of the config: routing + route map,
-gate/up GEMM, down GEMM + scatter-add, shared experts and layer chaining
-where the config has them), experts resident in HBM. The arena-paged call of
-the same config is timed in its own loop and reported under "paged" (its
-bound is the host link). Under torchrun each rank runs its own replica on
-its own T tokens (weak scaling, no collective on the data path).
+One step = the MoE-layer prefill of one config through the C ABI over T
+tokens of seeded synthetic input (every layer of the config: routing + route
+map, gate/up GEMM with the row gather, SwiGLU, down GEMM + scatter-add,
+shared experts and layer chaining where the config has them), experts
+resident in HBM. The headline line is the Mixtral-shaped layer (T=4096,
+H=4096, F=14336: the largest config, tensor-core bound); every config of
+--configs is measured the same way under "configs" (resident, end to end,
+4-bit experts, router, and the arena-paged call, whose bound is the host
+link). Under torchrun each rank runs its own replica on its own T tokens
+(weak scaling, no collective on the data path).
 """
 from __future__ import annotations
 
@@ -25,11 +29,13 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
+from routed_expert_ffn_topk_gb300 import workloads as W  # noqa: E402  (seeded inputs only)
+
 METRIC = "MoE-layer prefill tokens/sec and grouped-GEMM TFLOP/s vs bf16 peak (1 GB300)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
-# DRAM bytes (read + write) of one fused expert-kernel launch, from the ncu
-# capture summarised in profiles/k_expert_ffn_olmoe_resident.md. Reported only while
+# DRAM bytes (read + write) of one fused expert-kernel launch on the
+# OLMoE-shaped layer, from an ncu capture of that kernel. Reported only while
 # the kernel source is the one that was captured.
 PROFILED_TRAFFIC = {
     "c2": {"kernel_sha256_16": "60876e9d8542c32e", "bytes": 859869696},
@@ -220,40 +226,92 @@ def oracle_tokens_per_s(cfg, wl, target_s=10.0, max_tokens=None):
 # GPU arm
 # --------------------------------------------------------------------------
 
-def run_ours(args, rank, world, local_rank):
+def roofline_of(cfg, stats, steps, n_active, peaks):
+    """Roofline of the routed fused expert kernel from the library's CUDA-event
+    times (launching stream): algorithmic bytes (active experts' weights + X
+    once + Y read and written) or FLOPs (6*H*F per route) per launch over the
+    average launch time. Tensor roof (sustained bf16) when the arithmetic
+    intensity is above the ridge, HBM roof below it."""
+    from routed_expert_ffn_topk_gb300 import estream as es
+    L = cfg.layers
+    ffn_b = ffn_f = 0.0
+    for l in range(L):
+        a, b, c, d = algorithmic(cfg, n_active[l])
+        ffn_b += a + b
+        ffn_f += c + d
+    n_ffn = max(1, stats["n_ffn"])
+    ffn_ms = stats["ms_ffn"] / n_ffn
+    launches_per_step = n_ffn / steps
+    per_launch_bytes = ffn_b / launches_per_step
+    per_launch_flops = ffn_f / launches_per_step
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    pair = cfg.T * cfg.k >= es.PAIR_MIN_ROWS * cfg.E   # the library's automatic form
+    kname = ("k_expert_ffn_pair (CTA pairs, 256-record tiles" if pair else
+             "k_expert_ffn (128-record tiles") + ": gather + gate/up + SwiGLU + down + scatter)"
+    if ffn_f / ffn_b < ridge:
+        achieved = per_launch_bytes / (ffn_ms / 1e3) / 1e9
+        roof = {"kernel": kname, "bound": "hbm", "achieved": round(achieved, 1),
+                "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None}
+    else:
+        # timed inside seconds of back-to-back steps: the sustained (power-capped)
+        # bf16 figure is the denominator; the burst one is kept beside it
+        sus = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+        achieved = per_launch_flops / (ffn_ms / 1e3) / 1e12
+        roof = {"kernel": kname, "bound": "tensor", "achieved": round(achieved, 1),
+                "peak": sus, "peak_kind": "sustained", "unit": "TFLOP/s",
+                "frac": round(achieved / sus, 4),
+                "frac_of_burst_peak": round(achieved / peaks["bf16_tflops"], 4), "traffic": None}
+    roof["peak_source"] = peaks["source"]
+    roof["traffic"] = profiled_traffic(cfg.key) if L == 1 else None
+    roof["algorithmic_bytes_per_launch"] = int(per_launch_bytes)
+    roof["algorithmic_flops_per_launch"] = int(per_launch_flops)
+    roof["arithmetic_intensity"] = round(ffn_f / ffn_b, 1)
+    roof["ms_per_launch"] = round(ffn_ms, 4)
+    kernels = {
+        "route_ms": round(stats["ms_route"] / steps, 4),
+        "ffn_ms": round(stats["ms_ffn"] / steps, 4),
+        "shared_ms": round(stats["ms_shared"] / steps, 4),
+        "ffn_GBps": round(ffn_b / (stats["ms_ffn"] / steps / 1e3) / 1e9, 1),
+        "ffn_TFLOPs": round(ffn_f / (stats["ms_ffn"] / steps / 1e3) / 1e12, 1),
+    }
+    return roof, kernels
+
+
+def measure_config(args, cfg, wl, dev, flush, peaks, world, rank):
+    """One config's resident step (every layer: routing + route map, the
+    fused expert kernel, shared experts and layer chaining where the config
+    has them), experts resident in HBM:
+      - device throughput: the step replayed from one CUDA graph, L2 flushed
+        before every step (outside the timed events), CUDA events on the
+        launching stream; per-kernel times from the library's own events on
+        an eager pass of the same steps;
+      - e2e: the same step as eager C-ABI calls with every step's inputs
+        copied from pinned host memory and Y read back to pinned host memory
+        inside the timed events, same L2 policy;
+      - e2e_pipelined_graph: requests pipelined over two buffer sets and two
+        copy streams around graph replays (a serving loop's form).
+    Then the router, the 4-bit experts and the arena-paged run of the config."""
     import torch
 
     from routed_expert_ffn_topk_gb300 import estream as es
-    from routed_expert_ffn_topk_gb300 import workloads as W
     from routed_expert_ffn_topk_gb300.layer import BoundLayerStack
 
-    dev = torch.device("cuda", local_rank)
-    torch.cuda.set_device(dev)
-    cfg = W.CONFIGS[args.config]
-    peaks = load_peaks()
-    wl = W.make_workload(cfg, seed=W.CONFIG_SEEDS[cfg.key] + 100 * rank)
     stream = torch.cuda.current_stream()
     L = cfg.layers
-
     X0 = wl.X.to(dev)
     logits = [lg.to(dev) for lg in wl.logits]
     Xbuf = [X0] + [torch.empty_like(X0) for _ in range(L - 1)]
     Y = [torch.empty(cfg.T, cfg.H, dtype=torch.float32, device=dev) for _ in range(L)]
-    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)  # > L2
-
-    mode = "resident"
+    one = cfg.__class__(**{**cfg.__dict__, "layers": 1})
     # one resident arena per layer (every expert of every layer in HBM)
-    stacks = [BoundLayerStack(W.Workload(cfg.__class__(**{**cfg.__dict__, "layers": 1}),
-                                         [wl.logits[l]], wl.X, [wl.layers[l]]), mode=mode)
+    stacks = [BoundLayerStack(W.Workload(one, [wl.logits[l]], wl.X, [wl.layers[l]]), mode="resident")
               for l in range(L)]
-
-    class _All:
-        ctx = None
 
     def make_step(X_in, lg_in, Y_out):
         """One step over the layer stack reading X_in / lg_in and leaving the
         last layer's Y in Y_out (the intermediate buffers are shared)."""
-        def run(_unused=None):
+        def run():
             for l in range(L):
                 X_l = X_in if l == 0 else Xbuf[l]
                 Y_l = Y_out if l == L - 1 else Y[l]
@@ -279,44 +337,33 @@ def run_ours(args, rank, world, local_rank):
                     out[k_] += v
         return out
 
-    stack = None
-
-    def timed_loop(st, steps, per_step_hook=None, graph=None):
-        times = []
+    def timed_loop(n, fn):
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(steps)]
-        for i in range(steps):
+              for _ in range(n)]
+        for i in range(n):
             flush.zero_()
-            if per_step_hook:
-                per_step_hook()
             ev[i][0].record(stream)
-            if graph is not None:
-                graph.replay()
-            else:
-                step(st)
+            fn()
             ev[i][1].record(stream)
         torch.cuda.synchronize()
-        for a, b in ev:
-            times.append(a.elapsed_time(b))
-        return times
+        return [a.elapsed_time(b) for a, b in ev]
 
     # ---- warm-up, then the timed region (clocks sampled throughout) ----
     for _ in range(args.warmup):
-        step(stack)
+        step()
     torch.cuda.synchronize()
     for_all(es.reset_stats)
     for_all(es.set_timing, True)
-    clocks = ClockSampler(local_rank, None)
+    clocks = ClockSampler(dev.index, None)
     graph, graph_note = None, "eager (--no-graph)"
     with clocks:
         t_end = time.time() + 0.6   # let the sampler see the GPU under this load
         while time.time() < t_end:
-            step(stack)
+            step()
         torch.cuda.synchronize()
         # per-kernel times from the library's own CUDA events (eager steps)
         for_all(es.reset_stats)
-        timed_loop(stack, args.steps)
-        torch.cuda.synchronize()
+        timed_loop(args.steps, step)
         stats = merged_stats()
         for_all(es.set_timing, False)
         assert all(e == es.OK for e in for_all(es.get_device_error))
@@ -330,168 +377,299 @@ def run_ours(args, rank, world, local_rank):
                 graph, graph_note = None, f"eager (graph capture failed: {type(ex).__name__})"
         barrier(world)
         torch.cuda.synchronize()
-        times = timed_loop(stack, args.steps, graph=graph)
-        torch.cuda.synchronize()
+        times = timed_loop(args.steps, graph.replay if graph is not None else step)
         barrier(world)
     assert all(e == es.OK for e in for_all(es.get_device_error))
-    total_ms = max_over_ranks(sum(times), world, dev)
-    ms_per_step = total_ms / args.steps
+    ms_per_step = max_over_ranks(sum(times), world, dev) / args.steps
     tokens = cfg.T * world
     value = tokens / (ms_per_step / 1e3)
     gpu_launches = stats["launches"] + (L - 1) * args.steps   # + the bf16 casts between layers
 
-    # ---- roofline of the fused expert kernel (CUDA events inside the library, same stream) ----
     n_active = active_experts(cfg, wl.logits)
-    ffn_b = ffn_f = 0.0
-    for l in range(L):
-        a, b, c, d = algorithmic(cfg, n_active[l])
-        ffn_b += a + b
-        ffn_f += c + d
-    n_ffn = max(1, stats["n_ffn"])
-    ffn_ms = stats["ms_ffn"] / n_ffn
-    launches_per_step = n_ffn / args.steps
-    per_launch_bytes = ffn_b / launches_per_step
-    per_launch_flops = ffn_f / launches_per_step
-    ai = ffn_f / ffn_b
-    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
-    # the form the library's automatic choice takes for this layer shape
-    pair = cfg.T * cfg.k >= es.PAIR_MIN_ROWS * cfg.E
-    kname = ("k_expert_ffn_pair (CTA pairs, 256-record tiles" if pair else
-             "k_expert_ffn (128-record tiles") + ": gather + gate/up + SwiGLU + down + scatter)"
-    if ai < ridge:
-        achieved = per_launch_bytes / (ffn_ms / 1e3) / 1e9
-        roof = {"kernel": kname, "bound": "hbm", "achieved": round(achieved, 1),
-                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                "traffic": None}
-    else:
-        # the kernel is timed inside a loop of back-to-back steps lasting seconds, so the
-        # denominator is the sustained (power-capped) bf16 figure; the burst one is kept beside it
-        sus = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
-        achieved = per_launch_flops / (ffn_ms / 1e3) / 1e12
-        roof = {"kernel": kname, "bound": "tensor", "achieved": round(achieved, 1),
-                "peak": sus, "peak_kind": "sustained", "unit": "TFLOP/s",
-                "frac": round(achieved / sus, 4),
-                "frac_of_burst_peak": round(achieved / peaks["bf16_tflops"], 4), "traffic": None}
-    roof["peak_source"] = peaks["source"]
-    roof["traffic"] = profiled_traffic(cfg.key) if L == 1 else None
-    roof["algorithmic_bytes_per_launch"] = int(per_launch_bytes)
-    roof["algorithmic_flops_per_launch"] = int(per_launch_flops)
-    roof["ms_per_launch"] = round(ffn_ms, 4)
+    roof, kernels = roofline_of(cfg, stats, args.steps, n_active, peaks)
     flops_step = cfg.flops_per_layer() * L
     gemm_ms = (stats["ms_ffn"] + stats["ms_shared"]) / args.steps
-    kernels = {
-        "route_ms": round(stats["ms_route"] / args.steps, 4),
-        "ffn_ms": round(stats["ms_ffn"] / args.steps, 4),
-        "shared_ms": round(stats["ms_shared"] / args.steps, 4),
-        "ffn_GBps": round(ffn_b / (stats["ms_ffn"] / args.steps / 1e3) / 1e9, 1),
-        "ffn_TFLOPs": round(ffn_f / (stats["ms_ffn"] / args.steps / 1e3) / 1e12, 1),
-    }
     tflops = flops_step / (ms_per_step / 1e3) / 1e12
     gemm_tflops = flops_step / (gemm_ms / 1e3) / 1e12
 
-    # ---- end to end through host buffers: requests pipelined ----
-    # Step i reads its inputs from pinned host memory and returns Y to pinned
-    # host memory. Two device buffer sets alternate: step i+1's host->device
-    # copies (one copy stream) overlap step i's compute, and step i's
-    # device->host copy (another copy stream) overlaps step i+1's compute.
-    # The timed region runs from the first input copy to the last output copy.
+    # ---- end to end through the C ABI with host buffers, eager calls ----
     Xh = wl.X.pin_memory()
     lgh = [lg.pin_memory() for lg in wl.logits]
-    Yh = [torch.empty(cfg.T, cfg.H, dtype=torch.float32).pin_memory() for _ in range(2)]
-    sets = [(Xbuf[0], logits, Y[L - 1])] + [(torch.empty_like(Xbuf[0]), [torch.empty_like(t) for t in logits],
-                                            torch.empty_like(Y[L - 1]))]
-    steps_b = [make_step(*sets[b]) for b in range(2)]
-    graphs_b = [graph, None]
-    if graph is not None:
-        try:
-            graphs_b[1] = capture_graph(steps_b[1])
-        except Exception:  # capture refused: both sets run eagerly
-            graphs_b = [None, None]
-    weights_bytes = cfg.expert_bytes() * cfg.E * L
-    flush_e2e = weights_bytes < 256 * 1024 * 1024   # the step's working set alone exceeds L2 otherwise
-    h2d_s, d2h_s = torch.cuda.Stream(), torch.cuda.Stream()
-    ev = {k_: [torch.cuda.Event() for _ in range(2)] for k_ in ("h2d", "comp", "d2h")}
-
-    def e2e_run(n):
-        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        t0.record(h2d_s)
-        for i in range(n):
-            b = i % 2
-            Xd, lgd, Yd = sets[b]
-            with torch.cuda.stream(h2d_s):
-                if i >= 2:
-                    h2d_s.wait_event(ev["comp"][b])     # step i-2 has read this set
-                Xd.copy_(Xh, non_blocking=True)
-                for l in range(L):
-                    lgd[l].copy_(lgh[l], non_blocking=True)
-                ev["h2d"][b].record(h2d_s)
-            stream.wait_event(ev["h2d"][b])
-            if i >= 2:
-                stream.wait_event(ev["d2h"][b])         # step i-2's Y has left the device
-            if flush_e2e:
-                flush.zero_()
-            if graphs_b[b] is not None:
-                graphs_b[b].replay()
-            else:
-                steps_b[b]()
-            ev["comp"][b].record(stream)
-            with torch.cuda.stream(d2h_s):
-                d2h_s.wait_event(ev["comp"][b])
-                Yh[b].copy_(Yd, non_blocking=True)
-                ev["d2h"][b].record(d2h_s)
-        t1.record(d2h_s)
-        torch.cuda.synchronize()
-        return t0.elapsed_time(t1)
-
-    e2e_run(4)
-    barrier(world)
-    e2e_ms = max_over_ranks(e2e_run(args.steps), world, dev) / args.steps
-    assert all(e == es.OK for e in for_all(es.get_device_error))
+    Yh = torch.empty(cfg.T, cfg.H, dtype=torch.float32).pin_memory()
     h2d_b = Xh.numel() * Xh.element_size() + sum(t.numel() * 4 for t in lgh)
-    d2h_b = Yh[0].numel() * 4
+    d2h_b = Yh.numel() * 4
+
+    def api_step():
+        Xbuf[0].copy_(Xh, non_blocking=True)
+        for l in range(L):
+            logits[l].copy_(lgh[l], non_blocking=True)
+        step()
+        Yh.copy_(Y[L - 1], non_blocking=True)
+
+    for _ in range(2):
+        api_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = max_over_ranks(sum(timed_loop(args.steps, api_step)), world, dev) / args.steps
+    assert all(e == es.OK for e in for_all(es.get_device_error))
+    e2e = {"value": round(tokens / (e2e_ms / 1e3), 1), "unit": "tokens/s",
+           "h2d_bytes_per_step": h2d_b, "d2h_bytes_per_step": d2h_b,
+           "mode": "eager C-ABI calls (estream_moe_layer_prefill_residual per layer) each step, "
+                   "inputs copied from pinned host memory and Y read back to pinned host memory "
+                   "inside the timed events on the compute stream",
+           "l2": "flushed before every step (outside the timed events), as for value"}
+
+    # ---- requests pipelined around graph replays (two buffer sets, two copy streams) ----
+    e2e_pipe = None
+    if graph is not None:
+        Yh2 = [Yh, torch.empty_like(Yh).pin_memory()]
+        sets = [(Xbuf[0], logits, Y[L - 1]),
+                (torch.empty_like(Xbuf[0]), [torch.empty_like(t) for t in logits],
+                 torch.empty_like(Y[L - 1]))]
+        try:
+            graphs_b = [graph, capture_graph(make_step(*sets[1]))]
+        except Exception:
+            graphs_b = None
+        if graphs_b is not None:
+            h2d_s, d2h_s = torch.cuda.Stream(), torch.cuda.Stream()
+            ev = {k_: [torch.cuda.Event() for _ in range(2)] for k_ in ("h2d", "comp", "d2h")}
+
+            def pipe_run(n):
+                t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                t0.record(h2d_s)
+                for i in range(n):
+                    b = i % 2
+                    Xd, lgd, Yd = sets[b]
+                    with torch.cuda.stream(h2d_s):
+                        if i >= 2:
+                            h2d_s.wait_event(ev["comp"][b])     # step i-2 has read this set
+                        Xd.copy_(Xh, non_blocking=True)
+                        for l in range(L):
+                            lgd[l].copy_(lgh[l], non_blocking=True)
+                        ev["h2d"][b].record(h2d_s)
+                    stream.wait_event(ev["h2d"][b])
+                    if i >= 2:
+                        stream.wait_event(ev["d2h"][b])         # step i-2's Y has left the device
+                    graphs_b[b].replay()
+                    ev["comp"][b].record(stream)
+                    with torch.cuda.stream(d2h_s):
+                        d2h_s.wait_event(ev["comp"][b])
+                        Yh2[b].copy_(Yd, non_blocking=True)
+                        ev["d2h"][b].record(d2h_s)
+                t1.record(d2h_s)
+                torch.cuda.synchronize()
+                return t0.elapsed_time(t1)
+
+            pipe_run(4)
+            barrier(world)
+            pipe_ms = max_over_ranks(pipe_run(args.steps), world, dev) / args.steps
+            assert all(e == es.OK for e in for_all(es.get_device_error))
+            e2e_pipe = {"value": round(tokens / (pipe_ms / 1e3), 1), "unit": "tokens/s",
+                        "h2d_bytes_per_step": h2d_b, "d2h_bytes_per_step": d2h_b,
+                        "mode": "requests pipelined: two device buffer sets, inputs copied on one "
+                                "copy stream and Y returned on another while the neighbouring "
+                                "steps' graph replays compute",
+                        "l2": "not flushed"}
+            graphs_b = None
     torch.cuda.synchronize()
     # the graphs reference the contexts' events: release them before the contexts go
     graph = None
-    graphs_b = None
     for st in stacks:
         st.close()
 
+    rec = {
+        "workload": workload_config(cfg, world)["workload"],
+        "tokens_per_s": round(value, 1), "ms_per_step": round(ms_per_step, 5),
+        "step": graph_note, "tflops": round(tflops, 1),
+        "grouped_gemm_tflops": round(gemm_tflops, 1),
+        "frac_bf16_peak": round(gemm_tflops / peaks["bf16_tflops"], 4),
+        "roofline": roof, "kernels": kernels, "e2e": e2e, "e2e_pipelined_graph": e2e_pipe,
+        "gpu_launches": gpu_launches, "clocks": clocks.summary(),
+    }
+
     # ---- router logits upstream of the top-k (its own kernel, not part of the step) ----
-    router = measure_router(cfg, X0, dev, stream, flush, peaks, args.steps) if cfg.dtype == "bf16" else None
-
+    if cfg.dtype == "bf16" and not args.no_router:
+        rec["router"] = measure_router(cfg, X0, dev, stream, flush, peaks, args.steps)
     # ---- the same layer with 4-bit experts ----
-    q4 = measure_q4(args, cfg, wl, dev, stream, flush, peaks) if cfg.dtype == "bf16" and not args.no_q4 else None
-
+    if cfg.dtype == "bf16" and not args.no_q4:
+        rec["q4"] = measure_q4(args, cfg, wl, dev, stream, flush, peaks)
     # ---- arena-paged run of the same config (host-link bound) ----
-    paged = measure_paged(args, cfg, wl, dev, stream, flush, peaks) if not args.no_paged else None
-    if paged is not None and args.pipeline_study and cfg.layers == 1:
-        paged["pipeline_study"] = pipeline_study(cfg, wl, dev, flush)
-    if paged is not None and args.pipeline_study and cfg.layers > 1:
-        paged["layer_granular_study"] = layer_granular_study(cfg, wl, dev, flush)
+    if not args.no_paged:
+        paged = measure_paged(args, cfg, wl, dev, stream, flush, peaks)
+        if args.pipeline_study and cfg.layers == 1:
+            paged["pipeline_study"] = pipeline_study(cfg, wl, dev, flush)
+        if args.pipeline_study and cfg.layers > 1:
+            paged["layer_granular_study"] = layer_granular_study(cfg, wl, dev, flush)
+        rec["paged"] = paged
+    del X0, logits, Xbuf, Y
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return rec
 
+
+def run_ours(args, rank, world, local_rank):
+    """The headline config's line, with every config of the set measured the
+    same way under "configs"."""
+    import torch
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    peaks = load_peaks()
+    # host threads (and so the pinned pools and staging buffers they allocate)
+    # on the CPU NUMA node attached to this GPU, when the host has several
+    host = bind_to_gpu_numa_node(dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)  # > L2
+    keys = [args.config] if args.no_configs else \
+        [k for k in args.configs.split(",") if k != args.config] + [args.config]
+    recs = {}
+    cpu_baseline = None
+    for key in keys:
+        cfg = W.CONFIGS[key]
+        wl = W.make_workload(cfg, seed=W.CONFIG_SEEDS[cfg.key] + 100 * rank)
+        recs[key] = measure_config(args, cfg, wl, dev, flush, peaks, world, rank)
+        if key == args.config and rank == 0 and not args.no_cpu_baseline:
+            # the oracle as it stands, on the host's cores, on a bounded sample
+            if host.get("restore") is not None:
+                os.sched_setaffinity(0, host["restore"])
+            tps, n, dt, cores = oracle_tokens_per_s(cfg, wl, target_s=10.0)
+            cpu_baseline = {"value": round(tps, 3), "unit": "tokens/s", "cores": cores,
+                            "kind": "oracle",
+                            "sample": f"routing of all {cfg.T} tokens + Eq.2 for {n} sampled "
+                                      f"tokens of layer 0 ({dt:.1f} s)"}
+        del wl
+    head = recs[args.config]
+    cfg = W.CONFIGS[args.config]
     line = {
-        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "metric": METRIC, "value": head["tokens_per_s"], "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16 gate/up, fp16 down (fp32 accumulate)" if cfg.dtype == "bf16" else "f32",
         "data": "synthetic (seeded; random-init weights)",
-        "config": {**workload_config(cfg, world, mode), "step": graph_note},
-        "tflops": round(tflops, 1), "grouped_gemm_tflops": round(gemm_tflops, 1),
-        "frac_bf16_peak": round(gemm_tflops / peaks["bf16_tflops"], 4),
-        "roofline": roof, "kernels": kernels,
-        "e2e": {"value": round(tokens / (e2e_ms / 1e3), 1), "unit": "tokens/s",
-                "h2d_bytes_per_step": h2d_b, "d2h_bytes_per_step": d2h_b,
-                "mode": "requests pipelined: inputs copied from pinned host memory and Y returned to it "
-                        "every step, on two copy streams overlapping the neighbouring steps' compute",
-                "l2": "flushed before every step" if flush_e2e else
-                      "not flushed: the step's expert weights alone exceed L2"},
-        "gpu_launches": gpu_launches,
-        "clocks": clocks.summary(),
-        "router": router,
-        "q4": q4,
-        "paged": paged,
+        "config": {**workload_config(cfg, world), "step": head["step"]},
+        "tflops": head["tflops"], "grouped_gemm_tflops": head["grouped_gemm_tflops"],
+        "frac_bf16_peak": head["frac_bf16_peak"],
+        "roofline": head["roofline"], "kernels": head["kernels"],
+        "e2e": head["e2e"], "e2e_pipelined_graph": head["e2e_pipelined_graph"],
+        "gpu_launches": head["gpu_launches"], "clocks": head["clocks"],
+        "router": head.get("router"), "q4": head.get("q4"), "paged": head.get("paged"),
+        "h2d_link": h2d_link_by_numa_node(dev) if not args.no_paged else None,
+        "host_numa": {k: v for k, v in host.items() if k != "restore"},
     }
+    if cpu_baseline is not None:
+        line["cpu_baseline"] = cpu_baseline
+    if not args.no_configs:
+        line["configs"] = {k: recs[k] for k in sorted(recs)}
     return line
+
+
+def _numa_cpus():
+    """CPU NUMA nodes of this host: {node: set of CPUs} (nodes without CPUs,
+    such as a GPU's own memory exposed as a node, are left out)."""
+    import glob
+    out = {}
+    for d in sorted(glob.glob("/sys/devices/system/node/node[0-9]*")):
+        try:
+            with open(os.path.join(d, "cpulist")) as f:
+                spec = f.read().strip()
+        except OSError:
+            continue
+        cpus = set()
+        for part in filter(None, spec.split(",")):
+            a, _, b = part.partition("-")
+            cpus.update(range(int(a), int(b or a) + 1))
+        if cpus:
+            out[int(os.path.basename(d)[4:])] = cpus
+    return out
+
+
+def _gpu_numa_node(index: int):
+    """The CPU NUMA node nvidia-smi reports as the GPU's affinity, or None."""
+    try:
+        r = subprocess.run(["nvidia-smi", "topo", "-m"], capture_output=True, text=True, timeout=20)
+    except Exception:
+        return None
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    if not lines:
+        return None
+    head = lines[0].split("\t")
+    col = next((i for i, h in enumerate(head) if "NUMA Affinity" in h), None)
+    for ln in lines[1:]:
+        cells = ln.split("\t")
+        if cells and cells[0].strip() == f"GPU{index}" and col is not None and col < len(cells):
+            try:
+                return int(cells[col].strip().split(",")[0].split("-")[0])
+            except ValueError:
+                return None
+    return None
+
+
+def bind_to_gpu_numa_node(dev):
+    """Restrict this thread (and the threads it starts later) to the CPUs of
+    the NUMA node nvidia-smi names as the GPU's affinity, so that pinned host
+    buffers are placed there. Returns what was done, and the previous CPU set
+    under "restore"."""
+    nodes = _numa_cpus()
+    node = _gpu_numa_node(dev.index)
+    info = {"cpu_numa_nodes": sorted(nodes), "gpu_numa_node": node, "bound": False, "restore": None}
+    if node in nodes and len(nodes) > 1 and hasattr(os, "sched_setaffinity"):
+        info["restore"] = os.sched_getaffinity(0)
+        os.sched_setaffinity(0, nodes[node])
+        info["bound"] = True
+    return info
+
+
+def h2d_link_by_numa_node(dev, nbytes=1 << 30, reps=8):
+    """Host-to-device copy bandwidth of a 1 GiB pinned buffer allocated while
+    this thread runs on each CPU NUMA node in turn (pages are placed on the
+    allocating thread's node), best of `reps` cudaMemcpyAsync calls timed with
+    CUDA events: shows whether the pinned pools sit on the node attached to
+    the GPU and what the link gives from there."""
+    import ctypes
+
+    import torch
+
+    from routed_expert_ffn_topk_gb300 import estream as es
+    es.lib()                                     # loads the CUDA runtime it links
+    rt = ctypes.CDLL("libcudart.so.13")
+    rt.cudaHostAlloc.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_size_t, ctypes.c_uint]
+    rt.cudaFreeHost.argtypes = [ctypes.c_void_p]
+    rt.cudaMemcpyAsync.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int,
+                                   ctypes.c_void_p]
+    nodes = _numa_cpus()
+    gpu_node = _gpu_numa_node(dev.index)
+    out = {"gpu_numa_node": gpu_node, "cpu_numa_nodes": sorted(nodes), "by_node": {}}
+    if not hasattr(os, "sched_setaffinity") or not nodes:
+        return out
+    stream = torch.cuda.current_stream(dev)
+    dst = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    orig = os.sched_getaffinity(0)
+    try:
+        for n, cpus in sorted(nodes.items()):
+            os.sched_setaffinity(0, cpus)
+            p = ctypes.c_void_p()
+            if rt.cudaHostAlloc(ctypes.byref(p), nbytes, 0) != 0 or not p.value:
+                continue
+            try:
+                ctypes.memset(p, 1, nbytes)
+                best = None
+                for _ in range(reps):
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    rc = rt.cudaMemcpyAsync(dst.data_ptr(), p, nbytes, 1, stream.cuda_stream)
+                    b.record(stream)
+                    b.synchronize()
+                    if rc != 0:
+                        break
+                    ms = a.elapsed_time(b)
+                    best = ms if best is None else min(best, ms)
+            finally:
+                torch.cuda.synchronize()
+                rt.cudaFreeHost(p)
+            if best:
+                out["by_node"][str(n)] = round(nbytes / (best / 1e3) / 1e9, 1)
+    finally:
+        os.sched_setaffinity(0, orig)
+    return out
 
 
 def capture_graph(fn):
@@ -599,11 +777,23 @@ def measure_q4(args, cfg, wl, dev, stream, flush, peaks):
             n_act = active_experts(cfg, [wl.logits[0]])[0]
             ffn_ms = stats["ms_ffn"] / max(1, stats["n_ffn"])
             nbytes = n_act * 3 * cfg.H * cfg.F * 9 // 16 + cfg.T * cfg.H * 2 + 2 * cfg.T * cfg.H * 4
+            flops = 6.0 * cfg.H * cfg.F * cfg.T * cfg.k
             gbs = nbytes / (ffn_ms / 1e3) / 1e9
+            tfs = flops / (ffn_ms / 1e3) / 1e12
+            # the 4-bit weights move 3.56x fewer bytes for the same FLOPs: the
+            # roof is the tensor one whenever the intensity is above the ridge
+            ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+            sus = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+            tensor = flops / nbytes >= ridge
             rec.update({"kernel": "k_expert_ffn_q4", "ffn_ms": round(ffn_ms, 4),
-                        "algorithmic_bytes_per_launch": int(nbytes), "GBps": round(gbs, 1),
+                        "algorithmic_bytes_per_launch": int(nbytes),
+                        "algorithmic_flops_per_launch": int(flops),
+                        "arithmetic_intensity": round(flops / nbytes, 1),
+                        "GBps": round(gbs, 1), "TFLOPs": round(tfs, 1),
                         "frac_hbm": round(gbs / peaks["hbm_gbs"], 4),
-                        "TFLOPs": round(6.0 * cfg.H * cfg.F * cfg.T * cfg.k / (ffn_ms / 1e3) / 1e12, 1)})
+                        "frac_tensor_sustained": round(tfs / sus, 4),
+                        "bound": "tensor" if tensor else "hbm",
+                        "frac": round(tfs / sus if tensor else gbs / peaks["hbm_gbs"], 4)})
         else:
             h2d = stats["h2d_bytes"] / len(ms)
             rec.update({"schedule": "prefetch before routing", "h2d_bytes_per_layer": int(h2d),
@@ -723,6 +913,10 @@ def measure_paged(args, cfg, wl, dev, stream, flush, peaks):
         "hidden_fraction": round((t_io + t_exec - t_paged) / t_io, 4) if t_io > 0 else None,
         "compute_hidden_fraction": round((t_io + t_exec - t_paged) / t_exec, 4) if t_exec > 0 else None,
         "bubble_rate": round(1 - max(t_io, t_exec) / t_paged, 4),
+        "library_stats_overlap": {"hidden_fraction": round(stats["hidden_fraction"], 4),
+                                  "bubble_rate": round(stats["bubble_rate"], 4),
+                                  "from": "estream_last_stats over the timed calls (copy-stream "
+                                          "busy time vs execution and call time)"},
         "groups_loaded_per_layer": stats["groups_loaded"] / len(times),
         "groups_skipped_per_layer": stats["groups_skipped"] / len(times),
         "max_plus_model": model,
@@ -896,13 +1090,18 @@ def run_reference(args, rank, world):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", default="c2", choices=["c1", "c2", "c3", "c4", "c5"])
+    ap.add_argument("--config", default="c5", choices=["c1", "c2", "c3", "c4", "c5"],
+                    help="the headline workload (default: the Mixtral-shaped layer)")
+    ap.add_argument("--configs", default="c2,c3,c4,c5",
+                    help="workloads measured the same way under \"configs\"")
+    ap.add_argument("--no-configs", action="store_true", help="measure the headline workload only")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--paged-steps", type=int, default=10)
     ap.add_argument("--no-paged", action="store_true")
     ap.add_argument("--no-q4", action="store_true", help="skip the 4-bit-expert measurement")
+    ap.add_argument("--no-router", action="store_true", help="skip the router-logits measurement")
     ap.add_argument("--no-graph", action="store_true", help="time eager launches, not a CUDA-graph replay")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--pipeline-study", action="store_true",
@@ -910,6 +1109,9 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    bad = [k for k in args.configs.split(",") if k not in W.CONFIGS]
+    if bad:
+        ap.error(f"unknown configs {bad}")
     rank, world, local_rank = dist_env()
     if world > 1:
         import torch
@@ -925,15 +1127,6 @@ def main(argv=None):
         print(json.dumps(line))
         return 0
     line = run_ours(args, rank, world, local_rank)
-    if rank == 0 and not args.no_cpu_baseline:
-        from routed_expert_ffn_topk_gb300 import workloads as W
-        cfg = W.CONFIGS[args.config]
-        wl = W.make_workload(cfg)
-        tps, n, dt, cores = oracle_tokens_per_s(cfg, wl, target_s=10.0)
-        line["cpu_baseline"] = {"value": round(tps, 3), "unit": "tokens/s", "cores": cores,
-                                "kind": "oracle",
-                                "sample": f"routing of all {cfg.T} tokens + Eq.2 for {n} sampled "
-                                          f"tokens ({dt:.1f} s)"}
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

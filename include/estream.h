@@ -160,14 +160,28 @@ estream_status estream_router_logits(const void* X, int T, int H, const void* W_
  *     on it and give wrong results;
  *   - the first call on a device looks the array's address up (with that
  *     device current); make it before any stream capture on the device;
- *   - a phi entry outside [-1, P) is filed under the trailing bucket as
- *     estream_route_build does, but is not reported.
+ *   - errors found by the kernel (a phi entry outside [-1, P), a grid
+ *     barrier that gave up) are kept in the array's error word, which
+ *     estream_route_noalloc_error reads;
+ *   - logits and the outputs must be memory of the current device
+ *     (ESTREAM_ERR_INVALID_ARG otherwise).
  */
 estream_status estream_route_build_noalloc(const float* logits, int T, int E, int k, int renorm,
                                            const int32_t* phi, int P,
                                            int32_t* topk_ids, float* alpha, int32_t* offsets,
                                            int32_t* rec_tok, int32_t* rec_route,
                                            void* cuda_stream);
+
+/* Synchronises `cuda_stream`, then returns and clears the error word that
+ * estream_route_build_noalloc calls on the current device recorded in the
+ * static scratch array: ESTREAM_OK if none, ESTREAM_ERR_DEVICE for a phi
+ * entry outside [-1, P) (that route was filed under the trailing bucket),
+ * ESTREAM_ERR_TIMEOUT when a grid barrier of the route build gave up after
+ * its 1 s bound (that call left an empty route map: offsets all zero).
+ * Every call of estream_route_build_noalloc clears the word when it starts,
+ * so it reports the latest call on the device: read it after the call whose
+ * result matters, before the next one. */
+estream_status estream_route_noalloc_error(void* cuda_stream);
 
 /* ---------------------------------------------------------------------- */
 /* Expert arena, pager and layer prefill                                   */
@@ -233,7 +247,9 @@ size_t estream_shared_bytes(int n_shared, int H, int F_shared, estream_dtype wdt
  * the library workspace (sized for T_max, k_max). Copies no weights.
  * Shapes: H % 256 == 0, F % 128 == 0, F_shared % 128 == 0, 1 <= G, 1 <= B,
  * 1 <= E <= 1024. On success *out is a context owned by the caller, to be
- * released with estream_unbind. The current CUDA device is the one used.
+ * released with estream_unbind. The current CUDA device is the one used;
+ * every later call on the context must be made with that device current
+ * (ESTREAM_ERR_INVALID_ARG otherwise).
  */
 estream_status estream_bind_arena(estream_ctx** out, const estream_arena_desc* d);
 
@@ -346,11 +362,33 @@ typedef struct {
     double h2d_bytes;        /* bytes copied into the arena */
     int groups_loaded, groups_skipped, groups_hit;
     double ms_io_busy;       /* copy-stream busy time (timing on) */
+    /* Overlap of loading and execution over the same calls (timing on), with
+     * T_io = ms_io_busy, T_exec = ms_route + ms_ffn + ms_shared + ms_combine
+     * and T_total = ms_total:
+     *   hidden_fraction = (T_io + T_exec - T_total) / T_io, clamped to [0, 1]:
+     *     the share of the copy time that ran under execution (0 when nothing
+     *     was copied);
+     *   bubble_rate = 1 - max(T_io, T_exec) / T_total, clamped to [0, 1]: the
+     *     paper's bubble rate (section 3.4, Fig. 6 caption). */
+    double hidden_fraction;
+    double bubble_rate;
 } estream_stats;
 
 estream_status estream_set_timing(estream_ctx* c, int on);
 estream_status estream_reset_stats(estream_ctx* c);
 estream_status estream_last_stats(estream_ctx* c, estream_stats* out);
+
+/* Test aid for the cross-CTA ordering of the fused kernels: enqueues on
+ * `cuda_stream` a fill of every per-call buffer of the context's workspace
+ * (top-k ids, alpha, route records and offsets, the route build's scratch,
+ * the h intermediates, the deterministic mode's row buffers) with all-ones
+ * bytes -- NaN for the floating-point buffers -- and of the m-block
+ * completion counters and tile tickets with 0x7f bytes (a count past every
+ * target). A layer call after it must give the same Y as without it: every
+ * buffer is written before it is read, and every counter is zeroed by the
+ * call before it is waited on. The bind-time tables (storage order, down
+ * scales) and the error word are left alone. Not for production use. */
+estream_status estream_poison_workspace(estream_ctx* c, void* cuda_stream);
 
 /* Synchronises the library's streams, returns and clears the device error
  * words (ESTREAM_OK, ESTREAM_ERR_TIMEOUT or ESTREAM_ERR_DEVICE): the

@@ -23,6 +23,7 @@ constexpr int kDevErrNone = 0;
 constexpr int kDevErrSlotRange = 1;  // a phi entry outside [-1, P)
 constexpr int kDevErrTimeout = 2;    // a bounded wait ran out
 constexpr int kDevErrRange = 3;      // an intermediate h value outside the fp16 range
+constexpr int kDevErrLaunch = 4;     // a cluster kernel launched without its cluster shape
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -47,7 +48,9 @@ struct ResidualInit {
     int H;
 };
 
-// Enqueue the full route build (K1). `ws` must hold route_workspace_layout(T,k,P).
+// Enqueue the full route build (K1). `ws` holds ws_bytes bytes, which must
+// cover route_workspace_layout(T,k,P) (cudaErrorInvalidValue otherwise, before
+// anything is enqueued: a second guard behind every entry point's own check).
 // rec_pos (optional, [T*k]) receives, for route i, its position in the CSR.
 // done (optional) is zeroed over the route map's m-blocks (mblk[P] ints) for
 // the fused expert kernel's m-block counters, and tickets[0..n_tickets) (the
@@ -56,7 +59,7 @@ cudaError_t launch_route_build(const float* logits, int T, int E, int k, int ren
                                const int32_t* phi, int P, int32_t* topk_ids, float* alpha,
                                int32_t* offsets, int32_t* rec_tok, int32_t* rec_route,
                                int32_t* rec_pos, int32_t* done, int32_t* tickets, int n_tickets,
-                               void* ws, cudaStream_t stream, int* n_launches,
+                               void* ws, size_t ws_bytes, cudaStream_t stream, int* n_launches,
                                const ResidualInit* resid = nullptr, int withhold_arrival = 0);
 
 // Identity route map for the shared experts: n_shared segments of T rows,

@@ -52,6 +52,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <mutex>
+
 #include "estream_internal.h"
 
 namespace es {
@@ -1321,6 +1323,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ int warp_total[kThreads / 32];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
+    // The cta_group::2 tensor-memory and MMA instructions, the peer-CTA
+    // addresses and the leader's barriers all assume a cluster of exactly two
+    // CTAs. A launch of any other shape (for example a tool relaunching the
+    // kernel without its cluster attribute) returns here, before any of them,
+    // with an error recorded, instead of executing pair instructions outside
+    // a pair. The test is uniform over the grid.
+    if (cluster_num_ctas() != 2) {
+        if (threadIdx.x == 0) record_error(a.dev_err, kDevErrLaunch);
+        return;
+    }
     const GemmSegments& seg = a.seg;
     const uint32_t rank = cluster_rank();
     const int pair = static_cast<int>(blockIdx.x >> 1);
@@ -1769,8 +1781,10 @@ cudaError_t launch_expert_ffn(const CUtensorMap* tm_wg, const CUtensorMap* tm_wu
 // Co-resident CTA pairs of k_expert_ffn_pair at its largest shared-memory
 // size (the bound for every smaller launch), per device.
 static int max_pairs(int device) {
+    static std::mutex mu;
     static int cache[64] = {0};
     if (device < 0 || device >= 64) return 0;
+    std::lock_guard<std::mutex> lock(mu);
     if (cache[device] > 0) return cache[device];
     const size_t smem = pair_smem_bytes(kMaxP);
     if (cudaFuncSetAttribute(k_expert_ffn_pair, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -31,6 +31,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "estream_internal.h"
 
@@ -550,6 +551,31 @@ __global__ void k_cast_f32_bf16(const float* __restrict__ src, __nv_bfloat16* __
         dst[x] = __float2bfloat16_rn(src[x]);
 }
 
+// CTAs of k_route_fused that fit on the current device at once, at its
+// largest shared-memory size (the bound for every smaller launch). Looked up
+// once per device, under a lock; the kernel's shared-memory attribute is set
+// on each device as it is first seen (a device's attributes are its own).
+static int route_co_resident() {
+    constexpr int kMaxDevices = 64;
+    static std::mutex mu;
+    static int cache[kMaxDevices] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[dev] > 0) return cache[dev];
+    int sms = 0, per_sm = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    const size_t max_smem = route_scratch_bytes(kMaxP + 1) + kResidStageCta;
+    if (cudaFuncSetAttribute(k_route_fused, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(max_smem)) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_route_fused, kRouteThreads,
+                                                      max_smem) != cudaSuccess ||
+        per_sm <= 0)
+        return 0;
+    cache[dev] = sms * per_sm;
+    return cache[dev];
+}
+
 RouteWorkspace route_workspace_layout(int T, int k, int P) {
     RouteWorkspace w;
     (void)k;
@@ -572,9 +598,10 @@ cudaError_t launch_route_build(const float* logits, int T, int E, int k, int ren
                                const int32_t* phi, int P, int32_t* topk_ids, float* alpha,
                                int32_t* offsets, int32_t* rec_tok, int32_t* rec_route,
                                int32_t* rec_pos, int32_t* done, int32_t* tickets, int n_tickets,
-                               void* ws, cudaStream_t stream, int* n_launches,
+                               void* ws, size_t ws_bytes, cudaStream_t stream, int* n_launches,
                                const ResidualInit* resid_in, int withhold_arrival) {
     const RouteWorkspace w = route_workspace_layout(T, k, P);
+    if (!ws || w.total > ws_bytes) return cudaErrorInvalidValue;
     char* base = static_cast<char*>(ws);
     int* err = reinterpret_cast<int*>(base + w.err_off);
     int32_t* hist = reinterpret_cast<int32_t*>(base + w.hist_off);
@@ -597,18 +624,8 @@ cudaError_t launch_route_build(const float* logits, int T, int E, int k, int ren
     int* sync = reinterpret_cast<int*>(base + w.sync_off);
     ResidualInit resid{nullptr, 0, nullptr, 0};
     if (resid_in) resid = *resid_in;
-    static int co_resident = 0;  // CTAs of k_route_fused that fit on the device at once
-    if (co_resident == 0) {
-        int dev = 0, sms = 0, per_sm = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        const size_t max_smem = route_scratch_bytes(kMaxP + 1) + kResidStageCta;
-        cudaFuncSetAttribute(k_route_fused, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(max_smem));
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_route_fused, kRouteThreads,
-                                                      max_smem);
-        co_resident = sms * (per_sm > 0 ? per_sm : 1);
-    }
+    const int co_resident = route_co_resident();
+    if (co_resident <= 0) return cudaErrorLaunchOutOfResources;
     // with a residual, up to as many CTAs again for its rows
     const int grid = std::max(1, std::min(co_resident, resid.A ? 2 * w.nchunk : w.nchunk));
     const size_t smem = route_scratch_bytes(nb) + (resid.A ? kResidStageCta : 0);

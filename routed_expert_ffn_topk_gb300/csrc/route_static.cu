@@ -24,7 +24,10 @@
 //     order them on one stream or serialise them;
 //   - the first call on a device looks up the array's device address
 //     (cudaGetSymbolAddress, with that device current); make that first call
-//     before any stream capture begins on the device.
+//     before any stream capture begins on the device;
+//   - errors the kernel finds (a phi entry outside [-1, P), a grid barrier
+//     that gave up) stay in the array's error word until
+//     estream_route_noalloc_error reads and clears it.
 #include <mutex>
 
 #include "estream_internal.h"
@@ -59,6 +62,23 @@ void* scratch_on_current_device() {
 
 using namespace es;
 
+namespace {
+
+// True when p is device memory of the current device (or managed memory),
+// the only memory the route kernel can be given.
+bool on_current_device(const void* p) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    return (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) && at.device == dev;
+}
+
+}  // namespace
+
 extern "C" estream_status estream_route_build_noalloc(const float* logits, int T, int E, int k,
                                                       int renorm, const int32_t* phi, int P,
                                                       int32_t* topk_ids, float* alpha,
@@ -72,10 +92,30 @@ extern "C" estream_status estream_route_build_noalloc(const float* logits, int T
         return ESTREAM_ERR_INVALID_ARG;
     if (static_cast<long long>(T) * k > (1ll << 30)) return ESTREAM_ERR_CAPACITY;
     if (route_workspace_layout(T, k, P).total > kStaticScratchBytes) return ESTREAM_ERR_CAPACITY;
+    if (!on_current_device(offsets) || (T > 0 && !on_current_device(logits)) ||
+        (phi && !on_current_device(phi)))
+        return ESTREAM_ERR_INVALID_ARG;
     void* ws = scratch_on_current_device();
     if (!ws) return ESTREAM_ERR_CUDA;
     cudaError_t rc = launch_route_build(logits, T, E, k, renorm, phi, P, topk_ids, alpha, offsets,
                                         rec_tok, rec_route, nullptr, nullptr, nullptr, 0, ws,
-                                        static_cast<cudaStream_t>(cuda_stream), nullptr);
+                                        kStaticScratchBytes, static_cast<cudaStream_t>(cuda_stream),
+                                        nullptr);
     return rc == cudaSuccess ? ESTREAM_OK : ESTREAM_ERR_CUDA;
+}
+
+// The error word sits at the start of the static array (the route build's
+// workspace layout puts it at offset 0).
+extern "C" estream_status estream_route_noalloc_error(void* cuda_stream) {
+    void* ws = scratch_on_current_device();
+    if (!ws) return ESTREAM_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    int word = 0;
+    int* err = reinterpret_cast<int*>(static_cast<char*>(ws) + route_workspace_layout(0, 1, 0).err_off);
+    if (cudaStreamSynchronize(s) != cudaSuccess ||
+        cudaMemcpy(&word, err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return ESTREAM_ERR_CUDA;
+    if (word == kDevErrNone) return ESTREAM_OK;
+    if (cudaMemset(err, 0, sizeof(int)) != cudaSuccess) return ESTREAM_ERR_CUDA;
+    return word == kDevErrTimeout ? ESTREAM_ERR_TIMEOUT : ESTREAM_ERR_DEVICE;
 }

@@ -76,6 +76,12 @@ __global__ void __launch_bounds__(kRThreads, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
 
+    // the fixed-order sum reads the partials of a.S CTAs of one cluster: a
+    // launch without that cluster shape returns before any cluster access
+    if (cluster_num_ctas() != static_cast<uint32_t>(a.S)) {
+        if (threadIdx.x == 0 && a.dev_err) atomicCAS(a.dev_err, kDevErrNone, kDevErrLaunch);
+        return;
+    }
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int m0 = blockIdx.x * 128;

@@ -77,6 +77,11 @@ struct estream_ctx {
     float* d_scale = nullptr;                  // [L*E] down-weight scales, storage order
     int32_t *done = nullptr, *sh_done = nullptr;  // per-m-block counters of the fused expert kernel
     int32_t* tickets = nullptr;  // [E+2] dynamic tile counters: [0] shared experts, [1+i] i-th routed launch
+    // per-call part of the workspace (everything after the bind-time tables),
+    // and the counter regions inside it (for estream_poison_workspace)
+    size_t ws_call_off = 0;
+    size_t route_ws_bytes = 0;   // the route build's part of the workspace
+    size_t n_done = 0, n_sh_done = 0, n_tickets = 0;
     int n_ffn_launch = 0;        // routed expert-kernel launches so far in the current layer call
     std::vector<const float*> shared_scale;    // [L] device pointers into shared buffers
     void *route_ws = nullptr, *h = nullptr, *h_shared = nullptr;
@@ -160,6 +165,18 @@ bool device_supported(int dev) {
 }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+
+// The context's device is the current one (its kernels, tensor maps and
+// workspace live there; a call made with another device current would launch
+// on that device with this device's pointers).
+static bool on_bound_device(const estream_ctx* c) {
+    int dev = -1;
+    return cudaGetDevice(&dev) == cudaSuccess && dev == c->device;
+}
+
+namespace {
 
 float bf16_bits_to_float(uint16_t b) {
     uint32_t u = static_cast<uint32_t>(b) << 16;
@@ -377,7 +394,7 @@ const char* estream_status_string(estream_status s) {
     return "unknown status";
 }
 
-int estream_version(void) { return 10000; }
+int estream_version(void) { return 10100; }
 
 size_t estream_route_workspace_bytes(int T, int E, int k, int P) {
     if (T < 0 || E < 1 || k < 1 || P < 0 || P > kMaxP) return 0;
@@ -399,8 +416,8 @@ estream_status estream_route_build(const float* logits, int T, int E, int k, int
     if (workspace_bytes < route_workspace_layout(T, k, P).total) return ESTREAM_ERR_CAPACITY;
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
     cudaError_t rc = launch_route_build(logits, T, E, k, renorm, phi, P, topk_ids, alpha, offsets,
-                                        rec_tok, rec_route, nullptr, nullptr, nullptr, 0, workspace, s,
-                                        nullptr);
+                                        rec_tok, rec_route, nullptr, nullptr, nullptr, 0, workspace,
+                                        workspace_bytes, s, nullptr);
     return rc == cudaSuccess ? ESTREAM_OK : ESTREAM_ERR_CUDA;
 }
 
@@ -613,10 +630,15 @@ estream_status estream_bind_arena(estream_ctx** out, const estream_arena_desc* d
         c->rec_pos = reinterpret_cast<int32_t*>(c->ws + o_rpos);
         c->offsets = reinterpret_cast<int32_t*>(c->ws + o_offs);
         c->route_ws = c->ws + o_rws;
+        c->route_ws_bytes = route_workspace_layout(d->T_max, d->k_max, E).total;
         c->done = reinterpret_cast<int32_t*>(c->ws + o_done);
         c->tickets = reinterpret_cast<int32_t*>(c->ws + o_tick);
         c->h = c->ws + o_h;
+        c->ws_call_off = o_ids;
+        c->n_done = (R_cap + kBM - 1) / kBM + E + 1;
+        c->n_tickets = E + 2;
         if (d->n_shared > 0) {
+            c->n_sh_done = d->n_shared * ((d->T_max + kBM - 1) / kBM) + 1;
             c->sh_done = reinterpret_cast<int32_t*>(c->ws + o_sh_done);
             c->sh_offsets = reinterpret_cast<int32_t*>(c->ws + o_sh_offs);
             c->sh_mblk = reinterpret_cast<int32_t*>(c->ws + o_sh_mblk);
@@ -932,7 +954,7 @@ extern "C" {
 
 estream_status estream_arena_preload(estream_ctx* c, int layer, void* cuda_stream) {
     if (!c) return ESTREAM_ERR_NOT_BOUND;
-    if (layer < 0 || layer >= c->d.L) return ESTREAM_ERR_INVALID_ARG;
+    if (layer < 0 || layer >= c->d.L || !on_bound_device(c)) return ESTREAM_ERR_INVALID_ARG;
     if (c->n_groups > c->d.B) return ESTREAM_ERR_CAPACITY;
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
     c->trace.clear();
@@ -975,6 +997,7 @@ static estream_status prefill_impl(estream_ctx* c, int layer, const void* X, con
     if (layer < 0 || layer >= c->d.L || !X || !logits || !Y || T < 1 || k < 1 || k > c->d.E)
         return ESTREAM_ERR_INVALID_ARG;
     if (!aligned(X, 16) || !aligned(Y, 16) || (A && !aligned(A, 16))) return ESTREAM_ERR_INVALID_ARG;
+    if (!on_bound_device(c)) return ESTREAM_ERR_INVALID_ARG;
     if (T > c->d.T_max || k > c->d.k_max) return ESTREAM_ERR_CAPACITY;
     // this call's routed expert kernels: both tile phases, or (a test of the
     // bounded waits) the down tiles alone, whose m-block counters then never fill
@@ -1038,7 +1061,7 @@ static estream_status prefill_impl(estream_ctx* c, int layer, const void* X, con
         if (launch_route_build(logits, T, E, k, renorm, c->d_perm + static_cast<size_t>(layer) * E, E,
                                c->topk_ids, c->alpha, c->offsets, c->rec_tok, c->rec_route,
                                c->d.deterministic ? c->rec_pos : nullptr, c->done, c->tickets, E + 2,
-                               c->route_ws, s, &launches, A ? &ri : nullptr,
+                               c->route_ws, c->route_ws_bytes, s, &launches, A ? &ri : nullptr,
                                c->route_withhold_next ? 1 : 0) != cudaSuccess) {
             drain(c, s);
             return ESTREAM_ERR_CUDA;
@@ -1205,7 +1228,28 @@ estream_status estream_last_stats(estream_ctx* c, estream_stats* out) {
     }
     c->timed.clear();
     *out = c->stats;
+    // overlap of loading and execution over the calls since the last reset
+    const double t_io = out->ms_io_busy, t_total = out->ms_total;
+    const double t_exec = out->ms_route + out->ms_ffn + out->ms_shared + out->ms_combine;
+    auto clamp01 = [](double x) { return x < 0.0 ? 0.0 : (x > 1.0 ? 1.0 : x); };
+    out->hidden_fraction = t_io > 0.0 ? clamp01((t_io + t_exec - t_total) / t_io) : 0.0;
+    out->bubble_rate = t_total > 0.0 ? clamp01(1.0 - std::max(t_io, t_exec) / t_total) : 0.0;
     return st;
+}
+
+estream_status estream_poison_workspace(estream_ctx* c, void* cuda_stream) {
+    if (!c) return ESTREAM_ERR_NOT_BOUND;
+    if (!on_bound_device(c)) return ESTREAM_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    char* call = c->ws + c->ws_call_off;
+    if (cudaMemsetAsync(call, 0xff, c->ws_bytes - c->ws_call_off, s) != cudaSuccess)
+        return ESTREAM_ERR_CUDA;
+    struct { int32_t* p; size_t n; } counters[3] = {
+        {c->done, c->n_done}, {c->sh_done, c->n_sh_done}, {c->tickets, c->n_tickets}};
+    for (const auto& r : counters)
+        if (r.p && r.n && cudaMemsetAsync(r.p, 0x7f, sizeof(int32_t) * r.n, s) != cudaSuccess)
+            return ESTREAM_ERR_CUDA;
+    return ESTREAM_OK;
 }
 
 estream_status estream_get_device_error(estream_ctx* c) {

@@ -58,6 +58,7 @@ class Stats(ctypes.Structure):
         ("groups_loaded", ctypes.c_int), ("groups_skipped", ctypes.c_int),
         ("groups_hit", ctypes.c_int),
         ("ms_io_busy", ctypes.c_double),
+        ("hidden_fraction", ctypes.c_double), ("bubble_rate", ctypes.c_double),
     ]
 
 
@@ -72,6 +73,8 @@ SIGNATURES = {
     "estream_route_build": (_I, [_P, _I, _I, _I, _I, _P, _I, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "estream_workspace_error": (_I, [_P, _P]),
     "estream_route_build_noalloc": (_I, [_P, _I, _I, _I, _I, _P, _I, _P, _P, _P, _P, _P, _P]),
+    "estream_route_noalloc_error": (_I, [_P]),
+    "estream_poison_workspace": (_I, [_P, _P]),
     "estream_router_workspace_bytes": (_SZ, [_I, _I, _I]),
     "estream_router_logits": (_I, [_P, _I, _I, _P, _I, _P, _P, _SZ, _P]),
     "estream_arena_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
@@ -137,10 +140,25 @@ def _dptr(t: torch.Tensor | None):
     return t.data_ptr()
 
 
-def _stream(stream=None):
+def _stream(stream=None, device=None):
+    """The cuda_stream argument: `stream` (a torch.cuda.Stream or a raw
+    handle), else the current stream of `device`. A torch stream of another
+    device than `device` is refused."""
     if stream is None:
-        stream = torch.cuda.current_stream()
-    return stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
+        stream = torch.cuda.current_stream(device)
+    if hasattr(stream, "cuda_stream"):
+        if device is not None and stream.device != torch.device(device):
+            raise ValueError(f"stream belongs to {stream.device}, the tensors to {device}")
+        return stream.cuda_stream
+    return stream
+
+
+class _on(torch.cuda.device):
+    """Makes the tensors' device current for the duration of one library
+    call: the library launches on the current device, with these pointers."""
+
+    def __init__(self, t: torch.Tensor):
+        super().__init__(t.device)
 
 
 def version() -> int:
@@ -195,10 +213,13 @@ def route_build(logits: torch.Tensor, k: int, renorm: bool, phi: torch.Tensor | 
     nbytes = route_workspace_bytes(T, E, k, P)
     if workspace is None:
         workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
-    st = lib().estream_route_build(
-        _dptr(logits), T, E, k, int(bool(renorm)), _dptr(phi), P, _dptr(o["topk_ids"]),
-        _dptr(o["alpha"]), _dptr(o["offsets"]), _dptr(o["rec_tok"]), _dptr(o["rec_route"]),
-        _dptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    if workspace.device != dev:
+        raise ValueError(f"workspace must be on {dev}")
+    with _on(logits):
+        st = lib().estream_route_build(
+            _dptr(logits), T, E, k, int(bool(renorm)), _dptr(phi), P, _dptr(o["topk_ids"]),
+            _dptr(o["alpha"]), _dptr(o["offsets"]), _dptr(o["rec_tok"]), _dptr(o["rec_route"]),
+            _dptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream, dev))
     _check(st, "estream_route_build")
     o["workspace"] = workspace
     return o
@@ -225,8 +246,12 @@ def router_logits(X: torch.Tensor, W_r: torch.Tensor, logits: torch.Tensor | Non
                                 device=X.device)
     if tuple(logits.shape) != (T, E) or logits.dtype != torch.float32 or logits.device != X.device:
         raise ValueError(f"logits must be [{T}, {E}] fp32 on X's device")
-    st = lib().estream_router_logits(_dptr(X), T, H, _dptr(W_r), E, _dptr(logits), _dptr(workspace),
-                                     workspace.numel() * workspace.element_size(), _stream(stream))
+    if workspace.device != X.device:
+        raise ValueError("workspace must be on X's device")
+    with _on(X):
+        st = lib().estream_router_logits(_dptr(X), T, H, _dptr(W_r), E, _dptr(logits),
+                                         _dptr(workspace), workspace.numel() * workspace.element_size(),
+                                         _stream(stream, X.device))
     _check(st, "estream_router_logits")
     return logits
 
@@ -246,22 +271,35 @@ def route_build_noalloc(logits: torch.Tensor, k: int, renorm: bool, phi: torch.T
     o.setdefault("rec_tok", torch.empty(max(R, 1), dtype=torch.int32, device=dev))
     o.setdefault("rec_route", torch.empty(max(R, 1), dtype=torch.int32, device=dev))
     _check_route_args(logits, k, phi, P, o)
-    st = lib().estream_route_build_noalloc(
-        _dptr(logits), T, E, k, int(bool(renorm)), _dptr(phi), P, _dptr(o["topk_ids"]),
-        _dptr(o["alpha"]), _dptr(o["offsets"]), _dptr(o["rec_tok"]), _dptr(o["rec_route"]),
-        _stream(stream))
+    with _on(logits):
+        st = lib().estream_route_build_noalloc(
+            _dptr(logits), T, E, k, int(bool(renorm)), _dptr(phi), P, _dptr(o["topk_ids"]),
+            _dptr(o["alpha"]), _dptr(o["offsets"]), _dptr(o["rec_tok"]), _dptr(o["rec_route"]),
+            _stream(stream, dev))
     _check(st, "estream_route_build_noalloc")
     return o
 
 
+def route_noalloc_error(device=None, stream=None) -> int:
+    """estream_route_noalloc_error on `device` (default: the current one):
+    the status the latest allocation-free route build there recorded."""
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(device):
+        return lib().estream_route_noalloc_error(_stream(stream, device))
+
+
 def workspace_error(workspace: torch.Tensor, stream=None) -> int:
-    return lib().estream_workspace_error(_dptr(workspace), _stream(stream))
+    with _on(workspace):
+        return lib().estream_workspace_error(_dptr(workspace), _stream(stream, workspace.device))
 
 
 def cast_f32_bf16(src: torch.Tensor, dst: torch.Tensor, stream=None) -> None:
-    assert src.dtype == torch.float32 and dst.dtype == torch.bfloat16 and src.numel() == dst.numel()
-    _check(lib().estream_cast_f32_bf16(_dptr(src), _dptr(dst), src.numel(), _stream(stream)),
-           "estream_cast_f32_bf16")
+    if (src.dtype != torch.float32 or dst.dtype != torch.bfloat16 or src.numel() != dst.numel()
+            or not src.is_cuda or dst.device != src.device):
+        raise ValueError("src must be fp32 and dst bf16 of the same size, on one CUDA device")
+    with _on(src):
+        _check(lib().estream_cast_f32_bf16(_dptr(src), _dptr(dst), src.numel(),
+                                           _stream(stream, src.device)), "estream_cast_f32_bf16")
 
 
 # ---------------------------------------------------------------------------
@@ -363,9 +401,10 @@ def moe_layer_prefill(ctx, layer: int, X: torch.Tensor, logits: torch.Tensor, k:
                       renorm: bool, Y: torch.Tensor, stream=None) -> None:
     _check_layer_args(X, logits, Y)
     T = X.shape[0]
-    _check(lib().estream_moe_layer_prefill(ctx, layer, _dptr(X), _dptr(logits), T, k,
-                                           int(bool(renorm)), _dptr(Y), _stream(stream)),
-           "estream_moe_layer_prefill")
+    with _on(X):
+        _check(lib().estream_moe_layer_prefill(ctx, layer, _dptr(X), _dptr(logits), T, k,
+                                               int(bool(renorm)), _dptr(Y), _stream(stream, X.device)),
+               "estream_moe_layer_prefill")
 
 
 def moe_layer_prefill_residual(ctx, layer: int, X: torch.Tensor, logits: torch.Tensor, k: int,
@@ -373,10 +412,11 @@ def moe_layer_prefill_residual(ctx, layer: int, X: torch.Tensor, logits: torch.T
     """Y = A + the layer's MoE output (Y written, not read)."""
     _check_layer_args(X, logits, Y, A)
     T = X.shape[0]
-    _check(lib().estream_moe_layer_prefill_residual(ctx, layer, _dptr(X), _dptr(logits), T, k,
-                                                    int(bool(renorm)), _dptr(A), _dptr(Y),
-                                                    _stream(stream)),
-           "estream_moe_layer_prefill_residual")
+    with _on(X):
+        _check(lib().estream_moe_layer_prefill_residual(ctx, layer, _dptr(X), _dptr(logits), T, k,
+                                                        int(bool(renorm)), _dptr(A), _dptr(Y),
+                                                        _stream(stream, X.device)),
+               "estream_moe_layer_prefill_residual")
 
 
 def set_timing(ctx, on: bool) -> None:
@@ -395,6 +435,12 @@ def last_stats(ctx) -> dict:
 
 def get_device_error(ctx) -> int:
     return lib().estream_get_device_error(ctx)
+
+
+def poison_workspace(ctx, stream=None) -> None:
+    """estream_poison_workspace (test aid): NaN / past-target fill of the
+    context's per-call buffers on the stream, before a layer call."""
+    _check(lib().estream_poison_workspace(ctx, _stream(stream)), "estream_poison_workspace")
 
 
 def residency_trace(ctx, cap: int = 4096):

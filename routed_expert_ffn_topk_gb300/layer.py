@@ -25,6 +25,10 @@ class BoundLayerStack:
                  Q=1, ffn_form=es.FFN_AUTO, wdtype=None, device="cuda"):
         cfg = wl.cfg
         self.cfg, self.wl, self.mode = cfg, wl, mode
+        device = torch.device(device)
+        if device.type == "cuda" and device.index is None:
+            device = torch.device("cuda", torch.cuda.current_device())
+        self.device = device
         # wdtype=es.Q4 packs the (bf16) weights of a bf16 workload as 4-bit experts
         self.dtype = wdtype if wdtype is not None else (es.BF16 if cfg.dtype == "bf16" else es.F32)
         L = len(wl.layers)
@@ -62,11 +66,13 @@ class BoundLayerStack:
             n_shared=cfg.n_shared, F_shared=cfg.F_shared, shared=self.shared or None,
             T_max=self.T_max, k_max=self.k_max, deterministic=deterministic, schedule=schedule, Q=Q,
             ffn_form=ffn_form)
-        self.ctx = es.bind_arena(self.desc)
-        if mode == "resident":
-            if L != 1:
-                raise ValueError("resident mode holds one layer")
-            es.arena_preload(self.ctx, 0)
+        if mode == "resident" and L != 1:
+            raise ValueError("resident mode holds one layer")
+        # the context lives on the arena's device: bind and preload with it current
+        with torch.cuda.device(device):
+            self.ctx = es.bind_arena(self.desc)
+            if mode == "resident":
+                es.arena_preload(self.ctx, 0)
 
     def prefill(self, layer: int, X: torch.Tensor, logits: torch.Tensor, Y: torch.Tensor,
                 k=None, renorm=None, stream=None, residual: torch.Tensor | None = None) -> None:
@@ -77,6 +83,8 @@ class BoundLayerStack:
         want = torch.float32 if self.dtype == es.F32 else torch.bfloat16
         if X.dtype != want:
             raise ValueError(f"X must be {want} for this arena")
+        if X.device != self.device:
+            raise ValueError(f"X is on {X.device}, the arena on {self.device}")
         k = cfg.k if k is None else k
         renorm = cfg.renorm if renorm is None else renorm
         if residual is None:
@@ -101,9 +109,16 @@ class BoundLayerStack:
         self.prefill(layer, X, logits, Y, k=k, renorm=renorm, stream=stream)
         return logits
 
+    def poison(self, stream=None) -> None:
+        """Test aid: NaN / past-target fill of the context's per-call buffers
+        (estream_poison_workspace) on the stream, before a layer call."""
+        with torch.cuda.device(self.device):
+            es.poison_workspace(self.ctx, stream)
+
     def close(self) -> None:
         if getattr(self, "ctx", None):
-            es.unbind(self.ctx)
+            with torch.cuda.device(self.device):
+                es.unbind(self.ctx)
             self.ctx = None
 
     def __del__(self):  # pragma: no cover

@@ -1,8 +1,9 @@
 """One MoE layer's prefill through the C ABI against the oracle.
 
 Small shapes of every model family are compared element by element (all of
-Y); the full-size layer shapes are compared on a seeded sample of token rows
-that the oracle evaluates one by one.
+Y); the full-size layer shapes are compared on token rows that the oracle
+evaluates one by one, chosen so that every (expert, 128-record block) of the
+route map holds a checked record.
 """
 import numpy as np
 import pytest
@@ -86,9 +87,10 @@ def test_layer_full_size_sampled(key, mode, form):
         y = run_layer(st, wl)
     finally:
         st.close()
-    rows = W.sample_rows(cfg.T, 24 if cfg.H * cfg.F < 2e7 else 10, seed=3)
-    ref = _gpu.oracle_layer(wl, 0, wl.X, rows=rows.numpy())
-    _gpu.assert_y_close(y[rows.numpy()], ref, f"{key}/{mode}/{form} sampled")
+    # a checked record in every (expert, 128-record block) of the route map
+    rows = _gpu.rows_covering_mblocks(wl.logits[0].numpy(), cfg.k)
+    ref = _gpu.oracle_layer(wl, 0, wl.X, rows=rows)
+    _gpu.assert_y_close(y[rows], ref, f"{key}/{mode}/{form} {len(rows)} rows")
 
 
 def test_layer_stack_chained_full_size():
@@ -101,10 +103,10 @@ def test_layer_stack_chained_full_size():
     wl = W.make_workload(cfg)
     dev = _gpu.device()
     st = BoundLayerStack(wl, mode="paged")
-    rows = W.sample_rows(cfg.T, 8, seed=4).numpy()
     try:
         X = wl.X.to(dev)
         for l in range(cfg.layers):
+            rows = _gpu.rows_covering_mblocks(wl.logits[l].numpy(), cfg.k)
             Y = X.float()
             st.prefill(l, X, wl.logits[l].to(dev), Y)
             torch.cuda.synchronize()

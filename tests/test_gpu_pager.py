@@ -172,3 +172,36 @@ def test_pipeline_trace_matches_max_plus_model(Q):
     L, X = d - a, f - s
     t_model, _ = es.maxplus_pipeline(L, X, Q, 2, t_ne)
     assert abs(t_model - f[-1]) <= 0.25 * f[-1] + 0.05, (t_model, f[-1])
+
+
+def test_stats_overlap_measures():
+    """estream_last_stats's hidden_fraction and bubble_rate (section 3.4,
+    Fig. 6): from the same calls' copy, execution and total times, within
+    [0, 1]; a resident call copies nothing and hides nothing."""
+    from routed_expert_ffn_topk_gb300 import estream as es
+    wl = small_workload("c2")
+    for mode in ("paged", "resident"):
+        st = _stack(wl, mode=mode, G=4, B=2) if mode == "paged" else _stack(wl, mode=mode)
+        try:
+            run_layer(st, wl)
+            es.reset_stats(st.ctx)
+            es.set_timing(st.ctx, True)
+            for _ in range(3):
+                if mode == "paged":
+                    es.arena_invalidate(st.ctx)
+                run_layer(st, wl)
+            s = es.last_stats(st.ctx)
+        finally:
+            st.close()
+        t_io, t_tot = s["ms_io_busy"], s["ms_total"]
+        t_ex = s["ms_route"] + s["ms_ffn"] + s["ms_shared"] + s["ms_combine"]
+        assert 0.0 <= s["hidden_fraction"] <= 1.0 and 0.0 <= s["bubble_rate"] <= 1.0
+        assert t_tot > 0
+        want_b = min(1.0, max(0.0, 1.0 - max(t_io, t_ex) / t_tot))
+        assert s["bubble_rate"] == pytest.approx(want_b, abs=1e-12)
+        if mode == "paged":
+            assert t_io > 0 and s["h2d_bytes"] > 0
+            want_h = min(1.0, max(0.0, (t_io + t_ex - t_tot) / t_io))
+            assert s["hidden_fraction"] == pytest.approx(want_h, abs=1e-12)
+        else:
+            assert t_io == 0 and s["hidden_fraction"] == 0.0

@@ -1,0 +1,184 @@
+"""Ordering checks of the fused expert kernels with poisoned buffers.
+
+Inside one fused launch the down tiles of an m-block wait on counters for h
+rows that other CTAs write; the route build zeroes those counters, and the
+route map, h and the deterministic mode's row buffers are rewritten by every
+call. A call that read any of them too early would read the previous call's
+values -- identical when the inputs repeat -- and pass every test that
+repeats its inputs. Here estream_poison_workspace fills every per-call buffer
+with NaN (ints with all-ones) and every completion counter with a value past
+its target before each call, and consecutive calls get different inputs: an
+early read of h then yields NaN in Y, and a counter that was not zeroed lets
+a down tile read unwritten h. Each call is compared with the oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+from routed_expert_ffn_topk_gb300 import workloads as W
+from tests import _gpu
+
+pytestmark = pytest.mark.gpu
+
+SMALL = {
+    "c2": dict(T=384, H=512, E=16, k=4, F=384),
+    "c3": dict(T=320, H=512, E=12, k=3, F=256, F_shared=384),
+    "c4": dict(T=300, H=768, E=10, k=4, F=256, F_shared=640, layers=1),
+    "c5": dict(T=520, H=512, E=4, k=2, F=1152),
+}
+
+
+def _inputs(cfg, seed):
+    """A second, independent input set for the same layer: X and logits from
+    another seed (the weights stay)."""
+    wl = W.make_workload(cfg, seed=seed, weights=False)
+    return wl.X, wl.logits[0]
+
+
+def _check_calls(st, wl, seeds, residual=False, stream_poison=True, dq=None):
+    from routed_expert_ffn_topk_gb300 import estream as es
+    cfg = wl.cfg
+    dev = _gpu.device()
+    for n, seed in enumerate(seeds):
+        X_cpu, lg_cpu = (wl.X, wl.logits[0]) if seed is None else _inputs(cfg, seed)
+        X, lg = X_cpu.to(dev), lg_cpu.to(dev)
+        Y = torch.full((cfg.T, cfg.H), float("nan"), dtype=torch.float32, device=dev)
+        if not residual:
+            Y.zero_()
+        if stream_poison:
+            st.poison()
+        st.prefill(0, X, lg, Y, residual=X if residual else None)
+        torch.cuda.synchronize()
+        assert es.get_device_error(st.ctx) == es.OK
+        wl_n = W.Workload(cfg, [lg_cpu], X_cpu, wl.layers)
+        A = X_cpu.double().numpy() if residual else None
+        if dq is not None:
+            ref = _gpu.oracle_layer_q4(wl_n, 0, X_cpu, dq=dq)
+        else:
+            ref = _gpu.oracle_layer(wl_n, 0, X_cpu, residual=A)
+        y = Y.cpu().numpy()
+        if residual:
+            y, ref = y - A, ref - A
+        _gpu.assert_y_close(y, ref, f"{cfg.key} poisoned call {n}")
+
+
+@pytest.mark.parametrize("key,form,mode,det", [
+    ("c2", "single", "resident", False), ("c2", "pair", "resident", False),
+    ("c5", "pair", "resident", False), ("c5", "single", "paged", False),
+    ("c3", "auto", "resident", False), ("c4", "auto", "paged", False),
+    ("c2", "auto", "resident", True), ("c3", "pair", "paged", True),
+])
+def test_poisoned_consecutive_calls(key, form, mode, det):
+    from routed_expert_ffn_topk_gb300 import estream as es
+    from routed_expert_ffn_topk_gb300.layer import BoundLayerStack
+    cfg = W.scaled(W.CONFIGS[key], **SMALL[key])
+    wl = W.make_workload(cfg)
+    f = {"auto": es.FFN_AUTO, "single": es.FFN_SINGLE, "pair": es.FFN_PAIR}[form]
+    st = BoundLayerStack(wl, mode=mode, ffn_form=f, deterministic=det)
+    try:
+        _check_calls(st, wl, [None, 77, None])
+    finally:
+        st.close()
+
+
+@pytest.mark.parametrize("mode", ["resident", "paged"])
+def test_poisoned_consecutive_calls_q4(mode):
+    from routed_expert_ffn_topk_gb300 import estream as es
+    from routed_expert_ffn_topk_gb300.layer import BoundLayerStack
+    cfg = W.scaled(W.CONFIGS["c3"], **SMALL["c3"])
+    wl = W.make_workload(cfg)
+    dq = _gpu.q4_weights(wl.layers[0])
+    st = BoundLayerStack(wl, mode=mode, wdtype=es.Q4)
+    try:
+        _check_calls(st, wl, [None, 78], dq=dq)
+    finally:
+        st.close()
+
+
+@pytest.mark.parametrize("form", ["single", "pair", "q4"])
+def test_poisoned_graph_replay_with_new_inputs(form):
+    """A captured layer call replayed on new inputs copied into its buffers,
+    with the workspace poisoned before each replay."""
+    from routed_expert_ffn_topk_gb300 import estream as es
+    from routed_expert_ffn_topk_gb300.layer import BoundLayerStack
+    cfg = W.scaled(W.CONFIGS["c2"], **SMALL["c2"])
+    wl = W.make_workload(cfg)
+    dev = _gpu.device()
+    kw = {"wdtype": es.Q4} if form == "q4" else {
+        "ffn_form": es.FFN_PAIR if form == "pair" else es.FFN_SINGLE}
+    dq = _gpu.q4_weights(wl.layers[0]) if form == "q4" else None
+    st = BoundLayerStack(wl, mode="resident", **kw)
+    try:
+        X = wl.X.to(dev).clone()
+        lg = wl.logits[0].to(dev).clone()
+        Y = torch.empty(cfg.T, cfg.H, dtype=torch.float32, device=dev)
+
+        def step():
+            st.prefill(0, X, lg, Y, residual=X)
+
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for _ in range(2):
+                step()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step()
+        torch.cuda.synchronize()
+        for n, seed in enumerate([79, None, 80]):
+            X_cpu, lg_cpu = (wl.X, wl.logits[0]) if seed is None else _inputs(cfg, seed)
+            X.copy_(X_cpu.to(dev))
+            lg.copy_(lg_cpu.to(dev))
+            Y.fill_(float("nan"))
+            st.poison()
+            g.replay()
+            torch.cuda.synchronize()
+            assert es.get_device_error(st.ctx) == es.OK
+            wl_n = W.Workload(cfg, [lg_cpu], X_cpu, wl.layers)
+            A = X_cpu.double().numpy()
+            if dq is not None:
+                ref = _gpu.oracle_layer_q4(wl_n, 0, X_cpu, dq=dq) + A
+            else:
+                ref = _gpu.oracle_layer(wl_n, 0, X_cpu, residual=A)
+            _gpu.assert_y_close(Y.cpu().numpy() - A, ref - A, f"{form} graph replay {n}")
+        del g
+    finally:
+        st.close()
+
+
+@pytest.mark.parametrize("key", ["c5", "c4"])
+def test_poisoned_full_size_every_mblock(key):
+    """Full-size resident layers (Mixtral-shaped: the CTA-pair kernel over 8
+    experts of about 1024 records; Qwen-shaped layer 0: 60 Zipf-skewed
+    experts and the shared expert), two consecutive poisoned calls with
+    different inputs, checked on token rows that put at least one record in
+    every (expert, 128-record block) of the route map -- every m-block and
+    every pair half of the fused kernel, including each ragged last block."""
+    from routed_expert_ffn_topk_gb300 import estream as es
+    from routed_expert_ffn_topk_gb300.layer import BoundLayerStack
+    cfg0 = W.CONFIGS[key]
+    cfg = W.scaled(cfg0, layers=1, key_suffix="") if cfg0.layers > 1 else cfg0
+    wl = W.make_workload(cfg)
+    dev = _gpu.device()
+    st = BoundLayerStack(wl, mode="resident")
+    try:
+        for n, seed in enumerate([None, 91]):
+            X_cpu, lg_cpu = (wl.X, wl.logits[0]) if seed is None else _inputs(cfg, W.CONFIG_SEEDS[key] + seed)
+            X, lg = X_cpu.to(dev), lg_cpu.to(dev)
+            Y = torch.empty(cfg.T, cfg.H, dtype=torch.float32, device=dev)
+            st.poison()
+            st.prefill(0, X, lg, Y, residual=X)
+            torch.cuda.synchronize()
+            assert es.get_device_error(st.ctx) == es.OK
+            y = Y.cpu().numpy()
+            assert np.isfinite(y).all()
+            rows = _gpu.rows_covering_mblocks(lg_cpu.numpy(), cfg.k)
+            wl_n = W.Workload(cfg, [lg_cpu], X_cpu, wl.layers)
+            A = X_cpu.double().numpy()
+            ref = _gpu.oracle_layer(wl_n, 0, X_cpu, rows=rows, residual=A)
+            _gpu.assert_y_close(y[rows] - A[rows], ref - A[rows],
+                                f"{key} full size, {len(rows)} rows covering every m-block, call {n}")
+    finally:
+        st.close()
