@@ -423,9 +423,10 @@ def measure_config(args, cfg, wl, dev, flush, peaks, world, rank):
     e2e_pipe = None
     if graph is not None:
         Yh2 = [Yh, torch.empty_like(Yh).pin_memory()]
+        # the second set starts as a copy of the first: the capture's warm-up
+        # runs read it before the pipelined loop writes it
         sets = [(Xbuf[0], logits, Y[L - 1]),
-                (torch.empty_like(Xbuf[0]), [torch.empty_like(t) for t in logits],
-                 torch.empty_like(Y[L - 1]))]
+                (Xbuf[0].clone(), [t.clone() for t in logits], torch.empty_like(Y[L - 1]))]
         try:
             graphs_b = [graph, capture_graph(make_step(*sets[1]))]
         except Exception:

@@ -175,7 +175,9 @@ __device__ __forceinline__ void topk_token(
         const int i = t * k + lane;
         topk_ids[i] = id_mine;
         alpha[i] = a_mine;
-        int slot = phi ? phi[id_mine] : id_mine;
+        // no candidate is selected only for logits outside the contract (a
+        // row of NaNs with every bit set): file the route as unresolved
+        int slot = id_mine < 0 ? P + 1 : (phi ? phi[id_mine] : id_mine);
         if (slot < -1 || slot >= P) {
             record_error(err, kDevErrSlotRange);
             slot = -1;
@@ -350,7 +352,7 @@ __device__ void scatter_chunk(int c, int nchunk, const int32_t* __restrict__ top
         int b = P;
         if (valid) {
             const int e = topk_ids[i];
-            const int slot = phi ? phi[e] : e;
+            const int slot = e < 0 ? -1 : (phi ? phi[e] : e);
             b = (slot < 0 || slot >= P) ? P : slot;
         }
         // the chunk's base inside the slot, loaded by every thread before the
