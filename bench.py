@@ -718,11 +718,50 @@ def measure_router(cfg, X0, dev, stream, flush, peaks, steps):
     t = sorted(ms)[len(ms) // 2]
     nbytes = T * H * 2 + E * H * 2 + T * E * 4
     gbs = nbytes / (t / 1e3) / 1e9
+
+    # routing from the layer input: router logits + top-k + route map, as one
+    # fused launch, against the router kernel followed by the route build
+    k = cfg.k
+    rws = torch.empty(es.route_workspace_bytes(T, E, k, E), dtype=torch.uint8, device=dev)
+    out = es.route_build_from_x(X0, W_r, k, cfg.renorm, workspace=rws)
+
+    def timed(fn, n):
+        for _ in range(3):
+            fn()
+        res = []
+        for _ in range(n):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            b.synchronize()
+            res.append(a.elapsed_time(b))
+        return sorted(res)[len(res) // 2]
+
+    t_fused = timed(lambda: es.route_build_from_x(X0, W_r, k, cfg.renorm, out=out, workspace=rws),
+                    max(steps, 5))
+    assert es.workspace_error(rws) == es.OK
+    lg = out["logits"]
+
+    def two():
+        es.router_logits(X0, W_r, logits=lg, workspace=ws)
+        es.route_build(lg, k, cfg.renorm, out=out, workspace=rws)
+
+    t_two = timed(two, max(steps, 5))
+    assert es.workspace_error(rws) == es.OK
     return {"kernel": "k_router_partial (tcgen05, K split over a CTA cluster, fixed-order DSMEM sum)",
             "ms": round(t, 4), "algorithmic_bytes": nbytes, "GBps": round(gbs, 1),
             "frac_hbm": round(gbs / peaks["hbm_gbs"], 4),
             "TFLOPs": round(2.0 * T * H * E / (t / 1e3) / 1e12, 1),
-            "workspace_bytes": int(ws.numel())}
+            "workspace_bytes": int(ws.numel()),
+            "routing_from_x": {
+                "fused_single_launch": es.route_build_from_x_fused(T, H, E),
+                "kernel": "k_route_from_x (router tile per cluster, top-k from shared memory, route map)",
+                "ms": round(t_fused, 4),
+                "two_launches_ms": round(t_two, 4),
+                "note": "router logits + top-k + route map (no residual rows); two launches = "
+                        "k_router_partial then the route build's memset + k_route_fused"}}
 
 
 def measure_q4(args, cfg, wl, dev, stream, flush, peaks):

@@ -144,6 +144,43 @@ estream_status estream_router_logits(const void* X, int T, int H, const void* W_
                                      void* cuda_stream);
 
 /*
+ * Router logits and route map in one call: logits = X W_r^T as
+ * estream_router_logits computes them (bf16 products, fp32 accumulation,
+ * the K range split into chunks whose partial sums are added in a fixed
+ * order), then the top-k and route map of estream_route_build on those
+ * logits, which are also written to `logits`. The pages run routing on the
+ * accelerator from the layer input (section 1, section 4); this is that
+ * operator as one kernel: a cooperative launch of thread-block clusters in
+ * which each cluster computes a 128-token tile of logits on the tensor cores,
+ * sums the chunks' partials in shared memory, ranks the tile's tokens there
+ * and then joins the grid-wide route-map construction -- the logits never
+ * make a round trip through device memory before the top-k. Shapes the
+ * single launch cannot take (E > 128, or more 128-token tiles than clusters
+ * the device holds at once) run the router kernel and the route build as
+ * two launches on the same stream, with the same results;
+ * estream_route_build_from_x_fused tells which form a shape gets.
+ *
+ * X, W_r, T, H, E  as in estream_router_logits (H a multiple of 64).
+ * k, renorm, phi, P, topk_ids, alpha, offsets, rec_tok, rec_route, workspace,
+ *           workspace_bytes: as in estream_route_build (the workspace size is
+ *           estream_route_workspace_bytes(T, E, k, P)).
+ * logits    device, [T][E] fp32 out.
+ * Errors the kernels find (a phi entry out of range, a bounded wait that ran
+ * out) are reported by estream_workspace_error; a wait that ran out leaves
+ * an empty route map. Nothing is synchronised.
+ */
+estream_status estream_route_build_from_x(const void* X, int T, int H, const void* W_r, int E,
+                                          int k, int renorm, const int32_t* phi, int P,
+                                          float* logits, int32_t* topk_ids, float* alpha,
+                                          int32_t* offsets, int32_t* rec_tok, int32_t* rec_route,
+                                          void* workspace, size_t workspace_bytes,
+                                          void* cuda_stream);
+
+/* 1 if estream_route_build_from_x (and estream_moe_layer_prefill_from_x)
+ * run these sizes as one fused launch on the current device, 0 if as two. */
+int estream_route_build_from_x_fused(int T, int H, int E, int P);
+
+/*
  * estream_route_build without a workspace argument, for callers that cannot
  * give this library device scratch memory (for example a serving process
  * that reserved all device memory up front and allows no cudaMalloc on its
@@ -346,6 +383,22 @@ estream_status estream_moe_layer_prefill(estream_ctx* c, int layer, const void* 
 estream_status estream_moe_layer_prefill_residual(estream_ctx* c, int layer, const void* X,
                                                   const float* logits, int T, int k, int renorm,
                                                   const void* A, float* Y, void* cuda_stream);
+
+/*
+ * The layer call with routing from the layer input: router logits
+ * X W_r^T, top-k and route map in one launch (estream_route_build_from_x),
+ * then the experts as in estream_moe_layer_prefill.
+ * W_r        device, [E][H] bf16 (one row per expert), 16-byte aligned.
+ * A          NULL: Y is accumulated into (Y += ...); else the residual of
+ *            Eq. 2 as in estream_moe_layer_prefill_residual (Y written).
+ * logits_out device, [T][E] fp32, or NULL: receives the router logits.
+ * Contexts of type ESTREAM_F32 are refused (ESTREAM_ERR_INVALID_ARG). The
+ * other arguments and the behaviour are those of estream_moe_layer_prefill.
+ */
+estream_status estream_moe_layer_prefill_from_x(estream_ctx* c, int layer, const void* X,
+                                                const void* W_r, int T, int k, int renorm,
+                                                const void* A, float* Y, float* logits_out,
+                                                void* cuda_stream);
 
 /* Timings and counters accumulated since the last estream_reset_stats. The
  * per-kernel times are CUDA-event times on the launching stream, recorded

@@ -44,8 +44,8 @@ def _stale(out: str, deps) -> bool:
 def build(force: bool = False, verbose: bool = False) -> str:
     nvcc = _nvcc()
     os.makedirs(OBJ_DIR, exist_ok=True)
-    headers = [os.path.join(CSRC, "estream_internal.h"), os.path.join(CSRC, "tc_ptx.cuh"),
-               os.path.join(INCLUDE, "estream.h")]
+    headers = sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh")))
+    headers.append(os.path.join(INCLUDE, "estream.h"))
     common = [nvcc, *ARCH, "-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
               "-I" + INCLUDE, "-I" + CSRC]
     jobs = []

@@ -36,6 +36,10 @@
 #include "estream_internal.h"
 
 namespace es {
+namespace {
+#include "tc_ptx.cuh"
+#include "router_tile.cuh"
+}  // namespace
 
 // ---------------------------------------------------------------------------
 // Written fp32 exponential, the same written definition the CPU oracle uses,
@@ -67,10 +71,6 @@ __device__ __forceinline__ float route_exp(float x) {
     return __fmul_rn(p, __int_as_float((n + 127) << 23));
 }
 
-__device__ __forceinline__ void record_error(int* err, int code) {
-    if (err) atomicCAS(err, kDevErrNone, code);
-}
-
 // One warp per token; lane l holds the logits of experts l, l+32, l+64, ...
 // The softmax denominator is summed in ascending expert order (the same
 // sequence of fp32 additions as the written definition): the warp streams the
@@ -87,13 +87,13 @@ constexpr uint64_t kGridWaitLimitNs = 1000000000ull;  // 1 s
 
 // kJ: logits held per lane (E <= 32 kJ), so that small E keeps the arrays in
 // registers.
+// l: the token's E logits (global or shared memory).
 template <int kJ>
 __device__ __forceinline__ void topk_token(
-    int t, const float* __restrict__ logits, int E, int k, int renorm,
+    int t, const float* l, int E, int k, int renorm,
     const int32_t* __restrict__ phi, int P, int32_t* __restrict__ topk_ids,
     float* __restrict__ alpha, int* counts, int* __restrict__ err) {
     const int lane = threadIdx.x & 31;
-    const float* l = logits + static_cast<size_t>(t) * E;
     const int nj = (E + 31) >> 5;
     const float kNegInf = __int_as_float(0xff800000);
     float v[kJ];
@@ -434,6 +434,26 @@ __device__ void empty_route_map(int32_t* offsets, int32_t* mblk, int P) {
     }
 }
 
+// This CTA's share of the L2 prefetch ranges: contiguous pieces of at most
+// 256 KB (16-byte granules) handed to the bulk-copy unit, which fetches them
+// into L2 without involving the SM further.
+__device__ void issue_l2_prefetch(const L2Prefetch& pf) {
+    constexpr size_t kPiece = 256 * 1024;
+    const size_t nct = gridDim.x, cta = blockIdx.x;
+    for (int r = 0; r < kMaxL2Ranges; ++r) {
+        const size_t units = pf.bytes[r] / 16;
+        if (!pf.base[r] || units == 0) continue;
+        const size_t u0 = units * cta / nct, u1 = units * (cta + 1) / nct;
+        const char* base = static_cast<const char*>(pf.base[r]);
+        for (size_t off = u0 * 16; off < u1 * 16; off += kPiece) {
+            const size_t n = min(kPiece, u1 * 16 - off);
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(base + off),
+                         "r"(static_cast<uint32_t>(n))
+                         : "memory");
+        }
+    }
+}
+
 __global__ void __launch_bounds__(kRouteThreads, 2) k_route_fused(
     const float* __restrict__ logits, int T, int E, int k, int renorm,
     const int32_t* __restrict__ phi, int P, int32_t* __restrict__ topk_ids,
@@ -441,7 +461,7 @@ __global__ void __launch_bounds__(kRouteThreads, 2) k_route_fused(
     int32_t* __restrict__ rec_route, int32_t* __restrict__ rec_pos, int32_t* __restrict__ hist,
     int32_t* __restrict__ mblk, int32_t* __restrict__ totals, int32_t* __restrict__ done,
     int32_t* __restrict__ tickets, int n_tickets, int* __restrict__ sync, int* __restrict__ err,
-    int nchunk, ResidualInit resid, int withhold_arrival) {
+    int nchunk, ResidualInit resid, int withhold_arrival, L2Prefetch pf) {
     extern __shared__ int smem[];
     __shared__ int ok_flag;
     const int R = T * k;
@@ -462,22 +482,24 @@ __global__ void __launch_bounds__(kRouteThreads, 2) k_route_fused(
     int rrow = resid.A ? (cta >= nc ? cta - nc : cta + grid - nc) * kChunkTokens + warp : T;
     bool pre = rrow < T && cta >= nc;
     int staged = pre ? stage_residual_row(rrow, resid, rstage) : 0;
+    if (threadIdx.x == 0) issue_l2_prefetch(pf);
     // 1. router + the chunk's slot counts, one warp per token
     for (int c = blockIdx.x; c < nchunk; c += gridDim.x) {
         for (int x = threadIdx.x; x < nb; x += blockDim.x) smem[x] = 0;
         __syncthreads();
         const int t = c * kChunkTokens + warp;
         if (t < T) {
+            const float* l = logits + static_cast<size_t>(t) * E;
             if (E <= 32)
-                topk_token<1>(t, logits, E, k, renorm, phi, P, topk_ids, alpha, smem, err);
+                topk_token<1>(t, l, E, k, renorm, phi, P, topk_ids, alpha, smem, err);
             else if (E <= 64)
-                topk_token<2>(t, logits, E, k, renorm, phi, P, topk_ids, alpha, smem, err);
+                topk_token<2>(t, l, E, k, renorm, phi, P, topk_ids, alpha, smem, err);
             else if (E <= 128)
-                topk_token<4>(t, logits, E, k, renorm, phi, P, topk_ids, alpha, smem, err);
+                topk_token<4>(t, l, E, k, renorm, phi, P, topk_ids, alpha, smem, err);
             else if (E <= 256)
-                topk_token<8>(t, logits, E, k, renorm, phi, P, topk_ids, alpha, smem, err);
+                topk_token<8>(t, l, E, k, renorm, phi, P, topk_ids, alpha, smem, err);
             else
-                topk_token<kMaxPerLane>(t, logits, E, k, renorm, phi, P, topk_ids, alpha, smem, err);
+                topk_token<kMaxPerLane>(t, l, E, k, renorm, phi, P, topk_ids, alpha, smem, err);
         }
         __syncthreads();
         for (int x = threadIdx.x; x < nb; x += blockDim.x)
@@ -532,6 +554,220 @@ __global__ void __launch_bounds__(kRouteThreads, 2) k_route_fused(
     __syncthreads();
     for (int c = blockIdx.x; c < nchunk; c += gridDim.x)
         scatter_chunk(c, nchunk, topk_ids, phi, P, k, R, hist, off, rec_tok, rec_route, rec_pos, mb);
+}
+
+// ---------------------------------------------------------------------------
+// Router logits fused with the route build: one cooperative launch of
+// clusters, from X and W_r to the route map.
+//
+// Cluster m (S CTAs) owns tokens [128 m, 128 m + 128). CTA s of the cluster
+// multiplies the tile's X rows by W_r over its share of the k-blocks on the
+// tensor cores (router_tile.cuh: TMA ring, tcgen05.mma, fp32 accumulator in
+// TMEM, partial sums to shared memory) while its warps 6-15 write the tile's
+// residual rows Y = A. After a cluster barrier CTA s takes the tile's 16-token
+// chunks s, s + S, ...: a warp per token adds the S partials of each of its
+// logits in ascending chunk order over distributed shared memory (the
+// standalone router's order), keeps the row in shared memory (and writes it
+// out when asked), and runs the same top-k and slot counting as k_route_fused
+// on it. The rest is k_route_fused's route map: bounded grid barrier, per-slot
+// scans over chunks, barrier, slot offsets and m-block prefix, stable
+// placement of the CTA's chunks.
+// ---------------------------------------------------------------------------
+struct FusedRouter {
+    int KB, S, N;        // k-blocks of H, CTAs per tile (the cluster), experts per tile
+    uint32_t tx_bytes;   // bytes one ring stage's two boxes deliver
+    float* logits;       // [T][E] out, or null
+};
+
+constexpr int kFusedMaxE = 128;
+constexpr int kFusedChunksPerTile = 128 / kChunkTokens;
+
+__host__ __device__ constexpr size_t fused_ring_bytes(int N) {
+    return router_ring_bytes(N) > router_part_bytes(N) ? router_ring_bytes(N) : router_part_bytes(N);
+}
+__host__ __device__ constexpr size_t fused_rows_bytes(int N) {
+    return static_cast<size_t>(kChunkTokens) * N * sizeof(float);
+}
+__host__ __device__ constexpr size_t fused_smem_bytes(int N, int P) {
+    return 1024 + fused_ring_bytes(N) + fused_rows_bytes(N) + route_scratch_bytes(P + 1) +
+           8 * (2 * kRStages + 1) + 16;
+}
+
+__global__ void __launch_bounds__(kRouteThreads, 1) k_route_from_x(
+    const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
+    const FusedRouter fr, int T, int E, int k, int renorm, const int32_t* __restrict__ phi, int P,
+    int32_t* __restrict__ topk_ids, float* __restrict__ alpha, int32_t* __restrict__ offsets,
+    int32_t* __restrict__ rec_tok, int32_t* __restrict__ rec_route, int32_t* __restrict__ rec_pos,
+    int32_t* __restrict__ hist, int32_t* __restrict__ mblk, int32_t* __restrict__ totals,
+    int32_t* __restrict__ done, int32_t* __restrict__ tickets, int n_tickets, int* __restrict__ sync,
+    int* __restrict__ err, int nchunk, ResidualInit resid, int withhold_arrival, L2Prefetch pf) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ int ok_flag;
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    const int R = T * k;
+    const int nb = P + 1;
+    const int S = fr.S, N = fr.N;
+    // the partial sums are read across a cluster of S CTAs: any other launch
+    // shape leaves an empty route map before any cluster or tensor access
+    if (cluster_num_ctas() != static_cast<uint32_t>(S)) {
+        if (threadIdx.x == 0) record_error(err, kDevErrLaunch);
+        empty_route_map(offsets, mblk, P);
+        return;
+    }
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    uint32_t s_rank;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(s_rank));
+    const int s = static_cast<int>(s_rank);
+    const int m = static_cast<int>(blockIdx.x) / S;  // the cluster's token tile
+
+    const uint32_t sbase = smem_addr(smem);
+    const size_t ring = fused_ring_bytes(N);
+    float* lrows = reinterpret_cast<float*>(smem + ring);                            // [16][N]
+    int* scratch = reinterpret_cast<int*>(smem + ring + fused_rows_bytes(N));         // route scratch
+    const size_t bar_off = ring + fused_rows_bytes(N) + route_scratch_bytes(nb);
+    uint8_t* misc = smem + bar_off + 8 * (2 * kRStages + 1);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
+    RouterTile rt;
+    rt.sA = sbase;
+    rt.sB = sbase + kRStages * kRTileA;
+    rt.bar0 = sbase + static_cast<uint32_t>(bar_off);
+    rt.part = reinterpret_cast<float*>(smem);
+    rt.m0 = m * 128;
+    rt.n0 = 0;
+    rt.N = N;
+    rt.tx_bytes = fr.tx_bytes;
+    rt.kb0 = static_cast<int>(static_cast<long long>(s) * fr.KB / S);
+    rt.kb1 = static_cast<int>(static_cast<long long>(s + 1) * fr.KB / S);
+    const uint32_t tmem_cols = router_tmem_cols(N);
+
+    if (threadIdx.x == 0) {
+        router_tile_init(rt);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_addr(tmem_slot), tmem_cols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    // 1. logits tile on the tensor cores; beside it, the residual rows
+    if (warp < 6) {
+        router_tile_roles(rt, &tm_x, &tm_w, tmem_base, abort_flag, err);
+    } else {
+        if (warp == 6 && lane == 0) issue_l2_prefetch(pf);
+        if (resid.A) {
+            const int rows_per = (128 + S - 1) / S;
+            const int r0 = rt.m0 + s * rows_per;
+            const int r1 = min(T, min(rt.m0 + 128, r0 + rows_per));
+            const int row_bytes = resid.H * resid.elem_bytes;
+            for (int t = r0 + (warp - 6); t < r1; t += kRouteThreads / 32 - 6)
+                widen_residual(resid, t, static_cast<const char*>(resid.A) + static_cast<size_t>(t) * row_bytes,
+                               0, row_bytes);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();  // every CTA's partial is in place
+    const bool gemm_ok = !*abort_flag;
+
+    // 2. the logits of this CTA's chunks (fixed-order sums over the cluster),
+    //    their top-k, and the chunks' slot counts
+    int* counts = scratch;
+    for (int j = s; j < kFusedChunksPerTile; j += S) {
+        const int c = m * kFusedChunksPerTile + j;
+        if (c >= nchunk) break;
+        for (int x = threadIdx.x; x < nb; x += blockDim.x) counts[x] = 0;
+        __syncthreads();
+        const int t = c * kChunkTokens + warp;
+        if (t < T) {
+            float* row = lrows + warp * N;
+            const int r = t - rt.m0;
+            for (int e = lane; e < E; e += 32) {
+                const uint32_t off = sbase + static_cast<uint32_t>((r * (N + 1) + e) * 4);
+                const float v = gemm_ok ? sum_cluster_partials(off, S) : 0.0f;
+                row[e] = v;
+                if (fr.logits) fr.logits[static_cast<size_t>(t) * E + e] = v;
+            }
+            __syncwarp();
+            if (E <= 32)
+                topk_token<1>(t, row, E, k, renorm, phi, P, topk_ids, alpha, counts, err);
+            else if (E <= 64)
+                topk_token<2>(t, row, E, k, renorm, phi, P, topk_ids, alpha, counts, err);
+            else
+                topk_token<4>(t, row, E, k, renorm, phi, P, topk_ids, alpha, counts, err);
+        }
+        __syncthreads();
+        for (int x = threadIdx.x; x < nb; x += blockDim.x)
+            hist[static_cast<size_t>(x) * nchunk + c] = counts[x];
+        __syncthreads();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();  // the peers have read this CTA's partials
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, tmem_cols);
+    }
+
+    // 3. the route map, as in k_route_fused over every CTA of the grid
+    const int ncta = static_cast<int>(gridDim.x);
+    if (!grid_barrier(sync, 1, ncta, err, &ok_flag, withhold_arrival != 0 && blockIdx.x == 0)) {
+        empty_route_map(offsets, mblk, P);
+        return;
+    }
+    // a tile whose logits did not complete (a bounded wait ran out, recorded
+    // before the barrier) leaves the whole route map empty
+    int e0;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(e0) : "l"(err) : "memory");
+    if (e0 == kDevErrTimeout) {
+        empty_route_map(offsets, mblk, P);
+        return;
+    }
+    scan_slots(hist, nchunk, nb, totals, ncta);
+    if (!grid_barrier(sync, 2, ncta, err, &ok_flag)) {
+        empty_route_map(offsets, mblk, P);
+        return;
+    }
+    int* off = scratch;
+    int* mb = scratch + nb;
+    int* warp_sums = scratch + 2 * nb;
+    for (int b = threadIdx.x; b < nb; b += blockDim.x) {
+        const int v = __ldcg(totals + b);
+        off[b] = v;
+        mb[b] = b < P ? (v + kBM - 1) / kBM : 0;
+    }
+    __syncthreads();
+    block_exclusive_scan(off, nb, warp_sums);
+    const int mb_total = block_exclusive_scan(mb, nb, warp_sums);
+    if (blockIdx.x == 0) {
+        for (int b = threadIdx.x; b < nb; b += blockDim.x) {
+            offsets[b] = off[b];
+            mblk[b] = mb[b];
+        }
+        if (tickets)
+            for (int x = threadIdx.x; x < n_tickets; x += blockDim.x) tickets[x] = 0;
+        if (threadIdx.x == 0) {
+            offsets[P + 1] = R;
+            mblk[P + 1] = mb_total;
+        }
+    }
+    if (done)
+        for (int q = blockIdx.x * blockDim.x + threadIdx.x; q < mb_total; q += ncta * blockDim.x)
+            done[q] = 0;
+    __syncthreads();
+    for (int j = s; j < kFusedChunksPerTile; j += S) {
+        const int c = m * kFusedChunksPerTile + j;
+        if (c >= nchunk) break;
+        scatter_chunk(c, nchunk, topk_ids, phi, P, k, R, hist, off, rec_tok, rec_route, rec_pos, mb);
+    }
 }
 
 __global__ void k_identity_map(int T, int n_shared, int32_t* __restrict__ offsets,
@@ -601,7 +837,8 @@ cudaError_t launch_route_build(const float* logits, int T, int E, int k, int ren
                                int32_t* offsets, int32_t* rec_tok, int32_t* rec_route,
                                int32_t* rec_pos, int32_t* done, int32_t* tickets, int n_tickets,
                                void* ws, size_t ws_bytes, cudaStream_t stream, int* n_launches,
-                               const ResidualInit* resid_in, int withhold_arrival) {
+                               const ResidualInit* resid_in, int withhold_arrival,
+                               const L2Prefetch* prefetch, bool clear_err) {
     const RouteWorkspace w = route_workspace_layout(T, k, P);
     if (!ws || w.total > ws_bytes) return cudaErrorInvalidValue;
     char* base = static_cast<char*>(ws);
@@ -619,13 +856,19 @@ cudaError_t launch_route_build(const float* logits, int T, int E, int k, int ren
         if (rc == cudaSuccess) rc = cudaMemsetAsync(mblk, 0, sizeof(int32_t) * (P + 2), stream);
         return rc;
     }
-    // clear the error word and the grid-barrier counter (the kernel writes
-    // every per-chunk count itself)
-    rc = cudaMemsetAsync(base + w.err_off, 0, 2 * sizeof(int32_t), stream);
+    // clear the error word (unless an earlier kernel of the same call wrote
+    // it) and the grid-barrier counter; the kernel writes every per-chunk
+    // count itself
+    rc = clear_err ? cudaMemsetAsync(base + w.err_off, 0, 2 * sizeof(int32_t), stream)
+                   : cudaMemsetAsync(base + w.sync_off, 0, sizeof(int32_t), stream);
     if (rc != cudaSuccess) return rc;
     int* sync = reinterpret_cast<int*>(base + w.sync_off);
     ResidualInit resid{nullptr, 0, nullptr, 0};
     if (resid_in) resid = *resid_in;
+    L2Prefetch pf{};
+    if (prefetch) pf = *prefetch;
+    for (int r = 0; r < kMaxL2Ranges; ++r)  // bulk prefetches move 16-byte granules
+        if (pf.base[r] && reinterpret_cast<uintptr_t>(pf.base[r]) % 16 != 0) pf.base[r] = nullptr;
     const int co_resident = route_co_resident();
     if (co_resident <= 0) return cudaErrorLaunchOutOfResources;
     // with a residual, up to as many CTAs again for its rows
@@ -634,12 +877,158 @@ cudaError_t launch_route_build(const float* logits, int T, int E, int k, int ren
     void* args[] = {&logits, &T, &E, &k, &renorm, &phi, &P, &topk_ids, &alpha, &offsets,
                     &rec_tok, &rec_route, &rec_pos, &hist, &mblk, &totals, &done, &tickets,
                     &n_tickets, &sync, &err, const_cast<int*>(&w.nchunk), &resid,
-                    &withhold_arrival};
+                    &withhold_arrival, &pf};
     rc = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(k_route_fused), grid,
                                      kRouteThreads, args, smem, stream);
     if (rc != cudaSuccess) return rc;
     ++launches;
     if (n_launches) *n_launches += launches;
+    return cudaGetLastError();
+}
+
+// Largest number of clusters of S CTAs (each with smem bytes of dynamic shared
+// memory) that the current device holds at once, cached per (device, S, smem).
+static int fused_max_clusters(int S, size_t smem) {
+    struct Key { int dev, S; size_t smem; int n; };
+    static std::mutex mu;
+    static Key cache[64];
+    static int n_cache = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < n_cache; ++i)
+        if (cache[i].dev == dev && cache[i].S == S && cache[i].smem == smem) return cache[i].n;
+    if (cudaFuncSetAttribute(k_route_from_x, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+        return 0;
+    if (S > 8 && cudaFuncSetAttribute(k_route_from_x, cudaFuncAttributeNonPortableClusterSizeAllowed,
+                                      1) != cudaSuccess)
+        return 0;
+    int sms = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = static_cast<unsigned>(S);
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(sms / S * S));
+    cfg.blockDim = dim3(kRouteThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(k_route_from_x), &cfg) !=
+        cudaSuccess) {
+        (void)cudaGetLastError();
+        n = 0;
+    }
+    if (n_cache < 64) cache[n_cache++] = {dev, S, smem, n};
+    return n;
+}
+
+FusedRoutePlan fused_route_plan(int T, int H, int E, int P) {
+    FusedRoutePlan p{};
+    p.ok = false;
+    if (T <= 0 || H < 64 || H % 64 != 0 || E < 1 || E > kFusedMaxE || P < 0 || P > kMaxP) return p;
+    p.N = ((E + 15) / 16) * 16;
+    p.m_tiles = (T + 127) / 128;
+    p.KB = H / 64;
+    p.smem = fused_smem_bytes(p.N, P);
+    int dev = 0, sms = 0, max_smem = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+        return p;
+    if (p.smem > static_cast<size_t>(max_smem)) return p;
+    // about one wave of CTAs, at least four k-blocks per CTA, a portable
+    // cluster, and every cluster resident at once (cooperative launch)
+    long long S = (sms + p.m_tiles - 1) / p.m_tiles;
+    if (S > p.KB / 4) S = p.KB / 4;
+    if (S > kRMaxSplit) S = kRMaxSplit;
+    if (S < 1) S = 1;
+    for (; S >= 1; --S)
+        if (fused_max_clusters(static_cast<int>(S), p.smem) >= p.m_tiles) break;
+    if (S < 1) return p;
+    p.S = static_cast<int>(S);
+    p.ok = true;
+    return p;
+}
+
+cudaError_t launch_route_from_x(const void* X, int T, int H, const void* W_r, int E, int k,
+                                int renorm, const int32_t* phi, int P, float* logits,
+                                int32_t* topk_ids, float* alpha, int32_t* offsets,
+                                int32_t* rec_tok, int32_t* rec_route, int32_t* rec_pos,
+                                int32_t* done, int32_t* tickets, int n_tickets, void* ws,
+                                size_t ws_bytes, cudaStream_t stream, int* n_launches,
+                                const ResidualInit* resid_in, int withhold_arrival,
+                                const L2Prefetch* prefetch) {
+    const RouteWorkspace w = route_workspace_layout(T, k, P);
+    if (!ws || w.total > ws_bytes) return cudaErrorInvalidValue;
+    char* base = static_cast<char*>(ws);
+    int* err = reinterpret_cast<int*>(base + w.err_off);
+    int32_t* hist = reinterpret_cast<int32_t*>(base + w.hist_off);
+    int32_t* mblk = reinterpret_cast<int32_t*>(base + w.mblk_off);
+    int32_t* totals = reinterpret_cast<int32_t*>(base + w.tot_off);
+    int* sync = reinterpret_cast<int*>(base + w.sync_off);
+    cudaError_t rc;
+    if (T * k == 0) {
+        rc = cudaMemsetAsync(err, 0, sizeof(int), stream);
+        if (rc == cudaSuccess) rc = cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (P + 2), stream);
+        if (rc == cudaSuccess) rc = cudaMemsetAsync(mblk, 0, sizeof(int32_t) * (P + 2), stream);
+        return rc;
+    }
+    const FusedRoutePlan p = fused_route_plan(T, H, E, P);
+    if (!p.ok) return cudaErrorNotSupported;
+    // boxes no taller than the tensors; the MMA still reads 128 x N rows, the
+    // rows past T or E hold stale data whose results are never used
+    CUtensorMap tm_x, tm_w;
+    const CUtensorMapDataType BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const uint32_t box_x = static_cast<uint32_t>(T < 128 ? T : 128);
+    const uint32_t box_w = static_cast<uint32_t>(E < p.N ? E : p.N);
+    if (encode_tmap_2d(&tm_x, BF, X, static_cast<uint64_t>(H), static_cast<uint64_t>(T),
+                       static_cast<uint64_t>(H) * 2, 64, box_x) != CUDA_SUCCESS ||
+        encode_tmap_2d(&tm_w, BF, W_r, static_cast<uint64_t>(H), static_cast<uint64_t>(E),
+                       static_cast<uint64_t>(H) * 2, 64, box_w) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    rc = cudaMemsetAsync(base + w.err_off, 0, 2 * sizeof(int32_t), stream);
+    if (rc != cudaSuccess) return rc;
+    rc = cudaFuncSetAttribute(k_route_from_x, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(p.smem));
+    if (rc != cudaSuccess) return rc;
+    FusedRouter fr;
+    fr.KB = p.KB;
+    fr.S = p.S;
+    fr.N = p.N;
+    fr.tx_bytes = (box_x + box_w) * 128u;
+    fr.logits = logits;
+    ResidualInit resid{nullptr, 0, nullptr, 0};
+    if (resid_in) resid = *resid_in;
+    L2Prefetch pf{};
+    if (prefetch) pf = *prefetch;
+    for (int r = 0; r < kMaxL2Ranges; ++r)
+        if (pf.base[r] && reinterpret_cast<uintptr_t>(pf.base[r]) % 16 != 0) pf.base[r] = nullptr;
+    int nchunk = w.nchunk;
+    void* args[] = {&tm_x, &tm_w, &fr, &T, &E, &k, &renorm, &phi, &P, &topk_ids, &alpha, &offsets,
+                    &rec_tok, &rec_route, &rec_pos, &hist, &mblk, &totals, &done, &tickets,
+                    &n_tickets, &sync, &err, &nchunk, &resid, &withhold_arrival, &pf};
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute at[2];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = static_cast<unsigned>(p.S);
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    at[1].id = cudaLaunchAttributeCooperative;
+    at[1].val.cooperative = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(p.m_tiles * p.S));
+    cfg.blockDim = dim3(kRouteThreads);
+    cfg.dynamicSmemBytes = p.smem;
+    cfg.stream = stream;
+    cfg.attrs = at;
+    cfg.numAttrs = 2;
+    rc = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(k_route_from_x), args);
+    if (rc != cudaSuccess) return rc;
+    if (n_launches) *n_launches += 1;
     return cudaGetLastError();
 }
 

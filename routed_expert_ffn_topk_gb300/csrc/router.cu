@@ -29,10 +29,9 @@ namespace {
 
 #include "tc_ptx.cuh"
 
-constexpr int kRStages = 4;
+#include "router_tile.cuh"
+
 constexpr int kRThreads = 192;
-constexpr int kRTileA = 128 * 128;  // 128 tokens x 64 bf16
-constexpr int kRMaxSplit = 8;       // portable cluster size
 
 struct RouterArgs {
     float* logits;      // [T][E]
@@ -41,20 +40,8 @@ struct RouterArgs {
     uint32_t tx_bytes;  // bytes one stage's two boxes deliver
 };
 
-__device__ __forceinline__ void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
-                     : "memory");
-}
-__device__ __forceinline__ float ld_cluster_f32(uint32_t local_addr, uint32_t rank) {
-    uint32_t remote;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-    return v;
-}
-
 size_t router_smem_bytes(int N) {
-    return 1024 + static_cast<size_t>(kRStages) * (kRTileA + N * 128) + 8 * (2 * kRStages + 1) + 16;
+    return 1024 + router_ring_bytes(N) + 8 * (2 * kRStages + 1) + 16;
 }
 
 __global__ void __launch_bounds__(kRThreads, 1)
@@ -63,40 +50,34 @@ __global__ void __launch_bounds__(kRThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
-    const int N = a.N;
-    const int tileB = N * 128;
-    const uint32_t sbase = smem_addr(smem);
-    const uint32_t sA = sbase;
-    const uint32_t sB = sbase + kRStages * kRTileA;
-    const uint32_t bar0 = sB + kRStages * tileB;
-    auto full_bar = [&](int s) { return bar0 + 8u * s; };
-    auto empty_bar = [&](int s) { return bar0 + 8u * (kRStages + s); };
-    const uint32_t acc_bar = bar0 + 8u * (2 * kRStages);
-    uint8_t* misc = smem + (bar0 - sbase) + 8 * (2 * kRStages + 1);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
-
     // the fixed-order sum reads the partials of a.S CTAs of one cluster: a
     // launch without that cluster shape returns before any cluster access
     if (cluster_num_ctas() != static_cast<uint32_t>(a.S)) {
         if (threadIdx.x == 0 && a.dev_err) atomicCAS(a.dev_err, kDevErrNone, kDevErrLaunch);
         return;
     }
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    const int m0 = blockIdx.x * 128;
-    const int n0 = blockIdx.y * N;
+    const int N = a.N;
+    const uint32_t sbase = smem_addr(smem);
+    RouterTile rt;
+    rt.sA = sbase;
+    rt.sB = sbase + kRStages * kRTileA;
+    rt.bar0 = sbase + static_cast<uint32_t>(router_ring_bytes(N));
+    rt.part = reinterpret_cast<float*>(smem);
+    rt.m0 = blockIdx.x * 128;
+    rt.n0 = blockIdx.y * N;
+    rt.N = N;
+    rt.tx_bytes = a.tx_bytes;
     const int s = blockIdx.z;
-    const int kb0 = static_cast<int>(static_cast<long long>(s) * a.KB / a.S);
-    const int kb1 = static_cast<int>(static_cast<long long>(s + 1) * a.KB / a.S);
-    const uint32_t tmem_cols = N <= 32 ? 32u : (N <= 64 ? 64u : (N <= 128 ? 128u : 256u));
+    rt.kb0 = static_cast<int>(static_cast<long long>(s) * a.KB / a.S);
+    rt.kb1 = static_cast<int>(static_cast<long long>(s + 1) * a.KB / a.S);
+    uint8_t* misc = smem + router_ring_bytes(N) + 8 * (2 * kRStages + 1);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
+    const int warp = threadIdx.x >> 5;
+    const uint32_t tmem_cols = router_tmem_cols(N);
 
     if (threadIdx.x == 0) {
-        for (int q = 0; q < kRStages; ++q) {
-            mbar_init(full_bar(q), 1);
-            mbar_init(empty_bar(q), 1);
-        }
-        mbar_init(acc_bar, 1);
+        router_tile_init(rt);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -109,80 +90,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-
-    if (warp == 0) {
-        if (lane == 0) {
-            int issued[kRStages];
-            for (int q = 0; q < kRStages; ++q) issued[q] = -1;
-            bool ok = true;
-            for (int kb = kb0, i = 0; kb < kb1; ++kb, ++i) {
-                const int st = i % kRStages;
-                const uint32_t ph = static_cast<uint32_t>(i / kRStages) & 1u;
-                if (!mbar_wait(empty_bar(st), ph ^ 1u, abort_flag, a.dev_err)) {
-                    ok = false;
-                    break;
-                }
-                mbar_arrive_expect_tx(full_bar(st), a.tx_bytes);
-                issued[st] = static_cast<int>(ph);
-                tma_load_2d(sA + st * kRTileA, &tm_x, kb * 64, m0, full_bar(st));
-                tma_load_2d(sB + st * tileB, &tm_w, kb * 64, n0, full_bar(st));
-            }
-            if (!ok)
-                for (int q = 0; q < kRStages; ++q)
-                    if (issued[q] >= 0)
-                        mbar_wait_drain(full_bar(q), static_cast<uint32_t>(issued[q]));
-        }
-        __syncwarp();
-    } else if (warp == 1) {
-        if (lane == 0) {
-            const uint32_t idesc = make_idesc(true, 128, N);
-            bool any = false;
-            for (int kb = kb0, i = 0; kb < kb1; ++kb, ++i) {
-                const int st = i % kRStages;
-                const uint32_t ph = static_cast<uint32_t>(i / kRStages) & 1u;
-                if (!mbar_wait(full_bar(st), ph, abort_flag, a.dev_err)) break;
-                tc_fence_after();
-                const uint64_t adesc = sw128_desc(sA + st * kRTileA);
-                const uint64_t bdesc = sw128_desc(sB + st * tileB);
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    umma_f16(tmem_base, adesc + 2u * kk, bdesc + 2u * kk, idesc, (i | kk) != 0 ? 1u : 0u);
-                any = true;
-                umma_commit(empty_bar(st));
-            }
-            // the accumulator barrier completes once every MMA issued so far
-            // has finished (also after an abort, so TMEM can be freed)
-            if (any) umma_commit(acc_bar);
-            else mbar_arrive(acc_bar);
-        }
-        __syncwarp();
-    } else {
-        // the tile's partial sums into this CTA's shared memory (the stage
-        // buffers are free once every MMA has completed), rows padded by one
-        // float against bank conflicts
-        const int quarter = warp & 3;
-        const int row = quarter * 32 + lane;
-        bool w = true;
-        if (lane == 0) {
-            w = mbar_wait(acc_bar, 0, abort_flag, a.dev_err);
-            // after an abort the MMAs already issued still complete (the MMA
-            // thread always commits this barrier) before TMEM is freed
-            if (!w) mbar_wait_drain(acc_bar, 0);
-        }
-        w = __shfl_sync(0xffffffffu, w, 0);
-        tc_fence_after();
-        if (w && !*abort_flag) {
-            float* part = reinterpret_cast<float*>(smem) + row * (N + 1);
-            for (int c0 = 0; c0 < N; c0 += 32) {
-                uint32_t v[32];
-                tmem_ld32(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + c0, v);
-                tmem_ld_wait();
-#pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    if (c0 + j < N) part[c0 + j] = __uint_as_float(v[j]);
-            }
-        }
-    }
+    router_tile_roles(rt, &tm_x, &tm_w, tmem_base, abort_flag, a.dev_err);
     tc_fence_before();
     __syncthreads();
     cluster_sync_all();  // every chunk's partial is in place
@@ -194,19 +102,10 @@ __global__ void __launch_bounds__(kRThreads, 1)
         const bool ok = !*abort_flag;
         for (int i = threadIdx.x; ok && i < (r1 - r0) * N; i += kRThreads) {
             const int r = r0 + i / N, c = i % N;
-            const int t = m0 + r, e = n0 + c;
+            const int t = rt.m0 + r, e = rt.n0 + c;
             if (t >= a.T || e >= a.E) continue;
             const uint32_t off = sbase + static_cast<uint32_t>((r * (N + 1) + c) * 4);
-            // every partial's load in flight at once, then the sum in ascending chunk order
-            float v[kRMaxSplit];
-#pragma unroll
-            for (int q = 0; q < kRMaxSplit; ++q)
-                if (q < a.S) v[q] = ld_cluster_f32(off, static_cast<uint32_t>(q));
-            float acc = v[0];
-#pragma unroll
-            for (int q = 1; q < kRMaxSplit; ++q)
-                if (q < a.S) acc += v[q];
-            a.logits[static_cast<size_t>(t) * a.E + e] = acc;
+            a.logits[static_cast<size_t>(t) * a.E + e] = sum_cluster_partials(off, a.S);
         }
     }
     cluster_sync_all();  // no CTA leaves while its partial may still be read

@@ -40,6 +40,11 @@ namespace {
 
 enum BankState { kAvailable = 0, kFilling = 1, kReady = 2, kInUse = 3 };
 
+// Gate/up weight bytes of the first resident slots that the route build asks
+// L2 to prefetch (half of L2: the expert kernel's first wave reads about
+// this much, and the rest of L2 keeps the gathered rows, h and Y).
+constexpr size_t kL2PrefetchBytes = size_t(64) << 20;
+
 struct Bank {
     int layer = -1, group = -1;  // contents (valid while layer >= 0)
     bool release_pending = false;
@@ -81,6 +86,7 @@ struct estream_ctx {
     // and the counter regions inside it (for estream_poison_workspace)
     size_t ws_call_off = 0;
     size_t route_ws_bytes = 0;   // the route build's part of the workspace
+    float* logits_buf = nullptr; // [T_max][E]: router logits of a layer call from X (two-launch form)
     size_t n_done = 0, n_sh_done = 0, n_tickets = 0;
     int n_ffn_launch = 0;        // routed expert-kernel launches so far in the current layer call
     std::vector<const float*> shared_scale;    // [L] device pointers into shared buffers
@@ -394,7 +400,7 @@ const char* estream_status_string(estream_status s) {
     return "unknown status";
 }
 
-int estream_version(void) { return 10100; }
+int estream_version(void) { return 10200; }
 
 size_t estream_route_workspace_bytes(int T, int E, int k, int P) {
     if (T < 0 || E < 1 || k < 1 || P < 0 || P > kMaxP) return 0;
@@ -419,6 +425,67 @@ estream_status estream_route_build(const float* logits, int T, int E, int k, int
                                         rec_tok, rec_route, nullptr, nullptr, nullptr, 0, workspace,
                                         workspace_bytes, s, nullptr);
     return rc == cudaSuccess ? ESTREAM_OK : ESTREAM_ERR_CUDA;
+}
+
+// Router logits + route map from X and W_r. One cooperative launch where the
+// fused kernel takes the shape; otherwise the router kernel, then the route
+// build, on the same stream (the router's error goes to the same word, which
+// the route build then keeps).
+static cudaError_t route_from_x_any(const void* X, int T, int H, const void* W_r, int E, int k,
+                                    int renorm, const int32_t* phi, int P, float* logits,
+                                    int32_t* topk_ids, float* alpha, int32_t* offsets,
+                                    int32_t* rec_tok, int32_t* rec_route, int32_t* rec_pos,
+                                    int32_t* done, int32_t* tickets, int n_tickets, void* ws,
+                                    size_t ws_bytes, cudaStream_t s, int* launches,
+                                    const ResidualInit* resid, int withhold, const L2Prefetch* pf,
+                                    int num_sms, bool* fused) {
+    cudaError_t rc = launch_route_from_x(X, T, H, W_r, E, k, renorm, phi, P, logits, topk_ids, alpha,
+                                         offsets, rec_tok, rec_route, rec_pos, done, tickets,
+                                         n_tickets, ws, ws_bytes, s, launches, resid, withhold, pf);
+    if (fused) *fused = rc != cudaErrorNotSupported;
+    if (rc != cudaErrorNotSupported) return rc;
+    (void)cudaGetLastError();
+    int* err = reinterpret_cast<int*>(static_cast<char*>(ws) + route_workspace_layout(T, k, P).err_off);
+    rc = cudaMemsetAsync(err, 0, sizeof(int), s);
+    if (rc != cudaSuccess) return rc;
+    rc = launch_router_logits(X, T, H, W_r, E, logits, router_plan(T, H, E, num_sms), err, s);
+    if (rc != cudaSuccess) return rc;
+    if (launches && T > 0) *launches += 1;
+    return launch_route_build(logits, T, E, k, renorm, phi, P, topk_ids, alpha, offsets, rec_tok,
+                              rec_route, rec_pos, done, tickets, n_tickets, ws, ws_bytes, s, launches,
+                              resid, withhold, pf, /*clear_err=*/false);
+}
+
+estream_status estream_route_build_from_x(const void* X, int T, int H, const void* W_r, int E,
+                                          int k, int renorm, const int32_t* phi, int P,
+                                          float* logits, int32_t* topk_ids, float* alpha,
+                                          int32_t* offsets, int32_t* rec_tok, int32_t* rec_route,
+                                          void* workspace, size_t workspace_bytes,
+                                          void* cuda_stream) {
+    if (T < 0 || E < 1 || E > kMaxE || k < 1 || k > E || k > kMaxK || P < 0 || P > kMaxP ||
+        H < 64 || H % 64 != 0)
+        return ESTREAM_ERR_INVALID_ARG;
+    if (!phi && P != E) return ESTREAM_ERR_INVALID_ARG;
+    if (!offsets || !workspace || !aligned(workspace, 256)) return ESTREAM_ERR_INVALID_ARG;
+    if (T > 0 && (!X || !W_r || !logits || !topk_ids || !alpha || !rec_tok || !rec_route ||
+                  !aligned(X, 16) || !aligned(W_r, 16)))
+        return ESTREAM_ERR_INVALID_ARG;
+    if (static_cast<long long>(T) * k > (1ll << 30)) return ESTREAM_ERR_CAPACITY;
+    if (workspace_bytes < route_workspace_layout(T, k, P).total) return ESTREAM_ERR_CAPACITY;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return ESTREAM_ERR_CUDA;
+    if (!device_supported(dev)) return ESTREAM_ERR_UNSUPPORTED;
+    const cudaError_t rc = route_from_x_any(
+        X, T, H, W_r, E, k, renorm, phi, P, logits, topk_ids, alpha, offsets, rec_tok, rec_route,
+        nullptr, nullptr, nullptr, 0, workspace, workspace_bytes, static_cast<cudaStream_t>(cuda_stream),
+        nullptr, nullptr, 0, nullptr, sms, nullptr);
+    return rc == cudaSuccess ? ESTREAM_OK : ESTREAM_ERR_CUDA;
+}
+
+int estream_route_build_from_x_fused(int T, int H, int E, int P) {
+    return fused_route_plan(T, H, E, P).ok ? 1 : 0;
 }
 
 estream_status estream_workspace_error(void* workspace, void* cuda_stream) {
@@ -598,6 +665,7 @@ estream_status estream_bind_arena(estream_ctx** out, const estream_arena_desc* d
     const size_t o_rroute = take(sizeof(int32_t) * R_cap);
     const size_t o_rpos = take(sizeof(int32_t) * R_cap);
     const size_t o_offs = take(sizeof(int32_t) * (E + 2));
+    const size_t o_lg = take(f32 ? 0 : sizeof(float) * static_cast<size_t>(d->T_max) * E);
     const size_t o_rws = take(route_workspace_layout(d->T_max, d->k_max, E).total);
     const size_t o_done = take(sizeof(int32_t) * ((R_cap + kBM - 1) / kBM + E + 1));
     const size_t o_tick = take(sizeof(int32_t) * (E + 2));
@@ -629,6 +697,7 @@ estream_status estream_bind_arena(estream_ctx** out, const estream_arena_desc* d
         c->rec_route = reinterpret_cast<int32_t*>(c->ws + o_rroute);
         c->rec_pos = reinterpret_cast<int32_t*>(c->ws + o_rpos);
         c->offsets = reinterpret_cast<int32_t*>(c->ws + o_offs);
+        c->logits_buf = f32 ? nullptr : reinterpret_cast<float*>(c->ws + o_lg);
         c->route_ws = c->ws + o_rws;
         c->route_ws_bytes = route_workspace_layout(d->T_max, d->k_max, E).total;
         c->done = reinterpret_cast<int32_t*>(c->ws + o_done);
@@ -990,13 +1059,19 @@ estream_status estream_arena_invalidate(estream_ctx* c) {
 }
 
 // One layer call; with A non-null the route build also initialises Y = A.
+// One layer call; with A non-null the route build also initialises Y = A.
+// Routing input: `logits`, or (logits null) the router weights W_r, whose
+// logits go to logits_out when given.
 static estream_status prefill_impl(estream_ctx* c, int layer, const void* X, const float* logits,
-                                   int T, int k, int renorm, const void* A, float* Y,
-                                   void* cuda_stream) {
+                                   const void* W_r, float* logits_out, int T, int k, int renorm,
+                                   const void* A, float* Y, void* cuda_stream) {
     if (!c) return ESTREAM_ERR_NOT_BOUND;
-    if (layer < 0 || layer >= c->d.L || !X || !logits || !Y || T < 1 || k < 1 || k > c->d.E)
+    if (layer < 0 || layer >= c->d.L || !X || (!logits && !W_r) || !Y || T < 1 || k < 1 ||
+        k > c->d.E)
         return ESTREAM_ERR_INVALID_ARG;
     if (!aligned(X, 16) || !aligned(Y, 16) || (A && !aligned(A, 16))) return ESTREAM_ERR_INVALID_ARG;
+    if (W_r && (c->d.wdtype == ESTREAM_F32 || !aligned(W_r, 16) || !aligned(logits_out, 4)))
+        return ESTREAM_ERR_INVALID_ARG;
     if (!on_bound_device(c)) return ESTREAM_ERR_INVALID_ARG;
     if (T > c->d.T_max || k > c->d.k_max) return ESTREAM_ERR_CAPACITY;
     // this call's routed expert kernels: both tile phases, or (a test of the
@@ -1058,11 +1133,29 @@ static estream_status prefill_impl(estream_ctx* c, int layer, const void* X, con
         TimedScope ts(c, s, kTRoute);
         int launches = 0;
         const ResidualInit ri{A, c->es, Y, H};
-        if (launch_route_build(logits, T, E, k, renorm, c->d_perm + static_cast<size_t>(layer) * E, E,
-                               c->topk_ids, c->alpha, c->offsets, c->rec_tok, c->rec_route,
-                               c->d.deterministic ? c->rec_pos : nullptr, c->done, c->tickets, E + 2,
-                               c->route_ws, c->route_ws_bytes, s, &launches, A ? &ri : nullptr,
-                               c->route_withhold_next ? 1 : 0) != cudaSuccess) {
+        // a resident layer's expert kernel starts with the first slots'
+        // gate/up weights: let L2 fetch them while the route build runs
+        L2Prefetch pf{};
+        if (resident && c->d.wdtype != ESTREAM_F32) {
+            const size_t per_plane = std::min(kL2PrefetchBytes / 2, static_cast<size_t>(E) * c->S_gu);
+            pf.base[0] = c->plane_g;
+            pf.base[1] = c->plane_u;
+            pf.bytes[0] = pf.bytes[1] = per_plane;
+        }
+        const int32_t* phi = c->d_perm + static_cast<size_t>(layer) * E;
+        int32_t* rec_pos = c->d.deterministic ? c->rec_pos : nullptr;
+        const int withhold = c->route_withhold_next ? 1 : 0;
+        const cudaError_t rc =
+            W_r ? route_from_x_any(X, T, H, W_r, E, k, renorm, phi, E,
+                                   logits_out ? logits_out : c->logits_buf, c->topk_ids, c->alpha,
+                                   c->offsets, c->rec_tok, c->rec_route, rec_pos, c->done,
+                                   c->tickets, E + 2, c->route_ws, c->route_ws_bytes, s, &launches,
+                                   A ? &ri : nullptr, withhold, &pf, c->num_sms, nullptr)
+                : launch_route_build(logits, T, E, k, renorm, phi, E, c->topk_ids, c->alpha,
+                                     c->offsets, c->rec_tok, c->rec_route, rec_pos, c->done,
+                                     c->tickets, E + 2, c->route_ws, c->route_ws_bytes, s,
+                                     &launches, A ? &ri : nullptr, withhold, &pf);
+        if (rc != cudaSuccess) {
             drain(c, s);
             return ESTREAM_ERR_CUDA;
         }
@@ -1174,7 +1267,8 @@ static estream_status prefill_impl(estream_ctx* c, int layer, const void* X, con
 estream_status estream_moe_layer_prefill(estream_ctx* c, int layer, const void* X,
                                          const float* logits, int T, int k, int renorm, float* Y,
                                          void* cuda_stream) {
-    return prefill_impl(c, layer, X, logits, T, k, renorm, nullptr, Y, cuda_stream);
+    if (!logits) return c ? ESTREAM_ERR_INVALID_ARG : ESTREAM_ERR_NOT_BOUND;
+    return prefill_impl(c, layer, X, logits, nullptr, nullptr, T, k, renorm, nullptr, Y, cuda_stream);
 }
 
 estream_status estream_moe_layer_prefill_residual(estream_ctx* c, int layer, const void* X,
@@ -1182,7 +1276,17 @@ estream_status estream_moe_layer_prefill_residual(estream_ctx* c, int layer, con
                                                   const void* A, float* Y, void* cuda_stream) {
     if (!c) return ESTREAM_ERR_NOT_BOUND;
     if (!A) return ESTREAM_ERR_INVALID_ARG;
-    return prefill_impl(c, layer, X, logits, T, k, renorm, A, Y, cuda_stream);
+    if (!logits) return ESTREAM_ERR_INVALID_ARG;
+    return prefill_impl(c, layer, X, logits, nullptr, nullptr, T, k, renorm, A, Y, cuda_stream);
+}
+
+estream_status estream_moe_layer_prefill_from_x(estream_ctx* c, int layer, const void* X,
+                                                const void* W_r, int T, int k, int renorm,
+                                                const void* A, float* Y, float* logits_out,
+                                                void* cuda_stream) {
+    if (!c) return ESTREAM_ERR_NOT_BOUND;
+    if (!W_r) return ESTREAM_ERR_INVALID_ARG;
+    return prefill_impl(c, layer, X, nullptr, W_r, logits_out, T, k, renorm, A, Y, cuda_stream);
 }
 
 estream_status estream_set_timing(estream_ctx* c, int on) {

@@ -75,6 +75,10 @@ SIGNATURES = {
     "estream_route_build_noalloc": (_I, [_P, _I, _I, _I, _I, _P, _I, _P, _P, _P, _P, _P, _P]),
     "estream_route_noalloc_error": (_I, [_P]),
     "estream_poison_workspace": (_I, [_P, _P]),
+    "estream_route_build_from_x": (_I, [_P, _I, _I, _P, _I, _I, _I, _P, _I, _P, _P, _P, _P, _P, _P,
+                                        _P, _SZ, _P]),
+    "estream_route_build_from_x_fused": (_I, [_I, _I, _I, _I]),
+    "estream_moe_layer_prefill_from_x": (_I, [_P, _I, _P, _P, _I, _I, _I, _P, _P, _P, _P]),
     "estream_router_workspace_bytes": (_SZ, [_I, _I, _I]),
     "estream_router_logits": (_I, [_P, _I, _I, _P, _I, _P, _P, _SZ, _P]),
     "estream_arena_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
@@ -256,6 +260,54 @@ def router_logits(X: torch.Tensor, W_r: torch.Tensor, logits: torch.Tensor | Non
     return logits
 
 
+def route_build_from_x(X: torch.Tensor, W_r: torch.Tensor, k: int, renorm: bool,
+                       phi: torch.Tensor | None = None, P: int | None = None, out: dict | None = None,
+                       workspace: torch.Tensor | None = None, stream=None) -> dict:
+    """estream_route_build_from_x: router logits X W_r^T and the route map in
+    one call. Returns route_build's dict plus "logits" [T, E] fp32."""
+    if (X.dim() != 2 or W_r.dim() != 2 or X.dtype != torch.bfloat16 or W_r.dtype != torch.bfloat16
+            or W_r.shape[1] != X.shape[1]):
+        raise ValueError("X must be [T, H] and W_r [E, H], both bf16")
+    if not X.is_cuda or W_r.device != X.device:
+        raise ValueError("X and W_r must be on one CUDA device")
+    T, H = X.shape
+    E = W_r.shape[0]
+    P = E if P is None else P
+    dev = X.device
+    R = T * k
+    o = dict(out or {})
+    o.setdefault("logits", torch.empty(T, E, dtype=torch.float32, device=dev))
+    o.setdefault("topk_ids", torch.empty(max(R, 1), dtype=torch.int32, device=dev))
+    o.setdefault("alpha", torch.empty(max(R, 1), dtype=torch.float32, device=dev))
+    o.setdefault("offsets", torch.empty(P + 2, dtype=torch.int32, device=dev))
+    o.setdefault("rec_tok", torch.empty(max(R, 1), dtype=torch.int32, device=dev))
+    o.setdefault("rec_route", torch.empty(max(R, 1), dtype=torch.int32, device=dev))
+    if tuple(o["logits"].shape) != (T, E) or o["logits"].dtype != torch.float32 \
+            or o["logits"].device != dev:
+        raise ValueError(f"logits must be [{T}, {E}] fp32 on X's device")
+    _check_route_args(o["logits"], k, phi, P, o)
+    nbytes = route_workspace_bytes(T, E, k, P)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
+    if workspace.device != dev:
+        raise ValueError(f"workspace must be on {dev}")
+    with _on(X):
+        st = lib().estream_route_build_from_x(
+            _dptr(X), T, H, _dptr(W_r), E, k, int(bool(renorm)), _dptr(phi), P, _dptr(o["logits"]),
+            _dptr(o["topk_ids"]), _dptr(o["alpha"]), _dptr(o["offsets"]), _dptr(o["rec_tok"]),
+            _dptr(o["rec_route"]), _dptr(workspace), workspace.numel() * workspace.element_size(),
+            _stream(stream, dev))
+    _check(st, "estream_route_build_from_x")
+    o["workspace"] = workspace
+    return o
+
+
+def route_build_from_x_fused(T: int, H: int, E: int, P: int | None = None) -> bool:
+    """Whether route_build_from_x runs these sizes as one fused launch on
+    the current device."""
+    return bool(lib().estream_route_build_from_x_fused(T, H, E, E if P is None else P))
+
+
 def route_build_noalloc(logits: torch.Tensor, k: int, renorm: bool, phi: torch.Tensor | None = None,
                         P: int | None = None, out: dict | None = None, stream=None) -> dict:
     """estream_route_build_noalloc: the same outputs as route_build, with the
@@ -376,23 +428,23 @@ def arena_invalidate(ctx) -> None:
     _check(lib().estream_arena_invalidate(ctx), "estream_arena_invalidate")
 
 
-def _check_layer_args(X: torch.Tensor, logits: torch.Tensor, Y: torch.Tensor,
+def _check_layer_args(X: torch.Tensor, logits: torch.Tensor | None, Y: torch.Tensor,
                       A: torch.Tensor | None = None) -> None:
     """Shapes and types the layer call reads and writes through plain
-    pointers: X [T, H] (bf16 or fp32), logits [T, E] fp32, Y [T, H] fp32 and
-    the residual A like X, all on one CUDA device."""
-    if X.dim() != 2 or logits.dim() != 2 or Y.dim() != 2:
+    pointers: X [T, H] (bf16 or fp32), logits [T, E] fp32 (when given), Y
+    [T, H] fp32 and the residual A like X, all on one CUDA device."""
+    if X.dim() != 2 or Y.dim() != 2 or (logits is not None and logits.dim() != 2):
         raise ValueError("X, logits and Y must be 2-d")
     T, H = X.shape
-    if logits.shape[0] != T or tuple(Y.shape) != (T, H):
+    if (logits is not None and logits.shape[0] != T) or tuple(Y.shape) != (T, H):
         raise ValueError(f"logits must be [T, E] and Y [T, H] with T={T}, H={H}")
     if X.dtype not in (torch.bfloat16, torch.float32):
         raise ValueError("X must be bf16 or fp32")
-    if logits.dtype != torch.float32 or Y.dtype != torch.float32:
+    if (logits is not None and logits.dtype != torch.float32) or Y.dtype != torch.float32:
         raise ValueError("logits and Y must be fp32")
     if A is not None and (tuple(A.shape) != (T, H) or A.dtype != X.dtype):
         raise ValueError("the residual must have X's shape and type")
-    tensors = [X, logits, Y] + ([A] if A is not None else [])
+    tensors = [X, Y] + [t for t in (logits, A) if t is not None]
     if any(not t.is_cuda for t in tensors) or len({t.device for t in tensors}) != 1:
         raise ValueError("X, logits, Y (and the residual) must be on one CUDA device")
 
@@ -417,6 +469,26 @@ def moe_layer_prefill_residual(ctx, layer: int, X: torch.Tensor, logits: torch.T
                                                         int(bool(renorm)), _dptr(A), _dptr(Y),
                                                         _stream(stream, X.device)),
                "estream_moe_layer_prefill_residual")
+
+
+def moe_layer_prefill_from_x(ctx, layer: int, X: torch.Tensor, W_r: torch.Tensor, k: int,
+                             renorm: bool, Y: torch.Tensor, A: torch.Tensor | None = None,
+                             logits_out: torch.Tensor | None = None, stream=None) -> None:
+    """Routing from the layer input (router logits, top-k and route map in
+    one launch), then the experts: Y += MoE(X), or Y = A + MoE(X)."""
+    if W_r.dim() != 2 or W_r.dtype != torch.bfloat16 or W_r.shape[1] != X.shape[1] \
+            or W_r.device != X.device:
+        raise ValueError("W_r must be [E, H] bf16 on X's device")
+    T = X.shape[0]
+    E = W_r.shape[0]
+    if logits_out is not None and tuple(logits_out.shape) != (T, E):
+        raise ValueError(f"logits_out must be [{T}, {E}]")
+    _check_layer_args(X, logits_out, Y, A)
+    with _on(X):
+        _check(lib().estream_moe_layer_prefill_from_x(ctx, layer, _dptr(X), _dptr(W_r), T, k,
+                                                      int(bool(renorm)), _dptr(A), _dptr(Y),
+                                                      _dptr(logits_out), _stream(stream, X.device)),
+               "estream_moe_layer_prefill_from_x")
 
 
 def set_timing(ctx, on: bool) -> None:

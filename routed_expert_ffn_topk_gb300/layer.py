@@ -115,6 +115,22 @@ class BoundLayerStack:
         with torch.cuda.device(self.device):
             es.poison_workspace(self.ctx, stream)
 
+    def prefill_from_x(self, layer: int, X: torch.Tensor, W_r: torch.Tensor, Y: torch.Tensor,
+                       k=None, renorm=None, stream=None, residual: torch.Tensor | None = None,
+                       logits_out: torch.Tensor | None = None) -> None:
+        """The layer call with routing from X and the router weights W_r [E, H]
+        (estream_moe_layer_prefill_from_x): Y += MoE(X), or Y = residual +
+        MoE(X); the router logits go to logits_out when given."""
+        cfg = self.cfg
+        if X.dim() != 2 or X.shape[1] != cfg.H or X.dtype != torch.bfloat16 or X.device != self.device:
+            raise ValueError(f"X must be [T, {cfg.H}] bf16 on {self.device}")
+        if W_r.shape[0] != cfg.E:
+            raise ValueError(f"W_r must have {cfg.E} rows")
+        k = cfg.k if k is None else k
+        renorm = cfg.renorm if renorm is None else renorm
+        es.moe_layer_prefill_from_x(self.ctx, layer, X, W_r, k, renorm, Y, A=residual,
+                                    logits_out=logits_out, stream=stream)
+
     def close(self) -> None:
         if getattr(self, "ctx", None):
             with torch.cuda.device(self.device):
