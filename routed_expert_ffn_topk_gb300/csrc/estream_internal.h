@@ -48,17 +48,6 @@ struct ResidualInit {
     int H;
 };
 
-// Weight bytes the route build asks L2 to prefetch while it runs (it is
-// latency-bound and leaves HBM idle): up to kMaxL2Ranges ranges, each split
-// evenly over the route kernel's CTAs and issued as bulk L2 prefetches at its
-// start. Used for the first expert slots' gate/up planes of a resident layer,
-// which the expert kernel's first wave of tiles reads next.
-constexpr int kMaxL2Ranges = 2;
-struct L2Prefetch {
-    const void* base[kMaxL2Ranges];
-    size_t bytes[kMaxL2Ranges];
-};
-
 // Enqueue the full route build (K1). `ws` holds ws_bytes bytes, which must
 // cover route_workspace_layout(T,k,P) (cudaErrorInvalidValue otherwise, before
 // anything is enqueued: a second guard behind every entry point's own check).
@@ -72,12 +61,12 @@ cudaError_t launch_route_build(const float* logits, int T, int E, int k, int ren
                                int32_t* rec_pos, int32_t* done, int32_t* tickets, int n_tickets,
                                void* ws, size_t ws_bytes, cudaStream_t stream, int* n_launches,
                                const ResidualInit* resid = nullptr, int withhold_arrival = 0,
-                               const L2Prefetch* prefetch = nullptr, bool clear_err = true);
+                               bool clear_err = true);
 
 // Router logits fused with the route build: one cooperative launch of
 // clusters from X [T][H] and W_r [E][H] (bf16) to the route map (and, when
 // `logits` is given, the logits [T][E] fp32), with the same outputs, optional
-// residual rows, test hook and L2 prefetch as launch_route_build. Shapes it
+// residual rows and test hook as launch_route_build. Shapes it
 // cannot take (E > 128, H not a multiple of 64, more token tiles than
 // resident clusters) return cudaErrorNotSupported before anything is
 // enqueued; the caller then runs the router and the route build separately.
@@ -93,8 +82,7 @@ cudaError_t launch_route_from_x(const void* X, int T, int H, const void* W_r, in
                                 int32_t* rec_tok, int32_t* rec_route, int32_t* rec_pos,
                                 int32_t* done, int32_t* tickets, int n_tickets, void* ws,
                                 size_t ws_bytes, cudaStream_t stream, int* n_launches,
-                                const ResidualInit* resid = nullptr, int withhold_arrival = 0,
-                                const L2Prefetch* prefetch = nullptr);
+                                const ResidualInit* resid = nullptr, int withhold_arrival = 0);
 
 // Identity route map for the shared experts: n_shared segments of T rows,
 // rec_tok[p] = p mod T, offsets[s] = s*T, mblk[s] = s*ceil(T/kBM); zeroes

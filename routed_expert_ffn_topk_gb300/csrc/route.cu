@@ -434,26 +434,6 @@ __device__ void empty_route_map(int32_t* offsets, int32_t* mblk, int P) {
     }
 }
 
-// This CTA's share of the L2 prefetch ranges: contiguous pieces of at most
-// 256 KB (16-byte granules) handed to the bulk-copy unit, which fetches them
-// into L2 without involving the SM further.
-__device__ void issue_l2_prefetch(const L2Prefetch& pf) {
-    constexpr size_t kPiece = 256 * 1024;
-    const size_t nct = gridDim.x, cta = blockIdx.x;
-    for (int r = 0; r < kMaxL2Ranges; ++r) {
-        const size_t units = pf.bytes[r] / 16;
-        if (!pf.base[r] || units == 0) continue;
-        const size_t u0 = units * cta / nct, u1 = units * (cta + 1) / nct;
-        const char* base = static_cast<const char*>(pf.base[r]);
-        for (size_t off = u0 * 16; off < u1 * 16; off += kPiece) {
-            const size_t n = min(kPiece, u1 * 16 - off);
-            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(base + off),
-                         "r"(static_cast<uint32_t>(n))
-                         : "memory");
-        }
-    }
-}
-
 __global__ void __launch_bounds__(kRouteThreads, 2) k_route_fused(
     const float* __restrict__ logits, int T, int E, int k, int renorm,
     const int32_t* __restrict__ phi, int P, int32_t* __restrict__ topk_ids,
@@ -461,7 +441,7 @@ __global__ void __launch_bounds__(kRouteThreads, 2) k_route_fused(
     int32_t* __restrict__ rec_route, int32_t* __restrict__ rec_pos, int32_t* __restrict__ hist,
     int32_t* __restrict__ mblk, int32_t* __restrict__ totals, int32_t* __restrict__ done,
     int32_t* __restrict__ tickets, int n_tickets, int* __restrict__ sync, int* __restrict__ err,
-    int nchunk, ResidualInit resid, int withhold_arrival, L2Prefetch pf) {
+    int nchunk, ResidualInit resid, int withhold_arrival) {
     extern __shared__ int smem[];
     __shared__ int ok_flag;
     const int R = T * k;
@@ -482,7 +462,6 @@ __global__ void __launch_bounds__(kRouteThreads, 2) k_route_fused(
     int rrow = resid.A ? (cta >= nc ? cta - nc : cta + grid - nc) * kChunkTokens + warp : T;
     bool pre = rrow < T && cta >= nc;
     int staged = pre ? stage_residual_row(rrow, resid, rstage) : 0;
-    if (threadIdx.x == 0) issue_l2_prefetch(pf);
     // 1. router + the chunk's slot counts, one warp per token
     for (int c = blockIdx.x; c < nchunk; c += gridDim.x) {
         for (int x = threadIdx.x; x < nb; x += blockDim.x) smem[x] = 0;
@@ -600,7 +579,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1) k_route_from_x(
     int32_t* __restrict__ rec_tok, int32_t* __restrict__ rec_route, int32_t* __restrict__ rec_pos,
     int32_t* __restrict__ hist, int32_t* __restrict__ mblk, int32_t* __restrict__ totals,
     int32_t* __restrict__ done, int32_t* __restrict__ tickets, int n_tickets, int* __restrict__ sync,
-    int* __restrict__ err, int nchunk, ResidualInit resid, int withhold_arrival, L2Prefetch pf) {
+    int* __restrict__ err, int nchunk, ResidualInit resid, int withhold_arrival) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ int ok_flag;
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -661,17 +640,14 @@ __global__ void __launch_bounds__(kRouteThreads, 1) k_route_from_x(
     // 1. logits tile on the tensor cores; beside it, the residual rows
     if (warp < 6) {
         router_tile_roles(rt, &tm_x, &tm_w, tmem_base, abort_flag, err);
-    } else {
-        if (warp == 6 && lane == 0) issue_l2_prefetch(pf);
-        if (resid.A) {
-            const int rows_per = (128 + S - 1) / S;
-            const int r0 = rt.m0 + s * rows_per;
-            const int r1 = min(T, min(rt.m0 + 128, r0 + rows_per));
-            const int row_bytes = resid.H * resid.elem_bytes;
-            for (int t = r0 + (warp - 6); t < r1; t += kRouteThreads / 32 - 6)
-                widen_residual(resid, t, static_cast<const char*>(resid.A) + static_cast<size_t>(t) * row_bytes,
-                               0, row_bytes);
-        }
+    } else if (resid.A) {
+        const int rows_per = (128 + S - 1) / S;
+        const int r0 = rt.m0 + s * rows_per;
+        const int r1 = min(T, min(rt.m0 + 128, r0 + rows_per));
+        const int row_bytes = resid.H * resid.elem_bytes;
+        for (int t = r0 + (warp - 6); t < r1; t += kRouteThreads / 32 - 6)
+            widen_residual(resid, t, static_cast<const char*>(resid.A) + static_cast<size_t>(t) * row_bytes,
+                           0, row_bytes);
     }
     tc_fence_before();
     __syncthreads();
@@ -838,7 +814,7 @@ cudaError_t launch_route_build(const float* logits, int T, int E, int k, int ren
                                int32_t* rec_pos, int32_t* done, int32_t* tickets, int n_tickets,
                                void* ws, size_t ws_bytes, cudaStream_t stream, int* n_launches,
                                const ResidualInit* resid_in, int withhold_arrival,
-                               const L2Prefetch* prefetch, bool clear_err) {
+                               bool clear_err) {
     const RouteWorkspace w = route_workspace_layout(T, k, P);
     if (!ws || w.total > ws_bytes) return cudaErrorInvalidValue;
     char* base = static_cast<char*>(ws);
@@ -865,10 +841,6 @@ cudaError_t launch_route_build(const float* logits, int T, int E, int k, int ren
     int* sync = reinterpret_cast<int*>(base + w.sync_off);
     ResidualInit resid{nullptr, 0, nullptr, 0};
     if (resid_in) resid = *resid_in;
-    L2Prefetch pf{};
-    if (prefetch) pf = *prefetch;
-    for (int r = 0; r < kMaxL2Ranges; ++r)  // bulk prefetches move 16-byte granules
-        if (pf.base[r] && reinterpret_cast<uintptr_t>(pf.base[r]) % 16 != 0) pf.base[r] = nullptr;
     const int co_resident = route_co_resident();
     if (co_resident <= 0) return cudaErrorLaunchOutOfResources;
     // with a residual, up to as many CTAs again for its rows
@@ -877,7 +849,7 @@ cudaError_t launch_route_build(const float* logits, int T, int E, int k, int ren
     void* args[] = {&logits, &T, &E, &k, &renorm, &phi, &P, &topk_ids, &alpha, &offsets,
                     &rec_tok, &rec_route, &rec_pos, &hist, &mblk, &totals, &done, &tickets,
                     &n_tickets, &sync, &err, const_cast<int*>(&w.nchunk), &resid,
-                    &withhold_arrival, &pf};
+                    &withhold_arrival};
     rc = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(k_route_fused), grid,
                                      kRouteThreads, args, smem, stream);
     if (rc != cudaSuccess) return rc;
@@ -961,8 +933,7 @@ cudaError_t launch_route_from_x(const void* X, int T, int H, const void* W_r, in
                                 int32_t* rec_tok, int32_t* rec_route, int32_t* rec_pos,
                                 int32_t* done, int32_t* tickets, int n_tickets, void* ws,
                                 size_t ws_bytes, cudaStream_t stream, int* n_launches,
-                                const ResidualInit* resid_in, int withhold_arrival,
-                                const L2Prefetch* prefetch) {
+                                const ResidualInit* resid_in, int withhold_arrival) {
     const RouteWorkspace w = route_workspace_layout(T, k, P);
     if (!ws || w.total > ws_bytes) return cudaErrorInvalidValue;
     char* base = static_cast<char*>(ws);
@@ -1004,14 +975,10 @@ cudaError_t launch_route_from_x(const void* X, int T, int H, const void* W_r, in
     fr.logits = logits;
     ResidualInit resid{nullptr, 0, nullptr, 0};
     if (resid_in) resid = *resid_in;
-    L2Prefetch pf{};
-    if (prefetch) pf = *prefetch;
-    for (int r = 0; r < kMaxL2Ranges; ++r)
-        if (pf.base[r] && reinterpret_cast<uintptr_t>(pf.base[r]) % 16 != 0) pf.base[r] = nullptr;
     int nchunk = w.nchunk;
     void* args[] = {&tm_x, &tm_w, &fr, &T, &E, &k, &renorm, &phi, &P, &topk_ids, &alpha, &offsets,
                     &rec_tok, &rec_route, &rec_pos, &hist, &mblk, &totals, &done, &tickets,
-                    &n_tickets, &sync, &err, &nchunk, &resid, &withhold_arrival, &pf};
+                    &n_tickets, &sync, &err, &nchunk, &resid, &withhold_arrival};
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute at[2];
     at[0].id = cudaLaunchAttributeClusterDimension;

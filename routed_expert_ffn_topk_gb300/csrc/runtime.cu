@@ -40,11 +40,6 @@ namespace {
 
 enum BankState { kAvailable = 0, kFilling = 1, kReady = 2, kInUse = 3 };
 
-// Gate/up weight bytes of the first resident slots that the route build asks
-// L2 to prefetch (half of L2: the expert kernel's first wave reads about
-// this much, and the rest of L2 keeps the gathered rows, h and Y).
-constexpr size_t kL2PrefetchBytes = size_t(64) << 20;
-
 struct Bank {
     int layer = -1, group = -1;  // contents (valid while layer >= 0)
     bool release_pending = false;
@@ -437,11 +432,11 @@ static cudaError_t route_from_x_any(const void* X, int T, int H, const void* W_r
                                     int32_t* rec_tok, int32_t* rec_route, int32_t* rec_pos,
                                     int32_t* done, int32_t* tickets, int n_tickets, void* ws,
                                     size_t ws_bytes, cudaStream_t s, int* launches,
-                                    const ResidualInit* resid, int withhold, const L2Prefetch* pf,
-                                    int num_sms, bool* fused) {
+                                    const ResidualInit* resid, int withhold, int num_sms,
+                                    bool* fused) {
     cudaError_t rc = launch_route_from_x(X, T, H, W_r, E, k, renorm, phi, P, logits, topk_ids, alpha,
                                          offsets, rec_tok, rec_route, rec_pos, done, tickets,
-                                         n_tickets, ws, ws_bytes, s, launches, resid, withhold, pf);
+                                         n_tickets, ws, ws_bytes, s, launches, resid, withhold);
     if (fused) *fused = rc != cudaErrorNotSupported;
     if (rc != cudaErrorNotSupported) return rc;
     (void)cudaGetLastError();
@@ -453,7 +448,7 @@ static cudaError_t route_from_x_any(const void* X, int T, int H, const void* W_r
     if (launches && T > 0) *launches += 1;
     return launch_route_build(logits, T, E, k, renorm, phi, P, topk_ids, alpha, offsets, rec_tok,
                               rec_route, rec_pos, done, tickets, n_tickets, ws, ws_bytes, s, launches,
-                              resid, withhold, pf, /*clear_err=*/false);
+                              resid, withhold, /*clear_err=*/false);
 }
 
 estream_status estream_route_build_from_x(const void* X, int T, int H, const void* W_r, int E,
@@ -480,7 +475,7 @@ estream_status estream_route_build_from_x(const void* X, int T, int H, const voi
     const cudaError_t rc = route_from_x_any(
         X, T, H, W_r, E, k, renorm, phi, P, logits, topk_ids, alpha, offsets, rec_tok, rec_route,
         nullptr, nullptr, nullptr, 0, workspace, workspace_bytes, static_cast<cudaStream_t>(cuda_stream),
-        nullptr, nullptr, 0, nullptr, sms, nullptr);
+        nullptr, nullptr, 0, sms, nullptr);
     return rc == cudaSuccess ? ESTREAM_OK : ESTREAM_ERR_CUDA;
 }
 
@@ -1133,15 +1128,6 @@ static estream_status prefill_impl(estream_ctx* c, int layer, const void* X, con
         TimedScope ts(c, s, kTRoute);
         int launches = 0;
         const ResidualInit ri{A, c->es, Y, H};
-        // a resident layer's expert kernel starts with the first slots'
-        // gate/up weights: let L2 fetch them while the route build runs
-        L2Prefetch pf{};
-        if (resident && c->d.wdtype != ESTREAM_F32) {
-            const size_t per_plane = std::min(kL2PrefetchBytes / 2, static_cast<size_t>(E) * c->S_gu);
-            pf.base[0] = c->plane_g;
-            pf.base[1] = c->plane_u;
-            pf.bytes[0] = pf.bytes[1] = per_plane;
-        }
         const int32_t* phi = c->d_perm + static_cast<size_t>(layer) * E;
         int32_t* rec_pos = c->d.deterministic ? c->rec_pos : nullptr;
         const int withhold = c->route_withhold_next ? 1 : 0;
@@ -1150,11 +1136,11 @@ static estream_status prefill_impl(estream_ctx* c, int layer, const void* X, con
                                    logits_out ? logits_out : c->logits_buf, c->topk_ids, c->alpha,
                                    c->offsets, c->rec_tok, c->rec_route, rec_pos, c->done,
                                    c->tickets, E + 2, c->route_ws, c->route_ws_bytes, s, &launches,
-                                   A ? &ri : nullptr, withhold, &pf, c->num_sms, nullptr)
+                                   A ? &ri : nullptr, withhold, c->num_sms, nullptr)
                 : launch_route_build(logits, T, E, k, renorm, phi, E, c->topk_ids, c->alpha,
                                      c->offsets, c->rec_tok, c->rec_route, rec_pos, c->done,
                                      c->tickets, E + 2, c->route_ws, c->route_ws_bytes, s,
-                                     &launches, A ? &ri : nullptr, withhold, &pf);
+                                     &launches, A ? &ri : nullptr, withhold);
         if (rc != cudaSuccess) {
             drain(c, s);
             return ESTREAM_ERR_CUDA;
