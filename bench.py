@@ -226,7 +226,7 @@ def oracle_tokens_per_s(cfg, wl, target_s=10.0, max_tokens=None):
 # GPU arm
 # --------------------------------------------------------------------------
 
-def roofline_of(cfg, stats, steps, n_active, peaks):
+def roofline_of(cfg, stats, steps, n_active, peaks, form="auto"):
     """Roofline of the routed fused expert kernel from the library's CUDA-event
     times (launching stream): algorithmic bytes (active experts' weights + X
     once + Y read and written) or FLOPs (6*H*F per route) per launch over the
@@ -245,7 +245,8 @@ def roofline_of(cfg, stats, steps, n_active, peaks):
     per_launch_bytes = ffn_b / launches_per_step
     per_launch_flops = ffn_f / launches_per_step
     ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
-    pair = cfg.T * cfg.k >= es.PAIR_MIN_ROWS * cfg.E   # the library's automatic form
+    pair = form == "pair" or (form == "auto" and   # the library's automatic choice
+                              cfg.T * cfg.k >= es.PAIR_MIN_ROWS * cfg.E)
     kname = ("k_expert_ffn_pair (CTA pairs, 256-record tiles" if pair else
              "k_expert_ffn (128-record tiles") + ": gather + gate/up + SwiGLU + down + scatter)"
     if ffn_f / ffn_b < ridge:
@@ -305,7 +306,9 @@ def measure_config(args, cfg, wl, dev, flush, peaks, world, rank):
     Y = [torch.empty(cfg.T, cfg.H, dtype=torch.float32, device=dev) for _ in range(L)]
     one = cfg.__class__(**{**cfg.__dict__, "layers": 1})
     # one resident arena per layer (every expert of every layer in HBM)
-    stacks = [BoundLayerStack(W.Workload(one, [wl.logits[l]], wl.X, [wl.layers[l]]), mode="resident")
+    form = {"auto": es.FFN_AUTO, "single": es.FFN_SINGLE, "pair": es.FFN_PAIR}[args.ffn_form]
+    stacks = [BoundLayerStack(W.Workload(one, [wl.logits[l]], wl.X, [wl.layers[l]]), mode="resident",
+                              ffn_form=form)
               for l in range(L)]
 
     def make_step(X_in, lg_in, Y_out):
@@ -386,7 +389,7 @@ def measure_config(args, cfg, wl, dev, flush, peaks, world, rank):
     gpu_launches = stats["launches"] + (L - 1) * args.steps   # + the bf16 casts between layers
 
     n_active = active_experts(cfg, wl.logits)
-    roof, kernels = roofline_of(cfg, stats, args.steps, n_active, peaks)
+    roof, kernels = roofline_of(cfg, stats, args.steps, n_active, peaks, args.ffn_form)
     flops_step = cfg.flops_per_layer() * L
     gemm_ms = (stats["ms_ffn"] + stats["ms_shared"]) / args.steps
     tflops = flops_step / (ms_per_step / 1e3) / 1e12
@@ -1143,6 +1146,8 @@ def main(argv=None):
     ap.add_argument("--no-q4", action="store_true", help="skip the 4-bit-expert measurement")
     ap.add_argument("--no-router", action="store_true", help="skip the router-logits measurement")
     ap.add_argument("--no-graph", action="store_true", help="time eager launches, not a CUDA-graph replay")
+    ap.add_argument("--ffn-form", default="auto", choices=["auto", "single", "pair"],
+                    help="form of the fused expert kernel in the resident step (default: the library's choice)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--pipeline-study", action="store_true",
                     help="also measure the loading schedules and the (G, B) auto-configuration")

@@ -1282,13 +1282,22 @@ __device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
         : "memory");
 }
 
+// A pair tile covers 256 records (M = 256: 128 per CTA), except the last one
+// of a segment whose remainder fits 128 records: that one is a half tile
+// (M = 128: 64 records per CTA), which costs half the MMA time -- so a
+// segment pads to a multiple of 128 records, not 256. In a half tile the
+// accumulator rows land in TMEM lanes 0-63 of each CTA, read by the epilogue
+// warps of quarters 0 and 1; the other quarters hold no valid rows.
 struct PairTile {
-    int seg;    // segment index relative to seg_begin
-    int pm;     // pair m-block inside the segment
-    int nb;     // n-block
-    int row0;   // first record of this CTA's half
-    int rows;   // valid records in this CTA's half (0..kBM)
-    int rows1;  // valid records in rank 1's half (0..kBM)
+    int seg;     // segment index relative to seg_begin
+    int pm;      // pair m-block inside the segment
+    int nb;      // n-block
+    int row0;    // first record of this CTA's part
+    int rows;    // valid records in this CTA's part (0..kBM, 0..kBM/2 in a half tile)
+    int rows1;   // valid records in rank 1's part
+    bool half;   // M = 128 tile
+    int cnt;     // m-block counter of this CTA's h rows, relative to the segment's first
+    int npub;    // CTAs whose epilogues publish on that counter per gate/up tile
 };
 
 __device__ __forceinline__ PairTile decode_pair(int t, const int* table, int seg_count, int NB,
@@ -1308,9 +1317,16 @@ __device__ __forceinline__ PairTile decode_pair(int t, const int* table, int seg
     const int s_hi = offsets[seg_begin + lo + 1];
     const int pr0 = s_lo + ti.pm * kPairRows;
     const int tot = min(kPairRows, s_hi - pr0);
-    ti.row0 = pr0 + kBM * rank;
-    ti.rows = max(0, min(kBM, tot - kBM * rank));
-    ti.rows1 = max(0, min(kBM, tot - kBM));
+    ti.half = tot <= kBM;
+    // records [pr0, pr0 + tot) are the single m-blocks 2 pm (and 2 pm + 1):
+    // in a full tile rank r's rows are m-block 2 pm + r with its own counter;
+    // a half tile is one m-block whose counter both ranks publish on
+    const int part = ti.half ? kBM / 2 : kBM;
+    ti.row0 = pr0 + part * rank;
+    ti.rows = max(0, min(part, tot - part * rank));
+    ti.rows1 = max(0, min(part, tot - part));
+    ti.cnt = 2 * ti.pm + (ti.half ? 0 : rank);
+    ti.npub = ti.half ? 1 + (tot > part ? 1 : 0) : 1;
     return ti;
 }
 
@@ -1444,12 +1460,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (load_h) {
                 // this half's h rows are complete once every epilogue warp of
                 // every gate/up n-block of its m-block has published
-                const int* cnt = a.done + seg.mblk[seg.seg_begin + ti.seg] + 2 * ti.pm +
-                                 static_cast<int>(rank);
+                const int* cnt = a.done + seg.mblk[seg.seg_begin + ti.seg] + ti.cnt;
+                const int target = ti.npub * done_target;
                 bool w = true;
-                if (lane == 0 && ld_acquire(cnt) < done_target) {
+                if (lane == 0 && ld_acquire(cnt) < target) {
                     const uint64_t t0 = global_ns();
-                    while (ld_acquire(cnt) < done_target) {
+                    while (ld_acquire(cnt) < target) {
                         if (*abort_flag) {
                             w = false;
                             break;
@@ -1604,6 +1620,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0 && rank == 0) {
             const uint32_t idesc_gu = make_idesc(true, kPairRows, 256);   // bf16 x bf16
             const uint32_t idesc_dn = make_idesc(false, kPairRows, 256);  // fp16 x fp16
+            const uint32_t idesc_gu_half = make_idesc(true, kBM, 256);    // half tiles: M = 128
+            const uint32_t idesc_dn_half = make_idesc(false, kBM, 256);
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
@@ -1613,7 +1631,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int it = 0, t; ok && (t = tile_of(pair, n_pairs, TA, TB, KBA, KBB, it)) >= 0; ++it) {
                 const bool gu = t < TA;
                 const int num_kb = gu ? KBA : KBB;
-                const uint32_t idesc = gu ? idesc_gu : idesc_dn;
+                const PairTile ti = decode_pair(gu ? t : t - TA, table, seg.seg_count, gu ? NBA : NBB,
+                                                seg.offsets, seg.seg_begin, 0);
+                const uint32_t idesc = gu ? (ti.half ? idesc_gu_half : idesc_gu)
+                                          : (ti.half ? idesc_dn_half : idesc_dn);
                 if (!mbar_wait_cl(acce_bar(acc), acc_phase ^ 1u, abort_flag, a.dev_err)) {
                     ok = false;
                     break;
@@ -1679,9 +1700,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __threadfence();
                 __syncwarp();
                 if (lane == 0 && (a.phases & 2) && ti.rows > 0)
-                    red_release_add(a.done + seg.mblk[seg.seg_begin + ti.seg] + 2 * ti.pm +
-                                        static_cast<int>(rank),
-                                    1);
+                    red_release_add(a.done + seg.mblk[seg.seg_begin + ti.seg] + ti.cnt, 1);
             } else {
                 float al = 0.0f;
                 int tok = 0;
