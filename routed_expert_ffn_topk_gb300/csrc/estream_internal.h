@@ -122,10 +122,13 @@ cudaError_t launch_expert_ffn(const CUtensorMap* tm_wg, const CUtensorMap* tm_wu
                               int F, int phases, int* dev_err, int num_sms, cudaStream_t stream);
 
 // The same operator on CTA pairs (clusters of two, tcgen05.mma.cta_group::2,
-// 256-record pair tiles); tm_wd_half maps the down planes with 64 x 128
-// boxes (each CTA loads half of a 256-row W_d box).
+// 256-record pair tiles, and 128-record half tiles for segment remainders);
+// tm_wd_half maps the down planes with 64 x 128 boxes (each CTA loads half of
+// a 256-row W_d box); tm_wg64 / tm_wu64 map the gate / up planes with 64 x 64
+// boxes (a half tile's CTA loads 64 gate and 64 up rows of an n-block).
 cudaError_t launch_expert_ffn_pair(const CUtensorMap* tm_wg, const CUtensorMap* tm_wu,
                                    const CUtensorMap* tm_wd_half, const CUtensorMap* tm_h,
+                                   const CUtensorMap* tm_wg64, const CUtensorMap* tm_wu64,
                                    const GemmSegments& seg, const void* X, void* h, float* Y,
                                    float* out_rows, int* done, int H, int F, int phases,
                                    int* dev_err, cudaStream_t stream);

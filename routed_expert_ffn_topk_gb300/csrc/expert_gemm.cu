@@ -280,23 +280,26 @@ __device__ __forceinline__ T* row_of_step(T* my_row, int i, int lane) {
 }
 
 // Gate/up epilogue through the stage: h = fp16(SiLU(g) u) of this lane's
-// record goes to dst_row[0 .. 128) (null for a padding record), 64 columns
-// (128 bytes) per pass.
+// record goes to dst_row[0 .. 64 n_halves) (null for a padding record), 64
+// columns (128 bytes) per pass. The gate value of h column j is accumulator
+// column j and the up value column u_off + j (u_off = 128 for a full tile's
+// 128 columns; 64 for the 64 columns a lane holds in a half pair tile).
 __device__ __forceinline__ void epilogue_gate_up_staged(uint32_t tacc, __half* dst_row,
-                                                        uint32_t stg, int lane, int* dev_err) {
+                                                        uint32_t stg, int lane, int* dev_err,
+                                                        int n_halves = 2, uint32_t u_off = 128) {
     bool in_range = true;
     __half* dst[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) dst[i] = row_of_step(dst_row, i, lane);
     const int j = lane & 7;
 #pragma unroll 1
-    for (int half = 0; half < 2; ++half) {
+    for (int half = 0; half < n_halves; ++half) {
 #pragma unroll 1
         for (int c2 = 0; c2 < 2; ++c2) {
             const int c = 2 * half + c2;
             uint32_t g[32], u[32];
             tmem_ld32(tacc + c * 32, g);
-            tmem_ld32(tacc + 128 + c * 32, u);
+            tmem_ld32(tacc + u_off + c * 32, u);
             tmem_ld_wait();
             uint32_t packed[16];
 #pragma unroll
@@ -323,18 +326,20 @@ __device__ __forceinline__ void epilogue_gate_up_staged(uint32_t tacc, __half* d
     if (dst_row && !in_range) record_error(dev_err, kDevErrRange);
 }
 
-// Down epilogue through the stage: the 256 accumulator columns of this
-// lane's record times `al` are added into dst_row[0 .. 256) with vector
+// Down epilogue through the stage: the first 32 n_chunks accumulator columns
+// of this lane's record (256 in a full tile, the 128 a lane holds in a half
+// pair tile) times `al` are added into dst_row[0 .. 32 n_chunks) with vector
 // reductions (reduce) or stored there (the scaled-row buffer of the
 // deterministic mode); dst_row is null for a padding record.
 __device__ __forceinline__ void epilogue_down_staged(uint32_t tacc, float al, float* dst_row,
-                                                     bool reduce, uint32_t stg, int lane) {
+                                                     bool reduce, uint32_t stg, int lane,
+                                                     int n_chunks = 8) {
     float* dst[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) dst[i] = row_of_step(dst_row, i, lane);
     const int j = lane & 7;
 #pragma unroll 1
-    for (int c = 0; c < 8; ++c) {
+    for (int c = 0; c < n_chunks; ++c) {
         uint32_t v[32];
         tmem_ld32(tacc + c * 32, v);
         tmem_ld_wait();
@@ -1334,7 +1339,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     k_expert_ffn_pair(const __grid_constant__ CUtensorMap tm_wg,
                       const __grid_constant__ CUtensorMap tm_wu,
                       const __grid_constant__ CUtensorMap tm_wd,
-                      const __grid_constant__ CUtensorMap tm_h, const FfnArgs a) {
+                      const __grid_constant__ CUtensorMap tm_h,
+                      const __grid_constant__ CUtensorMap tm_wg64,
+                      const __grid_constant__ CUtensorMap tm_wu64, const FfnArgs a) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ int warp_total[kThreads / 32];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -1497,7 +1504,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) {
                     if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), tx);
                     const uint32_t lbar = map_rank(full_bar(stage), 0);
-                    if (only_reader)
+                    if (gu && ti.half) {
+                        // half tile: CTA r's B half = gate rows [64 r, 64 r + 64) of the
+                        // n-block, then up rows [64 r, 64 r + 64) (8 KB each)
+                        const int r64 = brow0 + kb * brow_step + 64 * static_cast<int>(rank);
+                        const uint32_t dst = sB + stage * kPHalf;
+                        if (only_reader) {
+                            tma_load_2d_pair_hint(dst, &tm_wg64, 0, r64, lbar, policy_evict_first());
+                            tma_load_2d_pair_hint(dst + kPHalf / 2, &tm_wu64, 0, r64, lbar,
+                                                  policy_evict_first());
+                        } else {
+                            tma_load_2d_pair(dst, &tm_wg64, 0, r64, lbar);
+                            tma_load_2d_pair(dst + kPHalf / 2, &tm_wu64, 0, r64, lbar);
+                        }
+                    } else if (only_reader)
                         tma_load_2d_pair_hint(sB + stage * kPHalf, tm_b, 0, brow0 + kb * brow_step,
                                               lbar, policy_evict_first());
                     else
@@ -1689,13 +1709,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             w = __shfl_sync(0xffffffffu, w, 0);
             if (!w) break;
             tc_fence_after();
-            const bool valid = row < ti.rows;
-            const int p = ti.row0 + row;
+            // A half tile's 64 rows per CTA fill TMEM lanes 0-63 with accumulator
+            // columns 0-127 and lanes 64-127 with columns 128-255 of the same
+            // rows: quarters q and q + 2 hold one row range, different columns.
+            const int trow = ti.half ? (quarter & 1) * 32 + lane : row;
+            const int cpart = ti.half ? quarter >> 1 : 0;   // column half of a half tile
+            const bool valid = trow < ti.rows;
+            const int p = ti.row0 + trow;
             const uint32_t tacc = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                   static_cast<uint32_t>(acc * kAccCols);
             if (gu) {
-                __half* dst = a.h + static_cast<size_t>(p) * F + static_cast<size_t>(ti.nb) * 128;
-                epilogue_gate_up_staged(tacc, valid ? dst : nullptr, stg, lane, a.dev_err);
+                // half tiles: the B half of each CTA is 64 gate rows then 64 up
+                // rows, so a lane holds g in columns 0-63 and u in 64-127 of h
+                // columns 64 cpart .. 64 cpart + 63 of the n-block
+                __half* dst = a.h + static_cast<size_t>(p) * F + static_cast<size_t>(ti.nb) * 128 +
+                              64 * cpart;
+                if (ti.half)
+                    epilogue_gate_up_staged(tacc, valid ? dst : nullptr, stg, lane, a.dev_err, 1, 64);
+                else
+                    epilogue_gate_up_staged(tacc, valid ? dst : nullptr, stg, lane, a.dev_err);
                 fence_proxy_async_global();
                 __threadfence();
                 __syncwarp();
@@ -1711,8 +1743,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 float* dst = a.out_rows ? a.out_rows + static_cast<size_t>(p) * H
                                         : a.Y + static_cast<size_t>(tok) * H;
-                epilogue_down_staged(tacc, al, valid ? dst + ti.nb * 256 : nullptr, !a.out_rows, stg,
-                                     lane);
+                epilogue_down_staged(tacc, al, valid ? dst + ti.nb * 256 + 128 * cpart : nullptr,
+                                     !a.out_rows, stg, lane, ti.half ? 4 : 8);
             }
             tc_fence_before();
             __syncwarp();
@@ -1832,6 +1864,7 @@ static int max_pairs(int device) {
 
 cudaError_t launch_expert_ffn_pair(const CUtensorMap* tm_wg, const CUtensorMap* tm_wu,
                                    const CUtensorMap* tm_wd_half, const CUtensorMap* tm_h,
+                                   const CUtensorMap* tm_wg64, const CUtensorMap* tm_wu64,
                                    const GemmSegments& seg, const void* X, void* h, float* Y,
                                    float* out_rows, int* done, int H, int F, int phases,
                                    int* dev_err, cudaStream_t stream) {
@@ -1861,7 +1894,8 @@ cudaError_t launch_expert_ffn_pair(const CUtensorMap* tm_wg, const CUtensorMap* 
     args.F = F;
     args.phases = phases;
     void* kargs[] = {const_cast<CUtensorMap*>(tm_wg), const_cast<CUtensorMap*>(tm_wu),
-                     const_cast<CUtensorMap*>(tm_wd_half), const_cast<CUtensorMap*>(tm_h), &args};
+                     const_cast<CUtensorMap*>(tm_wd_half), const_cast<CUtensorMap*>(tm_h),
+                     const_cast<CUtensorMap*>(tm_wg64), const_cast<CUtensorMap*>(tm_wu64), &args};
     // clusters of two CTAs; cooperative, so every pair is resident and a down
     // tile may wait for gate/up tiles that other pairs own
     cudaLaunchConfig_t cfg = {};

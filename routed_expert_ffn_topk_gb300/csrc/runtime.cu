@@ -65,7 +65,8 @@ struct estream_ctx {
     std::vector<const void*> shared_dev;
     char *plane_g = nullptr, *plane_u = nullptr, *plane_d = nullptr;
     CUtensorMap tm_wg{}, tm_wu{}, tm_wd{}, tm_wd_half{}, tm_h{}, tm_hs{};
-    std::vector<CUtensorMap> tm_sg, tm_su, tm_sd, tm_sd_half;
+    CUtensorMap tm_wg64{}, tm_wu64{};   // 64-row boxes of the gate / up planes (half pair tiles)
+    std::vector<CUtensorMap> tm_sg, tm_su, tm_sd, tm_sd_half, tm_sg64, tm_su64;
 
     // library-owned device workspace
     char* ws = nullptr;
@@ -766,6 +767,10 @@ estream_status estream_bind_arena(estream_ctx** out, const estream_arena_desc* d
                                             256) == CUDA_SUCCESS;
             tm_ok = tm_ok && encode_tmap_2d(&c->tm_wd_half, HF, c->plane_d, 64, plane_rows, 128,
                                             64, 128) == CUDA_SUCCESS;
+            tm_ok = tm_ok && encode_tmap_2d(&c->tm_wg64, BF, c->plane_g, 64, plane_rows, 128, 64,
+                                            64) == CUDA_SUCCESS;
+            tm_ok = tm_ok && encode_tmap_2d(&c->tm_wu64, BF, c->plane_u, 64, plane_rows, 128, 64,
+                                            64) == CUDA_SUCCESS;
         }
         if (!f32) {
             tm_ok = tm_ok && encode_tmap_2d(&c->tm_h, HF, c->h, d->F, static_cast<uint64_t>(R_cap),
@@ -783,6 +788,8 @@ estream_status estream_bind_arena(estream_ctx** out, const estream_arena_desc* d
                 c->tm_su.resize(d->L);
                 c->tm_sd.resize(d->L);
                 c->tm_sd_half.resize(d->L);
+                c->tm_sg64.resize(d->L);
+                c->tm_su64.resize(d->L);
                 const size_t sp = static_cast<size_t>(d->n_shared) * Fs * d->H * 2;
                 for (int l = 0; l < d->L && tm_ok; ++l) {
                     const char* base = static_cast<const char*>(c->shared_dev[l]);
@@ -795,6 +802,10 @@ estream_status estream_bind_arena(estream_ctx** out, const estream_arena_desc* d
                                                     64, 256) == CUDA_SUCCESS;
                     tm_ok = tm_ok && encode_tmap_2d(&c->tm_sd_half[l], HF, base + 2 * sp, 64,
                                                     srows, 128, 64, 128) == CUDA_SUCCESS;
+                    tm_ok = tm_ok && encode_tmap_2d(&c->tm_sg64[l], BF, base, 64, srows, 128, 64,
+                                                    64) == CUDA_SUCCESS;
+                    tm_ok = tm_ok && encode_tmap_2d(&c->tm_su64[l], BF, base + sp, 64, srows, 128,
+                                                    64, 64) == CUDA_SUCCESS;
                 }
             }
         }
@@ -900,7 +911,8 @@ estream_status run_routed(estream_ctx* c, cudaStream_t s, const void* X, int lay
         c->stats.launches += 1;
     } else {
         rc = pair
-                 ? launch_expert_ffn_pair(&c->tm_wg, &c->tm_wu, &c->tm_wd_half, &c->tm_h, seg, X, c->h,
+                 ? launch_expert_ffn_pair(&c->tm_wg, &c->tm_wu, &c->tm_wd_half, &c->tm_h, &c->tm_wg64,
+                                          &c->tm_wu64, seg, X, c->h,
                                           Y, c->out_rows, c->done, c->d.H, c->d.F, c->ffn_phases, c->dev_err, s)
                  : launch_expert_ffn(&c->tm_wg, &c->tm_wu, &c->tm_wd, &c->tm_h, seg, X, c->h, Y,
                                      c->out_rows, c->done, nullptr, c->d.H, c->d.F, c->ffn_phases, c->dev_err,
@@ -951,7 +963,8 @@ estream_status run_shared(estream_ctx* c, cudaStream_t s, const void* X,
     } else {
         rc = pair_form(c, T, 1)
                  ? launch_expert_ffn_pair(&c->tm_sg[layer], &c->tm_su[layer], &c->tm_sd_half[layer],
-                                          &c->tm_hs, seg, X, c->h_shared, Y, c->out_shared,
+                                          &c->tm_hs, &c->tm_sg64[layer], &c->tm_su64[layer],
+                                          seg, X, c->h_shared, Y, c->out_shared,
                                           c->sh_done, c->d.H, Fs, 3, c->dev_err, s)
                  : launch_expert_ffn(&c->tm_sg[layer], &c->tm_su[layer], &c->tm_sd[layer], &c->tm_hs,
                                      seg, X, c->h_shared, Y, c->out_shared, c->sh_done, nullptr,
