@@ -142,6 +142,14 @@ cudaError_t launch_expert_ffn_q4(const uint8_t* plane_g, const uint8_t* plane_u,
                                  float* out_rows, int* done, int* ticket, int H, int F, int phases,
                                  int* dev_err, int num_sms, cudaStream_t stream);
 
+// The 4-bit operator on CTA pairs: each CTA streams and expands its half of
+// every packed weight box (the pair form's tiles, without half tiles).
+cudaError_t launch_expert_ffn_pair_q4(const uint8_t* plane_g, const uint8_t* plane_u,
+                                      const uint8_t* plane_d, size_t S_gu, size_t S_d,
+                                      const CUtensorMap* tm_h, const GemmSegments& seg,
+                                      const void* X, void* h, float* Y, float* out_rows, int* done,
+                                      int H, int F, int phases, int* dev_err, cudaStream_t stream);
+
 // fp32 path (CUDA-core FMA): the same two steps for fp32 X and weights.
 // Weight planes are [slots][F][H] (gate, up) and [slots][H][F] (down).
 cudaError_t launch_gateup_f32(const float* X, const float* wg, const float* wu,

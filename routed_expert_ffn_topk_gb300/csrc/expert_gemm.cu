@@ -1169,8 +1169,25 @@ constexpr int kPairRows = 2 * kBM;
 constexpr int kLoaderWarps = 4;
 constexpr int kEpiWarps = 4;
 
-size_t pair_smem_bytes(int seg_count) {
-    return 1024 + kPOffTable + sizeof(int) * static_cast<size_t>(seg_count + 1);
+// 4-bit weights in the pair form: each CTA streams only its half of a packed
+// box (the gate box on rank 0 and the up box on rank 1, or rows
+// [128 r, 128 r + 128) of the down box: 4608 bytes either way) into a
+// 3-deep packed ring, and four converter warps (one B row per thread)
+// expand it into the CTA's half of the operand tile -- half of the
+// conversion of the single-SM 4-bit kernel per SM.
+constexpr int kPQConvWarps = 4;
+constexpr int kPQConvWarp0 = 10;
+constexpr int kPQThreads = kThreads + 32 * kPQConvWarps;
+constexpr int kPQPStages = 3;
+constexpr int kPQBox = 128 * 32 + 128 * 4;  // 4608 B
+constexpr int kPQOffPk = kPOffBar;            // packed ring where the bf16 form's barriers start
+constexpr int kPQOffBar = kPQOffPk + kPQPStages * kPQBox;
+constexpr int kPQNumBars = kPNumBars + 2 * kPQPStages;
+constexpr int kPQOffMisc = kPQOffBar + 8 * kPQNumBars;
+constexpr int kPQOffTable = kPQOffMisc + 16;
+
+size_t pair_smem_bytes(int seg_count, bool q4 = false) {
+    return 1024 + (q4 ? kPQOffTable : kPOffTable) + sizeof(int) * static_cast<size_t>(seg_count + 1);
 }
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -1306,7 +1323,8 @@ struct PairTile {
 };
 
 __device__ __forceinline__ PairTile decode_pair(int t, const int* table, int seg_count, int NB,
-                                                const int32_t* offsets, int seg_begin, int rank) {
+                                                const int32_t* offsets, int seg_begin, int rank,
+                                                bool allow_half = true) {
     int lo = 0, hi = seg_count;  // largest lo with table[lo] * NB <= t
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
@@ -1322,7 +1340,7 @@ __device__ __forceinline__ PairTile decode_pair(int t, const int* table, int seg
     const int s_hi = offsets[seg_begin + lo + 1];
     const int pr0 = s_lo + ti.pm * kPairRows;
     const int tot = min(kPairRows, s_hi - pr0);
-    ti.half = tot <= kBM;
+    ti.half = allow_half && tot <= kBM;
     // records [pr0, pr0 + tot) are the single m-blocks 2 pm (and 2 pm + 1):
     // in a full tile rank r's rows are m-block 2 pm + r with its own counter;
     // a half tile is one m-block whose counter both ranks publish on
@@ -1335,15 +1353,22 @@ __device__ __forceinline__ PairTile decode_pair(int t, const int* table, int seg
     return ti;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+// kQ4: 4-bit weights (Q4Planes, packed producer and converter warps in
+// place of the weight TMA; no half tiles, whose B half mixes gate and up
+// rows). The bf16 form ignores `planes`, the 4-bit form the weight maps.
+template <bool kQ4>
+__global__ void __launch_bounds__(kQ4 ? kPQThreads : kThreads, 1)
     k_expert_ffn_pair(const __grid_constant__ CUtensorMap tm_wg,
                       const __grid_constant__ CUtensorMap tm_wu,
                       const __grid_constant__ CUtensorMap tm_wd,
                       const __grid_constant__ CUtensorMap tm_h,
                       const __grid_constant__ CUtensorMap tm_wg64,
-                      const __grid_constant__ CUtensorMap tm_wu64, const FfnArgs a) {
+                      const __grid_constant__ CUtensorMap tm_wu64, const Q4Planes planes,
+                      const FfnArgs a) {
+    constexpr int kNT = kQ4 ? kPQThreads : kThreads;
+    constexpr bool kHalfTiles = !kQ4;
     extern __shared__ uint8_t smem_raw[];
-    __shared__ int warp_total[kThreads / 32];
+    __shared__ int warp_total[kNT / 32];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
     // The cta_group::2 tensor-memory and MMA instructions, the peer-CTA
@@ -1363,15 +1388,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sbase = smem_addr(smem);
     const uint32_t sA = sbase + kPOffA;
     const uint32_t sB = sbase + kPOffB;
-    const uint32_t bar0 = sbase + kPOffBar;
+    const uint32_t sPk = sbase + kPQOffPk;  // packed ring (4-bit form)
+    constexpr int kOffBar = kQ4 ? kPQOffBar : kPOffBar;
+    constexpr int kOffMisc = kQ4 ? kPQOffMisc : kPOffMisc;
+    constexpr int kOffTable = kQ4 ? kPQOffTable : kPOffTable;
+    const uint32_t bar0 = sbase + kOffBar;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (kPStages + s); };
     auto accf_bar = [&](int q) { return bar0 + 8u * (2 * kPStages + q); };
     auto acce_bar = [&](int q) { return bar0 + 8u * (2 * kPStages + 2 + q); };
     const uint32_t drain_bar = bar0 + 8u * (2 * kPStages + 4);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kPOffMisc);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kPOffMisc + 4);
-    int* table = reinterpret_cast<int*>(smem + kPOffTable);
+    auto pfull_bar = [&](int s) { return bar0 + 8u * (kPNumBars + s); };
+    auto pempty_bar = [&](int s) { return bar0 + 8u * (kPNumBars + kPQPStages + s); };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
+    int* table = reinterpret_cast<int*>(smem + kOffTable);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -1379,7 +1410,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // pair m-blocks per segment (ceil(count / 256)), exclusive prefix in table
     {
         const int n = seg.seg_count;
-        const int per = (n + kThreads - 1) / kThreads;
+        const int per = (n + kNT - 1) / kNT;
         const int lo = min(n, static_cast<int>(threadIdx.x) * per);
         const int hi = min(n, lo + per);
         int sum = 0;
@@ -1402,15 +1433,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int cnt = seg.offsets[seg.seg_begin + s + 1] - seg.offsets[seg.seg_begin + s];
             run += (cnt + kPairRows - 1) / kPairRows;
         }
-        if (threadIdx.x == kThreads - 1) table[n] = run;
+        if (threadIdx.x == kNT - 1) table[n] = run;
     }
     if (threadIdx.x == 0) {
         for (int s = 0; s < kPStages; ++s) {
-            // leader: the producer's expect_tx + one arrival per loader warp
+            // leader: the expect_tx (producer, or converter warp 0 in the 4-bit
+            // form) + one arrival per loader warp -- and per converter warp --
             // of both CTAs (the peer's full barriers stay unused)
-            mbar_init(full_bar(s), 1 + 2 * kLoaderWarps);
+            mbar_init(full_bar(s), 1 + 2 * kLoaderWarps + (kQ4 ? 2 * kPQConvWarps : 0));
             mbar_init(empty_bar(s), 1);
         }
+        if (kQ4)
+            for (int s = 0; s < kPQPStages; ++s) {
+                mbar_init(pfull_bar(s), 1);                // the packed producer's expect_tx
+                mbar_init(pempty_bar(s), kPQConvWarps);   // one per converter warp
+            }
         for (int q = 0; q < 2; ++q) {
             mbar_init(accf_bar(q), 1);
             mbar_init(acce_bar(q), 2 * kEpiWarps);
@@ -1438,7 +1475,119 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int TB = (a.phases & 2) ? PM * NBB : 0;
     const int done_target = kEpiWarps * NBA;
 
-    if (warp == 0) {
+    if (kQ4 && warp == 0) {
+        // ------------------------------ packed-weight producer (4-bit) ------------------------------
+        // this CTA's half of every packed box: the gate (rank 0) or up (rank 1)
+        // box of the n-block, or rows [128 r, 128 r + 128) of the down box,
+        // laid out in the stage as [codes 0-31: 2 KB][codes 32-63: 2 KB][scales: 512 B]
+        if (lane == 0) {
+            int issued[kPQPStages];
+            for (int q = 0; q < kPQPStages; ++q) issued[q] = -1;
+            bool ok = true;
+            int g = 0;
+            for (int it = 0, t; ok && (t = tile_of(pair, n_pairs, TA, TB, KBA, KBB, it)) >= 0; ++it) {
+                const bool gu = t < TA;
+                const PairTile ti = decode_pair(gu ? t : t - TA, table, seg.seg_count,
+                                                gu ? NBA : NBB, seg.offsets, seg.seg_begin,
+                                                static_cast<int>(rank), kHalfTiles);
+                const size_t slot = static_cast<size_t>(seg.slot_base + ti.seg);
+                const int num_kb = gu ? KBA : KBB;
+                const uint8_t* box0 =
+                    gu ? (rank == 0 ? planes.g : planes.u) + slot * planes.S_gu +
+                             static_cast<size_t>(ti.nb) * KBA * kQBoxGU
+                       : planes.d + slot * planes.S_d + static_cast<size_t>(ti.nb) * KBB * kQBoxDn;
+                for (int kb = 0; kb < num_kb; ++kb, ++g) {
+                    const int ps = g % kPQPStages;
+                    const uint32_t pph = static_cast<uint32_t>(g / kPQPStages) & 1u;
+                    if (!mbar_wait(pempty_bar(ps), pph ^ 1u, abort_flag, a.dev_err)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(pfull_bar(ps), kPQBox);
+                    issued[ps] = static_cast<int>(pph);
+                    const uint32_t dst = sPk + ps * kPQBox;
+                    if (gu) {
+                        bulk_load(dst, box0 + static_cast<size_t>(kb) * kQBoxGU, kPQBox, pfull_bar(ps));
+                    } else {
+                        const uint8_t* box = box0 + static_cast<size_t>(kb) * kQBoxDn;
+                        bulk_load(dst, box + 2048 * rank, 2048, pfull_bar(ps));
+                        bulk_load(dst + 2048, box + 4096 + 2048 * rank, 2048, pfull_bar(ps));
+                        bulk_load(dst + 4096, box + 8192 + 512 * rank, 512, pfull_bar(ps));
+                    }
+                }
+            }
+            if (!ok)
+                for (int q = 0; q < kPQPStages; ++q)
+                    if (issued[q] >= 0) mbar_wait_drain(pfull_bar(q), static_cast<uint32_t>(issued[q]));
+        }
+        __syncwarp();
+    } else if (kQ4 && warp >= kPQConvWarp0) {
+        // ------------------------------ converters (4-bit) ------------------------------
+        // thread ct expands B row ct of this CTA's half of every stage; converter
+        // warp 0 also loads the h rows of down tiles (after the m-block's gate/up
+        // tiles have published), and on the leader posts the stage's expected bytes
+        const int cw = warp - kPQConvWarp0;
+        const int ct = cw * 32 + lane;
+        int g = 0;
+        bool ok = true;
+        for (int it = 0, t; ok && (t = tile_of(pair, n_pairs, TA, TB, KBA, KBB, it)) >= 0; ++it) {
+            const bool gu = t < TA;
+            const PairTile ti = decode_pair(gu ? t : t - TA, table, seg.seg_count, gu ? NBA : NBB,
+                                            seg.offsets, seg.seg_begin, static_cast<int>(rank),
+                                            kHalfTiles);
+            const int num_kb = gu ? KBA : KBB;
+            const bool load_h = !gu && ti.rows > 0;
+            const uint32_t tx = gu ? 0u : static_cast<uint32_t>(kPHalf * (1 + (ti.rows1 > 0 ? 1 : 0)));
+            for (int kb = 0; kb < num_kb; ++kb, ++g) {
+                const int s = g % kPStages;
+                const uint32_t ph = static_cast<uint32_t>(g / kPStages) & 1u;
+                const int ps = g % kPQPStages;
+                const uint32_t pph = static_cast<uint32_t>(g / kPQPStages) & 1u;
+                bool wt = true;
+                if (lane == 0)
+                    wt = mbar_wait(pfull_bar(ps), pph, abort_flag, a.dev_err) &&
+                         mbar_wait_cl(empty_bar(s), ph ^ 1u, abort_flag, a.dev_err);
+                if (cw == 0 && lane == 0 && wt && load_h && kb == 0) {
+                    wt = wait_counter(a.done + seg.mblk[seg.seg_begin + ti.seg] + ti.cnt,
+                                      ti.npub * done_target, abort_flag, a.dev_err);
+                    fence_proxy_async_global();  // before the TMA reads of h
+                }
+                wt = __shfl_sync(0xffffffffu, wt, 0);
+                if (!wt) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t pb = sPk + ps * kPQBox;
+                const uint32_t bb = sB + s * kPHalf;
+                if (gu)
+                    expand_row<false>(pb + ct * 16, pb + 2048 + ct * 16, pb + 4096 + ct * 4,
+                                      bb + ct * kRowBytes, ct);
+                else
+                    expand_row<true>(pb + ct * 16, pb + 2048 + ct * 16, pb + 4096 + ct * 4,
+                                     bb + ct * kRowBytes, ct);
+                fence_proxy_async();
+                __syncwarp();
+                if (lane == 0) {
+                    const uint32_t lbar = map_rank(full_bar(s), 0);
+                    if (cw == 0) {
+                        if (rank == 0) mbar_arrive_expect_tx(full_bar(s), tx);
+                        if (load_h) tma_load_2d_pair(sA + s * kPHalf, &tm_h, kb * 64, ti.row0, lbar);
+                    }
+                    if (rank == 0)
+                        mbar_arrive(full_bar(s));
+                    else
+                        mbar_arrive_remote_smem_release(lbar);
+                    mbar_arrive(pempty_bar(ps));
+                }
+            }
+        }
+        if (!ok && cw == 0 && lane == 0) {
+            // give an h load already issued time to land before the CTA goes away
+            const uint64_t t0 = global_ns();
+            while (global_ns() - t0 < kDrainLimitNs / 100) {
+            }
+        }
+    } else if (warp == 0) {
         // ------------------------------ TMA producer ------------------------------
         int stage = 0;
         uint32_t phase = 0;
@@ -1446,7 +1595,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int it = 0, t; ok && (t = tile_of(pair, n_pairs, TA, TB, KBA, KBB, it)) >= 0; ++it) {
             const bool gu = t < TA;
             const PairTile ti = decode_pair(gu ? t : t - TA, table, seg.seg_count, gu ? NBA : NBB,
-                                            seg.offsets, seg.seg_begin, static_cast<int>(rank));
+                                            seg.offsets, seg.seg_begin, static_cast<int>(rank),
+                                            kHalfTiles);
             const int slot = seg.slot_base + ti.seg;
             const int num_kb = gu ? KBA : KBB;
             // tile-major planes: the (n-block, k-block) box of a slot is one
@@ -1538,7 +1688,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             while (global_ns() - t0 < kDrainLimitNs / 100) {
             }
         }
-    } else if (warp >= kLoaderWarp0) {
+    } else if (warp >= kLoaderWarp0 && warp < kLoaderWarp0 + kLoaderWarps) {
         // ------------------------------ A-operand loader ------------------------------
         // As in the single-CTA kernel, but each warp arrives once per stage
         // (after every lane's copies completed and were fenced) on the
@@ -1563,7 +1713,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int it = 0, t; ok && (t = tile_of(pair, n_pairs, TA, TB, KBA, KBB, it)) >= 0; ++it) {
             const bool gu = t < TA;
             const PairTile ti = decode_pair(gu ? t : t - TA, table, seg.seg_count, gu ? NBA : NBB,
-                                            seg.offsets, seg.seg_begin, static_cast<int>(rank));
+                                            seg.offsets, seg.seg_begin, static_cast<int>(rank),
+                                            kHalfTiles);
             const int num_kb = gu ? KBA : KBB;
             if (!gu) {
                 if (npend > 0) {
@@ -1652,7 +1803,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool gu = t < TA;
                 const int num_kb = gu ? KBA : KBB;
                 const PairTile ti = decode_pair(gu ? t : t - TA, table, seg.seg_count, gu ? NBA : NBB,
-                                                seg.offsets, seg.seg_begin, 0);
+                                                seg.offsets, seg.seg_begin, 0, kHalfTiles);
                 const uint32_t idesc = gu ? (ti.half ? idesc_gu_half : idesc_gu)
                                           : (ti.half ? idesc_dn_half : idesc_dn);
                 if (!mbar_wait_cl(acce_bar(acc), acc_phase ^ 1u, abort_flag, a.dev_err)) {
@@ -1703,7 +1854,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int it = 0, t; (t = tile_of(pair, n_pairs, TA, TB, KBA, KBB, it)) >= 0; ++it) {
             const bool gu = t < TA;
             const PairTile ti = decode_pair(gu ? t : t - TA, table, seg.seg_count, gu ? NBA : NBB,
-                                            seg.offsets, seg.seg_begin, static_cast<int>(rank));
+                                            seg.offsets, seg.seg_begin, static_cast<int>(rank),
+                                            kHalfTiles);
             bool w = true;
             if (lane == 0) w = mbar_wait_cl(accf_bar(acc), acc_phase, abort_flag, a.dev_err);
             w = __shfl_sync(0xffffffffu, w, 0);
@@ -1829,16 +1981,19 @@ cudaError_t launch_expert_ffn(const CUtensorMap* tm_wg, const CUtensorMap* tm_wu
     return cudaGetLastError();
 }
 
-// Co-resident CTA pairs of k_expert_ffn_pair at its largest shared-memory
-// size (the bound for every smaller launch), per device.
+// Co-resident CTA pairs of a pair kernel form at its largest shared-memory
+// size (the bound for every smaller launch), per device and form.
+template <bool kQ4>
 static int max_pairs(int device) {
     static std::mutex mu;
     static int cache[64] = {0};
     if (device < 0 || device >= 64) return 0;
     std::lock_guard<std::mutex> lock(mu);
     if (cache[device] > 0) return cache[device];
-    const size_t smem = pair_smem_bytes(kMaxP);
-    if (cudaFuncSetAttribute(k_expert_ffn_pair, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    // the largest segment count a launch of this form takes: slots of an arena,
+    // or the experts of one layer for 4-bit weights
+    const size_t smem = pair_smem_bytes(kQ4 ? kQMaxSegs : kMaxP, kQ4);
+    if (cudaFuncSetAttribute(k_expert_ffn_pair<kQ4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
         return 0;
     cudaLaunchConfig_t cfg = {};
@@ -1850,35 +2005,38 @@ static int max_pairs(int device) {
     int nsm = 0;
     cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, device);
     cfg.gridDim = dim3(static_cast<unsigned>(nsm & ~1));
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(kQ4 ? kPQThreads : kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.attrs = at;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(k_expert_ffn_pair), &cfg) !=
-        cudaSuccess)
+    if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(k_expert_ffn_pair<kQ4>),
+                                       &cfg) != cudaSuccess)
         return 0;
     cache[device] = n;
     return n;
 }
 
-cudaError_t launch_expert_ffn_pair(const CUtensorMap* tm_wg, const CUtensorMap* tm_wu,
-                                   const CUtensorMap* tm_wd_half, const CUtensorMap* tm_h,
-                                   const CUtensorMap* tm_wg64, const CUtensorMap* tm_wu64,
-                                   const GemmSegments& seg, const void* X, void* h, float* Y,
-                                   float* out_rows, int* done, int H, int F, int phases,
-                                   int* dev_err, cudaStream_t stream) {
+// One cooperative launch of clusters of two CTAs: every pair is resident, so
+// a down tile may wait for gate/up tiles that other pairs own.
+template <bool kQ4>
+static cudaError_t launch_pair(const CUtensorMap* tm_wg, const CUtensorMap* tm_wu,
+                               const CUtensorMap* tm_wd_half, const CUtensorMap* tm_h,
+                               const CUtensorMap* tm_wg64, const CUtensorMap* tm_wu64,
+                               const Q4Planes& planes, const GemmSegments& seg, const void* X,
+                               void* h, float* Y, float* out_rows, int* done, int H, int F,
+                               int phases, int* dev_err, cudaStream_t stream) {
     const long long max_tiles = static_cast<long long>(seg.max_tiles_m) *
                                 (((phases & 1) ? F / 128 : 0) + ((phases & 2) ? H / 256 : 0));
     if (max_tiles <= 0 || seg.seg_count <= 0) return cudaSuccess;
     int device = 0;
     cudaError_t rc = cudaGetDevice(&device);
     if (rc != cudaSuccess) return rc;
-    const int cap = max_pairs(device);
+    const int cap = max_pairs<kQ4>(device);
     if (cap <= 0) return cudaErrorLaunchOutOfResources;
     const int pairs = static_cast<int>(max_tiles < cap ? max_tiles : cap);
-    const size_t smem = pair_smem_bytes(seg.seg_count);
-    rc = cudaFuncSetAttribute(k_expert_ffn_pair, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const size_t smem = pair_smem_bytes(seg.seg_count, kQ4);
+    rc = cudaFuncSetAttribute(k_expert_ffn_pair<kQ4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               static_cast<int>(smem));
     if (rc != cudaSuccess) return rc;
     FfnArgs args;
@@ -1893,11 +2051,11 @@ cudaError_t launch_expert_ffn_pair(const CUtensorMap* tm_wg, const CUtensorMap* 
     args.H = H;
     args.F = F;
     args.phases = phases;
+    Q4Planes pl = planes;
     void* kargs[] = {const_cast<CUtensorMap*>(tm_wg), const_cast<CUtensorMap*>(tm_wu),
                      const_cast<CUtensorMap*>(tm_wd_half), const_cast<CUtensorMap*>(tm_h),
-                     const_cast<CUtensorMap*>(tm_wg64), const_cast<CUtensorMap*>(tm_wu64), &args};
-    // clusters of two CTAs; cooperative, so every pair is resident and a down
-    // tile may wait for gate/up tiles that other pairs own
+                     const_cast<CUtensorMap*>(tm_wg64), const_cast<CUtensorMap*>(tm_wu64), &pl,
+                     &args};
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute at[2];
     at[0].id = cudaLaunchAttributeClusterDimension;
@@ -1907,14 +2065,37 @@ cudaError_t launch_expert_ffn_pair(const CUtensorMap* tm_wg, const CUtensorMap* 
     at[1].id = cudaLaunchAttributeCooperative;
     at[1].val.cooperative = 1;
     cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(kQ4 ? kPQThreads : kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cfg.attrs = at;
     cfg.numAttrs = 2;
-    rc = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(k_expert_ffn_pair), kargs);
+    rc = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(k_expert_ffn_pair<kQ4>), kargs);
     if (rc != cudaSuccess) return rc;
     return cudaGetLastError();
+}
+
+cudaError_t launch_expert_ffn_pair(const CUtensorMap* tm_wg, const CUtensorMap* tm_wu,
+                                   const CUtensorMap* tm_wd_half, const CUtensorMap* tm_h,
+                                   const CUtensorMap* tm_wg64, const CUtensorMap* tm_wu64,
+                                   const GemmSegments& seg, const void* X, void* h, float* Y,
+                                   float* out_rows, int* done, int H, int F, int phases,
+                                   int* dev_err, cudaStream_t stream) {
+    const Q4Planes none{nullptr, nullptr, nullptr, 0, 0};
+    return launch_pair<false>(tm_wg, tm_wu, tm_wd_half, tm_h, tm_wg64, tm_wu64, none, seg, X, h, Y,
+                              out_rows, done, H, F, phases, dev_err, stream);
+}
+
+cudaError_t launch_expert_ffn_pair_q4(const uint8_t* plane_g, const uint8_t* plane_u,
+                                      const uint8_t* plane_d, size_t S_gu, size_t S_d,
+                                      const CUtensorMap* tm_h, const GemmSegments& seg,
+                                      const void* X, void* h, float* Y, float* out_rows, int* done,
+                                      int H, int F, int phases, int* dev_err, cudaStream_t stream) {
+    if (seg.seg_count > kQMaxSegs) return cudaErrorInvalidValue;
+    const Q4Planes planes{plane_g, plane_u, plane_d, S_gu, S_d};
+    // the weight maps are not read by the 4-bit form; h's map stands in for them
+    return launch_pair<true>(tm_h, tm_h, tm_h, tm_h, tm_h, tm_h, planes, seg, X, h, Y, out_rows,
+                             done, H, F, phases, dev_err, stream);
 }
 
 cudaError_t launch_expert_ffn_q4(const uint8_t* plane_g, const uint8_t* plane_u, const uint8_t* plane_d,

@@ -585,7 +585,6 @@ estream_status estream_bind_arena(estream_ctx** out, const estream_arena_desc* d
     if (d->ffn_form != ESTREAM_FFN_AUTO && d->ffn_form != ESTREAM_FFN_SINGLE &&
         d->ffn_form != ESTREAM_FFN_PAIR)
         return ESTREAM_ERR_INVALID_ARG;
-    if (d->ffn_form == ESTREAM_FFN_PAIR && d->wdtype == ESTREAM_Q4) return ESTREAM_ERR_UNSUPPORTED;
     if (d->n_shared < 0 || (d->n_shared > 0 && (d->F_shared < 128 || d->F_shared % 128 != 0 ||
                                                  !d->shared_dev)))
         return ESTREAM_ERR_INVALID_ARG;
@@ -863,8 +862,8 @@ estream_status fill_bank(estream_ctx* c, int layer, int q, int b, size_t* bytes,
 // expert segments: ESTREAM_FFN_AUTO takes the CTA-pair form (256-record
 // tiles) when a segment holds on average at least ESTREAM_PAIR_MIN_ROWS.
 bool pair_form(const estream_ctx* c, long long rows, int segments) {
-    if (c->d.wdtype == ESTREAM_Q4) return false;  // 4-bit weights: single-SM form only
     if (c->d.ffn_form == ESTREAM_FFN_PAIR) return true;
+    if (c->d.wdtype == ESTREAM_Q4 && c->d.ffn_form == ESTREAM_FFN_AUTO) return false;
     if (c->d.ffn_form == ESTREAM_FFN_SINGLE) return false;
     return segments > 0 && rows >= static_cast<long long>(ESTREAM_PAIR_MIN_ROWS) * segments;
 }
@@ -903,11 +902,17 @@ estream_status run_routed(estream_ctx* c, cudaStream_t s, const void* X, int lay
                                  c->d.H, c->d.F, max_rows, s);
         c->stats.launches += 2;
     } else if (c->d.wdtype == ESTREAM_Q4) {
-        rc = launch_expert_ffn_q4(reinterpret_cast<const uint8_t*>(c->plane_g),
-                                  reinterpret_cast<const uint8_t*>(c->plane_u),
-                                  reinterpret_cast<const uint8_t*>(c->plane_d), c->S_gu, c->S_d,
-                                  &c->tm_h, seg, X, c->h, Y, c->out_rows, c->done, ticket, c->d.H,
-                                  c->d.F, c->ffn_phases, c->dev_err, c->num_sms, s);
+        rc = pair ? launch_expert_ffn_pair_q4(reinterpret_cast<const uint8_t*>(c->plane_g),
+                                              reinterpret_cast<const uint8_t*>(c->plane_u),
+                                              reinterpret_cast<const uint8_t*>(c->plane_d), c->S_gu,
+                                              c->S_d, &c->tm_h, seg, X, c->h, Y, c->out_rows,
+                                              c->done, c->d.H, c->d.F, c->ffn_phases, c->dev_err, s)
+                  : launch_expert_ffn_q4(reinterpret_cast<const uint8_t*>(c->plane_g),
+                                         reinterpret_cast<const uint8_t*>(c->plane_u),
+                                         reinterpret_cast<const uint8_t*>(c->plane_d), c->S_gu,
+                                         c->S_d, &c->tm_h, seg, X, c->h, Y, c->out_rows, c->done,
+                                         ticket, c->d.H, c->d.F, c->ffn_phases, c->dev_err,
+                                         c->num_sms, s);
         c->stats.launches += 1;
     } else {
         rc = pair
@@ -957,9 +962,13 @@ estream_status run_shared(estream_ctx* c, cudaStream_t s, const void* X,
         const uint8_t* base = static_cast<const uint8_t*>(c->shared_dev[layer]);
         const size_t S1 = plane_slot_bytes(ESTREAM_Q4, Fs, c->d.H);  // one shared expert's plane
         const size_t sp = static_cast<size_t>(ns) * S1;
-        rc = launch_expert_ffn_q4(base, base + sp, base + 2 * sp, S1, S1, &c->tm_hs, seg, X,
-                                  c->h_shared, Y, c->out_shared, c->sh_done, c->tickets, c->d.H, Fs,
-                                  3, c->dev_err, c->num_sms, s);
+        rc = pair_form(c, T, 1)
+                 ? launch_expert_ffn_pair_q4(base, base + sp, base + 2 * sp, S1, S1, &c->tm_hs, seg, X,
+                                             c->h_shared, Y, c->out_shared, c->sh_done, c->d.H, Fs, 3,
+                                             c->dev_err, s)
+                 : launch_expert_ffn_q4(base, base + sp, base + 2 * sp, S1, S1, &c->tm_hs, seg, X,
+                                        c->h_shared, Y, c->out_shared, c->sh_done, c->tickets, c->d.H,
+                                        Fs, 3, c->dev_err, c->num_sms, s);
     } else {
         rc = pair_form(c, T, 1)
                  ? launch_expert_ffn_pair(&c->tm_sg[layer], &c->tm_su[layer], &c->tm_sd_half[layer],

@@ -51,7 +51,7 @@ def test_route_barrier_timeout_is_reported(mode, deterministic):
         st.close()
 
 
-@pytest.mark.parametrize("form", ["single", "pair", "q4"])
+@pytest.mark.parametrize("form", ["single", "pair", "q4", "q4pair"])
 def test_expert_kernel_timeout_is_reported(form):
     """The expert kernels' bounded waits: a call that runs the down tiles
     without their gate/up tiles (a test hook) waits 2 s for m-block counters
@@ -62,7 +62,9 @@ def test_expert_kernel_timeout_is_reported(form):
     wl = small_workload("c2")
     dev = _gpu.device()
     kw = {"ffn_form": es.FFN_PAIR} if form == "pair" else (
-        {"wdtype": es.Q4} if form == "q4" else {"ffn_form": es.FFN_SINGLE})
+        {"wdtype": es.Q4} if form == "q4" else (
+            {"wdtype": es.Q4, "ffn_form": es.FFN_PAIR} if form == "q4pair" else
+            {"ffn_form": es.FFN_SINGLE}))
     st = BoundLayerStack(wl, mode="resident", deterministic=True, **kw)
     try:
         X = wl.X.to(dev)

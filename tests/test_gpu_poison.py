@@ -81,21 +81,23 @@ def test_poisoned_consecutive_calls(key, form, mode, det):
         st.close()
 
 
-@pytest.mark.parametrize("mode", ["resident", "paged"])
-def test_poisoned_consecutive_calls_q4(mode):
+@pytest.mark.parametrize("mode,form", [("resident", "auto"), ("paged", "auto"),
+                                       ("resident", "pair"), ("paged", "pair")])
+def test_poisoned_consecutive_calls_q4(mode, form):
     from routed_expert_ffn_topk_gb300 import estream as es
     from routed_expert_ffn_topk_gb300.layer import BoundLayerStack
     cfg = W.scaled(W.CONFIGS["c3"], **SMALL["c3"])
     wl = W.make_workload(cfg)
     dq = _gpu.q4_weights(wl.layers[0])
-    st = BoundLayerStack(wl, mode=mode, wdtype=es.Q4)
+    st = BoundLayerStack(wl, mode=mode, wdtype=es.Q4,
+                         ffn_form=es.FFN_PAIR if form == "pair" else es.FFN_AUTO)
     try:
         _check_calls(st, wl, [None, 78], dq=dq)
     finally:
         st.close()
 
 
-@pytest.mark.parametrize("form", ["single", "pair", "q4"])
+@pytest.mark.parametrize("form", ["single", "pair", "q4", "q4pair"])
 def test_poisoned_graph_replay_with_new_inputs(form):
     """A captured layer call replayed on new inputs copied into its buffers,
     with the workspace poisoned before each replay."""
@@ -104,9 +106,11 @@ def test_poisoned_graph_replay_with_new_inputs(form):
     cfg = W.scaled(W.CONFIGS["c2"], **SMALL["c2"])
     wl = W.make_workload(cfg)
     dev = _gpu.device()
-    kw = {"wdtype": es.Q4} if form == "q4" else {
-        "ffn_form": es.FFN_PAIR if form == "pair" else es.FFN_SINGLE}
-    dq = _gpu.q4_weights(wl.layers[0]) if form == "q4" else None
+    if form.startswith("q4"):
+        kw = {"wdtype": es.Q4, "ffn_form": es.FFN_PAIR if form == "q4pair" else es.FFN_AUTO}
+    else:
+        kw = {"ffn_form": es.FFN_PAIR if form == "pair" else es.FFN_SINGLE}
+    dq = _gpu.q4_weights(wl.layers[0]) if form.startswith("q4") else None
     st = BoundLayerStack(wl, mode="resident", **kw)
     try:
         X = wl.X.to(dev).clone()
