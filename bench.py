@@ -786,7 +786,8 @@ def measure_q4(args, cfg, wl, dev, stream, flush, peaks):
         # paged: banks free before routing are filled in storage order (the
         # pages' prefetch schedule); with 28 MB groups the route-and-decide
         # time at the start of a call is a larger share than with bf16
-        st = BoundLayerStack(wl1, mode=mode, wdtype=es.Q4,
+        form = {"auto": es.FFN_AUTO, "single": es.FFN_SINGLE, "pair": es.FFN_PAIR}[args.q4_form]
+        st = BoundLayerStack(wl1, mode=mode, wdtype=es.Q4, ffn_form=form,
                              schedule=es.SCHED_PREFETCH if mode == "paged" else es.SCHED_AFTER_ROUTING)
         try:
             def one():
@@ -1146,6 +1147,8 @@ def main(argv=None):
     ap.add_argument("--no-q4", action="store_true", help="skip the 4-bit-expert measurement")
     ap.add_argument("--no-router", action="store_true", help="skip the router-logits measurement")
     ap.add_argument("--no-graph", action="store_true", help="time eager launches, not a CUDA-graph replay")
+    ap.add_argument("--q4-form", default="auto", choices=["auto", "single", "pair"],
+                    help="form of the 4-bit fused expert kernel (default: the library's choice)")
     ap.add_argument("--ffn-form", default="auto", choices=["auto", "single", "pair"],
                     help="form of the fused expert kernel in the resident step (default: the library's choice)")
     ap.add_argument("--no-cpu-baseline", action="store_true")

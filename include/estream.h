@@ -262,9 +262,8 @@ typedef struct {
     int T_max, k_max;       /* largest T and k a layer call will see (workspace capacity) */
     int deterministic;      /* 1: per-route outputs + fixed-order combine (bit-reproducible Y) */
     int schedule;           /* ESTREAM_SCHED_* */
-    int ffn_form;           /* ESTREAM_FFN_* (fp32 ignores it; for Q4, AUTO takes the
-                               single-SM form and PAIR the CTA-pair form, in which each SM
-                               expands half of every packed weight tile) */
+    int ffn_form;           /* ESTREAM_FFN_* (fp32 ignores it; Q4 follows the same rule, its
+                               CTA-pair form expanding half of every packed weight tile per SM) */
 } estream_arena_desc;
 
 typedef struct estream_ctx estream_ctx;

@@ -1156,15 +1156,9 @@ __global__ void __launch_bounds__(kQThreads, 1)
 // leader's full barrier; the leader's commits are multicast to both CTAs'
 // empty and accumulator-full barriers; both CTAs' epilogue warps arrive on
 // the leader's accumulator-empty barrier.
-constexpr int kPStages = 6;
+constexpr int kPStages = 6;                            // MMA ring of the bf16 form
 constexpr int kPHalf = 128 * kRowBytes;                // 16 KB
 constexpr int kPOffA = 0;
-constexpr int kPOffB = kPStages * kPHalf;
-constexpr int kPOffStg = kPOffB + kPStages * kPHalf;  // epilogue stages, 4 x 4 KB
-constexpr int kPOffBar = kPOffStg + 4 * 32 * 128;
-constexpr int kPNumBars = 2 * kPStages + 5;
-constexpr int kPOffMisc = kPOffBar + 8 * kPNumBars;
-constexpr int kPOffTable = kPOffMisc + 16;
 constexpr int kPairRows = 2 * kBM;
 constexpr int kLoaderWarps = 4;
 constexpr int kEpiWarps = 4;
@@ -1178,16 +1172,32 @@ constexpr int kEpiWarps = 4;
 constexpr int kPQConvWarps = 4;
 constexpr int kPQConvWarp0 = 10;
 constexpr int kPQThreads = kThreads + 32 * kPQConvWarps;
-constexpr int kPQPStages = 3;
+// The packed boxes come from L2 or HBM with a latency of microseconds, so the
+// 4-bit form keeps many of them in flight: it gives one stage of the MMA ring
+// (measured as fast with five stages as with six) to nine packed stages.
+constexpr int kPQStages = 5;    // MMA ring of the 4-bit form
+constexpr int kPQPStages = 9;   // packed-weight ring
 constexpr int kPQBox = 128 * 32 + 128 * 4;  // 4608 B
-constexpr int kPQOffPk = kPOffBar;            // packed ring where the bf16 form's barriers start
-constexpr int kPQOffBar = kPQOffPk + kPQPStages * kPQBox;
-constexpr int kPQNumBars = kPNumBars + 2 * kPQPStages;
-constexpr int kPQOffMisc = kPQOffBar + 8 * kPQNumBars;
-constexpr int kPQOffTable = kPQOffMisc + 16;
+
+// Shared-memory map of a pair-kernel form: A and B halves of the MMA ring,
+// the epilogue stages, the packed ring (4-bit form), barriers, misc, table.
+struct PairLayout {
+    int stages, pstages, off_b, off_stg, off_pk, off_bar, num_bars, off_misc, off_table;
+};
+__host__ __device__ constexpr PairLayout pair_layout(bool q4) {
+    const int st = q4 ? kPQStages : kPStages;
+    const int pst = q4 ? kPQPStages : 0;
+    const int off_b = st * kPHalf;
+    const int off_stg = off_b + st * kPHalf;
+    const int off_pk = off_stg + 4 * 32 * 128;
+    const int off_bar = off_pk + pst * kPQBox;
+    const int num_bars = 2 * st + 5 + 2 * pst;
+    const int off_misc = off_bar + 8 * num_bars;
+    return PairLayout{st, pst, off_b, off_stg, off_pk, off_bar, num_bars, off_misc, off_misc + 16};
+}
 
 size_t pair_smem_bytes(int seg_count, bool q4 = false) {
-    return 1024 + (q4 ? kPQOffTable : kPOffTable) + sizeof(int) * static_cast<size_t>(seg_count + 1);
+    return 1024 + pair_layout(q4).off_table + sizeof(int) * static_cast<size_t>(seg_count + 1);
 }
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -1385,21 +1395,23 @@ __global__ void __launch_bounds__(kQ4 ? kPQThreads : kThreads, 1)
     const uint32_t rank = cluster_rank();
     const int pair = static_cast<int>(blockIdx.x >> 1);
     const int n_pairs = static_cast<int>(gridDim.x >> 1);
+    constexpr PairLayout kL = pair_layout(kQ4);
+    constexpr int kST = kL.stages;      // MMA ring stages
+    constexpr int kPST = kL.pstages;    // packed ring stages (4-bit form)
+    constexpr int kOffMisc = kL.off_misc;
+    constexpr int kOffTable = kL.off_table;
     const uint32_t sbase = smem_addr(smem);
     const uint32_t sA = sbase + kPOffA;
-    const uint32_t sB = sbase + kPOffB;
-    const uint32_t sPk = sbase + kPQOffPk;  // packed ring (4-bit form)
-    constexpr int kOffBar = kQ4 ? kPQOffBar : kPOffBar;
-    constexpr int kOffMisc = kQ4 ? kPQOffMisc : kPOffMisc;
-    constexpr int kOffTable = kQ4 ? kPQOffTable : kPOffTable;
-    const uint32_t bar0 = sbase + kOffBar;
+    const uint32_t sB = sbase + kL.off_b;
+    const uint32_t sPk = sbase + kL.off_pk;  // packed ring (4-bit form)
+    const uint32_t bar0 = sbase + kL.off_bar;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
-    auto empty_bar = [&](int s) { return bar0 + 8u * (kPStages + s); };
-    auto accf_bar = [&](int q) { return bar0 + 8u * (2 * kPStages + q); };
-    auto acce_bar = [&](int q) { return bar0 + 8u * (2 * kPStages + 2 + q); };
-    const uint32_t drain_bar = bar0 + 8u * (2 * kPStages + 4);
-    auto pfull_bar = [&](int s) { return bar0 + 8u * (kPNumBars + s); };
-    auto pempty_bar = [&](int s) { return bar0 + 8u * (kPNumBars + kPQPStages + s); };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (kST + s); };
+    auto accf_bar = [&](int q) { return bar0 + 8u * (2 * kST + q); };
+    auto acce_bar = [&](int q) { return bar0 + 8u * (2 * kST + 2 + q); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * kST + 4);
+    auto pfull_bar = [&](int s) { return bar0 + 8u * (2 * kST + 5 + s); };
+    auto pempty_bar = [&](int s) { return bar0 + 8u * (2 * kST + 5 + kPST + s); };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
     int* table = reinterpret_cast<int*>(smem + kOffTable);
@@ -1436,7 +1448,7 @@ __global__ void __launch_bounds__(kQ4 ? kPQThreads : kThreads, 1)
         if (threadIdx.x == kNT - 1) table[n] = run;
     }
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kPStages; ++s) {
+        for (int s = 0; s < kST; ++s) {
             // leader: the expect_tx (producer, or converter warp 0 in the 4-bit
             // form) + one arrival per loader warp -- and per converter warp --
             // of both CTAs (the peer's full barriers stay unused)
@@ -1444,7 +1456,7 @@ __global__ void __launch_bounds__(kQ4 ? kPQThreads : kThreads, 1)
             mbar_init(empty_bar(s), 1);
         }
         if (kQ4)
-            for (int s = 0; s < kPQPStages; ++s) {
+            for (int s = 0; s < kPST; ++s) {
                 mbar_init(pfull_bar(s), 1);                // the packed producer's expect_tx
                 mbar_init(pempty_bar(s), kPQConvWarps);   // one per converter warp
             }
@@ -1481,8 +1493,8 @@ __global__ void __launch_bounds__(kQ4 ? kPQThreads : kThreads, 1)
         // box of the n-block, or rows [128 r, 128 r + 128) of the down box,
         // laid out in the stage as [codes 0-31: 2 KB][codes 32-63: 2 KB][scales: 512 B]
         if (lane == 0) {
-            int issued[kPQPStages];
-            for (int q = 0; q < kPQPStages; ++q) issued[q] = -1;
+            int issued[kPST > 0 ? kPST : 1];
+            for (int q = 0; q < kPST; ++q) issued[q] = -1;
             bool ok = true;
             int g = 0;
             for (int it = 0, t; ok && (t = tile_of(pair, n_pairs, TA, TB, KBA, KBB, it)) >= 0; ++it) {
@@ -1497,8 +1509,8 @@ __global__ void __launch_bounds__(kQ4 ? kPQThreads : kThreads, 1)
                              static_cast<size_t>(ti.nb) * KBA * kQBoxGU
                        : planes.d + slot * planes.S_d + static_cast<size_t>(ti.nb) * KBB * kQBoxDn;
                 for (int kb = 0; kb < num_kb; ++kb, ++g) {
-                    const int ps = g % kPQPStages;
-                    const uint32_t pph = static_cast<uint32_t>(g / kPQPStages) & 1u;
+                    const int ps = g % kPST;
+                    const uint32_t pph = static_cast<uint32_t>(g / kPST) & 1u;
                     if (!mbar_wait(pempty_bar(ps), pph ^ 1u, abort_flag, a.dev_err)) {
                         ok = false;
                         break;
@@ -1517,7 +1529,7 @@ __global__ void __launch_bounds__(kQ4 ? kPQThreads : kThreads, 1)
                 }
             }
             if (!ok)
-                for (int q = 0; q < kPQPStages; ++q)
+                for (int q = 0; q < kPST; ++q)
                     if (issued[q] >= 0) mbar_wait_drain(pfull_bar(q), static_cast<uint32_t>(issued[q]));
         }
         __syncwarp();
@@ -1539,10 +1551,10 @@ __global__ void __launch_bounds__(kQ4 ? kPQThreads : kThreads, 1)
             const bool load_h = !gu && ti.rows > 0;
             const uint32_t tx = gu ? 0u : static_cast<uint32_t>(kPHalf * (1 + (ti.rows1 > 0 ? 1 : 0)));
             for (int kb = 0; kb < num_kb; ++kb, ++g) {
-                const int s = g % kPStages;
-                const uint32_t ph = static_cast<uint32_t>(g / kPStages) & 1u;
-                const int ps = g % kPQPStages;
-                const uint32_t pph = static_cast<uint32_t>(g / kPQPStages) & 1u;
+                const int s = g % kST;
+                const uint32_t ph = static_cast<uint32_t>(g / kST) & 1u;
+                const int ps = g % kPST;
+                const uint32_t pph = static_cast<uint32_t>(g / kPST) & 1u;
                 bool wt = true;
                 if (lane == 0)
                     wt = mbar_wait(pfull_bar(ps), pph, abort_flag, a.dev_err) &&
@@ -1676,7 +1688,7 @@ __global__ void __launch_bounds__(kQ4 ? kPQThreads : kThreads, 1)
                         tma_load_2d_pair(sA + stage * kPHalf, &tm_h, kb * 64, ti.row0, lbar);
                 }
                 __syncwarp();
-                if (++stage == kPStages) {
+                if (++stage == kST) {
                     stage = 0;
                     phase ^= 1u;
                 }
@@ -1732,7 +1744,7 @@ __global__ void __launch_bounds__(kQ4 ? kPQThreads : kThreads, 1)
                         break;
                     }
                     publish(stage);
-                    if (++stage == kPStages) {
+                    if (++stage == kST) {
                         stage = 0;
                         phase ^= 1u;
                     }
@@ -1777,7 +1789,7 @@ __global__ void __launch_bounds__(kQ4 ? kPQThreads : kThreads, 1)
                     for (int q = 0; q < kLoaderDepth; ++q) pend[q] = pend[q + 1];
                     --npend;
                 }
-                if (++stage == kPStages) {
+                if (++stage == kST) {
                     stage = 0;
                     phase ^= 1u;
                 }
@@ -1826,7 +1838,7 @@ __global__ void __launch_bounds__(kQ4 ? kPQThreads : kThreads, 1)
                                       (kb | kk) != 0 ? 1u : 0u);
                     issued_any = true;
                     umma_commit_pair(empty_bar(stage));
-                    if (++stage == kPStages) {
+                    if (++stage == kST) {
                         stage = 0;
                         phase ^= 1u;
                     }
@@ -1846,7 +1858,7 @@ __global__ void __launch_bounds__(kQ4 ? kPQThreads : kThreads, 1)
         // ------------------------------ epilogue (warps 2-5) ------------------------------
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
-        const uint32_t stg = sbase + kPOffStg + static_cast<uint32_t>(quarter * kStageWarpBytes);
+        const uint32_t stg = sbase + kL.off_stg + static_cast<uint32_t>(quarter * kStageWarpBytes);
         const uint32_t leader_acce0 = map_rank(acce_bar(0), 0);
         const uint32_t leader_acce1 = map_rank(acce_bar(1), 0);
         int acc = 0;

@@ -863,7 +863,6 @@ estream_status fill_bank(estream_ctx* c, int layer, int q, int b, size_t* bytes,
 // tiles) when a segment holds on average at least ESTREAM_PAIR_MIN_ROWS.
 bool pair_form(const estream_ctx* c, long long rows, int segments) {
     if (c->d.ffn_form == ESTREAM_FFN_PAIR) return true;
-    if (c->d.wdtype == ESTREAM_Q4 && c->d.ffn_form == ESTREAM_FFN_AUTO) return false;
     if (c->d.ffn_form == ESTREAM_FFN_SINGLE) return false;
     return segments > 0 && rows >= static_cast<long long>(ESTREAM_PAIR_MIN_ROWS) * segments;
 }
