@@ -942,41 +942,6 @@ __device__ __forceinline__ void expand_row(uint32_t codes_lo, uint32_t codes_hi,
     }
 }
 
-// Half of expand_row: the 32 weights of code block hf (16 bytes at `codes`)
-// of row r, with the row's scale word at `scales`, into chunks 4 hf .. 4 hf + 3.
-template <bool kFp16>
-__device__ __forceinline__ void expand_half_row(uint32_t codes, uint32_t scales, int hf,
-                                                uint32_t dst_row, int r) {
-    uint32_t w[4], sc;
-    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]) : "r"(codes));
-    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(sc) : "r"(scales));
-    const uint32_t magic = kFp16 ? 0x64006400u : 0x43004300u;
-    const uint32_t offset = kFp16 ? 0x64086408u : 0x43084308u;
-    const uint32_t d2 = (hf ? (sc >> 16) : (sc & 0xFFFFu)) * 0x10001u;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        uint32_t o[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t v = ((w[c] >> (4 * i)) & 0x000F000Fu) | magic;
-            uint32_t t;
-            if (kFp16) {
-                asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(t) : "r"(v), "r"(offset));
-                asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(o[i]) : "r"(t), "r"(d2));
-            } else {
-                asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(t) : "r"(v), "r"(offset));
-                asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(o[i]) : "r"(t), "r"(d2));
-            }
-        }
-        const uint32_t dst =
-            dst_row + ((static_cast<uint32_t>(4 * hf + c) ^ static_cast<uint32_t>(r & 7)) << 4);
-        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(o[0]), "r"(o[1]),
-                     "r"(o[2]), "r"(o[3])
-                     : "memory");
-    }
-}
-
 // Converter warps (cw = 0..7, thread ct = 32 cw + lane expands B row ct of
 // every stage: rows 0-127 the gate box, 128-255 the up box, or the 256 rows
 // of the down box).
@@ -1201,18 +1166,17 @@ constexpr int kEpiWarps = 4;
 // 4-bit weights in the pair form: each CTA streams only its half of a packed
 // box (the gate box on rank 0 and the up box on rank 1, or rows
 // [128 r, 128 r + 128) of the down box: 4608 bytes either way) into a
-// 3-deep packed ring, and eight converter warps expand it into the CTA's
-// half of the operand tile -- half of the single-SM 4-bit kernel's
-// conversion per SM. A converter thread expands half a row (32 weights, one
-// code block): warps 0-3 the first block of rows 0-127, warps 4-7 the second
-// (a whole row per thread left the converters issue-bound: the stage's
-// conversion, not the MMA, set the pace).
-constexpr int kPQConvWarps = 8;
+// 3-deep packed ring, and four converter warps (one B row per thread)
+// expand it into the CTA's half of the operand tile -- half of the
+// conversion of the single-SM 4-bit kernel per SM.
+constexpr int kPQConvWarps = 4;
 constexpr int kPQConvWarp0 = 10;
 constexpr int kPQThreads = kThreads + 32 * kPQConvWarps;
-// (Five MMA stages with nine packed stages measured no faster.)
-constexpr int kPQStages = 6;    // MMA ring of the 4-bit form
-constexpr int kPQPStages = 3;   // packed-weight ring
+// The packed boxes come from L2 or HBM with a latency of microseconds, so the
+// 4-bit form keeps many of them in flight: it gives one stage of the MMA ring
+// (measured as fast with five stages as with six) to nine packed stages.
+constexpr int kPQStages = 5;    // MMA ring of the 4-bit form
+constexpr int kPQPStages = 9;   // packed-weight ring
 constexpr int kPQBox = 128 * 32 + 128 * 4;  // 4608 B
 
 // Shared-memory map of a pair-kernel form: A and B halves of the MMA ring,
@@ -1575,8 +1539,7 @@ __global__ void __launch_bounds__(kQ4 ? kPQThreads : kThreads, 1)
         // warp 0 also loads the h rows of down tiles (after the m-block's gate/up
         // tiles have published), and on the leader posts the stage's expected bytes
         const int cw = warp - kPQConvWarp0;
-        const int ct = (cw * 32 + lane) & 127;     // the B row
-        const int hf = cw >> 2;                    // its code block
+        const int ct = cw * 32 + lane;
         int g = 0;
         bool ok = true;
         for (int it = 0, t; ok && (t = tile_of(pair, n_pairs, TA, TB, KBA, KBB, it)) >= 0; ++it) {
@@ -1609,11 +1572,11 @@ __global__ void __launch_bounds__(kQ4 ? kPQThreads : kThreads, 1)
                 const uint32_t pb = sPk + ps * kPQBox;
                 const uint32_t bb = sB + s * kPHalf;
                 if (gu)
-                    expand_half_row<false>(pb + 2048 * hf + ct * 16, pb + 4096 + ct * 4, hf,
-                                           bb + ct * kRowBytes, ct);
+                    expand_row<false>(pb + ct * 16, pb + 2048 + ct * 16, pb + 4096 + ct * 4,
+                                      bb + ct * kRowBytes, ct);
                 else
-                    expand_half_row<true>(pb + 2048 * hf + ct * 16, pb + 4096 + ct * 4, hf,
-                                          bb + ct * kRowBytes, ct);
+                    expand_row<true>(pb + ct * 16, pb + 2048 + ct * 16, pb + 4096 + ct * 4,
+                                     bb + ct * kRowBytes, ct);
                 fence_proxy_async();
                 __syncwarp();
                 if (lane == 0) {
