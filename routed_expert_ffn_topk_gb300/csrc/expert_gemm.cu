@@ -1172,11 +1172,12 @@ constexpr int kEpiWarps = 4;
 constexpr int kPQConvWarps = 4;
 constexpr int kPQConvWarp0 = 10;
 constexpr int kPQThreads = kThreads + 32 * kPQConvWarps;
-// The packed boxes come from L2 or HBM with a latency of microseconds, so the
-// 4-bit form keeps many of them in flight: it gives one stage of the MMA ring
-// (measured as fast with five stages as with six) to nine packed stages.
-constexpr int kPQStages = 5;    // MMA ring of the 4-bit form
-constexpr int kPQPStages = 9;   // packed-weight ring
+// Measured: five MMA stages with nine packed stages are no faster, and eight
+// converter warps of half a row each are slower (the block's registers then
+// spill): the conversion is bound by the SM's instruction issue, shared with
+// the other roles.
+constexpr int kPQStages = 6;    // MMA ring of the 4-bit form
+constexpr int kPQPStages = 3;   // packed-weight ring
 constexpr int kPQBox = 128 * 32 + 128 * 4;  // 4608 B
 
 // Shared-memory map of a pair-kernel form: A and B halves of the MMA ring,
