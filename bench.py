@@ -829,7 +829,10 @@ def measure_q4(args, cfg, wl, dev, stream, flush, peaks):
             ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
             sus = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
             tensor = flops / nbytes >= ridge
-            rec.update({"kernel": "k_expert_ffn_q4", "ffn_ms": round(ffn_ms, 4),
+            # the library's automatic form choice, the same rule as for bf16
+            q4_pair = cfg.T * cfg.k >= es.PAIR_MIN_ROWS * cfg.E
+            rec.update({"kernel": "k_expert_ffn_pair<4-bit> (CTA pairs)" if q4_pair else "k_expert_ffn_q4",
+                        "ffn_ms": round(ffn_ms, 4),
                         "algorithmic_bytes_per_launch": int(nbytes),
                         "algorithmic_flops_per_launch": int(flops),
                         "arithmetic_intensity": round(flops / nbytes, 1),
