@@ -1399,6 +1399,7 @@ __global__ void __launch_bounds__(kQ4 ? kPQThreads : kThreads, 1)
     constexpr PairLayout kL = pair_layout(kQ4);
     constexpr int kST = kL.stages;      // MMA ring stages
     constexpr int kPST = kL.pstages;    // packed ring stages (4-bit form)
+    constexpr int kPSTm = kPST > 0 ? kPST : 1;  // its modulus (the bf16 form never uses it)
     constexpr int kOffMisc = kL.off_misc;
     constexpr int kOffTable = kL.off_table;
     const uint32_t sbase = smem_addr(smem);
@@ -1510,8 +1511,8 @@ __global__ void __launch_bounds__(kQ4 ? kPQThreads : kThreads, 1)
                              static_cast<size_t>(ti.nb) * KBA * kQBoxGU
                        : planes.d + slot * planes.S_d + static_cast<size_t>(ti.nb) * KBB * kQBoxDn;
                 for (int kb = 0; kb < num_kb; ++kb, ++g) {
-                    const int ps = g % kPST;
-                    const uint32_t pph = static_cast<uint32_t>(g / kPST) & 1u;
+                    const int ps = g % kPSTm;
+                    const uint32_t pph = static_cast<uint32_t>(g / kPSTm) & 1u;
                     if (!mbar_wait(pempty_bar(ps), pph ^ 1u, abort_flag, a.dev_err)) {
                         ok = false;
                         break;
@@ -1554,8 +1555,8 @@ __global__ void __launch_bounds__(kQ4 ? kPQThreads : kThreads, 1)
             for (int kb = 0; kb < num_kb; ++kb, ++g) {
                 const int s = g % kST;
                 const uint32_t ph = static_cast<uint32_t>(g / kST) & 1u;
-                const int ps = g % kPST;
-                const uint32_t pph = static_cast<uint32_t>(g / kPST) & 1u;
+                const int ps = g % kPSTm;
+                const uint32_t pph = static_cast<uint32_t>(g / kPSTm) & 1u;
                 bool wt = true;
                 if (lane == 0)
                     wt = mbar_wait(pfull_bar(ps), pph, abort_flag, a.dev_err) &&
