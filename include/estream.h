@@ -30,6 +30,11 @@
  *     reported by estream_get_device_error / estream_workspace_error.
  *   - Only sm_100-family GPUs built for here (sm_103a) are supported; other
  *     devices get ESTREAM_ERR_UNSUPPORTED.
+ *   - Tracing: the calling thread's work is marked with NVTX ranges in the
+ *     domain "estream" ("layer", "route build", "route from X", "routed
+ *     experts", "shared experts", "combine", "bank fill", "preload"; payload:
+ *     the layer, or layer * 65536 + group for a bank fill). They cost nothing
+ *     measurable unless a tool is attached.
  */
 #ifndef ESTREAM_H
 #define ESTREAM_H

@@ -22,6 +22,7 @@
 // on by the copy stream before the bank is refilled.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
 #include <cmath>
@@ -48,6 +49,59 @@ struct Bank {
 };
 
 enum TimedKind { kTRoute = 0, kTFfn, kTShared, kTCombine, kTTotal, kTIo, kTKinds };
+
+// NVTX ranges (domain "estream") for timeline tools: one per layer call, route
+// build, expert launch, combine and bank fill, and per standalone route build
+// or preload. Names are registered once, so a range costs no formatting; the
+// payload carries the layer (bank fills: layer * 65536 + group). Without an
+// attached tool NVTX's calls are no-ops.
+enum NvtxName {
+    kNvRoute = kTRoute, kNvRouted = kTFfn, kNvShared = kTShared, kNvCombine = kTCombine,
+    kNvLayer = kTTotal, kNvBankFill = kTIo, kNvRouteFromX, kNvPreload, kNvNames
+};
+struct NvtxNames {
+    nvtxDomainHandle_t dom = nullptr;
+    nvtxStringHandle_t name[kNvNames] = {};
+};
+const NvtxNames& nvtx_names() {
+    static const NvtxNames n = [] {
+        NvtxNames r;
+        r.dom = nvtxDomainCreateA("estream");
+        const char* text[kNvNames] = {"route build",  "routed experts", "shared experts",
+                                      "combine",      "layer",          "bank fill",
+                                      "route from X", "preload"};
+        for (int i = 0; i < kNvNames; ++i) r.name[i] = nvtxDomainRegisterStringA(r.dom, text[i]);
+        return r;
+    }();
+    return n;
+}
+void nvtx_push(int name, long long payload) {
+    static const uint32_t color[kNvNames] = {0xff2e9e44, 0xff2a6fdb, 0xff1aa3a3, 0xff8a4fd0,
+                                             0xff808080, 0xffe08a1e, 0xff2e9e44, 0xffe08a1e};
+    const NvtxNames& n = nvtx_names();
+    nvtxEventAttributes_t at = {};
+    at.version = NVTX_VERSION;
+    at.size = NVTX_EVENT_ATTRIB_STRUCT_SIZE;
+    at.colorType = NVTX_COLOR_ARGB;
+    at.color = color[name];
+    at.payloadType = NVTX_PAYLOAD_TYPE_INT64;
+    at.payload.llValue = payload;
+    at.messageType = NVTX_MESSAGE_TYPE_REGISTERED;
+    at.message.registered = n.name[name];
+    nvtxDomainRangePushEx(n.dom, &at);
+}
+void nvtx_pop() { nvtxDomainRangePop(nvtx_names().dom); }
+struct NvtxRange {
+    bool on;
+    NvtxRange(int name, long long payload, bool on_ = true) : on(on_) {
+        if (on) nvtx_push(name, payload);
+    }
+    ~NvtxRange() {
+        if (on) nvtx_pop();
+    }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 struct Timed {
     int kind;
@@ -130,13 +184,22 @@ struct TimedScope {
     cudaStream_t s;
     int kind;
     cudaEvent_t a = nullptr;
-    TimedScope(estream_ctx* c_, cudaStream_t s_, int kind_) : c(c_), s(s_), kind(kind_) {
+    bool open = true;  // its NVTX range (same name as the kind) is pushed
+    TimedScope(estream_ctx* c_, cudaStream_t s_, int kind_, long long payload)
+        : c(c_), s(s_), kind(kind_) {
+        nvtx_push(kind, payload);
         if (c->timing) {
             a = pool_event(c);
             if (a) cudaEventRecord(a, s);
         }
     }
+    TimedScope(const TimedScope&) = delete;
+    TimedScope& operator=(const TimedScope&) = delete;
     void end() {
+        if (open) {
+            nvtx_pop();
+            open = false;
+        }
         if (!a) return;
         cudaEvent_t b = pool_event(c);
         if (b) {
@@ -408,6 +471,7 @@ estream_status estream_route_build(const float* logits, int T, int E, int k, int
                                    const int32_t* phi, int P, int32_t* topk_ids, float* alpha,
                                    int32_t* offsets, int32_t* rec_tok, int32_t* rec_route,
                                    void* workspace, size_t workspace_bytes, void* cuda_stream) {
+    NvtxRange range(kNvRoute, -1);
     if (T < 0 || E < 1 || E > kMaxE || k < 1 || k > E || k > kMaxK || P < 0 || P > kMaxP)
         return ESTREAM_ERR_INVALID_ARG;
     if (!phi && P != E) return ESTREAM_ERR_INVALID_ARG;
@@ -458,6 +522,7 @@ estream_status estream_route_build_from_x(const void* X, int T, int H, const voi
                                           int32_t* offsets, int32_t* rec_tok, int32_t* rec_route,
                                           void* workspace, size_t workspace_bytes,
                                           void* cuda_stream) {
+    NvtxRange range(kNvRouteFromX, -1);
     if (T < 0 || E < 1 || E > kMaxE || k < 1 || k > E || k > kMaxK || P < 0 || P > kMaxP ||
         H < 64 || H % 64 != 0)
         return ESTREAM_ERR_INVALID_ARG;
@@ -841,7 +906,7 @@ estream_status fill_bank(estream_ctx* c, int layer, int q, int b, size_t* bytes,
     trace_state(c, b, layer, q, kFilling);
     bk.layer = layer;
     bk.group = q;
-    TimedScope io(c, cs, kTIo);
+    TimedScope io(c, cs, kTIo, static_cast<long long>(layer) * 65536 + q);
     const size_t slot0 = static_cast<size_t>(b) * G;
     if (cudaMemcpyAsync(c->plane_g + slot0 * c->S_gu, src, gbytes, cudaMemcpyHostToDevice, cs) !=
             cudaSuccess ||
@@ -883,7 +948,7 @@ estream_status run_routed(estream_ctx* c, cudaStream_t s, const void* X, int lay
     seg.seg_count = seg_count;
     seg.slot_base = slot_base;
     seg.max_tiles_m = max_tiles_m;
-    TimedScope ts(c, s, kTFfn);
+    TimedScope ts(c, s, kTFfn, layer);
     // this launch's dynamic tile counter, zeroed by the call's route build. The
     // 4-bit kernel takes its tiles dynamically (measured 5.5% faster on the
     // OLMoE shape); the bf16 kernel keeps the balanced static order (3% faster
@@ -931,7 +996,7 @@ estream_status run_routed(estream_ctx* c, cudaStream_t s, const void* X, int lay
 // Shared experts: identity route map over all T tokens, weight 1.
 estream_status run_shared(estream_ctx* c, cudaStream_t s, const void* X,
                           int layer, int T, float* Y) {
-    TimedScope ts(c, s, kTShared);
+    TimedScope ts(c, s, kTShared, layer);
     const int ns = c->d.n_shared;
     if (launch_identity_map(T, ns, c->sh_offsets, c->sh_rec_tok, c->sh_mblk, c->sh_done, s) !=
         cudaSuccess)
@@ -1038,6 +1103,7 @@ void release_pipe_events(estream_ctx* c) {
 extern "C" {
 
 estream_status estream_arena_preload(estream_ctx* c, int layer, void* cuda_stream) {
+    NvtxRange range(kNvPreload, layer);
     if (!c) return ESTREAM_ERR_NOT_BOUND;
     if (layer < 0 || layer >= c->d.L || !on_bound_device(c)) return ESTREAM_ERR_INVALID_ARG;
     if (c->n_groups > c->d.B) return ESTREAM_ERR_CAPACITY;
@@ -1099,7 +1165,7 @@ static estream_status prefill_impl(estream_ctx* c, int layer, const void* X, con
     c->trace.clear();
     c->stats.calls += 1;
     c->n_ffn_launch = 0;
-    TimedScope total(c, s, kTTotal);
+    TimedScope total(c, s, kTTotal, layer);
     release_pipe_events(c);
     const bool trace_pipe = c->timing;
     if (trace_pipe) {
@@ -1146,7 +1212,8 @@ static estream_status prefill_impl(estream_ctx* c, int layer, const void* X, con
 
     // K1: routing + route map over logical experts in storage order (Phi = pi, P = E)
     {
-        TimedScope ts(c, s, kTRoute);
+        TimedScope ts(c, s, kTRoute, layer);
+        NvtxRange from_x(kNvRouteFromX, layer, W_r != nullptr);   // routing from the layer input
         int launches = 0;
         const ResidualInit ri{A, c->es, Y, H};
         const int32_t* phi = c->d_perm + static_cast<size_t>(layer) * E;
@@ -1260,7 +1327,7 @@ static estream_status prefill_impl(estream_ctx* c, int layer, const void* X, con
     }
     c->stats.h2d_bytes += static_cast<double>(bytes);
     if (c->d.deterministic) {
-        TimedScope ts(c, s, kTCombine);
+        TimedScope ts(c, s, kTCombine, layer);
         if (launch_combine(c->out_rows, c->rec_pos, T, k, H, c->out_shared, c->d.n_shared, Y, s) !=
             cudaSuccess) {
             drain(c, s);
