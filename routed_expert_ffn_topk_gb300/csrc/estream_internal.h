@@ -126,12 +126,14 @@ cudaError_t launch_expert_ffn(const CUtensorMap* tm_wg, const CUtensorMap* tm_wu
 // tm_wd_half maps the down planes with 64 x 128 boxes (each CTA loads half of
 // a 256-row W_d box); tm_wg64 / tm_wu64 map the gate / up planes with 64 x 64
 // boxes (a half tile's CTA loads 64 gate and 64 up rows of an n-block).
+// m_first: tiles m-block-major inside a segment (for weights that stay in L2
+// across m-blocks, as a shared expert's do), else n-block-major.
 cudaError_t launch_expert_ffn_pair(const CUtensorMap* tm_wg, const CUtensorMap* tm_wu,
                                    const CUtensorMap* tm_wd_half, const CUtensorMap* tm_h,
                                    const CUtensorMap* tm_wg64, const CUtensorMap* tm_wu64,
                                    const GemmSegments& seg, const void* X, void* h, float* Y,
                                    float* out_rows, int* done, int H, int F, int phases,
-                                   int* dev_err, cudaStream_t stream);
+                                   int* dev_err, bool m_first, cudaStream_t stream);
 
 // The same operator on 4-bit weights (single-SM form): planes hold
 // Q4_0-style packed boxes (see estream_pack_experts), slot s of a plane at

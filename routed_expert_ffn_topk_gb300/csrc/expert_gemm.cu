@@ -1333,6 +1333,9 @@ struct PairTile {
     int npub;    // CTAs whose epilogues publish on that counter per gate/up tile
 };
 
+// kMFirst: inside a segment the tiles run m-block-major (all n-blocks of pair
+// m-block 0, then of m-block 1, ...) instead of n-block-major.
+template <bool kMFirst>
 __device__ __forceinline__ PairTile decode_pair(int t, const int* table, int seg_count, int NB,
                                                 const int32_t* offsets, int seg_begin, int rank,
                                                 bool allow_half = true) {
@@ -1345,8 +1348,13 @@ __device__ __forceinline__ PairTile decode_pair(int t, const int* table, int seg
     ti.seg = lo;
     const int npm = table[lo + 1] - table[lo];
     const int l = t - table[lo] * NB;
-    ti.nb = l / npm;
-    ti.pm = l - ti.nb * npm;
+    if (kMFirst) {
+        ti.pm = l / NB;
+        ti.nb = l - ti.pm * NB;
+    } else {
+        ti.nb = l / npm;
+        ti.pm = l - ti.nb * npm;
+    }
     const int s_lo = offsets[seg_begin + lo];
     const int s_hi = offsets[seg_begin + lo + 1];
     const int pr0 = s_lo + ti.pm * kPairRows;
@@ -1367,7 +1375,12 @@ __device__ __forceinline__ PairTile decode_pair(int t, const int* table, int seg
 // kQ4: 4-bit weights (Q4Planes, packed producer and converter warps in
 // place of the weight TMA; no half tiles, whose B half mixes gate and up
 // rows). The bf16 form ignores `planes`, the 4-bit form the weight maps.
-template <bool kQ4>
+// kMFirst: the m-block-major tile order (decode_pair), for launches whose
+// weights stay in L2 across m-blocks (shared experts): a down tile needs
+// every gate/up n-block of its m-block, and in this order the first m-blocks
+// complete early, so pairs that finish their gate/up tiles find down tiles
+// ready instead of waiting for the end of the gate/up phase.
+template <bool kQ4, bool kMFirst>
 __global__ void __launch_bounds__(kQ4 ? kPQThreads : kThreads, 1)
     k_expert_ffn_pair(const __grid_constant__ CUtensorMap tm_wg,
                       const __grid_constant__ CUtensorMap tm_wu,
@@ -1501,7 +1514,7 @@ __global__ void __launch_bounds__(kQ4 ? kPQThreads : kThreads, 1)
             int g = 0;
             for (int it = 0, t; ok && (t = tile_of(pair, n_pairs, TA, TB, KBA, KBB, it)) >= 0; ++it) {
                 const bool gu = t < TA;
-                const PairTile ti = decode_pair(gu ? t : t - TA, table, seg.seg_count,
+                const PairTile ti = decode_pair<kMFirst>(gu ? t : t - TA, table, seg.seg_count,
                                                 gu ? NBA : NBB, seg.offsets, seg.seg_begin,
                                                 static_cast<int>(rank), kHalfTiles);
                 const size_t slot = static_cast<size_t>(seg.slot_base + ti.seg);
@@ -1546,7 +1559,7 @@ __global__ void __launch_bounds__(kQ4 ? kPQThreads : kThreads, 1)
         bool ok = true;
         for (int it = 0, t; ok && (t = tile_of(pair, n_pairs, TA, TB, KBA, KBB, it)) >= 0; ++it) {
             const bool gu = t < TA;
-            const PairTile ti = decode_pair(gu ? t : t - TA, table, seg.seg_count, gu ? NBA : NBB,
+            const PairTile ti = decode_pair<kMFirst>(gu ? t : t - TA, table, seg.seg_count, gu ? NBA : NBB,
                                             seg.offsets, seg.seg_begin, static_cast<int>(rank),
                                             kHalfTiles);
             const int num_kb = gu ? KBA : KBB;
@@ -1608,7 +1621,7 @@ __global__ void __launch_bounds__(kQ4 ? kPQThreads : kThreads, 1)
         bool ok = true;
         for (int it = 0, t; ok && (t = tile_of(pair, n_pairs, TA, TB, KBA, KBB, it)) >= 0; ++it) {
             const bool gu = t < TA;
-            const PairTile ti = decode_pair(gu ? t : t - TA, table, seg.seg_count, gu ? NBA : NBB,
+            const PairTile ti = decode_pair<kMFirst>(gu ? t : t - TA, table, seg.seg_count, gu ? NBA : NBB,
                                             seg.offsets, seg.seg_begin, static_cast<int>(rank),
                                             kHalfTiles);
             const int slot = seg.slot_base + ti.seg;
@@ -1726,7 +1739,7 @@ __global__ void __launch_bounds__(kQ4 ? kPQThreads : kThreads, 1)
         };
         for (int it = 0, t; ok && (t = tile_of(pair, n_pairs, TA, TB, KBA, KBB, it)) >= 0; ++it) {
             const bool gu = t < TA;
-            const PairTile ti = decode_pair(gu ? t : t - TA, table, seg.seg_count, gu ? NBA : NBB,
+            const PairTile ti = decode_pair<kMFirst>(gu ? t : t - TA, table, seg.seg_count, gu ? NBA : NBB,
                                             seg.offsets, seg.seg_begin, static_cast<int>(rank),
                                             kHalfTiles);
             const int num_kb = gu ? KBA : KBB;
@@ -1816,7 +1829,7 @@ __global__ void __launch_bounds__(kQ4 ? kPQThreads : kThreads, 1)
             for (int it = 0, t; ok && (t = tile_of(pair, n_pairs, TA, TB, KBA, KBB, it)) >= 0; ++it) {
                 const bool gu = t < TA;
                 const int num_kb = gu ? KBA : KBB;
-                const PairTile ti = decode_pair(gu ? t : t - TA, table, seg.seg_count, gu ? NBA : NBB,
+                const PairTile ti = decode_pair<kMFirst>(gu ? t : t - TA, table, seg.seg_count, gu ? NBA : NBB,
                                                 seg.offsets, seg.seg_begin, 0, kHalfTiles);
                 const uint32_t idesc = gu ? (ti.half ? idesc_gu_half : idesc_gu)
                                           : (ti.half ? idesc_dn_half : idesc_dn);
@@ -1867,7 +1880,7 @@ __global__ void __launch_bounds__(kQ4 ? kPQThreads : kThreads, 1)
         uint32_t acc_phase = 0;
         for (int it = 0, t; (t = tile_of(pair, n_pairs, TA, TB, KBA, KBB, it)) >= 0; ++it) {
             const bool gu = t < TA;
-            const PairTile ti = decode_pair(gu ? t : t - TA, table, seg.seg_count, gu ? NBA : NBB,
+            const PairTile ti = decode_pair<kMFirst>(gu ? t : t - TA, table, seg.seg_count, gu ? NBA : NBB,
                                             seg.offsets, seg.seg_begin, static_cast<int>(rank),
                                             kHalfTiles);
             bool w = true;
@@ -1997,7 +2010,7 @@ cudaError_t launch_expert_ffn(const CUtensorMap* tm_wg, const CUtensorMap* tm_wu
 
 // Co-resident CTA pairs of a pair kernel form at its largest shared-memory
 // size (the bound for every smaller launch), per device and form.
-template <bool kQ4>
+template <bool kQ4, bool kMFirst>
 static int max_pairs(int device) {
     static std::mutex mu;
     static int cache[64] = {0};
@@ -2007,7 +2020,7 @@ static int max_pairs(int device) {
     // the largest segment count a launch of this form takes: slots of an arena,
     // or the experts of one layer for 4-bit weights
     const size_t smem = pair_smem_bytes(kQ4 ? kQMaxSegs : kMaxP, kQ4);
-    if (cudaFuncSetAttribute(k_expert_ffn_pair<kQ4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(k_expert_ffn_pair<kQ4, kMFirst>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
         return 0;
     cudaLaunchConfig_t cfg = {};
@@ -2024,7 +2037,7 @@ static int max_pairs(int device) {
     cfg.attrs = at;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(k_expert_ffn_pair<kQ4>),
+    if (cudaOccupancyMaxActiveClusters(&n, reinterpret_cast<const void*>(k_expert_ffn_pair<kQ4, kMFirst>),
                                        &cfg) != cudaSuccess)
         return 0;
     cache[device] = n;
@@ -2033,7 +2046,7 @@ static int max_pairs(int device) {
 
 // One cooperative launch of clusters of two CTAs: every pair is resident, so
 // a down tile may wait for gate/up tiles that other pairs own.
-template <bool kQ4>
+template <bool kQ4, bool kMFirst>
 static cudaError_t launch_pair(const CUtensorMap* tm_wg, const CUtensorMap* tm_wu,
                                const CUtensorMap* tm_wd_half, const CUtensorMap* tm_h,
                                const CUtensorMap* tm_wg64, const CUtensorMap* tm_wu64,
@@ -2046,11 +2059,11 @@ static cudaError_t launch_pair(const CUtensorMap* tm_wg, const CUtensorMap* tm_w
     int device = 0;
     cudaError_t rc = cudaGetDevice(&device);
     if (rc != cudaSuccess) return rc;
-    const int cap = max_pairs<kQ4>(device);
+    const int cap = max_pairs<kQ4, kMFirst>(device);
     if (cap <= 0) return cudaErrorLaunchOutOfResources;
     const int pairs = static_cast<int>(max_tiles < cap ? max_tiles : cap);
     const size_t smem = pair_smem_bytes(seg.seg_count, kQ4);
-    rc = cudaFuncSetAttribute(k_expert_ffn_pair<kQ4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    rc = cudaFuncSetAttribute(k_expert_ffn_pair<kQ4, kMFirst>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               static_cast<int>(smem));
     if (rc != cudaSuccess) return rc;
     FfnArgs args;
@@ -2084,7 +2097,7 @@ static cudaError_t launch_pair(const CUtensorMap* tm_wg, const CUtensorMap* tm_w
     cfg.stream = stream;
     cfg.attrs = at;
     cfg.numAttrs = 2;
-    rc = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(k_expert_ffn_pair<kQ4>), kargs);
+    rc = cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(k_expert_ffn_pair<kQ4, kMFirst>), kargs);
     if (rc != cudaSuccess) return rc;
     return cudaGetLastError();
 }
@@ -2094,10 +2107,13 @@ cudaError_t launch_expert_ffn_pair(const CUtensorMap* tm_wg, const CUtensorMap* 
                                    const CUtensorMap* tm_wg64, const CUtensorMap* tm_wu64,
                                    const GemmSegments& seg, const void* X, void* h, float* Y,
                                    float* out_rows, int* done, int H, int F, int phases,
-                                   int* dev_err, cudaStream_t stream) {
+                                   int* dev_err, bool m_first, cudaStream_t stream) {
     const Q4Planes none{nullptr, nullptr, nullptr, 0, 0};
-    return launch_pair<false>(tm_wg, tm_wu, tm_wd_half, tm_h, tm_wg64, tm_wu64, none, seg, X, h, Y,
-                              out_rows, done, H, F, phases, dev_err, stream);
+    if (m_first)
+        return launch_pair<false, true>(tm_wg, tm_wu, tm_wd_half, tm_h, tm_wg64, tm_wu64, none, seg,
+                                        X, h, Y, out_rows, done, H, F, phases, dev_err, stream);
+    return launch_pair<false, false>(tm_wg, tm_wu, tm_wd_half, tm_h, tm_wg64, tm_wu64, none, seg, X,
+                                     h, Y, out_rows, done, H, F, phases, dev_err, stream);
 }
 
 cudaError_t launch_expert_ffn_pair_q4(const uint8_t* plane_g, const uint8_t* plane_u,
@@ -2108,8 +2124,8 @@ cudaError_t launch_expert_ffn_pair_q4(const uint8_t* plane_g, const uint8_t* pla
     if (seg.seg_count > kQMaxSegs) return cudaErrorInvalidValue;
     const Q4Planes planes{plane_g, plane_u, plane_d, S_gu, S_d};
     // the weight maps are not read by the 4-bit form; h's map stands in for them
-    return launch_pair<true>(tm_h, tm_h, tm_h, tm_h, tm_h, tm_h, planes, seg, X, h, Y, out_rows,
-                             done, H, F, phases, dev_err, stream);
+    return launch_pair<true, false>(tm_h, tm_h, tm_h, tm_h, tm_h, tm_h, planes, seg, X, h, Y,
+                                    out_rows, done, H, F, phases, dev_err, stream);
 }
 
 cudaError_t launch_expert_ffn_q4(const uint8_t* plane_g, const uint8_t* plane_u, const uint8_t* plane_d,

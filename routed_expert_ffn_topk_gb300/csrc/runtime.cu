@@ -982,7 +982,8 @@ estream_status run_routed(estream_ctx* c, cudaStream_t s, const void* X, int lay
         rc = pair
                  ? launch_expert_ffn_pair(&c->tm_wg, &c->tm_wu, &c->tm_wd_half, &c->tm_h, &c->tm_wg64,
                                           &c->tm_wu64, seg, X, c->h,
-                                          Y, c->out_rows, c->done, c->d.H, c->d.F, c->ffn_phases, c->dev_err, s)
+                                          Y, c->out_rows, c->done, c->d.H, c->d.F, c->ffn_phases, c->dev_err,
+                                          false, s)
                  : launch_expert_ffn(&c->tm_wg, &c->tm_wu, &c->tm_wd, &c->tm_h, seg, X, c->h, Y,
                                      c->out_rows, c->done, nullptr, c->d.H, c->d.F, c->ffn_phases, c->dev_err,
                                      c->num_sms, s);
@@ -1038,7 +1039,7 @@ estream_status run_shared(estream_ctx* c, cudaStream_t s, const void* X,
                  ? launch_expert_ffn_pair(&c->tm_sg[layer], &c->tm_su[layer], &c->tm_sd_half[layer],
                                           &c->tm_hs, &c->tm_sg64[layer], &c->tm_su64[layer],
                                           seg, X, c->h_shared, Y, c->out_shared,
-                                          c->sh_done, c->d.H, Fs, 3, c->dev_err, s)
+                                          c->sh_done, c->d.H, Fs, 3, c->dev_err, true, s)
                  : launch_expert_ffn(&c->tm_sg[layer], &c->tm_su[layer], &c->tm_sd[layer], &c->tm_hs,
                                      seg, X, c->h_shared, Y, c->out_shared, c->sh_done, nullptr,
                                      c->d.H, Fs, 3, c->dev_err, c->num_sms, s);
