@@ -1197,8 +1197,17 @@ __host__ __device__ constexpr PairLayout pair_layout(bool q4) {
     return PairLayout{st, pst, off_b, off_stg, off_pk, off_bar, num_bars, off_misc, off_misc + 16};
 }
 
+// The launch's segment offsets are copied next to the segment table when
+// that fits the shared memory of the largest table (seg_count + 1 at most
+// half of it), so a tile decode reads no global memory.
+constexpr int pair_seg_cap(bool q4) { return q4 ? kQMaxSegs : kMaxP; }
+__host__ __device__ constexpr bool pair_offsets_cached(int seg_count, bool q4) {
+    return 2 * (seg_count + 1) <= (q4 ? kQMaxSegs : kMaxP) + 1;
+}
 size_t pair_smem_bytes(int seg_count, bool q4 = false) {
-    return 1024 + pair_layout(q4).off_table + sizeof(int) * static_cast<size_t>(seg_count + 1);
+    const size_t n = static_cast<size_t>(seg_count + 1);
+    return 1024 + pair_layout(q4).off_table + sizeof(int) * n +
+           (pair_offsets_cached(seg_count, q4) ? sizeof(int) * n : 0);
 }
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -1430,6 +1439,10 @@ __global__ void __launch_bounds__(kQ4 ? kPQThreads : kThreads, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
     int* table = reinterpret_cast<int*>(smem + kOffTable);
+    // the segment offsets (relative to seg_begin), in shared memory when cached
+    const bool offs_cached = pair_offsets_cached(seg.seg_count, kQ4);
+    int* offs_cache = table + seg.seg_count + 1;
+    const int32_t* offs = offs_cached ? offs_cache : seg.offsets + seg.seg_begin;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -1442,9 +1455,12 @@ __global__ void __launch_bounds__(kQ4 ? kPQThreads : kThreads, 1)
         const int hi = min(n, lo + per);
         int sum = 0;
         for (int s = lo; s < hi; ++s) {
-            const int cnt = seg.offsets[seg.seg_begin + s + 1] - seg.offsets[seg.seg_begin + s];
+            const int s0 = seg.offsets[seg.seg_begin + s];
+            const int cnt = seg.offsets[seg.seg_begin + s + 1] - s0;
+            if (offs_cached) offs_cache[s] = s0;
             sum += (cnt + kPairRows - 1) / kPairRows;
         }
+        if (offs_cached && threadIdx.x == kNT - 1) offs_cache[n] = seg.offsets[seg.seg_begin + n];
         int incl = sum;
 #pragma unroll
         for (int d = 1; d < 32; d <<= 1) {
@@ -1515,7 +1531,7 @@ __global__ void __launch_bounds__(kQ4 ? kPQThreads : kThreads, 1)
             for (int it = 0, t; ok && (t = tile_of(pair, n_pairs, TA, TB, KBA, KBB, it)) >= 0; ++it) {
                 const bool gu = t < TA;
                 const PairTile ti = decode_pair<kMFirst>(gu ? t : t - TA, table, seg.seg_count,
-                                                gu ? NBA : NBB, seg.offsets, seg.seg_begin,
+                                                gu ? NBA : NBB, offs, 0,
                                                 static_cast<int>(rank), kHalfTiles);
                 const size_t slot = static_cast<size_t>(seg.slot_base + ti.seg);
                 const int num_kb = gu ? KBA : KBB;
@@ -1560,7 +1576,7 @@ __global__ void __launch_bounds__(kQ4 ? kPQThreads : kThreads, 1)
         for (int it = 0, t; ok && (t = tile_of(pair, n_pairs, TA, TB, KBA, KBB, it)) >= 0; ++it) {
             const bool gu = t < TA;
             const PairTile ti = decode_pair<kMFirst>(gu ? t : t - TA, table, seg.seg_count, gu ? NBA : NBB,
-                                            seg.offsets, seg.seg_begin, static_cast<int>(rank),
+                                            offs, 0, static_cast<int>(rank),
                                             kHalfTiles);
             const int num_kb = gu ? KBA : KBB;
             const bool load_h = !gu && ti.rows > 0;
@@ -1622,7 +1638,7 @@ __global__ void __launch_bounds__(kQ4 ? kPQThreads : kThreads, 1)
         for (int it = 0, t; ok && (t = tile_of(pair, n_pairs, TA, TB, KBA, KBB, it)) >= 0; ++it) {
             const bool gu = t < TA;
             const PairTile ti = decode_pair<kMFirst>(gu ? t : t - TA, table, seg.seg_count, gu ? NBA : NBB,
-                                            seg.offsets, seg.seg_begin, static_cast<int>(rank),
+                                            offs, 0, static_cast<int>(rank),
                                             kHalfTiles);
             const int slot = seg.slot_base + ti.seg;
             const int num_kb = gu ? KBA : KBB;
@@ -1740,7 +1756,7 @@ __global__ void __launch_bounds__(kQ4 ? kPQThreads : kThreads, 1)
         for (int it = 0, t; ok && (t = tile_of(pair, n_pairs, TA, TB, KBA, KBB, it)) >= 0; ++it) {
             const bool gu = t < TA;
             const PairTile ti = decode_pair<kMFirst>(gu ? t : t - TA, table, seg.seg_count, gu ? NBA : NBB,
-                                            seg.offsets, seg.seg_begin, static_cast<int>(rank),
+                                            offs, 0, static_cast<int>(rank),
                                             kHalfTiles);
             const int num_kb = gu ? KBA : KBB;
             if (!gu) {
@@ -1830,7 +1846,7 @@ __global__ void __launch_bounds__(kQ4 ? kPQThreads : kThreads, 1)
                 const bool gu = t < TA;
                 const int num_kb = gu ? KBA : KBB;
                 const PairTile ti = decode_pair<kMFirst>(gu ? t : t - TA, table, seg.seg_count, gu ? NBA : NBB,
-                                                seg.offsets, seg.seg_begin, 0, kHalfTiles);
+                                                offs, 0, 0, kHalfTiles);
                 const uint32_t idesc = gu ? (ti.half ? idesc_gu_half : idesc_gu)
                                           : (ti.half ? idesc_dn_half : idesc_dn);
                 if (!mbar_wait_cl(acce_bar(acc), acc_phase ^ 1u, abort_flag, a.dev_err)) {
@@ -1881,7 +1897,7 @@ __global__ void __launch_bounds__(kQ4 ? kPQThreads : kThreads, 1)
         for (int it = 0, t; (t = tile_of(pair, n_pairs, TA, TB, KBA, KBB, it)) >= 0; ++it) {
             const bool gu = t < TA;
             const PairTile ti = decode_pair<kMFirst>(gu ? t : t - TA, table, seg.seg_count, gu ? NBA : NBB,
-                                            seg.offsets, seg.seg_begin, static_cast<int>(rank),
+                                            offs, 0, static_cast<int>(rank),
                                             kHalfTiles);
             bool w = true;
             if (lane == 0) w = mbar_wait_cl(accf_bar(acc), acc_phase, abort_flag, a.dev_err);
@@ -2019,7 +2035,7 @@ static int max_pairs(int device) {
     if (cache[device] > 0) return cache[device];
     // the largest segment count a launch of this form takes: slots of an arena,
     // or the experts of one layer for 4-bit weights
-    const size_t smem = pair_smem_bytes(kQ4 ? kQMaxSegs : kMaxP, kQ4);
+    const size_t smem = pair_smem_bytes(pair_seg_cap(kQ4), kQ4);
     if (cudaFuncSetAttribute(k_expert_ffn_pair<kQ4, kMFirst>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
         return 0;
