@@ -1162,6 +1162,7 @@ constexpr int kPOffA = 0;
 constexpr int kPairRows = 2 * kBM;
 constexpr int kLoaderWarps = 4;
 constexpr int kEpiWarps = 4;
+constexpr int kSplitMinKb = 128;   // down tiles of at least this many k-blocks are split in K
 
 // 4-bit weights in the pair form: each CTA streams only its half of a packed
 // box (the gate box on rank 0 and the up box on rank 1, or rows
@@ -1513,9 +1514,17 @@ __global__ void __launch_bounds__(kQ4 ? kPQThreads : kThreads, 1)
     const int H = a.H, F = a.F;
     const int NBA = F / 128, NBB = H / 256;
     const int KBA = H / 64, KBB = F / 64;
+    // A long down tile is split in two halves of its K range, each adding its
+    // partial product into Y (not in the deterministic mode, which stores
+    // rows): the unit the tile hand-out balances halves (on the Mixtral shape
+    // a whole down tile is 224 k-blocks, ~5% of a pair's work). Down tile
+    // column v is n-block v / KS, K half v % KS.
+    const int KS = (!kQ4 && !a.out_rows && KBB >= kSplitMinKb && KBB % 2 == 0) ? 2 : 1;
+    const int NBBv = NBB * KS;
+    const int KBBs = KBB / KS;   // k-blocks of a down tile
     const int PM = table[seg.seg_count];
     const int TA = (a.phases & 1) ? PM * NBA : 0;
-    const int TB = (a.phases & 2) ? PM * NBB : 0;
+    const int TB = (a.phases & 2) ? PM * NBBv : 0;
     const int done_target = kEpiWarps * NBA;
 
     if (kQ4 && warp == 0) {
@@ -1528,13 +1537,13 @@ __global__ void __launch_bounds__(kQ4 ? kPQThreads : kThreads, 1)
             for (int q = 0; q < kPST; ++q) issued[q] = -1;
             bool ok = true;
             int g = 0;
-            for (int it = 0, t; ok && (t = tile_of(pair, n_pairs, TA, TB, KBA, KBB, it)) >= 0; ++it) {
+            for (int it = 0, t; ok && (t = tile_of(pair, n_pairs, TA, TB, KBA, KBBs, it)) >= 0; ++it) {
                 const bool gu = t < TA;
                 const PairTile ti = decode_pair<kMFirst>(gu ? t : t - TA, table, seg.seg_count,
-                                                gu ? NBA : NBB, offs, 0,
+                                                gu ? NBA : NBBv, offs, 0,
                                                 static_cast<int>(rank), kHalfTiles);
                 const size_t slot = static_cast<size_t>(seg.slot_base + ti.seg);
-                const int num_kb = gu ? KBA : KBB;
+                const int num_kb = gu ? KBA : KBBs;
                 const uint8_t* box0 =
                     gu ? (rank == 0 ? planes.g : planes.u) + slot * planes.S_gu +
                              static_cast<size_t>(ti.nb) * KBA * kQBoxGU
@@ -1573,12 +1582,12 @@ __global__ void __launch_bounds__(kQ4 ? kPQThreads : kThreads, 1)
         const int ct = cw * 32 + lane;
         int g = 0;
         bool ok = true;
-        for (int it = 0, t; ok && (t = tile_of(pair, n_pairs, TA, TB, KBA, KBB, it)) >= 0; ++it) {
+        for (int it = 0, t; ok && (t = tile_of(pair, n_pairs, TA, TB, KBA, KBBs, it)) >= 0; ++it) {
             const bool gu = t < TA;
-            const PairTile ti = decode_pair<kMFirst>(gu ? t : t - TA, table, seg.seg_count, gu ? NBA : NBB,
+            const PairTile ti = decode_pair<kMFirst>(gu ? t : t - TA, table, seg.seg_count, gu ? NBA : NBBv,
                                             offs, 0, static_cast<int>(rank),
                                             kHalfTiles);
-            const int num_kb = gu ? KBA : KBB;
+            const int num_kb = gu ? KBA : KBBs;
             const bool load_h = !gu && ti.rows > 0;
             const uint32_t tx = gu ? 0u : static_cast<uint32_t>(kPHalf * (1 + (ti.rows1 > 0 ? 1 : 0)));
             for (int kb = 0; kb < num_kb; ++kb, ++g) {
@@ -1635,22 +1644,23 @@ __global__ void __launch_bounds__(kQ4 ? kPQThreads : kThreads, 1)
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
-        for (int it = 0, t; ok && (t = tile_of(pair, n_pairs, TA, TB, KBA, KBB, it)) >= 0; ++it) {
+        for (int it = 0, t; ok && (t = tile_of(pair, n_pairs, TA, TB, KBA, KBBs, it)) >= 0; ++it) {
             const bool gu = t < TA;
-            const PairTile ti = decode_pair<kMFirst>(gu ? t : t - TA, table, seg.seg_count, gu ? NBA : NBB,
+            const PairTile ti = decode_pair<kMFirst>(gu ? t : t - TA, table, seg.seg_count, gu ? NBA : NBBv,
                                             offs, 0, static_cast<int>(rank),
                                             kHalfTiles);
             const int slot = seg.slot_base + ti.seg;
-            const int num_kb = gu ? KBA : KBB;
+            const int num_kb = gu ? KBA : KBBs;
             // tile-major planes: the (n-block, k-block) box of a slot is one
             // contiguous run of 128 (gate, up) or 256 (down) rows of 128 bytes
             int brow0;
             const CUtensorMap* tm_b;
+            const int kb0 = gu ? 0 : (ti.nb % KS) * KBBs;   // first k-block of the tile
             if (gu) {
                 brow0 = (slot * NBA + ti.nb) * KBA * 128;
                 tm_b = rank == 0 ? &tm_wg : &tm_wu;
             } else {
-                brow0 = (slot * NBB + ti.nb) * KBB * 256 + kBM * static_cast<int>(rank);
+                brow0 = (slot * NBB + ti.nb / KS) * KBB * 256 + kBM * static_cast<int>(rank);
                 tm_b = &tm_wd;
             }
             const int brow_step = gu ? 128 : 256;
@@ -1711,12 +1721,14 @@ __global__ void __launch_bounds__(kQ4 ? kPQThreads : kThreads, 1)
                             tma_load_2d_pair(dst + kPHalf / 2, &tm_wu64, 0, r64, lbar);
                         }
                     } else if (only_reader)
-                        tma_load_2d_pair_hint(sB + stage * kPHalf, tm_b, 0, brow0 + kb * brow_step,
-                                              lbar, policy_evict_first());
+                        tma_load_2d_pair_hint(sB + stage * kPHalf, tm_b, 0,
+                                              brow0 + (kb0 + kb) * brow_step, lbar,
+                                              policy_evict_first());
                     else
-                        tma_load_2d_pair(sB + stage * kPHalf, tm_b, 0, brow0 + kb * brow_step, lbar);
+                        tma_load_2d_pair(sB + stage * kPHalf, tm_b, 0, brow0 + (kb0 + kb) * brow_step,
+                                         lbar);
                     if (load_h)
-                        tma_load_2d_pair(sA + stage * kPHalf, &tm_h, kb * 64, ti.row0, lbar);
+                        tma_load_2d_pair(sA + stage * kPHalf, &tm_h, (kb0 + kb) * 64, ti.row0, lbar);
                 }
                 __syncwarp();
                 if (++stage == kST) {
@@ -1753,12 +1765,12 @@ __global__ void __launch_bounds__(kQ4 ? kPQThreads : kThreads, 1)
                     mbar_arrive_remote_smem_release(map_rank(full_bar(s), 0));
             }
         };
-        for (int it = 0, t; ok && (t = tile_of(pair, n_pairs, TA, TB, KBA, KBB, it)) >= 0; ++it) {
+        for (int it = 0, t; ok && (t = tile_of(pair, n_pairs, TA, TB, KBA, KBBs, it)) >= 0; ++it) {
             const bool gu = t < TA;
-            const PairTile ti = decode_pair<kMFirst>(gu ? t : t - TA, table, seg.seg_count, gu ? NBA : NBB,
+            const PairTile ti = decode_pair<kMFirst>(gu ? t : t - TA, table, seg.seg_count, gu ? NBA : NBBv,
                                             offs, 0, static_cast<int>(rank),
                                             kHalfTiles);
-            const int num_kb = gu ? KBA : KBB;
+            const int num_kb = gu ? KBA : KBBs;
             if (!gu) {
                 if (npend > 0) {
                     cp_async_wait<0>();
@@ -1842,10 +1854,10 @@ __global__ void __launch_bounds__(kQ4 ? kPQThreads : kThreads, 1)
             uint32_t acc_phase = 0;
             bool ok = true;
             bool issued_any = false;
-            for (int it = 0, t; ok && (t = tile_of(pair, n_pairs, TA, TB, KBA, KBB, it)) >= 0; ++it) {
+            for (int it = 0, t; ok && (t = tile_of(pair, n_pairs, TA, TB, KBA, KBBs, it)) >= 0; ++it) {
                 const bool gu = t < TA;
-                const int num_kb = gu ? KBA : KBB;
-                const PairTile ti = decode_pair<kMFirst>(gu ? t : t - TA, table, seg.seg_count, gu ? NBA : NBB,
+                const int num_kb = gu ? KBA : KBBs;
+                const PairTile ti = decode_pair<kMFirst>(gu ? t : t - TA, table, seg.seg_count, gu ? NBA : NBBv,
                                                 offs, 0, 0, kHalfTiles);
                 const uint32_t idesc = gu ? (ti.half ? idesc_gu_half : idesc_gu)
                                           : (ti.half ? idesc_dn_half : idesc_dn);
@@ -1894,9 +1906,9 @@ __global__ void __launch_bounds__(kQ4 ? kPQThreads : kThreads, 1)
         const uint32_t leader_acce1 = map_rank(acce_bar(1), 0);
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int it = 0, t; (t = tile_of(pair, n_pairs, TA, TB, KBA, KBB, it)) >= 0; ++it) {
+        for (int it = 0, t; (t = tile_of(pair, n_pairs, TA, TB, KBA, KBBs, it)) >= 0; ++it) {
             const bool gu = t < TA;
-            const PairTile ti = decode_pair<kMFirst>(gu ? t : t - TA, table, seg.seg_count, gu ? NBA : NBB,
+            const PairTile ti = decode_pair<kMFirst>(gu ? t : t - TA, table, seg.seg_count, gu ? NBA : NBBv,
                                             offs, 0, static_cast<int>(rank),
                                             kHalfTiles);
             bool w = true;
@@ -1938,7 +1950,7 @@ __global__ void __launch_bounds__(kQ4 ? kPQThreads : kThreads, 1)
                 }
                 float* dst = a.out_rows ? a.out_rows + static_cast<size_t>(p) * H
                                         : a.Y + static_cast<size_t>(tok) * H;
-                epilogue_down_staged(tacc, al, valid ? dst + ti.nb * 256 + 128 * cpart : nullptr,
+                epilogue_down_staged(tacc, al, valid ? dst + (ti.nb / KS) * 256 + 128 * cpart : nullptr,
                                      !a.out_rows, stg, lane, ti.half ? 4 : 8);
             }
             tc_fence_before();

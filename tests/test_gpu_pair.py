@@ -94,3 +94,25 @@ def test_invalid_form_rejected():
     with pytest.raises(es.EStreamError) as ei:
         BoundLayerStack(wl, mode="resident", ffn_form=3)
     assert ei.value.status == es.ERR_INVALID_ARG
+
+
+def test_split_down_tiles():
+    """Down tiles of at least 128 k-blocks (F >= 8192) run as two K halves
+    that each add their partial product into Y; Y against the oracle on
+    every element, and against the deterministic mode (whole down tiles,
+    rows combined in a fixed order) within the fp32 summation order."""
+    from routed_expert_ffn_topk_gb300 import estream as es
+    from routed_expert_ffn_topk_gb300.layer import BoundLayerStack
+    cfg = W.scaled(W.CONFIGS["c5"], T=520, H=512, E=4, k=2, F=8192)
+    wl = W.make_workload(cfg)
+    ys = {}
+    for det in (False, True):
+        st = BoundLayerStack(wl, mode="resident", ffn_form=es.FFN_PAIR, deterministic=det)
+        try:
+            ys[det] = run_layer(st, wl)
+        finally:
+            st.close()
+    ref = _gpu.oracle_layer(wl, 0, wl.X)
+    _gpu.assert_y_close(ys[False], ref, "F=8192 split down tiles")
+    d = np.abs(ys[False] - ys[True]).max() / np.abs(ys[True]).max()
+    assert d <= 1e-5, d
