@@ -770,8 +770,10 @@ def measure_router(cfg, X0, dev, stream, flush, peaks, steps):
 def measure_q4(args, cfg, wl, dev, stream, flush, peaks):
     """The same layer (layer 0) with 4-bit experts (ESTREAM_Q4): resident,
     timed like the main step, with the fused kernel's roofline from the
-    packed weight bytes (3*H*F*9/16 per active expert) + X + Y; and paged
-    through the config's arena, every group streamed (arena invalidated)."""
+    packed weight bytes (3*H*F*9/16 per active expert) + X + Y; and paged,
+    every group streamed (arena invalidated), through an arena of the config's
+    group size G and as many banks as fit in the bytes of the config's bf16
+    arena (the paper's fixed memory budget: 4-bit slots are 3.56x smaller)."""
     import torch
 
     from routed_expert_ffn_topk_gb300 import estream as es
@@ -787,8 +789,15 @@ def measure_q4(args, cfg, wl, dev, stream, flush, peaks):
         # pages' prefetch schedule); with 28 MB groups the route-and-decide
         # time at the start of a call is a larger share than with bf16
         form = {"auto": es.FFN_AUTO, "single": es.FFN_SINGLE, "pair": es.FFN_PAIR}[args.q4_form]
+        kw = {}
+        if mode == "paged":
+            budget = es.arena_bytes(cfg.E, cfg.H, cfg.F, cfg.G, cfg.B, es.BF16)
+            bank = es.arena_bytes(cfg.E, cfg.H, cfg.F, cfg.G, 1, es.Q4)
+            kw = {"B": max(1, min(-(-cfg.E // cfg.G), budget // bank))}
         st = BoundLayerStack(wl1, mode=mode, wdtype=es.Q4, ffn_form=form,
-                             schedule=es.SCHED_PREFETCH if mode == "paged" else es.SCHED_AFTER_ROUTING)
+                             schedule=es.SCHED_PREFETCH if mode == "paged" else es.SCHED_AFTER_ROUTING,
+                             **kw)
+        arena = f"P={st.G * st.B} (G={st.G}, B={st.B})"
         try:
             def one():
                 if mode == "paged":
@@ -843,7 +852,9 @@ def measure_q4(args, cfg, wl, dev, stream, flush, peaks):
                         "frac": round(tfs / sus if tensor else gbs / peaks["hbm_gbs"], 4)})
         else:
             h2d = stats["h2d_bytes"] / len(ms)
-            rec.update({"schedule": "prefetch before routing", "h2d_bytes_per_layer": int(h2d),
+            rec.update({"schedule": "prefetch before routing",
+                        "arena": arena + ", within the bytes of the bf16 arena",
+                        "h2d_bytes_per_layer": int(h2d),
                         "h2d_GBps": round(h2d / (t / 1e3) / 1e9, 1)})
         out[mode] = rec
     return out
