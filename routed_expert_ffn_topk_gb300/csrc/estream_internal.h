@@ -104,7 +104,27 @@ struct GemmSegments {
     int seg_begin, seg_count;  // segments [seg_begin, seg_begin+seg_count)
     int slot_base;             // arena slot of segment seg_begin
     int max_tiles_m;           // host upper bound on m-blocks in the range
+    // Residual rows Y = A, written by this launch's epilogue warps before
+    // their first tile (the first expert launch of a layer call with a
+    // residual; resid_A null otherwise): A [resid_T][H] with resid_elem bytes
+    // per element (bf16 2, fp32 4) into resid_Y [resid_T][H]. Each epilogue warp then adds 1 to
+    // *resid_done (zeroed by the route build), and a down epilogue waits for
+    // every epilogue warp of the launch before it adds into Y.
+    const void* resid_A;
+    float* resid_Y;
+    int resid_elem, resid_T;
+    int* resid_done;
 };
+
+// Residual rows (T given) that the route build copies beside its top-k on
+// CTAs it adds for them; rows beyond it are copied by the chunk CTAs after
+// the top-k, ahead of the route build's grid barriers.
+int route_residual_overlap_rows(int T);
+
+// Y[t][:] = fp32(A[t][:]) for t < T (A bf16 or fp32 by elem_bytes): the
+// residual rows of a layer call whose expert launches did not write them.
+cudaError_t launch_residual_rows(const void* A, int elem_bytes, float* Y, int T, int H,
+                                 cudaStream_t stream);
 
 // Fused expert FFN (one cooperative launch), phases bit 0 / bit 1:
 //   gate/up: h[p, :] = fp16(SiLU(X[tok(p)] Wg_slot^T) * (X[tok(p)] Wu_slot^T)) (bf16 MMA);

@@ -607,6 +607,54 @@ __device__ void role_mma(const FfnArgs& a, const TileWalk& w, Ring ring, uint32_
     }
 }
 
+// The launch's residual rows (GemmSegments::resid_A), by its epilogue warps
+// before their first tile (they wait for the first accumulator anyway; no
+// tile adds into Y before the gate/up phase ends): epilogue warp w of n_warps
+// writes Y[t] = fp32(A[t]) for t = w, w + n_warps, ..., four 16-byte loads
+// per lane in flight, then publishes its rows with one release-add.
+__device__ void residual_rows(const GemmSegments& seg, int H, int w, int n_warps, int lane) {
+    float* Y = seg.resid_Y;
+    const int row_bytes = H * seg.resid_elem;
+    for (int t = w; t < seg.resid_T; t += n_warps) {
+        const char* src = static_cast<const char*>(seg.resid_A) + static_cast<size_t>(t) * row_bytes;
+        float* y = Y + static_cast<size_t>(t) * H;
+        for (int base = lane * 16; base < row_bytes; base += 4 * 32 * 16) {
+            uint4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int off = base + u * 32 * 16;
+                if (off < row_bytes) v[u] = __ldg(reinterpret_cast<const uint4*>(src + off));
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int off = base + u * 32 * 16;
+                if (off >= row_bytes) continue;
+                if (seg.resid_elem == 2) {  // 8 bf16: a bf16 is the high half of its fp32
+                    float4* d = reinterpret_cast<float4*>(y + off / 2);
+                    d[0] = make_float4(__uint_as_float(v[u].x << 16), __uint_as_float(v[u].x & 0xFFFF0000u),
+                                       __uint_as_float(v[u].y << 16), __uint_as_float(v[u].y & 0xFFFF0000u));
+                    d[1] = make_float4(__uint_as_float(v[u].z << 16), __uint_as_float(v[u].z & 0xFFFF0000u),
+                                       __uint_as_float(v[u].w << 16), __uint_as_float(v[u].w & 0xFFFF0000u));
+                } else {
+                    *reinterpret_cast<uint4*>(y + off / 4) = v[u];
+                }
+            }
+        }
+    }
+    __threadfence();
+    __syncwarp();
+    if (lane == 0) red_release_add(seg.resid_done, 1);
+}
+
+// Before a down epilogue's first addition into Y: wait (bounded) until every
+// epilogue warp of the launch has published its residual rows.
+__device__ __forceinline__ bool residual_ready(const GemmSegments& seg, int n_warps, int lane,
+                                               volatile int* abort_flag, int* dev_err) {
+    bool ok = true;
+    if (lane == 0) ok = wait_counter(seg.resid_done, n_warps, abort_flag, dev_err);
+    return __shfl_sync(0xffffffffu, ok, 0);
+}
+
 // Epilogue (4 warps, TMEM lanes = records): gate/up tiles write
 // h = fp16(SiLU(g) u) and publish the m-block counter; down tiles add
 // alpha * scale * acc into Y (or store the row in deterministic mode).
@@ -619,11 +667,19 @@ __device__ void role_epilogue(const FfnArgs& a, const TileWalk& w, uint32_t accf
     const int quarter = warp & 3;  // TMEM lanes this warp may read
     const int row = quarter * 32 + lane;
     const uint32_t stg = stage0 + static_cast<uint32_t>(quarter * kStageWarpBytes);
+    const int n_epi = static_cast<int>(gridDim.x) * 4;   // epilogue warps of the launch
+    if (seg.resid_A) residual_rows(seg, a.H, static_cast<int>(blockIdx.x) * 4 + warp - 2, n_epi, lane);
+    // the deterministic mode adds into Y only in the combine, a later launch
+    bool resid_ok = !seg.resid_A || a.out_rows;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int it = 0, t; (t = w.tile(it)) >= 0; ++it) {
         const bool gu = t < w.TA;
         const Tile ti = w.decode(t);
+        if (!gu && !resid_ok) {
+            if (!residual_ready(seg, n_epi, lane, abort_flag, a.dev_err)) break;
+            resid_ok = true;
+        }
         bool wt = true;
         if (lane == 0) wt = mbar_wait(accf0 + 8u * acc, acc_phase, abort_flag, a.dev_err);
         wt = __shfl_sync(0xffffffffu, wt, 0);
@@ -1904,10 +1960,19 @@ __global__ void __launch_bounds__(kQ4 ? kPQThreads : kThreads, 1)
         const uint32_t stg = sbase + kL.off_stg + static_cast<uint32_t>(quarter * kStageWarpBytes);
         const uint32_t leader_acce0 = map_rank(acce_bar(0), 0);
         const uint32_t leader_acce1 = map_rank(acce_bar(1), 0);
+        const int n_epi = static_cast<int>(gridDim.x) * kEpiWarps;   // epilogue warps of the launch
+        if (seg.resid_A)
+            residual_rows(seg, a.H, static_cast<int>(blockIdx.x) * kEpiWarps + warp - 2, n_epi, lane);
+        // the deterministic mode adds into Y only in the combine, a later launch
+        bool resid_ok = !seg.resid_A || a.out_rows;
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int it = 0, t; (t = tile_of(pair, n_pairs, TA, TB, KBA, KBBs, it)) >= 0; ++it) {
             const bool gu = t < TA;
+            if (!gu && !resid_ok) {
+                if (!residual_ready(seg, n_epi, lane, abort_flag, a.dev_err)) break;
+                resid_ok = true;
+            }
             const PairTile ti = decode_pair<kMFirst>(gu ? t : t - TA, table, seg.seg_count, gu ? NBA : NBBv,
                                             offs, 0, static_cast<int>(rank),
                                             kHalfTiles);

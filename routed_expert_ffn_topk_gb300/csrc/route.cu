@@ -758,6 +758,16 @@ __global__ void k_identity_map(int T, int n_shared, int32_t* __restrict__ offset
     }
 }
 
+// Y = fp32(A), one warp per row (grid-stride over rows).
+__global__ void k_residual_rows(ResidualInit r, int T) {
+    const int warp = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+    const int n_warps = static_cast<int>((gridDim.x * blockDim.x) >> 5);
+    const int row_bytes = r.H * r.elem_bytes;
+    for (int t = warp; t < T; t += n_warps)
+        widen_residual(r, t, static_cast<const char*>(r.A) + static_cast<size_t>(t) * row_bytes, 0,
+                       row_bytes);
+}
+
 __global__ void k_cast_f32_bf16(const float* __restrict__ src, __nv_bfloat16* __restrict__ dst,
                                 size_t n) {
     const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
@@ -788,6 +798,16 @@ static int route_co_resident() {
         return 0;
     cache[dev] = sms * per_sm;
     return cache[dev];
+}
+
+// Residual rows the route build copies on CTAs it adds beside the top-k
+// chunks (those copies overlap the top-k; later rows follow it on the chunk
+// CTAs, ahead of the grid barriers).
+int route_residual_overlap_rows(int T) {
+    const int co = route_co_resident();
+    const int nchunk = (T + kChunkTokens - 1) / kChunkTokens;
+    const int grid = std::max(1, std::min(co, 2 * nchunk));
+    return std::max(0, grid - std::min(nchunk, grid)) * kChunkTokens;
 }
 
 RouteWorkspace route_workspace_layout(int T, int k, int P) {
@@ -1003,6 +1023,15 @@ cudaError_t launch_identity_map(int T, int n_shared, int32_t* offsets, int32_t* 
                                 int32_t* mblk, int32_t* done, cudaStream_t stream) {
     const int n = T * n_shared > n_shared + 1 ? T * n_shared : n_shared + 1;
     k_identity_map<<<(n + 255) / 256, 256, 0, stream>>>(T, n_shared, offsets, rec_tok, mblk, done);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_residual_rows(const void* A, int elem_bytes, float* Y, int T, int H,
+                                 cudaStream_t stream) {
+    if (T <= 0) return cudaSuccess;
+    const ResidualInit r{A, elem_bytes, Y, H};
+    const int blocks = (T + 7) / 8 < 1024 ? (T + 7) / 8 : 1024;   // 8 warps of 32 per block
+    k_residual_rows<<<blocks, 256, 0, stream>>>(r, T);
     return cudaGetLastError();
 }
 

@@ -131,7 +131,8 @@ struct estream_ctx {
     float *alpha = nullptr, *out_rows = nullptr, *out_shared = nullptr;
     float* d_scale = nullptr;                  // [L*E] down-weight scales, storage order
     int32_t *done = nullptr, *sh_done = nullptr;  // per-m-block counters of the fused expert kernel
-    int32_t* tickets = nullptr;  // [E+2] dynamic tile counters: [0] shared experts, [1+i] i-th routed launch
+    int32_t* tickets = nullptr;  // [E+3] zeroed per call: [0] shared experts' and [1+i] the i-th routed
+                                 // launch's tile counters, [E+2] the residual rows' counter
     // per-call part of the workspace (everything after the bind-time tables),
     // and the counter regions inside it (for estream_poison_workspace)
     size_t ws_call_off = 0;
@@ -162,6 +163,12 @@ struct estream_ctx {
     int fault_layer = -1, fault_group = -1;
     bool route_withhold_next = false;  // test: the next route build withholds an arrival
     int ffn_phases = 3;                // routed expert kernels: bit 0 gate/up tiles, bit 1 down tiles
+    // residual rows of the current call still to be written by an expert
+    // launch (the first one takes them; estream_moe_layer_prefill_residual)
+    bool resid_pending = false;
+    const void* resid_A = nullptr;
+    float* resid_Y = nullptr;
+    int resid_T = 0;
     bool ffn_down_only_next = false;   // test: the next call runs the down tiles alone
 };
 
@@ -728,7 +735,7 @@ estream_status estream_bind_arena(estream_ctx** out, const estream_arena_desc* d
     const size_t o_lg = take(f32 ? 0 : sizeof(float) * static_cast<size_t>(d->T_max) * E);
     const size_t o_rws = take(route_workspace_layout(d->T_max, d->k_max, E).total);
     const size_t o_done = take(sizeof(int32_t) * ((R_cap + kBM - 1) / kBM + E + 1));
-    const size_t o_tick = take(sizeof(int32_t) * (E + 2));
+    const size_t o_tick = take(sizeof(int32_t) * (E + 3));
     const size_t o_h = take(static_cast<size_t>(R_cap) * d->F * c->es);
     size_t o_sh_offs = 0, o_sh_mblk = 0, o_sh_tok = 0, o_hs = 0, o_outs = 0, o_out = 0;
     const int RS_cap = d->n_shared * d->T_max;
@@ -765,7 +772,7 @@ estream_status estream_bind_arena(estream_ctx** out, const estream_arena_desc* d
         c->h = c->ws + o_h;
         c->ws_call_off = o_ids;
         c->n_done = (R_cap + kBM - 1) / kBM + E + 1;
-        c->n_tickets = E + 2;
+        c->n_tickets = E + 3;
         if (d->n_shared > 0) {
             c->n_sh_done = d->n_shared * ((d->T_max + kBM - 1) / kBM) + 1;
             c->sh_done = reinterpret_cast<int32_t*>(c->ws + o_sh_done);
@@ -932,6 +939,18 @@ bool pair_form(const estream_ctx* c, long long rows, int segments) {
     return segments > 0 && rows >= static_cast<long long>(ESTREAM_PAIR_MIN_ROWS) * segments;
 }
 
+// Hands the call's pending residual rows to an expert launch over `seg`
+// (which will launch: segments and m-blocks to cover).
+void take_residual(estream_ctx* c, GemmSegments& seg) {
+    if (!c->resid_pending || seg.seg_count <= 0 || seg.max_tiles_m <= 0) return;
+    seg.resid_A = c->resid_A;
+    seg.resid_Y = c->resid_Y;
+    seg.resid_elem = c->es;
+    seg.resid_T = c->resid_T;
+    seg.resid_done = c->tickets + c->d.E + 2;
+    c->resid_pending = false;
+}
+
 // K2 + K3 over segments [seg_begin, seg_begin + seg_count) of the routed
 // route map, whose experts sit in consecutive arena slots from slot_base.
 estream_status run_routed(estream_ctx* c, cudaStream_t s, const void* X, int layer,
@@ -948,6 +967,7 @@ estream_status run_routed(estream_ctx* c, cudaStream_t s, const void* X, int lay
     seg.seg_count = seg_count;
     seg.slot_base = slot_base;
     seg.max_tiles_m = max_tiles_m;
+    if (c->d.wdtype != ESTREAM_F32) take_residual(c, seg);
     TimedScope ts(c, s, kTFfn, layer);
     // this launch's dynamic tile counter, zeroed by the call's route build. The
     // 4-bit kernel takes its tiles dynamically (measured 5.5% faster on the
@@ -1013,6 +1033,7 @@ estream_status run_shared(estream_ctx* c, cudaStream_t s, const void* X,
     seg.seg_count = ns;
     seg.slot_base = 0;
     seg.max_tiles_m = ns * ((T + kBM - 1) / kBM);
+    if (c->d.wdtype != ESTREAM_F32) take_residual(c, seg);
     const int Fs = c->d.F_shared;
     cudaError_t rc;
     if (c->d.wdtype == ESTREAM_F32) {
@@ -1161,6 +1182,7 @@ static estream_status prefill_impl(estream_ctx* c, int layer, const void* X, con
     // bounded waits) the down tiles alone, whose m-block counters then never fill
     c->ffn_phases = c->ffn_down_only_next ? 2 : 3;
     c->ffn_down_only_next = false;
+    c->resid_pending = false;
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
     const int E = c->d.E, G = c->d.G, H = c->d.H;
     c->trace.clear();
@@ -1217,6 +1239,21 @@ static estream_status prefill_impl(estream_ctx* c, int layer, const void* X, con
         NvtxRange from_x(kNvRouteFromX, layer, W_r != nullptr);   // routing from the layer input
         int launches = 0;
         const ResidualInit ri{A, c->es, Y, H};
+        // The residual rows: the route build copies them on CTAs it adds beside
+        // the top-k, but rows beyond what those cover wait for the top-k and
+        // hold up the grid barriers (T = 4096: 100 MB on the Mixtral shape,
+        // ~30 us). From logits, a bf16 or 4-bit layer then has them written by
+        // its first expert launch instead (its epilogue warps are idle until
+        // their first accumulator is ready, and nothing adds into Y before the
+        // down tiles). From X, the routing launch writes them beside the
+        // router tile.
+        const bool resid_in_ffn = A && !W_r && c->d.wdtype != ESTREAM_F32 &&
+                                  T > route_residual_overlap_rows(T);
+        c->resid_pending = resid_in_ffn;
+        c->resid_A = A;
+        c->resid_Y = Y;
+        c->resid_T = T;
+        const ResidualInit* ri_route = A && !resid_in_ffn ? &ri : nullptr;
         const int32_t* phi = c->d_perm + static_cast<size_t>(layer) * E;
         int32_t* rec_pos = c->d.deterministic ? c->rec_pos : nullptr;
         const int withhold = c->route_withhold_next ? 1 : 0;
@@ -1224,12 +1261,12 @@ static estream_status prefill_impl(estream_ctx* c, int layer, const void* X, con
             W_r ? route_from_x_any(X, T, H, W_r, E, k, renorm, phi, E,
                                    logits_out ? logits_out : c->logits_buf, c->topk_ids, c->alpha,
                                    c->offsets, c->rec_tok, c->rec_route, rec_pos, c->done,
-                                   c->tickets, E + 2, c->route_ws, c->route_ws_bytes, s, &launches,
-                                   A ? &ri : nullptr, withhold, c->num_sms, nullptr)
+                                   c->tickets, E + 3, c->route_ws, c->route_ws_bytes, s, &launches,
+                                   ri_route, withhold, c->num_sms, nullptr)
                 : launch_route_build(logits, T, E, k, renorm, phi, E, c->topk_ids, c->alpha,
                                      c->offsets, c->rec_tok, c->rec_route, rec_pos, c->done,
-                                     c->tickets, E + 2, c->route_ws, c->route_ws_bytes, s,
-                                     &launches, A ? &ri : nullptr, withhold);
+                                     c->tickets, E + 3, c->route_ws, c->route_ws_bytes, s,
+                                     &launches, ri_route, withhold);
         if (rc != cudaSuccess) {
             drain(c, s);
             return ESTREAM_ERR_CUDA;
@@ -1327,6 +1364,15 @@ static estream_status prefill_impl(estream_ctx* c, int layer, const void* X, con
         return st;
     }
     c->stats.h2d_bytes += static_cast<double>(bytes);
+    if (c->resid_pending) {
+        // no expert launch took the residual rows (no routed group had work)
+        c->resid_pending = false;
+        if (launch_residual_rows(A, c->es, Y, T, H, s) != cudaSuccess) {
+            drain(c, s);
+            return ESTREAM_ERR_CUDA;
+        }
+        c->stats.launches += 1;
+    }
     if (c->d.deterministic) {
         TimedScope ts(c, s, kTCombine, layer);
         if (launch_combine(c->out_rows, c->rec_pos, T, k, H, c->out_shared, c->d.n_shared, Y, s) !=
