@@ -1,5 +1,6 @@
 """estream_moe_layer_prefill_residual: Y = A + MoE(X) with the residual rows
-written by the route build, against an explicit copy of A into Y followed by
+written by the route build (or, when T exceeds the rows its added CTAs cover,
+by the first expert launch), against an explicit copy of A into Y followed by
 the accumulating call (bit for bit in deterministic mode) and the oracle."""
 import numpy as np
 import pytest
@@ -77,3 +78,43 @@ def test_residual_rows_bit_exact(T, E, k):
         assert torch.equal(Y1.view(torch.int32), Y2.view(torch.int32))
     finally:
         st.close()
+
+
+@pytest.mark.parametrize("mode", ["resident", "paged"])
+def test_residual_rows_when_routing_times_out(mode):
+    """At T = 4096 an expert launch writes the residual rows (more rows than
+    the route build's added CTAs cover). When the route build's bounded
+    barrier runs out (one CTA withholds its arrival) the route map is empty:
+    resident, the routed launch still runs and writes the rows; paged, no
+    group has work, no expert launch runs, and a copy kernel writes them. Y
+    equals A bit for bit, the timeout is reported, and the next call is
+    normal."""
+    from routed_expert_ffn_topk_gb300 import estream as es
+    from routed_expert_ffn_topk_gb300 import workloads as W
+    from routed_expert_ffn_topk_gb300.layer import BoundLayerStack
+    cfg = W.scaled(W.CONFIGS["c2"], T=4096, H=256, E=8, k=2, F=128, key_suffix="-resid-timeout")
+    wl = W.make_workload(cfg, seed=4242)
+    dev = _gpu.device()
+    kw = dict(G=2, B=2) if mode == "paged" else {}
+    st = BoundLayerStack(wl, mode=mode, **kw)
+    try:
+        X = wl.X.to(dev)
+        lg = wl.logits[0].to(dev)
+        A = torch.randn(X.shape, generator=torch.Generator().manual_seed(5), dtype=torch.float32)
+        A = A.to(X.dtype).to(dev)
+        es.inject_route_timeout(st.ctx)
+        Y = torch.full((cfg.T, cfg.H), float("nan"), device=dev)
+        st.prefill(0, X, lg, Y, residual=A)
+        torch.cuda.synchronize()
+        assert es.get_device_error(st.ctx) == es.ERR_TIMEOUT
+        assert torch.equal(Y.view(torch.int32), A.float().view(torch.int32))
+        Y2 = torch.full_like(Y, float("nan"))
+        st.prefill(0, X, lg, Y2, residual=A)
+        torch.cuda.synchronize()
+        assert es.get_device_error(st.ctx) == es.OK
+        y2 = Y2.cpu().numpy()
+    finally:
+        st.close()
+    Ac = A.cpu().double().numpy()
+    ref = _gpu.oracle_layer(wl, 0, wl.X)
+    _gpu.assert_y_close(y2 - Ac, ref, f"T=4096 residual after a route timeout ({mode})")
