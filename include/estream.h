@@ -377,9 +377,10 @@ estream_status estream_moe_layer_prefill(estream_ctx* c, int layer, const void* 
 /*
  * The same layer with the residual of Eq. 2 given explicitly:
  * Y = A + sum_j alpha_{t,j} F_{e_{t,j}}(X_t) (+ shared experts). Y is written,
- * not read: the route build initialises the rows from A in the same pass
- * that ranks the tokens' experts, so the caller needs no separate copy of A
- * into Y.
+ * not read: the call initialises the rows from A itself -- the route build
+ * beside its ranking of the tokens' experts, or, when T exceeds the rows it
+ * covers there (bf16 and Q4 contexts), the first expert kernel before its
+ * first tile -- so the caller needs no separate copy of A into Y.
  * A       device, [T][H] in X's type (bf16, or fp32 for ESTREAM_F32), 16-byte
  *         aligned; A == X (the usual residual stream) is allowed.
  * The other arguments and the behaviour are those of
