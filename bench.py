@@ -905,28 +905,33 @@ def measure_paged(args, cfg, wl, dev, stream, flush, peaks):
                  "groups": int(len(adsf)), "q": 1, "b": cfg.B, "T_ne_ms": round(t_ne, 4)}
     bytes_per_call = stats["h2d_bytes"] / len(times)
 
-    # the same layers through the prefetch-before-routing schedule
-    stp = BoundLayerStack(wl, mode="paged", schedule=es.SCHED_PREFETCH)
-    try:
-        for _ in range(2):
-            es.arena_invalidate(stp.ctx)
-            stp.prefill(0, X, logits[0], Y)
-        torch.cuda.synchronize()
-        times_pf = []
-        for i in range(steps):
-            for l in range(L):
-                flush.zero_()
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                es.arena_invalidate(stp.ctx)
-                a.record(stream)
-                stp.prefill(l, X, logits[l], Y)
-                b.record(stream)
-                b.synchronize()
-                times_pf.append(a.elapsed_time(b))
-        assert es.get_device_error(stp.ctx) == es.OK
-    finally:
-        stp.close()
-    t_pf = sum(times_pf) / len(times_pf)
+    def time_schedule(B, schedule):
+        """The same layers through another schedule of EStream Fig. 6: mean
+        ms per layer call, every group streamed."""
+        sts = BoundLayerStack(wl, mode="paged", B=B, schedule=schedule)
+        try:
+            for _ in range(2):
+                es.arena_invalidate(sts.ctx)
+                sts.prefill(0, X, logits[0], Y)
+            torch.cuda.synchronize()
+            ts = []
+            for i in range(steps):
+                for l in range(L):
+                    flush.zero_()
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    es.arena_invalidate(sts.ctx)
+                    a.record(stream)
+                    sts.prefill(l, X, logits[l], Y)
+                    b.record(stream)
+                    b.synchronize()
+                    ts.append(a.elapsed_time(b))
+            assert es.get_device_error(sts.ctx) == es.OK
+        finally:
+            sts.close()
+        return sum(ts) / len(ts)
+
+    t_pf = time_schedule(cfg.B, es.SCHED_PREFETCH)     # prefetch before routing
+    t_od = time_schedule(1, es.SCHED_AFTER_ROUTING)    # on demand: one bank
 
     # the same bytes, copy only (host link alone), and the link's own peak
     pool = st.pools[0]
@@ -963,7 +968,11 @@ def measure_paged(args, cfg, wl, dev, stream, flush, peaks):
         "arena": f"P={cfg.P} (G={cfg.G}, B={cfg.B})", "schedule": "after routing",
         "tokens_per_s": round(cfg.T / (t_paged / 1e3), 1),
         "prefetch_before_routing": {"ms_per_layer": round(t_pf, 4),
-                                    "tokens_per_s": round(cfg.T / (t_pf / 1e3), 1)},
+                                    "tokens_per_s": round(cfg.T / (t_pf / 1e3), 1),
+                                    "bubble_rate": round(1 - max(t_io, t_exec) / t_pf, 4)},
+        "on_demand": {"arena": f"P={cfg.G} (G={cfg.G}, B=1)", "ms_per_layer": round(t_od, 4),
+                      "tokens_per_s": round(cfg.T / (t_od / 1e3), 1),
+                      "bubble_rate": round(1 - max(t_io, t_exec) / t_od, 4)},
         "ms_per_layer": round(t_paged, 4), "h2d_bytes_per_layer": int(bytes_per_call),
         "h2d_GBps": round(h2d_gbs, 1), "h2d_peak_GBps": round(h2d_peak, 1),
         "frac_h2d_peak": round(h2d_gbs / h2d_peak, 4),
