@@ -396,7 +396,9 @@ estream_status estream_moe_layer_prefill_residual(estream_ctx* c, int layer, con
  * then the experts as in estream_moe_layer_prefill.
  * W_r        device, [E][H] bf16 (one row per expert), 16-byte aligned.
  * A          NULL: Y is accumulated into (Y += ...); else the residual of
- *            Eq. 2 as in estream_moe_layer_prefill_residual (Y written).
+ *            Eq. 2 as in estream_moe_layer_prefill_residual (Y written; the
+ *            routing launch initialises the rows beside its router tile, or
+ *            past the rows it covers there, the first expert kernel does).
  * logits_out device, [T][E] fp32, or NULL: receives the router logits.
  * Contexts of type ESTREAM_F32 are refused (ESTREAM_ERR_INVALID_ARG). The
  * other arguments and the behaviour are those of estream_moe_layer_prefill.

@@ -1240,14 +1240,13 @@ static estream_status prefill_impl(estream_ctx* c, int layer, const void* X, con
         int launches = 0;
         const ResidualInit ri{A, c->es, Y, H};
         // The residual rows: the route build copies them on CTAs it adds beside
-        // the top-k, but rows beyond what those cover wait for the top-k and
-        // hold up the grid barriers (T = 4096: 100 MB on the Mixtral shape,
-        // ~30 us). From logits, a bf16 or 4-bit layer then has them written by
-        // its first expert launch instead (its epilogue warps are idle until
-        // their first accumulator is ready, and nothing adds into Y before the
-        // down tiles). From X, the routing launch writes them beside the
-        // router tile.
-        const bool resid_in_ffn = A && !W_r && c->d.wdtype != ESTREAM_F32 &&
+        // the top-k (from X: on warps beside the router tile), but rows beyond
+        // what those cover wait for the top-k and hold up the grid barriers
+        // (T = 4096: 100 MB on the Mixtral shape, ~30 us). A bf16 or 4-bit
+        // layer then has them written by its first expert launch instead (its
+        // epilogue warps are idle until their first accumulator is ready, and
+        // nothing adds into Y before the down tiles).
+        const bool resid_in_ffn = A && c->d.wdtype != ESTREAM_F32 &&
                                   T > route_residual_overlap_rows(T);
         c->resid_pending = resid_in_ffn;
         c->resid_A = A;

@@ -197,3 +197,35 @@ def test_layer_from_x_route_timeout_then_normal():
     A = wl.X.double().numpy()
     ref = _gpu.oracle_layer(wl2, 0, wl.X, residual=A)
     _gpu.assert_y_close(y - A, ref - A, "c2 from X after a route timeout")
+
+
+def test_layer_from_x_residual_at_4096():
+    """A layer call routed from X at T = 4096 with a residual: the rows go to
+    the first expert launch (more than the routing launch covers beside its
+    router tile). Y - A against the oracle fed the GPU's logits, on every row,
+    with the workspace poisoned before the call."""
+    from routed_expert_ffn_topk_gb300 import estream as es
+    from routed_expert_ffn_topk_gb300.layer import BoundLayerStack
+    cfg = W.scaled(W.CONFIGS["c5"], T=4096, H=256, E=8, k=2, F=256, key_suffix="-fromx4096")
+    wl = W.make_workload(cfg, seed=4097)
+    _, W_r = W.make_router(1, cfg.H, cfg.E, seed=37)
+    dev = _gpu.device()
+    st = BoundLayerStack(wl, mode="resident")
+    try:
+        X = wl.X.to(dev)
+        A = torch.randn(X.shape, generator=torch.Generator().manual_seed(6), dtype=torch.float32)
+        A = A.to(X.dtype).to(dev)
+        Y = torch.full((cfg.T, cfg.H), float("nan"), device=dev)
+        lg = torch.empty(cfg.T, cfg.E, dtype=torch.float32, device=dev)
+        st.poison()
+        st.prefill_from_x(0, X, W_r.to(dev), Y, residual=A, logits_out=lg)
+        torch.cuda.synchronize()
+        assert es.get_device_error(st.ctx) == es.OK
+        y = Y.cpu().numpy()
+        lg_cpu = lg.cpu()
+    finally:
+        st.close()
+    wl2 = W.Workload(cfg, [lg_cpu], wl.X, wl.layers)
+    Ac = A.cpu().double().numpy()
+    ref = _gpu.oracle_layer(wl2, 0, wl.X)
+    _gpu.assert_y_close(y - Ac, ref, "from X, T = 4096, residual in the expert launch")
