@@ -12,7 +12,8 @@ resident in HBM. The headline line is the Mixtral-shaped layer (T=4096,
 H=4096, F=14336: the largest config, tensor-core bound); every config of
 --configs is measured the same way under "configs" (resident, end to end,
 4-bit experts, router, and the arena-paged call, whose bound is the host
-link). Under torchrun each rank runs its own replica on its own T tokens
+link, in the three loading schedules of EStream Fig. 6: after routing,
+prefetch before routing, and on demand through one bank). Under torchrun each rank runs its own replica on its own T tokens
 (weak scaling, no collective on the data path).
 """
 from __future__ import annotations
